@@ -1,0 +1,134 @@
+"""Seeded synthetic inputs for the gated delta rule forward pass.
+
+This module only draws random numbers and shapes them; it holds none of the
+method's arithmetic.  Both the CUDA path and the oracle are fed from it.
+
+Recipe (one ``numpy.random.default_rng(seed)`` stream per workload, drawn in
+this order, everything as fp64 standard normals first):
+
+1. varlen only: sequence lengths ``rng.integers(lo, hi + 1, num_seqs)``;
+2. q, then k: N(0, 1), each (token, head) row divided by its L2 norm in fp64;
+3. v: N(0, 1);
+4. gate normal z_g: g = -softplus(z_g) * gate_scale, stored as fp32
+   (softplus(z) = log1p(exp(z)), evaluated stably);
+5. beta normal z_b: beta = sigmoid(z_b), stored in the input dtype;
+6. initial state (when requested): N(0, 0.02^2), fp32, shape [N, H, dk, dv].
+
+Values are cast to the storage dtype with round-to-nearest-even (torch's
+``.to(torch.bfloat16)``).  The shapes stand in for the GDN layer shapes on
+the HyMo pages ("Model Architecture Walkthrough" section 5.5: B=4, T=4096,
+H=40, S=D=32), scaled to the five named workloads below; no dataset is used.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field, replace
+
+import numpy as np
+import torch
+
+_DTYPES = {"fp32": torch.float32, "bf16": torch.bfloat16}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    H: int
+    dk: int
+    dv: int
+    dtype: str
+    B: int = 1
+    T: int = 0
+    num_seqs: int = 0            # > 0 selects packed variable-length sequences
+    len_range: tuple = (0, 0)    # inclusive length range for varlen draws
+    gate_scale: float = 1.0
+    init_state: bool = False
+    seed: int = 0
+    notes: str = field(default="", compare=False)
+
+    @property
+    def varlen(self) -> bool:
+        return self.num_seqs > 0
+
+
+WORKLOADS = {
+    "tiny_fp32": Workload("tiny_fp32", B=1, T=256, H=2, dk=32, dv=32, dtype="fp32",
+                          gate_scale=0.1, init_state=False,
+                          notes="latency-bound; parity focus"),
+    "hymo_bf16": Workload("hymo_bf16", B=8, T=4096, H=16, dk=64, dv=64, dtype="bf16",
+                          gate_scale=1.0, init_state=False,
+                          notes="HyMo-shaped GDN layer; the benchmark workload"),
+    "wide_bf16": Workload("wide_bf16", B=4, T=8192, H=16, dk=128, dv=128, dtype="bf16",
+                          gate_scale=1.0, init_state=True),
+    "long_bf16": Workload("long_bf16", B=1, T=65536, H=16, dk=128, dv=128, dtype="bf16",
+                          gate_scale=0.01, init_state=False,
+                          notes="slow gates stress long-range state carry"),
+    "varlen_bf16": Workload("varlen_bf16", num_seqs=32, len_range=(128, 8192), H=8,
+                            dk=128, dv=256, dtype="bf16", gate_scale=1.0, init_state=True),
+}
+
+
+def custom(name="custom", **kw) -> Workload:
+    """A workload with explicit fields (edge-case tests)."""
+    return Workload(name=name, **kw)
+
+
+def with_seed(w: Workload, seed: int) -> Workload:
+    return replace(w, seed=seed)
+
+
+def _l2_rows(x: np.ndarray) -> np.ndarray:
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True))
+
+
+def _softplus(z: np.ndarray) -> np.ndarray:
+    return np.maximum(z, 0.0) + np.log1p(np.exp(-np.abs(z)))
+
+
+def _sigmoid(z: np.ndarray) -> np.ndarray:
+    return 0.5 * (1.0 + np.tanh(0.5 * z))
+
+
+def generate(w: Workload, lengths=None):
+    """Draw the inputs of workload ``w`` on the host.
+
+    Returns a dict of CPU torch tensors: q, k ``[B, T, H, dk]``; v ``[B, T, H, dv]``
+    (storage dtype); g ``[B, T, H]`` fp32; beta ``[B, T, H]`` (storage dtype);
+    initial_state ``[N, H, dk, dv]`` fp32 or None; cu_seqlens int32 ``[N+1]`` or
+    None; plus ``N`` and ``tokens``.  ``lengths`` overrides the varlen draw (the
+    draw still happens, so the stream order is unchanged).
+    """
+    rng = np.random.default_rng(w.seed)
+    dt = _DTYPES[w.dtype]
+    cu = None
+    if w.varlen:
+        drawn = rng.integers(w.len_range[0], w.len_range[1] + 1, w.num_seqs)
+        lens = np.asarray(drawn if lengths is None else lengths, dtype=np.int64)
+        cu_np = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+        B, T, N = 1, int(cu_np[-1]), len(lens)
+        cu = torch.from_numpy(cu_np.astype(np.int32))
+    else:
+        B, T, N = w.B, w.T, w.B
+    H, dk, dv = w.H, w.dk, w.dv
+
+    def draw(shape):
+        return rng.standard_normal(shape)
+
+    q = torch.from_numpy(_l2_rows(draw((B, T, H, dk)))).to(dt)
+    k = torch.from_numpy(_l2_rows(draw((B, T, H, dk)))).to(dt)
+    v = torch.from_numpy(draw((B, T, H, dv))).to(dt)
+    g = torch.from_numpy(-_softplus(draw((B, T, H))) * w.gate_scale).to(torch.float32)
+    beta = torch.from_numpy(_sigmoid(draw((B, T, H)))).to(dt)
+    s0 = None
+    if w.init_state:
+        s0 = torch.from_numpy(0.02 * draw((N, H, dk, dv))).to(torch.float32)
+    return {"q": q.contiguous(), "k": k.contiguous(), "v": v.contiguous(),
+            "g": g.contiguous(), "beta": beta.contiguous(), "initial_state": s0,
+            "cu_seqlens": cu, "N": N, "tokens": B * T}
+
+
+def head_tokens(w: Workload, inputs=None) -> int:
+    if inputs is not None:
+        return inputs["tokens"] * w.H
+    if w.varlen:
+        raise ValueError("varlen head-token count needs the drawn inputs")
+    return w.B * w.T * w.H
