@@ -1,0 +1,450 @@
+#!/usr/bin/env python3
+"""Benchmark of the gated delta rule forward pass on one GB300 per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload hymo_bf16]
+
+A step is one ``gdn_fwd`` call over the whole workload (every step of the hot
+path runs inside it).  The workload is the HyMo-shaped bf16 layer (B=8,
+T=4096, H=16, dk=dv=64).  Inputs live in HBM before the timed region; two
+input sets of 201 MB each (larger than the 129 MB L2) alternate between
+steps so no step reads inputs the previous step left in L2.  Under torchrun
+(N > 1) every rank runs its own replica (weak scaling, no data-path
+collective); the timed region is bracketed by a barrier and a device
+synchronisation on both sides and the maximum time over ranks is reported.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference for this
+method) on the host cores instead, on one batch row of the workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from linear_attention_recurrence_gated_gb300 import workloads as W  # noqa: E402
+
+METRIC = "GDN fwd tokens/s and TFLOP/s (% of GB300 bf16 roofline), 1 GPU"
+UNIT = "tokens/s"
+CHUNK = 64
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# --------------------------------------------------------------------------
+# algorithmic work (per head-token; chunk C = 64; MMA flops = 2 per FMA)
+# --------------------------------------------------------------------------
+def flops_per_head_token(dk: int, dv: int, C: int = CHUNK) -> float:
+    """KK^T, QK^T, W, U~, W.H, K~^T U, Q.H, P.U and the triangular inverse, per token."""
+    return C * (6 * dk + 4 * dv) + 6 * dk * dv + C * C / 3.0
+
+
+def bytes_per_head_token(dk: int, dv: int, elem: int) -> float:
+    """q, k, v, beta read and o written at `elem` bytes, g read as fp32."""
+    return elem * (2 * dk + 2 * dv + 1) + 4
+
+
+def algorithmic_bytes(w: W.Workload, tokens: int, N: int, with_init: bool) -> float:
+    elem = 4 if w.dtype == "fp32" else 2
+    state = 4 * w.dk * w.dv * N * w.H * (2 if with_init else 1)
+    return tokens * w.H * bytes_per_head_token(w.dk, w.dv, elem) + state
+
+
+def algorithmic_flops(w: W.Workload, tokens: int) -> float:
+    return tokens * w.H * flops_per_head_token(w.dk, w.dv)
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (barrier + max over ranks; no data-path collective)
+# --------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        torch.distributed.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world: int):
+    if world > 1:
+        if torch.distributed.get_backend() == "nccl":
+            torch.distributed.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, period_ms: int = 50):
+        self.rows = []
+        self.proc = None
+        self.period_ms = period_ms
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(self.period_ms)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self._t is not None:
+                self._t.join(timeout=5)
+
+    def summary(self, t0: float, t1: float, bus_id: str | None):
+        sel = []
+        for ts, line in self.rows:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 11:
+                continue
+            if bus_id and bus_id.lower() not in parts[2].lower():
+                continue
+            sel.append((ts, parts))
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
+                    "samples": 0}
+        inside = [p for ts, p in sel if t0 - 0.06 <= ts <= t1 + 0.06]
+        use = inside or [min(sel, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[1]]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[3]) for p in use if num(p[3]) is not None]
+        mx = [num(p[4]) for p in use if num(p[4]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in use for i in range(4)
+                          if p[7 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "power_w_max": max(
+                    (num(p[5]) for p in use if num(p[5]) is not None), default=None)}
+
+
+# --------------------------------------------------------------------------
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_sources_hash() -> str:
+    import hashlib
+    from linear_attention_recurrence_gated_gb300 import build as B
+    h = hashlib.sha256()
+    for p in sorted(B._deps()):
+        if p.endswith("build.py"):
+            continue
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, workload: str):
+    """dram bytes per launch from the committed ncu summary of this kernel and
+    workload, or None when absent or taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"source_sha:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_sources_hash():
+        return None
+    return float(m.group(1))
+
+
+def run_cpu_baseline(w: W.Workload, inputs, rows=None):
+    """Time the oracle as it stands on the host cores; return (tokens/s, cores, secs)."""
+    import oracle
+    oracle.build()
+    sel = slice(None) if rows is None else rows
+    q, k, v = inputs["q"][sel], inputs["k"][sel], inputs["v"][sel]
+    g, beta = inputs["g"][sel], inputs["beta"][sel]
+    s0 = inputs["initial_state"]
+    if s0 is not None and rows is not None:
+        s0 = s0[sel]
+    cores = oracle.default_threads()
+    t = time.perf_counter()
+    oracle.forward(q, k, v, g, beta, s0, inputs["cu_seqlens"], threads=cores)
+    dt = time.perf_counter() - t
+    return q.shape[0] * q.shape[1] / dt, cores, dt
+
+
+# --------------------------------------------------------------------------
+def bench_reference(args, w: W.Workload, rank: int, world: int):
+    if rank != 0:
+        return 0
+    inputs = W.generate(w)
+    B = inputs["q"].shape[0]
+    for i in range(args.warmup):
+        run_cpu_baseline(w, inputs, rows=slice(i % B, i % B + 1))
+    times, toks = [], 0
+    cores = 1
+    for i in range(args.steps):
+        rate, cores, dt = run_cpu_baseline(w, inputs, rows=slice(i % B, i % B + 1))
+        times.append(dt)
+        toks += w.T
+    total = sum(times)
+    value = toks / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+                   "storage": w.dtype, "chunk": CHUNK,
+                   "step": "one batch row (T tokens x H heads) per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"one batch row of {w.name} per step ({w.T} tokens x "
+                                   f"{w.H} heads), {args.steps} steps"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
+    from linear_attention_recurrence_gated_gb300 import gdn as G
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU (no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    G.lib()
+
+    host = W.generate(W.with_seed(w, w.seed + rank))
+    N, tokens = host["N"], host["tokens"]
+    names = ("q", "k", "v", "g", "beta")
+    sets = []
+    for _ in range(2):  # two resident input sets, alternated between steps
+        d = {n: host[n].to(dev) for n in names}
+        d["initial_state"] = None if host["initial_state"] is None else host["initial_state"].to(dev)
+        d["cu_seqlens"] = None if host["cu_seqlens"] is None else host["cu_seqlens"].to(dev)
+        d["o"] = torch.empty_like(d["v"])
+        d["final_state"] = torch.empty((N, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
+        sets.append(d)
+    ws = G.new_workspace(N, w.H, w.dk, w.dv, device=dev)
+    kname = G.gdn_fwd_kernel_name(w.dk, w.dv, host["q"].dtype)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        d = sets[i & 1]
+        G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"],
+                  d["cu_seqlens"], o=d["o"], final_state=d["final_state"], workspace=ws,
+                  stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    st = G.gdn_check(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {G.status_string(st)}")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler()
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step(i)
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    barrier(world)
+    time.sleep(0.15)
+    clocks.stop()
+    st = G.gdn_check(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {G.status_string(st)}")
+
+    local_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(local_ms, world)
+    per_launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    value = tokens * world * args.steps / (total_ms / 1e3)
+
+    # ---- end to end: pinned host inputs -> device -> gdn_fwd -> host result ----
+    pinned = {n: host[n].pin_memory() for n in names}
+    s0_pinned = None if host["initial_state"] is None else host["initial_state"].pin_memory()
+    o_host = torch.empty(host["v"].shape, dtype=host["v"].dtype).pin_memory()
+    s_host = torch.empty((N, w.H, w.dk, w.dv), dtype=torch.float32).pin_memory()
+    e2e_steps = max(1, min(args.steps, 50))
+    d = sets[0]
+    h2d = sum(pinned[n].numel() * pinned[n].element_size() for n in names) + \
+        (0 if s0_pinned is None else s0_pinned.numel() * 4)
+    d2h = o_host.numel() * o_host.element_size() + s_host.numel() * 4
+
+    def e2e_step():
+        for n in names:
+            d[n].copy_(pinned[n], non_blocking=True)
+        if s0_pinned is not None:
+            d["initial_state"].copy_(s0_pinned, non_blocking=True)
+        G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"],
+                  d["cu_seqlens"], o=d["o"], final_state=d["final_state"], workspace=ws,
+                  stream=stream)
+        o_host.copy_(d["o"], non_blocking=True)
+        s_host.copy_(d["final_state"], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    barrier(world)
+    st = G.gdn_check(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status after e2e steps: {G.status_string(st)}")
+    e2e_value = tokens * world * e2e_steps / (e2e_ms / 1e3)
+
+    if rank != 0:
+        return 0
+
+    hbm_gbs, bf16_tflops, peak_src = measured_peaks()
+    alg_bytes = algorithmic_bytes(w, tokens, N, host["initial_state"] is not None)
+    alg_flops = algorithmic_flops(w, tokens)
+    achieved_gbs = alg_bytes / (per_launch_ms / 1e3) / 1e9
+    achieved_tflops = alg_flops / (per_launch_ms / 1e3) / 1e12
+    traffic = committed_traffic(kname, w.name)
+    cpu_rate, cores, cpu_secs = run_cpu_baseline(w, host)
+    clk = clocks.summary(wall0, wall1, _bus_id(local))
+    arith = "f32" if kname.startswith("simt") else "bf16"
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": arith, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+                   "storage": w.dtype, "chunk": CHUNK, "kernel": kname,
+                   "l2": "two resident input sets of "
+                         f"{sum(sets[0][n].numel() * sets[0][n].element_size() for n in names) / 1e6:.0f}"
+                         " MB each (> 129 MB L2) alternate between steps",
+                   "parallelism": f"replicas x{world}"},
+        "tflops": achieved_tflops, "head_tokens_per_s": value * w.H,
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": achieved_gbs / hbm_gbs, "traffic": traffic,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "kernel_ms": per_launch_ms,
+                     "tensor_frac": achieved_tflops / bf16_tflops},
+        "cpu_baseline": {"value": cpu_rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"the whole {w.name} workload ({tokens} tokens x {w.H} "
+                                   f"heads), one pass, {cpu_secs:.1f} s"},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps * launches_per_step(kname),
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def launches_per_step(kernel_name: str) -> int:
+    return 1
+
+
+def _bus_id(local: int):
+    try:
+        p = torch.cuda.get_device_properties(local)
+        dom = getattr(p, "pci_domain_id", None)
+        bus = getattr(p, "pci_bus_id", None)
+        devid = getattr(p, "pci_device_id", None)
+        if bus is None:
+            return None
+        return f"{bus:02X}:{devid or 0:02X}" if dom is None else f"{dom:08X}:{bus:02X}:{devid or 0:02X}"
+    except Exception:
+        return None
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="hymo_bf16", choices=sorted(W.WORKLOADS))
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_setup()
+    w = W.WORKLOADS[args.workload]
+    try:
+        if args.impl == "reference":
+            return bench_reference(args, w, rank, world)
+        return bench_ours(args, w, rank, world, local)
+    finally:
+        if world > 1 and torch.distributed.is_initialized():
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,158 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) forward pass of the gated delta rule.
+ *
+ * The operation (per sequence n and head h, tokens t = 1..L_n):
+ *
+ *     S_t = alpha_t * S_{t-1} * (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *     o_t = S_t q_t,            alpha_t = exp(g_t)
+ *
+ * is the gated delta rule of Yang et al., "Gated Delta Networks" (arXiv
+ * 2412.06464), which "v1.0 Architecture & Design Spec", section 2.3 (Gated
+ * Delta Net block) and section 12a.1 (Fused Triton GDN kernel) name as the
+ * algorithm of HyMo's GDN kernel.  q_t is the read key and k_t the write key
+ * (c and b on the HyMo pages: "Model Architecture Walkthrough", section 5.2.1
+ * and 5.2.3); the decay is alpha_t = exp(g_t) with g_t <= 0 the natural-log
+ * gate (same page, section 5.2.1 and 5.3.1).  The state S_t (dv x dk) is
+ * stored TRANSPOSED, as H_t = S_t^T (dk rows x dv columns, fp32).  There is no
+ * 1/sqrt(dk) scale on q: o_t = S_t q_t exactly as written above.
+ *
+ * Method of the library: the tokens of each sequence are cut into chunks of
+ * 64 ("v1.0 Architecture & Design Spec", section 2.3: chunk_size 64 default;
+ * "Optimization Quartet", Triton GDN kernel section 3.2: intra-chunk parallel
+ * work, inter-chunk serial carry of the state).  Chunks restart at every
+ * sequence start.  Arithmetic is fp32 inside, with the state held in fp32 on
+ * chip; the output is stored in the caller's dtype ("Optimization Quartet",
+ * Triton GDN kernel section 3.3, "FP32 inside, cast back outside").
+ *
+ * Conventions common to every entry point
+ * ---------------------------------------
+ *  - Pointers named device pointers must point to memory of the current CUDA
+ *    device (cudaMalloc, cudaMallocAsync or a PyTorch CUDA tensor).  Every
+ *    device pointer must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  All work is enqueued asynchronously on it; no entry point
+ *    except gdn_check synchronises.
+ *  - The caller owns every buffer.  The library allocates no device memory,
+ *    keeps no per-call state, and only caches device attributes.
+ *  - There is no CPU fallback: when the library cannot run a call it returns
+ *    an error code and enqueues nothing.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  Host-side validation errors (INVALID_ARG, UNSUPPORTED,
+ * WORKSPACE) are returned before anything is enqueued.  Device-detected errors
+ * (TIMEOUT, BAD_SEQLENS, DEVICE_CHECK) are recorded in the workspace status
+ * word by the kernels and reported later by gdn_check. */
+typedef enum gdn_status {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or aliasing  */
+  GDN_ERR_UNSUPPORTED = 2,  /* well-formed but not implemented (head dims...) */
+  GDN_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than required        */
+  GDN_ERR_CUDA = 4,         /* a CUDA runtime call or a launch failed         */
+  GDN_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up             */
+  GDN_ERR_BAD_SEQLENS = 6,  /* cu_seqlens not 0 = cu[0] < cu[1] < ... = T     */
+  GDN_ERR_DEVICE_CHECK = 7  /* a device-side consistency check failed         */
+} gdn_status;
+
+/* Storage type of q, k, v, beta and o.  g, the states and all arithmetic are
+ * fp32 regardless. */
+typedef enum gdn_dtype { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* Flags for gdn_fwd. */
+enum {
+  /* Normalise q_t and k_t in-kernel: x / sqrt(sum(x^2) + 1e-6), fp32. */
+  GDN_QK_L2NORM = 1u << 0,
+  /* Use the fp32 CUDA-core kernel even for bf16 storage (the tensor-core
+   * kernel is the default for bf16).  fp32 storage always uses it. */
+  GDN_FORCE_SIMT = 1u << 1
+};
+
+/* Bytes of device workspace gdn_fwd needs for these sizes (>= 256; the first
+ * 256 bytes hold the device status word).  Never fails; returns 0 only for
+ * nonsensical sizes (any argument <= 0). */
+size_t gdn_fwd_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_dim_k,
+                              int32_t head_dim_v, uint32_t flags);
+
+/* Enqueue a zero fill of the first `workspace_bytes` bytes of `workspace` on
+ * `stream`.  A workspace must be zeroed once before its first use by gdn_fwd
+ * (gdn_check clears the status word it reports, so one fill is enough). */
+gdn_status gdn_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * gdn_fwd -- forward pass of the gated delta rule (the operation above).
+ *
+ * Shapes (all dense, row-major, "token-major, head-minor"):
+ *   q, k          [batch, seq_len, num_heads, head_dim_k]    dtype     device
+ *   v             [batch, seq_len, num_heads, head_dim_v]    dtype     device
+ *   g             [batch, seq_len, num_heads]                float32   device
+ *   beta          [batch, seq_len, num_heads]                dtype     device
+ *   initial_state [num_seqs, num_heads, head_dim_k, head_dim_v] float32 device, or NULL (= zeros)
+ *   cu_seqlens    [num_seqs + 1] int32 device, or NULL
+ *   o             [batch, seq_len, num_heads, head_dim_v]    dtype     device (written)
+ *   final_state   [num_seqs, num_heads, head_dim_k, head_dim_v] float32 device (written), or NULL
+ *
+ * Sequences: with cu_seqlens == NULL the batch rows are the sequences and
+ * num_seqs must equal batch.  With cu_seqlens != NULL, batch must be 1 and
+ * sequence n covers tokens cu_seqlens[n] .. cu_seqlens[n+1]-1 of the packed
+ * seq_len tokens; the offsets must satisfy cu_seqlens[0] = 0, strictly
+ * increasing (empty sequences are rejected), cu_seqlens[num_seqs] = seq_len.
+ * These offsets live in device memory, so they are checked by the kernel:
+ * a sequence whose bounds break the rule writes nothing and records
+ * GDN_ERR_BAD_SEQLENS for gdn_check.  No state crosses a sequence boundary.
+ *
+ * Values: g_t is the natural log of the decay alpha_t (expected <= 0; not
+ * clamped).  beta_t is used as given (expected in [0, 1]; not clamped).  The
+ * state element (i, j) of H = S^T multiplies key dimension i and value
+ * dimension j.
+ *
+ * Supported sizes: head_dim_k in {32, 64, 128}; head_dim_v a multiple of 32
+ * in [32, 256]; num_heads >= 1; num_seqs in [1, 65535]; chunk_size == 64.
+ * Anything else returns GDN_ERR_UNSUPPORTED (or INVALID_ARG if malformed).
+ *
+ * Aliasing: o and final_state must not overlap any input.  final_state may be
+ * the same buffer as initial_state (each state is read before it is written),
+ * which chains calls: a sequence split in two calls, with the first call's
+ * final_state passed as the second call's initial_state, gives the result of
+ * one call up to rounding.
+ *
+ * workspace: device, at least gdn_fwd_workspace_size(...) bytes, zeroed once
+ * before first use (gdn_workspace_init).  Calls that share a workspace must
+ * not run concurrently on different streams.
+ *
+ * Returns GDN_OK once the work is enqueued (errors detected on the device are
+ * reported by gdn_check), or an error code with nothing enqueued.
+ */
+gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
+                   const void *beta, const float *initial_state,
+                   const int32_t *cu_seqlens, void *o, float *final_state,
+                   int32_t batch, int32_t seq_len, int32_t num_heads,
+                   int32_t head_dim_k, int32_t head_dim_v, int32_t num_seqs,
+                   int32_t chunk_size, gdn_dtype dtype, uint32_t flags,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronise `stream`, read the status word in `workspace`, clear it, and
+ * return it (GDN_OK if no kernel recorded an error since the last check).
+ * Also returns GDN_ERR_CUDA if the stream synchronisation itself failed. */
+gdn_status gdn_check(void *workspace, void *stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *gdn_status_string(int32_t status);
+
+/* Name of the kernel gdn_fwd would launch for these arguments ("simt_fp32",
+ * "tc_bf16", ...) or NULL when the arguments are unsupported.  Host only. */
+const char *gdn_fwd_kernel_name(int32_t head_dim_k, int32_t head_dim_v,
+                                gdn_dtype dtype, uint32_t flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,138 @@
+// Host side of the C ABI declared in include/gdn.h: argument validation,
+// kernel selection and launch, and the status-word check.  Nothing here
+// computes any part of the recurrence; every step runs in the CUDA kernels.
+#include <stdint.h>
+#include <string.h>
+
+#include "gdn_internal.cuh"
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Half-open byte ranges [a, a+na) and [b, b+nb) overlap.
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+bool supported_dk(int dk) { return dk == 32 || dk == 64 || dk == 128; }
+bool supported_dv(int dv) { return dv >= 32 && dv <= 256 && dv % 32 == 0; }
+
+}  // namespace
+
+extern "C" {
+
+size_t gdn_fwd_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_dim_k,
+                              int32_t head_dim_v, uint32_t flags) {
+  (void)flags;
+  if (num_seqs <= 0 || num_heads <= 0 || head_dim_k <= 0 || head_dim_v <= 0) return 0;
+  return gdn::kStatusBytes;
+}
+
+gdn_status gdn_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
+  if (!workspace || workspace_bytes < gdn::kStatusBytes) return GDN_ERR_WORKSPACE;
+  if (cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
+const char *gdn_fwd_kernel_name(int32_t head_dim_k, int32_t head_dim_v, gdn_dtype dtype,
+                                uint32_t flags) {
+  (void)flags;
+  if (!supported_dk(head_dim_k) || !supported_dv(head_dim_v)) return nullptr;
+  if (dtype != GDN_F32 && dtype != GDN_BF16) return nullptr;
+  return dtype == GDN_F32 ? "simt_fp32" : "simt_bf16";
+}
+
+gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
+                   const void *beta, const float *initial_state, const int32_t *cu_seqlens,
+                   void *o, float *final_state, int32_t batch, int32_t seq_len,
+                   int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
+                   int32_t num_seqs, int32_t chunk_size, gdn_dtype dtype, uint32_t flags,
+                   void *workspace, size_t workspace_bytes, void *stream) {
+  // ---- shapes ----
+  if (batch <= 0 || seq_len <= 0 || num_heads <= 0 || head_dim_k <= 0 || head_dim_v <= 0 ||
+      num_seqs <= 0)
+    return GDN_ERR_INVALID_ARG;
+  if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  if (flags & ~(uint32_t)(GDN_QK_L2NORM | GDN_FORCE_SIMT)) return GDN_ERR_INVALID_ARG;
+  if (cu_seqlens ? batch != 1 : num_seqs != batch) return GDN_ERR_INVALID_ARG;
+  if (chunk_size != gdn::kChunk) return GDN_ERR_UNSUPPORTED;
+  if (!supported_dk(head_dim_k) || !supported_dv(head_dim_v)) return GDN_ERR_UNSUPPORTED;
+  if (num_seqs > 65535 || num_heads > 65535) return GDN_ERR_UNSUPPORTED;
+
+  // ---- pointers ----
+  if (!q || !k || !v || !g || !beta || !o) return GDN_ERR_INVALID_ARG;
+  const void *ptrs[] = {q, k, v, g, beta, initial_state, cu_seqlens, o, final_state};
+  for (const void *ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+  if (!workspace) return GDN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return GDN_ERR_INVALID_ARG;
+  if (workspace_bytes <
+      gdn_fwd_workspace_size(num_seqs, num_heads, head_dim_k, head_dim_v, flags))
+    return GDN_ERR_WORKSPACE;
+
+  // ---- aliasing: outputs must not overlap inputs (initial_state == final_state allowed) ----
+  const size_t e = dtype == GDN_F32 ? 4 : 2;
+  const size_t rows = (size_t)batch * (size_t)seq_len * (size_t)num_heads;
+  const size_t b_qk = rows * head_dim_k * e, b_v = rows * head_dim_v * e;
+  const size_t b_g = rows * 4, b_beta = rows * e;
+  const size_t b_state = (size_t)num_seqs * num_heads * head_dim_k * head_dim_v * 4;
+  const size_t b_cu = cu_seqlens ? (size_t)(num_seqs + 1) * 4 : 0;
+  struct Range { const void *p; size_t n; };
+  const Range inputs[] = {{q, b_qk}, {k, b_qk}, {v, b_v}, {g, b_g}, {beta, b_beta},
+                          {cu_seqlens, b_cu}, {workspace, workspace_bytes}};
+  for (const Range &r : inputs) {
+    if (overlaps(o, b_v, r.p, r.n)) return GDN_ERR_INVALID_ARG;
+    if (overlaps(final_state, b_state, r.p, r.n)) return GDN_ERR_INVALID_ARG;
+  }
+  if (overlaps(o, b_v, initial_state, b_state) || overlaps(o, b_v, final_state, b_state))
+    return GDN_ERR_INVALID_ARG;
+  if (initial_state && final_state && initial_state != final_state &&
+      overlaps(initial_state, b_state, final_state, b_state))
+    return GDN_ERR_INVALID_ARG;
+  if (overlaps(workspace, workspace_bytes, initial_state, b_state)) return GDN_ERR_INVALID_ARG;
+
+  gdn::FwdParams p;
+  p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g;
+  p.s0 = initial_state; p.cu = cu_seqlens; p.o = o; p.sN = final_state;
+  p.status = static_cast<gdn::DeviceStatus *>(workspace);
+  p.seq_len = seq_len;
+  p.num_heads = num_heads; p.dk = head_dim_k; p.dv = head_dim_v; p.num_seqs = num_seqs;
+  p.flags = flags;
+
+  const cudaError_t err = gdn::launch_fwd_simt(p, dtype, (cudaStream_t)stream);
+  return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_check(void *workspace, void *stream) {
+  if (!workspace) return GDN_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  gdn::DeviceStatus st;
+  memset(&st, 0, sizeof st);
+  if (cudaMemcpyAsync(&st, workspace, sizeof st, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (st.code == 0) return GDN_OK;
+  if (cudaMemsetAsync(workspace, 0, sizeof st, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+  return st.code <= GDN_ERR_DEVICE_CHECK ? (gdn_status)st.code : GDN_ERR_DEVICE_CHECK;
+}
+
+const char *gdn_status_string(int32_t status) {
+  switch (status) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: bad pointer, size or aliasing";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: sizes not implemented";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace missing or too small";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA runtime call or launch failed";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a bounded device wait gave up";
+    case GDN_ERR_BAD_SEQLENS: return "GDN_ERR_BAD_SEQLENS: cu_seqlens not strictly increasing from 0 to T";
+    case GDN_ERR_DEVICE_CHECK: return "GDN_ERR_DEVICE_CHECK: a device-side check failed";
+    default: return "GDN_ERR_UNKNOWN";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,77 @@
+// Internal declarations shared by the CUDA translation units of libgdn.
+// Not part of the public ABI (that is include/gdn.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+constexpr int kChunk = 64;  // tokens per chunk
+
+// Device status record at the start of the workspace.  The first error wins
+// (atomicCAS from 0); `seq` and `head` locate it, `aux` carries a detail.
+struct DeviceStatus {
+  uint32_t code;
+  uint32_t seq;
+  uint32_t head;
+  uint32_t aux;
+};
+constexpr size_t kStatusBytes = 256;
+
+// Everything one gdn_fwd launch needs, passed by value as a kernel argument.
+struct FwdParams {
+  const void *q, *k, *v, *beta;
+  const float *g;
+  const float *s0;
+  const int32_t *cu;
+  void *o;
+  float *sN;
+  DeviceStatus *status;
+  int64_t seq_len;      // tokens per batch row (dense) or packed total (varlen)
+  int32_t num_heads, dk, dv, num_seqs;
+  uint32_t flags;
+};
+
+__device__ __forceinline__ void report(DeviceStatus *st, uint32_t code, uint32_t seq,
+                                       uint32_t head, uint32_t aux) {
+  if (atomicCAS(&st->code, 0u, code) == 0u) {
+    st->seq = seq;
+    st->head = head;
+    st->aux = aux;
+  }
+}
+
+// Bounds of sequence n: [start, start + len).  Returns false (after recording
+// GDN_ERR_BAD_SEQLENS) when cu_seqlens breaks 0 = cu[0] < ... < cu[N] = T.
+__device__ __forceinline__ bool sequence_bounds(const FwdParams &p, int n, int h,
+                                                int64_t &start, int64_t &len) {
+  if (p.cu == nullptr) {
+    start = (int64_t)n * p.seq_len;
+    len = p.seq_len;
+    return true;
+  }
+  const int64_t s = p.cu[n], e = p.cu[n + 1];
+  const bool ok = s >= 0 && e > s && e <= p.seq_len && (n != 0 || s == 0) &&
+                  (n != p.num_seqs - 1 || e == p.seq_len);
+  if (!ok) {
+    report(p.status, GDN_ERR_BAD_SEQLENS, (uint32_t)n, (uint32_t)h, 0u);
+    return false;
+  }
+  start = s;
+  len = e - s;
+  return true;
+}
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void store_out(float *p, float x) { *p = x; }
+__device__ __forceinline__ void store_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+// Launchers (one per kernel family).  Return a cudaError_t from the launch.
+cudaError_t launch_fwd_simt(const FwdParams &p, gdn_dtype dtype, cudaStream_t stream);
+
+}  // namespace gdn

@@ -1,0 +1,182 @@
+"""Python binding of the C ABI in ``include/gdn.h`` (argument marshalling only).
+
+Every function here has the name of the C entry point it calls.  The binding
+checks tensor devices, dtypes, shapes and contiguity, passes raw device
+pointers and the current CUDA stream, and turns status codes into
+exceptions.  It computes nothing itself and has no fallback: if ``libgdn.so``
+is missing or CUDA is unavailable it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdn.so")
+
+GDN_OK = 0
+STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED",
+                3: "GDN_ERR_WORKSPACE", 4: "GDN_ERR_CUDA", 5: "GDN_ERR_TIMEOUT",
+                6: "GDN_ERR_BAD_SEQLENS", 7: "GDN_ERR_DEVICE_CHECK"}
+GDN_F32, GDN_BF16 = 0, 1
+GDN_QK_L2NORM = 1 << 0
+GDN_FORCE_SIMT = 1 << 1
+CHUNK_SIZE = 64
+
+# Every symbol include/gdn.h declares.
+EXPORTED = ("gdn_fwd_workspace_size", "gdn_workspace_init", "gdn_fwd", "gdn_check",
+            "gdn_status_string", "gdn_fwd_kernel_name")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def lib() -> ctypes.CDLL:
+    """Load ``libgdn.so`` (raises if it was not built; there is no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} not found: build it with "
+                    "`python -m linear_attention_recurrence_gated_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, u32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_size_t
+            L.gdn_fwd_workspace_size.restype = sz
+            L.gdn_fwd_workspace_size.argtypes = [i32, i32, i32, i32, u32]
+            L.gdn_workspace_init.restype = ctypes.c_int
+            L.gdn_workspace_init.argtypes = [vp, sz, vp]
+            L.gdn_fwd.restype = ctypes.c_int
+            L.gdn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                  i32, i32, i32, i32, i32, i32, i32, ctypes.c_int, u32,
+                                  vp, sz, vp]
+            L.gdn_check.restype = ctypes.c_int
+            L.gdn_check.argtypes = [vp, vp]
+            L.gdn_status_string.restype = ctypes.c_char_p
+            L.gdn_status_string.argtypes = [i32]
+            L.gdn_fwd_kernel_name.restype = ctypes.c_char_p
+            L.gdn_fwd_kernel_name.argtypes = [i32, i32, ctypes.c_int, u32]
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().gdn_status_string(int(status)).decode()
+    except RuntimeError:
+        return STATUS_NAMES.get(int(status), f"status {status}")
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return GDN_F32
+    if t == torch.bfloat16:
+        return GDN_BF16
+    raise TypeError(f"gdn: unsupported storage dtype {t} (float32 or bfloat16)")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def gdn_fwd_workspace_size(num_seqs: int, num_heads: int, head_dim_k: int, head_dim_v: int,
+                           flags: int = 0) -> int:
+    return int(lib().gdn_fwd_workspace_size(num_seqs, num_heads, head_dim_k, head_dim_v, flags))
+
+
+def gdn_workspace_init(workspace: torch.Tensor, stream=None) -> None:
+    st = lib().gdn_workspace_init(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream_handle(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_workspace_init")
+
+
+def new_workspace(num_seqs, num_heads, head_dim_k, head_dim_v, flags=0, device=None):
+    """A zeroed workspace of the size gdn_fwd needs (the caller keeps it)."""
+    n = gdn_fwd_workspace_size(num_seqs, num_heads, head_dim_k, head_dim_v, flags)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def gdn_check(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    return int(lib().gdn_check(_ptr(workspace), _stream_handle(stream)))
+
+
+def gdn_fwd_kernel_name(head_dim_k, head_dim_v, dtype: torch.dtype, flags: int = 0):
+    r = lib().gdn_fwd_kernel_name(head_dim_k, head_dim_v, _dtype_code(dtype), flags)
+    return None if r is None else r.decode()
+
+
+def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
+            final_state=None, output_final_state=True, workspace=None,
+            qk_l2norm=False, force_simt=False, stream=None, check=False):
+    """Forward pass of the gated delta rule through the C ABI.
+
+    q, k ``[B, T, H, dk]``; v ``[B, T, H, dv]``; g ``[B, T, H]`` fp32; beta
+    ``[B, T, H]``; all CUDA, contiguous, q/k/v/beta/o in one storage dtype
+    (float32 or bfloat16).  initial_state ``[N, H, dk, dv]`` fp32 or None;
+    cu_seqlens int32 ``[N+1]`` on the device (then B must be 1) or None.
+    ``o`` / ``final_state`` may be given to write into preallocated outputs
+    (``final_state`` may be ``initial_state``).  Returns ``(o, final_state)``.
+    With ``check=True`` the call synchronises and raises on a device-side error.
+    """
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    tensors = [q, k, v, g, beta] + [t for t in (initial_state, cu_seqlens, o, final_state)
+                                    if t is not None]
+    for t in tensors:
+        if not t.is_cuda:
+            raise ValueError("gdn_fwd: every tensor must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("gdn_fwd: every tensor must be contiguous")
+    dcode = _dtype_code(q.dtype)
+    if k.dtype != q.dtype or v.dtype != q.dtype or beta.dtype != q.dtype:
+        raise TypeError("gdn_fwd: q, k, v and beta must share one storage dtype")
+    if g.dtype != torch.float32:
+        raise TypeError("gdn_fwd: g must be float32")
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3] or g.shape != (B, T, H) or \
+            beta.shape != (B, T, H):
+        raise ValueError("gdn_fwd: shape mismatch among q, k, v, g, beta")
+    if initial_state is not None and (initial_state.dtype != torch.float32 or
+                                      initial_state.shape != (N, H, dk, dv)):
+        raise ValueError("gdn_fwd: initial_state must be float32 [N, H, dk, dv]")
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("gdn_fwd: cu_seqlens must be int32")
+    if o is None:
+        o = torch.empty_like(v)
+    elif o.shape != v.shape or o.dtype != v.dtype:
+        raise ValueError("gdn_fwd: o must match v in shape and dtype")
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    if final_state is not None and (final_state.dtype != torch.float32 or
+                                    final_state.shape != (N, H, dk, dv)):
+        raise ValueError("gdn_fwd: final_state must be float32 [N, H, dk, dv]")
+    flags = (GDN_QK_L2NORM if qk_l2norm else 0) | (GDN_FORCE_SIMT if force_simt else 0)
+    if workspace is None:
+        workspace = new_workspace(N, H, dk, dv, flags, device=q.device)
+    st = lib().gdn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                       _ptr(cu_seqlens), _ptr(o), _ptr(final_state), B, T, H, dk, dv, N,
+                       CHUNK_SIZE, dcode, flags, _ptr(workspace),
+                       workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_fwd")
+    if check:
+        st = gdn_check(workspace, stream)
+        if st != GDN_OK:
+            raise GdnError(st, "gdn_fwd (device)")
+    return o, final_state

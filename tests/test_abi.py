@@ -1,0 +1,99 @@
+"""CPU tests of the C-ABI library: it loads, exports every symbol that
+include/gdn.h declares, and rejects malformed calls on the host before
+touching the GPU (no call here launches anything)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_attention_recurrence_gated_gb300 import build as gbuild
+from linear_attention_recurrence_gated_gb300 import gdn as G
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    gbuild.build()
+    return G.lib()
+
+
+def declared_functions():
+    hdr = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_0-9]+)\s*\(", hdr)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared_functions() == sorted(G.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for code, name in G.STATUS_NAMES.items():
+        assert G.status_string(code).startswith(name)
+    assert G.status_string(99) == "GDN_ERR_UNKNOWN"
+
+
+def test_workspace_size(L):
+    assert G.gdn_fwd_workspace_size(8, 16, 64, 64) >= 256
+    assert G.gdn_fwd_workspace_size(0, 16, 64, 64) == 0
+
+
+def test_kernel_names(L):
+    import torch
+    assert G.gdn_fwd_kernel_name(64, 64, torch.float32) == "simt_fp32"
+    assert G.gdn_fwd_kernel_name(48, 64, torch.bfloat16) is None
+    assert G.gdn_fwd_kernel_name(64, 48, torch.bfloat16) is None
+
+
+# ---- host-side validation with fake (never dereferenced) device addresses ----
+BASE = 1 << 40
+
+
+def call(L, **over):
+    B, T, H, dk, dv = 2, 100, 3, 64, 64
+    rows = B * T * H
+    a = dict(q=BASE, k=BASE + (1 << 30), v=BASE + (2 << 30), g=BASE + (3 << 30),
+             beta=BASE + (4 << 30), s0=None, cu=None, o=BASE + (5 << 30),
+             sN=BASE + (6 << 30), B=B, T=T, H=H, dk=dk, dv=dv, N=B, chunk=64,
+             dtype=G.GDN_BF16, flags=0, ws=BASE + (7 << 30), ws_bytes=256)
+    a.update(over)
+    vp = ctypes.c_void_p
+    return L.gdn_fwd(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]),
+                     vp(a["s0"]), vp(a["cu"]), vp(a["o"]), vp(a["sN"]), a["B"], a["T"],
+                     a["H"], a["dk"], a["dv"], a["N"], a["chunk"], a["dtype"], a["flags"],
+                     vp(a["ws"]), a["ws_bytes"], vp(0))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(dk=48), 2), (dict(dk=256), 2), (dict(dv=48), 2), (dict(dv=288), 2),
+    (dict(chunk=32), 2), (dict(dtype=7), 1), (dict(flags=1 << 9), 1),
+    (dict(q=None), 1), (dict(o=None), 1), (dict(g=None), 1), (dict(beta=None), 1),
+    (dict(q=BASE + 8), 1), (dict(o=BASE + (5 << 30) + 4), 1), (dict(sN=BASE + (6 << 30) + 2), 1),
+    (dict(ws=None), 3), (dict(ws_bytes=255), 3), (dict(ws=BASE + (7 << 30) + 8), 1),
+    (dict(B=0), 1), (dict(T=0), 1), (dict(H=0), 1), (dict(N=3), 1),
+    (dict(cu=BASE + (8 << 30)), 1),                        # cu_seqlens needs batch == 1
+    (dict(B=1, N=70000, cu=BASE + (8 << 30)), 2),          # too many sequences
+    (dict(o=BASE), 1),                                     # o aliases q
+    (dict(o=BASE + (2 << 30) + 64), 1),                    # o overlaps v
+    (dict(sN=BASE + (4 << 30)), 1),                        # final_state aliases beta
+    (dict(s0=BASE + (6 << 30) + 16), 1),                   # initial/final partial overlap
+    (dict(ws=BASE + (5 << 30)), 1),                        # workspace inside o
+])
+def test_host_validation_rejects_before_launch(L, over, code):
+    assert call(L, **over) == code
+
+
+def test_workspace_init_rejects_small(L):
+    assert L.gdn_workspace_init(ctypes.c_void_p(BASE), 16, ctypes.c_void_p(0)) == 3
+    assert L.gdn_workspace_init(None, 4096, ctypes.c_void_p(0)) == 3
+
+
+def test_check_rejects_null_workspace(L):
+    assert L.gdn_check(None, ctypes.c_void_p(0)) == 3

@@ -1,0 +1,171 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded inputs.  Relative L2 over whole tensors; bounds in parity.TOL."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+from linear_attention_recurrence_gated_gb300 import gdn as G
+from linear_attention_recurrence_gated_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA not available: the GPU tests need a GB300")
+    G.lib()
+    oracle.build()
+
+
+def _check(inp, dtype, **kw):
+    ro, rs, o, s = parity.compare(inp, gpu_kw=kw.get("gpu"), oracle_kw=kw.get("orc"))
+    to, ts = parity.TOL[dtype]
+    assert ro <= to and rs <= ts, f"rel L2 o={ro:.3e} (<= {to}), state={rs:.3e} (<= {ts})"
+    return ro, rs
+
+
+# ---------------- the five named workloads, full size ----------------
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_workload_full_size(name):
+    w = W.WORKLOADS[name]
+    inp = W.generate(w)
+    ro, rs = _check(inp, W._DTYPES[w.dtype])
+    print(f"{name}: rel L2 o={ro:.3e} state={rs:.3e}")
+
+
+@pytest.mark.parametrize("name", ["hymo_bf16", "wide_bf16"])
+def test_workload_full_size_simt(name):
+    """The fp32 CUDA-core kernel on the bf16 workloads (forced)."""
+    w = W.WORKLOADS[name]
+    inp = W.generate(w)
+    _check(inp, torch.bfloat16, gpu=dict(force_simt=True))
+
+
+# ---------------- edge cases: ragged tails, tiny T, head-dim mixes ----------------
+SHAPES = [(1, 1, 1, 32, 32), (1, 63, 2, 64, 64), (2, 64, 1, 32, 64), (1, 65, 2, 64, 32),
+          (2, 130, 3, 128, 64), (1, 200, 2, 32, 256), (1, 129, 1, 128, 256),
+          (3, 77, 2, 64, 128), (1, 1000, 1, 128, 128)]
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("B,T,H,dk,dv", SHAPES)
+@pytest.mark.parametrize("init", [False, True])
+def test_edge_shapes(dtype, B, T, H, dk, dv, init):
+    w = W.custom(B=B, T=T, H=H, dk=dk, dv=dv, dtype=dtype, gate_scale=1.0,
+                 init_state=init, seed=1000 + T + dk + dv)
+    _check(W.generate(w), W._DTYPES[dtype])
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_varlen_small(dtype):
+    lens = [1, 63, 64, 65, 2, 300, 17]
+    w = W.custom(num_seqs=len(lens), len_range=(1, 300), H=3, dk=64, dv=96, dtype=dtype,
+                 init_state=True, seed=21)
+    _check(W.generate(w, lengths=lens), W._DTYPES[dtype])
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_varlen_bitwise_equals_separate_runs(dtype):
+    lens = [5, 64, 129, 1, 250]
+    w = W.custom(num_seqs=len(lens), len_range=(1, 300), H=2, dk=128, dv=64, dtype=dtype,
+                 init_state=True, seed=22)
+    inp = W.generate(w, lengths=lens)
+    o, s = parity.gpu_forward(inp)
+    cu = inp["cu_seqlens"].tolist()
+    for n in range(len(lens)):
+        a, b = cu[n], cu[n + 1]
+        part = {"q": inp["q"][:, a:b].contiguous(), "k": inp["k"][:, a:b].contiguous(),
+                "v": inp["v"][:, a:b].contiguous(), "g": inp["g"][:, a:b].contiguous(),
+                "beta": inp["beta"][:, a:b].contiguous(),
+                "initial_state": inp["initial_state"][n:n + 1].contiguous(),
+                "cu_seqlens": None}
+        o1, s1 = parity.gpu_forward(part)
+        assert torch.equal(o1, o[:, a:b]), f"sequence {n}: o differs"
+        assert torch.equal(s1, s[n:n + 1]), f"sequence {n}: final state differs"
+
+
+def test_qk_l2norm_flag():
+    w = W.custom(B=2, T=150, H=2, dk=64, dv=64, dtype="fp32", seed=23)
+    inp = W.generate(w)
+    scale = torch.rand(2, 150, 2, 1) * 5 + 0.5
+    inp["q"] = (inp["q"] * scale).contiguous()
+    inp["k"] = (inp["k"] * scale.flip(1)).contiguous()
+    _check(inp, torch.float32, gpu=dict(qk_l2norm=True), orc=dict(qk_l2norm=True))
+
+
+def test_beta_zero_closed_form_on_gpu():
+    w = W.custom(B=1, T=300, H=2, dk=64, dv=64, dtype="fp32", init_state=True, seed=24)
+    inp = W.generate(w)
+    inp["beta"] = torch.zeros_like(inp["beta"])
+    o, s = parity.gpu_forward(inp)
+    G_ = torch.cumsum(inp["g"].double(), dim=1)
+    H0 = inp["initial_state"].double()
+    o_ref = torch.exp(G_)[..., None] * torch.einsum("bhkd,bthk->bthd", H0, inp["q"].double())
+    s_ref = torch.exp(G_[:, -1])[..., None, None] * H0
+    assert parity.rel(o.double().cpu(), o_ref) < 1e-4
+    assert parity.rel(s.double().cpu(), s_ref) < 1e-4
+
+
+def test_golden_two_token_on_gpu():
+    """The hand-worked example of tests/golden, embedded in dk = dv = 32 with zeros."""
+    import json, os
+    gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                       "two_token_hand.json")))
+    q = torch.zeros(1, 2, 1, 32); k = torch.zeros(1, 2, 1, 32); v = torch.zeros(1, 2, 1, 32)
+    q[0, :, 0, :2] = torch.tensor(gold["q"]); k[0, :, 0, :2] = torch.tensor(gold["k"])
+    v[0, :, 0, :2] = torch.tensor(gold["v"])
+    g = torch.log(torch.tensor(gold["alpha"], dtype=torch.float32)).view(1, 2, 1)
+    beta = torch.tensor(gold["beta"], dtype=torch.float32).view(1, 2, 1)
+    inp = {"q": q, "k": k, "v": v, "g": g, "beta": beta, "initial_state": None,
+           "cu_seqlens": None}
+    o, s = parity.gpu_forward(inp)
+    assert np.allclose(o[0, :, 0, :2].cpu().numpy(), gold["o"], rtol=1e-5, atol=1e-6)
+    assert np.allclose(s[0, 0, :2, :2].cpu().numpy(), gold["final_state_dk_by_dv"],
+                       rtol=1e-5, atol=1e-6)
+    assert float(o[..., 2:].abs().max()) == 0.0
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_state_chaining_and_in_place(dtype):
+    w = W.custom(B=2, T=300, H=2, dk=64, dv=64, dtype=dtype, init_state=True, seed=25)
+    inp = parity.to_dev(W.generate(w))
+    o, s = G.gdn_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                     inp["initial_state"], check=True)
+    T1 = 100
+    state = inp["initial_state"].clone()
+    parts = []
+    for a, b in ((0, T1), (T1, 300)):
+        sl = lambda x: x[:, a:b].contiguous()
+        oo, _ = G.gdn_fwd(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["g"]),
+                          sl(inp["beta"]), state, final_state=state, check=True)  # in place
+        parts.append(oo)
+    to, ts = parity.TOL[W._DTYPES[dtype]]
+    assert parity.rel(torch.cat(parts, 1).double().cpu(), o.double().cpu()) < to
+    assert parity.rel(state.double().cpu(), s.double().cpu()) < ts
+
+
+def test_no_final_state():
+    w = W.custom(B=1, T=70, H=1, dk=32, dv=32, dtype="bf16", seed=26)
+    inp = parity.to_dev(W.generate(w))
+    o1, s1 = G.gdn_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], check=True)
+    o2, s2 = G.gdn_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                       output_final_state=False, check=True)
+    assert s2 is None and torch.equal(o1, o2)
+
+
+@pytest.mark.parametrize("cu", [[0, 10, 10, 40], [0, 30, 20, 40], [0, 10, 20, 39], [1, 10, 20, 40]])
+def test_bad_seqlens_reported(cu):
+    """Malformed offsets are found on the device and reported by gdn_check;
+    the affected sequences write nothing."""
+    w = W.custom(B=1, T=40, H=2, dk=32, dv=32, dtype="fp32", seed=27)
+    inp = parity.to_dev(W.generate(w))
+    cu_t = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    ws = G.new_workspace(3, 2, 32, 32)
+    o = torch.full_like(inp["v"], 7.0)
+    G.gdn_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], None, cu_t, o=o,
+              workspace=ws)
+    assert G.gdn_check(ws) == 6
+    assert G.gdn_check(ws) == 0  # the check cleared the status word
