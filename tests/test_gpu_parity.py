@@ -97,7 +97,9 @@ def test_qk_l2norm_flag():
 
 
 def test_beta_zero_closed_form_on_gpu():
-    w = W.custom(B=1, T=300, H=2, dk=64, dv=64, dtype="fp32", init_state=True, seed=24)
+    # gentle gates keep exp(sum g) inside fp32 range over the 300 tokens
+    w = W.custom(B=1, T=300, H=2, dk=64, dv=64, dtype="fp32", init_state=True,
+                 gate_scale=0.02, seed=24)
     inp = W.generate(w)
     inp["beta"] = torch.zeros_like(inp["beta"])
     o, s = parity.gpu_forward(inp)
