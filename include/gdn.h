@@ -30,10 +30,11 @@
  *    device (cudaMalloc, cudaMallocAsync or a PyTorch CUDA tensor).  Every
  *    device pointer must be 16-byte aligned.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
- *    stream).  All work is enqueued asynchronously on it; no entry point
- *    except gdn_check synchronises.
- *  - The caller owns every buffer.  The library allocates no device memory,
- *    keeps no per-call state, and only caches device attributes.
+ *    stream).  All work is enqueued asynchronously on it; only gdn_check,
+ *    and gdn_fwd_static_scratch when asked to check, synchronise.
+ *  - The caller owns every buffer.  The library allocates no device memory
+ *    and keeps no per-call state; it caches device attributes, and holds one
+ *    256-byte static device array used only by gdn_fwd_static_scratch.
  *  - There is no CPU fallback: when the library cannot run a call it returns
  *    an error code and enqueues nothing.
  */
@@ -137,6 +138,43 @@ gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
                    int32_t head_dim_k, int32_t head_dim_v, int32_t num_seqs,
                    int32_t chunk_size, gdn_dtype dtype, uint32_t flags,
                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * gdn_fwd_static_scratch -- gdn_fwd for callers that cannot allocate device
+ * memory.  The pages have no counterpart to this entry point; it exists for
+ * callers that must not call cudaMalloc: a plugin or extension running inside
+ * a host framework that owns every device allocation through its own pool, a
+ * latency-critical loop where an allocation could synchronise the device, or
+ * a process held to a fixed device-memory budget.  Such a caller still passes
+ * its inputs and outputs, but no workspace.
+ *
+ * Instead of a caller workspace, the 256-byte device status record lives in a
+ * file-scope __device__ array inside the library.  Every GPU that loads the
+ * library holds those 256 bytes until the process exits.  The array is shared
+ * by every call on that device and keeps the last call's contents, so each
+ * call first enqueues a zero fill of it on `stream`.  Calls that overlap on
+ * the GPU (different streams, no ordering between them) race on the array and
+ * may report each other's device errors; serialise them.
+ *
+ * The first call on a device, with that device current, looks up the array's
+ * device address (cudaGetSymbolAddress) and caches it; make that first call
+ * before any stream capture begins.
+ *
+ * Arguments are those of gdn_fwd without workspace/workspace_bytes, plus
+ * `check`: when nonzero the call synchronises `stream` after the launch and
+ * returns any error the kernel recorded (GDN_ERR_BAD_SEQLENS, ...); when zero
+ * it returns once the work is enqueued and device-detected errors are not
+ * reported.  Sizes whose scratch need (gdn_fwd_workspace_size) exceeds the
+ * 256-byte array are rejected with GDN_ERR_WORKSPACE before anything is
+ * enqueued.  The call performs no device allocation or free.
+ */
+gdn_status gdn_fwd_static_scratch(const void *q, const void *k, const void *v, const float *g,
+                                  const void *beta, const float *initial_state,
+                                  const int32_t *cu_seqlens, void *o, float *final_state,
+                                  int32_t batch, int32_t seq_len, int32_t num_heads,
+                                  int32_t head_dim_k, int32_t head_dim_v, int32_t num_seqs,
+                                  int32_t chunk_size, gdn_dtype dtype, uint32_t flags,
+                                  int32_t check, void *stream);
 
 /* Synchronise `stream`, read the status word in `workspace`, clear it, and
  * return it (GDN_OK if no kernel recorded an error since the last check).

@@ -1,0 +1,72 @@
+// gdn_fwd_static_scratch: the forward pass for callers that cannot allocate
+// device memory.  The status record that gdn_fwd keeps in the caller's
+// workspace lives here in a file-scope __device__ array instead, so the
+// caller passes only inputs and outputs.  No cudaMalloc/cudaFree is called.
+#include <mutex>
+#include <string.h>
+
+#include "gdn_internal.cuh"
+
+namespace {
+
+// Scratch for one call: the device status record.  Every GPU that loads the
+// library holds these bytes until the process exits; all calls on a device
+// share them.
+constexpr size_t kStaticScratchBytes = 256;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the array on the current device, looked up once per
+// device (host code may not use the symbol itself as a device pointer).
+gdn_status scratch_address(void **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_addr[dev] == nullptr) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr)
+      return GDN_ERR_CUDA;
+    g_scratch_addr[dev] = ptr;
+  }
+  *out = g_scratch_addr[dev];
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" gdn_status gdn_fwd_static_scratch(
+    const void *q, const void *k, const void *v, const float *g, const void *beta,
+    const float *initial_state, const int32_t *cu_seqlens, void *o, float *final_state,
+    int32_t batch, int32_t seq_len, int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
+    int32_t num_seqs, int32_t chunk_size, gdn_dtype dtype, uint32_t flags, int32_t check,
+    void *stream) {
+  const size_t need =
+      gdn_fwd_workspace_size(num_seqs, num_heads, head_dim_k, head_dim_v, flags);
+  if (need == 0) return GDN_ERR_INVALID_ARG;
+  if (need > kStaticScratchBytes) return GDN_ERR_WORKSPACE;  // beyond the static maximum
+
+  void *scratch = nullptr;
+  gdn_status st = scratch_address(&scratch);
+  if (st != GDN_OK) return st;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  // The array keeps the previous call's contents: the status must start at zero.
+  if (cudaMemsetAsync(scratch, 0, kStaticScratchBytes, s) != cudaSuccess) return GDN_ERR_CUDA;
+
+  st = gdn_fwd(q, k, v, g, beta, initial_state, cu_seqlens, o, final_state, batch, seq_len,
+               num_heads, head_dim_k, head_dim_v, num_seqs, chunk_size, dtype, flags, scratch,
+               kStaticScratchBytes, stream);
+  if (st != GDN_OK || !check) return st;
+
+  gdn::DeviceStatus rec;
+  memset(&rec, 0, sizeof rec);
+  if (cudaMemcpyAsync(&rec, scratch, sizeof rec, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (rec.code == 0) return GDN_OK;
+  return rec.code <= GDN_ERR_DEVICE_CHECK ? (gdn_status)rec.code : GDN_ERR_DEVICE_CHECK;
+}

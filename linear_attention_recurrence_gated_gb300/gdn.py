@@ -28,7 +28,7 @@ CHUNK_SIZE = 64
 
 # Every symbol include/gdn.h declares.
 EXPORTED = ("gdn_fwd_workspace_size", "gdn_workspace_init", "gdn_fwd", "gdn_check",
-            "gdn_status_string", "gdn_fwd_kernel_name")
+            "gdn_status_string", "gdn_fwd_kernel_name", "gdn_fwd_static_scratch")
 
 _lib = None
 _lock = threading.Lock()
@@ -65,6 +65,10 @@ def lib() -> ctypes.CDLL:
             L.gdn_status_string.argtypes = [i32]
             L.gdn_fwd_kernel_name.restype = ctypes.c_char_p
             L.gdn_fwd_kernel_name.argtypes = [i32, i32, ctypes.c_int, u32]
+            L.gdn_fwd_static_scratch.restype = ctypes.c_int
+            L.gdn_fwd_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                 i32, i32, i32, i32, i32, i32, i32,
+                                                 ctypes.c_int, u32, i32, vp]
             _lib = L
     return _lib
 
@@ -180,3 +184,23 @@ def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
         if st != GDN_OK:
             raise GdnError(st, "gdn_fwd (device)")
     return o, final_state
+
+
+def gdn_fwd_static_scratch(q, k, v, g, beta, initial_state, cu_seqlens, o, final_state, *,
+                           qk_l2norm=False, force_simt=False, check=True, stream=None) -> int:
+    """Forward pass for callers that cannot allocate device memory.
+
+    Same tensors as ``gdn_fwd`` but every output must be passed in (this call
+    allocates nothing, not even through torch) and there is no workspace: the
+    library's own 256-byte device array holds the status record.  With
+    ``check`` the call synchronises and returns the device status code; the
+    status is returned, not raised, so the caller decides.
+    """
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    flags = (GDN_QK_L2NORM if qk_l2norm else 0) | (GDN_FORCE_SIMT if force_simt else 0)
+    return int(lib().gdn_fwd_static_scratch(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens),
+        _ptr(o), _ptr(final_state), B, T, H, dk, dv, N, CHUNK_SIZE, _dtype_code(q.dtype),
+        flags, 1 if check else 0, _stream_handle(stream)))
