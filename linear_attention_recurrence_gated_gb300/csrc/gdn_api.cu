@@ -38,11 +38,20 @@ gdn_status gdn_workspace_init(void *workspace, size_t workspace_bytes, void *str
   return GDN_OK;
 }
 
+namespace {
+bool use_tc(int dk, int dv, gdn_dtype dtype, uint32_t flags) {
+  // The tensor-core kernel multiplies the TMA-loaded q/k tiles as they arrive,
+  // so in-kernel q/k normalisation runs on the fp32 kernel.
+  return dtype == GDN_BF16 && !(flags & (GDN_FORCE_SIMT | GDN_QK_L2NORM)) &&
+         gdn::tc_supported(dk, dv);
+}
+}  // namespace
+
 const char *gdn_fwd_kernel_name(int32_t head_dim_k, int32_t head_dim_v, gdn_dtype dtype,
                                 uint32_t flags) {
-  (void)flags;
   if (!supported_dk(head_dim_k) || !supported_dv(head_dim_v)) return nullptr;
   if (dtype != GDN_F32 && dtype != GDN_BF16) return nullptr;
+  if (use_tc(head_dim_k, head_dim_v, dtype, flags)) return "tc_bf16";
   return dtype == GDN_F32 ? "simt_fp32" : "simt_bf16";
 }
 
@@ -103,7 +112,9 @@ gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
   p.num_heads = num_heads; p.dk = head_dim_k; p.dv = head_dim_v; p.num_seqs = num_seqs;
   p.flags = flags;
 
-  const cudaError_t err = gdn::launch_fwd_simt(p, dtype, (cudaStream_t)stream);
+  const cudaError_t err = use_tc(head_dim_k, head_dim_v, dtype, flags)
+                              ? gdn::launch_fwd_tc(p, (cudaStream_t)stream)
+                              : gdn::launch_fwd_simt(p, dtype, (cudaStream_t)stream);
   return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
