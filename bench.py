@@ -181,13 +181,27 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def kernel_sources_hash() -> str:
+# The translation unit each kernel is compiled from; with the shared headers it
+# fixes the machine code whose counters a profile summary records.
+KERNEL_SOURCES = {
+    "simt_fp32": "gdn_fwd_simt.cu",
+    "simt_bf16": "gdn_fwd_simt.cu",
+    "tc64_bf16": "gdn_fwd_tc64.cu",
+    "tc128_bf16": "gdn_fwd_tc.cu",
+}
+
+
+def kernel_sources_hash(kernel: str) -> str:
+    """sha256 prefix over the kernel's .cu file, every csrc header and the
+    public header (host-side files such as the ABI layer are left out)."""
+    import glob
     import hashlib
-    from linear_attention_recurrence_gated_gb300 import build as B
+    csrc = os.path.join(ROOT, "linear_attention_recurrence_gated_gb300", "csrc")
+    files = [os.path.join(csrc, KERNEL_SOURCES[kernel])]
+    files += sorted(glob.glob(os.path.join(csrc, "*.cuh")))
+    files.append(os.path.join(ROOT, "include", "gdn.h"))
     h = hashlib.sha256()
-    for p in sorted(B._deps()):
-        if p.endswith("build.py"):
-            continue
+    for p in files:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -203,7 +217,7 @@ def committed_traffic(kernel: str, workload: str):
         return None
     m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     s = re.search(r"source_sha:\s*([0-9a-f]+)", text)
-    if not m or not s or s.group(1) != kernel_sources_hash():
+    if not m or not s or kernel not in KERNEL_SOURCES or s.group(1) != kernel_sources_hash(kernel):
         return None
     return float(m.group(1))
 

@@ -185,7 +185,8 @@ gdn_status gdn_check(void *workspace, void *stream);
 const char *gdn_status_string(int32_t status);
 
 /* Name of the kernel gdn_fwd would launch for these arguments ("simt_fp32",
- * "tc_bf16", ...) or NULL when the arguments are unsupported.  Host only. */
+ * "simt_bf16", "tc64_bf16", "tc128_bf16") or NULL when the arguments are
+ * unsupported.  Host only. */
 const char *gdn_fwd_kernel_name(int32_t head_dim_k, int32_t head_dim_v,
                                 gdn_dtype dtype, uint32_t flags);
 

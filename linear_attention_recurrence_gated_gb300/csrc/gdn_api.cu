@@ -51,7 +51,8 @@ const char *gdn_fwd_kernel_name(int32_t head_dim_k, int32_t head_dim_v, gdn_dtyp
                                 uint32_t flags) {
   if (!supported_dk(head_dim_k) || !supported_dv(head_dim_v)) return nullptr;
   if (dtype != GDN_F32 && dtype != GDN_BF16) return nullptr;
-  if (use_tc(head_dim_k, head_dim_v, dtype, flags)) return "tc_bf16";
+  if (use_tc(head_dim_k, head_dim_v, dtype, flags))
+    return head_dim_k == 64 ? "tc64_bf16" : "tc128_bf16";
   return dtype == GDN_F32 ? "simt_fp32" : "simt_bf16";
 }
 

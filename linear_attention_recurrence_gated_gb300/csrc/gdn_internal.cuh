@@ -73,7 +73,8 @@ __device__ __forceinline__ void store_out(__nv_bfloat16 *p, float x) { *p = __fl
 
 // Launchers (one per kernel family).  Return a cudaError_t from the launch.
 cudaError_t launch_fwd_simt(const FwdParams &p, gdn_dtype dtype, cudaStream_t stream);
-cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t stream);  // bf16 storage only
+cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t stream);    // bf16 storage only
+cudaError_t launch_fwd_tc64(const FwdParams &p, cudaStream_t stream);  // bf16, head_dim_k 64
 bool tc_supported(int dk, int dv);
 
 }  // namespace gdn

@@ -50,6 +50,14 @@ def test_kernel_names(L):
     assert G.gdn_fwd_kernel_name(64, 64, torch.float32) == "simt_fp32"
     assert G.gdn_fwd_kernel_name(48, 64, torch.bfloat16) is None
     assert G.gdn_fwd_kernel_name(64, 48, torch.bfloat16) is None
+    # bf16 storage: tensor-core kernels where the head sizes allow, else the fp32 kernel
+    assert G.gdn_fwd_kernel_name(64, 64, torch.bfloat16) == "tc64_bf16"
+    assert G.gdn_fwd_kernel_name(64, 128, torch.bfloat16) == "tc64_bf16"
+    assert G.gdn_fwd_kernel_name(128, 128, torch.bfloat16) == "tc128_bf16"
+    assert G.gdn_fwd_kernel_name(32, 64, torch.bfloat16) == "simt_bf16"
+    assert G.gdn_fwd_kernel_name(64, 96, torch.bfloat16) == "simt_bf16"
+    assert G.gdn_fwd_kernel_name(64, 64, torch.bfloat16, G.GDN_QK_L2NORM) == "simt_bf16"
+    assert G.gdn_fwd_kernel_name(64, 64, torch.bfloat16, G.GDN_FORCE_SIMT) == "simt_bf16"
 
 
 # ---- host-side validation with fake (never dereferenced) device addresses ----
