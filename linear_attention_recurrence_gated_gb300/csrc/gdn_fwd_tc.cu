@@ -458,7 +458,7 @@ gdn_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_q,
     // if a wait gave up.
     auto s_epilogue = [&](int cc) -> bool {
       const int slot = cc % NIN, buf = cc & 1;
-      const int c = cc;  // phase stamps of the drain go to chunk cc, phases 8..11
+      [[maybe_unused]] const int c = cc;  // phase stamps of the drain go to chunk cc
       GDN_PHASE(8);
       bool ok = role_wait(tmem_full(buf), (cc >> 1) & 1, S, p, n, h, 7);
       if (ok) ok = role_wait(full_in(slot), (cc / NIN) & 1, S, p, n, h, 8);

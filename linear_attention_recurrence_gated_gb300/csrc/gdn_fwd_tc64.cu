@@ -19,7 +19,7 @@
 // Walkthrough", section 5.3.1).  The carry per chunk, all M = 128 products:
 //   MMA1  D1  = [W; Q] H            rows 0..63 = W H, rows 64..127 = Q H
 //   E1    U = U~ - W H, Ud = diag(exp(G_C - G)) U  -> shared (bf16, row-major)
-//   MMA3  DH  = [K^T; *] Ud          rows 0..63 = K^T Ud  (the state increment)
+//   MMA3  DH  = [*; K^T] Ud          rows 64..127 = K^T Ud  (the state increment)
 //   MMA2  DPU = [*; P] U             rows 64..127 = P U
 //   E2a   H <- gamma_C H + DH  (registers), bf16 copy -> shared for the next MMA1
 //   E2b   O = diag(gamma) Q H + P U -> bf16 -> TMA store
@@ -28,16 +28,26 @@
 // operands (row-major tiles, no transposes); K^T is the MN-major view of the
 // TMA-loaded K tile.
 //
-// Roles (320 threads, one CTA per SM):
-//   warp 8     producer: gate vectors + TMA loads of Q, K, V (ring of 3 slots)
-//   warp 9     MMA issuer: one thread polls the ready-barriers of every
-//              product and issues whichever is ready (tcgen05.mma + commit)
-//   warps 0-3  prep: diagonal 16x16 inverses of (I + A) (fp32), couplings
-//              (tf32 mma), blocked substitution for W (into the input slot,
-//              right before Q) and U~ (bf16 mma); warps 0,1 first drain the
-//              P rows of the chunk's Q K^T accumulator
-//   warps 4,5  carry chain (E1, E2a), the state in registers
-//   warps 6,7  output (E2b) + drain of the A rows of K K^T two chunks ahead
+// Roles (20 warps, one CTA per SM; warp w reaches the TMEM lanes 32*(w%4)..+31
+// and issues on SM sub-partition w%4):
+//   warp 16        producer: gate vectors + TMA loads of Q, K, V (ring of 3
+//                  slots), and an L2 prefetch of the tiles that next reuse the slot
+//   warp 13        [Q; K] K^T issuer (tcgen05.mma + commit); owns tensor memory
+//   warp 12        carry-chain issuer: MMA1, then MMA3 + MMA2, per chunk
+//   warps 8,9      drain the P rows of [Q; K] K^T (masked decay, bf16)
+//   warps 18,19    drain the A rows (masked decay and beta, fp32)
+//   warps 0-3      prep: diagonal 16x16 inverses of (I + A) (fp32), couplings
+//                  (tf32 mma), blocked substitution for W (into the input slot,
+//                  right before Q) and U~ (bf16 mma)
+//   warps 4,5      E1 (U, Ud from W H) on lane quarters 0,1
+//   warps 6,7,10,11  E2a (state update) on lane quarters 2,3, 32 value columns
+//                  per warp, the state in registers
+//   warps 14,15    output (E2b) and its TMA store
+//   warp 17        idle
+// E1 and E2a, the two halves of the serial chain, issue on different
+// sub-partitions.
+// The issuers wait on mbarriers with try_wait (the thread sleeps until the
+// phase completes), so a ready operand is picked up without polling delay.
 // Every wait is bounded; a timeout records GDN_ERR_TIMEOUT and ends the loops.
 #include "gdn_tc_common.cuh"
 
@@ -48,8 +58,14 @@ using namespace ptx;
 using namespace tc;
 
 constexpr int DK = 64, NIN = 3;
-constexpr int kThreads64 = 320;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+// Warp map.  A warp reaches the TMEM lanes 32*(warp%4)..+31 and issues on SM
+// sub-partition warp%4, so the roles are spread to balance the sub-partitions.
+constexpr int kThreads64 = 640;  // 20 warps
+constexpr int kWarpSIssue = 13, kWarpProducer = 16;
+constexpr int kWarpE1Issue = 4, kWarpE2aIssue = 6;  // lane 0 of these issues the carry products
+__device__ __forceinline__ bool is_drain_warp(int w) { return w == 8 || w == 9 || w == 18 || w == 19; }
+__device__ __forceinline__ bool is_e1_warp(int w) { return w == 4 || w == 5 || w == 12 || w == 17; }
+__device__ __forceinline__ bool is_e2a_warp(int w) { return w == 6 || w == 7 || w == 10 || w == 11; }
 constexpr uint32_t kBarPrep = 1;
 constexpr uint32_t kTmemCols = 512;
 // TMEM column map: S double buffer, D1 double buffer, DPU double buffer, DH.
@@ -64,17 +80,17 @@ struct L64 {
   // input slot: W (written by prep) | Q | K | V | gates  -> [W;Q] and [Q;K] contiguous
   static constexpr int SW = 0, SQ = SUB, SK = 2 * SUB, SV = 3 * SUB, SG = 4 * SUB;
   static constexpr int SLOT = 4 * SUB + 2048;
-  // stage: U~ | P  -> [U~; P] contiguous
-  static constexpr int TU = 0, TP = SUB;
-  static constexpr int STAGE = 2 * SUB;
   static constexpr int OFF_IN = 0;
-  static constexpr int OFF_ST = OFF_IN + NIN * SLOT;
-  static constexpr int OFF_H = OFF_ST + 2 * STAGE;   // state H [dk][dv] bf16
-  static constexpr int OFF_U = OFF_H + SUB;          // U  [token][dv] bf16
-  static constexpr int OFF_UD = OFF_U + SUB;         // Ud [token][dv] bf16
-  static constexpr int OFF_OST = OFF_UD + SUB;       // O staging [token][dv] bf16
+  static constexpr int OFF_UT = OFF_IN + NIN * SLOT;  // U~ ring [2][token][dv] bf16
+  static constexpr int OFF_H = OFF_UT + 2 * SUB;      // state H [dk][dv] bf16
+  static constexpr int OFF_U = OFF_H + SUB;           // U  [token][dv] bf16
+  static constexpr int OFF_UD = OFF_U + SUB;          // Ud [token][dv] bf16
+  static constexpr int OFF_OST = OFF_UD + SUB;        // O staging [token][dv] bf16
+  // P ring [3][token][token] bf16, right after the staging tile: the 8 KB tile
+  // before P_i completes the M = 128 operand [*; P_i] of MMA2
+  static constexpr int OFF_P = OFF_OST + SUB;
   static constexpr int A_LD = 68;
-  static constexpr int OFF_A = OFF_OST + SUB;        // f32 [2][64][A_LD]
+  static constexpr int OFF_A = OFF_P + 3 * SUB;       // f32 [2][64][A_LD]
   static constexpr int TF_LD = 20;
   static constexpr int OFF_TF = OFF_A + 2 * 64 * A_LD * 4;
   static constexpr int TB_LD = 24;
@@ -88,27 +104,30 @@ struct L64 {
   static constexpr int OFF_FLAG = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_FLAG + 16;
   static constexpr int ALLOC = BYTES + 1024;
-  static_assert(SLOT % 1024 == 0 && OFF_ST % 1024 == 0 && OFF_H % 1024 == 0, "alignment");
+  static_assert(SLOT % 1024 == 0 && OFF_UT % 1024 == 0 && OFF_H % 1024 == 0 && OFF_P % 1024 == 0,
+                "alignment");
   static_assert(ALLOC <= 232448, "shared memory budget");
 };
 
 // mbarrier indices
 enum : int {
   B_FULL_IN = 0,     // [3]  TMA bytes landed (+ producer arrival)
-  B_EMPTY_IN = 3,    // [3]  carry warps done with the slot (128)
+  B_EMPTY_IN = 3,    // [3]  E2a and output warps done with the slot (192)
   B_FULL_ST = 6,     // [2]  prep wrote W and U~ (128)
   B_TMEM_FULL = 8,   // [2]  Q K^T / K K^T accumulator ready (commit)
-  B_TMEM_EMPTY = 10, // [2]  ... drained (128)
-  B_S_READY = 12,    // [2]  P and A in shared memory (128)
-  B_H_READY = 14,    //      bf16 state written for the next MMA1 (64)
+  B_TMEM_EMPTY = 10, // [2]  ... drained (128, the drain warps)
+  B_S_READY = 12,    // [2]  P and A in shared memory (128, the drain warps)
+  B_H_READY = 14,    //      bf16 state written for the next MMA1 (128)
   B_D1_FULL = 15,    // [2]  MMA1 done (commit)
-  B_D1_FREE = 17,    // [2]  D1 drained (128)
+  B_D1_FREE = 17,    // [2]  D1 drained (E1 64 + output 64)
   B_U_READY = 19,    //      U and Ud written (64)
   B_DH_FULL = 20,    //      MMA3 done (commit)
   B_PU_FULL = 21,    // [2]  MMA2 done (commit)
   B_PU_FREE = 23,    // [2]  DPU drained (64)
   B_OST_FULL = 25,   //      O rows staged (64)
   B_OST_FREE = 26,   //      staging tile read by the store (1)
+  B_UT_FREE = 27,    // [2]  U~ buffer read by E1 (128)
+  B_P_FREE = 29,     // [3]  P buffer read by MMA2 (commit)
 };
 
 // One thread drains one row i of a 64-column fp32 accumulator of [Q; K] K^T
@@ -203,7 +222,8 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
   float *sgc = reinterpret_cast<float *>(smem + L::OFF_GC);
   auto bar = [&](int i) { return sbase + L::OFF_BAR + 8u * i; };
   auto slot_base = [&](int s) { return sbase + L::OFF_IN + s * L::SLOT; };
-  auto stage_base = [&](int s) { return sbase + L::OFF_ST + s * L::STAGE; };
+  auto ut_base = [&](int s) { return sbase + L::OFF_UT + s * L::SUB; };
+  auto p_base = [&](int s) { return sbase + L::OFF_P + s * L::SUB; };
   auto gate_ptr = [&](int s) {
     return reinterpret_cast<float *>(smem + L::OFF_IN + s * L::SLOT + L::SG);
   };
@@ -214,7 +234,7 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
   if (tid == 0) {
     for (int s = 0; s < NIN; ++s) {
       mbar_init(bar(B_FULL_IN + s), 1);
-      mbar_init(bar(B_EMPTY_IN + s), 128);
+      mbar_init(bar(B_EMPTY_IN + s), 192);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(B_FULL_ST + s), 128);
@@ -222,19 +242,21 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
       mbar_init(bar(B_TMEM_EMPTY + s), 128);
       mbar_init(bar(B_S_READY + s), 128);
       mbar_init(bar(B_D1_FULL + s), 1);
-      mbar_init(bar(B_D1_FREE + s), 128);
+      mbar_init(bar(B_D1_FREE + s), 192);
+      mbar_init(bar(B_UT_FREE + s), 128);
       mbar_init(bar(B_PU_FULL + s), 1);
       mbar_init(bar(B_PU_FREE + s), 64);
     }
-    mbar_init(bar(B_H_READY), 64);
-    mbar_init(bar(B_U_READY), 64);
+    mbar_init(bar(B_H_READY), 128);
+    mbar_init(bar(B_U_READY), 128);
+    for (int s = 0; s < 3; ++s) mbar_init(bar(B_P_FREE + s), 1);
     mbar_init(bar(B_DH_FULL), 1);
     mbar_init(bar(B_OST_FULL), 64);
     mbar_init(bar(B_OST_FREE), 1);
     *S.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) tmem_alloc(sbase + L::OFF_TMEM, kTmemCols);
+  if (warp == kWarpSIssue) tmem_alloc(sbase + L::OFF_TMEM, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -248,48 +270,7 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
     return *reinterpret_cast<uint32_t *>(smem + (addr - sbase));
   };
 
-  // Drain the [Q; K] K^T accumulator of chunk cc.  A warp reaches the TMEM lane
-  // quarter warp % 4: quarters 0,1 hold rows of P = Q K^T (drained by prep warps
-  // 0,1), quarters 2,3 rows of A = K K^T (drained by the output warps 6,7).
-  auto s_epilogue = [&](int cc) -> bool {
-  const int wq = warp & 3;
-  const bool chain = wq < 2;  // P rows
-  const int row = 32 * (wq & 1) + lane;
-  const int cw = wq;
-  auto tm = [&](uint32_t col) { return tmem_base + ((uint32_t)(32 * wq) << 16) + col; };
-    const int slot = cc % NIN, buf = cc & 1;
-    [[maybe_unused]] const int c = cc;  // chunk index of the phase stamps
-    GDN_PHASE(8);
-    bool ok = role_wait(bar(B_TMEM_FULL + buf), (cc >> 1) & 1, S, p, n, h, 7);
-    if (ok) ok = role_wait(bar(B_FULL_IN + slot), (cc / NIN) & 1, S, p, n, h, 8);
-    // the P tile of this stage was last read by MMA2 of chunk cc-2
-    if (ok && chain && cc >= 2)
-      ok = role_wait(bar(B_PU_FULL + buf), ((cc - 2) >> 1) & 1, S, p, n, h, 10);
-    GDN_PHASE(9);
-    if (!__all_sync(0xffffffffu, ok)) return false;
-    tc_fence_after();
-    const int valid = valid_rows(cc);
-    const float *gate = gate_ptr(slot);
-    const float *G2 = gate, *beta = gate + 192, *E = gate + 256;
-    const bool isP = chain;
-    const int i = row;
-    const int ilim = isP ? i + 1 : i;  // P keeps j <= i, A keeps j < i
-    const bool rowok = i < valid;
-    const float bi = isP ? 1.f : beta[i];
-    const uint32_t Ps = stage_base(buf) + L::TP;
-    float *Arow = reinterpret_cast<float *>(smem + L::OFF_A) + (buf * 64 + i) * L::A_LD;
-    drain_s_row(tm(kColS + buf * 64), G2, E, i, cw & 1, isP, bi, ilim, rowok, Ps, Arow, smem,
-                sbase);
-    tc_fence_before();
-    mbar_arrive(bar(B_TMEM_EMPTY + buf));
-    if (isP) fence_proxy_async_smem();
-    GDN_PHASE(10);
-    mbar_arrive(bar(B_S_READY + buf));
-    return true;
-  };
-
-
-  if (warp == kProducerWarp) {
+  if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
     const __nv_bfloat16 *betap = static_cast<const __nv_bfloat16 *>(p.beta);
     float gv0 = 0.f, gv1 = 0.f, bv0 = 0.f, bv1 = 0.f;
@@ -348,6 +329,12 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
         tma_load_3d(sb + L::SQ, &tmap_q, 0, h, row, bar(B_FULL_IN + slot));
         tma_load_3d(sb + L::SK, &tmap_k, 0, h, row, bar(B_FULL_IN + slot));
         tma_load_3d(sb + L::SV, &tmap_v, col0, h, row, bar(B_FULL_IN + slot));
+        if (c + NIN < nc) {  // warm L2 with the tiles of the chunk that reuses this slot
+          const int prow = row + NIN * 64;
+          tma_prefetch_3d(&tmap_q, 0, h, prow);
+          tma_prefetch_3d(&tmap_k, 0, h, prow);
+          tma_prefetch_3d(&tmap_v, col0, h, prow);
+        }
       }
       GDN_PHASE(2);
       ++issued;
@@ -355,85 +342,65 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
     if (lane == 0)
       for (int c = issued - NIN < 0 ? 0 : issued - NIN; c < issued; ++c)
         mbar_wait_bounded(bar(B_FULL_IN + c % NIN), (c / NIN) & 1, kWaitTimeoutNs);
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    // One thread polls the barriers of three independent product streams and
-    // issues whichever is ready: Q K^T of chunk cs, MMA1 of chunk c1, MMA3 and
-    // MMA2 of chunk c3 (c3 <= c1 <= c3 + 1 keeps one carry product in flight).
+  } else if (is_drain_warp(warp)) {
+    // ------------------------------------------------------------ S drains
+    // The [Q; K] K^T accumulator of each chunk: lane quarters 0,1 hold the P
+    // rows (warps 8,9), quarters 2,3 the A rows (warps 18,19).
+    const int wq = warp & 3;
+    const bool isP = wq < 2;
+    const int i = 32 * (wq & 1) + lane;
+    const uint32_t tq = tmem_base + ((uint32_t)(32 * wq) << 16);
+    for (int c = 0; c < nc; ++c) {
+      const int slot = c % NIN, buf = c & 1;
+      GDN_PHASE(8);
+      bool ok = role_wait(bar(B_TMEM_FULL + buf), (c >> 1) & 1, S, p, n, h, 7);
+      if (ok) ok = role_wait(bar(B_FULL_IN + slot), (c / NIN) & 1, S, p, n, h, 8);
+      // the P buffer was last read by MMA2 of chunk c-3; the A buffer by the
+      // prep of chunk c-2
+      if (ok && isP && c >= 3)
+        ok = role_wait(bar(B_P_FREE + c % 3), ((c / 3) - 1) & 1, S, p, n, h, 10);
+      if (ok && !isP && c >= 2)
+        ok = role_wait(bar(B_FULL_ST + buf), ((c - 2) >> 1) & 1, S, p, n, h, 21);
+      GDN_PHASE(9);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const int valid = valid_rows(c);
+      const float *gate = gate_ptr(slot);
+      const float *G2 = gate, *beta = gate + 192, *E = gate + 256;
+      const int ilim = isP ? i + 1 : i;  // P keeps j <= i, A keeps j < i
+      const float bi = isP ? 1.f : beta[i];
+      float *Arow = reinterpret_cast<float *>(smem + L::OFF_A) + (buf * 64 + i) * L::A_LD;
+      drain_s_row(tq + kColS + buf * 64, G2, E, i, wq & 1, isP, bi, ilim, i < valid,
+                  p_base(c % 3), Arow, smem, sbase);
+      tc_fence_before();
+      mbar_arrive(bar(B_TMEM_EMPTY + buf));
+      if (isP) fence_proxy_async_smem();  // P is read by MMA2 (async proxy)
+      GDN_PHASE(10);
+      mbar_arrive(bar(B_S_READY + buf));
+    }
+  } else if (warp == kWarpSIssue) {
+    // ------------------------------------------------------------ [Q; K] K^T issuer
     if (lane == 0) {
-      int cs = 0, c1 = 0, c3 = 0;
-      uint64_t last = globaltimer_ns();
-      uint32_t spins = 0;
-      while (c3 < nc) {
-        bool prog = false;
-        if (cs < nc && mbar_test(bar(B_FULL_IN + cs % NIN), (cs / NIN) & 1) &&
-            (cs < 2 || mbar_test(bar(B_TMEM_EMPTY + (cs & 1)), ((cs >> 1) - 1) & 1))) {
-          tc_fence_after();
-          const uint32_t a = slot_base(cs % NIN) + L::SQ;  // [Q; K]
+      int issued = 0;
+      for (int c = 0; c < nc; ++c) {
+        bool ok = role_wait(bar(B_FULL_IN + c % NIN), (c / NIN) & 1, S, p, n, h, 5);
+        if (ok && c >= 2)
+          ok = role_wait(bar(B_TMEM_EMPTY + (c & 1)), ((c >> 1) - 1) & 1, S, p, n, h, 6);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t a = slot_base(c % NIN) + L::SQ;  // [Q; K]
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem_base + kColS + (cs & 1) * 64, umma_desc_sw128(a + kk * 32),
-                      umma_desc_sw128(a + L::SUB + kk * 32), kIdescS, kk > 0);
-          umma_commit(bar(B_TMEM_FULL + (cs & 1)));
-          ++cs;
-          prog = true;
-        }
-        if (c1 < nc && c1 == c3 && mbar_test(bar(B_FULL_ST + (c1 & 1)), (c1 >> 1) & 1) &&
-            mbar_test(bar(B_H_READY), c1 & 1) &&
-            (c1 < 2 || mbar_test(bar(B_D1_FREE + (c1 & 1)), ((c1 >> 1) - 1) & 1))) {
-          tc_fence_after();
-          const uint32_t a = slot_base(c1 % NIN) + L::SW;  // [W; Q]
-          const uint32_t b = sbase + L::OFF_H;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem_base + kColD1 + (c1 & 1) * 64, umma_desc_sw128(a + kk * 32),
-                      umma_desc_sw128_mn(b + kk * 2048, L::SUB), kIdescKM, kk > 0);
-          umma_commit(bar(B_D1_FULL + (c1 & 1)));
-          ++c1;
-          prog = true;
-        }
-        if (c3 < c1 && mbar_test(bar(B_U_READY), c3 & 1) &&
-            (c3 < 2 || mbar_test(bar(B_PU_FREE + (c3 & 1)), ((c3 >> 1) - 1) & 1))) {
-          tc_fence_after();
-          // MMA3: state increment [K^T; V^T] Ud (K^T = MN-major view of the K tile;
-          // the V tile is the second, unread, M block)
-          const uint32_t kt = slot_base(c3 % NIN) + L::SK;
-          const uint32_t ud = sbase + L::OFF_UD, u = sbase + L::OFF_U;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem_base + kColH, umma_desc_sw128_mn(kt + kk * 2048, L::SUB),
-                      umma_desc_sw128_mn(ud + kk * 2048, L::SUB), kIdescMM, kk > 0);
-          umma_commit(bar(B_DH_FULL));
-          // MMA2: [U~; P] U  (rows 64..127 = P U)
-          const uint32_t ap = stage_base(c3 & 1) + L::TU;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem_base + kColPU + (c3 & 1) * 64, umma_desc_sw128(ap + kk * 32),
-                      umma_desc_sw128_mn(u + kk * 2048, L::SUB), kIdescKM, kk > 0);
-          umma_commit(bar(B_PU_FULL + (c3 & 1)));
-          ++c3;
-          prog = true;
-        }
-        if (prog) {
-          spins = 0;
-        } else if (__nanosleep(20), (++spins & 255u) == 0) {  // back off: leave issue slots to the warps sharing this SMSP
-          const uint64_t now = globaltimer_ns();
-          if (*S.abort_flag) break;
-          if (spins == 256) last = now;
-          else if (now - last > kWaitTimeoutNs) {
-            *S.abort_flag = 1;
-            report(p.status, GDN_ERR_TIMEOUT, (uint32_t)n, (uint32_t)h, 9);
-            break;
-          }
-        }
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(tmem_base + kColS + (c & 1) * 64, umma_desc_sw128(a + kk * 32),
+                    umma_desc_sw128(a + L::SUB + kk * 32), kIdescS, kk > 0);
+        umma_commit(bar(B_TMEM_FULL + (c & 1)));
+        GDN_PROBE_AT(warp, c, 0, clock64());
+        ++issued;
       }
-      // every issued MMA has completed before tensor memory is released
-      if (c3 > 0) {
-        mbar_wait_bounded(bar(B_PU_FULL + ((c3 - 1) & 1)), ((c3 - 1) >> 1) & 1, kWaitTimeoutNs);
-        mbar_wait_bounded(bar(B_DH_FULL), (c3 - 1) & 1, kWaitTimeoutNs);
-      }
-      if (c1 > c3) mbar_wait_bounded(bar(B_D1_FULL + ((c1 - 1) & 1)), ((c1 - 1) >> 1) & 1, kWaitTimeoutNs);
-      if (cs > 0) mbar_wait_bounded(bar(B_TMEM_FULL + ((cs - 1) & 1)), ((cs - 1) >> 1) & 1, kWaitTimeoutNs);
+      // the last product has completed before tensor memory is released
+      if (issued > 0)
+        mbar_wait_bounded(bar(B_TMEM_FULL + ((issued - 1) & 1)), ((issued - 1) >> 1) & 1,
+                          kWaitTimeoutNs);
     }
     __syncwarp();
   } else if (warp < 4) {
@@ -449,11 +416,11 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
       const int slot = c % NIN, stage = c & 1;
       const int valid = valid_rows(c);
       GDN_PHASE(0);
-      // warps 0,1 drain the P rows of this chunk's [Q; K] K^T accumulator
-      bool ok = warp < 2 ? s_epilogue(c) : true;
       // P and A of this chunk are in shared memory; the carry is done with the
       // stage's previous contents (the P drain waited for MMA2 of chunk c-2)
-      if (ok) ok = role_wait(bar(B_S_READY + stage), (c >> 1) & 1, S, p, n, h, 2);
+      bool ok = role_wait(bar(B_S_READY + stage), (c >> 1) & 1, S, p, n, h, 2);
+      // the U~ buffer was last read by E1 of chunk c-2
+      if (ok && c >= 2) ok = role_wait(bar(B_UT_FREE + stage), ((c >> 1) - 1) & 1, S, p, n, h, 22);
       if (ok) ok = role_wait(bar(B_FULL_IN + slot), (c / NIN) & 1, S, p, n, h, 3);
       ok = __all_sync(0xffffffffu, ok) && !*S.abort_flag;
       GDN_PHASE(1);
@@ -463,7 +430,7 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
       const float *gate = gate_ptr(slot);
       const float *gam = gate + 64, *beta = gate + 192;
       const float *sA = reinterpret_cast<const float *>(smem + L::OFF_A) + stage * 64 * L::A_LD;
-      const uint32_t Us = stage_base(stage) + L::TU;
+      const uint32_t Us = ut_base(stage);
 
       // rows past the end of the sequence: zero Q, K, V (the Q K^T MMA has read them)
       if (ok && valid < 64) {
@@ -481,27 +448,52 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
         if (!(v[0] && v[1] && v[2] && v[3])) break;
       }
 
-      // ---- 16x16 diagonal blocks of T = (I + A)^-1 (right-looking, fp32) ----
-      if (lane < 16) {
-        const int l = lane, w = warp;
-        const float *Ab = sA + (16 * w) * L::A_LD + 16 * w;
+      // ---- 16x16 diagonal blocks of T = (I + A)^-1 (fp32).  Warps 2,3 take two
+      // blocks each, one per half-warp; lane l builds column l of its block by
+      // forward substitution, T_rl = [r == l] - sum_{k<r} A_rk T_kl, reading
+      // rows of A as float4 (broadcast within the half-warp).  T is stored
+      // column-major: fp32 for the couplings, and as bf16 T diag(beta gamma) and
+      // T diag(beta) for the substitution. ----
+      if (warp >= 2) {
+        const int blk = 2 * (warp - 2) + (lane >> 4), l = lane & 15;
+        const float *Ab = sA + (16 * blk) * L::A_LD + 16 * blk;
         float x[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = (r == l) ? 1.f : 0.f;
-#pragma unroll
-        for (int k = 0; k < 15; ++k) {
-          const float xk = x[k];
-#pragma unroll
-          for (int r = k + 1; r < 16; ++r) x[r] = fmaf(-Ab[r * L::A_LD + k], xk, x[r]);
-        }
-        const float bj = beta[16 * w + l];
-        const float bgj = bj * gam[16 * w + l];
-#pragma unroll
         for (int r = 0; r < 16; ++r) {
-          sTf[(w * 16 + r) * L::TF_LD + l] = x[r];
-          sTB[((0 * 4 + w) * 16 + r) * L::TB_LD + l] = __float2bfloat16_rn(x[r] * bgj);
-          sTB[((1 * 4 + w) * 16 + r) * L::TB_LD + l] = __float2bfloat16_rn(x[r] * bj);
+          float s0 = (r == l) ? 1.f : 0.f, s1 = 0.f;
+#pragma unroll
+          for (int k4 = 0; k4 < r; k4 += 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(Ab + r * L::A_LD + k4);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (k4 + e < r) {
+                if (e & 1) s1 = fmaf(-av[e], x[k4 + e], s1);
+                else s0 = fmaf(-av[e], x[k4 + e], s0);
+              }
+            }
+          }
+          x[r] = s0 + s1;
         }
+        float *tcol = sTf + (blk * 16 + l) * L::TF_LD;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<float4 *>(tcol + 4 * q) =
+              make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        const float bj = beta[16 * blk + l];
+        const float bgj = bj * gam[16 * blk + l];
+        uint32_t wg[8], wb[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          wg[e] = pack_bf16(x[2 * e] * bgj, x[2 * e + 1] * bgj);
+          wb[e] = pack_bf16(x[2 * e] * bj, x[2 * e + 1] * bj);
+        }
+        uint4 *tg = reinterpret_cast<uint4 *>(sTB + ((0 * 4 + blk) * 16 + l) * L::TB_LD);
+        uint4 *tb = reinterpret_cast<uint4 *>(sTB + ((1 * 4 + blk) * 16 + l) * L::TB_LD);
+        tg[0] = make_uint4(wg[0], wg[1], wg[2], wg[3]);
+        tg[1] = make_uint4(wg[4], wg[5], wg[6], wg[7]);
+        tb[0] = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+        tb[1] = make_uint4(wb[4], wb[5], wb[6], wb[7]);
       }
       GDN_PHASE(3);
       named_sync(kBarPrep, 128);
@@ -512,15 +504,15 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
       for (int blk = warp; blk < 6; blk += 4) {
         const int i = blk == 0 ? 1 : (blk < 3 ? 2 : 3);
         const int k = blk - (i * (i - 1)) / 2;
-        const float *T = sTf + (i * 16) * L::TF_LD;
+        const float *T = sTf + (i * 16) * L::TF_LD;  // column-major: T(row, col) = T[col * TF_LD + row]
         const float *Ak = sA + (16 * i) * L::A_LD + 16 * k;
         float acc[2][4] = {};
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
-          const uint32_t a0 = to_tf32(T[g * L::TF_LD + 8 * ks + t]);
-          const uint32_t a1 = to_tf32(T[(g + 8) * L::TF_LD + 8 * ks + t]);
-          const uint32_t a2 = to_tf32(T[g * L::TF_LD + 8 * ks + t + 4]);
-          const uint32_t a3 = to_tf32(T[(g + 8) * L::TF_LD + 8 * ks + t + 4]);
+          const uint32_t a0 = to_tf32(T[(8 * ks + t) * L::TF_LD + g]);
+          const uint32_t a1 = to_tf32(T[(8 * ks + t) * L::TF_LD + g + 8]);
+          const uint32_t a2 = to_tf32(T[(8 * ks + t + 4) * L::TF_LD + g]);
+          const uint32_t a3 = to_tf32(T[(8 * ks + t + 4) * L::TF_LD + g + 8]);
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
             const uint32_t b0 = to_tf32(Ak[(8 * ks + t) * L::A_LD + 8 * nt + g]);
@@ -541,97 +533,65 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
       named_sync(kBarPrep, 128);
       GDN_PHASE(6);
 
-      // ---- block forward substitution: X_i = T_ii B_i + sum_k (-M_ik) X_k, X = [W | U~] ----
+      // ---- block forward substitution, left-looking (a compact loop):
+      // X_i = T_ii B_i + sum_{k<i} (-M_ik) X_k for X = [W | U~], B = [K | V] (the
+      // beta, gamma scalings are folded into the T_ii tiles).  Warps 0,1 build W,
+      // warps 2,3 U~, 32 columns each; a warp reads back only its own columns of
+      // the earlier block rows, so the levels need no CTA-wide barrier. ----
       {
-        constexpr int PPW = 2;  // 16-column pairs per warp: warps 0,1 -> W, warps 2,3 -> U~
         const int arow = lrow + (lmi & 1) * 8, acol = (lmi >> 1) * 8;
+        const int trow = lrow + (lmi >> 1) * 8, tcol = (lmi & 1) * 8;  // column-major T tiles
         const bool isW = warp < 2;
         const uint32_t xt = isW ? Ws : Us;
         const uint32_t bsrc = isW ? Ks : Vs;
         const int tbv = isW ? 0 : 1;
-        float lacc[4][PPW][2][4];
-        {
-          // T_ii B_i for every block row: all operand loads first, then the products
-          uint32_t ta[4][4], tb[4][PPW][4];
+        const int col = 32 * (warp & 1);
+#pragma unroll 1
+        for (int lv = 0; lv < 4; ++lv) {
+          float acc[2][2][4];
+          {
+            uint32_t ta[4], tb[2][4];
+            ldsm_x4_t(TBa + (((tbv * 4 + lv) * 16 + trow) * L::TB_LD + tcol) * 2, ta[0], ta[1],
+                      ta[2], ta[3]);
 #pragma unroll
-          for (int lv = 0; lv < 4; ++lv) {
-            ldsm_x4(TBa + (((tbv * 4 + lv) * 16 + arow) * L::TB_LD + acol) * 2, ta[lv][0],
-                    ta[lv][1], ta[lv][2], ta[lv][3]);
+            for (int pp = 0; pp < 2; ++pp)
+              ldsm_x4_t(tile_addr(bsrc, 16 * lv + arow, col + 16 * pp + acol), tb[pp][0],
+                        tb[pp][1], tb[pp][2], tb[pp][3]);
 #pragma unroll
-            for (int pp = 0; pp < PPW; ++pp) {
-              const int col = 32 * (warp & 1) + 16 * pp;
-              ldsm_x4_t(tile_addr(bsrc, 16 * lv + lrow + (lmi & 1) * 8, col + (lmi >> 1) * 8),
-                        tb[lv][pp][0], tb[lv][pp][1], tb[lv][pp][2], tb[lv][pp][3]);
-            }
-          }
-#pragma unroll
-          for (int lv = 0; lv < 4; ++lv)
-#pragma unroll
-            for (int pp = 0; pp < PPW; ++pp)
+            for (int pp = 0; pp < 2; ++pp)
 #pragma unroll
               for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) lacc[lv][pp][nt][e] = 0.f;
-                mma_bf16(lacc[lv][pp][nt], ta[lv][0], ta[lv][1], ta[lv][2], ta[lv][3],
-                         tb[lv][pp][2 * nt], tb[lv][pp][2 * nt + 1]);
+                for (int e = 0; e < 4; ++e) acc[pp][nt][e] = 0.f;
+                mma_bf16(acc[pp][nt], ta[0], ta[1], ta[2], ta[3], tb[pp][2 * nt],
+                         tb[pp][2 * nt + 1]);
               }
-        }
-#pragma unroll
-        for (int lv = 0; lv < 4; ++lv) {
-          if (lv > 0) {
-            // X_{lv-1} (just written by all prep warps) and every coupling M_{l2, lv-1}
-            uint32_t xb[PPW][4], ma[4][4];
-#pragma unroll
-            for (int pp = 0; pp < PPW; ++pp) {
-              const int col = 32 * (warp & 1) + 16 * pp;
-              ldsm_x4_t(tile_addr(xt, 16 * (lv - 1) + lrow + (lmi & 1) * 8, col + (lmi >> 1) * 8),
-                        xb[pp][0], xb[pp][1], xb[pp][2], xb[pp][3]);
-            }
-#pragma unroll
-            for (int l2 = lv; l2 < 4; ++l2) {
-              const int blk = (l2 * (l2 - 1)) / 2 + (lv - 1);
-              ldsm_x4(MBa + ((blk * 16 + arow) * L::TB_LD + acol) * 2, ma[l2][0], ma[l2][1],
-                      ma[l2][2], ma[l2][3]);
-            }
-            // the product on the critical path first
-#pragma unroll
-            for (int pp = 0; pp < PPW; ++pp)
-#pragma unroll
-              for (int nt = 0; nt < 2; ++nt)
-                mma_bf16(lacc[lv][pp][nt], ma[lv][0], ma[lv][1], ma[lv][2], ma[lv][3],
-                         xb[pp][2 * nt], xb[pp][2 * nt + 1]);
-#pragma unroll
-            for (int pp = 0; pp < PPW; ++pp) {
-              const int col = 32 * (warp & 1) + 16 * pp;
-#pragma unroll
-              for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
-                  S1(tile_addr(xt, 16 * lv + g + 8 * hf, col + 8 * nt + 2 * t)) =
-                      pack_bf16(lacc[lv][pp][nt][2 * hf], lacc[lv][pp][nt][2 * hf + 1]);
-            }
-            // X_{lv-1} terms of the later block rows, while the other warps catch up
-#pragma unroll
-            for (int l2 = lv + 1; l2 < 4; ++l2)
-#pragma unroll
-              for (int pp = 0; pp < PPW; ++pp)
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-                  mma_bf16(lacc[l2][pp][nt], ma[l2][0], ma[l2][1], ma[l2][2], ma[l2][3],
-                           xb[pp][2 * nt], xb[pp][2 * nt + 1]);
-          } else {
-#pragma unroll
-            for (int pp = 0; pp < PPW; ++pp) {
-              const int col = 32 * (warp & 1) + 16 * pp;
-#pragma unroll
-              for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
-                  S1(tile_addr(xt, 16 * lv + g + 8 * hf, col + 8 * nt + 2 * t)) =
-                      pack_bf16(lacc[lv][pp][nt][2 * hf], lacc[lv][pp][nt][2 * hf + 1]);
-            }
           }
-          if (lv < 3) named_sync(kBarPrep, 128);
+#pragma unroll 1
+          for (int k = 0; k < lv; ++k) {
+            const int blk = (lv * (lv - 1)) / 2 + k;
+            uint32_t ma[4], xb[2][4];
+            ldsm_x4(MBa + ((blk * 16 + arow) * L::TB_LD + acol) * 2, ma[0], ma[1], ma[2], ma[3]);
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp)
+              ldsm_x4_t(tile_addr(xt, 16 * k + arow, col + 16 * pp + acol), xb[pp][0], xb[pp][1],
+                        xb[pp][2], xb[pp][3]);
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt)
+                mma_bf16(acc[pp][nt], ma[0], ma[1], ma[2], ma[3], xb[pp][2 * nt],
+                         xb[pp][2 * nt + 1]);
+          }
+#pragma unroll
+          for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf)
+                S1(tile_addr(xt, 16 * lv + g + 8 * hf, col + 16 * pp + 8 * nt + 2 * t)) =
+                    pack_bf16(acc[pp][nt][2 * hf], acc[pp][nt][2 * hf + 1]);
+          __syncwarp();
         }
       }
       // W, U~ and the zeroed rows are read by the tensor cores (async proxy)
@@ -640,28 +600,194 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
       mbar_arrive(bar(B_FULL_ST + stage));
     }
   } else {
-    // ------------------------------------------------------------ carry / output
-    const int cw = warp - 4;             // TMEM lane quarter of this warp
-    const int r = 32 * cw + lane;        // TMEM lane = accumulator row
-    const bool chain = cw < 2;           // warps 4,5: state chain; warps 6,7: output
-    const int row = chain ? r : r - 64;  // key row (chain) or token (output)
-    const size_t state_row =
-        ((size_t)n * H + h) * (size_t)DK * dv + (size_t)row * dv + col0;
-    auto tm = [&](uint32_t col) { return tmem_base + ((uint32_t)(32 * cw) << 16) + col; };
-
-    // the state row of this thread (warps 4,5): H[row][0..63], fp32
-    float hrow[64];
+    // ------------------------------------------------------------ carry chain / output
+    const int wq = warp & 3;                // TMEM lane quarter
+    const int r = 32 * wq + lane;           // TMEM lane = accumulator row
+    const int row = 32 * (wq & 1) + lane;   // token (E1, output) or key row (E2a)
+    auto tm = [&](uint32_t col) { return tmem_base + ((uint32_t)(32 * wq) << 16) + col; };
     const uint32_t Hs = sbase + L::OFF_H, Ust = sbase + L::OFF_U, Uds = sbase + L::OFF_UD;
-    auto store_row_bf16 = [&](uint32_t tilebase, int rr, const float *x) {
+    // MMA1 of chunk c: [W; Q] H (rows 0..63 = W H, rows 64..127 = Q H)
+    auto issue_mma1 = [&](int c) {
+      const uint32_t a = slot_base(c % NIN) + L::SW;
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        S4(tile_addr(tilebase, rr, 8 * q)) =
-            make_uint4(pack_bf16(x[8 * q], x[8 * q + 1]), pack_bf16(x[8 * q + 2], x[8 * q + 3]),
-                       pack_bf16(x[8 * q + 4], x[8 * q + 5]), pack_bf16(x[8 * q + 6], x[8 * q + 7]));
+      for (int kk = 0; kk < 4; ++kk)
+        umma_bf16(tmem_base + kColD1 + (c & 1) * 64, umma_desc_sw128(a + kk * 32),
+                  umma_desc_sw128_mn(Hs + kk * 2048, L::SUB), kIdescKM, kk > 0);
+      umma_commit(bar(B_D1_FULL + (c & 1)));
     };
-    if (chain) {
+    // the operands and the accumulator of MMA1(c) are ready (one thread)
+    auto mma1_ready = [&](int c) {
+      bool ok = role_wait(bar(B_H_READY), c & 1, S, p, n, h, 17);
+      if (ok && c >= 2)
+        ok = role_wait(bar(B_D1_FREE + (c & 1)), ((c >> 1) - 1) & 1, S, p, n, h, 18);
+      if (ok) ok = role_wait(bar(B_FULL_ST + (c & 1)), (c >> 1) & 1, S, p, n, h, 16);
+      return ok;
+    };
+    if (is_e1_warp(warp)) {
+      // ---- E1 (warps 4,5,12,17): U = U~ - W H (row = token), Ud = U * exp(G_C - G),
+      // 32 value columns per warp; warp 4 lane 0 then issues MMA3 and MMA2
+      const int cb = warp >= 12 ? 32 : 0;
+      int done = 0;
+      for (int c = 0; c < nc; ++c) {
+        const int slot = c % NIN, buf = c & 1;
+        const float *gate = gate_ptr(slot);
+        GDN_PHASE(0);
+        bool ok = role_wait(bar(B_D1_FULL + buf), (c >> 1) & 1, S, p, n, h, 11);
+        // U is overwritten below: MMA2 of chunk c-1 (issued from another
+        // thread than MMA1) has finished reading it
+        if (ok && c >= 1) ok = role_wait(bar(B_PU_FULL + (buf ^ 1)), ((c - 1) >> 1) & 1, S, p, n, h, 23);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        GDN_PHASE(1);
+        tc_fence_after();
+        const uint32_t Ut = ut_base(buf);
+        const float dj = gate[128 + row];
+        {
+          uint32_t w[32];
+          tmem_ld32(tm(kColD1 + buf * 64 + cb), w);
+          uint4 xu[4];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
+          for (int q = 0; q < 4; ++q) xu[q] = S4(tile_addr(Ut, row, cb + 8 * q));
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t x[4] = {xu[q].x, xu[q].y, xu[q].z, xu[q].w};
+            uint32_t pu[4], pd[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float u0 = bf16_lo(x[e]) - __uint_as_float(w[8 * q + 2 * e]);
+              const float u1 = bf16_hi(x[e]) - __uint_as_float(w[8 * q + 2 * e + 1]);
+              pu[e] = pack_bf16(u0, u1);
+              pd[e] = pack_bf16(u0 * dj, u1 * dj);
+            }
+            S4(tile_addr(Ust, row, cb + 8 * q)) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
+            S4(tile_addr(Uds, row, cb + 8 * q)) = make_uint4(pd[0], pd[1], pd[2], pd[3]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar(B_D1_FREE + buf));
+        mbar_arrive(bar(B_UT_FREE + buf));
+        fence_proxy_async_smem();
+        mbar_arrive(bar(B_U_READY));
+        GDN_PHASE(2);
+        if (warp == kWarpE1Issue) {
+          if (lane == 0) {
+            GDN_PROBE_AT(warp, c, 6, clock64());
+            ok = role_wait(bar(B_U_READY), c & 1, S, p, n, h, 19);
+            GDN_PROBE_AT(warp, c, 7, clock64());
+            if (ok && c >= 2)
+              ok = role_wait(bar(B_PU_FREE + buf), ((c >> 1) - 1) & 1, S, p, n, h, 20);
+            GDN_PROBE_AT(warp, c, 8, clock64());
+            if (ok) {
+              tc_fence_after();
+              // MMA3: state increment [Q^T; K^T] Ud: MN-major views of the Q and K
+              // tiles (adjacent in the slot); rows 64..127 = K^T Ud land in the
+              // TMEM lanes of the E2a warps, rows 0..63 are not read
+              const uint32_t kt = slot_base(slot) + L::SQ;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_bf16(tmem_base + kColH, umma_desc_sw128_mn(kt + kk * 2048, L::SUB),
+                          umma_desc_sw128_mn(Uds + kk * 2048, L::SUB), kIdescMM, kk > 0);
+              GDN_PROBE_AT(warp, c, 9, clock64());
+              umma_commit(bar(B_DH_FULL));
+              GDN_PROBE_AT(warp, c, 10, clock64());
+              // MMA2: [*; P] U  (rows 64..127 = P U)
+              const uint32_t ap = p_base(c % 3) - L::SUB;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_bf16(tmem_base + kColPU + buf * 64, umma_desc_sw128(ap + kk * 32),
+                          umma_desc_sw128_mn(Ust + kk * 2048, L::SUB), kIdescKM, kk > 0);
+              GDN_PROBE_AT(warp, c, 11, clock64());
+              umma_commit(bar(B_PU_FULL + buf));
+              umma_commit(bar(B_P_FREE + c % 3));
+              GDN_PROBE_AT(warp, c, 5, clock64());
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          done = c + 1;
+        }
+      }
+      // the last products have completed before tensor memory is released
+      if (warp == kWarpE1Issue && lane == 0 && done > 0)
+        mbar_wait_bounded(bar(B_PU_FULL + ((done - 1) & 1)), ((done - 1) >> 1) & 1, kWaitTimeoutNs);
+    } else if (warp == 14 || warp == 15) {
+      // ---- output (warps 14,15) ----
+      for (int c = 0; c < nc; ++c) {
+        const int slot = c % NIN, buf = c & 1;
+        const int valid = valid_rows(c);
+        const float *gate = gate_ptr(slot);
+          // ---- E2b: O = diag(gamma) (Q H) + P U (row = token), then store ----
+          GDN_PHASE(0);
+          bool ok = role_wait(bar(B_PU_FULL + buf), (c >> 1) & 1, S, p, n, h, 13);
+          if (!__all_sync(0xffffffffu, ok)) break;
+          GDN_PHASE(1);
+          tc_fence_after();
+          // the staging tile must have been read by the previous chunk's store
+          if (c > 0) ok = role_wait(bar(B_OST_FREE), (c - 1) & 1, S, p, n, h, 14);
+          if (!__all_sync(0xffffffffu, ok)) break;
+          {
+            const float gi = gate[64 + row];
+            const bool full = valid == 64;
+            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) +
+                                  ((size_t)(start + (int64_t)c * 64 + row) * H + h) * dv + col0;
+#pragma unroll 1
+            for (int q2 = 0; q2 < 4; ++q2) {
+              uint32_t a[16], b[16];
+              tmem_ld16(tm(kColD1 + buf * 64 + 16 * q2), a);
+              tmem_ld16(tm(kColPU + buf * 64 + 16 * q2), b);
+              tmem_wait_ld();
+              uint32_t w8[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                w8[e] = pack_bf16(fmaf(gi, __uint_as_float(a[2 * e]), __uint_as_float(b[2 * e])),
+                                  fmaf(gi, __uint_as_float(a[2 * e + 1]), __uint_as_float(b[2 * e + 1])));
+              const uint4 lo = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+              const uint4 hi = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+              if (full) {
+                S4(tile_addr(sbase + L::OFF_OST, row, 16 * q2)) = lo;
+                S4(tile_addr(sbase + L::OFF_OST, row, 16 * q2 + 8)) = hi;
+              } else if (row < valid) {  // last partial chunk: this thread's row, directly
+                *reinterpret_cast<uint4 *>(orow + 16 * q2) = lo;
+                *reinterpret_cast<uint4 *>(orow + 16 * q2 + 8) = hi;
+              }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(B_D1_FREE + buf));
+            mbar_arrive(bar(B_PU_FREE + buf));
+            if (full) fence_proxy_async_smem();
+            mbar_arrive(bar(B_EMPTY_IN + slot));
+            mbar_arrive(bar(B_OST_FULL));
+            GDN_PHASE(2);
+            if (r == 64) {  // one thread stores the tile and frees it once read
+              ok = role_wait(bar(B_OST_FULL), c & 1, S, p, n, h, 15);
+              if (ok && full) {
+                tma_store_3d(&tmap_o, col0, h, (int)(start + (int64_t)c * 64), sbase + L::OFF_OST);
+                bulk_commit();
+                bulk_wait_read<0>();
+              }
+              mbar_arrive(bar(B_OST_FREE));
+            }
+          }
+          GDN_PHASE(3);
+      }
+      if (r == 64) bulk_wait_all();  // every O store has completed
+    } else if (is_e2a_warp(warp)) {
+      // ---- E2a (warps 6,7,10,11): H <- gamma_C H + K^T Ud (row = key index);
+      // this thread's part of the state, H[row][cb .. cb+31], stays in registers.
+      // Warp 6 lane 0 then issues MMA1 of the next chunk.
+      const int cb = warp >= 10 ? 32 : 0;
+      const size_t state_row =
+          ((size_t)n * H + h) * (size_t)DK * dv + (size_t)row * dv + col0 + cb;
+      float hrow[32];
+      auto store_seg = [&](uint32_t tilebase, const float *x) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          S4(tile_addr(tilebase, row, cb + 8 * q)) =
+              make_uint4(pack_bf16(x[8 * q], x[8 * q + 1]), pack_bf16(x[8 * q + 2], x[8 * q + 3]),
+                         pack_bf16(x[8 * q + 4], x[8 * q + 5]), pack_bf16(x[8 * q + 6], x[8 * q + 7]));
+      };
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
         float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
         if (p.s0) v4 = *reinterpret_cast<const float4 *>(p.s0 + state_row + 4 * q);
         hrow[4 * q] = v4.x;
@@ -669,153 +795,75 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
         hrow[4 * q + 2] = v4.z;
         hrow[4 * q + 3] = v4.w;
       }
-      store_row_bf16(Hs, row, hrow);
+      store_seg(Hs, hrow);
       fence_proxy_async_smem();
       mbar_arrive(bar(B_H_READY));
-    }
-
-    // chain warps: chunks 0 .. nc-1.  Output warps: chunks -2 .. nc-1, draining
-    // the A rows of chunk c+2 after storing O of chunk c.
-    bool alive = true;
-    for (int c = chain ? 0 : -2; c < nc && alive; ++c) {
-      const int slot = (c + NIN) % NIN, buf = c & 1;
-      const int valid = valid_rows(c);
-      const float *gate = gate_ptr(slot);
-      if (chain) {
-        // ---- E1: U = U~ - W H (row = token), Ud = U * exp(G_C - G) ----
-        GDN_PHASE(0);
-        bool ok = role_wait(bar(B_D1_FULL + buf), (c >> 1) & 1, S, p, n, h, 11);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        GDN_PHASE(1);
-        tc_fence_after();
-        {
-          const uint32_t Ut = stage_base(buf) + L::TU;
-          const float dj = gate[128 + row];
-          GDN_PHASE(10);
-          // compact loop over 16-column slices (keeps this code resident in the
-          // instruction cache between chunks)
-#pragma unroll 1
-          for (int q2 = 0; q2 < 4; ++q2) {
-            uint32_t w[16];
-            tmem_ld16(tm(kColD1 + buf * 64 + 16 * q2), w);
-            const uint4 xa = S4(tile_addr(Ut, row, 16 * q2)), xb = S4(tile_addr(Ut, row, 16 * q2 + 8));
-            tmem_wait_ld();
-            const uint32_t x[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-            uint32_t pu[8], pd[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float u0 = bf16_lo(x[e]) - __uint_as_float(w[2 * e]);
-              const float u1 = bf16_hi(x[e]) - __uint_as_float(w[2 * e + 1]);
-              pu[e] = pack_bf16(u0, u1);
-              pd[e] = pack_bf16(u0 * dj, u1 * dj);
-            }
-            S4(tile_addr(Ust, row, 16 * q2)) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
-            S4(tile_addr(Ust, row, 16 * q2 + 8)) = make_uint4(pu[4], pu[5], pu[6], pu[7]);
-            S4(tile_addr(Uds, row, 16 * q2)) = make_uint4(pd[0], pd[1], pd[2], pd[3]);
-            S4(tile_addr(Uds, row, 16 * q2 + 8)) = make_uint4(pd[4], pd[5], pd[6], pd[7]);
+      int issued = 0;  // MMA1 products issued (by warp 6 lane 0)
+      bool alive = true;
+      if (warp == kWarpE2aIssue) {
+        if (lane == 0) {
+          alive = mma1_ready(0);
+          if (alive) {
+            tc_fence_after();
+            issue_mma1(0);
           }
-          tc_fence_before();
-          mbar_arrive(bar(B_D1_FREE + buf));
         }
-        GDN_PHASE(11);
-        fence_proxy_async_smem();
-        GDN_PHASE(12);
-        mbar_arrive(bar(B_U_READY));
-        GDN_PHASE(2);
-
-        // ---- E2a: H <- gamma_C H + K^T Ud (row = key index) ----
-        ok = role_wait(bar(B_DH_FULL), c & 1, S, p, n, h, 12);
-        if (!__all_sync(0xffffffffu, ok)) break;
+        alive = __shfl_sync(0xffffffffu, alive, 0);
+        issued = alive ? 1 : 0;
+      }
+      for (int c = 0; c < nc && alive; ++c) {
+        const int slot = c % NIN;
         GDN_PHASE(3);
+        bool ok = role_wait(bar(B_DH_FULL), c & 1, S, p, n, h, 12);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        GDN_PHASE(4);
         tc_fence_after();
         {
           const float gC = sgc[slot];
-          uint32_t wa[32], wb[32];
-          tmem_ld32(tm(kColH), wa);
-          tmem_ld32(tm(kColH + 32), wb);
+          uint32_t w[32];
+          tmem_ld32(tm(kColH + cb), w);
           tmem_wait_ld();
+          GDN_PHASE(7);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            hrow[j] = fmaf(gC, hrow[j], __uint_as_float(wa[j]));
-            hrow[32 + j] = fmaf(gC, hrow[32 + j], __uint_as_float(wb[j]));
-          }
+          for (int j = 0; j < 32; ++j) hrow[j] = fmaf(gC, hrow[j], __uint_as_float(w[j]));
         }
+        GDN_PHASE(8);
         tc_fence_before();
-        store_row_bf16(Hs, row, hrow);
+        store_seg(Hs, hrow);
+        GDN_PHASE(9);
         fence_proxy_async_smem();
+        GDN_PHASE(10);
         mbar_arrive(bar(B_H_READY));
         mbar_arrive(bar(B_EMPTY_IN + slot));
-        GDN_PHASE(4);
-      } else if (c >= 0) {
-        // ---- E2b: O = diag(gamma) (Q H) + P U (row = token), then store ----
-        GDN_PHASE(0);
-        bool ok = role_wait(bar(B_PU_FULL + buf), (c >> 1) & 1, S, p, n, h, 13);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        GDN_PHASE(1);
-        tc_fence_after();
-        // the staging tile must have been read by the previous chunk's store
-        if (c > 0) ok = role_wait(bar(B_OST_FREE), (c - 1) & 1, S, p, n, h, 14);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        {
-          const float gi = gate[64 + row];
-          const bool full = valid == 64;
-          __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) +
-                                ((size_t)(start + (int64_t)c * 64 + row) * H + h) * dv + col0;
-#pragma unroll 1
-          for (int q2 = 0; q2 < 4; ++q2) {
-            uint32_t a[16], b[16];
-            tmem_ld16(tm(kColD1 + buf * 64 + 16 * q2), a);
-            tmem_ld16(tm(kColPU + buf * 64 + 16 * q2), b);
-            tmem_wait_ld();
-            uint32_t w8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              w8[e] = pack_bf16(fmaf(gi, __uint_as_float(a[2 * e]), __uint_as_float(b[2 * e])),
-                                fmaf(gi, __uint_as_float(a[2 * e + 1]), __uint_as_float(b[2 * e + 1])));
-            const uint4 lo = make_uint4(w8[0], w8[1], w8[2], w8[3]);
-            const uint4 hi = make_uint4(w8[4], w8[5], w8[6], w8[7]);
-            if (full) {
-              S4(tile_addr(sbase + L::OFF_OST, row, 16 * q2)) = lo;
-              S4(tile_addr(sbase + L::OFF_OST, row, 16 * q2 + 8)) = hi;
-            } else if (row < valid) {  // last partial chunk: this thread's row, directly
-              *reinterpret_cast<uint4 *>(orow + 16 * q2) = lo;
-              *reinterpret_cast<uint4 *>(orow + 16 * q2 + 8) = hi;
+        GDN_PHASE(5);
+        if (warp == kWarpE2aIssue && c + 1 < nc) {
+          if (lane == 0) {
+            ok = mma1_ready(c + 1);
+            if (ok) {
+              tc_fence_after();
+              issue_mma1(c + 1);
+              GDN_PROBE_AT(warp, c + 1, 6, clock64());
             }
           }
-          tc_fence_before();
-          mbar_arrive(bar(B_D1_FREE + buf));
-          mbar_arrive(bar(B_PU_FREE + buf));
-          if (full) fence_proxy_async_smem();
-          mbar_arrive(bar(B_EMPTY_IN + slot));
-          mbar_arrive(bar(B_OST_FULL));
-          GDN_PHASE(2);
-          if (r == 64) {  // one thread stores the tile and frees it once read
-            ok = role_wait(bar(B_OST_FULL), c & 1, S, p, n, h, 15);
-            if (ok && full) {
-              tma_store_3d(&tmap_o, col0, h, (int)(start + (int64_t)c * 64), sbase + L::OFF_OST);
-              bulk_commit();
-              bulk_wait_read<0>();
-            }
-            mbar_arrive(bar(B_OST_FREE));
-          }
+          alive = __shfl_sync(0xffffffffu, ok, 0);
+          if (alive) issued = c + 2;
         }
-        GDN_PHASE(3);
       }
-      // output warps: the A rows of the accumulator two chunks ahead
-      if (!chain && c + 2 < nc) alive = s_epilogue(c + 2);
-      GDN_PHASE(7);
-    }
-    if (r == 64) bulk_wait_all();  // every O store has completed
-    if (chain && p.sN && !*S.abort_flag) {
+      // the last MMA1 has completed before tensor memory is released
+      if (warp == kWarpE2aIssue && lane == 0 && issued > 0)
+        mbar_wait_bounded(bar(B_D1_FULL + ((issued - 1) & 1)), ((issued - 1) >> 1) & 1,
+                          kWaitTimeoutNs);
+      if (p.sN && !*S.abort_flag) {
 #pragma unroll
-      for (int q = 0; q < 16; ++q)
-        *reinterpret_cast<float4 *>(p.sN + state_row + 4 * q) =
-            make_float4(hrow[4 * q], hrow[4 * q + 1], hrow[4 * q + 2], hrow[4 * q + 3]);
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4 *>(p.sN + state_row + 4 * q) =
+              make_float4(hrow[4 * q], hrow[4 * q + 1], hrow[4 * q + 2], hrow[4 * q + 3]);
+      }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kWarpSIssue) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
@@ -845,5 +893,8 @@ cudaError_t launch_fwd_tc64(const FwdParams &p, cudaStream_t stream) {
 #ifdef GDN_PHASE_PROBE
 extern "C" int gdn_phase_probe_read(unsigned long long *host) {
   return (int)cudaMemcpyFromSymbol(host, gdn::tc::g_phase_probe, sizeof(gdn::tc::g_phase_probe));
+}
+extern "C" int gdn_wait_iters_read(unsigned long long *host) {
+  return (int)cudaMemcpyFromSymbol(host, gdn::tc::g_wait_iters, sizeof(gdn::tc::g_wait_iters));
 }
 #endif

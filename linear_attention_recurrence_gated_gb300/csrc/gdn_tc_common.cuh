@@ -14,15 +14,26 @@ using namespace ptx;
 
 #ifdef GDN_PHASE_PROBE
 // Phase timing build only: clock stamps of CTA (0,0,0), [warp][chunk][phase].
-static __device__ unsigned long long g_phase_probe[10 * 64 * 16];
+static __device__ unsigned long long g_phase_probe[32 * 64 * 16];
 #define GDN_PHASE(ph)                                                                      \
   do {                                                                                     \
-    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && lane == 0 && c >= 0 && c < 64) \
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && lane == 0 && c >= 0 &&    \
+        c < 64 && warp < 32)                                                               \
       ::gdn::tc::g_phase_probe[(warp * 64 + c) * 16 + (ph)] = clock64();                   \
+  } while (0)
+// Any value into slot [w][cc][ph] (thread-agnostic; used by single-thread roles).
+#define GDN_PROBE_AT(w, cc, ph, val)                                                       \
+  do {                                                                                     \
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (cc) >= 0 && (cc) < 64 && \
+        (w) >= 0 && (w) < 32)                                                              \
+      ::gdn::tc::g_phase_probe[((w) * 64 + (cc)) * 16 + (ph)] = (val);                     \
   } while (0)
 #else
 #define GDN_PHASE(ph) \
   do {                \
+  } while (0)
+#define GDN_PROBE_AT(w, cc, ph, val) \
+  do {                               \
   } while (0)
 #endif
 
@@ -50,23 +61,49 @@ struct Shared {
   volatile int *abort_flag;
 };
 
-__device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, const Shared &S,
-                                          const FwdParams &p, int n, int h, uint32_t where) {
-  if (mbar_try_wait(bar, parity)) return true;
+#ifdef GDN_PHASE_PROBE
+// Phase timing build only: try_wait calls per warp of CTA (0,0,0).
+static __device__ unsigned long long g_wait_iters[32];
+#define GDN_COUNT_WAIT(it)                                                                 \
+  do {                                                                                     \
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (threadIdx.x & 31) == 0)  \
+      atomicAdd(&::gdn::tc::g_wait_iters[threadIdx.x >> 5], (unsigned long long)(it));     \
+  } while (0)
+#else
+#define GDN_COUNT_WAIT(it) \
+  do {                     \
+  } while (0)
+#endif
+
+// Slow path of role_wait, one shared copy: keep polling (try_wait suspends the
+// thread until the phase completes or a hardware time limit passes), give up
+// after kWaitTimeoutNs or once another role has raised the abort flag.
+static __device__ __noinline__ bool role_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                                   DeviceStatus *status, int n, int h, uint32_t where) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) {
+      GDN_COUNT_WAIT(it);
+      return true;
+    }
     if ((it & 63u) == 0) {
-      if (*S.abort_flag) return false;
+      if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-        *S.abort_flag = 1;
-        report(p.status, GDN_ERR_TIMEOUT, (uint32_t)n, (uint32_t)h, where);
+        *abort_flag = 1;
+        report(status, GDN_ERR_TIMEOUT, (uint32_t)n, (uint32_t)h, where);
         return false;
       }
     }
   }
 }
 
+// Wait for phase `parity` of the mbarrier at `bar`; false once the wait gave
+// up (GDN_ERR_TIMEOUT recorded) or the CTA is aborting.
+__device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, const Shared &S,
+                                          const FwdParams &p, int n, int h, uint32_t where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return role_wait_slow(bar, parity, S.abort_flag, p.status, n, h, where);
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
