@@ -22,32 +22,28 @@
 //   MMA3  DH  = [*; K^T] Ud          rows 64..127 = K^T Ud  (the state increment)
 //   MMA2  DPU = [*; P] U             rows 64..127 = P U
 //   E2a   H <- gamma_C H + DH  (registers), bf16 copy -> shared for the next MMA1
-//   E2b   O = diag(gamma) Q H + P U -> bf16 -> TMA store
+//   E2b   O = diag(gamma) Q H + P U -> bf16 -> global
 // "*" rows are whatever finite tile precedes/follows in shared memory; their
 // products land in accumulator rows nobody reads.  H, U and Ud are MN-major
 // operands (row-major tiles, no transposes); K^T is the MN-major view of the
 // TMA-loaded K tile.
 //
-// Roles (20 warps, one CTA per SM; warp w reaches the TMEM lanes 32*(w%4)..+31
+// Roles (24 warps, one CTA per SM; warp w reaches the TMEM lanes 32*(w%4)..+31
 // and issues on SM sub-partition w%4):
 //   warp 16        producer: gate vectors + TMA loads of Q, K, V (ring of 3
 //                  slots), and an L2 prefetch of the tiles that next reuse the slot
 //   warp 13        [Q; K] K^T issuer (tcgen05.mma + commit); owns tensor memory
-//   warp 12        carry-chain issuer: MMA1, then MMA3 + MMA2, per chunk
 //   warps 8,9      drain the P rows of [Q; K] K^T (masked decay, bf16)
 //   warps 18,19    drain the A rows (masked decay and beta, fp32)
-//   warps 0-3      prep: diagonal 16x16 inverses of (I + A) (fp32), couplings
-//                  (tf32 mma), blocked substitution for W (into the input slot,
-//                  right before Q) and U~ (bf16 mma)
-//   warps 4,5      E1 (U, Ud from W H) on lane quarters 0,1
+//   warps 0-3, 20-23  prep, two teams on alternate chunks: diagonal 16x16
+//                  inverses of (I + A) (fp32), couplings (tf32 mma), blocked
+//                  substitution for W (into the input slot, right before Q) and
+//                  U~ (bf16 mma)
+//   warps 4,5,12,17  E1 (U, Ud from W H) on lane quarters 0,1; warp 4 then
+//                  issues MMA3 and MMA2
 //   warps 6,7,10,11  E2a (state update) on lane quarters 2,3, 32 value columns
-//                  per warp, the state in registers
-//   warps 14,15    output (E2b) and its TMA store
-//   warp 17        idle
-// E1 and E2a, the two halves of the serial chain, issue on different
-// sub-partitions.
-// The issuers wait on mbarriers with try_wait (the thread sleeps until the
-// phase completes), so a ready operand is picked up without polling delay.
+//                  per warp, the state in registers; warp 6 then issues the next MMA1
+//   warps 14,15    output (E2b): each thread stores its row of O
 // Every wait is bounded; a timeout records GDN_ERR_TIMEOUT and ends the loops.
 #include "gdn_tc_common.cuh"
 
@@ -57,16 +53,18 @@ namespace {
 using namespace ptx;
 using namespace tc;
 
-constexpr int DK = 64, NIN = 3;
+constexpr int DK = 64, NIN = 4;
 // Warp map.  A warp reaches the TMEM lanes 32*(warp%4)..+31 and issues on SM
 // sub-partition warp%4, so the roles are spread to balance the sub-partitions.
-constexpr int kThreads64 = 640;  // 20 warps
+constexpr int kThreads64 = 768;  // 24 warps
 constexpr int kWarpSIssue = 13, kWarpProducer = 16;
+// prep teams: warps 0-3 take the even chunks, warps 20-23 the odd ones
+__device__ __forceinline__ int prep_team(int w) { return w < 4 ? 0 : (w >= 20 ? 1 : -1); }
 constexpr int kWarpE1Issue = 4, kWarpE2aIssue = 6;  // lane 0 of these issues the carry products
 __device__ __forceinline__ bool is_drain_warp(int w) { return w == 8 || w == 9 || w == 18 || w == 19; }
 __device__ __forceinline__ bool is_e1_warp(int w) { return w == 4 || w == 5 || w == 12 || w == 17; }
 __device__ __forceinline__ bool is_e2a_warp(int w) { return w == 6 || w == 7 || w == 10 || w == 11; }
-constexpr uint32_t kBarPrep = 1;
+constexpr uint32_t kBarPrep = 1;  // + team: named barriers 1, 2
 constexpr uint32_t kTmemCols = 512;
 // TMEM column map: S double buffer, D1 double buffer, DPU double buffer, DH.
 constexpr uint32_t kColS = 0, kColD1 = 128, kColPU = 256, kColH = 384;
@@ -77,26 +75,33 @@ constexpr uint32_t kIdescMM = umma_idesc_bf16(128, 64, 1, 1);    // MN-major A a
 
 struct L64 {
   static constexpr int SUB = 8192;
-  // input slot: W (written by prep) | Q | K | V | gates  -> [W;Q] and [Q;K] contiguous
+  // input slot: W (written by prep) | Q | K | V, then U~ written over V by
+  // prep | gates  -> [W;Q] and [Q;K] contiguous
   static constexpr int SW = 0, SQ = SUB, SK = 2 * SUB, SV = 3 * SUB, SG = 4 * SUB;
-  static constexpr int SLOT = 4 * SUB + 2048;
+  // gates: G (log2) [0,64), 2^(G_C - G) [64,128), beta [128,192), E [192,256)
+  static constexpr int SLOT = 4 * SUB + 1024;
   static constexpr int OFF_IN = 0;
-  static constexpr int OFF_UT = OFF_IN + NIN * SLOT;  // U~ ring [2][token][dv] bf16
-  static constexpr int OFF_H = OFF_UT + 2 * SUB;      // state H [dk][dv] bf16
+  static constexpr int OFF_H = OFF_IN + NIN * SLOT;   // state H [dk][dv] bf16
   static constexpr int OFF_U = OFF_H + SUB;           // U  [token][dv] bf16
   static constexpr int OFF_UD = OFF_U + SUB;          // Ud [token][dv] bf16
-  static constexpr int OFF_OST = OFF_UD + SUB;        // O staging [token][dv] bf16
-  // P ring [3][token][token] bf16, right after the staging tile: the 8 KB tile
+  // P ring [3][token][token] bf16, right after the Ud tile: the 8 KB tile
   // before P_i completes the M = 128 operand [*; P_i] of MMA2
-  static constexpr int OFF_P = OFF_OST + SUB;
-  static constexpr int A_LD = 68;
-  static constexpr int OFF_A = OFF_P + 3 * SUB;       // f32 [2][64][A_LD]
-  static constexpr int TF_LD = 20;
-  static constexpr int OFF_TF = OFF_A + 2 * 64 * A_LD * 4;
-  static constexpr int TB_LD = 24;
-  static constexpr int OFF_TB = OFF_TF + 4 * 16 * TF_LD * 4;
-  static constexpr int OFF_MB = OFF_TB + 2 * 4 * 16 * TB_LD * 2;
-  static constexpr int OFF_GC = OFF_MB + 6 * 16 * TB_LD * 2;
+  static constexpr int OFF_P = OFF_UD + SUB;
+  // A, per S buffer: the 10 16x16 blocks on or below the diagonal, block (r, c)
+  // at index r (r + 1) / 2 + c, rows of A_LD floats
+  static constexpr int A_LD = 20;
+  static constexpr int A_BLK = 16 * A_LD;              // floats per block
+  static constexpr int A_BUF = 10 * A_BLK;             // floats per buffer
+  static constexpr int OFF_A = OFF_P + 3 * SUB;        // f32 [2][10][16][A_LD]
+  // per prep team: T_ii diag(beta gamma) and T_ii diag(beta) (bf16,
+  // column-major) and the couplings M_ik (bf16).  T_ii itself (fp32,
+  // column-major) overwrites the diagonal block A_ii once it has been read.
+  static constexpr int TB_LD = 16;
+  static constexpr int TB_TEAM = 2 * 4 * 16 * TB_LD * 2;
+  static constexpr int OFF_TB = OFF_A + 2 * A_BUF * 4;
+  static constexpr int MB_TEAM = 6 * 16 * TB_LD * 2;
+  static constexpr int OFF_MB = OFF_TB + 2 * TB_TEAM;
+  static constexpr int OFF_GC = OFF_MB + 2 * MB_TEAM;
   static constexpr int OFF_VOTE = OFF_GC + 64;
   static constexpr int OFF_TMEM = OFF_VOTE + 64;
   static constexpr int OFF_BAR = OFF_TMEM + 16;
@@ -104,35 +109,33 @@ struct L64 {
   static constexpr int OFF_FLAG = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_FLAG + 16;
   static constexpr int ALLOC = BYTES + 1024;
-  static_assert(SLOT % 1024 == 0 && OFF_UT % 1024 == 0 && OFF_H % 1024 == 0 && OFF_P % 1024 == 0,
+  static_assert(SLOT % 1024 == 0 && OFF_H % 1024 == 0 && OFF_P % 1024 == 0,
                 "alignment");
   static_assert(ALLOC <= 232448, "shared memory budget");
 };
 
 // mbarrier indices
 enum : int {
-  B_FULL_IN = 0,     // [3]  TMA bytes landed (+ producer arrival)
-  B_EMPTY_IN = 3,    // [3]  E2a and output warps done with the slot (192)
-  B_FULL_ST = 6,     // [2]  prep wrote W and U~ (128)
-  B_TMEM_FULL = 8,   // [2]  Q K^T / K K^T accumulator ready (commit)
-  B_TMEM_EMPTY = 10, // [2]  ... drained (128, the drain warps)
-  B_S_READY = 12,    // [2]  P and A in shared memory (128, the drain warps)
-  B_H_READY = 14,    //      bf16 state written for the next MMA1 (128)
-  B_D1_FULL = 15,    // [2]  MMA1 done (commit)
-  B_D1_FREE = 17,    // [2]  D1 drained (E1 64 + output 64)
-  B_U_READY = 19,    //      U and Ud written (64)
-  B_DH_FULL = 20,    //      MMA3 done (commit)
-  B_PU_FULL = 21,    // [2]  MMA2 done (commit)
-  B_PU_FREE = 23,    // [2]  DPU drained (64)
-  B_OST_FULL = 25,   //      O rows staged (64)
-  B_OST_FREE = 26,   //      staging tile read by the store (1)
-  B_UT_FREE = 27,    // [2]  U~ buffer read by E1 (128)
+  B_FULL_IN = 0,     // [4]  TMA bytes landed (+ producer arrival)
+  B_EMPTY_IN = 4,    // [4]  E2a and output warps done with the slot (192)
+  B_FULL_ST = 8,     // [2]  prep wrote W and U~ (128)
+  B_TMEM_FULL = 10,  // [2]  Q K^T / K K^T accumulator ready (commit)
+  B_TMEM_EMPTY = 12, // [2]  ... drained (128, the drain warps)
+  B_S_READY = 14,    // [2]  P and A in shared memory (128, the drain warps)
+  B_H_READY = 16,    //      bf16 state written for the next MMA1 (128)
+  B_D1_FULL = 17,    // [2]  MMA1 done (commit)
+  B_D1_FREE = 19,    // [2]  D1 drained (E1 128 + output 64)
+  B_U_READY = 21,    //      U and Ud written (128)
+  B_DH_FULL = 22,    //      MMA3 done (commit)
+  B_PU_FULL = 23,    // [2]  MMA2 done (commit)
+  B_PU_FREE = 25,    // [2]  DPU drained (64)
+  B_A_FREE = 27,     // [2]  A buffer read by the prep (inverse, couplings) (128)
   B_P_FREE = 29,     // [3]  P buffer read by MMA2 (commit)
 };
 
 // One thread drains one row i of a 64-column fp32 accumulator of [Q; K] K^T
 // (taddr: this warp's TMEM lane quarter at the buffer's first column) into a
-// masked, decayed row of P (bf16, swizzled tile at Ps) or of A (fp32, Arow):
+// masked, decayed row of P (bf16, swizzled tile at Ps) or of A (fp32, into the blocks at Ablk):
 //   P_ij = S_ij 2^(G_i - G_j) (j <= i),   A_ij = beta_i S_ij 2^(G_i - G_j) (j < i)
 // with G in log2 units.  The warp owns rows 32*half .. 32*half+31.  Per
 // 16-column block: blocks after those rows are zero (no load, no arithmetic);
@@ -143,7 +146,7 @@ enum : int {
 // small.
 __device__ __noinline__ void drain_s_row(uint32_t taddr, const float *G2, const float *E, int i,
                                          int half, bool isP, float bi, int ilim, bool rowok,
-                                         uint32_t Ps, float *Arow, uint8_t *smem,
+                                         uint32_t Ps, float *Ablk, uint8_t *smem,
                                          uint32_t sbase) {
   const float Gi = G2[i];
 #pragma unroll 1
@@ -187,10 +190,12 @@ __device__ __noinline__ void drain_s_row(uint32_t taddr, const float *G2, const 
       *reinterpret_cast<uint4 *>(smem + (tile_addr(Ps, i, 16 * cb + 8) - sbase)) =
           make_uint4(pack_bf16(val[8], val[9]), pack_bf16(val[10], val[11]),
                      pack_bf16(val[12], val[13]), pack_bf16(val[14], val[15]));
-    } else {
+    } else if (cb <= (i >> 4)) {  // blocks on or below the diagonal only
+      const int rb = i >> 4;
+      float *dst = Ablk + ((rb * (rb + 1)) / 2 + cb) * L64::A_BLK + (i & 15) * L64::A_LD;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<float4 *>(Arow + 16 * cb + 4 * q) =
+        *reinterpret_cast<float4 *>(dst + 4 * q) =
             make_float4(val[4 * q], val[4 * q + 1], val[4 * q + 2], val[4 * q + 3]);
     }
   }
@@ -199,8 +204,7 @@ __device__ __noinline__ void drain_s_row(uint32_t taddr, const float *G2, const 
 __global__ void __launch_bounds__(kThreads64, 1)
 gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_q,
                     const __grid_constant__ CUtensorMap tmap_k,
-                    const __grid_constant__ CUtensorMap tmap_v,
-                    const __grid_constant__ CUtensorMap tmap_o) {
+                    const __grid_constant__ CUtensorMap tmap_v) {
   using L = L64;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -222,7 +226,6 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
   float *sgc = reinterpret_cast<float *>(smem + L::OFF_GC);
   auto bar = [&](int i) { return sbase + L::OFF_BAR + 8u * i; };
   auto slot_base = [&](int s) { return sbase + L::OFF_IN + s * L::SLOT; };
-  auto ut_base = [&](int s) { return sbase + L::OFF_UT + s * L::SUB; };
   auto p_base = [&](int s) { return sbase + L::OFF_P + s * L::SUB; };
   auto gate_ptr = [&](int s) {
     return reinterpret_cast<float *>(smem + L::OFF_IN + s * L::SLOT + L::SG);
@@ -243,7 +246,7 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
       mbar_init(bar(B_S_READY + s), 128);
       mbar_init(bar(B_D1_FULL + s), 1);
       mbar_init(bar(B_D1_FREE + s), 192);
-      mbar_init(bar(B_UT_FREE + s), 128);
+      mbar_init(bar(B_A_FREE + s), 128);
       mbar_init(bar(B_PU_FULL + s), 1);
       mbar_init(bar(B_PU_FREE + s), 64);
     }
@@ -251,8 +254,6 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
     mbar_init(bar(B_U_READY), 128);
     for (int s = 0; s < 3; ++s) mbar_init(bar(B_P_FREE + s), 1);
     mbar_init(bar(B_DH_FULL), 1);
-    mbar_init(bar(B_OST_FULL), 64);
-    mbar_init(bar(B_OST_FREE), 1);
     *S.abort_flag = 0;
     fence_mbar_init();
   }
@@ -292,35 +293,37 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
     int issued = 0;
     for (int c = 0; c < nc; ++c) {
       const int slot = c % NIN;
+      // Gate vectors of chunk c, computed before the slot is free: G (log2
+      // units), the decay to the chunk end 2^(G_C - G), beta, and
+      // E_j = 2^(G_b - G_j) with b the last token of j's 16-token block.
+      const float x0 = gv0 * kLog2e, x1 = gv1 * kLog2e;
+      float s = x0 + x1;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, s, off);
+        if (lane >= off) s += y;
+      }
+      const float G0 = s - x1, G1 = s;
+      const float Gl = __shfl_sync(0xffffffffu, G1, 31);
+      const float Gb = __shfl_sync(0xffffffffu, G1, (lane & ~7) | 7);
+      const float2 vD = make_float2(ex2(Gl - G0), ex2(Gl - G1));
+      const float2 vE = make_float2(ex2(Gb - G0), ex2(Gb - G1));
+      const float2 vB = make_float2(bv0, bv1);
+      const float gC = ex2(Gl);
+      load_gates(c + 1);
       GDN_PHASE(0);
       bool ok = true;
       if (c >= NIN) ok = role_wait(bar(B_EMPTY_IN + slot), ((c / NIN) - 1) & 1, S, p, n, h, 1);
       GDN_PHASE(1);
       if (!__all_sync(0xffffffffu, ok)) break;
       {
-        // G (log2 units), gamma = 2^G, decay to the chunk end, beta, and
-        // E_j = 2^(G_b - G_j) with b the last token of j's 16-token block.
-        const float x0 = gv0 * kLog2e, x1 = gv1 * kLog2e;
-        float s = x0 + x1;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, s, off);
-          if (lane >= off) s += y;
-        }
-        const float G0 = s - x1, G1 = s;
-        const float Gl = __shfl_sync(0xffffffffu, G1, 31);
-        const float Gb = __shfl_sync(0xffffffffu, G1, (lane & ~7) | 7);
         float *gate = gate_ptr(slot);
         *reinterpret_cast<float2 *>(gate + 2 * lane) = make_float2(G0, G1);
-        *reinterpret_cast<float2 *>(gate + 64 + 2 * lane) = make_float2(ex2(G0), ex2(G1));
-        *reinterpret_cast<float2 *>(gate + 128 + 2 * lane) =
-            make_float2(ex2(Gl - G0), ex2(Gl - G1));
-        *reinterpret_cast<float2 *>(gate + 192 + 2 * lane) = make_float2(bv0, bv1);
-        *reinterpret_cast<float2 *>(gate + 256 + 2 * lane) =
-            make_float2(ex2(Gb - G0), ex2(Gb - G1));
-        if (lane == 0) sgc[slot] = ex2(Gl);
+        *reinterpret_cast<float2 *>(gate + 64 + 2 * lane) = vD;
+        *reinterpret_cast<float2 *>(gate + 128 + 2 * lane) = vB;
+        *reinterpret_cast<float2 *>(gate + 192 + 2 * lane) = vE;
+        if (lane == 0) sgc[slot] = gC;
       }
-      load_gates(c + 1);
       __syncwarp();
       if (lane == 0) {
         const uint32_t sb = slot_base(slot);
@@ -356,22 +359,22 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
       bool ok = role_wait(bar(B_TMEM_FULL + buf), (c >> 1) & 1, S, p, n, h, 7);
       if (ok) ok = role_wait(bar(B_FULL_IN + slot), (c / NIN) & 1, S, p, n, h, 8);
       // the P buffer was last read by MMA2 of chunk c-3; the A buffer by the
-      // prep of chunk c-2
+      // inverse and couplings of chunk c-2
       if (ok && isP && c >= 3)
         ok = role_wait(bar(B_P_FREE + c % 3), ((c / 3) - 1) & 1, S, p, n, h, 10);
       if (ok && !isP && c >= 2)
-        ok = role_wait(bar(B_FULL_ST + buf), ((c - 2) >> 1) & 1, S, p, n, h, 21);
+        ok = role_wait(bar(B_A_FREE + buf), ((c - 2) >> 1) & 1, S, p, n, h, 21);
       GDN_PHASE(9);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const int valid = valid_rows(c);
       const float *gate = gate_ptr(slot);
-      const float *G2 = gate, *beta = gate + 192, *E = gate + 256;
+      const float *G2 = gate, *beta = gate + 128, *E = gate + 192;
       const int ilim = isP ? i + 1 : i;  // P keeps j <= i, A keeps j < i
       const float bi = isP ? 1.f : beta[i];
-      float *Arow = reinterpret_cast<float *>(smem + L::OFF_A) + (buf * 64 + i) * L::A_LD;
+      float *Ablk = reinterpret_cast<float *>(smem + L::OFF_A) + buf * L::A_BUF;
       drain_s_row(tq + kColS + buf * 64, G2, E, i, wq & 1, isP, bi, ilim, i < valid,
-                  p_base(c % 3), Arow, smem, sbase);
+                  p_base(c % 3), Ablk, smem, sbase);
       tc_fence_before();
       mbar_arrive(bar(B_TMEM_EMPTY + buf));
       if (isP) fence_proxy_async_smem();  // P is read by MMA2 (async proxy)
@@ -403,24 +406,24 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
                           kWaitTimeoutNs);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (prep_team(warp) >= 0) {
     // ------------------------------------------------------------ prep
-    const int ptid = tid;
-    float *sTf = reinterpret_cast<float *>(smem + L::OFF_TF);
-    __nv_bfloat16 *sTB = reinterpret_cast<__nv_bfloat16 *>(smem + L::OFF_TB);
-    __nv_bfloat16 *sMB = reinterpret_cast<__nv_bfloat16 *>(smem + L::OFF_MB);
+    // Two teams of four warps take alternate chunks (team t: c = t, t + 2, ...),
+    // each with its own scratch and named barrier; pw is the warp within the team.
+    const int team = prep_team(warp), pw = warp & 3, ptid = 32 * pw + lane;
+    const uint32_t kBar = kBarPrep + team;
+    __nv_bfloat16 *sTB = reinterpret_cast<__nv_bfloat16 *>(smem + L::OFF_TB + team * L::TB_TEAM);
+    __nv_bfloat16 *sMB = reinterpret_cast<__nv_bfloat16 *>(smem + L::OFF_MB + team * L::MB_TEAM);
     const uint32_t TBa = smem_u32(sTB), MBa = smem_u32(sMB);
-    int *vote = votes;
+    int *vote = votes + team * 8;
 
-    for (int c = 0; c < nc; ++c) {
+    for (int c = team; c < nc; c += 2) {
       const int slot = c % NIN, stage = c & 1;
       const int valid = valid_rows(c);
       GDN_PHASE(0);
       // P and A of this chunk are in shared memory; the carry is done with the
       // stage's previous contents (the P drain waited for MMA2 of chunk c-2)
       bool ok = role_wait(bar(B_S_READY + stage), (c >> 1) & 1, S, p, n, h, 2);
-      // the U~ buffer was last read by E1 of chunk c-2
-      if (ok && c >= 2) ok = role_wait(bar(B_UT_FREE + stage), ((c >> 1) - 1) & 1, S, p, n, h, 22);
       if (ok) ok = role_wait(bar(B_FULL_IN + slot), (c / NIN) & 1, S, p, n, h, 3);
       ok = __all_sync(0xffffffffu, ok) && !*S.abort_flag;
       GDN_PHASE(1);
@@ -428,9 +431,9 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
       const uint32_t sb = slot_base(slot);
       const uint32_t Ws = sb + L::SW, Qs = sb + L::SQ, Ks = sb + L::SK, Vs = sb + L::SV;
       const float *gate = gate_ptr(slot);
-      const float *gam = gate + 64, *beta = gate + 192;
-      const float *sA = reinterpret_cast<const float *>(smem + L::OFF_A) + stage * 64 * L::A_LD;
-      const uint32_t Us = ut_base(stage);
+      const float *G2 = gate, *beta = gate + 128;
+      float *sA = reinterpret_cast<float *>(smem + L::OFF_A) + stage * L::A_BUF;
+      const uint32_t Us = Vs;  // U~ replaces V, block row by block row
 
       // rows past the end of the sequence: zero Q, K, V (the Q K^T MMA has read them)
       if (ok && valid < 64) {
@@ -440,11 +443,11 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
           S4(a) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      if (lane == 0) vote[(c & 1) * 4 + warp] = ok ? 1 : 0;
-      named_sync(kBarPrep, 128);
+      if (lane == 0) vote[((c >> 1) & 1) * 4 + pw] = ok ? 1 : 0;
+      named_sync(kBar, 128);
       GDN_PHASE(2);
       {
-        const int *v = vote + (c & 1) * 4;
+        const int *v = vote + ((c >> 1) & 1) * 4;
         if (!(v[0] && v[1] && v[2] && v[3])) break;
       }
 
@@ -454,9 +457,9 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
       // rows of A as float4 (broadcast within the half-warp).  T is stored
       // column-major: fp32 for the couplings, and as bf16 T diag(beta gamma) and
       // T diag(beta) for the substitution. ----
-      if (warp >= 2) {
-        const int blk = 2 * (warp - 2) + (lane >> 4), l = lane & 15;
-        const float *Ab = sA + (16 * blk) * L::A_LD + 16 * blk;
+      if (pw >= 2) {
+        const int blk = 2 * (pw - 2) + (lane >> 4), l = lane & 15;
+        const float *Ab = sA + ((blk * (blk + 1)) / 2 + blk) * L::A_BLK;
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
@@ -475,13 +478,14 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
           }
           x[r] = s0 + s1;
         }
-        float *tcol = sTf + (blk * 16 + l) * L::TF_LD;
+        __syncwarp();  // every lane of the half-warp is done reading A_bb
+        float *tcol = sA + ((blk * (blk + 1)) / 2 + blk) * L::A_BLK + l * L::A_LD;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           *reinterpret_cast<float4 *>(tcol + 4 * q) =
               make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
         const float bj = beta[16 * blk + l];
-        const float bgj = bj * gam[16 * blk + l];
+        const float bgj = bj * ex2(G2[16 * blk + l]);  // beta_j gamma_j
         uint32_t wg[8], wb[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -496,23 +500,24 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
         tb[1] = make_uint4(wb[4], wb[5], wb[6], wb[7]);
       }
       GDN_PHASE(3);
-      named_sync(kBarPrep, 128);
+      named_sync(kBar, 128);
       GDN_PHASE(4);
 
       // ---- M_ik = T_ii A_ik (i > k) on tf32 tensor cores, stored negated (bf16) ----
 #pragma unroll 1
-      for (int blk = warp; blk < 6; blk += 4) {
+      for (int blk = pw; blk < 6; blk += 4) {
         const int i = blk == 0 ? 1 : (blk < 3 ? 2 : 3);
         const int k = blk - (i * (i - 1)) / 2;
-        const float *T = sTf + (i * 16) * L::TF_LD;  // column-major: T(row, col) = T[col * TF_LD + row]
-        const float *Ak = sA + (16 * i) * L::A_LD + 16 * k;
+        // T_ii, column-major in the diagonal block of A: T(row, col) = T[col * A_LD + row]
+        const float *T = sA + ((i * (i + 1)) / 2 + i) * L::A_BLK;
+        const float *Ak = sA + ((i * (i + 1)) / 2 + k) * L::A_BLK;
         float acc[2][4] = {};
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
-          const uint32_t a0 = to_tf32(T[(8 * ks + t) * L::TF_LD + g]);
-          const uint32_t a1 = to_tf32(T[(8 * ks + t) * L::TF_LD + g + 8]);
-          const uint32_t a2 = to_tf32(T[(8 * ks + t + 4) * L::TF_LD + g]);
-          const uint32_t a3 = to_tf32(T[(8 * ks + t + 4) * L::TF_LD + g + 8]);
+          const uint32_t a0 = to_tf32(T[(8 * ks + t) * L::A_LD + g]);
+          const uint32_t a1 = to_tf32(T[(8 * ks + t) * L::A_LD + g + 8]);
+          const uint32_t a2 = to_tf32(T[(8 * ks + t + 4) * L::A_LD + g]);
+          const uint32_t a3 = to_tf32(T[(8 * ks + t + 4) * L::A_LD + g + 8]);
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
             const uint32_t b0 = to_tf32(Ak[(8 * ks + t) * L::A_LD + 8 * nt + g]);
@@ -530,7 +535,8 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
         }
       }
       GDN_PHASE(5);
-      named_sync(kBarPrep, 128);
+      named_sync(kBar, 128);
+      mbar_arrive(bar(B_A_FREE + stage));  // A of this buffer is no longer read
       GDN_PHASE(6);
 
       // ---- block forward substitution, left-looking (a compact loop):
@@ -541,11 +547,11 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
       {
         const int arow = lrow + (lmi & 1) * 8, acol = (lmi >> 1) * 8;
         const int trow = lrow + (lmi >> 1) * 8, tcol = (lmi & 1) * 8;  // column-major T tiles
-        const bool isW = warp < 2;
+        const bool isW = pw < 2;
         const uint32_t xt = isW ? Ws : Us;
         const uint32_t bsrc = isW ? Ks : Vs;
         const int tbv = isW ? 0 : 1;
-        const int col = 32 * (warp & 1);
+        const int col = 32 * (pw & 1);
 #pragma unroll 1
         for (int lv = 0; lv < 4; ++lv) {
           float acc[2][2][4];
@@ -602,7 +608,6 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
   } else {
     // ------------------------------------------------------------ carry chain / output
     const int wq = warp & 3;                // TMEM lane quarter
-    const int r = 32 * wq + lane;           // TMEM lane = accumulator row
     const int row = 32 * (wq & 1) + lane;   // token (E1, output) or key row (E2a)
     auto tm = [&](uint32_t col) { return tmem_base + ((uint32_t)(32 * wq) << 16) + col; };
     const uint32_t Hs = sbase + L::OFF_H, Ust = sbase + L::OFF_U, Uds = sbase + L::OFF_UD;
@@ -616,12 +621,21 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
       umma_commit(bar(B_D1_FULL + (c & 1)));
     };
     // the operands and the accumulator of MMA1(c) are ready (one thread)
-    auto mma1_ready = [&](int c) {
-      bool ok = role_wait(bar(B_H_READY), c & 1, S, p, n, h, 17);
-      if (ok && c >= 2)
+    // the operands and the accumulator of MMA1(c) are ready (one thread);
+    // `pre`: D1_FREE and FULL_ST were already seen complete
+    auto mma1_ready = [&](int c, bool pre) {
+      bool ok = true;
+      if (!pre && c >= 2)
         ok = role_wait(bar(B_D1_FREE + (c & 1)), ((c >> 1) - 1) & 1, S, p, n, h, 18);
-      if (ok) ok = role_wait(bar(B_FULL_ST + (c & 1)), (c >> 1) & 1, S, p, n, h, 16);
+      if (ok && !pre) ok = role_wait(bar(B_FULL_ST + (c & 1)), (c >> 1) & 1, S, p, n, h, 16);
+      GDN_PROBE_AT(warp, c, 8, clock64());
+      if (ok) ok = role_wait(bar(B_H_READY), c & 1, S, p, n, h, 17);
+      GDN_PROBE_AT(warp, c, 9, clock64());
       return ok;
+    };
+    auto mma1_pre = [&](int c) {
+      return (c < 2 || mbar_test(bar(B_D1_FREE + (c & 1)), ((c >> 1) - 1) & 1)) &&
+             mbar_test(bar(B_FULL_ST + (c & 1)), (c >> 1) & 1);
     };
     if (is_e1_warp(warp)) {
       // ---- E1 (warps 4,5,12,17): U = U~ - W H (row = token), Ud = U * exp(G_C - G),
@@ -639,8 +653,13 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
         if (!__all_sync(0xffffffffu, ok)) break;
         GDN_PHASE(1);
         tc_fence_after();
-        const uint32_t Ut = ut_base(buf);
-        const float dj = gate[128 + row];
+        // the issuing thread looks at the (usually long complete) barrier of
+        // MMA2's accumulator now, so that the check overlaps this epilogue
+        bool pu_free = true;
+        if (warp == kWarpE1Issue && lane == 0 && c >= 2)
+          pu_free = mbar_test(bar(B_PU_FREE + buf), ((c >> 1) - 1) & 1);
+        const uint32_t Ut = slot_base(slot) + L::SV;  // U~ (written over V by prep)
+        const float dj = gate[64 + row];
         {
           uint32_t w[32];
           tmem_ld32(tm(kColD1 + buf * 64 + cb), w);
@@ -665,7 +684,6 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
         }
         tc_fence_before();
         mbar_arrive(bar(B_D1_FREE + buf));
-        mbar_arrive(bar(B_UT_FREE + buf));
         fence_proxy_async_smem();
         mbar_arrive(bar(B_U_READY));
         GDN_PHASE(2);
@@ -674,7 +692,7 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
             GDN_PROBE_AT(warp, c, 6, clock64());
             ok = role_wait(bar(B_U_READY), c & 1, S, p, n, h, 19);
             GDN_PROBE_AT(warp, c, 7, clock64());
-            if (ok && c >= 2)
+            if (ok && !pu_free)
               ok = role_wait(bar(B_PU_FREE + buf), ((c >> 1) - 1) & 1, S, p, n, h, 20);
             GDN_PROBE_AT(warp, c, 8, clock64());
             if (ok) {
@@ -716,61 +734,40 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
         const int slot = c % NIN, buf = c & 1;
         const int valid = valid_rows(c);
         const float *gate = gate_ptr(slot);
-          // ---- E2b: O = diag(gamma) (Q H) + P U (row = token), then store ----
-          GDN_PHASE(0);
-          bool ok = role_wait(bar(B_PU_FULL + buf), (c >> 1) & 1, S, p, n, h, 13);
-          if (!__all_sync(0xffffffffu, ok)) break;
-          GDN_PHASE(1);
-          tc_fence_after();
-          // the staging tile must have been read by the previous chunk's store
-          if (c > 0) ok = role_wait(bar(B_OST_FREE), (c - 1) & 1, S, p, n, h, 14);
-          if (!__all_sync(0xffffffffu, ok)) break;
-          {
-            const float gi = gate[64 + row];
-            const bool full = valid == 64;
-            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) +
-                                  ((size_t)(start + (int64_t)c * 64 + row) * H + h) * dv + col0;
+        // ---- E2b: O = diag(gamma) (Q H) + P U (row = token); each thread
+        // stores its own 128-byte row of O ----
+        GDN_PHASE(0);
+        bool ok = role_wait(bar(B_PU_FULL + buf), (c >> 1) & 1, S, p, n, h, 13);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        GDN_PHASE(1);
+        tc_fence_after();
+        {
+          const float gi = ex2(gate[row]);  // gamma_i
+          __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) +
+                                ((size_t)(start + (int64_t)c * 64 + row) * H + h) * dv + col0;
 #pragma unroll 1
-            for (int q2 = 0; q2 < 4; ++q2) {
-              uint32_t a[16], b[16];
-              tmem_ld16(tm(kColD1 + buf * 64 + 16 * q2), a);
-              tmem_ld16(tm(kColPU + buf * 64 + 16 * q2), b);
-              tmem_wait_ld();
-              uint32_t w8[8];
+          for (int q2 = 0; q2 < 4; ++q2) {
+            uint32_t a[16], b[16];
+            tmem_ld16(tm(kColD1 + buf * 64 + 16 * q2), a);
+            tmem_ld16(tm(kColPU + buf * 64 + 16 * q2), b);
+            tmem_wait_ld();
+            uint32_t w8[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                w8[e] = pack_bf16(fmaf(gi, __uint_as_float(a[2 * e]), __uint_as_float(b[2 * e])),
-                                  fmaf(gi, __uint_as_float(a[2 * e + 1]), __uint_as_float(b[2 * e + 1])));
-              const uint4 lo = make_uint4(w8[0], w8[1], w8[2], w8[3]);
-              const uint4 hi = make_uint4(w8[4], w8[5], w8[6], w8[7]);
-              if (full) {
-                S4(tile_addr(sbase + L::OFF_OST, row, 16 * q2)) = lo;
-                S4(tile_addr(sbase + L::OFF_OST, row, 16 * q2 + 8)) = hi;
-              } else if (row < valid) {  // last partial chunk: this thread's row, directly
-                *reinterpret_cast<uint4 *>(orow + 16 * q2) = lo;
-                *reinterpret_cast<uint4 *>(orow + 16 * q2 + 8) = hi;
-              }
-            }
-            tc_fence_before();
-            mbar_arrive(bar(B_D1_FREE + buf));
-            mbar_arrive(bar(B_PU_FREE + buf));
-            if (full) fence_proxy_async_smem();
-            mbar_arrive(bar(B_EMPTY_IN + slot));
-            mbar_arrive(bar(B_OST_FULL));
-            GDN_PHASE(2);
-            if (r == 64) {  // one thread stores the tile and frees it once read
-              ok = role_wait(bar(B_OST_FULL), c & 1, S, p, n, h, 15);
-              if (ok && full) {
-                tma_store_3d(&tmap_o, col0, h, (int)(start + (int64_t)c * 64), sbase + L::OFF_OST);
-                bulk_commit();
-                bulk_wait_read<0>();
-              }
-              mbar_arrive(bar(B_OST_FREE));
+            for (int e = 0; e < 8; ++e)
+              w8[e] = pack_bf16(fmaf(gi, __uint_as_float(a[2 * e]), __uint_as_float(b[2 * e])),
+                                fmaf(gi, __uint_as_float(a[2 * e + 1]), __uint_as_float(b[2 * e + 1])));
+            if (row < valid) {
+              reinterpret_cast<uint4 *>(orow + 16 * q2)[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+              reinterpret_cast<uint4 *>(orow + 16 * q2)[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
             }
           }
-          GDN_PHASE(3);
+          tc_fence_before();
+          mbar_arrive(bar(B_D1_FREE + buf));
+          mbar_arrive(bar(B_PU_FREE + buf));
+          mbar_arrive(bar(B_EMPTY_IN + slot));
+        }
+        GDN_PHASE(2);
       }
-      if (r == 64) bulk_wait_all();  // every O store has completed
     } else if (is_e2a_warp(warp)) {
       // ---- E2a (warps 6,7,10,11): H <- gamma_C H + K^T Ud (row = key index);
       // this thread's part of the state, H[row][cb .. cb+31], stays in registers.
@@ -802,7 +799,7 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
       bool alive = true;
       if (warp == kWarpE2aIssue) {
         if (lane == 0) {
-          alive = mma1_ready(0);
+          alive = mma1_ready(0, false);
           if (alive) {
             tc_fence_after();
             issue_mma1(0);
@@ -818,27 +815,25 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
         if (!__all_sync(0xffffffffu, ok)) break;
         GDN_PHASE(4);
         tc_fence_after();
+        bool pre = false;
+        if (warp == kWarpE2aIssue && lane == 0 && c + 1 < nc) pre = mma1_pre(c + 1);
         {
           const float gC = sgc[slot];
           uint32_t w[32];
           tmem_ld32(tm(kColH + cb), w);
           tmem_wait_ld();
-          GDN_PHASE(7);
 #pragma unroll
           for (int j = 0; j < 32; ++j) hrow[j] = fmaf(gC, hrow[j], __uint_as_float(w[j]));
         }
-        GDN_PHASE(8);
         tc_fence_before();
         store_seg(Hs, hrow);
-        GDN_PHASE(9);
         fence_proxy_async_smem();
-        GDN_PHASE(10);
         mbar_arrive(bar(B_H_READY));
         mbar_arrive(bar(B_EMPTY_IN + slot));
         GDN_PHASE(5);
         if (warp == kWarpE2aIssue && c + 1 < nc) {
           if (lane == 0) {
-            ok = mma1_ready(c + 1);
+            ok = mma1_ready(c + 1, pre);
             if (ok) {
               tc_fence_after();
               issue_mma1(c + 1);
@@ -874,17 +869,16 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
 cudaError_t launch_fwd_tc64(const FwdParams &p, cudaStream_t stream) {
   using L = L64;
   const int64_t tokens = p.cu ? p.seq_len : (int64_t)p.num_seqs * p.seq_len;
-  CUtensorMap tq, tk, tv, to;
+  CUtensorMap tq, tk, tv;
   if (!make_tmap(&tq, p.q, DK, p.num_heads, tokens) ||
       !make_tmap(&tk, p.k, DK, p.num_heads, tokens) ||
-      !make_tmap(&tv, p.v, p.dv, p.num_heads, tokens) ||
-      !make_tmap(&to, p.o, p.dv, p.num_heads, tokens))
+      !make_tmap(&tv, p.v, p.dv, p.num_heads, tokens))
     return cudaErrorInvalidValue;
   cudaError_t err = cudaFuncSetAttribute(gdn_fwd_tc64_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (err != cudaSuccess) return err;
   const dim3 grid(p.dv / kDvt, p.num_heads, p.num_seqs);
-  gdn_fwd_tc64_kernel<<<grid, kThreads64, L::ALLOC, stream>>>(p, tq, tk, tv, to);
+  gdn_fwd_tc64_kernel<<<grid, kThreads64, L::ALLOC, stream>>>(p, tq, tk, tv);
   return cudaGetLastError();
 }
 
