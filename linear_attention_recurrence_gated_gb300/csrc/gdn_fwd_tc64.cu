@@ -149,6 +149,12 @@ __device__ __noinline__ void drain_s_row(uint32_t taddr, const float *G2, const 
                                          uint32_t Ps, float *Ablk, uint8_t *smem,
                                          uint32_t sbase) {
   const float Gi = G2[i];
+  // |beta_i| folded into the exponent (log2 0 = -inf gives 0; a negative beta
+  // flips the sign afterwards), rows past the end of the sequence by an empty
+  // column range
+  const float Gb = Gi + __log2f(fabsf(bi));
+  const bool neg = bi < 0.f;
+  const int jlim = rowok ? ilim : 0;
 #pragma unroll 1
   for (int cb = 0; cb < 4; ++cb) {
     float val[16];
@@ -172,14 +178,17 @@ __device__ __noinline__ void drain_s_row(uint32_t taddr, const float *G2, const 
       const float scale = before ? bi * ex2(Gi - G2[16 * cb + 15]) : bi;
       tmem_wait_ld();
       if (before) {
+        const float sc = rowok ? scale : 0.f;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) val[e] = rowok ? __uint_as_float(v[e]) * scale * f[e] : 0.f;
+        for (int e = 0; e < 16; ++e) val[e] = __uint_as_float(v[e]) * (sc * f[e]);
       } else {
+        const int lim = jlim - 16 * cb;  // columns e < lim are kept
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int j = 16 * cb + e;
-          const float x = __uint_as_float(v[e]) * scale * ex2(Gi - f[e]);
-          val[e] = (rowok && j < ilim) ? x : 0.f;
+        for (int e = 0; e < 16; ++e)
+          val[e] = e < lim ? __uint_as_float(v[e]) * ex2(Gb - f[e]) : 0.f;
+        if (neg) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) val[e] = -val[e];
         }
       }
     }
