@@ -184,6 +184,7 @@ def measured_peaks():
 # The translation unit each kernel is compiled from; with the shared headers it
 # fixes the machine code whose counters a profile summary records.
 KERNEL_SOURCES = {
+    "decode": "gdn_decode.cu",
     "simt_fp32": "gdn_fwd_simt.cu",
     "simt_bf16": "gdn_fwd_simt.cu",
     "tc64_bf16": "gdn_fwd_tc64.cu",
@@ -422,6 +423,132 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
     return 0
 
 
+def decode_bytes(w: W.Workload) -> float:
+    """HBM bytes of one decode step: the fp32 state read and written, q, k, v,
+    g, beta read and o written, for every (sequence, head)."""
+    e = 4 if w.dtype == "fp32" else 2
+    per_head = 2 * w.dk * w.dv * 4 + e * (2 * w.dk + 2 * w.dv + 1) + 4
+    return float(w.B * w.H * per_head)
+
+
+def bench_decode(args, w: W.Workload, rank: int, world: int, local: int):
+    """One recurrent step per sequence (gdn_decode), the state updated in place."""
+    from linear_attention_recurrence_gated_gb300 import gdn as G
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU (no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    G.lib()
+    host = W.generate_decode(W.with_seed(w, w.seed + rank))
+    names = ("q", "k", "v", "g", "beta")
+    d = {n: host[n].to(dev) for n in names}
+    state = host["state"].to(dev)
+    o = torch.empty_like(d["v"])
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        G.gdn_decode(d["q"], d["k"], d["v"], d["g"], d["beta"], state, o=o, state_out=state,
+                     stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler()
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    barrier(world)
+    time.sleep(0.15)
+    clocks.stop()
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    per_launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    tokens = w.B  # one token per sequence per step
+    value = tokens * world * args.steps / (total_ms / 1e3)
+
+    # end to end: the step's token inputs from pinned host memory, o back; the
+    # state stays resident on the device between steps, as in a serving loop
+    pinned = {n: host[n].pin_memory() for n in names}
+    o_host = torch.empty(host["v"].shape, dtype=host["v"].dtype).pin_memory()
+    h2d = sum(pinned[n].numel() * pinned[n].element_size() for n in names)
+    d2h = o_host.numel() * o_host.element_size()
+    e2e_steps = max(1, min(args.steps, 50))
+
+    def e2e_step():
+        for n in names:
+            d[n].copy_(pinned[n], non_blocking=True)
+        step()
+        o_host.copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    barrier(world)
+    if rank != 0:
+        return 0
+
+    hbm_gbs, _, peak_src = measured_peaks()
+    alg_bytes = decode_bytes(w)
+    achieved = alg_bytes / (per_launch_ms / 1e3) / 1e9
+    # CPU baseline: the oracle on a sample of the sequences, as one-token steps
+    import oracle
+    oracle.build()
+    rows = slice(0, 128)
+    t_c = time.perf_counter()
+    oracle.forward(host["q"][rows, None], host["k"][rows, None], host["v"][rows, None],
+                   host["g"][rows, None], host["beta"][rows, None], host["state"][rows], None,
+                   threads=oracle.default_threads())
+    cpu_secs = time.perf_counter() - t_c
+    clk = clocks.summary(wall0, wall1, _bus_id(local))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": 1, "H": w.H, "dk": w.dk, "dv": w.dv,
+                   "storage": w.dtype, "kernel": "decode",
+                   "l2": f"the {w.B * w.H * w.dk * w.dv * 4 / 1e6:.0f} MB state (> 129 MB L2) "
+                         "is read and written every step",
+                   "parallelism": f"replicas x{world}"},
+        "head_tokens_per_s": value * w.H,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": achieved / hbm_gbs, "traffic": committed_traffic("decode", w.name),
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": per_launch_ms},
+        "cpu_baseline": {"value": 128 / cpu_secs, "unit": UNIT, "cores": oracle.default_threads(),
+                         "kind": "oracle",
+                         "sample": f"128 of the {w.B} sequences x {w.H} heads, one step, "
+                                   f"{cpu_secs:.2f} s"},
+        "e2e": {"value": tokens * world * e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def launches_per_step(kernel_name: str) -> int:
     return 1
 
@@ -445,13 +572,18 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="hymo_bf16", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default="hymo_bf16",
+                    choices=sorted(W.WORKLOADS) + sorted(W.DECODE_WORKLOADS))
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_setup()
-    w = W.WORKLOADS[args.workload]
     try:
+        if args.workload in W.DECODE_WORKLOADS:
+            if args.impl == "reference":
+                raise SystemExit("the reference arm times the prefill workloads only")
+            return bench_decode(args, W.DECODE_WORKLOADS[args.workload], rank, world, local)
+        w = W.WORKLOADS[args.workload]
         if args.impl == "reference":
             return bench_reference(args, w, rank, world)
         return bench_ours(args, w, rank, world, local)

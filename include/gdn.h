@@ -176,6 +176,39 @@ gdn_status gdn_fwd_static_scratch(const void *q, const void *k, const void *v, c
                                   int32_t chunk_size, gdn_dtype dtype, uint32_t flags,
                                   int32_t check, void *stream);
 
+/*
+ * gdn_decode -- one recurrent step of the operation above per (sequence,
+ * head): the token-by-token form used for incremental inference, with the
+ * state carried between calls ("Model Architecture Walkthrough", section
+ * 5.5, step 5, is the per-token recurrence; section 5.2.1 the decay).  Per
+ * (n, h), with H = S^T the fp32 state:
+ *
+ *     u = beta (v - alpha H^T k),   H' = alpha H + k u^T,   o = H'^T q
+ *
+ * which is gdn_fwd on one token with initial_state H and final_state H', up
+ * to rounding.
+ *
+ *   q, k       [num_seqs, num_heads, head_dim_k]                 dtype    device
+ *   v          [num_seqs, num_heads, head_dim_v]                 dtype    device
+ *   g          [num_seqs, num_heads]                             float32  device
+ *   beta       [num_seqs, num_heads]                             dtype    device
+ *   state_in   [num_seqs, num_heads, head_dim_k, head_dim_v]     float32  device, or NULL (= zeros)
+ *   state_out  [num_seqs, num_heads, head_dim_k, head_dim_v]     float32  device (written)
+ *   o          [num_seqs, num_heads, head_dim_v]                 dtype    device (written)
+ *
+ * flags: GDN_QK_L2NORM only.  Sizes as gdn_fwd (head_dim_k in {32, 64, 128},
+ * head_dim_v a multiple of 32 in [32, 256], num_seqs and num_heads <= 65535).
+ * state_out may be the same buffer as state_in (updated in place); otherwise
+ * outputs must not overlap any input.  No workspace: the step has no
+ * device-detected error.  Returns GDN_OK once enqueued, or an error code with
+ * nothing enqueued.  The pages have no decode entry point; their model
+ * carries the state token by token in the same recurrence.
+ */
+gdn_status gdn_decode(const void *q, const void *k, const void *v, const float *g,
+                      const void *beta, const float *state_in, float *state_out, void *o,
+                      int32_t num_seqs, int32_t num_heads, int32_t head_dim_k,
+                      int32_t head_dim_v, gdn_dtype dtype, uint32_t flags, void *stream);
+
 /* Synchronise `stream`, read the status word in `workspace`, clear it, and
  * return it (GDN_OK if no kernel recorded an error since the last check).
  * Also returns GDN_ERR_CUDA if the stream synchronisation itself failed. */

@@ -28,7 +28,8 @@ CHUNK_SIZE = 64
 
 # Every symbol include/gdn.h declares.
 EXPORTED = ("gdn_fwd_workspace_size", "gdn_workspace_init", "gdn_fwd", "gdn_check",
-            "gdn_status_string", "gdn_fwd_kernel_name", "gdn_fwd_static_scratch")
+            "gdn_status_string", "gdn_fwd_kernel_name", "gdn_fwd_static_scratch",
+            "gdn_decode")
 
 _lib = None
 _lock = threading.Lock()
@@ -69,6 +70,9 @@ def lib() -> ctypes.CDLL:
             L.gdn_fwd_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                  i32, i32, i32, i32, i32, i32, i32,
                                                  ctypes.c_int, u32, i32, vp]
+            L.gdn_decode.restype = ctypes.c_int
+            L.gdn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp,
+                                     i32, i32, i32, i32, ctypes.c_int, u32, vp]
             _lib = L
     return _lib
 
@@ -204,3 +208,44 @@ def gdn_fwd_static_scratch(q, k, v, g, beta, initial_state, cu_seqlens, o, final
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens),
         _ptr(o), _ptr(final_state), B, T, H, dk, dv, N, CHUNK_SIZE, _dtype_code(q.dtype),
         flags, 1 if check else 0, _stream_handle(stream)))
+
+
+def gdn_decode(q, k, v, g, beta, state=None, *, o=None, state_out=None, qk_l2norm=False,
+               stream=None):
+    """One recurrent step per (sequence, head) through the C ABI.
+
+    q, k ``[N, H, dk]``; v ``[N, H, dv]``; g ``[N, H]`` fp32; beta ``[N, H]``;
+    q/k/v/beta/o in one storage dtype (float32 or bfloat16).  ``state``
+    ``[N, H, dk, dv]`` fp32 or None (zeros).  ``state_out`` may be given
+    (``state_out=state`` updates the state in place); otherwise a new tensor is
+    returned.  Returns ``(o, state_out)``.
+    """
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    for t in [q, k, v, g, beta] + [t for t in (state, o, state_out) if t is not None]:
+        if not t.is_cuda:
+            raise ValueError("gdn_decode: every tensor must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("gdn_decode: every tensor must be contiguous")
+    dcode = _dtype_code(q.dtype)
+    if k.dtype != q.dtype or v.dtype != q.dtype or beta.dtype != q.dtype:
+        raise TypeError("gdn_decode: q, k, v and beta must share one storage dtype")
+    if g.dtype != torch.float32:
+        raise TypeError("gdn_decode: g must be float32")
+    if k.shape != q.shape or v.shape[:2] != (N, H) or g.shape != (N, H) or beta.shape != (N, H):
+        raise ValueError("gdn_decode: shape mismatch among q, k, v, g, beta")
+    for name, t in (("state", state), ("state_out", state_out)):
+        if t is not None and (t.dtype != torch.float32 or t.shape != (N, H, dk, dv)):
+            raise ValueError(f"gdn_decode: {name} must be float32 [N, H, dk, dv]")
+    if o is None:
+        o = torch.empty_like(v)
+    elif o.shape != v.shape or o.dtype != v.dtype:
+        raise ValueError("gdn_decode: o must match v in shape and dtype")
+    if state_out is None:
+        state_out = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    st = lib().gdn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+                          _ptr(state_out), _ptr(o), N, H, dk, dv, dcode,
+                          GDN_QK_L2NORM if qk_l2norm else 0, _stream_handle(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_decode")
+    return o, state_out

@@ -67,6 +67,28 @@ WORKLOADS = {
 }
 
 
+# One recurrent step per sequence (the decode entry point): B sequences of one
+# token, with a running state.  1024 HyMo-shaped heads-by-sequences give a
+# 256 MB state, larger than the 129 MB L2, so a timed step streams it from HBM.
+DECODE_WORKLOADS = {
+    "decode_hymo_bf16": Workload("decode_hymo_bf16", B=1024, T=1, H=16, dk=64, dv=64,
+                                 dtype="bf16", gate_scale=1.0, init_state=True,
+                                 notes="1024 sequences x 16 heads, one step each"),
+}
+
+
+def generate_decode(w: Workload):
+    """Inputs of one decode step: the draws of ``generate`` for ``w`` (which must
+    have T == 1) with the token axis removed: q, k ``[N, H, dk]``, v ``[N, H, dv]``,
+    g, beta ``[N, H]``, state ``[N, H, dk, dv]`` fp32 or None."""
+    if w.T != 1 or w.varlen:
+        raise ValueError("a decode workload has B sequences of exactly one token")
+    d = generate(w)
+    return {"q": d["q"][:, 0].contiguous(), "k": d["k"][:, 0].contiguous(),
+            "v": d["v"][:, 0].contiguous(), "g": d["g"][:, 0].contiguous(),
+            "beta": d["beta"][:, 0].contiguous(), "state": d["initial_state"], "N": w.B}
+
+
 def custom(name="custom", **kw) -> Workload:
     """A workload with explicit fields (edge-case tests)."""
     return Workload(name=name, **kw)

@@ -105,3 +105,30 @@ def test_workspace_init_rejects_small(L):
 
 def test_check_rejects_null_workspace(L):
     assert L.gdn_check(None, ctypes.c_void_p(0)) == 3
+
+
+def call_decode(L, **over):
+    N, H, dk, dv = 4, 3, 64, 64
+    a = dict(q=BASE, k=BASE + (1 << 30), v=BASE + (2 << 30), g=BASE + (3 << 30),
+             beta=BASE + (4 << 30), s_in=BASE + (6 << 30), s_out=BASE + (6 << 30),
+             o=BASE + (5 << 30), N=N, H=H, dk=dk, dv=dv, dtype=G.GDN_BF16, flags=0)
+    a.update(over)
+    vp = ctypes.c_void_p
+    return L.gdn_decode(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]),
+                        vp(a["s_in"]), vp(a["s_out"]), vp(a["o"]), a["N"], a["H"], a["dk"],
+                        a["dv"], a["dtype"], a["flags"], vp(0))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(dk=48), 2), (dict(dk=256), 2), (dict(dv=48), 2), (dict(dv=288), 2),
+    (dict(dtype=7), 1), (dict(flags=G.GDN_FORCE_SIMT), 1), (dict(flags=1 << 9), 1),
+    (dict(q=None), 1), (dict(o=None), 1), (dict(s_out=None), 1), (dict(g=None), 1),
+    (dict(q=BASE + 8), 1), (dict(s_out=BASE + (6 << 30) + 4, s_in=None), 1),
+    (dict(N=0), 1), (dict(H=0), 1), (dict(N=70000), 2),
+    (dict(o=BASE), 1),                                      # o aliases q
+    (dict(s_out=BASE + (2 << 30)), 1),                      # state_out aliases v
+    (dict(s_in=BASE + (6 << 30) + 16), 1),                  # state in/out partial overlap
+    (dict(o=BASE + (6 << 30) + 64), 1),                     # o inside the state
+])
+def test_decode_host_validation_rejects_before_launch(L, over, code):
+    assert call_decode(L, **over) == code
