@@ -15,6 +15,10 @@ Contents
                  Architecture Walkthrough" section 5.5, Step 5.
 ``chunked``      an independent fp64 numpy statement of the chunked (WY/UT)
                  form, used only to pin the sequential oracle against it.
+``diag``         the HyMo pages' own recurrence, per-state-row decay
+                 exp(g_t A) with A = -exp(A_log), write key b, read key c
+                 ("Model Architecture Walkthrough" section 5.2.1), token by
+                 token in fp64 numpy.
 
 Parity status of each function is recorded in its docstring; every function
 here is pinned by a CPU test in ``tests/test_oracle_pins.py``.

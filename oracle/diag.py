@@ -1,0 +1,55 @@
+"""Oracle for the HyMo pages' own GDN recurrence -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/`` and the CPU-baseline leg of ``bench.py`` may use this module;
+the product path never imports it, and it imports nothing from the product.
+
+The recurrence, per (batch row, head), token by token in fp64:
+
+    h_t = exp(g_t * A) (.) h_{t-1} + b_t (x) v_t        h_t in R^{S x D}
+    o_t = c_t^T h_t                                      o_t in R^D
+
+with A = -exp(A_log[h]) in R^S, one decay rate per state row, and g_t a
+positive per-head scalar gate ("Model Architecture Walkthrough", section
+5.2.1, the recurrence and its symbol list; "Optimization Quartet", Triton GDN
+kernel section 3.2, the shapes v, b, c, g, A_log).  ``exp(g_t * A) (.)``
+scales row s of the state by exp(g_t A_s); ``b_t (x) v_t`` is the outer
+product.  The read follows the write, as the two lines are written.  There is
+no beta and no erase term: this is the pages' form, not the gated delta rule
+of the main path.
+
+Parity status: pinned by ``tests/test_oracle_diag_pins.py`` against the
+unrolled form of the pages ("Model Architecture Walkthrough", section 5.3.1),
+the no-decay limit (linear attention with separate read and write keys, same
+page, section 5.2.3) and the scalar-decay mode of the C oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _f64(x):
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").double().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def forward(v, b, c, g, A_log, initial_state=None):
+    """v ``[B, T, H, D]``; b, c ``[B, T, H, S]``; g ``[B, T, H]``; A_log ``[H, S]``;
+    initial_state ``[B, H, S, D]`` or None (zeros).  Returns ``(o, final_state)``
+    as fp64 arrays: o ``[B, T, H, D]``, final_state ``[B, H, S, D]``."""
+    v = _f64(v); b = _f64(b); c = _f64(c); g = _f64(g); A_log = _f64(A_log)
+    B, T, H, D = v.shape
+    S = b.shape[-1]
+    if b.shape != (B, T, H, S) or c.shape != (B, T, H, S) or g.shape != (B, T, H) or \
+            A_log.shape != (H, S):
+        raise ValueError("diag oracle: shape mismatch")
+    A = -np.exp(A_log)                                   # [H, S], negative
+    h = np.zeros((B, H, S, D)) if initial_state is None else _f64(initial_state).copy()
+    if h.shape != (B, H, S, D):
+        raise ValueError("diag oracle: initial_state must be [B, H, S, D]")
+    o = np.zeros((B, T, H, D))
+    for t in range(T):
+        decay = np.exp(g[:, t, :, None] * A[None, :, :])   # [B, H, S]
+        h = decay[..., None] * h + b[:, t, :, :, None] * v[:, t, :, None, :]
+        o[:, t] = np.einsum("bhs,bhsd->bhd", c[:, t], h)
+    return o, h
