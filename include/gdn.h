@@ -209,6 +209,56 @@ gdn_status gdn_decode(const void *q, const void *k, const void *v, const float *
                       int32_t num_seqs, int32_t num_heads, int32_t head_dim_k,
                       int32_t head_dim_v, gdn_dtype dtype, uint32_t flags, void *stream);
 
+/*
+ * gdn_diag_fwd -- the HyMo pages' own recurrence: per-state-row (diagonal)
+ * decay, separate write and read keys, no erase term ("Model Architecture
+ * Walkthrough", section 5.2.1; "Optimization Quartet", Triton GDN kernel
+ * section 3.2, whose wrapper takes the same five tensors v, b, c, g, A_log).
+ * Per batch row n and head h, tokens t = 1..seq_len:
+ *
+ *     h_t = exp(g_t A) (.) h_{t-1} + b_t v_t^T,    o_t = h_t^T c_t,
+ *     A   = -exp(A_log[h])   (one negative rate per state row s)
+ *
+ * where h_t is d_state x head_dim (fp32) and exp(g_t A) (.) scales row s of
+ * the state by exp(g_t A_s).  Arithmetic is fp32 inside; o is stored in the
+ * caller's dtype.
+ *
+ *   v              [batch, seq_len, num_heads, head_dim]       dtype    device
+ *   b, c           [batch, seq_len, num_heads, d_state]        dtype    device
+ *   g              [batch, seq_len, num_heads]                 float32  device
+ *   A_log          [num_heads, d_state]                        float32  device
+ *   initial_state  [batch, num_heads, d_state, head_dim]       float32  device, or NULL (= zeros)
+ *   o              [batch, seq_len, num_heads, head_dim]       dtype    device (written)
+ *   final_state    [batch, num_heads, d_state, head_dim]       float32  device (written), or NULL
+ *
+ * Values: g_t is the positive gate (a sigmoid output on the pages) and is
+ * used as given; any real g_t and A_log are accepted, the decay factors are
+ * products of exp(g_t A_s) and never overflow for g_t >= 0.
+ *
+ * Supported sizes: d_state == 32 and head_dim == 32 (the pages' production
+ * shape); batch, num_heads, seq_len >= 1 with batch * num_heads *
+ * ceil(seq_len / 128) < 2^31.  flags must be 0.  Anything else returns
+ * GDN_ERR_UNSUPPORTED (or INVALID_ARG if malformed).
+ *
+ * Aliasing as gdn_fwd: o and final_state overlap no input; final_state may be
+ * initial_state.
+ *
+ * workspace: device, at least gdn_diag_workspace_size(...) bytes, zeroed once
+ * before its first use (gdn_workspace_init); it carries a launch counter from
+ * call to call, so a call that failed to complete (a CUDA error) requires a
+ * new gdn_workspace_init.  Calls sharing a workspace must be ordered (same
+ * stream).  Device-detected errors (GDN_ERR_TIMEOUT) are reported by
+ * gdn_check.  Returns GDN_OK once enqueued, or an error code with nothing
+ * enqueued.
+ */
+size_t gdn_diag_workspace_size(int32_t batch, int32_t seq_len, int32_t num_heads,
+                               int32_t d_state, int32_t head_dim);
+gdn_status gdn_diag_fwd(const void *v, const void *b, const void *c, const float *g,
+                        const float *A_log, const float *initial_state, void *o,
+                        float *final_state, int32_t batch, int32_t seq_len, int32_t num_heads,
+                        int32_t d_state, int32_t head_dim, gdn_dtype dtype, uint32_t flags,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
 /* Synchronise `stream`, read the status word in `workspace`, clear it, and
  * return it (GDN_OK if no kernel recorded an error since the last check).
  * Also returns GDN_ERR_CUDA if the stream synchronisation itself failed. */

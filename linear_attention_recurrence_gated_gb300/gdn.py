@@ -29,7 +29,7 @@ CHUNK_SIZE = 64
 # Every symbol include/gdn.h declares.
 EXPORTED = ("gdn_fwd_workspace_size", "gdn_workspace_init", "gdn_fwd", "gdn_check",
             "gdn_status_string", "gdn_fwd_kernel_name", "gdn_fwd_static_scratch",
-            "gdn_decode")
+            "gdn_decode", "gdn_diag_workspace_size", "gdn_diag_fwd")
 
 _lib = None
 _lock = threading.Lock()
@@ -73,6 +73,11 @@ def lib() -> ctypes.CDLL:
             L.gdn_decode.restype = ctypes.c_int
             L.gdn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp,
                                      i32, i32, i32, i32, ctypes.c_int, u32, vp]
+            L.gdn_diag_workspace_size.restype = sz
+            L.gdn_diag_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+            L.gdn_diag_fwd.restype = ctypes.c_int
+            L.gdn_diag_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp,
+                                       i32, i32, i32, i32, i32, ctypes.c_int, u32, vp, sz, vp]
             _lib = L
     return _lib
 
@@ -249,3 +254,65 @@ def gdn_decode(q, k, v, g, beta, state=None, *, o=None, state_out=None, qk_l2nor
     if st != GDN_OK:
         raise GdnError(st, "gdn_decode")
     return o, state_out
+
+
+def gdn_diag_workspace_size(batch: int, seq_len: int, num_heads: int, d_state: int,
+                            head_dim: int) -> int:
+    return int(lib().gdn_diag_workspace_size(batch, seq_len, num_heads, d_state, head_dim))
+
+
+def new_diag_workspace(batch, seq_len, num_heads, d_state, head_dim, device=None):
+    """A zeroed workspace of the size gdn_diag_fwd needs (the caller keeps it)."""
+    n = gdn_diag_workspace_size(batch, seq_len, num_heads, d_state, head_dim)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def gdn_diag_fwd(v, b, c, g, A_log, initial_state=None, *, o=None, final_state=None,
+                 output_final_state=True, workspace=None, stream=None, check=False):
+    """The pages' diagonal-decay recurrence through the C ABI.
+
+    v ``[B, T, H, D]``; b, c ``[B, T, H, S]`` (v, b, c and o in one storage
+    dtype, float32 or bfloat16); g ``[B, T, H]`` fp32; A_log ``[H, S]`` fp32;
+    initial_state ``[B, H, S, D]`` fp32 or None.  Returns ``(o, final_state)``
+    (``final_state`` None when ``output_final_state`` is False and none is given).
+    A workspace made by ``new_diag_workspace`` for the same sizes may be reused
+    across calls on one stream.
+    """
+    B, T, H, D = v.shape
+    S = b.shape[-1]
+    for t in [v, b, c, g, A_log] + [t for t in (initial_state, o, final_state) if t is not None]:
+        if not t.is_cuda:
+            raise ValueError("gdn_diag_fwd: every tensor must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("gdn_diag_fwd: every tensor must be contiguous")
+    dcode = _dtype_code(v.dtype)
+    if b.dtype != v.dtype or c.dtype != v.dtype:
+        raise TypeError("gdn_diag_fwd: v, b and c must share one storage dtype")
+    if g.dtype != torch.float32 or A_log.dtype != torch.float32:
+        raise TypeError("gdn_diag_fwd: g and A_log must be float32")
+    if b.shape != (B, T, H, S) or c.shape != (B, T, H, S) or g.shape != (B, T, H) or \
+            A_log.shape != (H, S):
+        raise ValueError("gdn_diag_fwd: shape mismatch among v, b, c, g, A_log")
+    for name, t in (("initial_state", initial_state), ("final_state", final_state)):
+        if t is not None and (t.dtype != torch.float32 or t.shape != (B, H, S, D)):
+            raise ValueError(f"gdn_diag_fwd: {name} must be float32 [B, H, S, D]")
+    if o is None:
+        o = torch.empty_like(v)
+    elif o.shape != v.shape or o.dtype != v.dtype:
+        raise ValueError("gdn_diag_fwd: o must match v in shape and dtype")
+    if final_state is None and output_final_state:
+        final_state = torch.empty((B, H, S, D), dtype=torch.float32, device=v.device)
+    if workspace is None:
+        workspace = new_diag_workspace(B, T, H, S, D, device=v.device)
+    st = lib().gdn_diag_fwd(_ptr(v), _ptr(b), _ptr(c), _ptr(g), _ptr(A_log),
+                            _ptr(initial_state), _ptr(o), _ptr(final_state), B, T, H, S, D,
+                            dcode, 0, _ptr(workspace),
+                            workspace.numel() * workspace.element_size(),
+                            _stream_handle(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_diag_fwd")
+    if check:
+        st = gdn_check(workspace, stream)
+        if st != GDN_OK:
+            raise GdnError(st, "gdn_diag_fwd (device)")
+    return o, final_state

@@ -154,3 +154,67 @@ def head_tokens(w: Workload, inputs=None) -> int:
     if w.varlen:
         raise ValueError("varlen head-token count needs the drawn inputs")
     return w.B * w.T * w.H
+
+
+# ---------------------------------------------------------------------------
+# The pages' own recurrence (diagonal decay exp(g_t A), write key b, read key c)
+# ---------------------------------------------------------------------------
+@dataclass(frozen=True)
+class DiagWorkload:
+    """Inputs of ``gdn_diag_fwd``.  ``a_log`` selects the decay rates:
+    "pages": A_log[h, s] = log(h + 1) for every s, the initialisation the pages
+    give ("Model Architecture Walkthrough", section 5.3.2: A = -1 ... -H);
+    "uniform": A_log[h, s] ~ U(-2, 2) independently (a different rate per row);
+    "slow": A_log[h, s] ~ U(-6, -3) (per-token factors near 1: long memory)."""
+    name: str
+    B: int
+    T: int
+    H: int
+    S: int = 32
+    D: int = 32
+    dtype: str = "bf16"
+    a_log: str = "pages"
+    init_state: bool = False
+    seed: int = 0
+    notes: str = field(default="", compare=False)
+
+
+DIAG_WORKLOADS = {
+    "hymo_diag_bf16": DiagWorkload("hymo_diag_bf16", B=4, T=4096, H=40, dtype="bf16",
+                                   a_log="pages",
+                                   notes="the pages' production GDN layer (B=4, T=4096, "
+                                         "H=40, S=D=32); the diagonal-decay benchmark"),
+    "diag_small_fp32": DiagWorkload("diag_small_fp32", B=2, T=300, H=3, dtype="fp32",
+                                    a_log="uniform", init_state=True,
+                                    notes="parity case: several CTAs and a ragged tail"),
+}
+
+
+def generate_diag(w: DiagWorkload):
+    """Draw the inputs of ``w`` on the host, in this order from one
+    ``default_rng(seed)`` stream: v ~ N(0, 1) ``[B, T, H, D]``; b, c ~ N(0, 1/S)
+    ``[B, T, H, S]``; g = sigmoid(z), z ~ N(0, 1) ``[B, T, H]`` fp32 (the pages'
+    g is a sigmoid output); A_log ``[H, S]`` fp32 per ``w.a_log``; initial
+    state ~ N(0, 0.1^2) ``[B, H, S, D]`` fp32 when ``w.init_state``.  v, b, c
+    are cast to the storage dtype (round to nearest even)."""
+    rng = np.random.default_rng(w.seed)
+    dt = _DTYPES[w.dtype]
+    B, T, H, S, D = w.B, w.T, w.H, w.S, w.D
+    v = torch.from_numpy(rng.standard_normal((B, T, H, D))).to(dt)
+    b = torch.from_numpy(rng.standard_normal((B, T, H, S)) / np.sqrt(S)).to(dt)
+    c = torch.from_numpy(rng.standard_normal((B, T, H, S)) / np.sqrt(S)).to(dt)
+    g = torch.from_numpy(_sigmoid(rng.standard_normal((B, T, H)))).to(torch.float32)
+    if w.a_log == "pages":
+        a = np.repeat(np.log(np.arange(1, H + 1, dtype=np.float64))[:, None], S, axis=1)
+    elif w.a_log == "uniform":
+        a = rng.uniform(-2.0, 2.0, (H, S))
+    elif w.a_log == "slow":
+        a = rng.uniform(-6.0, -3.0, (H, S))
+    else:
+        raise ValueError(f"unknown a_log recipe {w.a_log!r}")
+    A_log = torch.from_numpy(a).to(torch.float32)
+    h0 = None
+    if w.init_state:
+        h0 = torch.from_numpy(0.1 * rng.standard_normal((B, H, S, D))).to(torch.float32)
+    return {"v": v.contiguous(), "b": b.contiguous(), "c": c.contiguous(),
+            "g": g.contiguous(), "A_log": A_log.contiguous(), "initial_state": h0}

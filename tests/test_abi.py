@@ -132,3 +132,47 @@ def call_decode(L, **over):
 ])
 def test_decode_host_validation_rejects_before_launch(L, over, code):
     assert call_decode(L, **over) == code
+
+
+# ---- gdn_diag_fwd (the pages' diagonal-decay recurrence) ----
+def test_diag_workspace_size(L):
+    # 4 x 40 heads x 32 blocks of 128 tokens: a flag, an aggregate map and an end state each
+    n = G.gdn_diag_workspace_size(4, 4096, 40, 32, 32)
+    tasks = 4 * 40 * 32
+    assert n >= 256 + tasks * (4 + (32 * 32 + 32) * 4 + 32 * 32 * 4)
+    assert G.gdn_diag_workspace_size(1, 1, 1, 32, 32) > 256
+    assert G.gdn_diag_workspace_size(0, 1, 1, 32, 32) == 0
+    assert G.gdn_diag_workspace_size(1, 0, 1, 32, 32) == 0
+
+
+def call_diag(L, **over):
+    B, T, H, S, D = 2, 300, 3, 32, 32
+    ws_need = G.gdn_diag_workspace_size(B, T, H, S, D)
+    a = dict(v=BASE, b=BASE + (1 << 30), c=BASE + (2 << 30), g=BASE + (3 << 30),
+             A=BASE + (4 << 30), s0=None, o=BASE + (5 << 30), sN=BASE + (6 << 30),
+             B=B, T=T, H=H, S=S, D=D, dtype=G.GDN_BF16, flags=0, ws=BASE + (7 << 30),
+             ws_bytes=ws_need)
+    a.update(over)
+    vp = ctypes.c_void_p
+    return L.gdn_diag_fwd(vp(a["v"]), vp(a["b"]), vp(a["c"]), vp(a["g"]), vp(a["A"]),
+                          vp(a["s0"]), vp(a["o"]), vp(a["sN"]), a["B"], a["T"], a["H"], a["S"],
+                          a["D"], a["dtype"], a["flags"], vp(a["ws"]), a["ws_bytes"], vp(0))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(S=16), 2), (dict(D=64), 2), (dict(S=0), 1), (dict(D=-1), 1),
+    (dict(B=0), 1), (dict(T=0), 1), (dict(H=0), 1),
+    (dict(dtype=5), 1), (dict(flags=1), 1),
+    (dict(v=None), 1), (dict(b=None), 1), (dict(c=None), 1), (dict(g=None), 1),
+    (dict(A=None), 1), (dict(o=None), 1),
+    (dict(c=BASE + (2 << 30) + 4), 1), (dict(sN=BASE + (6 << 30) + 8), 1),
+    (dict(ws=None), 3), (dict(ws_bytes=256), 3), (dict(ws=BASE + (7 << 30) + 2), 1),
+    (dict(o=BASE + (1 << 30)), 1),                           # o aliases b
+    (dict(sN=BASE + (3 << 30)), 1),                          # final state aliases g
+    (dict(s0=BASE + (5 << 30) + 1024), 1),                   # initial state inside o
+    (dict(s0=BASE + (6 << 30) + 16), 1),                     # state in/out partial overlap
+    (dict(sN=BASE + (7 << 30) + 4096), 1),                   # final state inside the workspace
+    (dict(B=1 << 16, H=1 << 16), 2),                         # too many blocks
+])
+def test_diag_host_validation_rejects_before_launch(L, over, code):
+    assert call_diag(L, **over) == code
