@@ -189,6 +189,8 @@ KERNEL_SOURCES = {
     "simt_bf16": "gdn_fwd_simt.cu",
     "tc64_bf16": "gdn_fwd_tc64.cu",
     "tc128_bf16": "gdn_fwd_tc.cu",
+    "diag_bf16": "gdn_diag.cu",
+    "diag_fp32": "gdn_diag.cu",
 }
 
 
@@ -549,6 +551,182 @@ def bench_decode(args, w: W.Workload, rank: int, world: int, local: int):
     return 0
 
 
+def diag_bytes(w: W.DiagWorkload) -> float:
+    """HBM bytes of one gdn_diag_fwd call: v, b, c read and o written in the
+    storage dtype, g read as fp32, per (token, head); the fp32 final state
+    written (and the initial state read, when given) per (batch row, head)."""
+    e = 4 if w.dtype == "fp32" else 2
+    per_head_token = e * (2 * w.D + 2 * w.S) + 4
+    state = 4 * w.S * w.D * w.B * w.H * (2 if w.init_state else 1)
+    return float(w.B * w.T * w.H * per_head_token + state)
+
+
+def _diag_oracle_pass(host, b_rows=None):
+    import oracle.diag
+    sel = slice(None) if b_rows is None else b_rows
+    h0 = host["initial_state"]
+    t = time.perf_counter()
+    oracle.diag.forward(host["v"][sel], host["b"][sel], host["c"][sel], host["g"][sel],
+                        host["A_log"], None if h0 is None else h0[sel])
+    return time.perf_counter() - t
+
+
+def bench_diag_reference(args, w: W.DiagWorkload, rank: int, world: int):
+    """The fp64 oracle of the diagonal-decay recurrence on the host, one batch
+    row of the workload per step."""
+    if rank != 0:
+        return 0
+    host = W.generate_diag(w)
+    for i in range(args.warmup):
+        _diag_oracle_pass(host, slice(i % w.B, i % w.B + 1))
+    total = sum(_diag_oracle_pass(host, slice(i % w.B, i % w.B + 1)) for i in range(args.steps))
+    value = w.T * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "S": w.S, "D": w.D,
+                   "storage": w.dtype, "step": "one batch row (T tokens x H heads) per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"one batch row of {w.name} per step ({w.T} tokens x "
+                                   f"{w.H} heads), {args.steps} steps"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_diag(args, w: W.DiagWorkload, rank: int, world: int, local: int):
+    """The pages' diagonal-decay recurrence (gdn_diag_fwd), one call per step."""
+    from linear_attention_recurrence_gated_gb300 import gdn as G
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU (no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    G.lib()
+    from dataclasses import replace
+    host = W.generate_diag(replace(w, seed=w.seed + rank))
+    names = ("v", "b", "c", "g")
+    sets = []
+    for _ in range(2):  # two resident input sets, alternated between steps
+        d = {n: host[n].to(dev) for n in names}
+        d["A_log"] = host["A_log"].to(dev)
+        d["initial_state"] = None if host["initial_state"] is None else host["initial_state"].to(dev)
+        d["o"] = torch.empty_like(d["v"])
+        d["final_state"] = torch.empty((w.B, w.H, w.S, w.D), dtype=torch.float32, device=dev)
+        sets.append(d)
+    ws = G.new_diag_workspace(w.B, w.T, w.H, w.S, w.D, device=dev)
+    kname = "diag_" + w.dtype
+    stream = torch.cuda.current_stream(dev)
+
+    def call(d):
+        G.gdn_diag_fwd(d["v"], d["b"], d["c"], d["g"], d["A_log"], d["initial_state"],
+                       o=d["o"], final_state=d["final_state"], workspace=ws, stream=stream)
+
+    for i in range(args.warmup):
+        call(sets[i & 1])
+    torch.cuda.synchronize(dev)
+    st = G.gdn_check(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {G.status_string(st)}")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler()
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        call(sets[i & 1])
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    barrier(world)
+    time.sleep(0.15)
+    clocks.stop()
+    st = G.gdn_check(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {G.status_string(st)}")
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    per_launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    tokens = w.B * w.T
+    value = tokens * world * args.steps / (total_ms / 1e3)
+
+    # end to end: pinned host inputs -> device -> gdn_diag_fwd -> o and final state back
+    pinned = {n: host[n].pin_memory() for n in names}
+    o_host = torch.empty(host["v"].shape, dtype=host["v"].dtype).pin_memory()
+    s_host = torch.empty((w.B, w.H, w.S, w.D), dtype=torch.float32).pin_memory()
+    h2d = sum(pinned[n].numel() * pinned[n].element_size() for n in names)
+    d2h = o_host.numel() * o_host.element_size() + s_host.numel() * 4
+    e2e_steps = max(1, min(args.steps, 50))
+    d = sets[0]
+
+    def e2e_step():
+        for n in names:
+            d[n].copy_(pinned[n], non_blocking=True)
+        call(d)
+        o_host.copy_(d["o"], non_blocking=True)
+        s_host.copy_(d["final_state"], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    barrier(world)
+    st = G.gdn_check(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status after e2e steps: {G.status_string(st)}")
+    if rank != 0:
+        return 0
+
+    hbm_gbs, _, peak_src = measured_peaks()
+    alg_bytes = diag_bytes(w)
+    achieved = alg_bytes / (per_launch_ms / 1e3) / 1e9
+    cpu_secs = _diag_oracle_pass(host)
+    clk = clocks.summary(wall0, wall1, _bus_id(local))
+    in_mb = sum(sets[0][n].numel() * sets[0][n].element_size() for n in names) / 1e6
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "S": w.S, "D": w.D,
+                   "storage": w.dtype, "a_log": w.a_log, "kernel": kname,
+                   "l2": f"two resident input sets of {in_mb:.0f} MB each alternate between "
+                         "steps (257 MB > 129 MB L2)",
+                   "parallelism": f"replicas x{world}"},
+        "head_tokens_per_s": value * w.H,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": achieved / hbm_gbs, "traffic": committed_traffic(kname, w.name),
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": per_launch_ms},
+        "cpu_baseline": {"value": tokens / cpu_secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"the whole {w.name} workload ({tokens} tokens x {w.H} "
+                                   f"heads), one pass of the numpy oracle, {cpu_secs:.1f} s"},
+        "e2e": {"value": tokens * world * e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def launches_per_step(kernel_name: str) -> int:
     return 1
 
@@ -573,12 +751,18 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="hymo_bf16",
-                    choices=sorted(W.WORKLOADS) + sorted(W.DECODE_WORKLOADS))
+                    choices=sorted(W.WORKLOADS) + sorted(W.DECODE_WORKLOADS) +
+                    sorted(W.DIAG_WORKLOADS))
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_setup()
     try:
+        if args.workload in W.DIAG_WORKLOADS:
+            dw = W.DIAG_WORKLOADS[args.workload]
+            if args.impl == "reference":
+                return bench_diag_reference(args, dw, rank, world)
+            return bench_diag(args, dw, rank, world, local)
         if args.workload in W.DECODE_WORKLOADS:
             if args.impl == "reference":
                 raise SystemExit("the reference arm times the prefill workloads only")

@@ -58,6 +58,20 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr uint32_t kAgg = 1, kIncl = 2;   // flag states (low 2 bits)
 
+#ifdef GDN_DIAG_PROBE
+// Phase-timing build only: globaltimer stamps of thread 0, [ticket][phase].
+static __device__ unsigned long long g_diag_probe[8192 * 12];
+#define GDN_DPROBE(k)                                                   \
+  do {                                                                  \
+    if (threadIdx.x == 0 && probe_id < 8192u)                           \
+      ::gdn::diag::g_diag_probe[probe_id * 12u + (k)] = globaltimer_ns(); \
+  } while (0)
+#else
+#define GDN_DPROBE(k) \
+  do {                \
+  } while (0)
+#endif
+
 // Workspace: [0, 256) status word (first 16 bytes) and counters at byte 64;
 // then one flag per (head, block), one aggregate map and one end state.
 struct Counters {
@@ -82,6 +96,7 @@ inline Workspace workspace_layout(int64_t tasks) {
 struct DiagParams {
   const float *g, *A_log, *h0;
   float *hN;
+  void *o;
   DeviceStatus *status;
   Counters *ctr;
   uint32_t *flags;
@@ -119,70 +134,29 @@ struct Lay {
 __device__ __forceinline__ uint32_t sw64(uint32_t base, int row, int byte) {
   return base + row * 64 + ((((byte >> 4) ^ (row >> 1)) & 3) << 4) + (byte & 15);
 }
-// Rows of 128 bytes (32 fp32) with the 128-byte swizzle (granule XOR row mod 8).
-__device__ __forceinline__ uint32_t sw128(uint32_t base, int row, int byte) {
-  return base + row * 128 + ((((byte >> 4) ^ row) & 7) << 4) + (byte & 15);
-}
-
-__device__ __forceinline__ uint32_t lds32(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-  return v;
-}
-__device__ __forceinline__ float2 lds64f(uint32_t a) {
-  float2 v;
-  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
-  return v;
-}
-__device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
-  asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
-}
 __device__ __forceinline__ void sts32f(uint32_t a, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
 }
 
-// One token's pair of inputs (state rows 2sp, 2sp+1, or value columns) as held
-// by a prep lane.
-template <typename T> struct Pair;
-template <> struct Pair<__nv_bfloat16> {
-  uint32_t r;
-  __device__ __forceinline__ float x() const { return bf16_lo(r); }
-  __device__ __forceinline__ float y() const { return bf16_hi(r); }
-};
-template <> struct Pair<float> {
-  float2 r;
-  __device__ __forceinline__ float x() const { return r.x; }
-  __device__ __forceinline__ float y() const { return r.y; }
-};
-
-template <typename T>
-__device__ __forceinline__ Pair<T> load_pair(uint32_t sub, int row, int pair);
-template <>
-__device__ __forceinline__ Pair<__nv_bfloat16> load_pair<__nv_bfloat16>(uint32_t sub, int row,
-                                                                        int pair) {
-  return Pair<__nv_bfloat16>{lds32(sw64(sub, row, 4 * pair))};
-}
-template <>
-__device__ __forceinline__ Pair<float> load_pair<float>(uint32_t sub, int row, int pair) {
-  return Pair<float>{lds64f(sw128(sub, row, 8 * pair))};
-}
-
-// Store (x, y) as bf16 into a staged plane; with NP == 2 also the residual
-// (x - bf16(x), y - bf16(y)) into the lo plane one PLANE further.
+// (x, y) as bf16 at plane + off; with NP == 2 also the residual into the lo
+// plane one PLANE further.
 template <int NP>
-__device__ __forceinline__ void put(uint32_t plane, int row, int pair, float x, float y) {
-  const uint32_t a = sw64(plane, row, 4 * pair);
-  const uint32_t hi = pack_bf16(x, y);
-  sts32(a, hi);
-  if (NP == 2) sts32(a + kCT * 64, pack_bf16(x - bf16_lo(hi), y - bf16_hi(hi)));
+__device__ __forceinline__ void put2(unsigned char *plane, int off, float2 v) {
+  const uint32_t hi = pack_bf16(v.x, v.y);
+  *reinterpret_cast<uint32_t *>(plane + off) = hi;
+  if constexpr (NP == 2)
+    *reinterpret_cast<uint32_t *>(plane + off + kCT * 64) =
+        pack_bf16(v.x - bf16_lo(hi), v.y - bf16_hi(hi));
 }
-template <typename T, int NP>
-__device__ __forceinline__ void put_raw(uint32_t plane, int row, int pair, const Pair<T> &v) {
-  if constexpr (NP == 1 && sizeof(T) == 2) {
-    sts32(sw64(plane, row, 4 * pair), v.r);
-  } else {
-    put<NP>(plane, row, pair, v.x(), v.y());
-  }
+
+// Two fp32 products in one packed instruction.
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+      "mul.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
 }
 
 // ---- warp MMA on (possibly split) bf16 operands ----
@@ -241,26 +215,10 @@ __device__ __forceinline__ void load_vt(uint32_t (&a)[NP][4], uint32_t vplane, i
     ldsm_x4_t(sw64(vplane + p * kCT * 64, row, 2 * col), a[p][0], a[p][1], a[p][2], a[p][3]);
 }
 
-__device__ __forceinline__ bool spin_flag(const uint32_t *f, uint32_t tag, uint32_t &state) {
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0;; ++it) {
-    const uint32_t v = ld_acquire_gpu(f);
-    if ((v & ~3u) == tag && (v & 3u) != 0) {
-      state = v & 3u;
-      return true;
-    }
-    if ((it & 15u) == 15u) {
-      if (globaltimer_ns() - t0 > kWaitNs) return false;
-      __nanosleep(64);
-    }
-  }
-}
-
 template <typename T>
 __global__ void __launch_bounds__(kThreads, Lay<T>::MIN_BLOCKS)
 gdn_diag_kernel(const DiagParams p, const __grid_constant__ CUtensorMap tm_v,
-                const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c,
-                const __grid_constant__ CUtensorMap tm_o) {
+                const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c) {
   using L = Lay<T>;
   constexpr int NP = L::NP;
   extern __shared__ unsigned char smem_raw[];
@@ -274,43 +232,69 @@ gdn_diag_kernel(const DiagParams p, const __grid_constant__ CUtensorMap tm_v,
   const int heads_total = p.batch * p.num_heads;
   const int64_t tasks = (int64_t)heads_total * p.nblk;
 
+#ifdef GDN_DIAG_PROBE
+  uint32_t probe_id = 0xffffffffu;
+#endif
   if (tid == 0) {
     const uint32_t ep = *reinterpret_cast<volatile uint32_t *>(&p.ctr->epoch);
-    const uint32_t t = atomicAdd(&p.ctr->ticket, 1u);
-    misc[2] = t;
+    misc[2] = atomicAdd(&p.ctr->ticket, 1u);
     misc[3] = (ep & 0x3fffffffu) << 2;
     mbar_init(bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
-  const uint32_t ticket = misc[2], tag = misc[3];
-  const bool valid = (int64_t)ticket < tasks;
-  const int blk = valid ? (int)(ticket / (uint32_t)heads_total) : 0;
-  const int head = valid ? (int)(ticket % (uint32_t)heads_total) : 0;
+  const uint32_t tag = misc[3];
+  uint32_t ticket = misc[2];
+
+  // Inputs of block `t`: v, b, c tiles by TMA (one thread), and the gates of
+  // this warp's 16 tokens into lanes 0..15 (0 past the end: no decay).
+  auto issue_tiles = [&](uint32_t t) {
+    const int hdx = (int)(t % (uint32_t)heads_total);
+    const int blk_ = (int)(t / (uint32_t)heads_total);
+    const int b_ = hdx / p.num_heads, h_ = hdx % p.num_heads;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, 3 * L::TILE);
+    tma_load_4d(sbase + L::OFF_V, &tm_v, 0, h_, blk_ * kSC, b_, bar);
+    tma_load_4d(sbase + L::OFF_B, &tm_b, 0, h_, blk_ * kSC, b_, bar);
+    tma_load_4d(sbase + L::OFF_C, &tm_c, 0, h_, blk_ * kSC, b_, bar);
+  };
+  auto load_gate = [&](uint32_t t) {
+    float x = 0.f;
+    if ((int64_t)t < tasks && lane < kCT) {
+      const int hdx = (int)(t % (uint32_t)heads_total);
+      const int tok = (int)(t / (uint32_t)heads_total) * kSC + kCT * warp + lane;
+      const int b_ = hdx / p.num_heads, h_ = hdx % p.num_heads;
+      if (tok < p.seq_len) x = __ldg(p.g + ((int64_t)b_ * p.seq_len + tok) * p.num_heads + h_);
+    }
+    return x;
+  };
+  if (tid == 0 && (int64_t)ticket < tasks) issue_tiles(ticket);
+  float gtok = load_gate(ticket);
+  const int sp = lane & 15, hh = lane >> 4;
+  uint32_t phase = 0;
+
+  // Persistent loop: one 128-token block per iteration.  The next block's
+  // ticket and tiles are taken as soon as this block's tiles are consumed.
+  while ((int64_t)ticket < tasks) {
+#ifdef GDN_DIAG_PROBE
+  probe_id = ticket;
+#endif
+  GDN_DPROBE(0);
+  const bool valid = true;
+  const int blk = (int)(ticket / (uint32_t)heads_total);
+  const int head = (int)(ticket % (uint32_t)heads_total);
   const int bb = head / p.num_heads, hd = head % p.num_heads;
   const int t0 = blk * kSC;
   const int64_t task = (int64_t)head * p.nblk + blk;
-  if (!valid && tid == 0) report(p.status, GDN_ERR_DEVICE_CHECK, 0u, 0u, ticket);
-
-  if (tid == 0 && valid) {
-    mbar_arrive_expect_tx(bar, 3 * L::TILE);
-    tma_load_4d(sbase + L::OFF_V, &tm_v, 0, hd, t0, bb, bar);
-    tma_load_4d(sbase + L::OFF_B, &tm_b, 0, hd, t0, bb, bar);
-    tma_load_4d(sbase + L::OFF_C, &tm_c, 0, hd, t0, bb, bar);
-  }
-
-  // gate of token (16 warp + lane) for lanes 0..15 (0 past the end: no decay)
   const int tok_w = t0 + kCT * warp;
-  float gtok = 0.f;
-  if (lane < kCT && tok_w + lane < p.seq_len)
-    gtok = __ldg(p.g + ((int64_t)bb * p.seq_len + tok_w + lane) * p.num_heads + hd);
   // scaled decay rates A_s log2(e) of this lane's state rows 2sp, 2sp+1
-  const int sp = lane & 15, hh = lane >> 4;
   const float ah0 = -__expf(__ldg(p.A_log + hd * kS + 2 * sp)) * kLog2e;
   const float ah1 = -__expf(__ldg(p.A_log + hd * kS + 2 * sp + 1)) * kLog2e;
+  __syncwarp();   // this warp's previous o tile is copied out of its exchange slot
 
-  if (valid && !mbar_wait_bounded(bar, 0, kWaitNs))
+  if (!mbar_wait_bounded(bar, phase, kWaitNs))
     report(p.status, GDN_ERR_TIMEOUT, (uint32_t)bb, (uint32_t)hd, 1u);
+  GDN_DPROBE(2);
 
   const uint32_t wbase = sbase + L::OFF_W + warp * L::WARP;
   const uint32_t xch = wbase, ctl = wbase + L::W_CT, bht = wbase + L::W_BH;
@@ -325,95 +309,123 @@ gdn_diag_kernel(const DiagParams p, const __grid_constant__ CUtensorMap tm_v,
   // =================== step 1: the chunk of this warp ===================
   // ---- prep: lane (sp, hh) owns state rows 2sp, 2sp+1 of tokens 8hh..8hh+7 ----
   {
-    Pair<T> cr[8], br[8];
-    float a0[8], a1[8];
+    // Byte offset of (row 8hh + u, pair sp) in a plane of 64-byte rows with the
+    // 64-byte swizzle is o64[(u >> 1) & 3] + 64 u; in a tile of 128-byte fp32
+    // rows with the 128-byte swizzle it is o128[u] + 128 u.
+    int o64[4];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int r = 8 * hh + u;
-      cr[u] = load_pair<T>(subc, r, sp);
-      br[u] = load_pair<T>(subb, r, sp);
-      const float gu = __shfl_sync(0xffffffffu, gtok, r);
-      a0[u] = exp2f(ah0 * gu);
-      a1[u] = exp2f(ah1 * gu);
-    }
-    if constexpr (L::SPLIT) {
+    for (int k = 0; k < 4; ++k) o64[k] = hh * 512 + ((((sp >> 2) ^ k) & 3) << 4) + (sp & 3) * 4;
+    unsigned char *const wp = sptr + (wbase - sbase);
+    unsigned char *const tb = sptr + L::OFF_B + warp * L::SUB;
+    unsigned char *const tcp = sptr + L::OFF_C + warp * L::SUB;
+    auto off = [&](int u) { return o64[(u >> 1) & 3] + 64 * u; };
+
+    float2 cf[8], bfv[8];
+    uint32_t braw[8];
+    if constexpr (!L::SPLIT) {
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int r = 8 * hh + u;
-        const Pair<T> vv = load_pair<T>(subv, r, sp);
-        put<2>(vplane, r, sp, vv.x(), vv.y());
-        put<2>(cdiag, r, sp, cr[u].x(), cr[u].y());
-        put<2>(bdiag, r, sp, br[u].x(), br[u].y());
+        const uint32_t rc = *reinterpret_cast<const uint32_t *>(tcp + off(u));
+        braw[u] = *reinterpret_cast<const uint32_t *>(tb + off(u));
+        cf[u] = make_float2(bf16_lo(rc), bf16_hi(rc));
+        bfv[u] = make_float2(bf16_lo(braw[u]), bf16_hi(braw[u]));
+      }
+    } else {
+      int o128[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) o128[u] = hh * 1024 + (((sp >> 1) ^ u) << 4) + (sp & 1) * 8;
+      unsigned char *const tv = sptr + L::OFF_V + warp * L::SUB;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int a = o128[u] + 128 * u;
+        cf[u] = *reinterpret_cast<const float2 *>(tcp + a);
+        bfv[u] = *reinterpret_cast<const float2 *>(tb + a);
+        const float2 vv = *reinterpret_cast<const float2 *>(tv + a);
+        put2<2>(wp + L::W_VS, off(u), vv);
+        put2<2>(wp + L::W_DG, off(u), cf[u]);
+        put2<2>(wp + L::W_DG + 2 * L::PLANE, off(u), bfv[u]);
+        braw[u] = 0u;
       }
     }
-    const uint32_t X0 = xch, X1 = xch + NP * L::PLANE, X2 = xch + 2 * NP * L::PLANE,
-                   X3 = xch + 3 * NP * L::PLANE;
+    // per-token decay factors alpha_u = 2^(A_s log2(e) g_u)
+    float2 al[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float gu = __shfl_sync(0xffffffffu, gtok, 8 * hh + u);
+      const float2 e = mul2(make_float2(ah0, ah1), make_float2(gu, gu));
+      al[u] = make_float2(ex2(e.x), ex2(e.y));
+    }
+    auto raw_b = [&](unsigned char *plane, int u) {
+      if constexpr (!L::SPLIT) *reinterpret_cast<uint32_t *>(plane + off(u)) = braw[u];
+      else put2<2>(plane, off(u), bfv[u]);
+    };
+    unsigned char *const X0 = wp, *const X1 = wp + NP * L::PLANE,
+                  *const X2 = wp + 2 * NP * L::PLANE, *const X3 = wp + 3 * NP * L::PLANE;
     // level 0: pairs (2m+1, 2m); upper (odd) rows c alpha, lower rows b
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int r = 8 * hh + u;
-      if (u & 1) put<NP>(X0, r, sp, cr[u].x() * a0[u], cr[u].y() * a1[u]);
-      else put_raw<T, NP>(X0, r, sp, br[u]);
+      if (u & 1) put2<NP>(X0, off(u), mul2(cf[u], al[u]));
+      else raw_b(X0, u);
     }
     // level 1: blocks {0,1 | 2,3} within each 4-block
-    {
-      const float p23x = a0[2] * a0[3], p23y = a1[2] * a1[3];
-      const float p67x = a0[6] * a0[7], p67y = a1[6] * a1[7];
-      put<NP>(X1, 8 * hh + 0, sp, br[0].x() * a0[1], br[0].y() * a1[1]);
-      put_raw<T, NP>(X1, 8 * hh + 1, sp, br[1]);
-      put<NP>(X1, 8 * hh + 2, sp, cr[2].x() * a0[2], cr[2].y() * a1[2]);
-      put<NP>(X1, 8 * hh + 3, sp, cr[3].x() * p23x, cr[3].y() * p23y);
-      put<NP>(X1, 8 * hh + 4, sp, br[4].x() * a0[5], br[4].y() * a1[5]);
-      put_raw<T, NP>(X1, 8 * hh + 5, sp, br[5]);
-      put<NP>(X1, 8 * hh + 6, sp, cr[6].x() * a0[6], cr[6].y() * a1[6]);
-      put<NP>(X1, 8 * hh + 7, sp, cr[7].x() * p67x, cr[7].y() * p67y);
-    }
+    const float2 p23 = mul2(al[2], al[3]), p67 = mul2(al[6], al[7]);
+    put2<NP>(X1, off(0), mul2(bfv[0], al[1]));
+    raw_b(X1, 1);
+    put2<NP>(X1, off(2), mul2(cf[2], al[2]));
+    put2<NP>(X1, off(3), mul2(cf[3], p23));
+    put2<NP>(X1, off(4), mul2(bfv[4], al[5]));
+    raw_b(X1, 5);
+    put2<NP>(X1, off(6), mul2(cf[6], al[6]));
+    put2<NP>(X1, off(7), mul2(cf[7], p67));
     // level 2: blocks {0..3 | 4..7}; up2 = prefix from 4, lo2 = suffix to 3
-    float up2x[8], up2y[8], lo2x[4], lo2y[4];
-    up2x[4] = a0[4]; up2y[4] = a1[4];
+    float2 up2[8], lo2[4];
+    up2[4] = al[4];
+    up2[5] = mul2(up2[4], al[5]);
+    up2[6] = mul2(up2[5], al[6]);
+    up2[7] = mul2(up2[6], al[7]);
+    lo2[2] = al[3];
+    lo2[1] = p23;
+    lo2[0] = mul2(p23, al[1]);
 #pragma unroll
-    for (int u = 5; u < 8; ++u) { up2x[u] = up2x[u - 1] * a0[u]; up2y[u] = up2y[u - 1] * a1[u]; }
-    lo2x[3] = 1.f; lo2y[3] = 1.f;
+    for (int u = 0; u < 3; ++u) put2<NP>(X2, off(u), mul2(bfv[u], lo2[u]));
+    raw_b(X2, 3);
 #pragma unroll
-    for (int u = 2; u >= 0; --u) { lo2x[u] = lo2x[u + 1] * a0[u + 1]; lo2y[u] = lo2y[u + 1] * a1[u + 1]; }
-#pragma unroll
-    for (int u = 0; u < 3; ++u) put<NP>(X2, 8 * hh + u, sp, br[u].x() * lo2x[u], br[u].y() * lo2y[u]);
-    put_raw<T, NP>(X2, 8 * hh + 3, sp, br[3]);
-#pragma unroll
-    for (int u = 4; u < 8; ++u) put<NP>(X2, 8 * hh + u, sp, cr[u].x() * up2x[u], cr[u].y() * up2y[u]);
+    for (int u = 4; u < 8; ++u) put2<NP>(X2, off(u), mul2(cf[u], up2[u]));
     // prefix (inclusive) and suffix (exclusive) products over this half
-    float prex[8], prey[8], sufx[8], sufy[8];
-    prex[0] = a0[0]; prey[0] = a1[0];
+    float2 pre[8], suf[8];
+    pre[0] = al[0];
 #pragma unroll
-    for (int u = 1; u < 4; ++u) { prex[u] = prex[u - 1] * a0[u]; prey[u] = prey[u - 1] * a1[u]; }
+    for (int u = 1; u < 4; ++u) pre[u] = mul2(pre[u - 1], al[u]);
 #pragma unroll
-    for (int u = 4; u < 8; ++u) { prex[u] = prex[3] * up2x[u]; prey[u] = prey[3] * up2y[u]; }
-    sufx[7] = 1.f; sufy[7] = 1.f;
+    for (int u = 4; u < 8; ++u) pre[u] = mul2(pre[3], up2[u]);
+    suf[7] = make_float2(1.f, 1.f);
+    suf[6] = al[7];
+    suf[5] = p67;
+    suf[4] = mul2(p67, al[5]);
+    suf[3] = up2[7];
 #pragma unroll
-    for (int u = 6; u >= 4; --u) { sufx[u] = sufx[u + 1] * a0[u + 1]; sufy[u] = sufy[u + 1] * a1[u + 1]; }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) { sufx[u] = lo2x[u] * up2x[7]; sufy[u] = lo2y[u] * up2y[7]; }
+    for (int u = 0; u < 3; ++u) suf[u] = mul2(lo2[u], up2[7]);
     // level 3: the two halves; upper half c prefix, lower half b suffix
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int r = 8 * hh + u;
-      if (hh) put<NP>(X3, r, sp, cr[u].x() * prex[u], cr[u].y() * prey[u]);
-      else put<NP>(X3, r, sp, br[u].x() * sufx[u], br[u].y() * sufy[u]);
+      const float2 x = hh ? cf[u] : bfv[u];
+      const float2 f = hh ? pre[u] : suf[u];
+      put2<NP>(X3, off(u), mul2(x, f));
     }
     // whole-chunk prefix E and suffix F: the other half's total product
-    const float ox = __shfl_xor_sync(0xffffffffu, prex[7], 16);
-    const float oy = __shfl_xor_sync(0xffffffffu, prey[7], 16);
-    const float ex = hh ? ox : 1.f, ey = hh ? oy : 1.f;   // E = ex * pre
-    const float fx = hh ? 1.f : ox, fy = hh ? 1.f : oy;   // F = fx * suf
+    const float2 ot = make_float2(__shfl_xor_sync(0xffffffffu, pre[7].x, 16),
+                                  __shfl_xor_sync(0xffffffffu, pre[7].y, 16));
+    const float2 one = make_float2(1.f, 1.f);
+    const float2 ex = hh ? ot : one;   // E = ex * pre
+    const float2 fx = hh ? one : ot;   // F = fx * suf
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int r = 8 * hh + u;
-      put<NP>(ctl, r, sp, cr[u].x() * (ex * prex[u]), cr[u].y() * (ey * prey[u]));
-      put<NP>(bht, r, sp, br[u].x() * (fx * sufx[u]), br[u].y() * (fy * sufy[u]));
+      put2<NP>(wp + L::W_CT, off(u), mul2(cf[u], mul2(ex, pre[u])));
+      put2<NP>(wp + L::W_BH, off(u), mul2(bfv[u], mul2(fx, suf[u])));
     }
     if (hh) {   // gamma = E of the last token
-      gam[warp * kS + 2 * sp] = ex * prex[7];
-      gam[warp * kS + 2 * sp + 1] = ey * prey[7];
+      const float2 gm = mul2(ex, pre[7]);
+      *reinterpret_cast<float2 *>(gam + warp * kS + 2 * sp) = gm;
     }
   }
   __syncwarp();
@@ -459,6 +471,9 @@ gdn_diag_kernel(const DiagParams p, const __grid_constant__ CUtensorMap tm_v,
   }
 
   // ---- dH^T (d x s) = V^T b^ ----
+  // (the V^T fragments are kept for the intra-chunk output: the tiles are
+  // refilled with the next block while this one finishes)
+  uint32_t va[2][NP][4];
   {
     float dH[2][4][4];
 #pragma unroll
@@ -467,7 +482,6 @@ gdn_diag_kernel(const DiagParams p, const __grid_constant__ CUtensorMap tm_v,
       for (int ns = 0; ns < 4; ++ns)
 #pragma unroll
         for (int q = 0; q < 4; ++q) dH[md][ns][q] = 0.f;
-    uint32_t va[2][NP][4];
     load_vt<NP>(va[0], vplane, 0, lane);
     load_vt<NP>(va[1], vplane, 1, lane);
     const int mi = lane >> 3;
@@ -500,7 +514,14 @@ gdn_diag_kernel(const DiagParams p, const __grid_constant__ CUtensorMap tm_v,
       }
   }
   __syncthreads();
+  // every read of this block's tiles is done: take the next block
+  if (warp == 2 && lane == 0) {
+    const uint32_t nt = atomicAdd(&p.ctr->ticket, 1u);
+    misc[6] = nt;
+    if ((int64_t)nt < tasks) issue_tiles(nt);
+  }
 
+  GDN_DPROBE(3);
   // =================== step 2: compose the chunk maps (all threads) ===================
   // Thread (warp rg, lane l) owns fragment block rg = 4 md + ns of every chunk:
   // state elements (d, s) = (16 md + g + 8 (q >> 1), 8 ns + 2 tq + (q & 1)).
@@ -530,10 +551,10 @@ gdn_diag_kernel(const DiagParams p, const __grid_constant__ CUtensorMap tm_v,
     float *ag = p.agg + task * kAggFloats;
     __stcg(reinterpret_cast<float4 *>(ag + fidx), agg);
     if (md == 0 && g == 0) __stcg(reinterpret_cast<float2 *>(ag + kS * kD + s0), G);
-    __threadfence();
   }
   __syncthreads();
   if (tid == 0 && valid && blk > 0) st_release_gpu(p.flags + task, tag | kAgg);
+  GDN_DPROBE(4);
 
   // ---- look-back: start state of this block ----
   auto init_at = [&]() {
@@ -547,58 +568,91 @@ gdn_diag_kernel(const DiagParams p, const __grid_constant__ CUtensorMap tm_v,
     }
     return h;
   };
-  float4 hs;
+  float4 hs = make_float4(0.f, 0.f, 0.f, 0.f);
   {
     float4 dF = make_float4(0.f, 0.f, 0.f, 0.f);
     float2 gF = make_float2(1.f, 1.f);
-    int j = blk - 1;
+    int j = blk - 1;   // nearest predecessor not yet composed
     int par = 0;
-    bool done = j < 0 || !valid;
-    hs = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (j < 0 && valid) hs = init_at();
+    bool done = !valid;
     while (!done) {
-      if (tid == 0) {
-        uint32_t st = 0;
-        if (!spin_flag(p.flags + head_task0 + j, tag, st)) {
-          report(p.status, GDN_ERR_TIMEOUT, (uint32_t)bb, (uint32_t)hd, 2u);
-          st = 3;
+      // warp 1 reads the flags of predecessors j, j-1, ..., j-31 at once and
+      // finds the nearest that published its end state (before the start of
+      // the sequence counts as one: the initial state); all nearer ones must
+      // have published their aggregate maps.  (Warp 0 may still be in the
+      // release store of this block's aggregate.)
+      if (warp == 1) {
+        const int jl = j - lane;
+        uint32_t st = jl < 0 ? kIncl : 0u;
+        int m = 33;
+        const uint64_t t_start = globaltimer_ns();
+        for (uint32_t it = 0;; ++it) {
+          if (st != kIncl) {
+            const uint32_t v = ld_acquire_gpu(p.flags + head_task0 + jl);
+            if ((v & ~3u) == tag && (v & 3u) != 0) st = v & 3u;
+          }
+          const uint32_t incl = __ballot_sync(0xffffffffu, st == kIncl);
+          const uint32_t ready = __ballot_sync(0xffffffffu, st != 0u);
+          const int first = incl ? __ffs(incl) - 1 : 32;
+          const uint32_t need = first == 32 ? 0xffffffffu : ((1u << first) - 1u);
+          if ((ready & need) == need) { m = first; break; }
+          if ((it & 15u) == 15u) {
+            if (globaltimer_ns() - t_start > kWaitNs) break;
+            __nanosleep(64);
+          }
         }
-        misc[4 + par] = st;
+        if (lane == 0) {
+          if (m > 32) report(p.status, GDN_ERR_TIMEOUT, (uint32_t)bb, (uint32_t)hd, 2u);
+          misc[4 + par] = (uint32_t)m;
+        }
       }
       __syncthreads();
-      const uint32_t st = misc[4 + par];
+      const int m = (int)misc[4 + par];
       par ^= 1;
-      if (st == kIncl) {
-        const float4 x = __ldcg(reinterpret_cast<const float4 *>(p.incl + (head_task0 + j) * kInclFloats + fidx));
+      if (m > 32) {   // timed out: carry on with what was composed so far
+        hs = dF;
+        break;
+      }
+      // compose the aggregate maps of j, j-1, ..., j-m+1 (nearest first)
+      for (int l = 0; l < m; l += 4) {
+        float4 x[4];
+        float2 gj[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (l + e < m) {
+            const float *ag = p.agg + (head_task0 + j - l - e) * kAggFloats;
+            x[e] = __ldcg(reinterpret_cast<const float4 *>(ag + fidx));
+            gj[e] = __ldcg(reinterpret_cast<const float2 *>(ag + kS * kD + s0));
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (l + e < m) {
+            dF.x = fmaf(gF.x, x[e].x, dF.x);
+            dF.y = fmaf(gF.y, x[e].y, dF.y);
+            dF.z = fmaf(gF.x, x[e].z, dF.z);
+            dF.w = fmaf(gF.y, x[e].w, dF.w);
+            gF.x *= gj[e].x;
+            gF.y *= gj[e].y;
+          }
+        }
+      }
+      if (m < 32) {
+        const int jm = j - m;
+        const float4 x = jm < 0 ? init_at()
+                                : __ldcg(reinterpret_cast<const float4 *>(
+                                      p.incl + (head_task0 + jm) * kInclFloats + fidx));
         hs.x = fmaf(gF.x, x.x, dF.x);
         hs.y = fmaf(gF.y, x.y, dF.y);
         hs.z = fmaf(gF.x, x.z, dF.z);
         hs.w = fmaf(gF.y, x.w, dF.w);
         done = true;
-      } else if (st == kAgg) {
-        const float *ag = p.agg + (head_task0 + j) * kAggFloats;
-        const float4 x = __ldcg(reinterpret_cast<const float4 *>(ag + fidx));
-        const float2 gj = __ldcg(reinterpret_cast<const float2 *>(ag + kS * kD + s0));
-        dF.x = fmaf(gF.x, x.x, dF.x);
-        dF.y = fmaf(gF.y, x.y, dF.y);
-        dF.z = fmaf(gF.x, x.z, dF.z);
-        dF.w = fmaf(gF.y, x.w, dF.w);
-        gF.x *= gj.x;
-        gF.y *= gj.y;
-        if (--j < 0) {
-          const float4 x0 = init_at();
-          hs.x = fmaf(gF.x, x0.x, dF.x);
-          hs.y = fmaf(gF.y, x0.y, dF.y);
-          hs.z = fmaf(gF.x, x0.z, dF.z);
-          hs.w = fmaf(gF.y, x0.w, dF.w);
-          done = true;
-        }
-      } else {   // timed out: carry on with what was composed so far
-        hs = dF;
-        done = true;
+      } else {
+        j -= 32;
       }
     }
   }
+  GDN_DPROBE(5);
   // ---- publish the end state of this block ----
   {
     float4 he;
@@ -608,7 +662,6 @@ gdn_diag_kernel(const DiagParams p, const __grid_constant__ CUtensorMap tm_v,
     he.w = fmaf(G.y, hs.w, agg.w);
     if (valid) {
       __stcg(reinterpret_cast<float4 *>(p.incl + task * kInclFloats + fidx), he);
-      __threadfence();
       if (blk == p.nblk - 1 && p.hN) {
         float *hn = p.hN + (int64_t)head * kS * kD;
         hn[s0 * kD + d0] = he.x;
@@ -620,6 +673,9 @@ gdn_diag_kernel(const DiagParams p, const __grid_constant__ CUtensorMap tm_v,
   }
   __syncthreads();
   if (tid == 0 && valid) st_release_gpu(p.flags + task, tag | kIncl);
+  const uint32_t next_ticket = misc[6];   // written by warp 2 before the barrier above
+  const float gnext = load_gate(next_ticket);
+  GDN_DPROBE(6);
 
   // ---- start state of every chunk, as bf16 A fragments of H^T ----
   uint32_t hf[kNW][NP][2];
@@ -658,6 +714,7 @@ gdn_diag_kernel(const DiagParams p, const __grid_constant__ CUtensorMap tm_v,
   }
   __syncthreads();
 
+  GDN_DPROBE(7);
   // =================== step 3: outputs of this warp's chunk ===================
   {
     float O[2][2][4];
@@ -696,15 +753,13 @@ gdn_diag_kernel(const DiagParams p, const __grid_constant__ CUtensorMap tm_v,
     // intra-chunk: O^T += V^T P^T
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
-      uint32_t va[NP][4];
-      load_vt<NP>(va, vplane, m, lane);
       uint32_t b0[NP], b1[NP];
 #pragma unroll
       for (int pp = 0; pp < NP; ++pp) { b0[pp] = pb0[pp][0]; b1[pp] = pb0[pp][1]; }
-      mma_np<NP>(O[m][0], va, b0, b1);
+      mma_np<NP>(O[m][0], va[m], b0, b1);
 #pragma unroll
       for (int pp = 0; pp < NP; ++pp) { b0[pp] = pb1[pp][0]; b1[pp] = pb1[pp][1]; }
-      mma_np<NP>(O[m][1], va, b0, b1);
+      mma_np<NP>(O[m][1], va[m], b0, b1);
     }
     __syncwarp();   // H fragments consumed: the exchange slot becomes the o tile
     // o tile [16 tokens][32 columns] in the storage type, row-major
@@ -726,25 +781,46 @@ gdn_diag_kernel(const DiagParams p, const __grid_constant__ CUtensorMap tm_v,
             sts32f(xch + i * 128 + d * 4, O[m][ni][q]);
           }
     }
-    fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0 && valid && tok_w < p.seq_len) {
-      tma_store_4d(&tm_o, 0, hd, tok_w, bb, xch);
-      bulk_commit();
-      bulk_wait_read<0>();
+    // coalesced 16-byte stores of the tile's rows that are inside the sequence
+    if (valid) {
+      constexpr int kChunks = kCT * kD * (int)sizeof(T) / 16;   // 16-byte pieces of the tile
+      constexpr int kPerRow = kD * (int)sizeof(T) / 16;
+      const unsigned char *src = sptr + (xch - sbase);
+#pragma unroll
+      for (int c = lane; c < kChunks; c += 32) {
+        const int i = c / kPerRow;
+        if (tok_w + i < p.seq_len) {
+          const int64_t row = ((int64_t)bb * p.seq_len + tok_w + i) * p.num_heads + hd;
+          *reinterpret_cast<uint4 *>(static_cast<unsigned char *>(p.o) + row * kD * sizeof(T) +
+                                     (c % kPerRow) * 16) =
+              *reinterpret_cast<const uint4 *>(src + c * 16);
+        }
+      }
     }
   }
 
-  // ---- launch bookkeeping: the last CTA resets the ticket and advances the epoch ----
-  __syncthreads();
+  GDN_DPROBE(9);
+#ifdef GDN_DIAG_PROBE
+  if (tid == 0 && probe_id < 8192u) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    g_diag_probe[probe_id * 12u + 10] = smid;
+  }
+#endif
+  ticket = next_ticket;
+  gtok = gnext;
+  phase ^= 1u;
+  }   // persistent loop
+
+  // ---- launch bookkeeping: the last CTA out resets the ticket and advances the epoch ----
   if (tid == 0) {
-    __threadfence();
     const uint32_t d = atomicAdd(&p.ctr->done, 1u);
-    if ((int64_t)d == tasks - 1) {
+    if (d == gridDim.x - 1) {
+      // every CTA of the launch has drawn its last ticket and read the epoch
       p.ctr->ticket = 0u;
       p.ctr->done = 0u;
       atomicAdd(&p.ctr->epoch, 1u);
-      __threadfence();
     }
   }
 }
@@ -752,8 +828,7 @@ gdn_diag_kernel(const DiagParams p, const __grid_constant__ CUtensorMap tm_v,
 namespace {
 
 // [B][T][H][32] tensor of the storage type viewed as 4-D (32, H, T, B).
-bool make_tmap4(CUtensorMap *m, const void *ptr, bool f32, int H, int T, int B, int box_t,
-                bool swizzle) {
+bool make_tmap4(CUtensorMap *m, const void *ptr, bool f32, int H, int T, int B, int box_t) {
   tc::EncodeTiledFn enc = tc::encode_fn();
   if (!enc) return false;
   const cuuint64_t e = f32 ? 4 : 2;
@@ -761,29 +836,42 @@ bool make_tmap4(CUtensorMap *m, const void *ptr, bool f32, int H, int T, int B, 
   const cuuint64_t strides[3] = {32 * e, 32 * e * H, 32 * e * H * (cuuint64_t)T};
   const cuuint32_t box[4] = {32, 1, (cuuint32_t)box_t, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUtensorMapSwizzle sw = !swizzle ? CU_TENSOR_MAP_SWIZZLE_NONE
-                                         : (f32 ? CU_TENSOR_MAP_SWIZZLE_128B
-                                                : CU_TENSOR_MAP_SWIZZLE_64B);
+  const CUtensorMapSwizzle sw = f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
              const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <typename T>
-cudaError_t launch_t(const DiagParams &p, const void *v, const void *b, const void *c, void *o,
+cudaError_t launch_t(const DiagParams &p, const void *v, const void *b, const void *c,
                      int64_t tasks, cudaStream_t stream) {
   using L = Lay<T>;
   const bool f32 = sizeof(T) == 4;
-  CUtensorMap tv, tb, tc_, to;
-  if (!make_tmap4(&tv, v, f32, p.num_heads, p.seq_len, p.batch, kSC, true) ||
-      !make_tmap4(&tb, b, f32, p.num_heads, p.seq_len, p.batch, kSC, true) ||
-      !make_tmap4(&tc_, c, f32, p.num_heads, p.seq_len, p.batch, kSC, true) ||
-      !make_tmap4(&to, o, f32, p.num_heads, p.seq_len, p.batch, kCT, false))
+  CUtensorMap tv, tb, tc_;
+  if (!make_tmap4(&tv, v, f32, p.num_heads, p.seq_len, p.batch, kSC) ||
+      !make_tmap4(&tb, b, f32, p.num_heads, p.seq_len, p.batch, kSC) ||
+      !make_tmap4(&tc_, c, f32, p.num_heads, p.seq_len, p.batch, kSC))
     return cudaErrorInvalidValue;
-  cudaError_t err = cudaFuncSetAttribute(gdn_diag_kernel<T>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+  // persistent CTAs: as many as fit on the device at once (cached per device)
+  static int resident[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  gdn_diag_kernel<T><<<(unsigned)tasks, kThreads, L::ALLOC, stream>>>(p, tv, tb, tc_, to);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (resident[dev] == 0) {
+    err = cudaFuncSetAttribute(gdn_diag_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               L::ALLOC);
+    if (err != cudaSuccess) return err;
+    int per_sm = 0, sms = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gdn_diag_kernel<T>, kThreads,
+                                                        L::ALLOC);
+    if (err != cudaSuccess) return err;
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    resident[dev] = per_sm > 0 && sms > 0 ? per_sm * sms : 1;
+  }
+  const int64_t grid = tasks < resident[dev] ? tasks : resident[dev];
+  gdn_diag_kernel<T><<<(unsigned)grid, kThreads, L::ALLOC, stream>>>(p, tv, tb, tc_);
   return cudaGetLastError();
 }
 
@@ -797,6 +885,12 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 }  // namespace
 }  // namespace diag
 }  // namespace gdn
+
+#ifdef GDN_DIAG_PROBE
+extern "C" int gdn_diag_probe_read(unsigned long long *host) {
+  return (int)cudaMemcpyFromSymbol(host, gdn::diag::g_diag_probe, sizeof(gdn::diag::g_diag_probe));
+}
+#endif
 
 extern "C" size_t gdn_diag_workspace_size(int32_t batch, int32_t seq_len, int32_t num_heads,
                                           int32_t d_state, int32_t head_dim) {
@@ -852,7 +946,7 @@ extern "C" gdn_status gdn_diag_fwd(const void *v, const void *b, const void *c, 
 
   unsigned char *ws = static_cast<unsigned char *>(workspace);
   DiagParams p;
-  p.g = g; p.A_log = A_log; p.h0 = initial_state; p.hN = final_state;
+  p.g = g; p.A_log = A_log; p.h0 = initial_state; p.hN = final_state; p.o = o;
   p.status = reinterpret_cast<DeviceStatus *>(ws);
   p.ctr = reinterpret_cast<Counters *>(ws + kCountersOff);
   p.flags = reinterpret_cast<uint32_t *>(ws + wl.flags);
@@ -860,7 +954,7 @@ extern "C" gdn_status gdn_diag_fwd(const void *v, const void *b, const void *c, 
   p.incl = reinterpret_cast<float *>(ws + wl.incl);
   p.batch = batch; p.seq_len = seq_len; p.num_heads = num_heads; p.nblk = (int32_t)nblk;
   const cudaError_t err =
-      dtype == GDN_F32 ? launch_t<float>(p, v, b, c, o, tasks, (cudaStream_t)stream)
-                       : launch_t<__nv_bfloat16>(p, v, b, c, o, tasks, (cudaStream_t)stream);
+      dtype == GDN_F32 ? launch_t<float>(p, v, b, c, tasks, (cudaStream_t)stream)
+                       : launch_t<__nv_bfloat16>(p, v, b, c, tasks, (cudaStream_t)stream);
   return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
