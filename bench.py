@@ -191,6 +191,8 @@ KERNEL_SOURCES = {
     "tc128_bf16": "gdn_fwd_tc.cu",
     "diag_bf16": "gdn_diag.cu",
     "diag_fp32": "gdn_diag.cu",
+    "conv_bf16": "gdn_conv.cu",
+    "conv_fp32": "gdn_conv.cu",
 }
 
 
@@ -727,6 +729,116 @@ def bench_diag(args, w: W.DiagWorkload, rank: int, world: int, local: int):
     return 0
 
 
+def bench_conv(args, w: W.ConvWorkload, rank: int, world: int, local: int):
+    """The GDN block prologue (gdn_conv_silu), one call per step."""
+    from linear_attention_recurrence_gated_gb300 import gdn as G
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU (no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    G.lib()
+    from dataclasses import replace
+    host = W.generate_conv(replace(w, seed=w.seed + rank))
+    nsets = 4   # 4 x (input + output) > 129 MB L2 for the pages' shape
+    sets = [{"x": host["x"].to(dev), "y": torch.empty_like(host["x"], device=dev)}
+            for _ in range(nsets)]
+    wd = host["w"].to(dev)
+    stream = torch.cuda.current_stream(dev)
+    kname = "conv_" + w.dtype
+
+    def call(d):
+        G.gdn_conv_silu(d["x"], wd, y=d["y"], stream=stream)
+
+    for i in range(args.warmup):
+        call(sets[i % nsets])
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler()
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        call(sets[i % nsets])
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    barrier(world)
+    time.sleep(0.15)
+    clocks.stop()
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    per_launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    tokens = w.B * w.T
+    value = tokens * world * args.steps / (total_ms / 1e3)
+    # end to end: pinned x in, y back
+    x_pin = host["x"].pin_memory()
+    y_host = torch.empty(host["x"].shape, dtype=host["x"].dtype).pin_memory()
+    d = sets[0]
+    e2e_steps = max(1, min(args.steps, 50))
+
+    def e2e_step():
+        d["x"].copy_(x_pin, non_blocking=True)
+        call(d)
+        y_host.copy_(d["y"], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    barrier(world)
+    if rank != 0:
+        return 0
+    hbm_gbs, _, peak_src = measured_peaks()
+    e = 4 if w.dtype == "fp32" else 2
+    alg_bytes = 2.0 * w.B * w.T * w.C * e + w.C * w.K * 4
+    achieved = alg_bytes / (per_launch_ms / 1e3) / 1e9
+    import oracle.block
+    rows = slice(0, 1)
+    t_c = time.perf_counter()
+    oracle.block.conv_silu(host["x"][rows], host["w"])
+    cpu_secs = time.perf_counter() - t_c
+    clk = clocks.summary(wall0, wall1, _bus_id(local))
+    nbytes = host["x"].numel() * host["x"].element_size()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "C": w.C, "K": w.K,
+                   "storage": w.dtype, "kernel": kname,
+                   "l2": f"{nsets} resident input/output sets of {2 * nbytes / 1e6:.0f} MB "
+                         f"alternate between steps ({2 * nsets * nbytes / 1e6:.0f} MB > 129 MB L2)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": achieved / hbm_gbs, "traffic": committed_traffic(kname, w.name),
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": per_launch_ms},
+        "cpu_baseline": {"value": w.T / cpu_secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"one batch row of {w.name} ({w.T} tokens x {w.C} channels), "
+                                   f"numpy oracle, {cpu_secs:.2f} s"},
+        "e2e": {"value": tokens * world * e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def launches_per_step(kernel_name: str) -> int:
     return 1
 
@@ -752,12 +864,16 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="hymo_bf16",
                     choices=sorted(W.WORKLOADS) + sorted(W.DECODE_WORKLOADS) +
-                    sorted(W.DIAG_WORKLOADS))
+                    sorted(W.DIAG_WORKLOADS) + sorted(W.CONV_WORKLOADS))
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_setup()
     try:
+        if args.workload in W.CONV_WORKLOADS:
+            if args.impl == "reference":
+                raise SystemExit("the reference arm times the recurrence workloads only")
+            return bench_conv(args, W.CONV_WORKLOADS[args.workload], rank, world, local)
         if args.workload in W.DIAG_WORKLOADS:
             dw = W.DIAG_WORKLOADS[args.workload]
             if args.impl == "reference":

@@ -73,7 +73,10 @@ enum {
   GDN_QK_L2NORM = 1u << 0,
   /* Use the fp32 CUDA-core kernel even for bf16 storage (the tensor-core
    * kernel is the default for bf16).  fp32 storage always uses it. */
-  GDN_FORCE_SIMT = 1u << 1
+  GDN_FORCE_SIMT = 1u << 1,
+  /* gdn_diag_fwd only: g holds the gate's logits dt and the kernel uses
+   * g = sigmoid(dt) ("Model Architecture Walkthrough", section 5.2.1). */
+  GDN_GATE_SIGMOID = 1u << 2
 };
 
 /* Bytes of device workspace gdn_fwd needs for these sizes (>= 256; the first
@@ -227,17 +230,27 @@ gdn_status gdn_decode(const void *q, const void *k, const void *v, const float *
  *   b, c           [batch, seq_len, num_heads, d_state]        dtype    device
  *   g              [batch, seq_len, num_heads]                 float32  device
  *   A_log          [num_heads, d_state]                        float32  device
+ *   D_skip         [num_heads]                                 float32  device, or NULL
+ *   out_gate       [batch, seq_len, num_heads]                 float32  device, or NULL
  *   initial_state  [batch, num_heads, d_state, head_dim]       float32  device, or NULL (= zeros)
  *   o              [batch, seq_len, num_heads, head_dim]       dtype    device (written)
  *   final_state    [batch, num_heads, d_state, head_dim]       float32  device (written), or NULL
  *
  * Values: g_t is the positive gate (a sigmoid output on the pages) and is
- * used as given; any real g_t and A_log are accepted, the decay factors are
- * products of exp(g_t A_s) and never overflow for g_t >= 0.
+ * used as given, or with flags = GDN_GATE_SIGMOID it holds the logits and
+ * g_t = sigmoid(g input); any real g_t and A_log are accepted, the decay
+ * factors are products of exp(g_t A_s) and never overflow for g_t >= 0.
+ *
+ * Block epilogue (same page, section 5.5, step 6), fused into the output
+ * store when D_skip or out_gate is given:
+ *
+ *     o_t <- (o_t + D_skip[h] v_t) * out_gate[n, t, h]
+ *
+ * with a missing D_skip read as 0 and a missing out_gate as 1.
  *
  * Supported sizes: d_state == 32 and head_dim == 32 (the pages' production
  * shape); batch, num_heads, seq_len >= 1 with batch * num_heads *
- * ceil(seq_len / 128) < 2^31.  flags must be 0.  Anything else returns
+ * ceil(seq_len / 128) < 2^31.  flags: 0 or GDN_GATE_SIGMOID.  Anything else returns
  * GDN_ERR_UNSUPPORTED (or INVALID_ARG if malformed).
  *
  * Aliasing as gdn_fwd: o and final_state overlap no input; final_state may be
@@ -254,10 +267,43 @@ gdn_status gdn_decode(const void *q, const void *k, const void *v, const float *
 size_t gdn_diag_workspace_size(int32_t batch, int32_t seq_len, int32_t num_heads,
                                int32_t d_state, int32_t head_dim);
 gdn_status gdn_diag_fwd(const void *v, const void *b, const void *c, const float *g,
-                        const float *A_log, const float *initial_state, void *o,
+                        const float *A_log, const float *D_skip, const float *out_gate,
+                        const float *initial_state, void *o,
                         float *final_state, int32_t batch, int32_t seq_len, int32_t num_heads,
                         int32_t d_state, int32_t head_dim, gdn_dtype dtype, uint32_t flags,
                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * gdn_conv_silu -- prologue of the HyMo GDN block: causal depthwise conv1d,
+ * then SiLU ("Model Architecture Walkthrough", section 5.4.1: a depthwise
+ * Conv1d over d_inner channels with d_conv taps and padding d_conv - 1, the
+ * tail trimmed so that it is causal; section 5.5, step 2: SiLU after it).
+ * Per batch row n, token t and channel ch:
+ *
+ *     y[n, t, ch] = silu( sum_{k < taps} w[ch, k] * x[n, t - (taps - 1) + k, ch] )
+ *     silu(z) = z / (1 + exp(-z))
+ *
+ * where x at t < 0 is x_prev[n, taps - 1 + t, ch] when x_prev is given, else 0.
+ * (w[ch, k] is PyTorch's Conv1d weight[ch, 0, k].)  fp32 arithmetic; y in the
+ * caller's dtype.
+ *
+ *   x        [batch, seq_len, channels]        dtype    device
+ *   w        [channels, taps]                  float32  device
+ *   x_prev   [batch, taps - 1, channels]       dtype    device, or NULL (= zeros)
+ *   y        [batch, seq_len, channels]        dtype    device (written)
+ *   x_tail   [batch, taps - 1, channels]       dtype    device (written), or NULL:
+ *            the last taps - 1 inputs (of x_prev followed by x), the x_prev of
+ *            the next call when a sequence is fed in pieces
+ *
+ * Supported: 1 <= taps <= 4 (the pages use 4); channels a multiple of 8
+ * (bf16) or 4 (fp32); batch <= 65535.  Outputs must not overlap any input
+ * (to chain calls, alternate two prefix buffers).  No workspace; no
+ * device-detected error.  Returns GDN_OK once enqueued, or an error code with
+ * nothing enqueued.
+ */
+gdn_status gdn_conv_silu(const void *x, const float *w, const void *x_prev, void *y,
+                         void *x_tail, int32_t batch, int32_t seq_len, int32_t channels,
+                         int32_t taps, gdn_dtype dtype, void *stream);
 
 /* Synchronise `stream`, read the status word in `workspace`, clear it, and
  * return it (GDN_OK if no kernel recorded an error since the last check).

@@ -95,6 +95,8 @@ inline Workspace workspace_layout(int64_t tasks) {
 
 struct DiagParams {
   const float *g, *A_log, *h0;
+  const float *D_skip, *out_gate;   // block epilogue (NULL = off)
+  uint32_t opts;                    // GDN_GATE_SIGMOID
   float *hN;
   void *o;
   DeviceStatus *status;
@@ -264,7 +266,10 @@ gdn_diag_kernel(const DiagParams p, const __grid_constant__ CUtensorMap tm_v,
       const int hdx = (int)(t % (uint32_t)heads_total);
       const int tok = (int)(t / (uint32_t)heads_total) * kSC + kCT * warp + lane;
       const int b_ = hdx / p.num_heads, h_ = hdx % p.num_heads;
-      if (tok < p.seq_len) x = __ldg(p.g + ((int64_t)b_ * p.seq_len + tok) * p.num_heads + h_);
+      if (tok < p.seq_len) {
+        x = __ldg(p.g + ((int64_t)b_ * p.seq_len + tok) * p.num_heads + h_);
+        if (p.opts & GDN_GATE_SIGMOID) x = 1.f / (1.f + __expf(-x));
+      }
     }
     return x;
   };
@@ -287,6 +292,10 @@ gdn_diag_kernel(const DiagParams p, const __grid_constant__ CUtensorMap tm_v,
   const int t0 = blk * kSC;
   const int64_t task = (int64_t)head * p.nblk + blk;
   const int tok_w = t0 + kCT * warp;
+  // output gate of token (16 warp + lane) for lanes 0..15 (block epilogue)
+  float ogate = 1.f;
+  if (p.out_gate && lane < kCT && tok_w + lane < p.seq_len)
+    ogate = __ldg(p.out_gate + ((int64_t)bb * p.seq_len + tok_w + lane) * p.num_heads + hd);
   // scaled decay rates A_s log2(e) of this lane's state rows 2sp, 2sp+1
   const float ah0 = -__expf(__ldg(p.A_log + hd * kS + 2 * sp)) * kLog2e;
   const float ah1 = -__expf(__ldg(p.A_log + hd * kS + 2 * sp + 1)) * kLog2e;
@@ -761,6 +770,28 @@ gdn_diag_kernel(const DiagParams p, const __grid_constant__ CUtensorMap tm_v,
       for (int pp = 0; pp < NP; ++pp) { b0[pp] = pb1[pp][0]; b1[pp] = pb1[pp][1]; }
       mma_np<NP>(O[m][1], va[m], b0, b1);
     }
+    // block epilogue: o <- (o + D_h v) * g_gate.  The V^T A fragments of m-tile
+    // m sit at the positions of the O^T accumulators: register 2 ni + (q >> 1)
+    // holds v at (d, i) = (16 m + g + 8 (q >> 1), 8 ni + 2 tq + (q & 1)).
+    if (p.D_skip || p.out_gate) {
+      const float Dh = p.D_skip ? __ldg(p.D_skip + hd) : 0.f;
+      float gt[2][2];
+#pragma unroll
+      for (int ni = 0; ni < 2; ++ni)
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) gt[ni][e2] = __shfl_sync(0xffffffffu, ogate, 8 * ni + 2 * tq + e2);
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int ni = 0; ni < 2; ++ni)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int r = 2 * ni + (q >> 1);
+            float vv = (q & 1) ? bf16_hi(va[m][0][r]) : bf16_lo(va[m][0][r]);
+            if constexpr (NP == 2) vv += (q & 1) ? bf16_hi(va[m][1][r]) : bf16_lo(va[m][1][r]);
+            O[m][ni][q] = fmaf(Dh, vv, O[m][ni][q]) * gt[ni][q & 1];
+          }
+    }
     __syncwarp();   // H fragments consumed: the exchange slot becomes the o tile
     // o tile [16 tokens][32 columns] in the storage type, row-major
     if constexpr (sizeof(T) == 2) {
@@ -901,7 +932,8 @@ extern "C" size_t gdn_diag_workspace_size(int32_t batch, int32_t seq_len, int32_
 }
 
 extern "C" gdn_status gdn_diag_fwd(const void *v, const void *b, const void *c, const float *g,
-                                   const float *A_log, const float *initial_state, void *o,
+                                   const float *A_log, const float *D_skip,
+                                   const float *out_gate, const float *initial_state, void *o,
                                    float *final_state, int32_t batch, int32_t seq_len,
                                    int32_t num_heads, int32_t d_state, int32_t head_dim,
                                    gdn_dtype dtype, uint32_t flags, void *workspace,
@@ -911,13 +943,13 @@ extern "C" gdn_status gdn_diag_fwd(const void *v, const void *b, const void *c, 
   if (batch <= 0 || seq_len <= 0 || num_heads <= 0 || d_state <= 0 || head_dim <= 0)
     return GDN_ERR_INVALID_ARG;
   if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
-  if (flags != 0u) return GDN_ERR_INVALID_ARG;
+  if (flags & ~(uint32_t)GDN_GATE_SIGMOID) return GDN_ERR_INVALID_ARG;
   if (d_state != kS || head_dim != kD) return GDN_ERR_UNSUPPORTED;
   const int64_t nblk = ((int64_t)seq_len + kSC - 1) / kSC;
   const int64_t tasks = (int64_t)batch * num_heads * nblk;
   if (tasks > 0x7fffffffLL || (int64_t)batch * num_heads > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
   if (!v || !b || !c || !g || !A_log || !o) return GDN_ERR_INVALID_ARG;
-  const void *ptrs[] = {v, b, c, g, A_log, initial_state, o, final_state};
+  const void *ptrs[] = {v, b, c, g, A_log, D_skip, out_gate, initial_state, o, final_state};
   for (const void *ptr : ptrs)
     if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
   if (!workspace) return GDN_ERR_WORKSPACE;
@@ -931,8 +963,9 @@ extern "C" gdn_status gdn_diag_fwd(const void *v, const void *b, const void *c, 
   const size_t b_A = (size_t)num_heads * kS * 4;
   const size_t b_state = (size_t)batch * num_heads * kS * kD * 4;
   struct Range { const void *p; size_t n; };
+  const size_t b_D = (size_t)num_heads * 4;
   const Range inputs[] = {{v, b_v}, {b, b_bc}, {c, b_bc}, {g, b_g}, {A_log, b_A},
-                          {workspace, workspace_bytes}};
+                          {D_skip, b_D}, {out_gate, b_g}, {workspace, workspace_bytes}};
   for (const Range &r : inputs) {
     if (overlaps(o, b_v, r.p, r.n)) return GDN_ERR_INVALID_ARG;
     if (overlaps(final_state, b_state, r.p, r.n)) return GDN_ERR_INVALID_ARG;
@@ -947,6 +980,7 @@ extern "C" gdn_status gdn_diag_fwd(const void *v, const void *b, const void *c, 
   unsigned char *ws = static_cast<unsigned char *>(workspace);
   DiagParams p;
   p.g = g; p.A_log = A_log; p.h0 = initial_state; p.hN = final_state; p.o = o;
+  p.D_skip = D_skip; p.out_gate = out_gate; p.opts = flags;
   p.status = reinterpret_cast<DeviceStatus *>(ws);
   p.ctr = reinterpret_cast<Counters *>(ws + kCountersOff);
   p.flags = reinterpret_cast<uint32_t *>(ws + wl.flags);

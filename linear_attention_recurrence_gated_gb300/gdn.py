@@ -24,12 +24,13 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED",
 GDN_F32, GDN_BF16 = 0, 1
 GDN_QK_L2NORM = 1 << 0
 GDN_FORCE_SIMT = 1 << 1
+GDN_GATE_SIGMOID = 1 << 2
 CHUNK_SIZE = 64
 
 # Every symbol include/gdn.h declares.
 EXPORTED = ("gdn_fwd_workspace_size", "gdn_workspace_init", "gdn_fwd", "gdn_check",
             "gdn_status_string", "gdn_fwd_kernel_name", "gdn_fwd_static_scratch",
-            "gdn_decode", "gdn_diag_workspace_size", "gdn_diag_fwd")
+            "gdn_decode", "gdn_diag_workspace_size", "gdn_diag_fwd", "gdn_conv_silu")
 
 _lib = None
 _lock = threading.Lock()
@@ -73,10 +74,12 @@ def lib() -> ctypes.CDLL:
             L.gdn_decode.restype = ctypes.c_int
             L.gdn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp,
                                      i32, i32, i32, i32, ctypes.c_int, u32, vp]
+            L.gdn_conv_silu.restype = ctypes.c_int
+            L.gdn_conv_silu.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_int, vp]
             L.gdn_diag_workspace_size.restype = sz
             L.gdn_diag_workspace_size.argtypes = [i32, i32, i32, i32, i32]
             L.gdn_diag_fwd.restype = ctypes.c_int
-            L.gdn_diag_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp,
+            L.gdn_diag_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                        i32, i32, i32, i32, i32, ctypes.c_int, u32, vp, sz, vp]
             _lib = L
     return _lib
@@ -267,20 +270,25 @@ def new_diag_workspace(batch, seq_len, num_heads, d_state, head_dim, device=None
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
-def gdn_diag_fwd(v, b, c, g, A_log, initial_state=None, *, o=None, final_state=None,
-                 output_final_state=True, workspace=None, stream=None, check=False):
+def gdn_diag_fwd(v, b, c, g, A_log, initial_state=None, *, D_skip=None, out_gate=None,
+                 gate_sigmoid=False, o=None, final_state=None, output_final_state=True,
+                 workspace=None, stream=None, check=False):
     """The pages' diagonal-decay recurrence through the C ABI.
 
     v ``[B, T, H, D]``; b, c ``[B, T, H, S]`` (v, b, c and o in one storage
     dtype, float32 or bfloat16); g ``[B, T, H]`` fp32; A_log ``[H, S]`` fp32;
-    initial_state ``[B, H, S, D]`` fp32 or None.  Returns ``(o, final_state)``
+    initial_state ``[B, H, S, D]`` fp32 or None.  ``D_skip`` ``[H]`` and
+    ``out_gate`` ``[B, T, H]`` (fp32) fuse the block epilogue
+    o <- (o + D_skip v) * out_gate; ``gate_sigmoid`` makes g the logits of the
+    decay gate (g = sigmoid(g) in the kernel).  Returns ``(o, final_state)``
     (``final_state`` None when ``output_final_state`` is False and none is given).
     A workspace made by ``new_diag_workspace`` for the same sizes may be reused
     across calls on one stream.
     """
     B, T, H, D = v.shape
     S = b.shape[-1]
-    for t in [v, b, c, g, A_log] + [t for t in (initial_state, o, final_state) if t is not None]:
+    for t in [v, b, c, g, A_log] + [t for t in (initial_state, o, final_state, D_skip, out_gate)
+                                    if t is not None]:
         if not t.is_cuda:
             raise ValueError("gdn_diag_fwd: every tensor must be on a CUDA device")
         if not t.is_contiguous():
@@ -296,6 +304,10 @@ def gdn_diag_fwd(v, b, c, g, A_log, initial_state=None, *, o=None, final_state=N
     for name, t in (("initial_state", initial_state), ("final_state", final_state)):
         if t is not None and (t.dtype != torch.float32 or t.shape != (B, H, S, D)):
             raise ValueError(f"gdn_diag_fwd: {name} must be float32 [B, H, S, D]")
+    if D_skip is not None and (D_skip.dtype != torch.float32 or D_skip.shape != (H,)):
+        raise ValueError("gdn_diag_fwd: D_skip must be float32 [H]")
+    if out_gate is not None and (out_gate.dtype != torch.float32 or out_gate.shape != (B, T, H)):
+        raise ValueError("gdn_diag_fwd: out_gate must be float32 [B, T, H]")
     if o is None:
         o = torch.empty_like(v)
     elif o.shape != v.shape or o.dtype != v.dtype:
@@ -304,9 +316,10 @@ def gdn_diag_fwd(v, b, c, g, A_log, initial_state=None, *, o=None, final_state=N
         final_state = torch.empty((B, H, S, D), dtype=torch.float32, device=v.device)
     if workspace is None:
         workspace = new_diag_workspace(B, T, H, S, D, device=v.device)
-    st = lib().gdn_diag_fwd(_ptr(v), _ptr(b), _ptr(c), _ptr(g), _ptr(A_log),
-                            _ptr(initial_state), _ptr(o), _ptr(final_state), B, T, H, S, D,
-                            dcode, 0, _ptr(workspace),
+    st = lib().gdn_diag_fwd(_ptr(v), _ptr(b), _ptr(c), _ptr(g), _ptr(A_log), _ptr(D_skip),
+                            _ptr(out_gate), _ptr(initial_state), _ptr(o), _ptr(final_state),
+                            B, T, H, S, D, dcode, GDN_GATE_SIGMOID if gate_sigmoid else 0,
+                            _ptr(workspace),
                             workspace.numel() * workspace.element_size(),
                             _stream_handle(stream))
     if st != GDN_OK:
@@ -316,3 +329,35 @@ def gdn_diag_fwd(v, b, c, g, A_log, initial_state=None, *, o=None, final_state=N
         if st != GDN_OK:
             raise GdnError(st, "gdn_diag_fwd (device)")
     return o, final_state
+
+
+def gdn_conv_silu(x, w, x_prev=None, *, y=None, x_tail=None, stream=None):
+    """Causal depthwise conv1d + SiLU through the C ABI (the GDN block prologue).
+
+    x ``[B, T, C]`` (float32 or bfloat16); w ``[C, K]`` fp32 (PyTorch's Conv1d
+    weight ``[C, 1, K]`` squeezed); x_prev ``[B, K-1, C]`` or None (zeros).
+    ``x_tail`` (``[B, K-1, C]``, x's dtype) receives the last K-1 inputs when
+    given.  Returns ``y``.
+    """
+    B, T, C = x.shape
+    K = w.shape[-1]
+    for t in [x, w] + [t for t in (x_prev, y, x_tail) if t is not None]:
+        if not t.is_cuda:
+            raise ValueError("gdn_conv_silu: every tensor must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("gdn_conv_silu: every tensor must be contiguous")
+    dcode = _dtype_code(x.dtype)
+    if w.dtype != torch.float32 or w.shape != (C, K):
+        raise ValueError("gdn_conv_silu: w must be float32 [C, K]")
+    for name, t in (("x_prev", x_prev), ("x_tail", x_tail)):
+        if t is not None and (t.dtype != x.dtype or t.shape != (B, K - 1, C)):
+            raise ValueError(f"gdn_conv_silu: {name} must be [B, K-1, C] in x's dtype")
+    if y is None:
+        y = torch.empty_like(x)
+    elif y.shape != x.shape or y.dtype != x.dtype:
+        raise ValueError("gdn_conv_silu: y must match x")
+    st = lib().gdn_conv_silu(_ptr(x), _ptr(w), _ptr(x_prev), _ptr(y), _ptr(x_tail), B, T, C, K,
+                             dcode, _stream_handle(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_conv_silu")
+    return y

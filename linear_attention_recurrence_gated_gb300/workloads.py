@@ -218,3 +218,34 @@ def generate_diag(w: DiagWorkload):
         h0 = torch.from_numpy(0.1 * rng.standard_normal((B, H, S, D))).to(torch.float32)
     return {"v": v.contiguous(), "b": b.contiguous(), "c": c.contiguous(),
             "g": g.contiguous(), "A_log": A_log.contiguous(), "initial_state": h0}
+
+
+# ---------------------------------------------------------------------------
+# The GDN block prologue (causal depthwise conv1d + SiLU)
+# ---------------------------------------------------------------------------
+@dataclass(frozen=True)
+class ConvWorkload:
+    name: str
+    B: int
+    T: int
+    C: int
+    K: int = 4
+    dtype: str = "bf16"
+    seed: int = 0
+    notes: str = field(default="", compare=False)
+
+
+CONV_WORKLOADS = {
+    "conv_hymo_bf16": ConvWorkload("conv_hymo_bf16", B=4, T=4096, C=1280, K=4, dtype="bf16",
+                                   notes="the pages' prologue: d_inner 1280, d_conv 4"),
+}
+
+
+def generate_conv(w: ConvWorkload):
+    """x ~ N(0, 1) ``[B, T, C]`` in the storage dtype, then the conv weights
+    w ~ N(0, 1/K) ``[C, K]`` fp32 (PyTorch's default Conv1d scale is of this
+    order), from one ``default_rng(seed)`` stream in that order."""
+    rng = np.random.default_rng(w.seed)
+    x = torch.from_numpy(rng.standard_normal((w.B, w.T, w.C))).to(_DTYPES[w.dtype])
+    wt = torch.from_numpy(rng.standard_normal((w.C, w.K)) / np.sqrt(w.K)).to(torch.float32)
+    return {"x": x.contiguous(), "w": wt.contiguous()}

@@ -149,20 +149,25 @@ def call_diag(L, **over):
     B, T, H, S, D = 2, 300, 3, 32, 32
     ws_need = G.gdn_diag_workspace_size(B, T, H, S, D)
     a = dict(v=BASE, b=BASE + (1 << 30), c=BASE + (2 << 30), g=BASE + (3 << 30),
-             A=BASE + (4 << 30), s0=None, o=BASE + (5 << 30), sN=BASE + (6 << 30),
+             A=BASE + (4 << 30), Dk=None, og=None, s0=None, o=BASE + (5 << 30),
+             sN=BASE + (6 << 30),
              B=B, T=T, H=H, S=S, D=D, dtype=G.GDN_BF16, flags=0, ws=BASE + (7 << 30),
              ws_bytes=ws_need)
     a.update(over)
     vp = ctypes.c_void_p
     return L.gdn_diag_fwd(vp(a["v"]), vp(a["b"]), vp(a["c"]), vp(a["g"]), vp(a["A"]),
-                          vp(a["s0"]), vp(a["o"]), vp(a["sN"]), a["B"], a["T"], a["H"], a["S"],
+                          vp(a["Dk"]), vp(a["og"]), vp(a["s0"]), vp(a["o"]), vp(a["sN"]),
+                          a["B"], a["T"], a["H"], a["S"],
                           a["D"], a["dtype"], a["flags"], vp(a["ws"]), a["ws_bytes"], vp(0))
 
 
 @pytest.mark.parametrize("over,code", [
     (dict(S=16), 2), (dict(D=64), 2), (dict(S=0), 1), (dict(D=-1), 1),
     (dict(B=0), 1), (dict(T=0), 1), (dict(H=0), 1),
-    (dict(dtype=5), 1), (dict(flags=1), 1),
+    (dict(dtype=5), 1), (dict(flags=1), 1), (dict(flags=G.GDN_FORCE_SIMT), 1),
+    (dict(Dk=BASE + (4 << 30) + 8), 1),                      # misaligned D_skip
+    (dict(og=BASE + (5 << 30)), 1),                          # out_gate aliases o
+    (dict(Dk=BASE + (6 << 30)), 1),                          # D_skip inside the final state
     (dict(v=None), 1), (dict(b=None), 1), (dict(c=None), 1), (dict(g=None), 1),
     (dict(A=None), 1), (dict(o=None), 1),
     (dict(c=BASE + (2 << 30) + 4), 1), (dict(sN=BASE + (6 << 30) + 8), 1),
