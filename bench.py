@@ -299,13 +299,15 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
         sets.append(d)
     ws = G.new_workspace(N, w.H, w.dk, w.dv, device=dev)
     kname = G.gdn_fwd_kernel_name(w.dk, w.dv, host["q"].dtype)
+    if args.chunk != CHUNK:   # other chunk sizes run on the fp32 CUDA-core kernel
+        kname = "simt_" + ("fp32" if w.dtype == "fp32" else "bf16")
     stream = torch.cuda.current_stream(dev)
 
     def step(i):
         d = sets[i & 1]
         G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"],
                   d["cu_seqlens"], o=d["o"], final_state=d["final_state"], workspace=ws,
-                  stream=stream)
+                  chunk_size=args.chunk, stream=stream)
 
     for i in range(args.warmup):
         step(i)
@@ -362,7 +364,7 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
             d["initial_state"].copy_(s0_pinned, non_blocking=True)
         G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"],
                   d["cu_seqlens"], o=d["o"], final_state=d["final_state"], workspace=ws,
-                  stream=stream)
+                  chunk_size=args.chunk, stream=stream)
         o_host.copy_(d["o"], non_blocking=True)
         s_host.copy_(d["final_state"], non_blocking=True)
 
@@ -389,7 +391,7 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
 
     hbm_gbs, bf16_tflops, peak_src = measured_peaks()
     alg_bytes = algorithmic_bytes(w, tokens, N, host["initial_state"] is not None)
-    alg_flops = algorithmic_flops(w, tokens)
+    alg_flops = algorithmic_flops(w, tokens)   # counted at the 64-token chunk
     achieved_gbs = alg_bytes / (per_launch_ms / 1e3) / 1e9
     achieved_tflops = alg_flops / (per_launch_ms / 1e3) / 1e12
     traffic = committed_traffic(kname, w.name)
@@ -402,7 +404,7 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": arith, "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
-                   "storage": w.dtype, "chunk": CHUNK, "kernel": kname,
+                   "storage": w.dtype, "chunk": args.chunk, "kernel": kname,
                    "l2": "two resident input sets of "
                          f"{sum(sets[0][n].numel() * sets[0][n].element_size() for n in names) / 1e6:.0f}"
                          " MB each (> 129 MB L2) alternate between steps",
@@ -862,6 +864,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--chunk", type=int, default=CHUNK, choices=(32, 64, 128),
+                    help="chunk size of gdn_fwd (32 and 128 run on the fp32 CUDA-core kernel)")
     ap.add_argument("--workload", default="hymo_bf16",
                     choices=sorted(W.WORKLOADS) + sorted(W.DECODE_WORKLOADS) +
                     sorted(W.DIAG_WORKLOADS) + sorted(W.CONV_WORKLOADS))

@@ -69,8 +69,8 @@ gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
   if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
   if (flags & ~(uint32_t)(GDN_QK_L2NORM | GDN_FORCE_SIMT)) return GDN_ERR_INVALID_ARG;
   if (cu_seqlens ? batch != 1 : num_seqs != batch) return GDN_ERR_INVALID_ARG;
-  if (chunk_size != gdn::kChunk) return GDN_ERR_UNSUPPORTED;
   if (!supported_dk(head_dim_k) || !supported_dv(head_dim_v)) return GDN_ERR_UNSUPPORTED;
+  if (!gdn::simt_chunk_supported(chunk_size, head_dim_k)) return GDN_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || num_heads > 65535) return GDN_ERR_UNSUPPORTED;
 
   // ---- pointers ----
@@ -113,9 +113,12 @@ gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
   p.num_heads = num_heads; p.dk = head_dim_k; p.dv = head_dim_v; p.num_seqs = num_seqs;
   p.flags = flags;
 
-  const cudaError_t err = use_tc(head_dim_k, head_dim_v, dtype, flags)
-                              ? gdn::launch_fwd_tc(p, (cudaStream_t)stream)
-                              : gdn::launch_fwd_simt(p, dtype, (cudaStream_t)stream);
+  // the tensor-core kernels are built for 64-token chunks; other chunk sizes
+  // run on the fp32 CUDA-core kernel
+  const cudaError_t err =
+      chunk_size == gdn::kChunk && use_tc(head_dim_k, head_dim_v, dtype, flags)
+          ? gdn::launch_fwd_tc(p, (cudaStream_t)stream)
+          : gdn::launch_fwd_simt(p, dtype, chunk_size, (cudaStream_t)stream);
   return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -1,7 +1,8 @@
 // Fused chunked forward of the gated delta rule on fp32 CUDA cores.
 //
 // One CTA owns one (sequence, head, 32-wide slice of the value dimension) and
-// walks that sequence's chunks of 64 tokens in order, keeping its slice of the
+// walks that sequence's chunks of C tokens (C = 32, 64 or 128; 64 is the
+// pages' default) in order, keeping its slice of the
 // fp32 state H = S^T (dk x 32) in shared memory for the whole sequence (state
 // kept on chip: "Model Architecture Walkthrough", section 6.3; chunked with a
 // serial inter-chunk carry: "Optimization Quartet", Triton GDN kernel
@@ -30,32 +31,30 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kDvTile = 32;
 
-template <int DK>
+template <int DK, int C>
 struct SimtSmem {
-  static constexpr int C = kChunk;
   static constexpr int QK_LD = DK + 1;      // padded rows: conflict-free column walks
   static constexpr int U_LD = kDvTile + 1;
   static constexpr int A_LD = C + 1;
   static constexpr int kFloats = 2 * C * QK_LD + C * U_LD + C * kDvTile + DK * kDvTile +
-                                 2 * C * A_LD + 4 * C;
+                                 C * A_LD + 4 * C;
   static constexpr size_t kBytes = sizeof(float) * kFloats;
 };
 
-template <int DK, typename Tin>
+template <int DK, int C, typename Tin>
 __global__ void __launch_bounds__(kThreads)
 gdn_fwd_simt_kernel(const FwdParams p) {
-  using L = SimtSmem<DK>;
-  constexpr int C = kChunk;
+  using L = SimtSmem<DK, C>;
   constexpr int DVT = kDvTile;
+  constexpr int PER_LANE = C / 32;       // gates per lane in the prefix sum
   extern __shared__ float smem[];
   float *sQ = smem;                      // [C][QK_LD]
   float *sK = sQ + C * L::QK_LD;         // [C][QK_LD]
   float *sU = sK + C * L::QK_LD;         // [C][U_LD]   V -> R -> U
   float *sO = sU + C * L::U_LD;          // [C][DVT]    diag(gamma) Q H0
   float *sH = sO + C * DVT;              // [DK][DVT]   the state slice
-  float *sA = sH + DK * DVT;             // [C][A_LD]
-  float *sP = sA + C * L::A_LD;          // [C][A_LD]
-  float *sG = sP + C * L::A_LD;          // [C] cumulative log-gate
+  float *sA = sH + DK * DVT;             // [C][A_LD]   A, then P (after the substitution)
+  float *sG = sA + C * L::A_LD;          // [C] cumulative log-gate
   float *sB = sG + C;                    // [C] beta
   float *sGam = sB + C;                  // [C] exp(G_i)
   float *sDec = sGam + C;                // [C] exp(G_last - G_j)
@@ -128,15 +127,21 @@ gdn_fwd_simt_kernel(const FwdParams p) {
 
     // ---- chunk-local inclusive prefix sum of the log-gates ----
     if (warp == 0) {
-      const float a = sG[2 * lane], b = sG[2 * lane + 1];
-      float s = a + b;
+      float part[PER_LANE];
+      float run = 0.f;
+#pragma unroll
+      for (int e = 0; e < PER_LANE; ++e) {
+        run += sG[PER_LANE * lane + e];
+        part[e] = run;
+      }
+      float s = run;
       for (int off = 1; off < 32; off <<= 1) {
         const float t = __shfl_up_sync(0xffffffffu, s, off);
         if (lane >= off) s += t;
       }
-      const float excl = s - (a + b);
-      sG[2 * lane] = excl + a;
-      sG[2 * lane + 1] = excl + a + b;
+      const float excl = s - run;
+#pragma unroll
+      for (int e = 0; e < PER_LANE; ++e) sG[PER_LANE * lane + e] = excl + part[e];
     }
     __syncthreads();
     if (tid < C) {
@@ -144,24 +149,18 @@ gdn_fwd_simt_kernel(const FwdParams p) {
       sDec[tid] = expf(sG[C - 1] - sG[tid]);
     }
 
-    // ---- A = strictly_lower(diag(beta) K K^T (.) Gamma), P = Q K^T (.) Gamma (i >= j) ----
+    // ---- A = strictly_lower(diag(beta) K K^T (.) Gamma) ----
     for (int idx = tid; idx < C * C; idx += kThreads) {
       const int i = idx / C, j = idx % C;
-      float a = 0.f, pp = 0.f;
-      if (j <= i) {
-        const float *qi = sQ + i * L::QK_LD, *ki = sK + i * L::QK_LD, *kj = sK + j * L::QK_LD;
-        float dqk = 0.f, dkk = 0.f;
+      float a = 0.f;
+      if (j < i) {
+        const float *ki = sK + i * L::QK_LD, *kj = sK + j * L::QK_LD;
+        float dkk = 0.f;
 #pragma unroll 8
-        for (int d = 0; d < DK; ++d) {
-          dqk = fmaf(qi[d], kj[d], dqk);
-          dkk = fmaf(ki[d], kj[d], dkk);
-        }
-        const float dec = expf(sG[i] - sG[j]);
-        pp = dqk * dec;
-        if (j < i) a = sB[i] * dkk * dec;
+        for (int d = 0; d < DK; ++d) dkk = fmaf(ki[d], kj[d], dkk);
+        a = sB[i] * dkk * expf(sG[i] - sG[j]);
       }
       sA[i * L::A_LD + j] = a;
-      sP[i * L::A_LD + j] = pp;
     }
     __syncthreads();
 
@@ -200,11 +199,26 @@ gdn_fwd_simt_kernel(const FwdParams p) {
     }
     __syncthreads();
 
+    // ---- P = Q K^T (.) Gamma (i >= j), into A's buffer (A is no longer needed) ----
+    for (int idx = tid; idx < C * C; idx += kThreads) {
+      const int i = idx / C, j = idx % C;
+      float pp = 0.f;
+      if (j <= i) {
+        const float *qi = sQ + i * L::QK_LD, *kj = sK + j * L::QK_LD;
+        float dqk = 0.f;
+#pragma unroll 8
+        for (int d = 0; d < DK; ++d) dqk = fmaf(qi[d], kj[d], dqk);
+        pp = dqk * expf(sG[i] - sG[j]);
+      }
+      sA[i * L::A_LD + j] = pp;
+    }
+    __syncthreads();
+
     // ---- O = sO + P U (stored); H_C = gamma_C H0 + (diag(dec) K)^T U ----
     for (int idx = tid; idx < C * DVT; idx += kThreads) {
       const int i = idx / DVT, c = idx % DVT;
       if (i < rows) {
-        const float *pi = sP + i * L::A_LD;
+        const float *pi = sA + i * L::A_LD;
         float acc = sO[i * DVT + c];
         for (int j = 0; j <= i; ++j) acc = fmaf(pi[j], sU[j * L::U_LD + c], acc);
         store_out(o + ((size_t)(start + c0 + i) * H + h) * dv + col0 + c, acc);
@@ -227,10 +241,10 @@ gdn_fwd_simt_kernel(const FwdParams p) {
     }
 }
 
-template <int DK, typename Tin>
+template <int DK, int C, typename Tin>
 cudaError_t launch_simt_dk(const FwdParams &p, cudaStream_t stream) {
-  auto kern = gdn_fwd_simt_kernel<DK, Tin>;
-  const size_t smem = SimtSmem<DK>::kBytes;
+  auto kern = gdn_fwd_simt_kernel<DK, C, Tin>;
+  const size_t smem = SimtSmem<DK, C>::kBytes;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
   if (err != cudaSuccess) return err;
@@ -239,21 +253,37 @@ cudaError_t launch_simt_dk(const FwdParams &p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <typename Tin>
-cudaError_t launch_simt_t(const FwdParams &p, cudaStream_t stream) {
+template <int C, typename Tin>
+cudaError_t launch_simt_c(const FwdParams &p, cudaStream_t stream) {
   switch (p.dk) {
-    case 32: return launch_simt_dk<32, Tin>(p, stream);
-    case 64: return launch_simt_dk<64, Tin>(p, stream);
-    case 128: return launch_simt_dk<128, Tin>(p, stream);
+    case 32: return launch_simt_dk<32, C, Tin>(p, stream);
+    case 64: return launch_simt_dk<64, C, Tin>(p, stream);
+    case 128:
+      if constexpr (C <= 64) return launch_simt_dk<128, C, Tin>(p, stream);
+      return cudaErrorInvalidValue;   // 128-token chunks with dk = 128 exceed shared memory
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename Tin>
+cudaError_t launch_simt_t(const FwdParams &p, int chunk, cudaStream_t stream) {
+  switch (chunk) {
+    case 32: return launch_simt_c<32, Tin>(p, stream);
+    case 64: return launch_simt_c<64, Tin>(p, stream);
+    case 128: return launch_simt_c<128, Tin>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_fwd_simt(const FwdParams &p, gdn_dtype dtype, cudaStream_t stream) {
-  return dtype == GDN_F32 ? launch_simt_t<float>(p, stream)
-                          : launch_simt_t<__nv_bfloat16>(p, stream);
+bool simt_chunk_supported(int chunk, int dk) {
+  return (chunk == 32 || chunk == 64 || chunk == 128) && !(chunk == 128 && dk == 128);
+}
+
+cudaError_t launch_fwd_simt(const FwdParams &p, gdn_dtype dtype, int chunk, cudaStream_t stream) {
+  return dtype == GDN_F32 ? launch_simt_t<float>(p, chunk, stream)
+                          : launch_simt_t<__nv_bfloat16>(p, chunk, stream);
 }
 
 }  // namespace gdn

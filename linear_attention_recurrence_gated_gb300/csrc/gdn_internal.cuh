@@ -10,7 +10,7 @@
 
 namespace gdn {
 
-constexpr int kChunk = 64;  // tokens per chunk
+constexpr int kChunk = 64;  // tokens per chunk of the tensor-core kernels (the default)
 
 // Device status record at the start of the workspace.  The first error wins
 // (atomicCAS from 0); `seq` and `head` locate it, `aux` carries a detail.
@@ -72,7 +72,8 @@ __device__ __forceinline__ void store_out(float *p, float x) { *p = x; }
 __device__ __forceinline__ void store_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 
 // Launchers (one per kernel family).  Return a cudaError_t from the launch.
-cudaError_t launch_fwd_simt(const FwdParams &p, gdn_dtype dtype, cudaStream_t stream);
+cudaError_t launch_fwd_simt(const FwdParams &p, gdn_dtype dtype, int chunk, cudaStream_t stream);
+bool simt_chunk_supported(int chunk, int dk);   // chunk in {32, 64, 128}, not 128 with dk 128
 cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t stream);    // bf16 storage only
 cudaError_t launch_fwd_tc64(const FwdParams &p, cudaStream_t stream);  // bf16, head_dim_k 64
 bool tc_supported(int dk, int dv);

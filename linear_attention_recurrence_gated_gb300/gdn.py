@@ -139,7 +139,7 @@ def gdn_fwd_kernel_name(head_dim_k, head_dim_v, dtype: torch.dtype, flags: int =
 
 def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
             final_state=None, output_final_state=True, workspace=None,
-            qk_l2norm=False, force_simt=False, stream=None, check=False):
+            qk_l2norm=False, force_simt=False, chunk_size=CHUNK_SIZE, stream=None, check=False):
     """Forward pass of the gated delta rule through the C ABI.
 
     q, k ``[B, T, H, dk]``; v ``[B, T, H, dv]``; g ``[B, T, H]`` fp32; beta
@@ -147,7 +147,8 @@ def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
     (float32 or bfloat16).  initial_state ``[N, H, dk, dv]`` fp32 or None;
     cu_seqlens int32 ``[N+1]`` on the device (then B must be 1) or None.
     ``o`` / ``final_state`` may be given to write into preallocated outputs
-    (``final_state`` may be ``initial_state``).  Returns ``(o, final_state)``.
+    (``final_state`` may be ``initial_state``).  ``chunk_size`` is 32, 64 (the
+    default) or 128.  Returns ``(o, final_state)``.
     With ``check=True`` the call synchronises and raises on a device-side error.
     """
     B, T, H, dk = q.shape
@@ -187,7 +188,7 @@ def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
         workspace = new_workspace(N, H, dk, dv, flags, device=q.device)
     st = lib().gdn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
                        _ptr(cu_seqlens), _ptr(o), _ptr(final_state), B, T, H, dk, dv, N,
-                       CHUNK_SIZE, dcode, flags, _ptr(workspace),
+                       chunk_size, dcode, flags, _ptr(workspace),
                        workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_fwd")

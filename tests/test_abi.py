@@ -81,7 +81,8 @@ def call(L, **over):
 
 @pytest.mark.parametrize("over,code", [
     (dict(dk=48), 2), (dict(dk=256), 2), (dict(dv=48), 2), (dict(dv=288), 2),
-    (dict(chunk=32), 2), (dict(dtype=7), 1), (dict(flags=1 << 9), 1),
+    (dict(chunk=16), 2), (dict(chunk=256), 2), (dict(chunk=128, dk=128, dv=128), 2),
+    (dict(dtype=7), 1), (dict(flags=1 << 9), 1),
     (dict(q=None), 1), (dict(o=None), 1), (dict(g=None), 1), (dict(beta=None), 1),
     (dict(q=BASE + 8), 1), (dict(o=BASE + (5 << 30) + 4), 1), (dict(sN=BASE + (6 << 30) + 2), 1),
     (dict(ws=None), 3), (dict(ws_bytes=255), 3), (dict(ws=BASE + (7 << 30) + 8), 1),

@@ -171,3 +171,47 @@ def test_bad_seqlens_reported(cu):
               workspace=ws)
     assert G.gdn_check(ws) == 6
     assert G.gdn_check(ws) == 0  # the check cleared the status word
+
+
+# ---------------- chunk-size variants (32 and 128, fp32 CUDA-core kernel) ----------------
+CHUNK_SHAPES = [(1, 1, 1, 32, 32), (2, 31, 2, 64, 64), (1, 32, 1, 32, 64), (1, 33, 2, 64, 32),
+                (2, 127, 2, 32, 96), (1, 128, 1, 64, 64), (1, 129, 2, 64, 128),
+                (2, 300, 3, 128, 64), (1, 1000, 1, 64, 64)]
+
+
+@pytest.mark.parametrize("chunk", [32, 128])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("B,T,H,dk,dv", CHUNK_SHAPES)
+def test_chunk_size_variants(chunk, dtype, B, T, H, dk, dv):
+    if chunk == 128 and dk == 128:
+        pytest.skip("128-token chunks with dk = 128 are not supported")
+    w = W.custom(B=B, T=T, H=H, dk=dk, dv=dv, dtype=dtype, gate_scale=1.0, init_state=True,
+                 seed=2000 + T + dk + dv + chunk)
+    _check(W.generate(w), W._DTYPES[dtype], gpu=dict(chunk_size=chunk))
+
+
+@pytest.mark.parametrize("chunk", [32, 128])
+def test_chunk_size_variants_varlen(chunk):
+    lens = [1, 31, 32, 33, 127, 128, 129, 300]
+    w = W.custom(num_seqs=len(lens), len_range=(1, 300), H=2, dk=64, dv=64, dtype="bf16",
+                 init_state=True, seed=31 + chunk)
+    _check(W.generate(w, lengths=lens), torch.bfloat16, gpu=dict(chunk_size=chunk))
+
+
+@pytest.mark.parametrize("chunk", [32, 128])
+def test_chunk_size_variants_full_size(chunk):
+    """The HyMo-shaped bench workload (B=8, T=4096, H=16, dk=dv=64) in 32- and
+    128-token chunks."""
+    w = W.WORKLOADS["hymo_bf16"]
+    _check(W.generate(w), torch.bfloat16, gpu=dict(chunk_size=chunk))
+
+
+def test_chunk_sizes_agree():
+    """The result does not depend on the chunk size beyond rounding."""
+    w = W.custom(B=2, T=500, H=2, dk=64, dv=64, dtype="fp32", gate_scale=1.0, init_state=True,
+                 seed=41)
+    inp = W.generate(w)
+    outs = [parity.gpu_forward(inp, chunk_size=c) for c in (32, 64, 128)]
+    for o, s in outs[1:]:
+        assert parity.rel(o.double().cpu().numpy(), outs[0][0].double().cpu().numpy()) <= 1e-5
+        assert parity.rel(s.double().cpu().numpy(), outs[0][1].double().cpu().numpy()) <= 1e-5
