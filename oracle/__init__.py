@@ -19,6 +19,8 @@ Contents
                  exp(g_t A) with A = -exp(A_log), write key b, read key c
                  ("Model Architecture Walkthrough" section 5.2.1), token by
                  token in fp64 numpy.
+``grad``         the backward pass (dq, dk, dv, dg, dbeta, d initial state):
+                 torch.autograd over the fp64 token loop on the CPU.
 ``block``        the GDN block's prologue (causal depthwise conv1d + SiLU) and
                  epilogue ((o + D v) * g_gate), same page, sections 5.4-5.5.
 
