@@ -310,6 +310,50 @@ gdn_status gdn_conv_silu(const void *x, const float *w, const void *x_prev, void
                          void *x_tail, int32_t batch, int32_t seq_len, int32_t channels,
                          int32_t taps, gdn_dtype dtype, void *stream);
 
+/*
+ * gdn_bwd -- backward pass of gdn_fwd's operation: the vector-Jacobian
+ * products of o (and of the final state) with respect to every input.  It
+ * recomputes what it needs from the inputs, as the pages' kernel does
+ * ("Optimization Quartet", Triton GDN kernel section 3.4; the backward runs
+ * the recurrence backwards in time: "Model Architecture Walkthrough", section
+ * 6.5).  With s_t = H_{t-1}^T k_t, u_t = beta_t (v_t - alpha_t s_t), and dH
+ * the running gradient of the state (d_final_state at the end), for t = T..1:
+ *
+ *   dH += q_t do_t^T,  dq_t = H_t do_t,  du = dH^T k_t,  dv_t = beta_t du,
+ *   dbeta_t = <du, v_t - alpha_t s_t>,  dg_t = alpha_t (<dH, H_{t-1}> - beta_t <du, s_t>),
+ *   dk_t = dH u_t - alpha_t beta_t H_{t-1} du,  dH <- alpha_t (dH - beta_t k_t du^T)
+ *
+ * and d_initial_state is the final dH.
+ *
+ *   q, k, v, g, beta, initial_state, cu_seqlens   as gdn_fwd (inputs)
+ *   d_o            [batch, seq_len, num_heads, head_dim_v]     dtype    device
+ *   d_final_state  [num_seqs, num_heads, head_dim_k, head_dim_v] float32 device, or NULL (= zeros)
+ *   dq, dk         [batch, seq_len, num_heads, head_dim_k]     float32  device (written)
+ *   dv             [batch, seq_len, num_heads, head_dim_v]     float32  device (written)
+ *   dg, dbeta      [batch, seq_len, num_heads]                 float32  device (written)
+ *   d_initial_state [num_seqs, num_heads, head_dim_k, head_dim_v] float32 device (written), or NULL
+ *
+ * All gradients are fp32 whatever the storage dtype.  dq, dk, dg and dbeta
+ * are summed with atomics over value-column slices, so they are not bitwise
+ * reproducible from run to run (they agree to fp32 rounding).  Sizes as
+ * gdn_fwd (chunk 64); flags must be 0.  No gradient buffer may overlap an
+ * input or another gradient.  workspace: at least gdn_bwd_workspace_size(...)
+ * bytes, the fp32 state at every 64-token chunk start plus per-CTA scratch;
+ * the first 256 bytes are the status word (zero it once with
+ * gdn_workspace_init).  Device-detected errors (bad cu_seqlens) are reported
+ * by gdn_check.  Returns GDN_OK once enqueued, or an error code with nothing
+ * enqueued.  seq_len is the packed token count when cu_seqlens is given.
+ */
+size_t gdn_bwd_workspace_size(int32_t num_seqs, int32_t seq_len, int32_t num_heads,
+                              int32_t head_dim_k, int32_t head_dim_v);
+gdn_status gdn_bwd(const void *q, const void *k, const void *v, const float *g,
+                   const void *beta, const float *initial_state, const int32_t *cu_seqlens,
+                   const void *d_o, const float *d_final_state, float *dq, float *dk,
+                   float *dv, float *dg, float *dbeta, float *d_initial_state, int32_t batch,
+                   int32_t seq_len, int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
+                   int32_t num_seqs, gdn_dtype dtype, uint32_t flags, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
 /* Synchronise `stream`, read the status word in `workspace`, clear it, and
  * return it (GDN_OK if no kernel recorded an error since the last check).
  * Also returns GDN_ERR_CUDA if the stream synchronisation itself failed. */

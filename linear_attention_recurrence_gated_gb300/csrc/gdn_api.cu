@@ -109,6 +109,7 @@ gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
   p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g;
   p.s0 = initial_state; p.cu = cu_seqlens; p.o = o; p.sN = final_state;
   p.status = static_cast<gdn::DeviceStatus *>(workspace);
+  p.ckpt = nullptr;
   p.seq_len = seq_len;
   p.num_heads = num_heads; p.dk = head_dim_k; p.dv = head_dim_v; p.num_seqs = num_seqs;
   p.flags = flags;

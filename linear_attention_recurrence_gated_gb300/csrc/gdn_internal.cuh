@@ -31,6 +31,7 @@ struct FwdParams {
   void *o;
   float *sN;
   DeviceStatus *status;
+  float *ckpt;          // backward only: state at every 64-token chunk start (else NULL)
   int64_t seq_len;      // tokens per batch row (dense) or packed total (varlen)
   int32_t num_heads, dk, dv, num_seqs;
   uint32_t flags;
@@ -70,6 +71,18 @@ __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ void store_out(float *p, float x) { *p = x; }
 __device__ __forceinline__ void store_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+// First checkpoint slot of sequence n in a [slots][H][dk][dv] array of
+// 64-token chunk-start states: dense rows n * ceil(T / 64); packed sequences
+// floor(start / 64) + n, which never overlaps the previous sequence's slots.
+__host__ __device__ inline int64_t ckpt_first_slot(int64_t n, int64_t start, int64_t seq_len,
+                                                   bool varlen) {
+  return varlen ? start / 64 + n : n * ((seq_len + 63) / 64);
+}
+__host__ __device__ inline int64_t ckpt_slots(int64_t num_seqs, int64_t seq_len) {
+  const int64_t dense = num_seqs * ((seq_len + 63) / 64), packed = seq_len / 64 + num_seqs + 1;
+  return dense > packed ? dense : packed;
+}
 
 // Launchers (one per kernel family).  Return a cudaError_t from the launch.
 cudaError_t launch_fwd_simt(const FwdParams &p, gdn_dtype dtype, int chunk, cudaStream_t stream);

@@ -30,7 +30,8 @@ CHUNK_SIZE = 64
 # Every symbol include/gdn.h declares.
 EXPORTED = ("gdn_fwd_workspace_size", "gdn_workspace_init", "gdn_fwd", "gdn_check",
             "gdn_status_string", "gdn_fwd_kernel_name", "gdn_fwd_static_scratch",
-            "gdn_decode", "gdn_diag_workspace_size", "gdn_diag_fwd", "gdn_conv_silu")
+            "gdn_decode", "gdn_diag_workspace_size", "gdn_diag_fwd", "gdn_conv_silu",
+            "gdn_bwd_workspace_size", "gdn_bwd")
 
 _lib = None
 _lock = threading.Lock()
@@ -74,6 +75,10 @@ def lib() -> ctypes.CDLL:
             L.gdn_decode.restype = ctypes.c_int
             L.gdn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp,
                                      i32, i32, i32, i32, ctypes.c_int, u32, vp]
+            L.gdn_bwd_workspace_size.restype = sz
+            L.gdn_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+            L.gdn_bwd.restype = ctypes.c_int
+            L.gdn_bwd.argtypes = [vp] * 15 + [i32] * 6 + [ctypes.c_int, u32, vp, sz, vp]
             L.gdn_conv_silu.restype = ctypes.c_int
             L.gdn_conv_silu.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_int, vp]
             L.gdn_diag_workspace_size.restype = sz
@@ -362,3 +367,59 @@ def gdn_conv_silu(x, w, x_prev=None, *, y=None, x_tail=None, stream=None):
     if st != GDN_OK:
         raise GdnError(st, "gdn_conv_silu")
     return y
+
+
+def gdn_bwd_workspace_size(num_seqs: int, seq_len: int, num_heads: int, head_dim_k: int,
+                           head_dim_v: int) -> int:
+    return int(lib().gdn_bwd_workspace_size(num_seqs, seq_len, num_heads, head_dim_k, head_dim_v))
+
+
+def gdn_bwd(q, k, v, g, beta, d_o, initial_state=None, cu_seqlens=None, d_final_state=None, *,
+            grads=None, workspace=None, stream=None, check=False):
+    """Backward pass of ``gdn_fwd`` through the C ABI.
+
+    Inputs as ``gdn_fwd`` plus ``d_o`` (like v) and ``d_final_state``
+    (``[N, H, dk, dv]`` fp32 or None).  Returns a dict of fp32 tensors
+    ``dq, dk, dv, dg, dbeta, dh0`` (``grads`` may supply them preallocated).
+    """
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    for t in [q, k, v, g, beta, d_o] + [t for t in (initial_state, cu_seqlens, d_final_state)
+                                        if t is not None]:
+        if not t.is_cuda:
+            raise ValueError("gdn_bwd: every tensor must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("gdn_bwd: every tensor must be contiguous")
+    dcode = _dtype_code(q.dtype)
+    if k.dtype != q.dtype or v.dtype != q.dtype or beta.dtype != q.dtype or d_o.dtype != q.dtype:
+        raise TypeError("gdn_bwd: q, k, v, beta and d_o must share one storage dtype")
+    if g.dtype != torch.float32:
+        raise TypeError("gdn_bwd: g must be float32")
+    if d_o.shape != v.shape:
+        raise ValueError("gdn_bwd: d_o must match v")
+    for name, t in (("initial_state", initial_state), ("d_final_state", d_final_state)):
+        if t is not None and (t.dtype != torch.float32 or t.shape != (N, H, dk, dv)):
+            raise ValueError(f"gdn_bwd: {name} must be float32 [N, H, dk, dv]")
+    f32 = dict(dtype=torch.float32, device=q.device)
+    if grads is None:
+        grads = {"dq": torch.empty((B, T, H, dk), **f32), "dk": torch.empty((B, T, H, dk), **f32),
+                 "dv": torch.empty((B, T, H, dv), **f32), "dg": torch.empty((B, T, H), **f32),
+                 "dbeta": torch.empty((B, T, H), **f32),
+                 "dh0": torch.empty((N, H, dk, dv), **f32)}
+    if workspace is None:
+        n = gdn_bwd_workspace_size(N, T, H, dk, dv)
+        workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
+    st = lib().gdn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                       _ptr(cu_seqlens), _ptr(d_o), _ptr(d_final_state), _ptr(grads["dq"]),
+                       _ptr(grads["dk"]), _ptr(grads["dv"]), _ptr(grads["dg"]),
+                       _ptr(grads["dbeta"]), _ptr(grads.get("dh0")), B, T, H, dk, dv, N, dcode,
+                       0, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                       _stream_handle(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_bwd")
+    if check:
+        st = gdn_check(workspace, stream)
+        if st != GDN_OK:
+            raise GdnError(st, "gdn_bwd (device)")
+    return grads

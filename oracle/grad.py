@@ -58,9 +58,9 @@ def backward(q, k, v, g, beta, initial_state, d_o, d_final_state=None, cu_seqlen
     leaves = [q, k, v, g, beta, h0]
     for x in leaves:
         x.requires_grad_(True)
-    o = torch.zeros(B, T, H, dv, dtype=torch.float64)
+    zero = torch.zeros(H, dv, dtype=torch.float64)
+    o_rows = [[zero] * T for _ in range(B)]
     finals = []
-    outs = []
     for n, (row, s, e) in enumerate(bounds):
         Hs = h0[n]                                                  # [H, dk, dv]
         for t in range(s, e):
@@ -69,10 +69,9 @@ def backward(q, k, v, g, beta, initial_state, d_o, d_final_state=None, cu_seqlen
             bt = beta[row, t][:, None, None]
             kH = torch.einsum("hk,hkv->hv", kt, Hs)                 # k^T H_{t-1}
             Hs = a * (Hs - bt * kt[:, :, None] * kH[:, None, :]) + bt * kt[:, :, None] * vt[:, None, :]
-            outs.append((row, t, torch.einsum("hkv,hk->hv", Hs, qt)))
+            o_rows[row][t] = torch.einsum("hkv,hk->hv", Hs, qt)
         finals.append(Hs)
-    for row, t, ot in outs:
-        o = o.index_put((torch.tensor([row]), torch.tensor([t])), ot[None])
+    o = torch.stack([torch.stack(r) for r in o_rows])
     hN = torch.stack(finals)
     loss = (o * d_o).sum()
     if dhN is not None:

@@ -108,8 +108,8 @@ MUTANTS = [
     ("erase sign", "Hs - bt * kt[:, :, None]", "Hs + bt * kt[:, :, None]"),
     ("decay on the write too", "Hs = a * (Hs - bt * kt[:, :, None] * kH[:, None, :]) + bt",
      "Hs = a * (Hs - bt * kt[:, :, None] * kH[:, None, :]) + a * bt"),
-    ("read with the write key", "torch.einsum(\"hkv,hk->hv\", Hs, qt)",
-     "torch.einsum(\"hkv,hk->hv\", Hs, kt)"),
+    ("read with the write key", "o_rows[row][t] = torch.einsum(\"hkv,hk->hv\", Hs, qt)",
+     "o_rows[row][t] = torch.einsum(\"hkv,hk->hv\", Hs, kt)"),
     ("final-state gradient dropped", "loss = loss + (hN * dhN).sum()", "loss = loss"),
     ("decay exp sign", "a = torch.exp(g[row, t])", "a = torch.exp(-g[row, t])"),
 ]
