@@ -841,6 +841,141 @@ def bench_conv(args, w: W.ConvWorkload, rank: int, world: int, local: int):
     return 0
 
 
+def bwd_bytes(w: W.Workload, tokens: int, N: int) -> float:
+    """HBM bytes of one gdn_bwd call at its algorithmic minimum: q, k, v, beta,
+    d_o read in the storage dtype and g as fp32; dq, dk, dv, dg, dbeta written
+    in fp32; the fp32 d initial state written per (sequence, head)."""
+    e = 4 if w.dtype == "fp32" else 2
+    per = e * (2 * w.dk + 2 * w.dv + 1) + 4 + 4 * (2 * w.dk + w.dv + 2)
+    return float(tokens * w.H * per + 4 * w.dk * w.dv * N * w.H)
+
+
+def bench_bwd(args, w: W.Workload, rank: int, world: int, local: int):
+    """The backward pass (gdn_bwd) on a forward workload, one call per step."""
+    from linear_attention_recurrence_gated_gb300 import gdn as G
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU (no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    G.lib()
+    host = W.generate(W.with_seed(w, w.seed + rank))
+    N, tokens = host["N"], host["tokens"]
+    names = ("q", "k", "v", "g", "beta")
+    rng = __import__("numpy").random.default_rng(17 + rank)
+    d_o_host = torch.from_numpy(rng.standard_normal(tuple(host["v"].shape))).to(host["v"].dtype)
+    d = {n: host[n].to(dev) for n in names}
+    d["d_o"] = d_o_host.to(dev)
+    s0 = None if host["initial_state"] is None else host["initial_state"].to(dev)
+    cu = None if host["cu_seqlens"] is None else host["cu_seqlens"].to(dev)
+    B, T = host["q"].shape[:2]
+    ws = torch.zeros(G.gdn_bwd_workspace_size(N, T, w.H, w.dk, w.dv), dtype=torch.uint8,
+                     device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    grads = {"dq": torch.empty((B, T, w.H, w.dk), **f32),
+             "dk": torch.empty((B, T, w.H, w.dk), **f32),
+             "dv": torch.empty((B, T, w.H, w.dv), **f32), "dg": torch.empty((B, T, w.H), **f32),
+             "dbeta": torch.empty((B, T, w.H), **f32),
+             "dh0": torch.empty((N, w.H, w.dk, w.dv), **f32)}
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        G.gdn_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["d_o"], s0, cu, None,
+                  grads=grads, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    st = G.gdn_check(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {G.status_string(st)}")
+    clocks = ClockSampler()
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t0.record(stream)
+    for _ in range(args.steps):
+        call()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    barrier(world)
+    time.sleep(0.15)
+    clocks.stop()
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    per_ms = total_ms / args.steps
+    value = tokens * world * args.steps / (total_ms / 1e3)
+    # end to end: inputs and d_o from pinned host memory, the five gradients back
+    pinned = {n: host[n].pin_memory() for n in names}
+    do_pin = d_o_host.pin_memory()
+    back = {n: torch.empty(t.shape, dtype=torch.float32).pin_memory()
+            for n, t in grads.items() if n != "dh0"}
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values()) + do_pin.numel() * do_pin.element_size()
+    d2h = sum(t.numel() * 4 for t in back.values())
+    e2e_steps = max(1, min(args.steps, 10))
+
+    def e2e_step():
+        for n in names:
+            d[n].copy_(pinned[n], non_blocking=True)
+        d["d_o"].copy_(do_pin, non_blocking=True)
+        call()
+        for n, t in back.items():
+            t.copy_(grads[n], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    barrier(world)
+    if rank != 0:
+        return 0
+    hbm_gbs, _, peak_src = measured_peaks()
+    alg = bwd_bytes(w, tokens, N)
+    achieved = alg / (per_ms / 1e3) / 1e9
+    # CPU baseline: the autograd oracle on one head of one batch row
+    import oracle.grad
+    t_c = time.perf_counter()
+    oracle.grad.backward(host["q"][:1, :, :1], host["k"][:1, :, :1], host["v"][:1, :, :1],
+                         host["g"][:1, :, :1], host["beta"][:1, :, :1], None,
+                         d_o_host[:1, :, :1], None)
+    cpu_secs = time.perf_counter() - t_c
+    clk = clocks.summary(wall0, wall1, _bus_id(local))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "pass": "backward", "B": w.B, "T": w.T, "H": w.H,
+                   "dk": w.dk, "dv": w.dv, "storage": w.dtype, "kernel": "bwd",
+                   "l2": "inputs, d_o and the fp32 gradients (> 129 MB) stream every step",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": achieved / hbm_gbs, "traffic": None,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": alg, "kernel_ms": per_ms,
+                     "launches_per_step": "4 zero fills, the checkpointing forward, the backward"},
+        "cpu_baseline": {"value": w.T / cpu_secs / w.H, "unit": UNIT, "cores": 1,
+                         "kind": "oracle",
+                         "sample": f"one head of one batch row ({w.T} tokens), torch.autograd "
+                                   f"fp64 oracle, {cpu_secs:.1f} s; value scaled to {w.H} heads"},
+        "e2e": {"value": tokens * world * e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps * 2,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def launches_per_step(kernel_name: str) -> int:
     return 1
 
@@ -864,6 +999,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--pass", dest="pass_", choices=("fwd", "bwd"), default="fwd",
+                    help="fwd: gdn_fwd; bwd: gdn_bwd (the prefill workloads)")
     ap.add_argument("--chunk", type=int, default=CHUNK, choices=(32, 64, 128),
                     help="chunk size of gdn_fwd (32 and 128 run on the fp32 CUDA-core kernel)")
     ap.add_argument("--workload", default="hymo_bf16",
@@ -888,6 +1025,10 @@ def main(argv=None):
                 raise SystemExit("the reference arm times the prefill workloads only")
             return bench_decode(args, W.DECODE_WORKLOADS[args.workload], rank, world, local)
         w = W.WORKLOADS[args.workload]
+        if args.pass_ == "bwd":
+            if args.impl == "reference":
+                raise SystemExit("the reference arm times the forward pass only")
+            return bench_bwd(args, w, rank, world, local)
         if args.impl == "reference":
             return bench_reference(args, w, rank, world)
         return bench_ours(args, w, rank, world, local)
