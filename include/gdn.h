@@ -300,8 +300,8 @@ gdn_status gdn_diag_fwd(const void *v, const void *b, const void *c, const float
  *            the last taps - 1 inputs (of x_prev followed by x), the x_prev of
  *            the next call when a sequence is fed in pieces
  *
- * Supported: 1 <= taps <= 4 (the pages use 4); channels a multiple of 8
- * (bf16) or 4 (fp32); batch <= 65535.  Outputs must not overlap any input
+ * Supported: 1 <= taps <= 4 (the pages use 4); channels a multiple of 4;
+ * batch <= 65535.  Outputs must not overlap any input
  * (to chain calls, alternate two prefix buffers).  No workspace; no
  * device-detected error.  Returns GDN_OK once enqueued, or an error code with
  * nothing enqueued.

@@ -8,12 +8,12 @@
 //
 // The pass is bound by HBM bandwidth: every input element is read once from
 // HBM (the K-1 token halo of a run is the previous run's data, an L1/L2 hit)
-// and every output element written once.  A thread owns one 16-byte channel
-// vector (8 bf16 or 4 fp32 channels) over a run of 8 tokens: it issues all
+// and every output element written once.  A thread owns a vector of 4
+// channels (8 bytes of bf16 or 16 of fp32) over a run of 8 tokens: it issues all
 // 8 + K-1 loads of its window at once, so that enough bytes are in flight to
 // cover the HBM latency, then produces the 8 outputs.  Consecutive lanes own
-// consecutive vectors, so each warp-wide load or store is 512 contiguous
-// bytes of one token row.
+// consecutive vectors, so each warp-wide load or store is 256 or 512
+// contiguous bytes of one token row.
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -25,34 +25,24 @@ constexpr int kVecWarps = 8;     // token runs per CTA (one per warp)
 
 template <typename T> struct Vec;
 template <> struct Vec<__nv_bfloat16> {
-  static constexpr int N = 8;
-  __device__ static void load(const void *p, float (&x)[N]) {
-    unpack(*reinterpret_cast<const uint4 *>(p), x);
-  }
-  __device__ static void unpack(const uint4 r, float (&x)[N]) {
-    const uint32_t u[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x[2 * i] = __uint_as_float(u[i] << 16);
-      x[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
-    }
+  static constexpr int N = 4;   // 4 channels: one 8-byte vector
+  using Raw = uint2;
+  __device__ static void unpack(const Raw r, float (&x)[N]) {
+    x[0] = __uint_as_float(r.x << 16);
+    x[1] = __uint_as_float(r.x & 0xffff0000u);
+    x[2] = __uint_as_float(r.y << 16);
+    x[3] = __uint_as_float(r.y & 0xffff0000u);
   }
   __device__ static void store(void *p, const float (&x)[N]) {
-    uint32_t u[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
-      u[i] = *reinterpret_cast<const uint32_t *>(&h);
-    }
-    *reinterpret_cast<uint4 *>(p) = make_uint4(u[0], u[1], u[2], u[3]);
+    const __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
+    *reinterpret_cast<uint2 *>(p) =
+        make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
   }
 };
 template <> struct Vec<float> {
-  static constexpr int N = 4;
-  __device__ static void load(const void *p, float (&x)[N]) {
-    unpack(*reinterpret_cast<const uint4 *>(p), x);
-  }
-  __device__ static void unpack(const uint4 r, float (&x)[N]) {
+  static constexpr int N = 4;   // 4 channels: one 16-byte vector
+  using Raw = uint4;
+  __device__ static void unpack(const Raw r, float (&x)[N]) {
     x[0] = __uint_as_float(r.x); x[1] = __uint_as_float(r.y);
     x[2] = __uint_as_float(r.z); x[3] = __uint_as_float(r.w);
   }
@@ -71,7 +61,7 @@ struct ConvParams {
 __device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kConvThreads)
+__global__ void __launch_bounds__(kConvThreads, 4)
 gdn_conv_silu_kernel(const ConvParams p) {
   using V = Vec<T>;
   constexpr int N = V::N;
@@ -106,17 +96,18 @@ gdn_conv_silu_kernel(const ConvParams p) {
   // raw[r] holds x[t0 - (K - 1) + r]: the halo, then this run's tokens, all
   // loads issued before the first use
   constexpr int R = kRun + K - 1;
-  uint4 raw[R];
+  typename V::Raw raw[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const int t = t0 - (K - 1) + r;
     if (t >= 0 && t < L) {
-      raw[r] = *reinterpret_cast<const uint4 *>(x + row(t) * e);
+      raw[r] = *reinterpret_cast<const typename V::Raw *>(x + row(t) * e);
     } else if (t < 0 && p.x_prev) {   // prefix: the K-1 inputs before token 0
-      raw[r] = *reinterpret_cast<const uint4 *>(static_cast<const unsigned char *>(p.x_prev) +
-                                                (((size_t)n * (K - 1) + (K - 1) + t) * C + c0) * e);
+      raw[r] = *reinterpret_cast<const typename V::Raw *>(
+          static_cast<const unsigned char *>(p.x_prev) +
+          (((size_t)n * (K - 1) + (K - 1) + t) * C + c0) * e);
     } else {
-      raw[r] = make_uint4(0u, 0u, 0u, 0u);
+      raw[r] = typename V::Raw{};
     }
   }
   const int t_end = t0 + kRun < L ? t0 + kRun : L;
@@ -151,8 +142,8 @@ gdn_conv_silu_kernel(const ConvParams p) {
     for (int r = 0; r < R; ++r) {
       const int k = r - base;
       if (k >= 0 && k < K - 1)
-        *reinterpret_cast<uint4 *>(static_cast<unsigned char *>(p.x_tail) +
-                                   (((size_t)n * (K - 1) + k) * C + c0) * e) = raw[r];
+        *reinterpret_cast<typename V::Raw *>(static_cast<unsigned char *>(p.x_tail) +
+                                             (((size_t)n * (K - 1) + k) * C + c0) * e) = raw[r];
     }
   }
 }
@@ -195,8 +186,7 @@ extern "C" gdn_status gdn_conv_silu(const void *x, const float *w, const void *x
   if (batch <= 0 || seq_len <= 0 || channels <= 0 || taps <= 0) return GDN_ERR_INVALID_ARG;
   if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
   if (taps > 4) return GDN_ERR_UNSUPPORTED;
-  const int vec = dtype == GDN_F32 ? 4 : 8;
-  if (channels % vec) return GDN_ERR_UNSUPPORTED;
+  if (channels % 4) return GDN_ERR_UNSUPPORTED;
   if (batch > 65535) return GDN_ERR_UNSUPPORTED;
   if (!x || !w || !y) return GDN_ERR_INVALID_ARG;
   if (x_tail && taps == 1) return GDN_ERR_INVALID_ARG;   // no prefix to keep
