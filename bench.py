@@ -347,37 +347,67 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
     value = tokens * world * args.steps / (total_ms / 1e3)
 
     # ---- end to end: pinned host inputs -> device -> gdn_fwd -> host result ----
+    # Double-buffered over the two device sets, as a serving loop would run it:
+    # the host-to-device copy of step i+1's inputs runs on its own stream while
+    # step i computes, and step i's result is read back on a third stream.
+    # Every step copies its whole input set in and its whole result out inside
+    # the timed region; a set is refilled only after the step that last read
+    # it has finished, and recomputed only after its result has been read back.
     pinned = {n: host[n].pin_memory() for n in names}
     s0_pinned = None if host["initial_state"] is None else host["initial_state"].pin_memory()
     o_host = torch.empty(host["v"].shape, dtype=host["v"].dtype).pin_memory()
     s_host = torch.empty((N, w.H, w.dk, w.dv), dtype=torch.float32).pin_memory()
     e2e_steps = max(1, min(args.steps, 50))
-    d = sets[0]
     h2d = sum(pinned[n].numel() * pinned[n].element_size() for n in names) + \
         (0 if s0_pinned is None else s0_pinned.numel() * 4)
     d2h = o_host.numel() * o_host.element_size() + s_host.numel() * 4
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    h2d_done = [torch.cuda.Event(), torch.cuda.Event()]
+    comp_done = [torch.cuda.Event(), torch.cuda.Event()]
+    d2h_done = [torch.cuda.Event(), torch.cuda.Event()]
 
-    def e2e_step():
-        for n in names:
-            d[n].copy_(pinned[n], non_blocking=True)
-        if s0_pinned is not None:
-            d["initial_state"].copy_(s0_pinned, non_blocking=True)
+    def e2e_step(i):
+        b = i & 1
+        d = sets[b]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(comp_done[b])    # step i-2 has read this input set
+            for n in names:
+                d[n].copy_(pinned[n], non_blocking=True)
+            if s0_pinned is not None:
+                d["initial_state"].copy_(s0_pinned, non_blocking=True)
+            h2d_done[b].record(s_in)
+        stream.wait_event(h2d_done[b])
+        if i >= 2:
+            stream.wait_event(d2h_done[b])       # step i-2's result has been read back
         G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"],
                   d["cu_seqlens"], o=d["o"], final_state=d["final_state"], workspace=ws,
                   chunk_size=args.chunk, stream=stream)
-        o_host.copy_(d["o"], non_blocking=True)
-        s_host.copy_(d["final_state"], non_blocking=True)
+        comp_done[b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[b])
+            o_host.copy_(d["o"], non_blocking=True)
+            s_host.copy_(d["final_state"], non_blocking=True)
+            d2h_done[b].record(s_out)
 
-    for _ in range(3):
-        e2e_step()
+    def e2e_run(nsteps, e_begin=None, e_end=None):
+        if e_begin is not None:
+            e_begin.record(stream)
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        for i in range(nsteps):
+            e2e_step(i)
+        for b in range(min(nsteps, 2)):
+            stream.wait_event(d2h_done[b])
+        if e_end is not None:
+            e_end.record(stream)
+
+    e2e_run(3)
     torch.cuda.synchronize(dev)
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e2e_run(e2e_steps, e0, e1)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     barrier(world)
@@ -421,7 +451,9 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
                          "sample": f"the whole {w.name} workload ({tokens} tokens x {w.H} "
                                    f"heads), one pass, {cpu_secs:.1f} s"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "overlap": "two device sets: step i+1's inputs copy in while step i "
+                           "computes and step i-1's result copies out"},
         "gpu_launches": args.steps * launches_per_step(kname),
         "clocks": clk,
     }
