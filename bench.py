@@ -994,7 +994,7 @@ def bench_bwd(args, w: W.Workload, rank: int, world: int, local: int):
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": alg, "kernel_ms": per_ms,
-                     "launches_per_step": "4 zero fills, the checkpointing forward, the backward"},
+                     "launches_per_step": "4 zero fills, the checkpoint scan, the backward"},
         "cpu_baseline": {"value": w.T / cpu_secs / w.H, "unit": UNIT, "cores": 1,
                          "kind": "oracle",
                          "sample": f"one head of one batch row ({w.T} tokens), torch.autograd "

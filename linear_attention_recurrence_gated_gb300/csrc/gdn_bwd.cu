@@ -20,9 +20,10 @@
 // Columns of H evolve independently, so a CTA owns 32 value columns of one
 // (sequence, head) and each of its 8 warps owns 4 of them, rows spread over
 // the lanes: the serial chain (du, the dH update, and in the recompute the
-// s_t reduction) needs warp shuffles only.  States are recomputed from the
-// forward's checkpoints (one per 64-token chunk): once per chunk to the start
-// of each 8-token sub-chunk, then per sub-chunk into shared memory.  The sums
+// s_t reduction) needs warp shuffles only.  States are recomputed from
+// checkpoints (one per 64-token chunk, written by a token-serial fp32 scan of
+// the forward with the same layout): once per chunk to the start of each
+// 8-token sub-chunk, then per sub-chunk into shared memory.  The sums
 // over columns (dq, dk, dbeta, dalpha) gather in shared memory per sub-chunk
 // and are added to the fp32 outputs with atomics (several CTAs share a head
 // when dv > 32).
@@ -343,6 +344,106 @@ gdn_bwd_kernel(const BwdParams P) {
   }
 }
 
+// Forward scan that keeps the state entering every 64-token chunk: the
+// checkpoints the backward kernel restarts from.  Token by token in fp32 --
+// the recurrence as written, the same step as the backward's recompute -- with
+// the CTA and warp layout of the backward kernel: a CTA owns 32 value columns
+// of one (sequence, head), each warp 4 of them with the key rows over the
+// lanes, and the tokens are staged a chunk at a time in shared memory.  The
+// last chunk's tokens are not scanned: no checkpoint follows them.
+template <int DK, typename Tin>
+__global__ void __launch_bounds__(kBT)
+gdn_bwd_ckpt_kernel(const FwdParams p) {
+  constexpr int NR = DK / 32;
+  __shared__ float sK[kCk * DK];
+  __shared__ float sV[kCk * kCols];
+  __shared__ float sAl[kCk], sBe[kCk];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tile = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+  const int H = p.num_heads, dv = p.dv;
+  const int col0 = tile * kCols, cw = 4 * warp;
+  int64_t start, len;
+  if (!sequence_bounds(p, n, h, start, len)) return;
+  const Tin *k = static_cast<const Tin *>(p.k);
+  const Tin *v = static_cast<const Tin *>(p.v);
+  const Tin *beta = static_cast<const Tin *>(p.beta);
+  const size_t state_base = ((size_t)n * H + h) * (size_t)DK * dv + col0 + cw;
+
+  float Hr[NR][4];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.s0) x = *reinterpret_cast<const float4 *>(p.s0 + state_base + (size_t)(lane + 32 * r) * dv);
+    Hr[r][0] = x.x; Hr[r][1] = x.y; Hr[r][2] = x.z; Hr[r][3] = x.w;
+  }
+  const int64_t ck0 = ckpt_first_slot(n, start, p.seq_len, p.cu != nullptr);
+  const int nck = (int)((len + kCk - 1) / kCk);
+  for (int c = 0; c < nck; ++c) {
+    float *ck = p.ckpt + ((ck0 + c) * H + h) * (size_t)DK * dv + col0 + cw;
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+      *reinterpret_cast<float4 *>(ck + (size_t)(lane + 32 * r) * dv) =
+          make_float4(Hr[r][0], Hr[r][1], Hr[r][2], Hr[r][3]);
+    if (c == nck - 1) break;
+    const int64_t t0 = (int64_t)c * kCk;
+    __syncthreads();   // the previous chunk's tokens are consumed
+    for (int idx = tid; idx < kCk * DK; idx += kBT) {
+      const int i = idx / DK, d = idx % DK;
+      sK[idx] = to_f32(k[((size_t)(start + t0 + i) * H + h) * DK + d]);
+    }
+    for (int idx = tid; idx < kCk * kCols; idx += kBT) {
+      const int i = idx / kCols, cc = idx % kCols;
+      sV[idx] = to_f32(v[((size_t)(start + t0 + i) * H + h) * dv + col0 + cc]);
+    }
+    if (tid < kCk) {
+      const size_t off = (size_t)(start + t0 + tid) * H + h;
+      sAl[tid] = expf(p.g[off]);
+      sBe[tid] = to_f32(beta[off]);
+    }
+    __syncthreads();
+    // every chunk but the last is full: 64 steps
+#pragma unroll 1
+    for (int i = 0; i < kCk; ++i) {
+      const float al = sAl[i], be = sBe[i];
+      float kr[NR], part[4], sv[4];
+#pragma unroll
+      for (int r = 0; r < NR; ++r) kr[r] = sK[i * DK + lane + 32 * r];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float a = 0.f;
+#pragma unroll
+        for (int r = 0; r < NR; ++r) a = fmaf(Hr[r][j], kr[r], a);
+        part[j] = a;
+      }
+      reduce4(part, sv, lane);
+      const float4 vj = *reinterpret_cast<const float4 *>(sV + i * kCols + cw);
+      const float u[4] = {be * (vj.x - al * sv[0]), be * (vj.y - al * sv[1]),
+                          be * (vj.z - al * sv[2]), be * (vj.w - al * sv[3])};
+#pragma unroll
+      for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) Hr[r][j] = fmaf(al, Hr[r][j], kr[r] * u[j]);
+    }
+  }
+}
+
+template <int DK, typename Tin>
+cudaError_t launch_ckpt_dk(const FwdParams &f, cudaStream_t s) {
+  const dim3 grid(f.dv / kCols, f.num_heads, f.num_seqs);
+  gdn_bwd_ckpt_kernel<DK, Tin><<<grid, kBT, 0, s>>>(f);
+  return cudaGetLastError();
+}
+
+template <typename Tin>
+cudaError_t launch_ckpt_t(const FwdParams &f, cudaStream_t s) {
+  switch (f.dk) {
+    case 32: return launch_ckpt_dk<32, Tin>(f, s);
+    case 64: return launch_ckpt_dk<64, Tin>(f, s);
+    case 128: return launch_ckpt_dk<128, Tin>(f, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 template <int DK, typename Tin>
 cudaError_t launch_bwd_dk(const BwdParams &P, cudaStream_t s) {
   auto kern = gdn_bwd_kernel<DK, Tin>;
@@ -462,8 +563,8 @@ extern "C" gdn_status gdn_bwd(const void *q, const void *k, const void *v, const
   f.seq_len = seq_len;
   f.num_heads = num_heads; f.dk = head_dim_k; f.dv = head_dim_v; f.num_seqs = num_seqs;
   f.flags = 0;
-  // forward on the fp32 CUDA-core kernel, keeping only the chunk-start states
-  cudaError_t err = launch_fwd_simt(f, dtype, kCk, s);
+  // the forward as a token-serial fp32 scan, keeping only the chunk-start states
+  cudaError_t err = dtype == GDN_F32 ? launch_ckpt_t<float>(f, s) : launch_ckpt_t<__nv_bfloat16>(f, s);
   if (err != cudaSuccess) return GDN_ERR_CUDA;
   f.ckpt = nullptr;
   P.dO = d_o; P.dHN = d_final_state; P.ckpt = ckpt; P.scratch = scratch;

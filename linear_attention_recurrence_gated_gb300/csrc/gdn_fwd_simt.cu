@@ -79,17 +79,9 @@ gdn_fwd_simt_kernel(const FwdParams p) {
     sH[idx] = p.s0 ? p.s0[state_base + (size_t)d * dv + c] : 0.f;
   }
 
-  const int64_t ck0 = ckpt_first_slot(n, start, p.seq_len, p.cu != nullptr);
   for (int64_t c0 = 0; c0 < len; c0 += C) {
     const int rows = (int)(len - c0 < C ? len - c0 : C);
     __syncthreads();  // previous chunk finished with every buffer
-    if (p.ckpt) {     // the state entering this chunk, for the backward pass
-      float *ck = p.ckpt + ((ck0 + c0 / C) * H + h) * (size_t)DK * dv + col0;
-      for (int idx = tid; idx < DK * DVT; idx += kThreads) {
-        const int d = idx / DVT, c = idx % DVT;
-        ck[(size_t)d * dv + c] = sH[idx];
-      }
-    }
 
     // ---- load the chunk (rows past the end are zero: no effect on H) ----
     for (int idx = tid; idx < C * DK; idx += kThreads) {
