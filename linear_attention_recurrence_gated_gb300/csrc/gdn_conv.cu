@@ -22,6 +22,8 @@ namespace {
 constexpr int kRun = 8;          // tokens per thread
 constexpr int kConvThreads = 256;
 constexpr int kVecWarps = 8;     // token runs per CTA (one per warp)
+// resident CTAs per SM: bf16 fits 64 registers, fp32 needs 80
+template <typename T> constexpr int kConvBlocks() { return sizeof(T) == 2 ? 4 : 3; }
 
 template <typename T> struct Vec;
 template <> struct Vec<__nv_bfloat16> {
@@ -58,10 +60,18 @@ struct ConvParams {
   int32_t batch, seq_len, channels, taps;
 };
 
-__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
+// silu(z) = z / (1 + e^-z) = z * rcp(1 + 2^(-z log2 e)) on the hardware's
+// approximate 2^x and reciprocal (flush-to-zero forms: no denormal fix-ups).
+// Large negative z gives 2^(+big) = inf, rcp(inf) = 0 and silu -> -0.
+__device__ __forceinline__ float silu(float z) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(z * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+  return z * r;
+}
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kConvThreads, 4)
+__global__ void __launch_bounds__(kConvThreads, kConvBlocks<T>())
 gdn_conv_silu_kernel(const ConvParams p) {
   using V = Vec<T>;
   constexpr int N = V::N;
@@ -94,44 +104,48 @@ gdn_conv_silu_kernel(const ConvParams p) {
     }
 
   // raw[r] holds x[t0 - (K - 1) + r]: the halo, then this run's tokens, all
-  // loads issued before the first use
+  // loads issued before the first use.  Runs away from the sequence ends (the
+  // common case) load without per-token tests, from one base pointer.
   constexpr int R = kRun + K - 1;
   typename V::Raw raw[R];
+  const size_t rstride = (size_t)C * e;                 // bytes between tokens
+  if (t0 >= K - 1 && t0 + kRun <= L) {
+    const unsigned char *xb = x + row(t0 - (K - 1)) * e;
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int t = t0 - (K - 1) + r;
-    if (t >= 0 && t < L) {
-      raw[r] = *reinterpret_cast<const typename V::Raw *>(x + row(t) * e);
-    } else if (t < 0 && p.x_prev) {   // prefix: the K-1 inputs before token 0
-      raw[r] = *reinterpret_cast<const typename V::Raw *>(
-          static_cast<const unsigned char *>(p.x_prev) +
-          (((size_t)n * (K - 1) + (K - 1) + t) * C + c0) * e);
-    } else {
-      raw[r] = typename V::Raw{};
+    for (int r = 0; r < R; ++r) raw[r] = *reinterpret_cast<const typename V::Raw *>(xb + r * rstride);
+  } else {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int t = t0 - (K - 1) + r;
+      if (t >= 0 && t < L) {
+        raw[r] = *reinterpret_cast<const typename V::Raw *>(x + row(t) * e);
+      } else if (t < 0 && p.x_prev) {   // prefix: the K-1 inputs before token 0
+        raw[r] = *reinterpret_cast<const typename V::Raw *>(
+            static_cast<const unsigned char *>(p.x_prev) +
+            (((size_t)n * (K - 1) + (K - 1) + t) * C + c0) * e);
+      } else {
+        raw[r] = typename V::Raw{};
+      }
     }
   }
   const int t_end = t0 + kRun < L ? t0 + kRun : L;
-  float win[K][N];
+  // every input unpacked once; output q reads inputs q .. q + K - 1
+  float xf[R][N];
 #pragma unroll
-  for (int k = 0; k < K - 1; ++k) V::unpack(raw[k], win[k]);
+  for (int r = 0; r < R; ++r) V::unpack(raw[r], xf[r]);
+  unsigned char *yb = static_cast<unsigned char *>(p.y) + row(t0) * e;
+  const bool full = t_end == t0 + kRun;
 #pragma unroll
   for (int q = 0; q < kRun; ++q) {
-    V::unpack(raw[q + K - 1], win[K - 1]);
-    if (t0 + q < t_end) {
-      float out[N];
+    float out[N];
 #pragma unroll
-      for (int j = 0; j < N; ++j) {
-        float a = 0.f;
+    for (int j = 0; j < N; ++j) {
+      float a = 0.f;
 #pragma unroll
-        for (int k = 0; k < K; ++k) a = fmaf(w[k][j], win[k][j], a);
-        out[j] = silu(a);
-      }
-      V::store(static_cast<unsigned char *>(p.y) + row(t0 + q) * e, out);
+      for (int k = 0; k < K; ++k) a = fmaf(w[k][j], xf[q + k][j], a);
+      out[j] = silu(a);
     }
-#pragma unroll
-    for (int k = 0; k < K - 1; ++k)
-#pragma unroll
-      for (int j = 0; j < N; ++j) win[k][j] = win[k + 1][j];
+    if (full || t0 + q < t_end) V::store(yb + q * rstride, out);
   }
   // the last K-1 inputs (prefix of the next call): written by the run that
   // holds them, which is the run ending at the last token
