@@ -89,6 +89,44 @@ def barrier(world: int):
             torch.distributed.barrier()
 
 
+def capture_steps(launch, steps: int, dev, stream, eager: bool):
+    """The K timed steps as one CUDA graph (None when timing eagerly).
+
+    launch(i, s) issues step i on stream s.  The graph is captured on a side
+    stream and replayed once, untimed, so that its upload is not timed either.
+    Replaying the graph runs every launch of every step; it only removes the
+    host's per-call overhead (argument marshalling, launch) from the timed
+    region, where back-to-back launches of a 20-150 us kernel would otherwise
+    leave the GPU idle between them."""
+    if eager:
+        return None
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    # relaxed: the library sets kernel attributes from the launching thread
+    with torch.cuda.graph(g, stream=cap, capture_error_mode="relaxed"):
+        for i in range(steps):
+            launch(i, cap)
+    stream.wait_stream(cap)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    return g
+
+
+def run_steps(graph, launch, steps: int, stream):
+    """Issue the K timed steps on `stream`: the captured graph, or eagerly."""
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(steps):
+            launch(i, stream)
+
+
+TIMING_NOTE = {False: "the K steps captured as one CUDA graph, replayed once between CUDA events "
+                      "(every launch runs; host launch overhead is not timed)",
+               True: "the K steps launched one by one from the host between CUDA events"}
+
+
 def max_over_ranks(x: float, world: int) -> float:
     if world == 1:
         return x
@@ -303,11 +341,11 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
         kname = "simt_" + ("fp32" if w.dtype == "fp32" else "bf16")
     stream = torch.cuda.current_stream(dev)
 
-    def step(i):
+    def step(i, s=stream):
         d = sets[i & 1]
         G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"],
                   d["cu_seqlens"], o=d["o"], final_state=d["final_state"], workspace=ws,
-                  chunk_size=args.chunk, stream=stream)
+                  chunk_size=args.chunk, stream=s)
 
     for i in range(args.warmup):
         step(i)
@@ -316,8 +354,7 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {G.status_string(st)}")
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    graph = capture_steps(step, args.steps, dev, stream, args.eager)
     clocks = ClockSampler()
     clocks.start()
     time.sleep(0.3)
@@ -327,10 +364,7 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
     t_end = torch.cuda.Event(enable_timing=True)
     wall0 = time.time()
     t_start.record(stream)
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        step(i)
-        ev[i][1].record(stream)
+    run_steps(graph, step, args.steps, stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     wall1 = time.time()
@@ -343,7 +377,7 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
 
     local_ms = t_start.elapsed_time(t_end)
     total_ms = max_over_ranks(local_ms, world)
-    per_launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    per_launch_ms = local_ms / args.steps   # one gdn_fwd launch per step
     value = tokens * world * args.steps / (total_ms / 1e3)
 
     # ---- end to end: pinned host inputs -> device -> gdn_fwd -> host result ----
@@ -433,6 +467,7 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": arith, "data": "synthetic",
+        "timing": TIMING_NOTE[args.eager],
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
                    "storage": w.dtype, "chunk": args.chunk, "kernel": kname,
                    "l2": "two resident input sets of "
@@ -484,15 +519,14 @@ def bench_decode(args, w: W.Workload, rank: int, world: int, local: int):
     o = torch.empty_like(d["v"])
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def step(i=0, s=stream):
         G.gdn_decode(d["q"], d["k"], d["v"], d["g"], d["beta"], state, o=o, state_out=state,
-                     stream=stream)
+                     stream=s)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    graph = capture_steps(step, args.steps, dev, stream, args.eager)
     clocks = ClockSampler()
     clocks.start()
     time.sleep(0.3)
@@ -501,10 +535,7 @@ def bench_decode(args, w: W.Workload, rank: int, world: int, local: int):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     wall0 = time.time()
     t0.record(stream)
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
+    run_steps(graph, step, args.steps, stream)
     t1.record(stream)
     torch.cuda.synchronize(dev)
     wall1 = time.time()
@@ -512,7 +543,7 @@ def bench_decode(args, w: W.Workload, rank: int, world: int, local: int):
     time.sleep(0.15)
     clocks.stop()
     total_ms = max_over_ranks(t0.elapsed_time(t1), world)
-    per_launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    per_launch_ms = t0.elapsed_time(t1) / args.steps   # one launch per step
     tokens = w.B  # one token per sequence per step
     value = tokens * world * args.steps / (total_ms / 1e3)
 
@@ -563,6 +594,7 @@ def bench_decode(args, w: W.Workload, rank: int, world: int, local: int):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
+        "timing": TIMING_NOTE[args.eager],
         "config": {"workload": w.name, "B": w.B, "T": 1, "H": w.H, "dk": w.dk, "dv": w.dv,
                    "storage": w.dtype, "kernel": "decode",
                    "l2": f"the {w.B * w.H * w.dk * w.dv * 4 / 1e6:.0f} MB state (> 129 MB L2) "
@@ -657,9 +689,9 @@ def bench_diag(args, w: W.DiagWorkload, rank: int, world: int, local: int):
     kname = "diag_" + w.dtype
     stream = torch.cuda.current_stream(dev)
 
-    def call(d):
+    def call(d, s=stream):
         G.gdn_diag_fwd(d["v"], d["b"], d["c"], d["g"], d["A_log"], d["initial_state"],
-                       o=d["o"], final_state=d["final_state"], workspace=ws, stream=stream)
+                       o=d["o"], final_state=d["final_state"], workspace=ws, stream=s)
 
     for i in range(args.warmup):
         call(sets[i & 1])
@@ -667,8 +699,7 @@ def bench_diag(args, w: W.DiagWorkload, rank: int, world: int, local: int):
     st = G.gdn_check(ws, stream)
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {G.status_string(st)}")
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    graph = capture_steps(lambda i, s: call(sets[i & 1], s), args.steps, dev, stream, args.eager)
     clocks = ClockSampler()
     clocks.start()
     time.sleep(0.3)
@@ -677,10 +708,7 @@ def bench_diag(args, w: W.DiagWorkload, rank: int, world: int, local: int):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     wall0 = time.time()
     t0.record(stream)
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        call(sets[i & 1])
-        ev[i][1].record(stream)
+    run_steps(graph, lambda i, s: call(sets[i & 1], s), args.steps, stream)
     t1.record(stream)
     torch.cuda.synchronize(dev)
     wall1 = time.time()
@@ -691,7 +719,7 @@ def bench_diag(args, w: W.DiagWorkload, rank: int, world: int, local: int):
     if st != 0:
         raise RuntimeError(f"device status after timed steps: {G.status_string(st)}")
     total_ms = max_over_ranks(t0.elapsed_time(t1), world)
-    per_launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    per_launch_ms = t0.elapsed_time(t1) / args.steps   # one launch per step
     tokens = w.B * w.T
     value = tokens * world * args.steps / (total_ms / 1e3)
 
@@ -740,6 +768,7 @@ def bench_diag(args, w: W.DiagWorkload, rank: int, world: int, local: int):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "timing": TIMING_NOTE[args.eager],
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "S": w.S, "D": w.D,
                    "storage": w.dtype, "a_log": w.a_log, "kernel": kname,
                    "l2": f"two resident input sets of {in_mb:.0f} MB each alternate between "
@@ -780,14 +809,13 @@ def bench_conv(args, w: W.ConvWorkload, rank: int, world: int, local: int):
     stream = torch.cuda.current_stream(dev)
     kname = "conv_" + w.dtype
 
-    def call(d):
-        G.gdn_conv_silu(d["x"], wd, y=d["y"], stream=stream)
+    def call(d, s=stream):
+        G.gdn_conv_silu(d["x"], wd, y=d["y"], stream=s)
 
     for i in range(args.warmup):
         call(sets[i % nsets])
     torch.cuda.synchronize(dev)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    graph = capture_steps(lambda i, s: call(sets[i % nsets], s), args.steps, dev, stream, args.eager)
     clocks = ClockSampler()
     clocks.start()
     time.sleep(0.3)
@@ -796,10 +824,7 @@ def bench_conv(args, w: W.ConvWorkload, rank: int, world: int, local: int):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     wall0 = time.time()
     t0.record(stream)
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        call(sets[i % nsets])
-        ev[i][1].record(stream)
+    run_steps(graph, lambda i, s: call(sets[i % nsets], s), args.steps, stream)
     t1.record(stream)
     torch.cuda.synchronize(dev)
     wall1 = time.time()
@@ -807,7 +832,7 @@ def bench_conv(args, w: W.ConvWorkload, rank: int, world: int, local: int):
     time.sleep(0.15)
     clocks.stop()
     total_ms = max_over_ranks(t0.elapsed_time(t1), world)
-    per_launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    per_launch_ms = t0.elapsed_time(t1) / args.steps   # one launch per step
     tokens = w.B * w.T
     value = tokens * world * args.steps / (total_ms / 1e3)
     # end to end: pinned x in, y back
@@ -851,6 +876,7 @@ def bench_conv(args, w: W.ConvWorkload, rank: int, world: int, local: int):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
+        "timing": TIMING_NOTE[args.eager],
         "config": {"workload": w.name, "B": w.B, "T": w.T, "C": w.C, "K": w.K,
                    "storage": w.dtype, "kernel": kname,
                    "l2": f"{nsets} resident input/output sets of {2 * nbytes / 1e6:.0f} MB "
@@ -910,9 +936,9 @@ def bench_bwd(args, w: W.Workload, rank: int, world: int, local: int):
              "dh0": torch.empty((N, w.H, w.dk, w.dv), **f32)}
     stream = torch.cuda.current_stream(dev)
 
-    def call():
+    def call(i=0, s=stream):
         G.gdn_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["d_o"], s0, cu, None,
-                  grads=grads, workspace=ws, stream=stream)
+                  grads=grads, workspace=ws, stream=s)
 
     for _ in range(args.warmup):
         call()
@@ -920,6 +946,7 @@ def bench_bwd(args, w: W.Workload, rank: int, world: int, local: int):
     st = G.gdn_check(ws, stream)
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {G.status_string(st)}")
+    graph = capture_steps(call, args.steps, dev, stream, args.eager)
     clocks = ClockSampler()
     clocks.start()
     time.sleep(0.3)
@@ -928,8 +955,7 @@ def bench_bwd(args, w: W.Workload, rank: int, world: int, local: int):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     wall0 = time.time()
     t0.record(stream)
-    for _ in range(args.steps):
-        call()
+    run_steps(graph, call, args.steps, stream)
     t1.record(stream)
     torch.cuda.synchronize(dev)
     wall1 = time.time()
@@ -985,6 +1011,7 @@ def bench_bwd(args, w: W.Workload, rank: int, world: int, local: int):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
+        "timing": TIMING_NOTE[args.eager],
         "config": {"workload": w.name, "pass": "backward", "B": w.B, "T": w.T, "H": w.H,
                    "dk": w.dk, "dv": w.dv, "storage": w.dtype, "kernel": "bwd",
                    "l2": "inputs, d_o and the fp32 gradients (> 129 MB) stream every step",
@@ -1038,6 +1065,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="hymo_bf16",
                     choices=sorted(W.WORKLOADS) + sorted(W.DECODE_WORKLOADS) +
                     sorted(W.DIAG_WORKLOADS) + sorted(W.CONV_WORKLOADS))
+    ap.add_argument("--eager", action="store_true",
+                    help="time the steps launched one by one instead of as one CUDA graph")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
