@@ -175,9 +175,11 @@ gdn_bwd_kernel(const BwdParams P) {
       part[j] = a;
     }
     reduce4(part, s, lane);
+    const float4 vq = *reinterpret_cast<const float4 *>(sV + i * kCols + cw);
+    const float vv[4] = {vq.x, vq.y, vq.z, vq.w};
     float u[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) u[j] = be * (sV[i * kCols + cw + j] - al * s[j]);
+    for (int j = 0; j < 4; ++j) u[j] = be * (vv[j] - al * s[j]);
 #pragma unroll
     for (int r = 0; r < NR; ++r)
 #pragma unroll
@@ -240,29 +242,31 @@ gdn_bwd_kernel(const BwdParams P) {
       }
       __syncwarp();   // s_t, u_t of this warp's columns are in place
 
+      // H_t of the step, carried from the previous (later) step's H_{t-1}
+      float Hc[NR][4];
+#pragma unroll
+      for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) Hc[r][j] = traj[(cnt * L::EL + r * 4 + j) * kBT + tid];
       for (int i = cnt - 1; i >= 0; --i) {
         const float al = sAl[i], be = sBe[i];
-        float kr[NR], qr[NR], dOj[4], vj[4], sj[4], uj[4];
+        float kr[NR], qr[NR];
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
           kr[r] = sK[i * DK + lane + 32 * r];
           qr[r] = sQ[i * DK + lane + 32 * r];
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          dOj[j] = sDO[i * kCols + cw + j];
-          vj[j] = sV[i * kCols + cw + j];
-          sj[j] = sS[i * kCols + cw + j];
-          uj[j] = sU[i * kCols + cw + j];
-        }
-        float Hp[NR][4], Hc[NR][4];   // H_{t-1}, H_t
+        const float4 dq4 = *reinterpret_cast<const float4 *>(sDO + i * kCols + cw);
+        const float4 v4 = *reinterpret_cast<const float4 *>(sV + i * kCols + cw);
+        const float4 s4 = *reinterpret_cast<const float4 *>(sS + i * kCols + cw);
+        const float4 u4 = *reinterpret_cast<const float4 *>(sU + i * kCols + cw);
+        const float dOj[4] = {dq4.x, dq4.y, dq4.z, dq4.w}, vj[4] = {v4.x, v4.y, v4.z, v4.w};
+        const float sj[4] = {s4.x, s4.y, s4.z, s4.w}, uj[4] = {u4.x, u4.y, u4.z, u4.w};
+        float Hp[NR][4];   // H_{t-1}
 #pragma unroll
         for (int r = 0; r < NR; ++r)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            Hp[r][j] = traj[(i * L::EL + r * 4 + j) * kBT + tid];
-            Hc[r][j] = traj[((i + 1) * L::EL + r * 4 + j) * kBT + tid];
-          }
+          for (int j = 0; j < 4; ++j) Hp[r][j] = traj[(i * L::EL + r * 4 + j) * kBT + tid];
         // dH += q do^T;  dq = H_t do
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
@@ -320,6 +324,10 @@ gdn_bwd_kernel(const BwdParams P) {
           }
           atomicAdd(&aK[i * DK + lane + 32 * r], dk);
         }
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) Hc[r][j] = Hp[r][j];
       }
       __syncthreads();   // every warp's sums are in
       // the column sums of this CTA into the fp32 outputs
