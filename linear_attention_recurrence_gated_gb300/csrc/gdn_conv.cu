@@ -14,10 +14,13 @@
 // cover the HBM latency, then produces the 8 outputs.  Consecutive lanes own
 // consecutive vectors, so each warp-wide load or store is 256 or 512
 // contiguous bytes of one token row.
-#include "gdn_internal.cuh"
+#include "gdn_tc_common.cuh"
 
 namespace gdn {
 namespace {
+
+using namespace ptx;
+constexpr uint64_t kConvWaitNs = 2000000000ull;  // bounded TMA waits: 2 s
 
 constexpr int kRun = 8;          // tokens per thread
 constexpr int kConvThreads = 256;
@@ -162,11 +165,236 @@ gdn_conv_silu_kernel(const ConvParams p) {
   }
 }
 
+// ---- two fp32 lanes in one 64-bit register (Blackwell's packed fp32 FMA/MUL/ADD:
+// each lane is an ordinary IEEE fp32 operation) ----
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// silu on a pair: z * rcp(1 + 2^(-z log2 e)), the scale, the 1 + and the
+// final product packed; 2^x and the reciprocal per lane (as in silu above)
+__device__ __forceinline__ void silu2(uint64_t z, float &o0, float &o1) {
+  float t0, t1, e0, e1, r0, r1;
+  upk2(mul2(z, pk2(-1.4426950408889634f, -1.4426950408889634f)), t0, t1);
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(t0));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(t1));
+  float s0, s1;
+  upk2(add2(pk2(e0, e1), pk2(1.f, 1.f)), s0, s1);
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(s0));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(s1));
+  upk2(mul2(z, pk2(r0, r1)), o0, o1);
+}
+
+// ---- TMA-staged variant (token rows of C * sizeof(T) bytes a multiple of 16) ----
+// A persistent CTA owns one block of 32 channel vectors for the whole call and
+// walks (batch row, 64-token) tiles of it.  One thread loads each tile, with
+// its K-1 token halo, as one 3-D TMA box into a shared-memory stage; the box
+// of the next tile is in flight while the current one computes.  Rows before
+// token 0 and past the end, and channels past C, arrive as zeros (the box may
+// start at a negative token coordinate); the prefix rows of a call's first
+// tile are then overwritten from x_prev.
+constexpr int kTileTok = kRun * kVecWarps;   // 64 tokens per tile
+
+template <typename T, int K>
+struct TmaTile {
+  static constexpr int VB = sizeof(typename Vec<T>::Raw);   // bytes per lane vector
+  static constexpr int ROWS = kTileTok + K - 1;              // tile + halo
+  static constexpr int ROWB = 32 * VB;                       // bytes per staged token row
+  static constexpr int STAGE = (ROWS * ROWB + 1023) / 1024 * 1024;
+  static constexpr int NS = 2;                               // stages (3 measured no faster)
+  static constexpr int BYTES = NS * STAGE + 1024;            // + alignment slack
+};
+
+template <typename T, int K>
+__global__ void __launch_bounds__(kConvThreads, kConvBlocks<T>())
+gdn_conv_silu_tma_kernel(const ConvParams p, const __grid_constant__ CUtensorMap tmap_x) {
+  using V = Vec<T>;
+  using TL = TmaTile<T, K>;
+  constexpr int N = V::N, VB = TL::VB, ROWS = TL::ROWS, ROWB = TL::ROWB;
+  extern __shared__ __align__(1024) unsigned char sraw[];
+  unsigned char *sx = sraw + ((1024u - (smem_u32(sraw) & 1023u)) & 1023u);
+  __shared__ __align__(8) uint64_t full_bar[TL::NS];
+  __shared__ int s_fail;
+  const int tid = threadIdx.x, lane = tid & 31, wrp = tid >> 5;
+  const int cbase = blockIdx.x * 32 * N;              // first channel of this CTA
+  const int c0 = cbase + lane * N;                    // first channel of this lane
+  const bool lane_ok = c0 < p.channels;
+  const int C = p.channels, L = p.seq_len;
+  const size_t e = sizeof(T);
+  const int ntb = (L + kTileTok - 1) / kTileTok;
+  const int ntile = ntb * p.batch;
+  const uint32_t bar0 = smem_u32(&full_bar[0]);
+
+  // the CTA's weights, staged tap-major ([K][32 N]) with one coalesced pass
+  __shared__ float4 s_w4[K * 32 * N / 4];
+  float *s_w = reinterpret_cast<float *>(s_w4);
+  for (int i = tid; i < 32 * N * K; i += kConvThreads) {
+    const int ch = i / K, k = i % K;
+    s_w[k * 32 * N + ch] = cbase + ch < C ? __ldg(p.w + (size_t)(cbase + ch) * K + k) : 0.f;
+  }
+  if (tid == 0) {
+    for (int b = 0; b < TL::NS; ++b) mbar_init(bar0 + 8 * b, 1);
+    s_fail = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  float w[K][N];
+#pragma unroll
+  for (int k = 0; k < K; ++k)
+#pragma unroll
+    for (int j4 = 0; j4 < N / 4; ++j4) {
+      const float4 q = s_w4[(k * 32 * N + lane * N) / 4 + j4];
+      w[k][4 * j4] = q.x; w[k][4 * j4 + 1] = q.y; w[k][4 * j4 + 2] = q.z; w[k][4 * j4 + 3] = q.w;
+    }
+  static_assert(N == 4, "two channel pairs per lane vector");
+  uint64_t wp[K][2];   // weights of channel pairs (0,1) and (2,3)
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    wp[k][0] = pk2(w[k][0], w[k][1]);
+    wp[k][1] = pk2(w[k][2], w[k][3]);
+  }
+  auto issue = [&](int tile, int b) {   // one thread
+    const int n = tile / ntb, t0 = (tile % ntb) * kTileTok;
+    mbar_arrive_expect_tx(bar0 + 8 * b, (uint32_t)(ROWS * ROWB));
+    tma_load_3d(smem_u32(sx) + b * TL::STAGE, &tmap_x, cbase, t0 - (K - 1), n, bar0 + 8 * b);
+  };
+
+  constexpr int NS = TL::NS;
+  const int gy = (int)gridDim.y;
+  int tile = blockIdx.y;
+  if (tid == 0)
+    for (int j = 0; j < NS - 1; ++j)
+      if (tile + j * gy < ntile) issue(tile + j * gy, j);
+  for (int it = 0; tile < ntile; ++it, tile += gy) {
+    const int b = it % NS;
+    // the box NS-1 tiles ahead goes to the stage every thread finished reading
+    // before the barrier that closed the previous iteration
+    const bool ahead = tile + (NS - 1) * gy < ntile;
+    if (tid == 0 && ahead) issue(tile + (NS - 1) * gy, (it + NS - 1) % NS);
+    if (!mbar_wait_bounded(bar0 + 8 * b, (it / NS) & 1, kConvWaitNs)) s_fail = 1;
+    const int n = tile / ntb, tt0 = (tile % ntb) * kTileTok;
+    unsigned char *st = sx + b * TL::STAGE;
+    // a sequence's first tile: the K-1 rows before token 0 from the prefix
+    if (tt0 == 0 && p.x_prev && lane_ok && wrp < K - 1)
+      *reinterpret_cast<typename V::Raw *>(st + wrp * ROWB + lane * VB) =
+          *reinterpret_cast<const typename V::Raw *>(
+              static_cast<const unsigned char *>(p.x_prev) +
+              (((size_t)n * (K - 1) + wrp) * C + c0) * e);
+    __syncthreads();
+    if (s_fail) {   // a box never arrived: leave after the ones still in flight
+      if (tid == 0)
+        for (int j = 1; j < NS; ++j)
+          if (tile + j * gy < ntile)
+            mbar_wait_bounded(bar0 + 8 * ((it + j) % NS), ((it + j) / NS) & 1, kConvWaitNs);
+      break;
+    }
+    const int t0 = tt0 + wrp * kRun;
+    if (lane_ok && t0 < L) {
+      const unsigned char *rb = st + wrp * kRun * ROWB + lane * VB;
+      constexpr int R = kRun + K - 1;
+      uint64_t xp[R][2];   // channel pairs of x[t0 - (K - 1) + r]
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        float f[N];
+        V::unpack(*reinterpret_cast<const typename V::Raw *>(rb + r * ROWB), f);
+        xp[r][0] = pk2(f[0], f[1]);
+        xp[r][1] = pk2(f[2], f[3]);
+      }
+      const int t_end = t0 + kRun < L ? t0 + kRun : L;
+      const size_t rstride = (size_t)C * e;
+      unsigned char *yb = static_cast<unsigned char *>(p.y) + (((size_t)n * L + t0) * C + c0) * e;
+#pragma unroll
+      for (int q = 0; q < kRun; ++q) {
+        float out[N];
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {
+          uint64_t a = mul2(wp[0][pr], xp[q][pr]);
+#pragma unroll
+          for (int k = 1; k < K; ++k) a = fma2(wp[k][pr], xp[q + k][pr], a);
+          silu2(a, out[2 * pr], out[2 * pr + 1]);
+        }
+        if (t0 + q < t_end) V::store(yb + q * rstride, out);
+      }
+      // the last K-1 inputs (prefix of the next call), by the warp whose run
+      // ends at the last token: input t_end - (K-1) + k is row t_end - t0 + k
+      if (p.x_tail && t_end == L) {
+#pragma unroll
+        for (int k = 0; k < K - 1; ++k)
+          *reinterpret_cast<typename V::Raw *>(static_cast<unsigned char *>(p.x_tail) +
+                                               (((size_t)n * (K - 1) + k) * C + c0) * e) =
+              *reinterpret_cast<const typename V::Raw *>(rb + (t_end - t0 + k) * ROWB);
+      }
+    }
+    // every thread is done with this stage (and its prefix rows, written by
+    // the generic proxy) before a box is issued into it again
+    fence_proxy_async_smem();
+    __syncthreads();
+  }
+}
+
+// x as a [batch][tokens][channels] tensor map; box = 32 lane vectors x (64 + K - 1) tokens x 1 row.
+template <typename T, int K>
+bool make_conv_tmap(CUtensorMap *m, const ConvParams &p) {
+  tc::EncodeTiledFn enc = tc::encode_fn();
+  const size_t e = sizeof(T);
+  if (!enc || ((size_t)p.channels * e) % 16 != 0) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)p.channels, (cuuint64_t)p.seq_len, (cuuint64_t)p.batch};
+  const cuuint64_t strides[2] = {(cuuint64_t)p.channels * e, (cuuint64_t)p.channels * e * p.seq_len};
+  const cuuint32_t box[3] = {(cuuint32_t)(32 * Vec<T>::N), (cuuint32_t)TmaTile<T, K>::ROWS, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+             const_cast<void *>(p.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename T, int K>
 cudaError_t launch_k(const ConvParams &p, cudaStream_t s) {
   constexpr int N = Vec<T>::N;
-  const dim3 grid((p.channels / N + 31) / 32, (p.seq_len + kRun * kVecWarps - 1) / (kRun * kVecWarps),
-                  p.batch);
+  const int cblocks = (p.channels / N + 31) / 32;
+  CUtensorMap tm;
+  if (make_conv_tmap<T, K>(&tm, p)) {
+    // TMA-staged persistent kernel: one wave of kConvBlocks CTAs per SM
+    static int sms = 0;
+    if (sms == 0) {
+      int dev = 0, v = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+        return cudaErrorInvalidDevice;
+      sms = v;
+    }
+    using TL = TmaTile<T, K>;
+    cudaError_t err = cudaFuncSetAttribute(gdn_conv_silu_tma_kernel<T, K>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, TL::BYTES);
+    if (err != cudaSuccess) return err;
+    const int64_t ntile = (int64_t)((p.seq_len + kTileTok - 1) / kTileTok) * p.batch;
+    int64_t per = ((int64_t)sms * kConvBlocks<T>() + cblocks - 1) / cblocks;
+    if (per > ntile) per = ntile;
+    if (per > 65535) per = 65535;
+    gdn_conv_silu_tma_kernel<T, K><<<dim3(cblocks, (unsigned)per, 1), kConvThreads, TL::BYTES, s>>>(p, tm);
+    return cudaGetLastError();
+  }
+  // token rows not 16-byte multiples: one 8-token run per warp, loads from registers
+  const dim3 grid(cblocks, (p.seq_len + kRun * kVecWarps - 1) / (kRun * kVecWarps), p.batch);
   gdn_conv_silu_kernel<T, K><<<grid, kConvThreads, 0, s>>>(p);
   return cudaGetLastError();
 }

@@ -29,8 +29,10 @@ def _conv_inputs(B, T, C, K, dtype, seed, prefix):
     return x, w, xp
 
 
+# C = 12 in bf16 (24-byte token rows) takes the kernel that loads through
+# registers; every other case the TMA-staged one
 CONV_CASES = [(1, 1, 8, 4), (2, 3, 16, 4), (1, 31, 40, 4), (2, 33, 1280, 4), (1, 257, 64, 3),
-              (1, 100, 24, 2), (1, 50, 8, 1), (3, 600, 136, 4)]
+              (1, 100, 24, 2), (1, 50, 8, 1), (3, 600, 136, 4), (2, 130, 12, 4), (1, 70, 12, 3)]
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
