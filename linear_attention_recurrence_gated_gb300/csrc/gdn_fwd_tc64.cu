@@ -133,6 +133,37 @@ enum : int {
   B_P_FREE = 29,     // [3]  P buffer read by MMA2 (commit)
 };
 
+// Two fp32 lanes in one 64-bit register: Blackwell's packed FMA/MUL/ADD run two
+// ordinary IEEE fp32 operations per instruction (used in the carry drains).
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(uint64_t v) {
+  float lo, hi;
+  upk2(v, lo, hi);
+  return pack_bf16(lo, hi);
+}
+
 // One thread drains one row i of a 64-column fp32 accumulator of [Q; K] K^T
 // (taddr: this warp's TMEM lane quarter at the buffer's first column) into a
 // masked, decayed row of P (bf16, swizzled tile at Ps) or of A (fp32, into the blocks at Ablk):
@@ -669,6 +700,7 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
           pu_free = mbar_test(bar(B_PU_FREE + buf), ((c >> 1) - 1) & 1);
         const uint32_t Ut = slot_base(slot) + L::SV;  // U~ (written over V by prep)
         const float dj = gate[64 + row];
+        const uint64_t dj2 = pk2(dj, dj);
         {
           uint32_t w[32];
           tmem_ld32(tm(kColD1 + buf * 64 + cb), w);
@@ -682,10 +714,11 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
             uint32_t pu[4], pd[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float u0 = bf16_lo(x[e]) - __uint_as_float(w[8 * q + 2 * e]);
-              const float u1 = bf16_hi(x[e]) - __uint_as_float(w[8 * q + 2 * e + 1]);
-              pu[e] = pack_bf16(u0, u1);
-              pd[e] = pack_bf16(u0 * dj, u1 * dj);
+              const uint64_t u = sub2(pk2(bf16_lo(x[e]), bf16_hi(x[e])),
+                                      pk2(__uint_as_float(w[8 * q + 2 * e]),
+                                          __uint_as_float(w[8 * q + 2 * e + 1])));
+              pu[e] = pack_bf16x2(u);
+              pd[e] = pack_bf16x2(mul2(u, dj2));
             }
             S4(tile_addr(Ust, row, cb + 8 * q)) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
             S4(tile_addr(Uds, row, cb + 8 * q)) = make_uint4(pd[0], pd[1], pd[2], pd[3]);
@@ -752,6 +785,7 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
         tc_fence_after();
         {
           const float gi = ex2(gate[row]);  // gamma_i
+          const uint64_t gi2 = pk2(gi, gi);
           __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) +
                                 ((size_t)(start + (int64_t)c * 64 + row) * H + h) * dv + col0;
 #pragma unroll 1
@@ -763,8 +797,8 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
             uint32_t w8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              w8[e] = pack_bf16(fmaf(gi, __uint_as_float(a[2 * e]), __uint_as_float(b[2 * e])),
-                                fmaf(gi, __uint_as_float(a[2 * e + 1]), __uint_as_float(b[2 * e + 1])));
+              w8[e] = pack_bf16x2(fma2(gi2, pk2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1])),
+                                       pk2(__uint_as_float(b[2 * e]), __uint_as_float(b[2 * e + 1]))));
             if (row < valid) {
               reinterpret_cast<uint4 *>(orow + 16 * q2)[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
               reinterpret_cast<uint4 *>(orow + 16 * q2)[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
@@ -831,8 +865,11 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
           uint32_t w[32];
           tmem_ld32(tm(kColH + cb), w);
           tmem_wait_ld();
+          const uint64_t gC2 = pk2(gC, gC);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) hrow[j] = fmaf(gC, hrow[j], __uint_as_float(w[j]));
+          for (int j = 0; j < 32; j += 2)
+            upk2(fma2(gC2, pk2(hrow[j], hrow[j + 1]), pk2(__uint_as_float(w[j]), __uint_as_float(w[j + 1]))),
+                 hrow[j], hrow[j + 1]);
         }
         tc_fence_before();
         store_seg(Hs, hrow);
