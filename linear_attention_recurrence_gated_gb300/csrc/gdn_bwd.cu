@@ -43,6 +43,7 @@ struct BwdParams {
   const float *dHN;
   const float *ckpt;
   float *scratch;           // per CTA: the sub-chunk start states of one chunk
+  int sub_ckpt;             // checkpoints per 64-token chunk: 8 (every sub-chunk) or 1
   float *dq, *dk, *dv, *dg, *dbeta, *dh0;
 };
 
@@ -203,25 +204,26 @@ gdn_bwd_kernel(const BwdParams P) {
     const int clen = (int)(len - cs < kCk ? len - cs : kCk);
     const int nsub = (clen + kSub - 1) / kSub;
 
-    // (a) from the chunk's checkpoint, the state at each sub-chunk start
+    // (a) from the chunk's checkpoint, the state at each sub-chunk start (when
+    // the scan kept only one checkpoint per chunk)
     float Hr[NR][4];
-    {
+    if (P.sub_ckpt == 1) {
       const float *ck = P.ckpt + ((ck0 + c) * H + h) * (size_t)DK * dv + col0 + cw;
 #pragma unroll
       for (int r = 0; r < NR; ++r)
 #pragma unroll
         for (int j = 0; j < 4; ++j) Hr[r][j] = ck[(size_t)(lane + 32 * r) * dv + j];
-    }
-    for (int sb = 0; sb < nsub; ++sb) {
+      for (int sb = 0; sb < nsub; ++sb) {
 #pragma unroll
-      for (int r = 0; r < NR; ++r)
+        for (int r = 0; r < NR; ++r)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) scr[((size_t)sb * L::EL + r * 4 + j) * kBT + tid] = Hr[r][j];
-      if (sb == nsub - 1) break;
-      __syncthreads();   // shared buffers free
-      load_sub(cs + (int64_t)sb * kSub, kSub, false);
-      __syncthreads();
-      for (int i = 0; i < kSub; ++i) fwd_step(Hr, i);
+          for (int j = 0; j < 4; ++j) scr[((size_t)sb * L::EL + r * 4 + j) * kBT + tid] = Hr[r][j];
+        if (sb == nsub - 1) break;
+        __syncthreads();   // shared buffers free
+        load_sub(cs + (int64_t)sb * kSub, kSub, false);
+        __syncthreads();
+        for (int i = 0; i < kSub; ++i) fwd_step(Hr, i);
+      }
     }
 
     // (b) sub-chunks in reverse: recompute their states, then step backwards
@@ -230,10 +232,19 @@ gdn_bwd_kernel(const BwdParams P) {
       const int cnt = (int)(clen - sb * kSub < kSub ? clen - sb * kSub : kSub);
       __syncthreads();   // shared buffers free (previous flush done)
       load_sub(t0, cnt, true);
+      if (P.sub_ckpt == 8) {   // the scan's checkpoint of this sub-chunk
+        const float *ck = P.ckpt + (((ck0 + c) * 8 + sb) * H + h) * (size_t)DK * dv + col0 + cw;
 #pragma unroll
-      for (int r = 0; r < NR; ++r)
+        for (int r = 0; r < NR; ++r) {
+          const float4 x = *reinterpret_cast<const float4 *>(ck + (size_t)(lane + 32 * r) * dv);
+          Hr[r][0] = x.x; Hr[r][1] = x.y; Hr[r][2] = x.z; Hr[r][3] = x.w;
+        }
+      } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) Hr[r][j] = scr[((size_t)sb * L::EL + r * 4 + j) * kBT + tid];
+        for (int r = 0; r < NR; ++r)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) Hr[r][j] = scr[((size_t)sb * L::EL + r * 4 + j) * kBT + tid];
+      }
       __syncthreads();
       traj_put(0, Hr);
       for (int i = 0; i < cnt; ++i) {
@@ -352,16 +363,17 @@ gdn_bwd_kernel(const BwdParams P) {
   }
 }
 
-// Forward scan that keeps the state entering every 64-token chunk: the
-// checkpoints the backward kernel restarts from.  Token by token in fp32 --
-// the recurrence as written, the same step as the backward's recompute -- with
-// the CTA and warp layout of the backward kernel: a CTA owns 32 value columns
-// of one (sequence, head), each warp 4 of them with the key rows over the
-// lanes, and the tokens are staged a chunk at a time in shared memory.  The
-// last chunk's tokens are not scanned: no checkpoint follows them.
+// Forward scan that keeps the checkpoints the backward kernel restarts from:
+// the state entering every 64-token chunk (sub_ckpt = 1) or every 8-token
+// sub-chunk (sub_ckpt = 8, slot (chunk slot) * 8 + sub-chunk).  Token by token
+// in fp32 -- the recurrence as written, the same step as the backward's
+// recompute -- with the CTA and warp layout of the backward kernel: a CTA owns
+// 32 value columns of one (sequence, head), each warp 4 of them with the key
+// rows over the lanes, and the tokens are staged a chunk at a time in shared
+// memory.  Tokens after the last checkpoint are not scanned.
 template <int DK, typename Tin>
 __global__ void __launch_bounds__(kBT)
-gdn_bwd_ckpt_kernel(const FwdParams p) {
+gdn_bwd_ckpt_kernel(const FwdParams p, const int sub_ckpt) {
   constexpr int NR = DK / 32;
   __shared__ float sK[kCk * DK];
   __shared__ float sV[kCk * kCols];
@@ -384,34 +396,40 @@ gdn_bwd_ckpt_kernel(const FwdParams p) {
     if (p.s0) x = *reinterpret_cast<const float4 *>(p.s0 + state_base + (size_t)(lane + 32 * r) * dv);
     Hr[r][0] = x.x; Hr[r][1] = x.y; Hr[r][2] = x.z; Hr[r][3] = x.w;
   }
-  const int64_t ck0 = ckpt_first_slot(n, start, p.seq_len, p.cu != nullptr);
-  const int nck = (int)((len + kCk - 1) / kCk);
-  for (int c = 0; c < nck; ++c) {
-    float *ck = p.ckpt + ((ck0 + c) * H + h) * (size_t)DK * dv + col0 + cw;
+  auto put = [&](int64_t slot) {
+    float *ck = p.ckpt + (slot * H + h) * (size_t)DK * dv + col0 + cw;
 #pragma unroll
     for (int r = 0; r < NR; ++r)
       *reinterpret_cast<float4 *>(ck + (size_t)(lane + 32 * r) * dv) =
           make_float4(Hr[r][0], Hr[r][1], Hr[r][2], Hr[r][3]);
-    if (c == nck - 1) break;
+  };
+  const int64_t ck0 = ckpt_first_slot(n, start, p.seq_len, p.cu != nullptr);
+  const int nck = (int)((len + kCk - 1) / kCk);
+  for (int c = 0; c < nck; ++c) {
     const int64_t t0 = (int64_t)c * kCk;
+    const int clen = (int)(len - t0 < kCk ? len - t0 : kCk);
+    put((ck0 + c) * sub_ckpt);
+    // tokens to scan in this chunk: up to the next checkpoint that exists
+    const int cnt = c < nck - 1 ? kCk : (sub_ckpt == 8 ? ((clen - 1) / kSub) * kSub : 0);
+    if (cnt == 0) break;
     __syncthreads();   // the previous chunk's tokens are consumed
-    for (int idx = tid; idx < kCk * DK; idx += kBT) {
+    for (int idx = tid; idx < cnt * DK; idx += kBT) {
       const int i = idx / DK, d = idx % DK;
       sK[idx] = to_f32(k[((size_t)(start + t0 + i) * H + h) * DK + d]);
     }
-    for (int idx = tid; idx < kCk * kCols; idx += kBT) {
+    for (int idx = tid; idx < cnt * kCols; idx += kBT) {
       const int i = idx / kCols, cc = idx % kCols;
       sV[idx] = to_f32(v[((size_t)(start + t0 + i) * H + h) * dv + col0 + cc]);
     }
-    if (tid < kCk) {
+    if (tid < cnt) {
       const size_t off = (size_t)(start + t0 + tid) * H + h;
       sAl[tid] = expf(p.g[off]);
       sBe[tid] = to_f32(beta[off]);
     }
     __syncthreads();
-    // every chunk but the last is full: 64 steps
 #pragma unroll 1
-    for (int i = 0; i < kCk; ++i) {
+    for (int i = 0; i < cnt; ++i) {
+      if (sub_ckpt == 8 && i > 0 && (i & (kSub - 1)) == 0) put((ck0 + c) * 8 + i / kSub);
       const float al = sAl[i], be = sBe[i];
       float kr[NR], part[4], sv[4];
 #pragma unroll
@@ -432,22 +450,27 @@ gdn_bwd_ckpt_kernel(const FwdParams p) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) Hr[r][j] = fmaf(al, Hr[r][j], kr[r] * u[j]);
     }
+    // the last sub-chunk start of a short final chunk follows its last scanned token
+    if (sub_ckpt == 8 && c == nck - 1) {
+      put((ck0 + c) * 8 + cnt / kSub);
+      break;
+    }
   }
 }
 
 template <int DK, typename Tin>
-cudaError_t launch_ckpt_dk(const FwdParams &f, cudaStream_t s) {
+cudaError_t launch_ckpt_dk(const FwdParams &f, int per_chunk, cudaStream_t s) {
   const dim3 grid(f.dv / kCols, f.num_heads, f.num_seqs);
-  gdn_bwd_ckpt_kernel<DK, Tin><<<grid, kBT, 0, s>>>(f);
+  gdn_bwd_ckpt_kernel<DK, Tin><<<grid, kBT, 0, s>>>(f, per_chunk);
   return cudaGetLastError();
 }
 
 template <typename Tin>
-cudaError_t launch_ckpt_t(const FwdParams &f, cudaStream_t s) {
+cudaError_t launch_ckpt_t(const FwdParams &f, int per_chunk, cudaStream_t s) {
   switch (f.dk) {
-    case 32: return launch_ckpt_dk<32, Tin>(f, s);
-    case 64: return launch_ckpt_dk<64, Tin>(f, s);
-    case 128: return launch_ckpt_dk<128, Tin>(f, s);
+    case 32: return launch_ckpt_dk<32, Tin>(f, per_chunk, s);
+    case 64: return launch_ckpt_dk<64, Tin>(f, per_chunk, s);
+    case 128: return launch_ckpt_dk<128, Tin>(f, per_chunk, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -474,6 +497,14 @@ cudaError_t launch_bwd_t(const BwdParams &P, cudaStream_t s) {
   }
 }
 
+// Checkpoints per 64-token chunk: one at every sub-chunk start while that
+// array stays within 4 GiB (the backward then skips recomputing the sub-chunk
+// starts), else one per chunk.
+int ckpt_per_chunk(int64_t num_seqs, int64_t seq_len, int64_t H, int64_t dk, int64_t dv) {
+  const int64_t fine = ckpt_slots(num_seqs, seq_len) * (kCk / kSub) * H * dk * dv * 4;
+  return fine <= (int64_t(4) << 30) ? kCk / kSub : 1;
+}
+
 size_t scratch_floats(int64_t num_seqs, int64_t H, int64_t dk, int64_t dv) {
   return (size_t)num_seqs * H * (dv / kCols) * (kCk / kSub) * (size_t)(dk / 32 * 4 * kBT);
 }
@@ -494,7 +525,9 @@ extern "C" size_t gdn_bwd_workspace_size(int32_t num_seqs, int32_t seq_len, int3
   if (num_seqs <= 0 || seq_len <= 0 || num_heads <= 0 || head_dim_k <= 0 || head_dim_v <= 0)
     return 0;
   if (head_dim_v % kCols) return 0;
-  const size_t ck = (size_t)ckpt_slots(num_seqs, seq_len) * num_heads * head_dim_k * head_dim_v;
+  const int per = ckpt_per_chunk(num_seqs, seq_len, num_heads, head_dim_k, head_dim_v);
+  const size_t ck =
+      (size_t)ckpt_slots(num_seqs, seq_len) * per * num_heads * head_dim_k * head_dim_v;
   return kStatusBytes + 4 * (ck + scratch_floats(num_seqs, num_heads, head_dim_k, head_dim_v));
 }
 
@@ -552,7 +585,8 @@ extern "C" gdn_status gdn_bwd(const void *q, const void *k, const void *v, const
   cudaStream_t s = (cudaStream_t)stream;
   unsigned char *ws = static_cast<unsigned char *>(workspace);
   float *ckpt = reinterpret_cast<float *>(ws + kStatusBytes);
-  float *scratch = ckpt + (size_t)ckpt_slots(num_seqs, seq_len) * num_heads * head_dim_k *
+  const int per = ckpt_per_chunk(num_seqs, seq_len, num_heads, head_dim_k, head_dim_v);
+  float *scratch = ckpt + (size_t)ckpt_slots(num_seqs, seq_len) * per * num_heads * head_dim_k *
                               head_dim_v;
 
   // the gradients gathered with atomics start from zero
@@ -571,11 +605,13 @@ extern "C" gdn_status gdn_bwd(const void *q, const void *k, const void *v, const
   f.seq_len = seq_len;
   f.num_heads = num_heads; f.dk = head_dim_k; f.dv = head_dim_v; f.num_seqs = num_seqs;
   f.flags = 0;
-  // the forward as a token-serial fp32 scan, keeping only the chunk-start states
-  cudaError_t err = dtype == GDN_F32 ? launch_ckpt_t<float>(f, s) : launch_ckpt_t<__nv_bfloat16>(f, s);
+  // the forward as a token-serial fp32 scan, keeping only the checkpoints
+  cudaError_t err = dtype == GDN_F32 ? launch_ckpt_t<float>(f, per, s)
+                                     : launch_ckpt_t<__nv_bfloat16>(f, per, s);
   if (err != cudaSuccess) return GDN_ERR_CUDA;
   f.ckpt = nullptr;
   P.dO = d_o; P.dHN = d_final_state; P.ckpt = ckpt; P.scratch = scratch;
+  P.sub_ckpt = per;
   P.dq = dq; P.dk = dk; P.dv = dv; P.dg = dg; P.dbeta = dbeta; P.dh0 = d_initial_state;
   err = dtype == GDN_F32 ? launch_bwd_t<float>(P, s) : launch_bwd_t<__nv_bfloat16>(P, s);
   return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

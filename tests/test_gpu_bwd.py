@@ -104,3 +104,30 @@ def test_bwd_full_size_sampled():
         for n in ("dq", "dk", "dv", "dg", "dbeta"):
             assert rel(gpu[n][b:b + 1, :, h:h + 1], ref[n]) <= GRAD_TOL, (n, b, h)
         assert rel(gpu["dh0"][b:b + 1, h:h + 1], ref["dh0"]) <= GRAD_TOL, ("dh0", b, h)
+
+
+def test_bwd_chunk_checkpoints_only():
+    """Many heads (B=1, T=130, H=4096, dk=dv=128, bf16): the 8-token checkpoints
+    would take more than 4 GiB, so the workspace holds one state per 64-token
+    chunk and the backward recomputes the sub-chunk starts.  The oracle runs on
+    sampled heads."""
+    B, T, H, dk, dv = 1, 130, 4096, 128, 128
+    fine = 3 * 8 * H * dk * dv * 4     # 3 chunks x 8 sub-chunk states
+    assert G.gdn_bwd_workspace_size(B, T, H, dk, dv) < fine
+    w = W.custom(B=B, T=T, H=H, dk=dk, dv=dv, dtype="bf16", gate_scale=1.0, init_state=True,
+                 seed=57)
+    inp = W.generate(w)
+    d_o, dhN = _upstream(inp, 58, True)
+    gr = G.gdn_bwd(_dev(inp["q"]), _dev(inp["k"]), _dev(inp["v"]), _dev(inp["g"]),
+                   _dev(inp["beta"]), _dev(d_o), _dev(inp["initial_state"]), None, _dev(dhN),
+                   check=True)
+    torch.cuda.synchronize()
+    for h in (0, 1234, 4095):
+        one = {n: inp[n][:, :, h:h + 1].contiguous() for n in ("q", "k", "v", "g", "beta")}
+        one.update(initial_state=inp["initial_state"][:, h:h + 1].contiguous(), cu_seqlens=None)
+        ref = _ref(one, d_o[:, :, h:h + 1].contiguous(), dhN[:, h:h + 1].contiguous())
+        for n in ("dq", "dk", "dv", "dg", "dbeta"):
+            got = gr[n][:, :, h:h + 1].double().cpu().numpy()
+            assert rel(got, ref[n]) <= GRAD_TOL, (n, h)
+        got = gr["dh0"][:, h:h + 1].double().cpu().numpy()
+        assert rel(got, ref["dh0"]) <= GRAD_TOL, ("dh0", h)
