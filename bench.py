@@ -908,6 +908,13 @@ def bwd_bytes(w: W.Workload, tokens: int, N: int) -> float:
     return float(tokens * w.H * per + 4 * w.dk * w.dv * N * w.H)
 
 
+# kernels per gdn_bwd call: (count, what they are), by path
+BWD_LAUNCHES = {
+    False: (2, "4 zero fills, the checkpoint scan, the backward"),
+    True: (4, "chunked: prep, forward state chain, reverse chain, gradients"),
+}
+
+
 def bench_bwd(args, w: W.Workload, rank: int, world: int, local: int):
     """The backward pass (gdn_bwd) on a forward workload, one call per step."""
     from linear_attention_recurrence_gated_gb300 import gdn as G
@@ -997,6 +1004,7 @@ def bench_bwd(args, w: W.Workload, rank: int, world: int, local: int):
         return 0
     hbm_gbs, _, peak_src = measured_peaks()
     alg = bwd_bytes(w, tokens, N)
+    chunked = w.dtype == "bf16" and w.dk <= 64 and w.dv <= 64
     achieved = alg / (per_ms / 1e3) / 1e9
     # CPU baseline: the autograd oracle on one head of one batch row
     import oracle.grad
@@ -1021,14 +1029,14 @@ def bench_bwd(args, w: W.Workload, rank: int, world: int, local: int):
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": alg, "kernel_ms": per_ms,
-                     "launches_per_step": "4 zero fills, the checkpoint scan, the backward"},
+                     "launches_per_step": BWD_LAUNCHES[chunked][1]},
         "cpu_baseline": {"value": w.T / cpu_secs / w.H, "unit": UNIT, "cores": 1,
                          "kind": "oracle",
                          "sample": f"one head of one batch row ({w.T} tokens), torch.autograd "
                                    f"fp64 oracle, {cpu_secs:.1f} s; value scaled to {w.H} heads"},
         "e2e": {"value": tokens * world * e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": args.steps * 2,
+        "gpu_launches": args.steps * BWD_LAUNCHES[chunked][0],
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

@@ -517,6 +517,13 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 }
 
 }  // namespace
+
+// The chunked tensor-core backward for bf16 storage (gdn_bwd_chunk.cu).
+bool bwd_chunked_supported(int dk, int dv);
+size_t bwd_chunked_ws_bytes(int64_t units, int dk, int dv);
+cudaError_t launch_bwd_chunked(const FwdParams &f, const void *dO, const float *dHN, float *dq,
+                               float *dk, float *dv, float *dg, float *dbeta, float *dh0,
+                               void *ws, int64_t slots, cudaStream_t s);
 }  // namespace gdn
 
 extern "C" size_t gdn_bwd_workspace_size(int32_t num_seqs, int32_t seq_len, int32_t num_heads,
@@ -528,7 +535,14 @@ extern "C" size_t gdn_bwd_workspace_size(int32_t num_seqs, int32_t seq_len, int3
   const int per = ckpt_per_chunk(num_seqs, seq_len, num_heads, head_dim_k, head_dim_v);
   const size_t ck =
       (size_t)ckpt_slots(num_seqs, seq_len) * per * num_heads * head_dim_k * head_dim_v;
-  return kStatusBytes + 4 * (ck + scratch_floats(num_seqs, num_heads, head_dim_k, head_dim_v));
+  size_t need = kStatusBytes + 4 * (ck + scratch_floats(num_seqs, num_heads, head_dim_k, head_dim_v));
+  // bf16 storage with small heads takes the chunked path, with its own records
+  if (bwd_chunked_supported(head_dim_k, head_dim_v)) {
+    const size_t chunked = kStatusBytes + bwd_chunked_ws_bytes(
+        ckpt_slots(num_seqs, seq_len) * num_heads, head_dim_k, head_dim_v);
+    if (chunked > need) need = chunked;
+  }
+  return need;
 }
 
 extern "C" gdn_status gdn_bwd(const void *q, const void *k, const void *v, const float *g,
@@ -584,6 +598,26 @@ extern "C" gdn_status gdn_bwd(const void *q, const void *k, const void *v, const
 
   cudaStream_t s = (cudaStream_t)stream;
   unsigned char *ws = static_cast<unsigned char *>(workspace);
+
+  BwdParams P;
+  FwdParams &f = P.f;
+  f.q = q; f.k = k; f.v = v; f.beta = beta; f.g = g;
+  f.s0 = initial_state; f.cu = cu_seqlens; f.o = nullptr; f.sN = nullptr;
+  f.status = reinterpret_cast<DeviceStatus *>(ws);
+  f.ckpt = nullptr;
+  f.seq_len = seq_len;
+  f.num_heads = num_heads; f.dk = head_dim_k; f.dv = head_dim_v; f.num_seqs = num_seqs;
+  f.flags = 0;
+
+  // bf16 storage, head_dim_k and head_dim_v up to 64: the chunked backward,
+  // which writes every gradient once (no zero fills, no atomics)
+  if (dtype == GDN_BF16 && bwd_chunked_supported(head_dim_k, head_dim_v)) {
+    const cudaError_t err = launch_bwd_chunked(
+        f, d_o, d_final_state, dq, dk, dv, dg, dbeta, d_initial_state, ws + kStatusBytes,
+        ckpt_slots(num_seqs, seq_len), s);
+    return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  }
+
   float *ckpt = reinterpret_cast<float *>(ws + kStatusBytes);
   const int per = ckpt_per_chunk(num_seqs, seq_len, num_heads, head_dim_k, head_dim_v);
   float *scratch = ckpt + (size_t)ckpt_slots(num_seqs, seq_len) * per * num_heads * head_dim_k *
@@ -596,15 +630,7 @@ extern "C" gdn_status gdn_bwd(const void *q, const void *k, const void *v, const
       cudaMemsetAsync(dbeta, 0, rows * 4, s) != cudaSuccess)
     return GDN_ERR_CUDA;
 
-  BwdParams P;
-  FwdParams &f = P.f;
-  f.q = q; f.k = k; f.v = v; f.beta = beta; f.g = g;
-  f.s0 = initial_state; f.cu = cu_seqlens; f.o = nullptr; f.sN = nullptr;
-  f.status = reinterpret_cast<DeviceStatus *>(ws);
   f.ckpt = ckpt;
-  f.seq_len = seq_len;
-  f.num_heads = num_heads; f.dk = head_dim_k; f.dv = head_dim_v; f.num_seqs = num_seqs;
-  f.flags = 0;
   // the forward as a token-serial fp32 scan, keeping only the checkpoints
   cudaError_t err = dtype == GDN_F32 ? launch_ckpt_t<float>(f, per, s)
                                      : launch_ckpt_t<__nv_bfloat16>(f, per, s);

@@ -1,0 +1,870 @@
+// Chunked backward of the gated delta rule for bf16 storage (head_dim_k and
+// head_dim_v up to 64), on warp-level bf16 tensor-core products with fp32
+// accumulation.  The pages' kernel ships a recompute-style backward
+// ("Optimization Quartet", Triton GDN kernel section 3.4); this one works in
+// the chunked WY form of the forward (chunk size 64, "v1.0 Architecture &
+// Design Spec" section 2.3), so that everything but two short state chains is
+// parallel over chunks.
+//
+// Per chunk, with H the state entering it (dk x dv, H = S^T), G the chunk-local
+// prefix sum of the log-gates, gamma = exp(G), Gamma_ij = exp(G_i - G_j),
+// dec_i = exp(G_C - G_i), K~ = diag(dec) K and T = (I + A)^-1:
+//   A  = strictly_lower(diag(beta) K K^T (.) Gamma)     P = (Q K^T (.) Gamma)_{i>=j}
+//   W  = T diag(beta gamma) K      U~ = T diag(beta) V      U = U~ - W H
+//   O  = diag(gamma) Q H + P U     H' = gamma_C H + K~^T U
+// Its reverse, with dH' the gradient of the state leaving the chunk:
+//   dU = P^T dO + K~ dH'           dH = gamma_C dH' + Q^T diag(gamma) dO - W^T dU
+//   dP = (dO U^T)_{i>=j}           dQ = diag(gamma) dO H^T + (dP (.) Gamma) K
+//   dK~ = U dH'^T                  dW = -dU H^T
+//   dR_W = T^T dW,  dR_U = T^T dU  (R_W = diag(beta gamma) K, R_U = diag(beta) V)
+//   dV = diag(beta) dR_U           dA = -(dR_W W^T + dR_U U~^T), strictly lower
+//   dK = diag(dec) dK~ + diag(beta gamma) dR_W + S K + (dP (.) Gamma)^T Q,
+//        S = diag(beta) D + D^T diag(beta),  D = dA (.) Gamma
+// and the gate gradient collects, per token, the terms through gamma, Gamma,
+// dec and gamma_C, then sums them over later tokens of the chunk (G is a
+// prefix sum).
+//
+// Four kernels:
+//   prep   (per chunk and head)  A, T (fp32 substitution), W, U~, K~, and the
+//          state-free products dO^T P and dO^T diag(gamma) Q of the reverse chain;
+//   chain  (per sequence and head, forward)  H at every chunk start;
+//   chain  (per sequence and head, reverse)  dH' at every chunk end and the
+//          gradient of the initial state;
+//   grad   (per chunk and head)  dq, dk, dv, dg, dbeta of the chunk.
+// dU and dW enter T^T dU and T^T dW as two bf16 operands each (the rounded
+// value and what the rounding left out), so that the diagonal of T (exactly 1)
+// passes them on at nearly fp32 precision: dbeta and dv sum over them.
+// The chains keep their state in the MMA accumulator registers of the warps
+// (16 value columns per warp, transposed, so that an accumulator is directly
+// the A operand of the next product).  No kernel waits on another CTA.
+#include "gdn_internal.cuh"
+#include "gdn_ptx.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace ptx;
+using bf16 = __nv_bfloat16;
+
+constexpr int kC = 64;          // tokens per chunk
+constexpr int kThreads = 128;   // 4 warps; warp w owns rows 16w..16w+15 of a chunk product
+constexpr int kLdC = kC + 8;    // bf16 row stride of C x C tiles
+
+// ---- fragment loads for mma.m16n8k16 (bf16 operands from shared memory) ----
+// A(16 x 16) of a matrix stored row-major as (m, k)
+__device__ __forceinline__ void lda_row(const bf16 *base, int ld, int m0, int k0, uint32_t (&a)[4]) {
+  const int l = threadIdx.x & 31;
+  const bf16 *p = base + (m0 + (l & 7) + ((l >> 3) & 1) * 8) * ld + k0 + (l >> 4) * 8;
+  ldsm_x4(smem_u32(p), a[0], a[1], a[2], a[3]);
+}
+// A(16 x 16) of a matrix stored as (k, m): element (m, k) at base[k * ld + m]
+__device__ __forceinline__ void lda_tr(const bf16 *base, int ld, int m0, int k0, uint32_t (&a)[4]) {
+  const int l = threadIdx.x & 31, i = l >> 3;
+  const bf16 *p = base + (k0 + (i >> 1) * 8 + (l & 7)) * ld + m0 + (i & 1) * 8;
+  ldsm_x4_t(smem_u32(p), a[0], a[1], a[2], a[3]);
+}
+// B(16 x 8) for the n-tiles n0 and n0 + 8 of a matrix stored row-major as (k, n)
+__device__ __forceinline__ void ldb_kn(const bf16 *base, int ld, int k0, int n0, uint32_t (&b)[4]) {
+  const int l = threadIdx.x & 31, i = l >> 3;
+  const bf16 *p = base + (k0 + (i & 1) * 8 + (l & 7)) * ld + n0 + (i >> 1) * 8;
+  ldsm_x4_t(smem_u32(p), b[0], b[1], b[2], b[3]);
+}
+// the same for a matrix stored as (n, k): element (k, n) at base[n * ld + k]
+__device__ __forceinline__ void ldb_nk(const bf16 *base, int ld, int k0, int n0, uint32_t (&b)[4]) {
+  const int l = threadIdx.x & 31, i = l >> 3;
+  const bf16 *p = base + (n0 + (i >> 1) * 8 + (l & 7)) * ld + k0 + (i & 1) * 8;
+  ldsm_x4(smem_u32(p), b[0], b[1], b[2], b[3]);
+}
+
+// acc(16 x 8 NT) += A(16 x K) B(K x 8 NT); A rows m0.., B columns n0..
+template <int NT, bool A_TR, bool B_NK>
+__device__ __forceinline__ void wmma(float (&acc)[NT][4], const bf16 *A, int lda, int m0,
+                                     const bf16 *B, int ldb, int n0, int K) {
+  static_assert(NT % 2 == 0, "n-tiles come in pairs");
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    uint32_t a[4];
+    if (A_TR) lda_tr(A, lda, m0, k0, a);
+    else lda_row(A, lda, m0, k0, a);
+#pragma unroll
+    for (int p = 0; p < NT / 2; ++p) {
+      uint32_t b[4];
+      if (B_NK) ldb_nk(B, ldb, k0, n0 + 16 * p, b);
+      else ldb_kn(B, ldb, k0, n0 + 16 * p, b);
+      mma_bf16(acc[2 * p], a[0], a[1], a[2], a[3], b[0], b[1]);
+      mma_bf16(acc[2 * p + 1], a[0], a[1], a[2], a[3], b[2], b[3]);
+    }
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void zero(float (&acc)[NT][4]) {
+#pragma unroll
+  for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+}
+
+// Visit the accumulator elements: f(row, col, value&) with row in m0.., col in n0..
+template <int NT, typename F>
+__device__ __forceinline__ void each(float (&acc)[NT][4], int m0, int n0, F &&f) {
+  const int l = threadIdx.x & 31, r = m0 + (l >> 2), c = n0 + 2 * (l & 3);
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    f(r, c + 8 * t, acc[t][0]);
+    f(r, c + 8 * t + 1, acc[t][1]);
+    f(r + 8, c + 8 * t, acc[t][2]);
+    f(r + 8, c + 8 * t + 1, acc[t][3]);
+  }
+}
+
+// Sum of a per-row partial over the 4 lanes that share a row of the fragment.
+__device__ __forceinline__ float quad_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  x += __shfl_xor_sync(0xffffffffu, x, 2);
+  return x;
+}
+
+// Copy rows [0, 64) of a bf16 matrix with `cols` columns from global (row stride
+// gstride elements) into a padded shared tile; rows >= valid are zero.
+template <int COLS>
+__device__ __forceinline__ void load_rows(bf16 *dst, int ld, const bf16 *src, size_t gstride,
+                                          int valid) {
+  constexpr int V = COLS / 8;  // 16-byte pieces per row
+  for (int idx = threadIdx.x; idx < kC * V; idx += kThreads) {
+    const int r = idx / V, c = (idx % V) * 8;
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (r < valid) x = *reinterpret_cast<const uint4 *>(src + (size_t)r * gstride + c);
+    *reinterpret_cast<uint4 *>(dst + r * ld + c) = x;
+  }
+}
+
+// Chunk gates for tokens i < 64 (threads 0..63): G (inclusive prefix sum of g in
+// fp32, the same order in every kernel), gamma, dec and beta.  Tokens past the
+// chunk's end have g = 0 and beta = 0.  Needs a __syncthreads() after.
+__device__ __forceinline__ void chunk_gates(const float *g, const bf16 *beta, int64_t tok0,
+                                            int H, int h, int valid, float *sG, float *sGam,
+                                            float *sDec, float *sBeta, float *sTmp) {
+  const int i = threadIdx.x, lane = i & 31;
+  float x = 0.f, b = 0.f;
+  if (i < kC && i < valid) {
+    const size_t off = (size_t)(tok0 + i) * H + h;
+    x = g[off];
+    b = __bfloat162float(beta[off]);
+  }
+  if (i < kC) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (i == 31) sTmp[0] = x;
+  }
+  __syncthreads();
+  if (i < kC) {
+    if (i >= 32) x += sTmp[0];
+    sG[i] = x;
+    sBeta[i] = b;
+    sGam[i] = expf(x);
+  }
+  __syncthreads();
+  if (i < kC) sDec[i] = expf(sG[kC - 1] - sG[i]);
+}
+
+// The sequence and chunk of a chunk slot (see ckpt_first_slot); false when the
+// slot holds no chunk or the sequence bounds are bad.
+__device__ __forceinline__ bool slot_chunk(const FwdParams &p, int64_t slot, int h, int &n,
+                                           int64_t &tok0, int &valid) {
+  int64_t start, len, c;
+  if (p.cu == nullptr) {
+    const int64_t nck = (p.seq_len + kC - 1) / kC;
+    n = (int)(slot / nck);
+    c = slot - (int64_t)n * nck;
+    if (n >= p.num_seqs) return false;
+  } else {
+    int lo = 0, hi = p.num_seqs - 1;   // last n with cu[n] / 64 + n <= slot
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((int64_t)p.cu[mid] / kC + mid <= slot) lo = mid;
+      else hi = mid - 1;
+    }
+    n = lo;
+    c = slot - ((int64_t)p.cu[n] / kC + n);
+    if (c < 0) return false;
+  }
+  if (!sequence_bounds(p, n, h, start, len)) return false;
+  if (c * kC >= len) return false;
+  tok0 = start + c * kC;
+  valid = (int)(len - c * kC < kC ? len - c * kC : kC);
+  return true;
+}
+
+// Per (chunk slot, head) records of the workspace.
+template <int DK, int DV>
+struct ChunkWs {
+  bf16 *W, *Ut, *T, *Kt;     // [64][DK], [64][DV], [64][64], [64][DK]
+  float *X1t, *X2t;          // [DV][64] = dO^T P,  [DV][DK] = dO^T diag(gamma) Q
+  float *Hs, *dHs;           // [DK][DV]: state entering / gradient leaving the chunk
+  float *gC;                 // [1] (padded to 4) gamma_C
+  static constexpr size_t kW = 64 * DK, kUt = 64 * DV, kT = 64 * 64, kKt = 64 * DK;
+  static constexpr size_t kX1 = (size_t)DV * 64, kX2 = (size_t)DV * DK, kH = (size_t)DK * DV;
+  static size_t bytes(int64_t units) {
+    return (size_t)units * (2 * (kW + kUt + kT + kKt) + 4 * (kX1 + kX2 + 2 * kH + 4));
+  }
+  __host__ __device__ void carve(void *base, int64_t units) {
+    uint8_t *b = static_cast<uint8_t *>(base);
+    W = reinterpret_cast<bf16 *>(b);   b += units * kW * 2;
+    Ut = reinterpret_cast<bf16 *>(b);  b += units * kUt * 2;
+    T = reinterpret_cast<bf16 *>(b);   b += units * kT * 2;
+    Kt = reinterpret_cast<bf16 *>(b);  b += units * kKt * 2;
+    X1t = reinterpret_cast<float *>(b); b += units * kX1 * 4;
+    X2t = reinterpret_cast<float *>(b); b += units * kX2 * 4;
+    Hs = reinterpret_cast<float *>(b);  b += units * kH * 4;
+    dHs = reinterpret_cast<float *>(b); b += units * kH * 4;
+    gC = reinterpret_cast<float *>(b);
+  }
+};
+
+struct ChunkBwdParams {
+  FwdParams f;
+  const bf16 *dO;
+  const float *dHN;
+  float *dq, *dk, *dv, *dg, *dbeta, *dh0;
+  void *ws;            // ChunkWs arrays
+  int64_t slots;       // chunk slots per head
+};
+
+// Pairs of adjacent accumulator elements: f(row, col, x0, x1) with col even.
+template <int NT, typename F>
+__device__ __forceinline__ void each2(float (&acc)[NT][4], int m0, int n0, F &&f) {
+  const int l = threadIdx.x & 31, r = m0 + (l >> 2), c = n0 + 2 * (l & 3);
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    f(r, c + 8 * t, acc[t][0], acc[t][1]);
+    f(r + 8, c + 8 * t, acc[t][2], acc[t][3]);
+  }
+}
+
+__device__ __forceinline__ float bf(const bf16 &x) { return __bfloat162float(x); }
+__device__ __forceinline__ float rbf(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+__device__ __forceinline__ void st_bf2(bf16 *p, float a, float b) {
+  *reinterpret_cast<uint32_t *>(p) = pack_bf16(a, b);
+}
+
+// ---------------------------------------------------------------- prep ----
+template <int DK, int DV>
+struct PrepSmem {
+  static constexpr int LK = DK + 8, LV = DV + 8, LA = 68;
+  bf16 q[64 * LK], k[64 * LK], gq[64 * LK], rw[64 * LK];
+  bf16 v[64 * LV], o[64 * LV], ru[64 * LV];
+  bf16 P[64 * kLdC], T[64 * kLdC];
+  float A[64 * LA];
+  float G[64], gam[64], dec[64], beta[64], tmp[4];
+};
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(kThreads) gdn_bwdc_prep_kernel(const ChunkBwdParams P) {
+  using S = PrepSmem<DK, DV>;
+  using WS = ChunkWs<DK, DV>;
+  constexpr int LK = S::LK, LV = S::LV, LA = S::LA;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  S &s = *reinterpret_cast<S *>(smem_raw);
+  const FwdParams &p = P.f;
+  const int64_t slot = blockIdx.x;
+  const int h = blockIdx.y;
+  int n, valid;
+  int64_t tok0;
+  if (!slot_chunk(p, slot, h, n, tok0, valid)) return;
+  const int H = p.num_heads, tid = threadIdx.x, warp = tid >> 5, m0 = 16 * warp;
+  const size_t unit = (size_t)slot * H + h;
+  WS ws;
+  ws.carve(P.ws, P.slots * H);
+
+  const size_t rq = ((size_t)tok0 * H + h) * DK, rv = ((size_t)tok0 * H + h) * DV;
+  load_rows<DK>(s.q, LK, static_cast<const bf16 *>(p.q) + rq, (size_t)H * DK, valid);
+  load_rows<DK>(s.k, LK, static_cast<const bf16 *>(p.k) + rq, (size_t)H * DK, valid);
+  load_rows<DV>(s.v, LV, static_cast<const bf16 *>(p.v) + rv, (size_t)H * DV, valid);
+  load_rows<DV>(s.o, LV, P.dO + rv, (size_t)H * DV, valid);
+  chunk_gates(p.g, static_cast<const bf16 *>(p.beta), tok0, H, h, valid, s.G, s.gam, s.dec,
+              s.beta, s.tmp);
+  __syncthreads();
+
+  // scaled operands (bf16): gamma q, beta gamma k, beta v; K~ = dec k to the workspace
+  for (int idx = tid; idx < 64 * DK / 2; idx += kThreads) {
+    const int i = idx / (DK / 2), d = 2 * (idx % (DK / 2));
+    const float q0 = bf(s.q[i * LK + d]), q1 = bf(s.q[i * LK + d + 1]);
+    const float k0 = bf(s.k[i * LK + d]), k1 = bf(s.k[i * LK + d + 1]);
+    const float ga = s.gam[i], bg = s.beta[i] * s.gam[i], de = s.dec[i];
+    st_bf2(&s.gq[i * LK + d], ga * q0, ga * q1);
+    st_bf2(&s.rw[i * LK + d], bg * k0, bg * k1);
+    st_bf2(ws.Kt + unit * WS::kKt + i * DK + d, de * k0, de * k1);
+  }
+  for (int idx = tid; idx < 64 * DV / 2; idx += kThreads) {
+    const int i = idx / (DV / 2), c = 2 * (idx % (DV / 2));
+    const float b = s.beta[i];
+    st_bf2(&s.ru[i * LV + c], b * bf(s.v[i * LV + c]), b * bf(s.v[i * LV + c + 1]));
+  }
+  if (tid == 0) ws.gC[unit * 4] = s.gam[kC - 1];
+
+  // A = strictly_lower(diag(beta) K K^T (.) Gamma) in fp32; P = (Q K^T (.) Gamma)_{i>=j}
+  {
+    float acc[8][4];
+    zero(acc);
+    wmma<8, false, true>(acc, s.k, LK, m0, s.k, LK, 0, DK);
+    each(acc, m0, 0, [&](int i, int j, float &x) {
+      s.A[i * LA + j] = i > j ? s.beta[i] * x * expf(s.G[i] - s.G[j]) : 0.f;
+    });
+    zero(acc);
+    wmma<8, false, true>(acc, s.q, LK, m0, s.k, LK, 0, DK);
+    each2(acc, m0, 0, [&](int i, int j, float &x0, float &x1) {
+      const float p0 = i >= j ? x0 * expf(s.G[i] - s.G[j]) : 0.f;
+      const float p1 = i >= j + 1 ? x1 * expf(s.G[i] - s.G[j + 1]) : 0.f;
+      st_bf2(&s.P[i * kLdC + j], p0, p1);
+    });
+  }
+  __syncthreads();
+
+  // T = (I + A)^-1 by forward substitution, one column per thread (fp32):
+  // T_ij = -sum_{j <= m < i} A_im T_mj below the diagonal, T_jj = 1.
+  if (tid < kC) {
+    const int j = tid;
+    float t[kC];
+#pragma unroll
+    for (int i = 0; i < kC; ++i) {
+      float a = 0.f;
+#pragma unroll
+      for (int m = 0; m < i; ++m) a = fmaf(s.A[i * LA + m], t[m], a);
+      t[i] = i < j ? 0.f : (i == j ? 1.f : -a);
+    }
+#pragma unroll
+    for (int i = 0; i < kC; ++i) {
+      const bf16 b = __float2bfloat16_rn(t[i]);
+      s.T[i * kLdC + j] = b;
+      ws.T[unit * WS::kT + i * kC + j] = b;
+    }
+  }
+  __syncthreads();
+
+  // W = T diag(beta gamma) K, U~ = T diag(beta) V (bf16 to the workspace)
+  {
+    float acc[DK / 8][4];
+    zero(acc);
+    wmma<DK / 8, false, false>(acc, s.T, kLdC, m0, s.rw, LK, 0, kC);
+    bf16 *W = ws.W + unit * WS::kW;
+    each2(acc, m0, 0, [&](int i, int d, float &x0, float &x1) { st_bf2(W + i * DK + d, x0, x1); });
+  }
+  {
+    float acc[DV / 8][4];
+    zero(acc);
+    wmma<DV / 8, false, false>(acc, s.T, kLdC, m0, s.ru, LV, 0, kC);
+    bf16 *Ut = ws.Ut + unit * WS::kUt;
+    each2(acc, m0, 0, [&](int i, int c, float &x0, float &x1) { st_bf2(Ut + i * DV + c, x0, x1); });
+  }
+  // the state-free products of the reverse chain: dO^T P and dO^T diag(gamma) Q (fp32)
+  for (int mt = warp; mt < DV / 16; mt += 4) {
+    float acc[8][4];
+    zero(acc);
+    wmma<8, true, false>(acc, s.o, LV, 16 * mt, s.P, kLdC, 0, kC);
+    float *X1 = ws.X1t + unit * WS::kX1;
+    each2(acc, 16 * mt, 0, [&](int c, int j, float &x0, float &x1) {
+      *reinterpret_cast<float2 *>(X1 + c * kC + j) = make_float2(x0, x1);
+    });
+    float acc2[DK / 8][4];
+    zero(acc2);
+    wmma<DK / 8, true, false>(acc2, s.o, LV, 16 * mt, s.gq, LK, 0, kC);
+    float *X2 = ws.X2t + unit * WS::kX2;
+    each2(acc2, 16 * mt, 0, [&](int c, int d, float &x0, float &x1) {
+      *reinterpret_cast<float2 *>(X2 + c * DK + d) = make_float2(x0, x1);
+    });
+  }
+}
+
+// --------------------------------------------------------------- chains ----
+__device__ __forceinline__ void cp16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// rows x (cols elements of `bytes_per` bytes) from a dense global matrix into a padded tile
+template <int ROWS, int ROW_BYTES>
+__device__ __forceinline__ void cp_rows(void *dst, int ld_bytes, const void *src) {
+  constexpr int V = ROW_BYTES / 16;
+  for (int idx = threadIdx.x; idx < ROWS * V; idx += kThreads) {
+    const int r = idx / V, c = (idx % V) * 16;
+    cp16(static_cast<uint8_t *>(dst) + r * ld_bytes + c,
+         static_cast<const uint8_t *>(src) + (size_t)r * ROW_BYTES + c);
+  }
+}
+
+template <int DK, int DV, bool REV>
+struct ChainSmem {
+  static constexpr int LK = DK + 8, LV = DV + 8, LX1 = kC + 4, LX2 = DK + 4;
+  bf16 W[2][64 * LK], Kt[2][64 * LK];
+  bf16 Ut[REV ? 1 : 2][REV ? 8 : 64 * LV];
+  float X1[REV ? 2 : 1][REV ? DV * LX1 : 4];
+  float X2[REV ? 2 : 1][REV ? DV * LX2 : 4];
+  float gC[2][4];
+};
+
+// A operand (16 x 16, k-step kk) from a 16 x K fp32 accumulator, times `sc`.
+template <int NT>
+__device__ __forceinline__ void acc_to_a(const float (&acc)[NT][4], int kk, float sc,
+                                         uint32_t (&a)[4]) {
+  a[0] = pack_bf16(sc * acc[2 * kk][0], sc * acc[2 * kk][1]);
+  a[1] = pack_bf16(sc * acc[2 * kk][2], sc * acc[2 * kk][3]);
+  a[2] = pack_bf16(sc * acc[2 * kk + 1][0], sc * acc[2 * kk + 1][1]);
+  a[3] = pack_bf16(sc * acc[2 * kk + 1][2], sc * acc[2 * kk + 1][3]);
+}
+// acc(16 x 8 NT) += (sc * X)(16 x 8 KT) B, X an accumulator, B in shared memory
+template <int NT, int KT, bool B_NK>
+__device__ __forceinline__ void wmma_ra(float (&acc)[NT][4], const float (&X)[KT][4], float sc,
+                                        const bf16 *B, int ldb) {
+#pragma unroll
+  for (int kk = 0; kk < KT / 2; ++kk) {
+    uint32_t a[4];
+    acc_to_a(X, kk, sc, a);
+#pragma unroll
+    for (int p = 0; p < NT / 2; ++p) {
+      uint32_t b[4];
+      if (B_NK) ldb_nk(B, ldb, 16 * kk, 16 * p, b);
+      else ldb_kn(B, ldb, 16 * kk, 16 * p, b);
+      mma_bf16(acc[2 * p], a[0], a[1], a[2], a[3], b[0], b[1]);
+      mma_bf16(acc[2 * p + 1], a[0], a[1], a[2], a[3], b[2], b[3]);
+    }
+  }
+}
+
+// Forward (REV = false): H at every chunk start, from the initial state.
+//   U^T = U~^T - H^T W^T,   H'^T = gamma_C H^T + U^T K~
+// Reverse (REV = true): dH' at every chunk end, from d_final_state, and the
+// gradient of the initial state.
+//   dU^T = (dO^T P) + dH'^T K~^T,   dH^T = gamma_C dH'^T + (dO^T diag(gamma) Q) - dU^T W
+// Warp w keeps the transposed state of value columns 16w..16w+15 (16 x DK) in
+// its accumulators; the next chunk's operands are staged while it works.
+template <int DK, int DV, bool REV>
+__global__ void __launch_bounds__(kThreads) gdn_bwdc_chain_kernel(const ChunkBwdParams P) {
+  using S = ChainSmem<DK, DV, REV>;
+  using WS = ChunkWs<DK, DV>;
+  constexpr int LK = S::LK, LV = S::LV, LX1 = S::LX1, LX2 = S::LX2;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  S &s = *reinterpret_cast<S *>(smem_raw);
+  const FwdParams &p = P.f;
+  const int h = blockIdx.x, n = blockIdx.y;
+  int64_t start, len;
+  if (!sequence_bounds(p, n, h, start, len)) return;
+  const int H = p.num_heads, warp = threadIdx.x >> 5;
+  const int c0 = 16 * warp;
+  const bool active = c0 < DV;
+  const int64_t ck0 = ckpt_first_slot(n, start, p.seq_len, p.cu != nullptr);
+  const int nck = (int)((len + kC - 1) / kC);
+  WS ws;
+  ws.carve(P.ws, P.slots * H);
+
+  auto stage = [&](int buf, int cc) {
+    const size_t unit = (size_t)(ck0 + cc) * H + h;
+    cp_rows<64, DK * 2>(s.W[buf], LK * 2, ws.W + unit * WS::kW);
+    cp_rows<64, DK * 2>(s.Kt[buf], LK * 2, ws.Kt + unit * WS::kKt);
+    if (REV) {
+      cp_rows<DV, kC * 4>(s.X1[buf], LX1 * 4, ws.X1t + unit * WS::kX1);
+      cp_rows<DV, DK * 4>(s.X2[buf], LX2 * 4, ws.X2t + unit * WS::kX2);
+    } else {
+      cp_rows<64, DV * 2>(s.Ut[buf], LV * 2, ws.Ut + unit * WS::kUt);
+    }
+    if (threadIdx.x == 0) cp16(s.gC[buf], ws.gC + unit * 4);
+    cp_commit();
+  };
+
+  // state^T: row = value column c0 + (lane/4) (+8), column = key row d
+  float st[DK / 8][4];
+  const size_t sbase = ((size_t)n * H + h) * DK * DV;
+  {
+    const float *src = REV ? P.dHN : p.s0;
+    each(st, c0, 0, [&](int c, int d, float &x) {
+      x = (src != nullptr && active) ? src[sbase + (size_t)d * DV + c] : 0.f;
+    });
+  }
+  stage(0, REV ? nck - 1 : 0);
+  for (int it = 0; it < nck; ++it) {
+    const int cc = REV ? nck - 1 - it : it, buf = it & 1;
+    if (it + 1 < nck) {
+      stage(buf ^ 1, REV ? cc - 1 : cc + 1);
+      cp_wait<1>();
+    } else {
+      cp_wait<0>();
+    }
+    __syncthreads();
+    const size_t unit = (size_t)(ck0 + cc) * H + h;
+    float *out = (REV ? ws.dHs : ws.Hs) + unit * WS::kH;
+    const float gC = s.gC[buf][0];
+    if (active) {
+      each2(st, c0, 0, [&](int c, int d, float &x0, float &x1) {
+        out[(size_t)d * DV + c] = x0;
+        out[(size_t)(d + 1) * DV + c] = x1;
+      });
+      float u[8][4];   // 16 value columns x 64 tokens
+      if (!REV) {
+        zero(u);
+        wmma_ra<8, DK / 8, true>(u, st, 1.f, s.W[buf], LK);   // H^T W^T
+        each(u, c0, 0, [&](int c, int i, float &x) { x = bf(s.Ut[buf][i * LV + c]) - x; });
+#pragma unroll
+        for (int t = 0; t < DK / 8; ++t)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) st[t][e] *= gC;
+        wmma_ra<DK / 8, 8, false>(st, u, 1.f, s.Kt[buf], LK);  // + U^T K~
+      } else {
+        each(u, c0, 0, [&](int c, int i, float &x) { x = s.X1[buf][c * LX1 + i]; });
+        wmma_ra<8, DK / 8, true>(u, st, 1.f, s.Kt[buf], LK);   // + dH'^T K~^T
+        each(st, c0, 0, [&](int c, int d, float &x) { x = gC * x + s.X2[buf][c * LX2 + d]; });
+        wmma_ra<DK / 8, 8, false>(st, u, -1.f, s.W[buf], LK);  // - dU^T W
+      }
+    }
+    __syncthreads();   // buffer `buf` is restaged two iterations on
+  }
+  if (REV && P.dh0 != nullptr && active)
+    each(st, c0, 0, [&](int c, int d, float &x) { P.dh0[sbase + (size_t)d * DV + c] = x; });
+}
+
+// ----------------------------------------------------------------- grad ----
+template <int DK, int DV>
+struct GradSmem {
+  static constexpr int LK = DK + 8, LV = DV + 8, LF = 68;
+  static constexpr int R1 = (DK * LV > 64 * LK ? DK * LV : 64 * LK);  // H, then dR_W
+  static constexpr int R2 = (DK * LV > 64 * LV ? DK * LV : 64 * LV);  // dH', then dR_U
+  bf16 q[64 * LK], k[64 * LK], W[64 * LK], KtDW[64 * LK];  // K~, then dW
+  bf16 v[64 * LV], o[64 * LV], Ut[64 * LV], U[64 * LV], dU[64 * LV];
+  bf16 dUlo[64 * LV], dWlo[64 * LK];  // what rounding dU and dW to bf16 left out
+  bf16 T[64 * kLdC], PDP[64 * kLdC], SA[64 * kLdC];        // P, then dP (.) Gamma
+  bf16 r1[R1], r2[R2];
+  float QK[64 * LF], KK[64 * LF], DA[64 * LF];             // QK, then the gate terms E
+  float G[64], gam[64], dec[64], beta[64];
+  float dgam[64], dbg[64], ddec[64], dbU[64], dbA[64], dG[64], dB[64];
+  float tmp[4], red[4], red2[4];
+};
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdParams P) {
+  using S = GradSmem<DK, DV>;
+  using WS = ChunkWs<DK, DV>;
+  constexpr int LK = S::LK, LV = S::LV, LF = S::LF;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  S &s = *reinterpret_cast<S *>(smem_raw);
+  const FwdParams &p = P.f;
+  const int64_t slot = blockIdx.x;
+  const int h = blockIdx.y;
+  int n, valid;
+  int64_t tok0;
+  if (!slot_chunk(p, slot, h, n, tok0, valid)) return;
+  const int H = p.num_heads, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int m0 = 16 * warp, r0 = m0 + (lane >> 2);
+  const size_t unit = (size_t)slot * H + h;
+  WS ws;
+  ws.carve(P.ws, P.slots * H);
+  bf16 *sH = s.r1, *sDRW = s.r1, *sDH = s.r2, *sDRU = s.r2;
+
+  // ---- loads: the chunk's inputs, the prep's tiles, H and dH' (bf16 copies) ----
+  const size_t rq = ((size_t)tok0 * H + h) * DK, rv = ((size_t)tok0 * H + h) * DV;
+  load_rows<DK>(s.q, LK, static_cast<const bf16 *>(p.q) + rq, (size_t)H * DK, valid);
+  load_rows<DK>(s.k, LK, static_cast<const bf16 *>(p.k) + rq, (size_t)H * DK, valid);
+  load_rows<DV>(s.v, LV, static_cast<const bf16 *>(p.v) + rv, (size_t)H * DV, valid);
+  load_rows<DV>(s.o, LV, P.dO + rv, (size_t)H * DV, valid);
+  load_rows<DK>(s.W, LK, ws.W + unit * WS::kW, DK, kC);
+  load_rows<DK>(s.KtDW, LK, ws.Kt + unit * WS::kKt, DK, kC);
+  load_rows<DV>(s.Ut, LV, ws.Ut + unit * WS::kUt, DV, kC);
+  load_rows<kC>(s.T, kLdC, ws.T + unit * WS::kT, kC, kC);
+  float part = 0.f;   // <dH', H>, the gradient of gamma_C
+  {
+    const float *Hs = ws.Hs + unit * WS::kH, *dHs = ws.dHs + unit * WS::kH;
+    for (int idx = tid; idx < DK * DV / 4; idx += kThreads) {
+      const int d = (4 * idx) / DV, c = (4 * idx) % DV;
+      const float4 a = *reinterpret_cast<const float4 *>(Hs + 4 * idx);
+      const float4 b = *reinterpret_cast<const float4 *>(dHs + 4 * idx);
+      part += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+      *reinterpret_cast<uint2 *>(sH + d * LV + c) = make_uint2(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w));
+      *reinterpret_cast<uint2 *>(sDH + d * LV + c) = make_uint2(pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  if (lane == 0) s.red[warp] = part;
+  chunk_gates(p.g, static_cast<const bf16 *>(p.beta), tok0, H, h, valid, s.G, s.gam, s.dec,
+              s.beta, s.tmp);
+  __syncthreads();
+  const float dgC = s.red[0] + s.red[1] + s.red[2] + s.red[3];
+  const float gC = s.gam[kC - 1];
+
+  // ---- P, Q K^T, K K^T, U = U~ - W H ----
+  {
+    float acc[8][4];
+    zero(acc);
+    wmma<8, false, true>(acc, s.q, LK, m0, s.k, LK, 0, DK);
+    each2(acc, m0, 0, [&](int i, int j, float &x0, float &x1) {
+      s.QK[i * LF + j] = x0;
+      s.QK[i * LF + j + 1] = x1;
+      const float p0 = i >= j ? x0 * expf(s.G[i] - s.G[j]) : 0.f;
+      const float p1 = i >= j + 1 ? x1 * expf(s.G[i] - s.G[j + 1]) : 0.f;
+      st_bf2(&s.PDP[i * kLdC + j], p0, p1);
+    });
+    zero(acc);
+    wmma<8, false, true>(acc, s.k, LK, m0, s.k, LK, 0, DK);
+    each2(acc, m0, 0, [&](int i, int j, float &x0, float &x1) {
+      s.KK[i * LF + j] = x0;
+      s.KK[i * LF + j + 1] = x1;
+    });
+  }
+  {
+    float acc[DV / 8][4];
+    zero(acc);
+    wmma<DV / 8, false, false>(acc, s.W, LK, m0, sH, LV, 0, DK);
+    each2(acc, m0, 0, [&](int i, int c, float &x0, float &x1) {
+      st_bf2(&s.U[i * LV + c], bf(s.Ut[i * LV + c]) - x0, bf(s.Ut[i * LV + c + 1]) - x1);
+    });
+  }
+  __syncthreads();
+  // dU = P^T dO + K~ dH'
+  {
+    float acc[DV / 8][4];
+    zero(acc);
+    wmma<DV / 8, true, false>(acc, s.PDP, kLdC, m0, s.o, LV, 0, kC);
+    wmma<DV / 8, false, false>(acc, s.KtDW, LK, m0, sDH, LV, 0, DK);
+    each2(acc, m0, 0, [&](int i, int c, float &x0, float &x1) {
+      st_bf2(&s.dU[i * LV + c], x0, x1);
+      st_bf2(&s.dUlo[i * LV + c], x0 - rbf(x0), x1 - rbf(x1));
+    });
+  }
+  __syncthreads();
+
+  // ---- dP, dW, dK~, dO H^T ----
+  {
+    float acc[8][4];
+    zero(acc);
+    wmma<8, false, true>(acc, s.o, LV, m0, s.U, LV, 0, DV);
+    each2(acc, m0, 0, [&](int i, int j, float &x0, float &x1) {
+      float d0 = 0.f, d1 = 0.f;
+      if (i >= j) d0 = x0 * expf(s.G[i] - s.G[j]);
+      if (i >= j + 1) d1 = x1 * expf(s.G[i] - s.G[j + 1]);
+      st_bf2(&s.PDP[i * kLdC + j], d0, d1);
+      s.QK[i * LF + j] = d0 * s.QK[i * LF + j];
+      s.QK[i * LF + j + 1] = d1 * s.QK[i * LF + j + 1];
+    });
+  }
+  {
+    float acc[DK / 8][4];
+    zero(acc);
+    wmma<DK / 8, false, true>(acc, s.dU, LV, m0, sH, LV, 0, DV);
+    each2(acc, m0, 0, [&](int i, int d, float &x0, float &x1) {
+      st_bf2(&s.KtDW[i * LK + d], -x0, -x1);
+      st_bf2(&s.dWlo[i * LK + d], rbf(x0) - x0, rbf(x1) - x1);
+    });
+  }
+  float dK[DK / 8][4], dQ[DK / 8][4];
+  {
+    zero(dK);
+    wmma<DK / 8, false, true>(dK, s.U, LV, m0, sDH, LV, 0, DV);   // dK~ = U dH'^T
+    float p0 = 0.f, p1 = 0.f;
+    each2(dK, m0, 0, [&](int i, int d, float &x0, float &x1) {
+      const float e = x0 * bf(s.k[i * LK + d]) + x1 * bf(s.k[i * LK + d + 1]);
+      if (i == r0) p0 += e; else p1 += e;
+      x0 *= s.dec[i];
+      x1 *= s.dec[i];
+    });
+    p0 = quad_sum(p0);
+    p1 = quad_sum(p1);
+    if ((lane & 3) == 0) { s.ddec[r0] = p0; s.ddec[r0 + 8] = p1; }
+    zero(dQ);
+    wmma<DK / 8, false, true>(dQ, s.o, LV, m0, sH, LV, 0, DV);   // dO H^T
+    p0 = p1 = 0.f;
+    each2(dQ, m0, 0, [&](int i, int d, float &x0, float &x1) {
+      const float e = x0 * bf(s.q[i * LK + d]) + x1 * bf(s.q[i * LK + d + 1]);
+      if (i == r0) p0 += e; else p1 += e;
+      x0 *= s.gam[i];
+      x1 *= s.gam[i];
+    });
+    p0 = quad_sum(p0);
+    p1 = quad_sum(p1);
+    if ((lane & 3) == 0) { s.dgam[r0] = p0; s.dgam[r0 + 8] = p1; }
+  }
+  __syncthreads();
+
+  // ---- dR_W = T^T dW, dR_U = T^T dU, dV, dQ ----
+  {
+    float acc[DK / 8][4];
+    zero(acc);
+    wmma<DK / 8, true, false>(acc, s.T, kLdC, m0, s.KtDW, LK, 0, kC);
+    wmma<DK / 8, true, false>(acc, s.T, kLdC, m0, s.dWlo, LK, 0, kC);
+    float p0 = 0.f, p1 = 0.f;
+    each2(acc, m0, 0, [&](int i, int d, float &x0, float &x1) {
+      const float e = x0 * bf(s.k[i * LK + d]) + x1 * bf(s.k[i * LK + d + 1]);
+      if (i == r0) p0 += e; else p1 += e;
+      st_bf2(&sDRW[i * LK + d], x0, x1);
+    });
+    const float bg0 = s.beta[r0] * s.gam[r0], bg1 = s.beta[r0 + 8] * s.gam[r0 + 8];
+#pragma unroll
+    for (int t = 0; t < DK / 8; ++t) {
+      dK[t][0] = fmaf(bg0, acc[t][0], dK[t][0]);
+      dK[t][1] = fmaf(bg0, acc[t][1], dK[t][1]);
+      dK[t][2] = fmaf(bg1, acc[t][2], dK[t][2]);
+      dK[t][3] = fmaf(bg1, acc[t][3], dK[t][3]);
+    }
+    p0 = quad_sum(p0);
+    p1 = quad_sum(p1);
+    if ((lane & 3) == 0) { s.dbg[r0] = p0; s.dbg[r0 + 8] = p1; }
+  }
+  {
+    float acc[DV / 8][4];
+    zero(acc);
+    wmma<DV / 8, true, false>(acc, s.T, kLdC, m0, s.dU, LV, 0, kC);
+    wmma<DV / 8, true, false>(acc, s.T, kLdC, m0, s.dUlo, LV, 0, kC);
+    float p0 = 0.f, p1 = 0.f;
+    each2(acc, m0, 0, [&](int i, int c, float &x0, float &x1) {
+      const float e = x0 * bf(s.v[i * LV + c]) + x1 * bf(s.v[i * LV + c + 1]);
+      if (i == r0) p0 += e; else p1 += e;
+      st_bf2(&sDRU[i * LV + c], x0, x1);
+      if (i < valid)
+        *reinterpret_cast<float2 *>(P.dv + ((size_t)(tok0 + i) * H + h) * DV + c) =
+            make_float2(s.beta[i] * x0, s.beta[i] * x1);
+    });
+    p0 = quad_sum(p0);
+    p1 = quad_sum(p1);
+    if ((lane & 3) == 0) { s.dbU[r0] = p0; s.dbU[r0 + 8] = p1; }
+  }
+  wmma<DK / 8, false, false>(dQ, s.PDP, kLdC, m0, s.k, LK, 0, kC);   // + (dP (.) Gamma) K
+  each2(dQ, m0, 0, [&](int i, int d, float &x0, float &x1) {
+    if (i < valid)
+      *reinterpret_cast<float2 *>(P.dq + ((size_t)(tok0 + i) * H + h) * DK + d) = make_float2(x0, x1);
+  });
+  __syncthreads();
+
+  // ---- dA = -(dR_W W^T + dR_U U~^T), D = dA (.) Gamma ----
+  {
+    float acc[8][4];
+    zero(acc);
+    wmma<8, false, true>(acc, sDRW, LK, m0, s.W, LK, 0, DK);
+    wmma<8, false, true>(acc, sDRU, LV, m0, s.Ut, LV, 0, DV);
+    float p0 = 0.f, p1 = 0.f;
+    each(acc, m0, 0, [&](int i, int j, float &x) {
+      float D = 0.f;
+      if (i > j) {
+        D = -x * expf(s.G[i] - s.G[j]);
+        const float kk = s.KK[i * LF + j];
+        s.QK[i * LF + j] += s.beta[i] * D * kk;
+        if (i == r0) p0 += D * kk; else p1 += D * kk;
+      }
+      s.DA[i * LF + j] = D;
+    });
+    p0 = quad_sum(p0);
+    p1 = quad_sum(p1);
+    if ((lane & 3) == 0) { s.dbA[r0] = p0; s.dbA[r0 + 8] = p1; }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < kC * kC / 2; idx += kThreads) {
+    const int i = idx / (kC / 2), j = 2 * (idx % (kC / 2));
+    st_bf2(&s.SA[i * kLdC + j], s.beta[i] * s.DA[i * LF + j] + s.DA[j * LF + i] * s.beta[j],
+           s.beta[i] * s.DA[i * LF + j + 1] + s.DA[(j + 1) * LF + i] * s.beta[j + 1]);
+  }
+  __syncthreads();
+
+  // ---- dK += S K + (dP (.) Gamma)^T Q ----
+  wmma<DK / 8, false, false>(dK, s.SA, kLdC, m0, s.k, LK, 0, kC);
+  wmma<DK / 8, true, false>(dK, s.PDP, kLdC, m0, s.q, LK, 0, kC);
+  each2(dK, m0, 0, [&](int i, int d, float &x0, float &x1) {
+    if (i < valid)
+      *reinterpret_cast<float2 *>(P.dk + ((size_t)(tok0 + i) * H + h) * DK + d) = make_float2(x0, x1);
+  });
+
+  // ---- gates: dG per token, then dg = its sum over later tokens of the chunk ----
+  float xdec = 0.f;
+  if (tid < kC) {
+    const int i = tid;
+    float rs = 0.f, cs = 0.f;
+    for (int m = 0; m < kC; ++m) {
+      rs += s.QK[i * LF + m];
+      cs += s.QK[m * LF + i];
+    }
+    const float dgt = s.dgam[i] + s.beta[i] * s.dbg[i];
+    s.dG[i] = rs - cs + s.gam[i] * dgt - s.dec[i] * s.ddec[i];
+    s.dB[i] = s.dbU[i] + s.dbA[i] + s.gam[i] * s.dbg[i];
+    xdec = s.dec[i] * s.ddec[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) xdec += __shfl_xor_sync(0xffffffffu, xdec, o);
+    if (lane == 0) s.red2[warp] = xdec;
+  }
+  __syncthreads();
+  if (tid < kC) {
+    // suffix sums: thread t takes token 63 - t
+    const int t = tid, i = kC - 1 - t;
+    float x = s.dG[i];
+    if (i == kC - 1) x += gC * dgC + s.red2[0] + s.red2[1];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (t == 31) s.tmp[1] = x;
+    s.dG[i] = x;   // own slot only; the other warp's total is added below
+  }
+  __syncthreads();
+  if (tid < kC) {
+    const int t = tid, i = kC - 1 - t;
+    const float x = s.dG[i] + (t >= 32 ? s.tmp[1] : 0.f);
+    if (i < valid) {
+      const size_t off = (size_t)(tok0 + i) * H + h;
+      P.dg[off] = x;
+      P.dbeta[off] = s.dB[i];
+    }
+  }
+}
+
+// ----------------------------------------------------------------- host ----
+template <typename K>
+cudaError_t smem_attr(K kern, size_t bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <int DK, int DV>
+cudaError_t launch_dims(const ChunkBwdParams &P, cudaStream_t s) {
+  auto prep = gdn_bwdc_prep_kernel<DK, DV>;
+  auto fwd = gdn_bwdc_chain_kernel<DK, DV, false>;
+  auto rev = gdn_bwdc_chain_kernel<DK, DV, true>;
+  auto grad = gdn_bwdc_grad_kernel<DK, DV>;
+  const size_t sp = sizeof(PrepSmem<DK, DV>), sf = sizeof(ChainSmem<DK, DV, false>);
+  const size_t sr = sizeof(ChainSmem<DK, DV, true>), sg = sizeof(GradSmem<DK, DV>);
+  cudaError_t e;
+  if ((e = smem_attr(prep, sp)) != cudaSuccess || (e = smem_attr(fwd, sf)) != cudaSuccess ||
+      (e = smem_attr(rev, sr)) != cudaSuccess || (e = smem_attr(grad, sg)) != cudaSuccess)
+    return e;
+  const dim3 per_chunk((unsigned)P.slots, (unsigned)P.f.num_heads);
+  const dim3 per_seq((unsigned)P.f.num_heads, (unsigned)P.f.num_seqs);
+  prep<<<per_chunk, kThreads, sp, s>>>(P);
+  fwd<<<per_seq, kThreads, sf, s>>>(P);
+  rev<<<per_seq, kThreads, sr, s>>>(P);
+  grad<<<per_chunk, kThreads, sg, s>>>(P);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool bwd_chunked_supported(int dk, int dv) {
+  return (dk == 32 || dk == 64) && (dv == 32 || dv == 64);
+}
+
+size_t bwd_chunked_ws_bytes(int64_t units, int dk, int dv) {
+  if (dk == 32) return dv == 32 ? ChunkWs<32, 32>::bytes(units) : ChunkWs<32, 64>::bytes(units);
+  return dv == 32 ? ChunkWs<64, 32>::bytes(units) : ChunkWs<64, 64>::bytes(units);
+}
+
+cudaError_t launch_bwd_chunked(const FwdParams &f, const void *dO, const float *dHN, float *dq,
+                               float *dk, float *dv, float *dg, float *dbeta, float *dh0,
+                               void *ws, int64_t slots, cudaStream_t s) {
+  ChunkBwdParams P;
+  P.f = f;
+  P.dO = static_cast<const bf16 *>(dO);
+  P.dHN = dHN;
+  P.dq = dq; P.dk = dk; P.dv = dv; P.dg = dg; P.dbeta = dbeta; P.dh0 = dh0;
+  P.ws = ws;
+  P.slots = slots;
+  if (f.dk == 32) return f.dv == 32 ? launch_dims<32, 32>(P, s) : launch_dims<32, 64>(P, s);
+  return f.dv == 32 ? launch_dims<64, 32>(P, s) : launch_dims<64, 64>(P, s);
+}
+
+}  // namespace gdn

@@ -1,9 +1,15 @@
 """GPU parity of the backward pass (``gdn_bwd``) against the fp64 autograd
 oracle ``oracle.grad`` on the same seeded inputs, through the C ABI.
 
-Every gradient is computed in fp32 from the stored inputs (bf16 storage only
-rounds the inputs, which the oracle sees as they are), so both storage dtypes
-are held to the fp32 bound, relative L2 over each whole gradient tensor."""
+Two paths, two bounds (relative L2 over each whole gradient tensor):
+- fp32 storage, and bf16 storage with head_dim_k or head_dim_v above 64, run
+  the token-serial fp32 backward; every gradient is computed in fp32 from the
+  stored inputs, so it is held to 1e-4.
+- bf16 storage with head_dim_k, head_dim_v <= 64 runs the chunked backward,
+  whose products take bf16 operands with fp32 accumulation, as the forward's
+  tensor-core path does; it is held to the forward's bf16 bound on o, 1e-2.
+  (Rounding every product operand of the chunked algebra to bf16 in an fp64
+  emulation gives 2e-3 to 4e-3 on these inputs.)"""
 from __future__ import annotations
 
 import numpy as np
@@ -18,6 +24,11 @@ from parity import rel
 pytestmark = pytest.mark.gpu
 
 GRAD_TOL = 1e-4
+BF16_GRAD_TOL = 1e-2
+
+
+def _tol(dtype, dk, dv):
+    return BF16_GRAD_TOL if dtype == "bf16" and dk <= 64 and dv <= 64 else GRAD_TOL
 NAMES = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
 
 
@@ -68,7 +79,7 @@ def test_bwd_matches_oracle(dtype, B, T, H, dk, dv, init):
                  seed=3000 + T + dk + dv)
     inp = W.generate(w)
     d_o, dhN = _upstream(inp, 7 + T, init)
-    _check(_run(inp, d_o, dhN), _ref(inp, d_o, dhN))
+    _check(_run(inp, d_o, dhN), _ref(inp, d_o, dhN), _tol(dtype, dk, dv))
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
@@ -78,7 +89,7 @@ def test_bwd_varlen(dtype):
                  init_state=True, seed=51)
     inp = W.generate(w, lengths=lens)
     d_o, dhN = _upstream(inp, 52, True)
-    _check(_run(inp, d_o, dhN), _ref(inp, d_o, dhN))
+    _check(_run(inp, d_o, dhN), _ref(inp, d_o, dhN), _tol(dtype, 64, 64))
 
 
 def test_bwd_slow_gates_long():
@@ -87,7 +98,7 @@ def test_bwd_slow_gates_long():
                  init_state=True, seed=53)
     inp = W.generate(w)
     d_o, dhN = _upstream(inp, 54, True)
-    _check(_run(inp, d_o, dhN), _ref(inp, d_o, dhN))
+    _check(_run(inp, d_o, dhN), _ref(inp, d_o, dhN), _tol("bf16", 64, 64))
 
 
 def test_bwd_full_size_sampled():
@@ -102,8 +113,8 @@ def test_bwd_full_size_sampled():
         one.update(initial_state=None, cu_seqlens=None)
         ref = _ref(one, d_o[b:b + 1, :, h:h + 1], None)
         for n in ("dq", "dk", "dv", "dg", "dbeta"):
-            assert rel(gpu[n][b:b + 1, :, h:h + 1], ref[n]) <= GRAD_TOL, (n, b, h)
-        assert rel(gpu["dh0"][b:b + 1, h:h + 1], ref["dh0"]) <= GRAD_TOL, ("dh0", b, h)
+            assert rel(gpu[n][b:b + 1, :, h:h + 1], ref[n]) <= BF16_GRAD_TOL, (n, b, h)
+        assert rel(gpu["dh0"][b:b + 1, h:h + 1], ref["dh0"]) <= BF16_GRAD_TOL, ("dh0", b, h)
 
 
 def test_bwd_chunk_checkpoints_only():
