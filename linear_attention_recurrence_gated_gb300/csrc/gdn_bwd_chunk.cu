@@ -31,9 +31,9 @@
 //   chain  (per sequence and head, reverse)  dH' at every chunk end and the
 //          gradient of the initial state;
 //   grad   (per chunk and head)  dq, dk, dv, dg, dbeta of the chunk.
-// dU and dW enter T^T dU and T^T dW as two bf16 operands each (the rounded
-// value and what the rounding left out), so that the diagonal of T (exactly 1)
-// passes them on at nearly fp32 precision: dbeta and dv sum over them.
+// dU and dW enter T^T dU and T^T dW as bf16 operands, and what rounding them
+// left out is added back on the diagonal of T (exactly 1), so that dR_U and
+// dR_W, over which dbeta and dv sum, keep it.
 // The chains keep their state in the MMA accumulator registers of the warps
 // (16 value columns per warp, transposed, so that an accumulator is directly
 // the A operand of the next product).  No kernel waits on another CTA.
@@ -122,17 +122,39 @@ __device__ __forceinline__ float quad_sum(float x) {
   return x;
 }
 
-// Copy rows [0, 64) of a bf16 matrix with `cols` columns from global (row stride
-// gstride elements) into a padded shared tile; rows >= valid are zero.
-template <int COLS>
-__device__ __forceinline__ void load_rows(bf16 *dst, int ld, const bf16 *src, size_t gstride,
-                                          int valid) {
+__device__ __forceinline__ void cp16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// rows x (cols elements of `bytes_per` bytes) from a dense global matrix into a padded tile
+template <int ROWS, int ROW_BYTES>
+__device__ __forceinline__ void cp_rows(void *dst, int ld_bytes, const void *src) {
+  constexpr int V = ROW_BYTES / 16;
+  for (int idx = threadIdx.x; idx < ROWS * V; idx += kThreads) {
+    const int r = idx / V, c = (idx % V) * 16;
+    cp16(static_cast<uint8_t *>(dst) + r * ld_bytes + c,
+         static_cast<const uint8_t *>(src) + (size_t)r * ROW_BYTES + c);
+  }
+}
+
+// rows [0, ROWS) of a bf16 matrix with COLS columns (global row stride gstride
+// elements) into a padded shared tile with cp.async; rows >= valid are zero.
+template <int ROWS, int COLS>
+__device__ __forceinline__ void cp_tile(bf16 *dst, int ld, const bf16 *src, size_t gstride,
+                                        int valid) {
   constexpr int V = COLS / 8;  // 16-byte pieces per row
-  for (int idx = threadIdx.x; idx < kC * V; idx += kThreads) {
+  for (int idx = threadIdx.x; idx < ROWS * V; idx += kThreads) {
     const int r = idx / V, c = (idx % V) * 8;
-    uint4 x = make_uint4(0u, 0u, 0u, 0u);
-    if (r < valid) x = *reinterpret_cast<const uint4 *>(src + (size_t)r * gstride + c);
-    *reinterpret_cast<uint4 *>(dst + r * ld + c) = x;
+    const bool ok = r < valid;
+    const bf16 *g = src + (ok ? (size_t)r * gstride + c : 0);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst + r * ld + c)),
+                 "l"(g), "r"(ok ? 16 : 0)
+                 : "memory");
   }
 }
 
@@ -200,13 +222,13 @@ __device__ __forceinline__ bool slot_chunk(const FwdParams &p, int64_t slot, int
 template <int DK, int DV>
 struct ChunkWs {
   bf16 *W, *Ut, *T, *Kt;     // [64][DK], [64][DV], [64][64], [64][DK]
+  bf16 *Hb, *dHb;            // [DK][DV]: state entering / gradient leaving the chunk
   float *X1t, *X2t;          // [DV][64] = dO^T P,  [DV][DK] = dO^T diag(gamma) Q
-  float *Hs, *dHs;           // [DK][DV]: state entering / gradient leaving the chunk
-  float *gC;                 // [1] (padded to 4) gamma_C
+  float *gC;                 // [4]: gamma_C, the gradient of gamma_C, 0, 0
   static constexpr size_t kW = 64 * DK, kUt = 64 * DV, kT = 64 * 64, kKt = 64 * DK;
   static constexpr size_t kX1 = (size_t)DV * 64, kX2 = (size_t)DV * DK, kH = (size_t)DK * DV;
   static size_t bytes(int64_t units) {
-    return (size_t)units * (2 * (kW + kUt + kT + kKt) + 4 * (kX1 + kX2 + 2 * kH + 4));
+    return (size_t)units * (2 * (kW + kUt + kT + kKt + 2 * kH) + 4 * (kX1 + kX2 + 4));
   }
   __host__ __device__ void carve(void *base, int64_t units) {
     uint8_t *b = static_cast<uint8_t *>(base);
@@ -214,10 +236,10 @@ struct ChunkWs {
     Ut = reinterpret_cast<bf16 *>(b);  b += units * kUt * 2;
     T = reinterpret_cast<bf16 *>(b);   b += units * kT * 2;
     Kt = reinterpret_cast<bf16 *>(b);  b += units * kKt * 2;
+    Hb = reinterpret_cast<bf16 *>(b);  b += units * kH * 2;
+    dHb = reinterpret_cast<bf16 *>(b); b += units * kH * 2;
     X1t = reinterpret_cast<float *>(b); b += units * kX1 * 4;
     X2t = reinterpret_cast<float *>(b); b += units * kX2 * 4;
-    Hs = reinterpret_cast<float *>(b);  b += units * kH * 4;
-    dHs = reinterpret_cast<float *>(b); b += units * kH * 4;
     gC = reinterpret_cast<float *>(b);
   }
 };
@@ -251,19 +273,87 @@ __device__ __forceinline__ void st_bf2(bf16 *p, float a, float b) {
 // ---------------------------------------------------------------- prep ----
 template <int DK, int DV>
 struct PrepSmem {
-  static constexpr int LK = DK + 8, LV = DV + 8, LA = 68;
-  bf16 q[64 * LK], k[64 * LK], gq[64 * LK], rw[64 * LK];
+  static constexpr int LK = DK + 8, LV = DV + 8, LA = 68, LB = 17;
+  bf16 q[64 * LK], k[64 * LK], rw[64 * LK];   // rw: diag(beta gamma) K, then diag(gamma) Q
   bf16 v[64 * LV], o[64 * LV], ru[64 * LV];
   bf16 P[64 * kLdC], T[64 * kLdC];
-  float A[64 * LA];
+  float A[64 * LA];            // A; its diagonal 16 x 16 blocks become T's
+  float Toff[6][16 * LB];      // T's blocks below the diagonal, (i, j) at i (i - 1) / 2 + j
+  float X[3][16 * LB];         // scratch of the block substitution
   float G[64], gam[64], dec[64], beta[64], tmp[4];
 };
+
+// T = (I + A)^-1 of a strictly lower A (fp32), in 16 x 16 blocks: the diagonal
+// blocks by forward substitution (in place over A's), then the blocks below by
+// diagonals, T_ij = -T_ii sum_{j <= m < i} A_im T_mj.
+template <int DK, int DV>
+__device__ __forceinline__ void block_inverse(PrepSmem<DK, DV> &s) {
+  constexpr int LA = PrepSmem<DK, DV>::LA, LB = PrepSmem<DK, DV>::LB;
+  const int tid = threadIdx.x, b = tid >> 4, j = tid & 15;
+  float t[16];
+  if (tid < kC) {
+    const float *Ab = s.A + 16 * b * LA + 16 * b;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float a = 0.f;
+#pragma unroll
+      for (int m = 0; m < i; ++m) a = fmaf(Ab[i * LA + m], t[m], a);
+      t[i] = i < j ? 0.f : (i == j ? 1.f : -a);
+    }
+  }
+  __syncthreads();   // every column has read its A block
+  if (tid < kC) {
+    float *Tb = s.A + 16 * b * LA + 16 * b;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) Tb[i * LA + j] = t[i];
+  }
+  __syncthreads();
+  for (int L = 1; L < 4; ++L) {
+    const int nb = 4 - L;   // blocks (j + L, j), j = 0..nb-1
+    for (int e = tid; e < nb * 256; e += kThreads) {
+      const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + L;
+      const float *Arow = s.A + (16 * i + r) * LA;
+      float x = 0.f;
+      for (int kb = j; kb < i; ++kb) {   // T_{kb, j}: the diagonal block (in A) or one below it
+        const bool diag = kb == j;
+        const float *Tc = diag ? s.A + 16 * j * LA + 16 * j + c : s.Toff[kb * (kb - 1) / 2 + j] + c;
+        const int ld = diag ? LA : LB;
+#pragma unroll
+        for (int m4 = 0; m4 < 4; ++m4) {
+          const float4 a = *reinterpret_cast<const float4 *>(Arow + 16 * kb + 4 * m4);
+          x = fmaf(a.x, Tc[(4 * m4) * ld], x);
+          x = fmaf(a.y, Tc[(4 * m4 + 1) * ld], x);
+          x = fmaf(a.z, Tc[(4 * m4 + 2) * ld], x);
+          x = fmaf(a.w, Tc[(4 * m4 + 3) * ld], x);
+        }
+      }
+      s.X[j][r * LB + c] = x;
+    }
+    __syncthreads();
+    for (int e = tid; e < nb * 256; e += kThreads) {
+      const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + L;
+      const float *Trow = s.A + (16 * i + r) * LA + 16 * i;   // T_ii, lower triangular
+      const float *Xc = s.X[j] + c;
+      float x = 0.f;
+#pragma unroll
+      for (int m4 = 0; m4 < 4; ++m4) {
+        const float4 t = *reinterpret_cast<const float4 *>(Trow + 4 * m4);
+        x = fmaf(t.x, Xc[(4 * m4) * LB], x);
+        x = fmaf(t.y, Xc[(4 * m4 + 1) * LB], x);
+        x = fmaf(t.z, Xc[(4 * m4 + 2) * LB], x);
+        x = fmaf(t.w, Xc[(4 * m4 + 3) * LB], x);
+      }
+      s.Toff[i * (i - 1) / 2 + j][r * LB + c] = -x;
+    }
+    __syncthreads();
+  }
+}
 
 template <int DK, int DV>
 __global__ void __launch_bounds__(kThreads) gdn_bwdc_prep_kernel(const ChunkBwdParams P) {
   using S = PrepSmem<DK, DV>;
   using WS = ChunkWs<DK, DV>;
-  constexpr int LK = S::LK, LV = S::LV, LA = S::LA;
+  constexpr int LK = S::LK, LV = S::LV, LA = S::LA, LB = S::LB;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   S &s = *reinterpret_cast<S *>(smem_raw);
   const FwdParams &p = P.f;
@@ -278,21 +368,21 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_prep_kernel(const ChunkBwdP
   ws.carve(P.ws, P.slots * H);
 
   const size_t rq = ((size_t)tok0 * H + h) * DK, rv = ((size_t)tok0 * H + h) * DV;
-  load_rows<DK>(s.q, LK, static_cast<const bf16 *>(p.q) + rq, (size_t)H * DK, valid);
-  load_rows<DK>(s.k, LK, static_cast<const bf16 *>(p.k) + rq, (size_t)H * DK, valid);
-  load_rows<DV>(s.v, LV, static_cast<const bf16 *>(p.v) + rv, (size_t)H * DV, valid);
-  load_rows<DV>(s.o, LV, P.dO + rv, (size_t)H * DV, valid);
+  cp_tile<64, DK>(s.q, LK, static_cast<const bf16 *>(p.q) + rq, (size_t)H * DK, valid);
+  cp_tile<64, DK>(s.k, LK, static_cast<const bf16 *>(p.k) + rq, (size_t)H * DK, valid);
+  cp_tile<64, DV>(s.v, LV, static_cast<const bf16 *>(p.v) + rv, (size_t)H * DV, valid);
+  cp_tile<64, DV>(s.o, LV, P.dO + rv, (size_t)H * DV, valid);
+  cp_commit();
   chunk_gates(p.g, static_cast<const bf16 *>(p.beta), tok0, H, h, valid, s.G, s.gam, s.dec,
               s.beta, s.tmp);
+  cp_wait<0>();
   __syncthreads();
 
-  // scaled operands (bf16): gamma q, beta gamma k, beta v; K~ = dec k to the workspace
+  // scaled operands (bf16): beta gamma k, beta v; K~ = dec k to the workspace
   for (int idx = tid; idx < 64 * DK / 2; idx += kThreads) {
     const int i = idx / (DK / 2), d = 2 * (idx % (DK / 2));
-    const float q0 = bf(s.q[i * LK + d]), q1 = bf(s.q[i * LK + d + 1]);
     const float k0 = bf(s.k[i * LK + d]), k1 = bf(s.k[i * LK + d + 1]);
-    const float ga = s.gam[i], bg = s.beta[i] * s.gam[i], de = s.dec[i];
-    st_bf2(&s.gq[i * LK + d], ga * q0, ga * q1);
+    const float bg = s.beta[i] * s.gam[i], de = s.dec[i];
     st_bf2(&s.rw[i * LK + d], bg * k0, bg * k1);
     st_bf2(ws.Kt + unit * WS::kKt + i * DK + d, de * k0, de * k1);
   }
@@ -301,7 +391,8 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_prep_kernel(const ChunkBwdP
     const float b = s.beta[i];
     st_bf2(&s.ru[i * LV + c], b * bf(s.v[i * LV + c]), b * bf(s.v[i * LV + c + 1]));
   }
-  if (tid == 0) ws.gC[unit * 4] = s.gam[kC - 1];
+  if (tid == 0)   // gamma_C; the reverse chain adds the gradient of gamma_C into slot 1
+    *reinterpret_cast<float4 *>(ws.gC + unit * 4) = make_float4(s.gam[kC - 1], 0.f, 0.f, 0.f);
 
   // A = strictly_lower(diag(beta) K K^T (.) Gamma) in fp32; P = (Q K^T (.) Gamma)_{i>=j}
   {
@@ -320,25 +411,21 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_prep_kernel(const ChunkBwdP
     });
   }
   __syncthreads();
-
-  // T = (I + A)^-1 by forward substitution, one column per thread (fp32):
-  // T_ij = -sum_{j <= m < i} A_im T_mj below the diagonal, T_jj = 1.
-  if (tid < kC) {
-    const int j = tid;
-    float t[kC];
-#pragma unroll
-    for (int i = 0; i < kC; ++i) {
-      float a = 0.f;
-#pragma unroll
-      for (int m = 0; m < i; ++m) a = fmaf(s.A[i * LA + m], t[m], a);
-      t[i] = i < j ? 0.f : (i == j ? 1.f : -a);
+  block_inverse(s);
+  // T to bf16 (shared tile and workspace)
+  for (int idx = tid; idx < 64 * 32; idx += kThreads) {
+    const int i = idx >> 5, j = 2 * (idx & 31), bi = i >> 4, bj = j >> 4;
+    float t0 = 0.f, t1 = 0.f;
+    if (bi == bj) {
+      t0 = s.A[i * LA + j];
+      t1 = s.A[i * LA + j + 1];
+    } else if (bi > bj) {
+      const float *Tb = s.Toff[bi * (bi - 1) / 2 + bj] + (i & 15) * LB + (j & 15);
+      t0 = Tb[0];
+      t1 = Tb[1];
     }
-#pragma unroll
-    for (int i = 0; i < kC; ++i) {
-      const bf16 b = __float2bfloat16_rn(t[i]);
-      s.T[i * kLdC + j] = b;
-      ws.T[unit * WS::kT + i * kC + j] = b;
-    }
+    st_bf2(&s.T[i * kLdC + j], t0, t1);
+    st_bf2(ws.T + unit * WS::kT + i * kC + j, t0, t1);
   }
   __syncthreads();
 
@@ -358,6 +445,13 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_prep_kernel(const ChunkBwdP
     each2(acc, m0, 0, [&](int i, int c, float &x0, float &x1) { st_bf2(Ut + i * DV + c, x0, x1); });
   }
   // the state-free products of the reverse chain: dO^T P and dO^T diag(gamma) Q (fp32)
+  __syncthreads();   // W is done with diag(beta gamma) K
+  for (int idx = tid; idx < 64 * DK / 2; idx += kThreads) {
+    const int i = idx / (DK / 2), d = 2 * (idx % (DK / 2));
+    const float ga = s.gam[i];
+    st_bf2(&s.rw[i * LK + d], ga * bf(s.q[i * LK + d]), ga * bf(s.q[i * LK + d + 1]));
+  }
+  __syncthreads();
   for (int mt = warp; mt < DV / 16; mt += 4) {
     float acc[8][4];
     zero(acc);
@@ -368,7 +462,7 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_prep_kernel(const ChunkBwdP
     });
     float acc2[DK / 8][4];
     zero(acc2);
-    wmma<DK / 8, true, false>(acc2, s.o, LV, 16 * mt, s.gq, LK, 0, kC);
+    wmma<DK / 8, true, false>(acc2, s.o, LV, 16 * mt, s.rw, LK, 0, kC);
     float *X2 = ws.X2t + unit * WS::kX2;
     each2(acc2, 16 * mt, 0, [&](int c, int d, float &x0, float &x1) {
       *reinterpret_cast<float2 *>(X2 + c * DK + d) = make_float2(x0, x1);
@@ -377,26 +471,6 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_prep_kernel(const ChunkBwdP
 }
 
 // --------------------------------------------------------------- chains ----
-__device__ __forceinline__ void cp16(void *dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-// rows x (cols elements of `bytes_per` bytes) from a dense global matrix into a padded tile
-template <int ROWS, int ROW_BYTES>
-__device__ __forceinline__ void cp_rows(void *dst, int ld_bytes, const void *src) {
-  constexpr int V = ROW_BYTES / 16;
-  for (int idx = threadIdx.x; idx < ROWS * V; idx += kThreads) {
-    const int r = idx / V, c = (idx % V) * 16;
-    cp16(static_cast<uint8_t *>(dst) + r * ld_bytes + c,
-         static_cast<const uint8_t *>(src) + (size_t)r * ROW_BYTES + c);
-  }
-}
-
 template <int DK, int DV, bool REV>
 struct ChainSmem {
   static constexpr int LK = DK + 8, LV = DV + 8, LX1 = kC + 4, LX2 = DK + 4;
@@ -404,6 +478,7 @@ struct ChainSmem {
   bf16 Ut[REV ? 1 : 2][REV ? 8 : 64 * LV];
   float X1[REV ? 2 : 1][REV ? DV * LX1 : 4];
   float X2[REV ? 2 : 1][REV ? DV * LX2 : 4];
+  bf16 Hb[REV ? 2 : 1][REV ? DK * LV : 8];   // the state entering the chunk
   float gC[2][4];
 };
 
@@ -468,6 +543,7 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_chain_kernel(const ChunkBwd
     if (REV) {
       cp_rows<DV, kC * 4>(s.X1[buf], LX1 * 4, ws.X1t + unit * WS::kX1);
       cp_rows<DV, DK * 4>(s.X2[buf], LX2 * 4, ws.X2t + unit * WS::kX2);
+      cp_rows<DK, DV * 2>(s.Hb[buf], LV * 2, ws.Hb + unit * WS::kH);
     } else {
       cp_rows<64, DV * 2>(s.Ut[buf], LV * 2, ws.Ut + unit * WS::kUt);
     }
@@ -495,13 +571,20 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_chain_kernel(const ChunkBwd
     }
     __syncthreads();
     const size_t unit = (size_t)(ck0 + cc) * H + h;
-    float *out = (REV ? ws.dHs : ws.Hs) + unit * WS::kH;
+    bf16 *out = (REV ? ws.dHb : ws.Hb) + unit * WS::kH;
     const float gC = s.gC[buf][0];
     if (active) {
+      float dot = 0.f;   // reverse: <dH', H>, the gradient of gamma_C
       each2(st, c0, 0, [&](int c, int d, float &x0, float &x1) {
-        out[(size_t)d * DV + c] = x0;
-        out[(size_t)(d + 1) * DV + c] = x1;
+        out[(size_t)d * DV + c] = __float2bfloat16_rn(x0);
+        out[(size_t)(d + 1) * DV + c] = __float2bfloat16_rn(x1);
+        if (REV) dot += x0 * bf(s.Hb[buf][d * LV + c]) + x1 * bf(s.Hb[buf][(d + 1) * LV + c]);
       });
+      if (REV) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        if ((threadIdx.x & 31) == 0) atomicAdd(ws.gC + unit * 4 + 1, dot);
+      }
       float u[8][4];   // 16 value columns x 64 tokens
       if (!REV) {
         zero(u);
@@ -528,25 +611,43 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_chain_kernel(const ChunkBwd
 // ----------------------------------------------------------------- grad ----
 template <int DK, int DV>
 struct GradSmem {
-  static constexpr int LK = DK + 8, LV = DV + 8, LF = 68;
+  static constexpr int LK = DK + 8, LV = DV + 8, LO = LV > kLdC ? LV : kLdC;
   static constexpr int R1 = (DK * LV > 64 * LK ? DK * LV : 64 * LK);  // H, then dR_W
   static constexpr int R2 = (DK * LV > 64 * LV ? DK * LV : 64 * LV);  // dH', then dR_U
   bf16 q[64 * LK], k[64 * LK], W[64 * LK], KtDW[64 * LK];  // K~, then dW
-  bf16 v[64 * LV], o[64 * LV], Ut[64 * LV], U[64 * LV], dU[64 * LV];
-  bf16 dUlo[64 * LV], dWlo[64 * LK];  // what rounding dU and dW to bf16 left out
-  bf16 T[64 * kLdC], PDP[64 * kLdC], SA[64 * kLdC];        // P, then dP (.) Gamma
+  bf16 UU[64 * LV];    // U~, U over it, then U~ again
+  bf16 dU[64 * LV];
+  bf16 oD[64 * LO];    // dO (row stride LV), then v (LV), then diag(beta) D (kLdC)
+  bf16 T[64 * kLdC], PDP[64 * kLdC];  // P, then dP (.) Gamma
   bf16 r1[R1], r2[R2];
-  float QK[64 * LF], KK[64 * LF], DA[64 * LF];             // QK, then the gate terms E
   float G[64], gam[64], dec[64], beta[64];
-  float dgam[64], dbg[64], ddec[64], dbU[64], dbA[64], dG[64], dB[64];
-  float tmp[4], red[4], red2[4];
+  float dgam[64], dbg[64], ddec[64], dB[64], Erow[64], Ecol[64], dG[64];
+  float tmp[4];
 };
+
+// Column sums over the warp's 16 rows of a 16 x 64 accumulator, added into col[].
+__device__ __forceinline__ void add_col_sums(const float (&e)[8][4], float *col) {
+  const int l = threadIdx.x & 31;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    float c0 = e[t][0] + e[t][2], c1 = e[t][1] + e[t][3];
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      c0 += __shfl_xor_sync(0xffffffffu, c0, o);
+      c1 += __shfl_xor_sync(0xffffffffu, c1, o);
+    }
+    if (l < 4) {
+      atomicAdd(col + 8 * t + 2 * l, c0);
+      atomicAdd(col + 8 * t + 2 * l + 1, c1);
+    }
+  }
+}
 
 template <int DK, int DV>
 __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdParams P) {
   using S = GradSmem<DK, DV>;
   using WS = ChunkWs<DK, DV>;
-  constexpr int LK = S::LK, LV = S::LV, LF = S::LF;
+  constexpr int LK = S::LK, LV = S::LV;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   S &s = *reinterpret_cast<S *>(smem_raw);
   const FwdParams &p = P.f;
@@ -562,105 +663,100 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdP
   ws.carve(P.ws, P.slots * H);
   bf16 *sH = s.r1, *sDRW = s.r1, *sDH = s.r2, *sDRU = s.r2;
 
-  // ---- loads: the chunk's inputs, the prep's tiles, H and dH' (bf16 copies) ----
+  // ---- loads: every tile in flight at once ----
   const size_t rq = ((size_t)tok0 * H + h) * DK, rv = ((size_t)tok0 * H + h) * DV;
-  load_rows<DK>(s.q, LK, static_cast<const bf16 *>(p.q) + rq, (size_t)H * DK, valid);
-  load_rows<DK>(s.k, LK, static_cast<const bf16 *>(p.k) + rq, (size_t)H * DK, valid);
-  load_rows<DV>(s.v, LV, static_cast<const bf16 *>(p.v) + rv, (size_t)H * DV, valid);
-  load_rows<DV>(s.o, LV, P.dO + rv, (size_t)H * DV, valid);
-  load_rows<DK>(s.W, LK, ws.W + unit * WS::kW, DK, kC);
-  load_rows<DK>(s.KtDW, LK, ws.Kt + unit * WS::kKt, DK, kC);
-  load_rows<DV>(s.Ut, LV, ws.Ut + unit * WS::kUt, DV, kC);
-  load_rows<kC>(s.T, kLdC, ws.T + unit * WS::kT, kC, kC);
-  float part = 0.f;   // <dH', H>, the gradient of gamma_C
-  {
-    const float *Hs = ws.Hs + unit * WS::kH, *dHs = ws.dHs + unit * WS::kH;
-    for (int idx = tid; idx < DK * DV / 4; idx += kThreads) {
-      const int d = (4 * idx) / DV, c = (4 * idx) % DV;
-      const float4 a = *reinterpret_cast<const float4 *>(Hs + 4 * idx);
-      const float4 b = *reinterpret_cast<const float4 *>(dHs + 4 * idx);
-      part += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
-      *reinterpret_cast<uint2 *>(sH + d * LV + c) = make_uint2(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w));
-      *reinterpret_cast<uint2 *>(sDH + d * LV + c) = make_uint2(pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-  if (lane == 0) s.red[warp] = part;
+  cp_tile<64, DK>(s.q, LK, static_cast<const bf16 *>(p.q) + rq, (size_t)H * DK, valid);
+  cp_tile<64, DK>(s.k, LK, static_cast<const bf16 *>(p.k) + rq, (size_t)H * DK, valid);
+  cp_tile<64, DV>(s.oD, LV, P.dO + rv, (size_t)H * DV, valid);
+  cp_tile<64, DK>(s.W, LK, ws.W + unit * WS::kW, DK, kC);
+  cp_tile<64, DK>(s.KtDW, LK, ws.Kt + unit * WS::kKt, DK, kC);
+  cp_tile<64, DV>(s.UU, LV, ws.Ut + unit * WS::kUt, DV, kC);
+  cp_tile<64, kC>(s.T, kLdC, ws.T + unit * WS::kT, kC, kC);
+  cp_tile<DK, DV>(sH, LV, ws.Hb + unit * WS::kH, DV, DK);
+  cp_tile<DK, DV>(sDH, LV, ws.dHb + unit * WS::kH, DV, DK);
+  cp_commit();
+  if (tid < kC) { s.Ecol[tid] = 0.f; }
   chunk_gates(p.g, static_cast<const bf16 *>(p.beta), tok0, H, h, valid, s.G, s.gam, s.dec,
               s.beta, s.tmp);
+  const float4 gcv = *reinterpret_cast<const float4 *>(ws.gC + unit * 4);
+  const float gC = gcv.x, dgC = gcv.y;
+  cp_wait<0>();
   __syncthreads();
-  const float dgC = s.red[0] + s.red[1] + s.red[2] + s.red[3];
-  const float gC = s.gam[kC - 1];
 
-  // ---- P, Q K^T, K K^T, U = U~ - W H ----
+  // ---- P, U = U~ - W H ----
   {
     float acc[8][4];
     zero(acc);
     wmma<8, false, true>(acc, s.q, LK, m0, s.k, LK, 0, DK);
     each2(acc, m0, 0, [&](int i, int j, float &x0, float &x1) {
-      s.QK[i * LF + j] = x0;
-      s.QK[i * LF + j + 1] = x1;
       const float p0 = i >= j ? x0 * expf(s.G[i] - s.G[j]) : 0.f;
       const float p1 = i >= j + 1 ? x1 * expf(s.G[i] - s.G[j + 1]) : 0.f;
       st_bf2(&s.PDP[i * kLdC + j], p0, p1);
-    });
-    zero(acc);
-    wmma<8, false, true>(acc, s.k, LK, m0, s.k, LK, 0, DK);
-    each2(acc, m0, 0, [&](int i, int j, float &x0, float &x1) {
-      s.KK[i * LF + j] = x0;
-      s.KK[i * LF + j + 1] = x1;
     });
   }
   {
     float acc[DV / 8][4];
     zero(acc);
     wmma<DV / 8, false, false>(acc, s.W, LK, m0, sH, LV, 0, DK);
-    each2(acc, m0, 0, [&](int i, int c, float &x0, float &x1) {
-      st_bf2(&s.U[i * LV + c], bf(s.Ut[i * LV + c]) - x0, bf(s.Ut[i * LV + c + 1]) - x1);
+    each2(acc, m0, 0, [&](int i, int c, float &x0, float &x1) {   // U over U~, in place
+      st_bf2(&s.UU[i * LV + c], bf(s.UU[i * LV + c]) - x0, bf(s.UU[i * LV + c + 1]) - x1);
     });
   }
   __syncthreads();
-  // dU = P^T dO + K~ dH'
+  // dU = P^T dO + K~ dH'; what rounding it to bf16 leaves out stays in registers
+  uint32_t dUr[DV / 8][2], dWr[DK / 8][2];
   {
     float acc[DV / 8][4];
     zero(acc);
-    wmma<DV / 8, true, false>(acc, s.PDP, kLdC, m0, s.o, LV, 0, kC);
+    wmma<DV / 8, true, false>(acc, s.PDP, kLdC, m0, s.oD, LV, 0, kC);
     wmma<DV / 8, false, false>(acc, s.KtDW, LK, m0, sDH, LV, 0, DK);
-    each2(acc, m0, 0, [&](int i, int c, float &x0, float &x1) {
-      st_bf2(&s.dU[i * LV + c], x0, x1);
-      st_bf2(&s.dUlo[i * LV + c], x0 - rbf(x0), x1 - rbf(x1));
-    });
+    each2(acc, m0, 0, [&](int i, int c, float &x0, float &x1) { st_bf2(&s.dU[i * LV + c], x0, x1); });
+#pragma unroll
+    for (int t = 0; t < DV / 8; ++t) {
+      dUr[t][0] = pack_bf16(acc[t][0] - rbf(acc[t][0]), acc[t][1] - rbf(acc[t][1]));
+      dUr[t][1] = pack_bf16(acc[t][2] - rbf(acc[t][2]), acc[t][3] - rbf(acc[t][3]));
+    }
   }
   __syncthreads();
 
-  // ---- dP, dW, dK~, dO H^T ----
+  // ---- dP (.) Gamma and its gate terms, dW, dK~, dO H^T ----
+  float erow0 = 0.f, erow1 = 0.f;   // row sums of the gate terms E (rows r0, r0 + 8)
   {
-    float acc[8][4];
+    float acc[8][4], qk[8][4];
     zero(acc);
-    wmma<8, false, true>(acc, s.o, LV, m0, s.U, LV, 0, DV);
-    each2(acc, m0, 0, [&](int i, int j, float &x0, float &x1) {
-      float d0 = 0.f, d1 = 0.f;
-      if (i >= j) d0 = x0 * expf(s.G[i] - s.G[j]);
-      if (i >= j + 1) d1 = x1 * expf(s.G[i] - s.G[j + 1]);
-      st_bf2(&s.PDP[i * kLdC + j], d0, d1);
-      s.QK[i * LF + j] = d0 * s.QK[i * LF + j];
-      s.QK[i * LF + j + 1] = d1 * s.QK[i * LF + j + 1];
-    });
+    wmma<8, false, true>(acc, s.oD, LV, m0, s.UU, LV, 0, DV);
+    zero(qk);
+    wmma<8, false, true>(qk, s.q, LK, m0, s.k, LK, 0, DK);
+    // E = dP (.) Gamma (.) Q K^T on and below the diagonal
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = r0 + (e >= 2 ? 8 : 0), j = 8 * t + 2 * (lane & 3) + (e & 1);
+        const float d = i >= j ? acc[t][e] * expf(s.G[i] - s.G[j]) : 0.f;
+        acc[t][e] = d;
+        qk[t][e] *= d;
+        if (e < 2) erow0 += qk[t][e]; else erow1 += qk[t][e];
+      }
+    }
+    each2(acc, m0, 0, [&](int i, int j, float &x0, float &x1) { st_bf2(&s.PDP[i * kLdC + j], x0, x1); });
+    add_col_sums(qk, s.Ecol);
   }
   {
     float acc[DK / 8][4];
     zero(acc);
     wmma<DK / 8, false, true>(acc, s.dU, LV, m0, sH, LV, 0, DV);
-    each2(acc, m0, 0, [&](int i, int d, float &x0, float &x1) {
-      st_bf2(&s.KtDW[i * LK + d], -x0, -x1);
-      st_bf2(&s.dWlo[i * LK + d], rbf(x0) - x0, rbf(x1) - x1);
-    });
+    each2(acc, m0, 0, [&](int i, int d, float &x0, float &x1) { st_bf2(&s.KtDW[i * LK + d], -x0, -x1); });
+#pragma unroll
+    for (int t = 0; t < DK / 8; ++t) {
+      dWr[t][0] = pack_bf16(rbf(acc[t][0]) - acc[t][0], rbf(acc[t][1]) - acc[t][1]);
+      dWr[t][1] = pack_bf16(rbf(acc[t][2]) - acc[t][2], rbf(acc[t][3]) - acc[t][3]);
+    }
   }
   float dK[DK / 8][4], dQ[DK / 8][4];
   {
     zero(dK);
-    wmma<DK / 8, false, true>(dK, s.U, LV, m0, sDH, LV, 0, DV);   // dK~ = U dH'^T
+    wmma<DK / 8, false, true>(dK, s.UU, LV, m0, sDH, LV, 0, DV);   // dK~ = U dH'^T
     float p0 = 0.f, p1 = 0.f;
     each2(dK, m0, 0, [&](int i, int d, float &x0, float &x1) {
       const float e = x0 * bf(s.k[i * LK + d]) + x1 * bf(s.k[i * LK + d + 1]);
@@ -672,7 +768,7 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdP
     p1 = quad_sum(p1);
     if ((lane & 3) == 0) { s.ddec[r0] = p0; s.ddec[r0 + 8] = p1; }
     zero(dQ);
-    wmma<DK / 8, false, true>(dQ, s.o, LV, m0, sH, LV, 0, DV);   // dO H^T
+    wmma<DK / 8, false, true>(dQ, s.oD, LV, m0, sH, LV, 0, DV);   // dO H^T
     p0 = p1 = 0.f;
     each2(dQ, m0, 0, [&](int i, int d, float &x0, float &x1) {
       const float e = x0 * bf(s.q[i * LK + d]) + x1 * bf(s.q[i * LK + d + 1]);
@@ -687,11 +783,19 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdP
   __syncthreads();
 
   // ---- dR_W = T^T dW, dR_U = T^T dU, dV, dQ ----
+  // U and dO are spent: U~ comes back for dA, v takes dO's place
+  cp_tile<64, DV>(s.UU, LV, ws.Ut + unit * WS::kUt, DV, kC);
+  cp_tile<64, DV>(s.oD, LV, static_cast<const bf16 *>(p.v) + rv, (size_t)H * DV, valid);
+  cp_commit();
   {
     float acc[DK / 8][4];
     zero(acc);
     wmma<DK / 8, true, false>(acc, s.T, kLdC, m0, s.KtDW, LK, 0, kC);
-    wmma<DK / 8, true, false>(acc, s.T, kLdC, m0, s.dWlo, LK, 0, kC);
+#pragma unroll
+    for (int t = 0; t < DK / 8; ++t) {   // T's diagonal is 1: the rounding remainder of dW
+      acc[t][0] += bf16_lo(dWr[t][0]); acc[t][1] += bf16_hi(dWr[t][0]);
+      acc[t][2] += bf16_lo(dWr[t][1]); acc[t][3] += bf16_hi(dWr[t][1]);
+    }
     float p0 = 0.f, p1 = 0.f;
     each2(acc, m0, 0, [&](int i, int d, float &x0, float &x1) {
       const float e = x0 * bf(s.k[i * LK + d]) + x1 * bf(s.k[i * LK + d + 1]);
@@ -714,10 +818,16 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdP
     float acc[DV / 8][4];
     zero(acc);
     wmma<DV / 8, true, false>(acc, s.T, kLdC, m0, s.dU, LV, 0, kC);
-    wmma<DV / 8, true, false>(acc, s.T, kLdC, m0, s.dUlo, LV, 0, kC);
+#pragma unroll
+    for (int t = 0; t < DV / 8; ++t) {
+      acc[t][0] += bf16_lo(dUr[t][0]); acc[t][1] += bf16_hi(dUr[t][0]);
+      acc[t][2] += bf16_lo(dUr[t][1]); acc[t][3] += bf16_hi(dUr[t][1]);
+    }
+    cp_wait<0>();
+    __syncthreads();   // v and U~ landed
     float p0 = 0.f, p1 = 0.f;
     each2(acc, m0, 0, [&](int i, int c, float &x0, float &x1) {
-      const float e = x0 * bf(s.v[i * LV + c]) + x1 * bf(s.v[i * LV + c + 1]);
+      const float e = x0 * bf(s.oD[i * LV + c]) + x1 * bf(s.oD[i * LV + c + 1]);
       if (i == r0) p0 += e; else p1 += e;
       st_bf2(&sDRU[i * LV + c], x0, x1);
       if (i < valid)
@@ -726,7 +836,7 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdP
     });
     p0 = quad_sum(p0);
     p1 = quad_sum(p1);
-    if ((lane & 3) == 0) { s.dbU[r0] = p0; s.dbU[r0 + 8] = p1; }
+    if ((lane & 3) == 0) { s.dB[r0] = p0; s.dB[r0 + 8] = p1; }
   }
   wmma<DK / 8, false, false>(dQ, s.PDP, kLdC, m0, s.k, LK, 0, kC);   // + (dP (.) Gamma) K
   each2(dQ, m0, 0, [&](int i, int d, float &x0, float &x1) {
@@ -735,37 +845,43 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdP
   });
   __syncthreads();
 
-  // ---- dA = -(dR_W W^T + dR_U U~^T), D = dA (.) Gamma ----
+  // ---- dA = -(dR_W W^T + dR_U U~^T), D = dA (.) Gamma below the diagonal ----
   {
-    float acc[8][4];
+    float acc[8][4], kk[8][4];
     zero(acc);
     wmma<8, false, true>(acc, sDRW, LK, m0, s.W, LK, 0, DK);
-    wmma<8, false, true>(acc, sDRU, LV, m0, s.Ut, LV, 0, DV);
+    wmma<8, false, true>(acc, sDRU, LV, m0, s.UU, LV, 0, DV);
+    zero(kk);
+    wmma<8, false, true>(kk, s.k, LK, m0, s.k, LK, 0, DK);
     float p0 = 0.f, p1 = 0.f;
-    each(acc, m0, 0, [&](int i, int j, float &x) {
-      float D = 0.f;
-      if (i > j) {
-        D = -x * expf(s.G[i] - s.G[j]);
-        const float kk = s.KK[i * LF + j];
-        s.QK[i * LF + j] += s.beta[i] * D * kk;
-        if (i == r0) p0 += D * kk; else p1 += D * kk;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = r0 + (e >= 2 ? 8 : 0), j = 8 * t + 2 * (lane & 3) + (e & 1);
+        const float D = i > j ? -acc[t][e] * expf(s.G[i] - s.G[j]) : 0.f;
+        const float dk = D * kk[t][e];            // the dbeta term; beta_i times it is E
+        if (e < 2) { p0 += dk; erow0 += s.beta[i] * dk; } else { p1 += dk; erow1 += s.beta[i] * dk; }
+        kk[t][e] = s.beta[i] * dk;
+        acc[t][e] = s.beta[i] * D;                // diag(beta) D
       }
-      s.DA[i * LF + j] = D;
-    });
+    }
+    add_col_sums(kk, s.Ecol);
+    each2(acc, m0, 0, [&](int i, int j, float &x0, float &x1) { st_bf2(&s.oD[i * kLdC + j], x0, x1); });
     p0 = quad_sum(p0);
     p1 = quad_sum(p1);
-    if ((lane & 3) == 0) { s.dbA[r0] = p0; s.dbA[r0 + 8] = p1; }
-  }
-  __syncthreads();
-  for (int idx = tid; idx < kC * kC / 2; idx += kThreads) {
-    const int i = idx / (kC / 2), j = 2 * (idx % (kC / 2));
-    st_bf2(&s.SA[i * kLdC + j], s.beta[i] * s.DA[i * LF + j] + s.DA[j * LF + i] * s.beta[j],
-           s.beta[i] * s.DA[i * LF + j + 1] + s.DA[(j + 1) * LF + i] * s.beta[j + 1]);
+    erow0 = quad_sum(erow0);
+    erow1 = quad_sum(erow1);
+    if ((lane & 3) == 0) {
+      s.dB[r0] += p0; s.dB[r0 + 8] += p1;
+      s.Erow[r0] = erow0; s.Erow[r0 + 8] = erow1;
+    }
   }
   __syncthreads();
 
-  // ---- dK += S K + (dP (.) Gamma)^T Q ----
-  wmma<DK / 8, false, false>(dK, s.SA, kLdC, m0, s.k, LK, 0, kC);
+  // ---- dK += (diag(beta) D) K + (diag(beta) D)^T K + (dP (.) Gamma)^T Q ----
+  wmma<DK / 8, false, false>(dK, s.oD, kLdC, m0, s.k, LK, 0, kC);
+  wmma<DK / 8, true, false>(dK, s.oD, kLdC, m0, s.k, LK, 0, kC);
   wmma<DK / 8, true, false>(dK, s.PDP, kLdC, m0, s.q, LK, 0, kC);
   each2(dK, m0, 0, [&](int i, int d, float &x0, float &x1) {
     if (i < valid)
@@ -773,35 +889,29 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdP
   });
 
   // ---- gates: dG per token, then dg = its sum over later tokens of the chunk ----
-  float xdec = 0.f;
   if (tid < kC) {
     const int i = tid;
-    float rs = 0.f, cs = 0.f;
-    for (int m = 0; m < kC; ++m) {
-      rs += s.QK[i * LF + m];
-      cs += s.QK[m * LF + i];
-    }
     const float dgt = s.dgam[i] + s.beta[i] * s.dbg[i];
-    s.dG[i] = rs - cs + s.gam[i] * dgt - s.dec[i] * s.ddec[i];
-    s.dB[i] = s.dbU[i] + s.dbA[i] + s.gam[i] * s.dbg[i];
-    xdec = s.dec[i] * s.ddec[i];
+    s.dG[i] = s.Erow[i] - s.Ecol[i] + s.gam[i] * dgt - s.dec[i] * s.ddec[i];
+    s.dB[i] += s.gam[i] * s.dbg[i];
+    float xdec = s.dec[i] * s.ddec[i];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) xdec += __shfl_xor_sync(0xffffffffu, xdec, o);
-    if (lane == 0) s.red2[warp] = xdec;
+    if (lane == 0) s.tmp[2 + warp] = xdec;
   }
   __syncthreads();
   if (tid < kC) {
     // suffix sums: thread t takes token 63 - t
     const int t = tid, i = kC - 1 - t;
     float x = s.dG[i];
-    if (i == kC - 1) x += gC * dgC + s.red2[0] + s.red2[1];
+    if (i == kC - 1) x += gC * dgC + s.tmp[2] + s.tmp[3];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float y = __shfl_up_sync(0xffffffffu, x, o);
       if (lane >= o) x += y;
     }
     if (t == 31) s.tmp[1] = x;
-    s.dG[i] = x;   // own slot only; the other warp's total is added below
+    s.dG[i] = x;
   }
   __syncthreads();
   if (tid < kC) {
