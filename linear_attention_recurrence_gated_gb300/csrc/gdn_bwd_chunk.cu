@@ -132,10 +132,10 @@ __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 // rows x (cols elements of `bytes_per` bytes) from a dense global matrix into a padded tile
-template <int ROWS, int ROW_BYTES>
+template <int ROWS, int ROW_BYTES, int NTH = kThreads>
 __device__ __forceinline__ void cp_rows(void *dst, int ld_bytes, const void *src) {
   constexpr int V = ROW_BYTES / 16;
-  for (int idx = threadIdx.x; idx < ROWS * V; idx += kThreads) {
+  for (int idx = threadIdx.x; idx < ROWS * V; idx += NTH) {
     const int r = idx / V, c = (idx % V) * 16;
     cp16(static_cast<uint8_t *>(dst) + r * ld_bytes + c,
          static_cast<const uint8_t *>(src) + (size_t)r * ROW_BYTES + c);
@@ -144,11 +144,11 @@ __device__ __forceinline__ void cp_rows(void *dst, int ld_bytes, const void *src
 
 // rows [0, ROWS) of a bf16 matrix with COLS columns (global row stride gstride
 // elements) into a padded shared tile with cp.async; rows >= valid are zero.
-template <int ROWS, int COLS>
+template <int ROWS, int COLS, int NTH = kThreads>
 __device__ __forceinline__ void cp_tile(bf16 *dst, int ld, const bf16 *src, size_t gstride,
                                         int valid) {
   constexpr int V = COLS / 8;  // 16-byte pieces per row
-  for (int idx = threadIdx.x; idx < ROWS * V; idx += kThreads) {
+  for (int idx = threadIdx.x; idx < ROWS * V; idx += NTH) {
     const int r = idx / V, c = (idx % V) * 8;
     const bool ok = r < valid;
     const bf16 *g = src + (ok ? (size_t)r * gstride + c : 0);
@@ -159,11 +159,12 @@ __device__ __forceinline__ void cp_tile(bf16 *dst, int ld, const bf16 *src, size
 }
 
 // Chunk gates for tokens i < 64 (threads 0..63): G (inclusive prefix sum of g in
-// fp32, the same order in every kernel), gamma, dec and beta.  Tokens past the
-// chunk's end have g = 0 and beta = 0.  Needs a __syncthreads() after.
+// fp32, the same order in every kernel), G log2(e), gamma, dec and beta.  Tokens
+// past the chunk's end have g = 0 and beta = 0.  Needs a __syncthreads() after.
 __device__ __forceinline__ void chunk_gates(const float *g, const bf16 *beta, int64_t tok0,
-                                            int H, int h, int valid, float *sG, float *sGam,
-                                            float *sDec, float *sBeta, float *sTmp) {
+                                            int H, int h, int valid, float *sG, float *sGl,
+                                            float *sGam, float *sDec, float *sBeta,
+                                            float *sTmp) {
   const int i = threadIdx.x, lane = i & 31;
   float x = 0.f, b = 0.f;
   if (i < kC && i < valid) {
@@ -183,6 +184,7 @@ __device__ __forceinline__ void chunk_gates(const float *g, const bf16 *beta, in
   if (i < kC) {
     if (i >= 32) x += sTmp[0];
     sG[i] = x;
+    sGl[i] = x * 1.4426950408889634f;
     sBeta[i] = b;
     sGam[i] = expf(x);
   }
@@ -265,12 +267,17 @@ __device__ __forceinline__ void each2(float (&acc)[NT][4], int m0, int n0, F &&f
 }
 
 __device__ __forceinline__ float bf(const bf16 &x) { return __bfloat162float(x); }
+// Gamma_ij = exp(G_i - G_j) <= 1 is taken as 2^(G_i log2 e - G_j log2 e) with the
+// hardware exp2 (decays below 2^-126 flush to zero).
 __device__ __forceinline__ float rbf(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 __device__ __forceinline__ void st_bf2(bf16 *p, float a, float b) {
   *reinterpret_cast<uint32_t *>(p) = pack_bf16(a, b);
 }
 
 // ---------------------------------------------------------------- prep ----
+// 8 warps: warp w owns rows 16 (w % 4).. of a chunk product and half of its columns.
+constexpr int kPrepThreads = 256;
+
 template <int DK, int DV>
 struct PrepSmem {
   static constexpr int LK = DK + 8, LV = DV + 8, LA = 68, LB = 17;
@@ -280,7 +287,7 @@ struct PrepSmem {
   float A[64 * LA];            // A; its diagonal 16 x 16 blocks become T's
   float Toff[6][16 * LB];      // T's blocks below the diagonal, (i, j) at i (i - 1) / 2 + j
   float X[3][16 * LB];         // scratch of the block substitution
-  float G[64], gam[64], dec[64], beta[64], tmp[4];
+  float G[64], Gl[64], gam[64], dec[64], beta[64], tmp[4];
 };
 
 // T = (I + A)^-1 of a strictly lower A (fp32), in 16 x 16 blocks: the diagonal
@@ -310,7 +317,7 @@ __device__ __forceinline__ void block_inverse(PrepSmem<DK, DV> &s) {
   __syncthreads();
   for (int L = 1; L < 4; ++L) {
     const int nb = 4 - L;   // blocks (j + L, j), j = 0..nb-1
-    for (int e = tid; e < nb * 256; e += kThreads) {
+    for (int e = tid; e < nb * 256; e += kPrepThreads) {
       const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + L;
       const float *Arow = s.A + (16 * i + r) * LA;
       float x = 0.f;
@@ -330,7 +337,7 @@ __device__ __forceinline__ void block_inverse(PrepSmem<DK, DV> &s) {
       s.X[j][r * LB + c] = x;
     }
     __syncthreads();
-    for (int e = tid; e < nb * 256; e += kThreads) {
+    for (int e = tid; e < nb * 256; e += kPrepThreads) {
       const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + L;
       const float *Trow = s.A + (16 * i + r) * LA + 16 * i;   // T_ii, lower triangular
       const float *Xc = s.X[j] + c;
@@ -350,7 +357,7 @@ __device__ __forceinline__ void block_inverse(PrepSmem<DK, DV> &s) {
 }
 
 template <int DK, int DV>
-__global__ void __launch_bounds__(kThreads) gdn_bwdc_prep_kernel(const ChunkBwdParams P) {
+__global__ void __launch_bounds__(kPrepThreads) gdn_bwdc_prep_kernel(const ChunkBwdParams P) {
   using S = PrepSmem<DK, DV>;
   using WS = ChunkWs<DK, DV>;
   constexpr int LK = S::LK, LV = S::LV, LA = S::LA, LB = S::LB;
@@ -362,31 +369,32 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_prep_kernel(const ChunkBwdP
   int n, valid;
   int64_t tok0;
   if (!slot_chunk(p, slot, h, n, tok0, valid)) return;
-  const int H = p.num_heads, tid = threadIdx.x, warp = tid >> 5, m0 = 16 * warp;
+  const int H = p.num_heads, tid = threadIdx.x, warp = tid >> 5, m0 = 16 * (warp & 3);
+  const int half = warp >> 2;   // column half of the products
   const size_t unit = (size_t)slot * H + h;
   WS ws;
   ws.carve(P.ws, P.slots * H);
 
   const size_t rq = ((size_t)tok0 * H + h) * DK, rv = ((size_t)tok0 * H + h) * DV;
-  cp_tile<64, DK>(s.q, LK, static_cast<const bf16 *>(p.q) + rq, (size_t)H * DK, valid);
-  cp_tile<64, DK>(s.k, LK, static_cast<const bf16 *>(p.k) + rq, (size_t)H * DK, valid);
-  cp_tile<64, DV>(s.v, LV, static_cast<const bf16 *>(p.v) + rv, (size_t)H * DV, valid);
-  cp_tile<64, DV>(s.o, LV, P.dO + rv, (size_t)H * DV, valid);
+  cp_tile<64, DK, kPrepThreads>(s.q, LK, static_cast<const bf16 *>(p.q) + rq, (size_t)H * DK, valid);
+  cp_tile<64, DK, kPrepThreads>(s.k, LK, static_cast<const bf16 *>(p.k) + rq, (size_t)H * DK, valid);
+  cp_tile<64, DV, kPrepThreads>(s.v, LV, static_cast<const bf16 *>(p.v) + rv, (size_t)H * DV, valid);
+  cp_tile<64, DV, kPrepThreads>(s.o, LV, P.dO + rv, (size_t)H * DV, valid);
   cp_commit();
-  chunk_gates(p.g, static_cast<const bf16 *>(p.beta), tok0, H, h, valid, s.G, s.gam, s.dec,
-              s.beta, s.tmp);
+  chunk_gates(p.g, static_cast<const bf16 *>(p.beta), tok0, H, h, valid, s.G, s.Gl, s.gam,
+              s.dec, s.beta, s.tmp);
   cp_wait<0>();
   __syncthreads();
 
   // scaled operands (bf16): beta gamma k, beta v; K~ = dec k to the workspace
-  for (int idx = tid; idx < 64 * DK / 2; idx += kThreads) {
+  for (int idx = tid; idx < 64 * DK / 2; idx += kPrepThreads) {
     const int i = idx / (DK / 2), d = 2 * (idx % (DK / 2));
     const float k0 = bf(s.k[i * LK + d]), k1 = bf(s.k[i * LK + d + 1]);
     const float bg = s.beta[i] * s.gam[i], de = s.dec[i];
     st_bf2(&s.rw[i * LK + d], bg * k0, bg * k1);
     st_bf2(ws.Kt + unit * WS::kKt + i * DK + d, de * k0, de * k1);
   }
-  for (int idx = tid; idx < 64 * DV / 2; idx += kThreads) {
+  for (int idx = tid; idx < 64 * DV / 2; idx += kPrepThreads) {
     const int i = idx / (DV / 2), c = 2 * (idx % (DV / 2));
     const float b = s.beta[i];
     st_bf2(&s.ru[i * LV + c], b * bf(s.v[i * LV + c]), b * bf(s.v[i * LV + c + 1]));
@@ -396,24 +404,24 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_prep_kernel(const ChunkBwdP
 
   // A = strictly_lower(diag(beta) K K^T (.) Gamma) in fp32; P = (Q K^T (.) Gamma)_{i>=j}
   {
-    float acc[8][4];
+    float acc[4][4];
     zero(acc);
-    wmma<8, false, true>(acc, s.k, LK, m0, s.k, LK, 0, DK);
-    each(acc, m0, 0, [&](int i, int j, float &x) {
-      s.A[i * LA + j] = i > j ? s.beta[i] * x * expf(s.G[i] - s.G[j]) : 0.f;
+    wmma<4, false, true>(acc, s.k, LK, m0, s.k, LK, 32 * half, DK);
+    each(acc, m0, 32 * half, [&](int i, int j, float &x) {
+      s.A[i * LA + j] = i > j ? s.beta[i] * x * ex2(s.Gl[i] - s.Gl[j]) : 0.f;
     });
     zero(acc);
-    wmma<8, false, true>(acc, s.q, LK, m0, s.k, LK, 0, DK);
-    each2(acc, m0, 0, [&](int i, int j, float &x0, float &x1) {
-      const float p0 = i >= j ? x0 * expf(s.G[i] - s.G[j]) : 0.f;
-      const float p1 = i >= j + 1 ? x1 * expf(s.G[i] - s.G[j + 1]) : 0.f;
+    wmma<4, false, true>(acc, s.q, LK, m0, s.k, LK, 32 * half, DK);
+    each2(acc, m0, 32 * half, [&](int i, int j, float &x0, float &x1) {
+      const float p0 = i >= j ? x0 * ex2(s.Gl[i] - s.Gl[j]) : 0.f;
+      const float p1 = i >= j + 1 ? x1 * ex2(s.Gl[i] - s.Gl[j + 1]) : 0.f;
       st_bf2(&s.P[i * kLdC + j], p0, p1);
     });
   }
   __syncthreads();
   block_inverse(s);
   // T to bf16 (shared tile and workspace)
-  for (int idx = tid; idx < 64 * 32; idx += kThreads) {
+  for (int idx = tid; idx < 64 * 32; idx += kPrepThreads) {
     const int i = idx >> 5, j = 2 * (idx & 31), bi = i >> 4, bj = j >> 4;
     float t0 = 0.f, t1 = 0.f;
     if (bi == bj) {
@@ -431,40 +439,40 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_prep_kernel(const ChunkBwdP
 
   // W = T diag(beta gamma) K, U~ = T diag(beta) V (bf16 to the workspace)
   {
-    float acc[DK / 8][4];
+    float acc[DK / 16][4];
     zero(acc);
-    wmma<DK / 8, false, false>(acc, s.T, kLdC, m0, s.rw, LK, 0, kC);
+    wmma<DK / 16, false, false>(acc, s.T, kLdC, m0, s.rw, LK, DK / 2 * half, kC);
     bf16 *W = ws.W + unit * WS::kW;
-    each2(acc, m0, 0, [&](int i, int d, float &x0, float &x1) { st_bf2(W + i * DK + d, x0, x1); });
+    each2(acc, m0, DK / 2 * half, [&](int i, int d, float &x0, float &x1) { st_bf2(W + i * DK + d, x0, x1); });
   }
   {
-    float acc[DV / 8][4];
+    float acc[DV / 16][4];
     zero(acc);
-    wmma<DV / 8, false, false>(acc, s.T, kLdC, m0, s.ru, LV, 0, kC);
+    wmma<DV / 16, false, false>(acc, s.T, kLdC, m0, s.ru, LV, DV / 2 * half, kC);
     bf16 *Ut = ws.Ut + unit * WS::kUt;
-    each2(acc, m0, 0, [&](int i, int c, float &x0, float &x1) { st_bf2(Ut + i * DV + c, x0, x1); });
+    each2(acc, m0, DV / 2 * half, [&](int i, int c, float &x0, float &x1) { st_bf2(Ut + i * DV + c, x0, x1); });
   }
   // the state-free products of the reverse chain: dO^T P and dO^T diag(gamma) Q (fp32)
   __syncthreads();   // W is done with diag(beta gamma) K
-  for (int idx = tid; idx < 64 * DK / 2; idx += kThreads) {
+  for (int idx = tid; idx < 64 * DK / 2; idx += kPrepThreads) {
     const int i = idx / (DK / 2), d = 2 * (idx % (DK / 2));
     const float ga = s.gam[i];
     st_bf2(&s.rw[i * LK + d], ga * bf(s.q[i * LK + d]), ga * bf(s.q[i * LK + d + 1]));
   }
   __syncthreads();
-  for (int mt = warp; mt < DV / 16; mt += 4) {
-    float acc[8][4];
+  for (int mt = warp & 3; mt < DV / 16; mt += 4) {
+    float acc[4][4];
     zero(acc);
-    wmma<8, true, false>(acc, s.o, LV, 16 * mt, s.P, kLdC, 0, kC);
+    wmma<4, true, false>(acc, s.o, LV, 16 * mt, s.P, kLdC, 32 * half, kC);
     float *X1 = ws.X1t + unit * WS::kX1;
-    each2(acc, 16 * mt, 0, [&](int c, int j, float &x0, float &x1) {
+    each2(acc, 16 * mt, 32 * half, [&](int c, int j, float &x0, float &x1) {
       *reinterpret_cast<float2 *>(X1 + c * kC + j) = make_float2(x0, x1);
     });
-    float acc2[DK / 8][4];
+    float acc2[DK / 16][4];
     zero(acc2);
-    wmma<DK / 8, true, false>(acc2, s.o, LV, 16 * mt, s.rw, LK, 0, kC);
+    wmma<DK / 16, true, false>(acc2, s.o, LV, 16 * mt, s.rw, LK, DK / 2 * half, kC);
     float *X2 = ws.X2t + unit * WS::kX2;
-    each2(acc2, 16 * mt, 0, [&](int c, int d, float &x0, float &x1) {
+    each2(acc2, 16 * mt, DK / 2 * half, [&](int c, int d, float &x0, float &x1) {
       *reinterpret_cast<float2 *>(X2 + c * DK + d) = make_float2(x0, x1);
     });
   }
@@ -620,7 +628,7 @@ struct GradSmem {
   bf16 oD[64 * LO];    // dO (row stride LV), then v (LV), then diag(beta) D (kLdC)
   bf16 T[64 * kLdC], PDP[64 * kLdC];  // P, then dP (.) Gamma
   bf16 r1[R1], r2[R2];
-  float G[64], gam[64], dec[64], beta[64];
+  float G[64], Gl[64], gam[64], dec[64], beta[64];
   float dgam[64], dbg[64], ddec[64], dB[64], Erow[64], Ecol[64], dG[64];
   float tmp[4];
 };
@@ -676,8 +684,8 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdP
   cp_tile<DK, DV>(sDH, LV, ws.dHb + unit * WS::kH, DV, DK);
   cp_commit();
   if (tid < kC) { s.Ecol[tid] = 0.f; }
-  chunk_gates(p.g, static_cast<const bf16 *>(p.beta), tok0, H, h, valid, s.G, s.gam, s.dec,
-              s.beta, s.tmp);
+  chunk_gates(p.g, static_cast<const bf16 *>(p.beta), tok0, H, h, valid, s.G, s.Gl, s.gam,
+              s.dec, s.beta, s.tmp);
   const float4 gcv = *reinterpret_cast<const float4 *>(ws.gC + unit * 4);
   const float gC = gcv.x, dgC = gcv.y;
   cp_wait<0>();
@@ -689,8 +697,8 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdP
     zero(acc);
     wmma<8, false, true>(acc, s.q, LK, m0, s.k, LK, 0, DK);
     each2(acc, m0, 0, [&](int i, int j, float &x0, float &x1) {
-      const float p0 = i >= j ? x0 * expf(s.G[i] - s.G[j]) : 0.f;
-      const float p1 = i >= j + 1 ? x1 * expf(s.G[i] - s.G[j + 1]) : 0.f;
+      const float p0 = i >= j ? x0 * ex2(s.Gl[i] - s.Gl[j]) : 0.f;
+      const float p1 = i >= j + 1 ? x1 * ex2(s.Gl[i] - s.Gl[j + 1]) : 0.f;
       st_bf2(&s.PDP[i * kLdC + j], p0, p1);
     });
   }
@@ -733,7 +741,7 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdP
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = r0 + (e >= 2 ? 8 : 0), j = 8 * t + 2 * (lane & 3) + (e & 1);
-        const float d = i >= j ? acc[t][e] * expf(s.G[i] - s.G[j]) : 0.f;
+        const float d = i >= j ? acc[t][e] * ex2(s.Gl[i] - s.Gl[j]) : 0.f;
         acc[t][e] = d;
         qk[t][e] *= d;
         if (e < 2) erow0 += qk[t][e]; else erow1 += qk[t][e];
@@ -859,7 +867,7 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdP
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = r0 + (e >= 2 ? 8 : 0), j = 8 * t + 2 * (lane & 3) + (e & 1);
-        const float D = i > j ? -acc[t][e] * expf(s.G[i] - s.G[j]) : 0.f;
+        const float D = i > j ? -acc[t][e] * ex2(s.Gl[i] - s.Gl[j]) : 0.f;
         const float dk = D * kk[t][e];            // the dbeta term; beta_i times it is E
         if (e < 2) { p0 += dk; erow0 += s.beta[i] * dk; } else { p1 += dk; erow1 += s.beta[i] * dk; }
         kk[t][e] = s.beta[i] * dk;
@@ -945,7 +953,7 @@ cudaError_t launch_dims(const ChunkBwdParams &P, cudaStream_t s) {
     return e;
   const dim3 per_chunk((unsigned)P.slots, (unsigned)P.f.num_heads);
   const dim3 per_seq((unsigned)P.f.num_heads, (unsigned)P.f.num_seqs);
-  prep<<<per_chunk, kThreads, sp, s>>>(P);
+  prep<<<per_chunk, kPrepThreads, sp, s>>>(P);
   fwd<<<per_seq, kThreads, sf, s>>>(P);
   rev<<<per_seq, kThreads, sr, s>>>(P);
   grad<<<per_chunk, kThreads, sg, s>>>(P);
