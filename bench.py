@@ -234,9 +234,35 @@ KERNEL_SOURCES = {
 }
 
 
+def code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments, trailing blanks and empty lines:
+    the part of a file that decides what a kernel does."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    lines = [ln.rstrip() for ln in "".join(out).splitlines()]
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_sources_hash(kernel: str) -> str:
-    """sha256 prefix over the kernel's .cu file, every csrc header and the
-    public header (host-side files such as the ABI layer are left out)."""
+    """sha256 prefix over the code (comments left out) of the kernel's .cu
+    file, every csrc header and the public header (host-side files such as the
+    ABI layer are left out).  A profile's counters stay valid while it matches."""
     import glob
     import hashlib
     csrc = os.path.join(ROOT, "linear_attention_recurrence_gated_gb300", "csrc")
@@ -245,8 +271,8 @@ def kernel_sources_hash(kernel: str) -> str:
     files.append(os.path.join(ROOT, "include", "gdn.h"))
     h = hashlib.sha256()
     for p in files:
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p, encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

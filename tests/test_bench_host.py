@@ -73,3 +73,28 @@ def test_reference_arm_line(capsys):
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_source_hash_ignores_comments_only():
+    """The profile hash covers code, not comments: editing a comment keeps a
+    profile's counters valid, editing code does not."""
+    src = 'int f(int x) {  // doubles\n  /* twice\n */ return 2 * x;  \n}\nconst char *s = "a // b";\n'
+    assert bench.code_only(src) == 'int f(int x) {\n   return 2 * x;\n}\nconst char *s = "a // b";'
+    assert bench.code_only(src.replace("doubles", "twice x")) == bench.code_only(src)
+    assert bench.code_only(src.replace("2 * x", "3 * x")) != bench.code_only(src)
+    assert bench.code_only("char c = '\\'';  // q\n") == "char c = '\\'';"
+
+
+def test_committed_profiles_name_their_sources():
+    """Every ncu summary that carries counters names a kernel bench.py knows
+    and the hash of the code it was taken on (bench.py reports the counters
+    only while that hash matches the sources)."""
+    import glob
+    import re
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        text = open(path).read()
+        if "dram_bytes_per_launch" not in text:
+            continue
+        name = os.path.basename(path)[:-3]
+        assert any(name.startswith(k + "_") for k in bench.KERNEL_SOURCES), path
+        assert re.search(r"source_sha:\s*[0-9a-f]{16}\b", text), path
