@@ -333,16 +333,22 @@ gdn_status gdn_conv_silu(const void *x, const float *w, const void *x_prev, void
  *   dg, dbeta      [batch, seq_len, num_heads]                 float32  device (written)
  *   d_initial_state [num_seqs, num_heads, head_dim_k, head_dim_v] float32 device (written), or NULL
  *
- * All gradients are fp32 whatever the storage dtype.  dq, dk, dg and dbeta
- * are summed with atomics over value-column slices, so they are not bitwise
- * reproducible from run to run (they agree to fp32 rounding).  Sizes as
- * gdn_fwd (chunk 64); flags must be 0.  No gradient buffer may overlap an
- * input or another gradient.  workspace: at least gdn_bwd_workspace_size(...)
- * bytes, the fp32 state at every 64-token chunk start plus per-CTA scratch;
- * the first 256 bytes are the status word (zero it once with
- * gdn_workspace_init).  Device-detected errors (bad cu_seqlens) are reported
- * by gdn_check.  Returns GDN_OK once enqueued, or an error code with nothing
- * enqueued.  seq_len is the packed token count when cu_seqlens is given.
+ * All gradients are fp32 whatever the storage dtype.  Two paths compute them:
+ * - bf16 storage with head_dim_k, head_dim_v in {32, 64}: the same algebra in
+ *   the chunked (WY) form of gdn_fwd, with bf16 tensor-core products and fp32
+ *   accumulation (the precision class of gdn_fwd's tensor-core path); every
+ *   gradient is written once, so results are bitwise reproducible;
+ * - otherwise: the recurrence above token by token in fp32, from state
+ *   checkpoints; dq, dk, dg and dbeta are summed with atomics over
+ *   value-column slices, so they agree from run to run to fp32 rounding only.
+ * Sizes as gdn_fwd (chunk 64); flags must be 0.  No gradient buffer may
+ * overlap an input or another gradient.  workspace: at least
+ * gdn_bwd_workspace_size(...) bytes, enough for either path (per-chunk
+ * records of the chunked form, or state checkpoints and per-CTA scratch); the
+ * first 256 bytes are the status word (zero it once with gdn_workspace_init).
+ * Device-detected errors (bad cu_seqlens) are reported by gdn_check.  Returns
+ * GDN_OK once enqueued, or an error code with nothing enqueued.  seq_len is
+ * the packed token count when cu_seqlens is given.
  */
 size_t gdn_bwd_workspace_size(int32_t num_seqs, int32_t seq_len, int32_t num_heads,
                               int32_t head_dim_k, int32_t head_dim_v);
