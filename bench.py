@@ -231,6 +231,7 @@ KERNEL_SOURCES = {
     "diag_fp32": "gdn_diag.cu",
     "conv_bf16": "gdn_conv.cu",
     "conv_fp32": "gdn_conv.cu",
+    "bwd_chunk": "gdn_bwd_chunk.cu",
 }
 
 
@@ -1051,7 +1052,9 @@ def bench_bwd(args, w: W.Workload, rank: int, world: int, local: int):
                    "l2": "inputs, d_o and the fp32 gradients (> 129 MB) stream every step",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
-                     "frac": achieved / hbm_gbs, "traffic": None,
+                     "frac": achieved / hbm_gbs,
+                     # DRAM bytes of the four kernels of one call, from the committed summary
+                     "traffic": committed_traffic("bwd_chunk", w.name) if chunked else None,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": alg, "kernel_ms": per_ms,
