@@ -1031,7 +1031,7 @@ def bench_bwd(args, w: W.Workload, rank: int, world: int, local: int):
         return 0
     hbm_gbs, _, peak_src = measured_peaks()
     alg = bwd_bytes(w, tokens, N)
-    chunked = w.dtype == "bf16" and w.dk <= 64 and w.dv <= 64
+    chunked = w.dtype == "bf16" and w.dk <= 128 and w.dv <= 128
     achieved = alg / (per_ms / 1e3) / 1e9
     # CPU baseline: the autograd oracle on one head of one batch row, at most
     # 4096 tokens of it (about 4 s), scaled to the workload's heads

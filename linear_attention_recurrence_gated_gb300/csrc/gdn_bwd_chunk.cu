@@ -1,6 +1,6 @@
 // Chunked backward of the gated delta rule for bf16 storage (head_dim_k and
-// head_dim_v up to 64), on warp-level bf16 tensor-core products with fp32
-// accumulation.  The pages' kernel ships a recompute-style backward
+// head_dim_v in {32, 64, 128}), on warp-level bf16 tensor-core products with
+// fp32 accumulation.  The pages' kernel ships a recompute-style backward
 // ("Optimization Quartet", Triton GDN kernel section 3.4); this one works in
 // the chunked WY form of the forward (chunk size 64, "v1.0 Architecture &
 // Design Spec" section 2.3), so that everything but two short state chains is
@@ -133,12 +133,13 @@ __device__ __forceinline__ void cp_wait() {
 }
 // rows x (cols elements of `bytes_per` bytes) from a dense global matrix into a padded tile
 template <int ROWS, int ROW_BYTES, int NTH = kThreads>
-__device__ __forceinline__ void cp_rows(void *dst, int ld_bytes, const void *src) {
+__device__ __forceinline__ void cp_rows(void *dst, int ld_bytes, const void *src,
+                                        size_t src_stride = ROW_BYTES) {
   constexpr int V = ROW_BYTES / 16;
   for (int idx = threadIdx.x; idx < ROWS * V; idx += NTH) {
     const int r = idx / V, c = (idx % V) * 16;
     cp16(static_cast<uint8_t *>(dst) + r * ld_bytes + c,
-         static_cast<const uint8_t *>(src) + (size_t)r * ROW_BYTES + c);
+         static_cast<const uint8_t *>(src) + (size_t)r * src_stride + c);
   }
 }
 
@@ -479,14 +480,16 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_bwdc_prep_kernel(const Chunk
 }
 
 // --------------------------------------------------------------- chains ----
+// A chain CTA owns a slice of SW = min(DV, 64) value columns (4 warps x 16).
 template <int DK, int DV, bool REV>
 struct ChainSmem {
-  static constexpr int LK = DK + 8, LV = DV + 8, LX1 = kC + 4, LX2 = DK + 4;
+  static constexpr int SW = DV < 64 ? DV : 64;
+  static constexpr int LK = DK + 8, LS = SW + 8, LX1 = kC + 4, LX2 = DK + 4;
   bf16 W[2][64 * LK], Kt[2][64 * LK];
-  bf16 Ut[REV ? 1 : 2][REV ? 8 : 64 * LV];
-  float X1[REV ? 2 : 1][REV ? DV * LX1 : 4];
-  float X2[REV ? 2 : 1][REV ? DV * LX2 : 4];
-  bf16 Hb[REV ? 2 : 1][REV ? DK * LV : 8];   // the state entering the chunk
+  bf16 Ut[REV ? 1 : 2][REV ? 8 : 64 * LS];    // the slice's columns of U~
+  float X1[REV ? 2 : 1][REV ? SW * LX1 : 4];  // the slice's rows of dO^T P
+  float X2[REV ? 2 : 1][REV ? SW * LX2 : 4];  // ... and of dO^T diag(gamma) Q
+  bf16 Hb[REV ? 2 : 1][REV ? DK * LS : 8];    // the state entering the chunk (slice)
   float gC[2][4];
 };
 
@@ -523,22 +526,23 @@ __device__ __forceinline__ void wmma_ra(float (&acc)[NT][4], const float (&X)[KT
 // Reverse (REV = true): dH' at every chunk end, from d_final_state, and the
 // gradient of the initial state.
 //   dU^T = (dO^T P) + dH'^T K~^T,   dH^T = gamma_C dH'^T + (dO^T diag(gamma) Q) - dU^T W
-// Warp w keeps the transposed state of value columns 16w..16w+15 (16 x DK) in
-// its accumulators; the next chunk's operands are staged while it works.
+// A CTA takes one slice of up to 64 value columns; its warp w keeps the
+// transposed state of 16 of them (16 x DK) in its accumulators.  The next
+// chunk's operands are staged while it works.
 template <int DK, int DV, bool REV>
 __global__ void __launch_bounds__(kThreads) gdn_bwdc_chain_kernel(const ChunkBwdParams P) {
   using S = ChainSmem<DK, DV, REV>;
   using WS = ChunkWs<DK, DV>;
-  constexpr int LK = S::LK, LV = S::LV, LX1 = S::LX1, LX2 = S::LX2;
+  constexpr int LK = S::LK, LS = S::LS, SW = S::SW, LX1 = S::LX1, LX2 = S::LX2;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   S &s = *reinterpret_cast<S *>(smem_raw);
   const FwdParams &p = P.f;
-  const int h = blockIdx.x, n = blockIdx.y;
+  const int h = blockIdx.x, n = blockIdx.y, cs = SW * blockIdx.z;  // first column of the slice
   int64_t start, len;
   if (!sequence_bounds(p, n, h, start, len)) return;
   const int H = p.num_heads, warp = threadIdx.x >> 5;
-  const int c0 = 16 * warp;
-  const bool active = c0 < DV;
+  const int c0 = cs + 16 * warp;   // this warp's value columns c0..c0+15
+  const bool active = 16 * warp < SW;
   const int64_t ck0 = ckpt_first_slot(n, start, p.seq_len, p.cu != nullptr);
   const int nck = (int)((len + kC - 1) / kC);
   WS ws;
@@ -549,11 +553,11 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_chain_kernel(const ChunkBwd
     cp_rows<64, DK * 2>(s.W[buf], LK * 2, ws.W + unit * WS::kW);
     cp_rows<64, DK * 2>(s.Kt[buf], LK * 2, ws.Kt + unit * WS::kKt);
     if (REV) {
-      cp_rows<DV, kC * 4>(s.X1[buf], LX1 * 4, ws.X1t + unit * WS::kX1);
-      cp_rows<DV, DK * 4>(s.X2[buf], LX2 * 4, ws.X2t + unit * WS::kX2);
-      cp_rows<DK, DV * 2>(s.Hb[buf], LV * 2, ws.Hb + unit * WS::kH);
+      cp_rows<SW, kC * 4>(s.X1[buf], LX1 * 4, ws.X1t + unit * WS::kX1 + (size_t)cs * kC);
+      cp_rows<SW, DK * 4>(s.X2[buf], LX2 * 4, ws.X2t + unit * WS::kX2 + (size_t)cs * DK);
+      cp_rows<DK, SW * 2>(s.Hb[buf], LS * 2, ws.Hb + unit * WS::kH + cs, (size_t)DV * 2);
     } else {
-      cp_rows<64, DV * 2>(s.Ut[buf], LV * 2, ws.Ut + unit * WS::kUt);
+      cp_rows<64, SW * 2>(s.Ut[buf], LS * 2, ws.Ut + unit * WS::kUt + cs, (size_t)DV * 2);
     }
     if (threadIdx.x == 0) cp16(s.gC[buf], ws.gC + unit * 4);
     cp_commit();
@@ -586,7 +590,8 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_chain_kernel(const ChunkBwd
       each2(st, c0, 0, [&](int c, int d, float &x0, float &x1) {
         out[(size_t)d * DV + c] = __float2bfloat16_rn(x0);
         out[(size_t)(d + 1) * DV + c] = __float2bfloat16_rn(x1);
-        if (REV) dot += x0 * bf(s.Hb[buf][d * LV + c]) + x1 * bf(s.Hb[buf][(d + 1) * LV + c]);
+        if (REV)
+          dot += x0 * bf(s.Hb[buf][d * LS + c - cs]) + x1 * bf(s.Hb[buf][(d + 1) * LS + c - cs]);
       });
       if (REV) {
 #pragma unroll
@@ -597,16 +602,16 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_chain_kernel(const ChunkBwd
       if (!REV) {
         zero(u);
         wmma_ra<8, DK / 8, true>(u, st, 1.f, s.W[buf], LK);   // H^T W^T
-        each(u, c0, 0, [&](int c, int i, float &x) { x = bf(s.Ut[buf][i * LV + c]) - x; });
+        each(u, c0, 0, [&](int c, int i, float &x) { x = bf(s.Ut[buf][i * LS + c - cs]) - x; });
 #pragma unroll
         for (int t = 0; t < DK / 8; ++t)
 #pragma unroll
           for (int e = 0; e < 4; ++e) st[t][e] *= gC;
         wmma_ra<DK / 8, 8, false>(st, u, 1.f, s.Kt[buf], LK);  // + U^T K~
       } else {
-        each(u, c0, 0, [&](int c, int i, float &x) { x = s.X1[buf][c * LX1 + i]; });
+        each(u, c0, 0, [&](int c, int i, float &x) { x = s.X1[buf][(c - cs) * LX1 + i]; });
         wmma_ra<8, DK / 8, true>(u, st, 1.f, s.Kt[buf], LK);   // + dH'^T K~^T
-        each(st, c0, 0, [&](int c, int d, float &x) { x = gC * x + s.X2[buf][c * LX2 + d]; });
+        each(st, c0, 0, [&](int c, int d, float &x) { x = gC * x + s.X2[buf][(c - cs) * LX2 + d]; });
         wmma_ra<DK / 8, 8, false>(st, u, -1.f, s.W[buf], LK);  // - dU^T W
       }
     }
@@ -617,6 +622,9 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_chain_kernel(const ChunkBwd
 }
 
 // ----------------------------------------------------------------- grad ----
+// NS = 1: 4 warps, warp w owns rows 16w.. of every chunk product.  NS = 2 (a
+// head dim of 128): 8 warps, warp w owns rows 16 (w % 4).. and half of the
+// columns, so that the per-warp accumulators stay within the registers.
 template <int DK, int DV>
 struct GradSmem {
   static constexpr int LK = DK + 8, LV = DV + 8, LO = LV > kLdC ? LV : kLdC;
@@ -633,11 +641,16 @@ struct GradSmem {
   float tmp[4];
 };
 
-// Column sums over the warp's 16 rows of a 16 x 64 accumulator, added into col[].
-__device__ __forceinline__ void add_col_sums(const float (&e)[8][4], float *col) {
+template <int DK, int DV>
+__host__ __device__ constexpr int grad_split() { return (DK > 64 || DV > 64) ? 2 : 1; }
+
+// Column sums over the warp's 16 rows of a 16 x 8NT accumulator at columns
+// n0.., added into col[].
+template <int NT>
+__device__ __forceinline__ void add_col_sums(const float (&e)[NT][4], int n0, float *col) {
   const int l = threadIdx.x & 31;
 #pragma unroll
-  for (int t = 0; t < 8; ++t) {
+  for (int t = 0; t < NT; ++t) {
     float c0 = e[t][0] + e[t][2], c1 = e[t][1] + e[t][3];
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
@@ -645,14 +658,34 @@ __device__ __forceinline__ void add_col_sums(const float (&e)[8][4], float *col)
       c1 += __shfl_xor_sync(0xffffffffu, c1, o);
     }
     if (l < 4) {
-      atomicAdd(col + 8 * t + 2 * l, c0);
-      atomicAdd(col + 8 * t + 2 * l + 1, c1);
+      atomicAdd(col + n0 + 8 * t + 2 * l, c0);
+      atomicAdd(col + n0 + 8 * t + 2 * l + 1, c1);
+    }
+  }
+}
+
+// Per-row partials of rows r0 and r0 + 8 (one per lane), summed over the quad
+// and, with column-split warps, over the two warps of a row block.
+template <int NS>
+__device__ __forceinline__ void put_rows(float *arr, int r0, float p0, float p1) {
+  p0 = quad_sum(p0);
+  p1 = quad_sum(p1);
+  if ((threadIdx.x & 3) == 0) {
+    if (NS == 1) {
+      arr[r0] = p0;
+      arr[r0 + 8] = p1;
+    } else {
+      atomicAdd(arr + r0, p0);
+      atomicAdd(arr + r0 + 8, p1);
     }
   }
 }
 
 template <int DK, int DV>
-__global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdParams P) {
+__global__ void __launch_bounds__(kThreads * grad_split<DK, DV>())
+gdn_bwdc_grad_kernel(const ChunkBwdParams P) {
+  constexpr int NS = grad_split<DK, DV>(), NTH = kThreads * NS;
+  constexpr int NC = 8 / NS, NK = DK / 8 / NS, NV = DV / 8 / NS;  // n-tiles per warp
   using S = GradSmem<DK, DV>;
   using WS = ChunkWs<DK, DV>;
   constexpr int LK = S::LK, LV = S::LV;
@@ -665,7 +698,8 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdP
   int64_t tok0;
   if (!slot_chunk(p, slot, h, n, tok0, valid)) return;
   const int H = p.num_heads, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int m0 = 16 * warp, r0 = m0 + (lane >> 2);
+  const int m0 = 16 * (warp & 3), r0 = m0 + (lane >> 2), hf = warp >> 2;
+  const int nc0 = hf * (kC / NS), nk0 = hf * (DK / NS), nv0 = hf * (DV / NS);  // column offsets
   const size_t unit = (size_t)slot * H + h;
   WS ws;
   ws.carve(P.ws, P.slots * H);
@@ -673,17 +707,20 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdP
 
   // ---- loads: every tile in flight at once ----
   const size_t rq = ((size_t)tok0 * H + h) * DK, rv = ((size_t)tok0 * H + h) * DV;
-  cp_tile<64, DK>(s.q, LK, static_cast<const bf16 *>(p.q) + rq, (size_t)H * DK, valid);
-  cp_tile<64, DK>(s.k, LK, static_cast<const bf16 *>(p.k) + rq, (size_t)H * DK, valid);
-  cp_tile<64, DV>(s.oD, LV, P.dO + rv, (size_t)H * DV, valid);
-  cp_tile<64, DK>(s.W, LK, ws.W + unit * WS::kW, DK, kC);
-  cp_tile<64, DK>(s.KtDW, LK, ws.Kt + unit * WS::kKt, DK, kC);
-  cp_tile<64, DV>(s.UU, LV, ws.Ut + unit * WS::kUt, DV, kC);
-  cp_tile<64, kC>(s.T, kLdC, ws.T + unit * WS::kT, kC, kC);
-  cp_tile<DK, DV>(sH, LV, ws.Hb + unit * WS::kH, DV, DK);
-  cp_tile<DK, DV>(sDH, LV, ws.dHb + unit * WS::kH, DV, DK);
+  cp_tile<64, DK, NTH>(s.q, LK, static_cast<const bf16 *>(p.q) + rq, (size_t)H * DK, valid);
+  cp_tile<64, DK, NTH>(s.k, LK, static_cast<const bf16 *>(p.k) + rq, (size_t)H * DK, valid);
+  cp_tile<64, DV, NTH>(s.oD, LV, P.dO + rv, (size_t)H * DV, valid);
+  cp_tile<64, DK, NTH>(s.W, LK, ws.W + unit * WS::kW, DK, kC);
+  cp_tile<64, DK, NTH>(s.KtDW, LK, ws.Kt + unit * WS::kKt, DK, kC);
+  cp_tile<64, DV, NTH>(s.UU, LV, ws.Ut + unit * WS::kUt, DV, kC);
+  cp_tile<64, kC, NTH>(s.T, kLdC, ws.T + unit * WS::kT, kC, kC);
+  cp_tile<DK, DV, NTH>(sH, LV, ws.Hb + unit * WS::kH, DV, DK);
+  cp_tile<DK, DV, NTH>(sDH, LV, ws.dHb + unit * WS::kH, DV, DK);
   cp_commit();
-  if (tid < kC) { s.Ecol[tid] = 0.f; }
+  if (tid < kC) {
+    s.Ecol[tid] = 0.f;
+    if (NS > 1) s.dgam[tid] = s.dbg[tid] = s.ddec[tid] = s.dB[tid] = s.Erow[tid] = 0.f;
+  }
   chunk_gates(p.g, static_cast<const bf16 *>(p.beta), tok0, H, h, valid, s.G, s.Gl, s.gam,
               s.dec, s.beta, s.tmp);
   const float4 gcv = *reinterpret_cast<const float4 *>(ws.gC + unit * 4);
@@ -693,34 +730,34 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdP
 
   // ---- P, U = U~ - W H ----
   {
-    float acc[8][4];
+    float acc[NC][4];
     zero(acc);
-    wmma<8, false, true>(acc, s.q, LK, m0, s.k, LK, 0, DK);
-    each2(acc, m0, 0, [&](int i, int j, float &x0, float &x1) {
+    wmma<NC, false, true>(acc, s.q, LK, m0, s.k, LK, nc0, DK);
+    each2(acc, m0, nc0, [&](int i, int j, float &x0, float &x1) {
       const float p0 = i >= j ? x0 * ex2(s.Gl[i] - s.Gl[j]) : 0.f;
       const float p1 = i >= j + 1 ? x1 * ex2(s.Gl[i] - s.Gl[j + 1]) : 0.f;
       st_bf2(&s.PDP[i * kLdC + j], p0, p1);
     });
   }
   {
-    float acc[DV / 8][4];
+    float acc[NV][4];
     zero(acc);
-    wmma<DV / 8, false, false>(acc, s.W, LK, m0, sH, LV, 0, DK);
-    each2(acc, m0, 0, [&](int i, int c, float &x0, float &x1) {   // U over U~, in place
+    wmma<NV, false, false>(acc, s.W, LK, m0, sH, LV, nv0, DK);
+    each2(acc, m0, nv0, [&](int i, int c, float &x0, float &x1) {   // U over U~, in place
       st_bf2(&s.UU[i * LV + c], bf(s.UU[i * LV + c]) - x0, bf(s.UU[i * LV + c + 1]) - x1);
     });
   }
   __syncthreads();
   // dU = P^T dO + K~ dH'; what rounding it to bf16 leaves out stays in registers
-  uint32_t dUr[DV / 8][2], dWr[DK / 8][2];
+  uint32_t dUr[NV][2], dWr[NK][2];
   {
-    float acc[DV / 8][4];
+    float acc[NV][4];
     zero(acc);
-    wmma<DV / 8, true, false>(acc, s.PDP, kLdC, m0, s.oD, LV, 0, kC);
-    wmma<DV / 8, false, false>(acc, s.KtDW, LK, m0, sDH, LV, 0, DK);
-    each2(acc, m0, 0, [&](int i, int c, float &x0, float &x1) { st_bf2(&s.dU[i * LV + c], x0, x1); });
+    wmma<NV, true, false>(acc, s.PDP, kLdC, m0, s.oD, LV, nv0, kC);
+    wmma<NV, false, false>(acc, s.KtDW, LK, m0, sDH, LV, nv0, DK);
+    each2(acc, m0, nv0, [&](int i, int c, float &x0, float &x1) { st_bf2(&s.dU[i * LV + c], x0, x1); });
 #pragma unroll
-    for (int t = 0; t < DV / 8; ++t) {
+    for (int t = 0; t < NV; ++t) {
       dUr[t][0] = pack_bf16(acc[t][0] - rbf(acc[t][0]), acc[t][1] - rbf(acc[t][1]));
       dUr[t][1] = pack_bf16(acc[t][2] - rbf(acc[t][2]), acc[t][3] - rbf(acc[t][3]));
     }
@@ -730,111 +767,105 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdP
   // ---- dP (.) Gamma and its gate terms, dW, dK~, dO H^T ----
   float erow0 = 0.f, erow1 = 0.f;   // row sums of the gate terms E (rows r0, r0 + 8)
   {
-    float acc[8][4], qk[8][4];
+    float acc[NC][4], qk[NC][4];
     zero(acc);
-    wmma<8, false, true>(acc, s.oD, LV, m0, s.UU, LV, 0, DV);
+    wmma<NC, false, true>(acc, s.oD, LV, m0, s.UU, LV, nc0, DV);
     zero(qk);
-    wmma<8, false, true>(qk, s.q, LK, m0, s.k, LK, 0, DK);
+    wmma<NC, false, true>(qk, s.q, LK, m0, s.k, LK, nc0, DK);
     // E = dP (.) Gamma (.) Q K^T on and below the diagonal
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
+    for (int t = 0; t < NC; ++t) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int i = r0 + (e >= 2 ? 8 : 0), j = 8 * t + 2 * (lane & 3) + (e & 1);
+        const int i = r0 + (e >= 2 ? 8 : 0), j = nc0 + 8 * t + 2 * (lane & 3) + (e & 1);
         const float d = i >= j ? acc[t][e] * ex2(s.Gl[i] - s.Gl[j]) : 0.f;
         acc[t][e] = d;
         qk[t][e] *= d;
         if (e < 2) erow0 += qk[t][e]; else erow1 += qk[t][e];
       }
     }
-    each2(acc, m0, 0, [&](int i, int j, float &x0, float &x1) { st_bf2(&s.PDP[i * kLdC + j], x0, x1); });
-    add_col_sums(qk, s.Ecol);
+    each2(acc, m0, nc0, [&](int i, int j, float &x0, float &x1) { st_bf2(&s.PDP[i * kLdC + j], x0, x1); });
+    add_col_sums(qk, nc0, s.Ecol);
   }
   {
-    float acc[DK / 8][4];
+    float acc[NK][4];
     zero(acc);
-    wmma<DK / 8, false, true>(acc, s.dU, LV, m0, sH, LV, 0, DV);
-    each2(acc, m0, 0, [&](int i, int d, float &x0, float &x1) { st_bf2(&s.KtDW[i * LK + d], -x0, -x1); });
+    wmma<NK, false, true>(acc, s.dU, LV, m0, sH, LV, nk0, DV);
+    each2(acc, m0, nk0, [&](int i, int d, float &x0, float &x1) { st_bf2(&s.KtDW[i * LK + d], -x0, -x1); });
 #pragma unroll
-    for (int t = 0; t < DK / 8; ++t) {
+    for (int t = 0; t < NK; ++t) {
       dWr[t][0] = pack_bf16(rbf(acc[t][0]) - acc[t][0], rbf(acc[t][1]) - acc[t][1]);
       dWr[t][1] = pack_bf16(rbf(acc[t][2]) - acc[t][2], rbf(acc[t][3]) - acc[t][3]);
     }
   }
-  float dK[DK / 8][4], dQ[DK / 8][4];
+  float dK[NK][4], dQ[NK][4];
   {
     zero(dK);
-    wmma<DK / 8, false, true>(dK, s.UU, LV, m0, sDH, LV, 0, DV);   // dK~ = U dH'^T
+    wmma<NK, false, true>(dK, s.UU, LV, m0, sDH, LV, nk0, DV);   // dK~ = U dH'^T
     float p0 = 0.f, p1 = 0.f;
-    each2(dK, m0, 0, [&](int i, int d, float &x0, float &x1) {
+    each2(dK, m0, nk0, [&](int i, int d, float &x0, float &x1) {
       const float e = x0 * bf(s.k[i * LK + d]) + x1 * bf(s.k[i * LK + d + 1]);
       if (i == r0) p0 += e; else p1 += e;
       x0 *= s.dec[i];
       x1 *= s.dec[i];
     });
-    p0 = quad_sum(p0);
-    p1 = quad_sum(p1);
-    if ((lane & 3) == 0) { s.ddec[r0] = p0; s.ddec[r0 + 8] = p1; }
+    put_rows<NS>(s.ddec, r0, p0, p1);
     zero(dQ);
-    wmma<DK / 8, false, true>(dQ, s.oD, LV, m0, sH, LV, 0, DV);   // dO H^T
+    wmma<NK, false, true>(dQ, s.oD, LV, m0, sH, LV, nk0, DV);   // dO H^T
     p0 = p1 = 0.f;
-    each2(dQ, m0, 0, [&](int i, int d, float &x0, float &x1) {
+    each2(dQ, m0, nk0, [&](int i, int d, float &x0, float &x1) {
       const float e = x0 * bf(s.q[i * LK + d]) + x1 * bf(s.q[i * LK + d + 1]);
       if (i == r0) p0 += e; else p1 += e;
       x0 *= s.gam[i];
       x1 *= s.gam[i];
     });
-    p0 = quad_sum(p0);
-    p1 = quad_sum(p1);
-    if ((lane & 3) == 0) { s.dgam[r0] = p0; s.dgam[r0 + 8] = p1; }
+    put_rows<NS>(s.dgam, r0, p0, p1);
   }
   __syncthreads();
 
   // ---- dR_W = T^T dW, dR_U = T^T dU, dV, dQ ----
   // U and dO are spent: U~ comes back for dA, v takes dO's place
-  cp_tile<64, DV>(s.UU, LV, ws.Ut + unit * WS::kUt, DV, kC);
-  cp_tile<64, DV>(s.oD, LV, static_cast<const bf16 *>(p.v) + rv, (size_t)H * DV, valid);
+  cp_tile<64, DV, NTH>(s.UU, LV, ws.Ut + unit * WS::kUt, DV, kC);
+  cp_tile<64, DV, NTH>(s.oD, LV, static_cast<const bf16 *>(p.v) + rv, (size_t)H * DV, valid);
   cp_commit();
   {
-    float acc[DK / 8][4];
+    float acc[NK][4];
     zero(acc);
-    wmma<DK / 8, true, false>(acc, s.T, kLdC, m0, s.KtDW, LK, 0, kC);
+    wmma<NK, true, false>(acc, s.T, kLdC, m0, s.KtDW, LK, nk0, kC);
 #pragma unroll
-    for (int t = 0; t < DK / 8; ++t) {   // T's diagonal is 1: the rounding remainder of dW
+    for (int t = 0; t < NK; ++t) {   // T's diagonal is 1: the rounding remainder of dW
       acc[t][0] += bf16_lo(dWr[t][0]); acc[t][1] += bf16_hi(dWr[t][0]);
       acc[t][2] += bf16_lo(dWr[t][1]); acc[t][3] += bf16_hi(dWr[t][1]);
     }
     float p0 = 0.f, p1 = 0.f;
-    each2(acc, m0, 0, [&](int i, int d, float &x0, float &x1) {
+    each2(acc, m0, nk0, [&](int i, int d, float &x0, float &x1) {
       const float e = x0 * bf(s.k[i * LK + d]) + x1 * bf(s.k[i * LK + d + 1]);
       if (i == r0) p0 += e; else p1 += e;
       st_bf2(&sDRW[i * LK + d], x0, x1);
     });
     const float bg0 = s.beta[r0] * s.gam[r0], bg1 = s.beta[r0 + 8] * s.gam[r0 + 8];
 #pragma unroll
-    for (int t = 0; t < DK / 8; ++t) {
+    for (int t = 0; t < NK; ++t) {
       dK[t][0] = fmaf(bg0, acc[t][0], dK[t][0]);
       dK[t][1] = fmaf(bg0, acc[t][1], dK[t][1]);
       dK[t][2] = fmaf(bg1, acc[t][2], dK[t][2]);
       dK[t][3] = fmaf(bg1, acc[t][3], dK[t][3]);
     }
-    p0 = quad_sum(p0);
-    p1 = quad_sum(p1);
-    if ((lane & 3) == 0) { s.dbg[r0] = p0; s.dbg[r0 + 8] = p1; }
+    put_rows<NS>(s.dbg, r0, p0, p1);
   }
   {
-    float acc[DV / 8][4];
+    float acc[NV][4];
     zero(acc);
-    wmma<DV / 8, true, false>(acc, s.T, kLdC, m0, s.dU, LV, 0, kC);
+    wmma<NV, true, false>(acc, s.T, kLdC, m0, s.dU, LV, nv0, kC);
 #pragma unroll
-    for (int t = 0; t < DV / 8; ++t) {
+    for (int t = 0; t < NV; ++t) {
       acc[t][0] += bf16_lo(dUr[t][0]); acc[t][1] += bf16_hi(dUr[t][0]);
       acc[t][2] += bf16_lo(dUr[t][1]); acc[t][3] += bf16_hi(dUr[t][1]);
     }
     cp_wait<0>();
     __syncthreads();   // v and U~ landed
     float p0 = 0.f, p1 = 0.f;
-    each2(acc, m0, 0, [&](int i, int c, float &x0, float &x1) {
+    each2(acc, m0, nv0, [&](int i, int c, float &x0, float &x1) {
       const float e = x0 * bf(s.oD[i * LV + c]) + x1 * bf(s.oD[i * LV + c + 1]);
       if (i == r0) p0 += e; else p1 += e;
       st_bf2(&sDRU[i * LV + c], x0, x1);
@@ -842,12 +873,16 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdP
         *reinterpret_cast<float2 *>(P.dv + ((size_t)(tok0 + i) * H + h) * DV + c) =
             make_float2(s.beta[i] * x0, s.beta[i] * x1);
     });
-    p0 = quad_sum(p0);
-    p1 = quad_sum(p1);
-    if ((lane & 3) == 0) { s.dB[r0] = p0; s.dB[r0 + 8] = p1; }
+    if (NS == 1) {
+      p0 = quad_sum(p0);
+      p1 = quad_sum(p1);
+      if ((lane & 3) == 0) { s.dB[r0] = p0; s.dB[r0 + 8] = p1; }
+    } else {
+      put_rows<NS>(s.dB, r0, p0, p1);
+    }
   }
-  wmma<DK / 8, false, false>(dQ, s.PDP, kLdC, m0, s.k, LK, 0, kC);   // + (dP (.) Gamma) K
-  each2(dQ, m0, 0, [&](int i, int d, float &x0, float &x1) {
+  wmma<NK, false, false>(dQ, s.PDP, kLdC, m0, s.k, LK, nk0, kC);   // + (dP (.) Gamma) K
+  each2(dQ, m0, nk0, [&](int i, int d, float &x0, float &x1) {
     if (i < valid)
       *reinterpret_cast<float2 *>(P.dq + ((size_t)(tok0 + i) * H + h) * DK + d) = make_float2(x0, x1);
   });
@@ -855,18 +890,18 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdP
 
   // ---- dA = -(dR_W W^T + dR_U U~^T), D = dA (.) Gamma below the diagonal ----
   {
-    float acc[8][4], kk[8][4];
+    float acc[NC][4], kk[NC][4];
     zero(acc);
-    wmma<8, false, true>(acc, sDRW, LK, m0, s.W, LK, 0, DK);
-    wmma<8, false, true>(acc, sDRU, LV, m0, s.UU, LV, 0, DV);
+    wmma<NC, false, true>(acc, sDRW, LK, m0, s.W, LK, nc0, DK);
+    wmma<NC, false, true>(acc, sDRU, LV, m0, s.UU, LV, nc0, DV);
     zero(kk);
-    wmma<8, false, true>(kk, s.k, LK, m0, s.k, LK, 0, DK);
+    wmma<NC, false, true>(kk, s.k, LK, m0, s.k, LK, nc0, DK);
     float p0 = 0.f, p1 = 0.f;
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
+    for (int t = 0; t < NC; ++t) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int i = r0 + (e >= 2 ? 8 : 0), j = 8 * t + 2 * (lane & 3) + (e & 1);
+        const int i = r0 + (e >= 2 ? 8 : 0), j = nc0 + 8 * t + 2 * (lane & 3) + (e & 1);
         const float D = i > j ? -acc[t][e] * ex2(s.Gl[i] - s.Gl[j]) : 0.f;
         const float dk = D * kk[t][e];            // the dbeta term; beta_i times it is E
         if (e < 2) { p0 += dk; erow0 += s.beta[i] * dk; } else { p1 += dk; erow1 += s.beta[i] * dk; }
@@ -874,24 +909,24 @@ __global__ void __launch_bounds__(kThreads) gdn_bwdc_grad_kernel(const ChunkBwdP
         acc[t][e] = s.beta[i] * D;                // diag(beta) D
       }
     }
-    add_col_sums(kk, s.Ecol);
-    each2(acc, m0, 0, [&](int i, int j, float &x0, float &x1) { st_bf2(&s.oD[i * kLdC + j], x0, x1); });
-    p0 = quad_sum(p0);
-    p1 = quad_sum(p1);
-    erow0 = quad_sum(erow0);
-    erow1 = quad_sum(erow1);
-    if ((lane & 3) == 0) {
-      s.dB[r0] += p0; s.dB[r0 + 8] += p1;
-      s.Erow[r0] = erow0; s.Erow[r0 + 8] = erow1;
+    add_col_sums(kk, nc0, s.Ecol);
+    each2(acc, m0, nc0, [&](int i, int j, float &x0, float &x1) { st_bf2(&s.oD[i * kLdC + j], x0, x1); });
+    if (NS == 1) {
+      p0 = quad_sum(p0);
+      p1 = quad_sum(p1);
+      if ((lane & 3) == 0) { s.dB[r0] += p0; s.dB[r0 + 8] += p1; }
+    } else {
+      put_rows<NS>(s.dB, r0, p0, p1);
     }
+    put_rows<NS>(s.Erow, r0, erow0, erow1);
   }
   __syncthreads();
 
   // ---- dK += (diag(beta) D) K + (diag(beta) D)^T K + (dP (.) Gamma)^T Q ----
-  wmma<DK / 8, false, false>(dK, s.oD, kLdC, m0, s.k, LK, 0, kC);
-  wmma<DK / 8, true, false>(dK, s.oD, kLdC, m0, s.k, LK, 0, kC);
-  wmma<DK / 8, true, false>(dK, s.PDP, kLdC, m0, s.q, LK, 0, kC);
-  each2(dK, m0, 0, [&](int i, int d, float &x0, float &x1) {
+  wmma<NK, false, false>(dK, s.oD, kLdC, m0, s.k, LK, nk0, kC);
+  wmma<NK, true, false>(dK, s.oD, kLdC, m0, s.k, LK, nk0, kC);
+  wmma<NK, true, false>(dK, s.PDP, kLdC, m0, s.q, LK, nk0, kC);
+  each2(dK, m0, nk0, [&](int i, int d, float &x0, float &x1) {
     if (i < valid)
       *reinterpret_cast<float2 *>(P.dk + ((size_t)(tok0 + i) * H + h) * DK + d) = make_float2(x0, x1);
   });
@@ -952,23 +987,44 @@ cudaError_t launch_dims(const ChunkBwdParams &P, cudaStream_t s) {
       (e = smem_attr(rev, sr)) != cudaSuccess || (e = smem_attr(grad, sg)) != cudaSuccess)
     return e;
   const dim3 per_chunk((unsigned)P.slots, (unsigned)P.f.num_heads);
-  const dim3 per_seq((unsigned)P.f.num_heads, (unsigned)P.f.num_seqs);
+  const dim3 per_seq((unsigned)P.f.num_heads, (unsigned)P.f.num_seqs,
+                     (unsigned)(DV / ChainSmem<DK, DV, false>::SW));
   prep<<<per_chunk, kPrepThreads, sp, s>>>(P);
   fwd<<<per_seq, kThreads, sf, s>>>(P);
   rev<<<per_seq, kThreads, sr, s>>>(P);
-  grad<<<per_chunk, kThreads, sg, s>>>(P);
+  grad<<<per_chunk, kThreads * grad_split<DK, DV>(), sg, s>>>(P);
   return cudaGetLastError();
+}
+
+template <int DK>
+cudaError_t launch_dk(const ChunkBwdParams &P, cudaStream_t s) {
+  switch (P.f.dv) {
+    case 32: return launch_dims<DK, 32>(P, s);
+    case 64: return launch_dims<DK, 64>(P, s);
+    case 128: return launch_dims<DK, 128>(P, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int DK>
+size_t ws_dk(int64_t units, int dv) {
+  switch (dv) {
+    case 32: return ChunkWs<DK, 32>::bytes(units);
+    case 64: return ChunkWs<DK, 64>::bytes(units);
+    default: return ChunkWs<DK, 128>::bytes(units);
+  }
 }
 
 }  // namespace
 
 bool bwd_chunked_supported(int dk, int dv) {
-  return (dk == 32 || dk == 64) && (dv == 32 || dv == 64);
+  return (dk == 32 || dk == 64 || dk == 128) && (dv == 32 || dv == 64 || dv == 128);
 }
 
 size_t bwd_chunked_ws_bytes(int64_t units, int dk, int dv) {
-  if (dk == 32) return dv == 32 ? ChunkWs<32, 32>::bytes(units) : ChunkWs<32, 64>::bytes(units);
-  return dv == 32 ? ChunkWs<64, 32>::bytes(units) : ChunkWs<64, 64>::bytes(units);
+  if (dk == 32) return ws_dk<32>(units, dv);
+  if (dk == 64) return ws_dk<64>(units, dv);
+  return ws_dk<128>(units, dv);
 }
 
 cudaError_t launch_bwd_chunked(const FwdParams &f, const void *dO, const float *dHN, float *dq,
@@ -981,8 +1037,9 @@ cudaError_t launch_bwd_chunked(const FwdParams &f, const void *dO, const float *
   P.dq = dq; P.dk = dk; P.dv = dv; P.dg = dg; P.dbeta = dbeta; P.dh0 = dh0;
   P.ws = ws;
   P.slots = slots;
-  if (f.dk == 32) return f.dv == 32 ? launch_dims<32, 32>(P, s) : launch_dims<32, 64>(P, s);
-  return f.dv == 32 ? launch_dims<64, 32>(P, s) : launch_dims<64, 64>(P, s);
+  if (f.dk == 32) return launch_dk<32>(P, s);
+  if (f.dk == 64) return launch_dk<64>(P, s);
+  return launch_dk<128>(P, s);
 }
 
 }  // namespace gdn
