@@ -159,3 +159,29 @@ def test_bwd_wide_sampled():
     for n in ("dq", "dk", "dv", "dg", "dbeta"):
         assert rel(gpu[n][b:b + 1, :, h:h + 1], ref[n]) <= BF16_GRAD_TOL, (n, b, h)
     assert rel(gpu["dh0"][b:b + 1, h:h + 1], ref["dh0"]) <= BF16_GRAD_TOL, ("dh0", b, h)
+
+
+def test_bwd_varlen_dk128():
+    """Packed sequences on the chunked path with head dims of 128."""
+    lens = [1, 63, 64, 65, 9, 140]
+    w = W.custom(num_seqs=len(lens), len_range=(1, 140), H=1, dk=128, dv=128, dtype="bf16",
+                 init_state=True, seed=61)
+    inp = W.generate(w, lengths=lens)
+    d_o, dhN = _upstream(inp, 62, True)
+    _check(_run(inp, d_o, dhN), _ref(inp, d_o, dhN), BF16_GRAD_TOL)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("cu", [[0, 10, 10, 40], [0, 30, 20, 40], [0, 10, 20, 39], [1, 10, 20, 40]])
+def test_bwd_bad_seqlens_reported(dtype, cu):
+    """Malformed offsets are found on the device by both backward paths and
+    reported by gdn_check (GDN_ERR_BAD_SEQLENS), which then clears the word."""
+    w = W.custom(B=1, T=40, H=2, dk=32, dv=32, dtype=dtype, seed=63)
+    inp = W.generate(w)
+    cu_t = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    q, k, v, g, beta = (inp[n].cuda() for n in ("q", "k", "v", "g", "beta"))
+    d_o = torch.ones_like(v)
+    ws = torch.zeros(G.gdn_bwd_workspace_size(3, 40, 2, 32, 32), dtype=torch.uint8, device="cuda")
+    G.gdn_bwd(q, k, v, g, beta, d_o, None, cu_t, None, workspace=ws)
+    assert G.gdn_check(ws) == 6
+    assert G.gdn_check(ws) == 0
