@@ -999,7 +999,12 @@ def bench_bwd(args, w: W.Workload, rank: int, world: int, local: int):
     total_ms = max_over_ranks(t0.elapsed_time(t1), world)
     per_ms = total_ms / args.steps
     value = tokens * world * args.steps / (total_ms / 1e3)
-    # end to end: inputs and d_o from pinned host memory, the five gradients back
+    # end to end: inputs and d_o from pinned host memory, the five gradients back.
+    # Double-buffered over two device sets, as a training loop would run it:
+    # step i+1's inputs copy in on one stream while step i computes, and step
+    # i's gradients copy out on a third; a set is refilled only after the step
+    # that read it has finished, and recomputed only after its gradients have
+    # been read back.
     pinned = {n: host[n].pin_memory() for n in names}
     do_pin = d_o_host.pin_memory()
     back = {n: torch.empty(t.shape, dtype=torch.float32).pin_memory()
@@ -1007,23 +1012,53 @@ def bench_bwd(args, w: W.Workload, rank: int, world: int, local: int):
     h2d = sum(t.numel() * t.element_size() for t in pinned.values()) + do_pin.numel() * do_pin.element_size()
     d2h = sum(t.numel() * 4 for t in back.values())
     e2e_steps = max(1, min(args.steps, 10))
+    sets = [(d, grads)]
+    d2 = {n: torch.empty_like(t) for n, t in d.items()}
+    sets.append((d2, {n: torch.empty_like(t) for n, t in grads.items()}))
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    h2d_done = [torch.cuda.Event(), torch.cuda.Event()]
+    comp_done = [torch.cuda.Event(), torch.cuda.Event()]
+    d2h_done = [torch.cuda.Event(), torch.cuda.Event()]
 
-    def e2e_step():
-        for n in names:
-            d[n].copy_(pinned[n], non_blocking=True)
-        d["d_o"].copy_(do_pin, non_blocking=True)
-        call()
-        for n, t in back.items():
-            t.copy_(grads[n], non_blocking=True)
+    def e2e_step(i):
+        bsel = i & 1
+        dd, gg = sets[bsel]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(comp_done[bsel])   # step i-2 has read this input set
+            for n in names:
+                dd[n].copy_(pinned[n], non_blocking=True)
+            dd["d_o"].copy_(do_pin, non_blocking=True)
+            h2d_done[bsel].record(s_in)
+        stream.wait_event(h2d_done[bsel])
+        if i >= 2:
+            stream.wait_event(d2h_done[bsel])      # step i-2's gradients have been read back
+        G.gdn_bwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["d_o"], s0, cu, None,
+                  grads=gg, workspace=ws, stream=stream)
+        comp_done[bsel].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[bsel])
+            for n, t in back.items():
+                t.copy_(gg[n], non_blocking=True)
+            d2h_done[bsel].record(s_out)
 
-    e2e_step()
+    def e2e_run(nsteps, e_begin=None, e_end=None):
+        if e_begin is not None:
+            e_begin.record(stream)
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        for i in range(nsteps):
+            e2e_step(i)
+        for bsel in range(min(nsteps, 2)):
+            stream.wait_event(d2h_done[bsel])
+        if e_end is not None:
+            e_end.record(stream)
+
+    e2e_run(2)
     torch.cuda.synchronize(dev)
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e2e_run(e2e_steps, e0, e1)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     barrier(world)
@@ -1066,7 +1101,9 @@ def bench_bwd(args, w: W.Workload, rank: int, world: int, local: int):
                          "sample": f"one head of one batch row ({ts} tokens), torch.autograd "
                                    f"fp64 oracle, {cpu_secs:.1f} s; value scaled to {w.H} heads"},
         "e2e": {"value": tokens * world * e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "overlap": "two device sets: step i+1's inputs copy in while step i "
+                           "computes, step i's gradients copy out on a third stream"},
         "gpu_launches": args.steps * BWD_LAUNCHES[chunked][0],
         "clocks": clk,
     }
