@@ -106,11 +106,14 @@ gdn_status gdn_workspace_init(void *workspace, size_t workspace_bytes, void *str
  * Sequences: with cu_seqlens == NULL the batch rows are the sequences and
  * num_seqs must equal batch.  With cu_seqlens != NULL, batch must be 1 and
  * sequence n covers tokens cu_seqlens[n] .. cu_seqlens[n+1]-1 of the packed
- * seq_len tokens; the offsets must satisfy cu_seqlens[0] = 0, strictly
- * increasing (empty sequences are rejected), cu_seqlens[num_seqs] = seq_len.
+ * seq_len tokens; the offsets must satisfy cu_seqlens[0] = 0, non-decreasing,
+ * cu_seqlens[num_seqs] = seq_len.  An empty sequence (equal offsets) reads
+ * nothing and its final state is its initial state (zeros without one).
  * These offsets live in device memory, so they are checked by the kernel:
  * a sequence whose bounds break the rule writes nothing and records
  * GDN_ERR_BAD_SEQLENS for gdn_check.  No state crosses a sequence boundary.
+ * seq_len = 0 (no tokens at all) is legal: nothing is read, cu_seqlens
+ * included, and every final state is its initial state.
  *
  * Values: g_t is the natural log of the decay alpha_t (expected <= 0; not
  * clamped).  beta_t is used as given (expected in [0, 1]; not clamped).  The
@@ -348,7 +351,9 @@ gdn_status gdn_conv_silu(const void *x, const float *w, const void *x_prev, void
  * first 256 bytes are the status word (zero it once with gdn_workspace_init).
  * Device-detected errors (bad cu_seqlens) are reported by gdn_check.  Returns
  * GDN_OK once enqueued, or an error code with nothing enqueued.  seq_len is
- * the packed token count when cu_seqlens is given.
+ * the packed token count when cu_seqlens is given.  Empty sequences and
+ * seq_len = 0 are legal as for gdn_fwd: d_initial_state of an empty sequence
+ * is its d_final_state (zeros without one).
  */
 size_t gdn_bwd_workspace_size(int32_t num_seqs, int32_t seq_len, int32_t num_heads,
                               int32_t head_dim_k, int32_t head_dim_v);

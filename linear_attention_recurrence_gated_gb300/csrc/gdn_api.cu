@@ -22,6 +22,20 @@ bool supported_dv(int dv) { return dv >= 32 && dv <= 256 && dv % 32 == 0; }
 
 }  // namespace
 
+namespace gdn {
+// A call with no tokens: copy each initial state to the final state (zeros
+// without one); nothing else is read or written.
+gdn_status pass_states(const float *from, float *to, size_t bytes, cudaStream_t s) {
+  if (to == nullptr) return GDN_OK;
+  if (!aligned16(to) || (from && !aligned16(from))) return GDN_ERR_INVALID_ARG;
+  if (from && from != to && overlaps(from, bytes, to, bytes)) return GDN_ERR_INVALID_ARG;
+  const cudaError_t e = from == nullptr ? cudaMemsetAsync(to, 0, bytes, s)
+                        : from == to    ? cudaSuccess
+                                        : cudaMemcpyAsync(to, from, bytes, cudaMemcpyDeviceToDevice, s);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+}  // namespace gdn
+
 extern "C" {
 
 size_t gdn_fwd_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_dim_k,
@@ -63,7 +77,7 @@ gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
                    int32_t num_seqs, int32_t chunk_size, gdn_dtype dtype, uint32_t flags,
                    void *workspace, size_t workspace_bytes, void *stream) {
   // ---- shapes ----
-  if (batch <= 0 || seq_len <= 0 || num_heads <= 0 || head_dim_k <= 0 || head_dim_v <= 0 ||
+  if (batch <= 0 || seq_len < 0 || num_heads <= 0 || head_dim_k <= 0 || head_dim_v <= 0 ||
       num_seqs <= 0)
     return GDN_ERR_INVALID_ARG;
   if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
@@ -72,6 +86,10 @@ gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
   if (!supported_dk(head_dim_k) || !supported_dv(head_dim_v)) return GDN_ERR_UNSUPPORTED;
   if (!gdn::simt_chunk_supported(chunk_size, head_dim_k)) return GDN_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || num_heads > 65535) return GDN_ERR_UNSUPPORTED;
+  if (seq_len == 0)   // no tokens: every state passes through, nothing else is read
+    return gdn::pass_states(initial_state, final_state,
+                            (size_t)num_seqs * num_heads * head_dim_k * head_dim_v * 4,
+                            (cudaStream_t)stream);
 
   // ---- pointers ----
   if (!q || !k || !v || !g || !beta || !o) return GDN_ERR_INVALID_ARG;
@@ -145,7 +163,7 @@ const char *gdn_status_string(int32_t status) {
     case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace missing or too small";
     case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA runtime call or launch failed";
     case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a bounded device wait gave up";
-    case GDN_ERR_BAD_SEQLENS: return "GDN_ERR_BAD_SEQLENS: cu_seqlens not strictly increasing from 0 to T";
+    case GDN_ERR_BAD_SEQLENS: return "GDN_ERR_BAD_SEQLENS: cu_seqlens does not rise from 0 to T without decreasing";
     case GDN_ERR_DEVICE_CHECK: return "GDN_ERR_DEVICE_CHECK: a device-side check failed";
     default: return "GDN_ERR_UNKNOWN";
   }

@@ -518,6 +518,9 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 
 }  // namespace
 
+// A call with no tokens (gdn_api.cu): the state gradient passes through.
+gdn_status pass_states(const float *from, float *to, size_t bytes, cudaStream_t s);
+
 // The chunked tensor-core backward for bf16 storage (gdn_bwd_chunk.cu).
 bool bwd_chunked_supported(int dk, int dv);
 size_t bwd_chunked_ws_bytes(int64_t units, int dk, int dv);
@@ -529,7 +532,7 @@ cudaError_t launch_bwd_chunked(const FwdParams &f, const void *dO, const float *
 extern "C" size_t gdn_bwd_workspace_size(int32_t num_seqs, int32_t seq_len, int32_t num_heads,
                                          int32_t head_dim_k, int32_t head_dim_v) {
   using namespace gdn;
-  if (num_seqs <= 0 || seq_len <= 0 || num_heads <= 0 || head_dim_k <= 0 || head_dim_v <= 0)
+  if (num_seqs <= 0 || seq_len < 0 || num_heads <= 0 || head_dim_k <= 0 || head_dim_v <= 0)
     return 0;
   if (head_dim_v % kCols) return 0;
   const int per = ckpt_per_chunk(num_seqs, seq_len, num_heads, head_dim_k, head_dim_v);
@@ -555,7 +558,7 @@ extern "C" gdn_status gdn_bwd(const void *q, const void *k, const void *v, const
                               uint32_t flags, void *workspace, size_t workspace_bytes,
                               void *stream) {
   using namespace gdn;
-  if (batch <= 0 || seq_len <= 0 || num_heads <= 0 || head_dim_k <= 0 || head_dim_v <= 0 ||
+  if (batch <= 0 || seq_len < 0 || num_heads <= 0 || head_dim_k <= 0 || head_dim_v <= 0 ||
       num_seqs <= 0)
     return GDN_ERR_INVALID_ARG;
   if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
@@ -564,6 +567,10 @@ extern "C" gdn_status gdn_bwd(const void *q, const void *k, const void *v, const
   if (!(head_dim_k == 32 || head_dim_k == 64 || head_dim_k == 128)) return GDN_ERR_UNSUPPORTED;
   if (head_dim_v < 32 || head_dim_v > 256 || head_dim_v % 32) return GDN_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || num_heads > 65535) return GDN_ERR_UNSUPPORTED;
+  if (seq_len == 0)   // no tokens: the state gradient passes through, nothing else is read
+    return pass_states(d_final_state, d_initial_state,
+                       (size_t)num_seqs * num_heads * head_dim_k * head_dim_v * 4,
+                       (cudaStream_t)stream);
   if (!q || !k || !v || !g || !beta || !d_o || !dq || !dk || !dv || !dg || !dbeta)
     return GDN_ERR_INVALID_ARG;
   const void *ptrs[] = {q, k, v, g, beta, initial_state, cu_seqlens, d_o, d_final_state,

@@ -66,6 +66,10 @@ gdn_fwd_simt_kernel(const FwdParams p) {
 
   int64_t start, len;
   if (!sequence_bounds(p, n, h, start, len)) return;
+  if (len == 0) {   // an empty sequence: the state passes through
+    pass_state_through(p, n, h, col0, DVT);
+    return;
+  }
 
   const Tin *q = static_cast<const Tin *>(p.q);
   const Tin *k = static_cast<const Tin *>(p.k);

@@ -258,6 +258,10 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
 
   int64_t start, len;
   if (!sequence_bounds(p, n, h, start, len)) return;  // uniform over the CTA
+  if (len == 0) {   // an empty sequence: the state passes through
+    pass_state_through(p, n, h, col0, kDvt);
+    return;
+  }
   const int nc = (int)((len + 63) / 64);
 
   Shared S;

@@ -46,8 +46,9 @@ __device__ __forceinline__ void report(DeviceStatus *st, uint32_t code, uint32_t
   }
 }
 
-// Bounds of sequence n: [start, start + len).  Returns false (after recording
-// GDN_ERR_BAD_SEQLENS) when cu_seqlens breaks 0 = cu[0] < ... < cu[N] = T.
+// Bounds of sequence n: [start, start + len), len = 0 for an empty sequence.
+// Returns false (after recording GDN_ERR_BAD_SEQLENS) when cu_seqlens breaks
+// 0 = cu[0] <= ... <= cu[N] = T.
 __device__ __forceinline__ bool sequence_bounds(const FwdParams &p, int n, int h,
                                                 int64_t &start, int64_t &len) {
   if (p.cu == nullptr) {
@@ -56,7 +57,7 @@ __device__ __forceinline__ bool sequence_bounds(const FwdParams &p, int n, int h
     return true;
   }
   const int64_t s = p.cu[n], e = p.cu[n + 1];
-  const bool ok = s >= 0 && e > s && e <= p.seq_len && (n != 0 || s == 0) &&
+  const bool ok = s >= 0 && e >= s && e <= p.seq_len && (n != 0 || s == 0) &&
                   (n != p.num_seqs - 1 || e == p.seq_len);
   if (!ok) {
     report(p.status, GDN_ERR_BAD_SEQLENS, (uint32_t)n, (uint32_t)h, 0u);
@@ -65,6 +66,19 @@ __device__ __forceinline__ bool sequence_bounds(const FwdParams &p, int n, int h
   start = s;
   len = e - s;
   return true;
+}
+
+// An empty sequence leaves its state as it came: the CTA that owns value
+// columns [col0, col0 + ncols) of (sequence n, head h) copies that slice of the
+// initial state (zeros without one) to the final state.
+__device__ __forceinline__ void pass_state_through(const FwdParams &p, int n, int h, int col0,
+                                                   int ncols) {
+  if (p.sN == nullptr) return;
+  const size_t base = ((size_t)n * p.num_heads + h) * (size_t)p.dk * p.dv;
+  for (int idx = threadIdx.x; idx < p.dk * ncols; idx += blockDim.x) {
+    const size_t off = base + (size_t)(idx / ncols) * p.dv + col0 + idx % ncols;
+    p.sN[off] = p.s0 ? p.s0[off] : 0.f;
+  }
 }
 
 __device__ __forceinline__ float to_f32(float x) { return x; }

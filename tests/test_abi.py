@@ -86,7 +86,8 @@ def call(L, **over):
     (dict(q=None), 1), (dict(o=None), 1), (dict(g=None), 1), (dict(beta=None), 1),
     (dict(q=BASE + 8), 1), (dict(o=BASE + (5 << 30) + 4), 1), (dict(sN=BASE + (6 << 30) + 2), 1),
     (dict(ws=None), 3), (dict(ws_bytes=255), 3), (dict(ws=BASE + (7 << 30) + 8), 1),
-    (dict(B=0), 1), (dict(T=0), 1), (dict(H=0), 1), (dict(N=3), 1),
+    (dict(B=0), 1), (dict(T=-1), 1), (dict(H=0), 1), (dict(N=3), 1),
+    (dict(T=0, sN=None), 0),                               # no tokens, no state: nothing to do
     (dict(cu=BASE + (8 << 30)), 1),                        # cu_seqlens needs batch == 1
     (dict(B=1, N=70000, cu=BASE + (8 << 30)), 2),          # too many sequences
     (dict(o=BASE), 1),                                     # o aliases q

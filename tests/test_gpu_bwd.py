@@ -172,7 +172,7 @@ def test_bwd_varlen_dk128():
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
-@pytest.mark.parametrize("cu", [[0, 10, 10, 40], [0, 30, 20, 40], [0, 10, 20, 39], [1, 10, 20, 40]])
+@pytest.mark.parametrize("cu", [[0, 10, 9, 40], [0, 30, 20, 40], [0, 10, 20, 39], [1, 10, 20, 40]])
 def test_bwd_bad_seqlens_reported(dtype, cu):
     """Malformed offsets are found on the device by both backward paths and
     reported by gdn_check (GDN_ERR_BAD_SEQLENS), which then clears the word."""
@@ -185,3 +185,33 @@ def test_bwd_bad_seqlens_reported(dtype, cu):
     G.gdn_bwd(q, k, v, g, beta, d_o, None, cu_t, None, workspace=ws)
     assert G.gdn_check(ws) == 6
     assert G.gdn_check(ws) == 0
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_bwd_varlen_empty_sequences(dtype):
+    """Empty sequences on both paths: no token gradients, and the gradient of
+    their initial state is d_final_state."""
+    lens = [5, 0, 70, 0, 64, 0]
+    w = W.custom(num_seqs=len(lens), len_range=(0, 70), H=2, dk=64, dv=64, dtype=dtype,
+                 init_state=True, seed=64)
+    inp = W.generate(w, lengths=lens)
+    d_o, dhN = _upstream(inp, 65, True)
+    gpu = _run(inp, d_o, dhN)
+    _check(gpu, _ref(inp, d_o, dhN), _tol(dtype, 64, 64))
+    for n in (1, 3, 5):
+        assert np.array_equal(gpu["dh0"][n], dhN[n].double().numpy())
+
+
+def test_bwd_zero_tokens():
+    """A call with no tokens passes d_final_state through to d initial_state."""
+    N, H, dk, dv = 2, 2, 64, 64
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    q = torch.empty((N, 0, H, dk), **bf)
+    v = torch.empty((N, 0, H, dv), **bf)
+    g = torch.empty((N, 0, H), dtype=torch.float32, device="cuda")
+    beta = torch.empty((N, 0, H), **bf)
+    dhN = torch.randn((N, H, dk, dv), device="cuda")
+    gr = G.gdn_bwd(q, q, v, g, beta, torch.empty_like(v), None, None, dhN, check=True)
+    assert torch.equal(gr["dh0"], dhN)
+    gr = G.gdn_bwd(q, q, v, g, beta, torch.empty_like(v), None, None, None, check=True)
+    assert torch.equal(gr["dh0"], torch.zeros_like(dhN))

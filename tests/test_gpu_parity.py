@@ -158,7 +158,7 @@ def test_no_final_state():
     assert s2 is None and torch.equal(o1, o2)
 
 
-@pytest.mark.parametrize("cu", [[0, 10, 10, 40], [0, 30, 20, 40], [0, 10, 20, 39], [1, 10, 20, 40]])
+@pytest.mark.parametrize("cu", [[0, 10, 9, 40], [0, 30, 20, 40], [0, 10, 20, 39], [1, 10, 20, 40]])
 def test_bad_seqlens_reported(cu):
     """Malformed offsets are found on the device and reported by gdn_check;
     the affected sequences write nothing."""
@@ -215,3 +215,38 @@ def test_chunk_sizes_agree():
     for o, s in outs[1:]:
         assert parity.rel(o.double().cpu().numpy(), outs[0][0].double().cpu().numpy()) <= 1e-5
         assert parity.rel(s.double().cpu().numpy(), outs[0][1].double().cpu().numpy()) <= 1e-5
+
+
+# ---------------- empty inputs ----------------
+@pytest.mark.parametrize("dtype,dk,dv", [("fp32", 64, 64), ("bf16", 64, 64), ("bf16", 128, 128)])
+def test_varlen_empty_sequences(dtype, dk, dv):
+    """Empty sequences (equal offsets) are legal: they read nothing and their
+    final state is their initial state, bit for bit."""
+    lens = [5, 0, 70, 0, 64, 0]
+    w = W.custom(num_seqs=len(lens), len_range=(0, 70), H=2, dk=dk, dv=dv, dtype=dtype,
+                 init_state=True, seed=28)
+    inp = W.generate(w, lengths=lens)
+    ro, rs, _, s = parity.compare(inp)
+    to, ts = parity.TOL[W._DTYPES[dtype]]
+    assert ro <= to and rs <= ts, (ro, rs)
+    for n in (1, 3, 5):
+        assert torch.equal(s[n].cpu(), inp["initial_state"][n])
+
+
+@pytest.mark.parametrize("varlen", [False, True])
+@pytest.mark.parametrize("init", [False, True])
+def test_zero_tokens(varlen, init):
+    """A call with no tokens reads nothing and passes every state through
+    (zeros without an initial state)."""
+    N, H, dk, dv = 3, 2, 64, 64
+    B = 1 if varlen else N
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    q = torch.empty((B, 0, H, dk), **bf)
+    v = torch.empty((B, 0, H, dv), **bf)
+    g = torch.empty((B, 0, H), dtype=torch.float32, device="cuda")
+    beta = torch.empty((B, 0, H), **bf)
+    cu = torch.zeros(N + 1, dtype=torch.int32, device="cuda") if varlen else None
+    s0 = torch.randn((N, H, dk, dv), device="cuda") if init else None
+    o, s = G.gdn_fwd(q, q, v, g, beta, s0, cu, check=True)
+    assert o.numel() == 0
+    assert torch.equal(s, s0 if init else torch.zeros_like(s))

@@ -49,7 +49,7 @@ def test_static_scratch_reports_and_clears_device_errors():
     d = _dev(W.generate(w))
     o = torch.empty_like(d["v"])
     s = torch.empty((3, 2, 32, 32), dtype=torch.float32, device="cuda")
-    bad = torch.tensor([0, 10, 10, 40], dtype=torch.int32, device="cuda")   # empty sequence
+    bad = torch.tensor([0, 10, 9, 40], dtype=torch.int32, device="cuda")    # offsets decrease
     good = torch.tensor([0, 10, 25, 40], dtype=torch.int32, device="cuda")
     assert G.gdn_fwd_static_scratch(d["q"], d["k"], d["v"], d["g"], d["beta"], None, bad,
                                     o, s, check=True) == 6
