@@ -215,3 +215,16 @@ def test_bwd_zero_tokens():
     assert torch.equal(gr["dh0"], dhN)
     gr = G.gdn_bwd(q, q, v, g, beta, torch.empty_like(v), None, None, None, check=True)
     assert torch.equal(gr["dh0"], torch.zeros_like(dhN))
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_bwd_varlen_many_short_sequences(dtype):
+    """600 packed sequences of 0 to 5 tokens on both paths: every chunk slot of
+    the chunked path is found by its binary search over the offsets."""
+    rng = np.random.default_rng(66)
+    lens = rng.integers(0, 6, 600).tolist()
+    w = W.custom(num_seqs=len(lens), len_range=(0, 5), H=1, dk=64, dv=64, dtype=dtype,
+                 init_state=True, seed=67)
+    inp = W.generate(w, lengths=lens)
+    d_o, dhN = _upstream(inp, 68, True)
+    _check(_run(inp, d_o, dhN), _ref(inp, d_o, dhN), _tol(dtype, 64, 64))

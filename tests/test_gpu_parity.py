@@ -250,3 +250,17 @@ def test_zero_tokens(varlen, init):
     o, s = G.gdn_fwd(q, q, v, g, beta, s0, cu, check=True)
     assert o.numel() == 0
     assert torch.equal(s, s0 if init else torch.zeros_like(s))
+
+
+@pytest.mark.parametrize("dtype,dk,dv", [("bf16", 64, 64), ("bf16", 128, 128), ("fp32", 64, 64)])
+def test_varlen_many_short_sequences(dtype, dk, dv):
+    """5000 packed sequences of 0 to 5 tokens (empty ones included): a large
+    grid of mostly single-chunk sequences."""
+    rng = np.random.default_rng(29)
+    lens = rng.integers(0, 6, 5000).tolist()
+    w = W.custom(num_seqs=len(lens), len_range=(0, 5), H=2, dk=dk, dv=dv, dtype=dtype,
+                 init_state=True, seed=30)
+    inp = W.generate(w, lengths=lens)
+    ro, rs, _, _ = parity.compare(inp)
+    to, ts = parity.TOL[W._DTYPES[dtype]]
+    assert ro <= to and rs <= ts, (ro, rs)
