@@ -32,6 +32,8 @@ EXPORTED = ("gdn_fwd_workspace_size", "gdn_workspace_init", "gdn_fwd", "gdn_chec
             "gdn_status_string", "gdn_fwd_kernel_name", "gdn_fwd_static_scratch",
             "gdn_decode", "gdn_diag_workspace_size", "gdn_diag_fwd", "gdn_conv_silu",
             "gdn_bwd_workspace_size", "gdn_bwd")
+# ... and include/gdn_debug.h (self-tests of the failure reporting).
+DEBUG_EXPORTED = ("gdn_debug_wait_timeout",)
 
 _lib = None
 _lock = threading.Lock()
@@ -64,6 +66,8 @@ def lib() -> ctypes.CDLL:
                                   vp, sz, vp]
             L.gdn_check.restype = ctypes.c_int
             L.gdn_check.argtypes = [vp, vp]
+            L.gdn_debug_wait_timeout.restype = ctypes.c_int
+            L.gdn_debug_wait_timeout.argtypes = [vp, sz, vp]
             L.gdn_status_string.restype = ctypes.c_char_p
             L.gdn_status_string.argtypes = [i32]
             L.gdn_fwd_kernel_name.restype = ctypes.c_char_p
@@ -135,6 +139,15 @@ def new_workspace(num_seqs, num_heads, head_dim_k, head_dim_v, flags=0, device=N
 def gdn_check(workspace: torch.Tensor, stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status word."""
     return int(lib().gdn_check(_ptr(workspace), _stream_handle(stream)))
+
+
+def gdn_debug_wait_timeout(workspace: torch.Tensor, stream=None) -> int:
+    """Enqueue the self-test whose bounded waits must give up (about 2 s) and
+    report GDN_ERR_TIMEOUT in the workspace status word; returns the launch
+    status (read the device status with gdn_check)."""
+    return int(lib().gdn_debug_wait_timeout(_ptr(workspace),
+                                            workspace.numel() * workspace.element_size(),
+                                            _stream_handle(stream)))
 
 
 def gdn_fwd_kernel_name(head_dim_k, head_dim_v, dtype: torch.dtype, flags: int = 0):

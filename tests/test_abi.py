@@ -34,6 +34,22 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(L, name), name
 
 
+def test_debug_header_symbols_are_exported(L):
+    hdr = open(os.path.join(ROOT, "include", "gdn_debug.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    names = sorted(set(re.findall(r"\b(gdn_[a-z_0-9]+)\s*\(", hdr)))
+    assert names == sorted(G.DEBUG_EXPORTED)
+    for name in names:
+        assert hasattr(L, name), name
+
+
+def test_debug_wait_timeout_validates_on_host(L):
+    vp = ctypes.c_void_p
+    assert L.gdn_debug_wait_timeout(vp(None), 256, vp(0)) == 3
+    assert L.gdn_debug_wait_timeout(vp(1 << 40), 255, vp(0)) == 3
+    assert L.gdn_debug_wait_timeout(vp((1 << 40) + 8), 256, vp(0)) == 1
+
+
 def test_status_strings(L):
     for code, name in G.STATUS_NAMES.items():
         assert G.status_string(code).startswith(name)

@@ -228,3 +228,32 @@ def test_bwd_varlen_many_short_sequences(dtype):
     inp = W.generate(w, lengths=lens)
     d_o, dhN = _upstream(inp, 68, True)
     _check(_run(inp, d_o, dhN), _ref(inp, d_o, dhN), _tol(dtype, 64, 64))
+
+
+@pytest.mark.parametrize("dtype,dk,dv", [("bf16", 64, 64), ("bf16", 128, 128), ("fp32", 64, 64)])
+def test_bwd_outputs_stay_inside_their_buffers(dtype, dk, dv):
+    """Canary regions around every gradient are untouched on both paths
+    (ragged varlen tails and an empty sequence included)."""
+    lens = [1, 63, 65, 0, 130]
+    w = W.custom(num_seqs=len(lens), len_range=(0, 130), H=2, dk=dk, dv=dv, dtype=dtype,
+                 init_state=True, seed=69)
+    inp = W.generate(w, lengths=lens)
+    d_o, dhN = _upstream(inp, 70, True)
+    B, T, H = inp["q"].shape[:3]
+    N = len(lens)
+    guard = 4096
+    shapes = {"dq": (B, T, H, dk), "dk": (B, T, H, dk), "dv": (B, T, H, dv), "dg": (B, T, H),
+              "dbeta": (B, T, H), "dh0": (N, H, dk, dv)}
+    bufs, grads = {}, {}
+    for name, shp in shapes.items():
+        n = int(np.prod(shp))
+        bufs[name] = torch.full((guard + n + guard,), -1234.5, dtype=torch.float32, device="cuda")
+        grads[name] = bufs[name][guard:guard + n].view(shp)
+    G.gdn_bwd(_dev(inp["q"]), _dev(inp["k"]), _dev(inp["v"]), _dev(inp["g"]), _dev(inp["beta"]),
+              _dev(d_o), _dev(inp["initial_state"]), _dev(inp["cu_seqlens"]), _dev(dhN),
+              grads=grads, check=True)
+    torch.cuda.synchronize()
+    for name, buf in bufs.items():
+        assert bool(torch.all(buf[:guard] == -1234.5)) and bool(torch.all(buf[-guard:] == -1234.5)), name
+    ref = _ref(inp, d_o, dhN)
+    _check({k: v.double().cpu().numpy() for k, v in grads.items()}, ref, _tol(dtype, dk, dv))

@@ -264,3 +264,44 @@ def test_varlen_many_short_sequences(dtype, dk, dv):
     ro, rs, _, _ = parity.compare(inp)
     to, ts = parity.TOL[W._DTYPES[dtype]]
     assert ro <= to and rs <= ts, (ro, rs)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128)])
+def test_long_sequence_with_one_token_tail(dk, dv):
+    """T = 64k + 1: 1024 full chunks and a one-token last chunk."""
+    w = W.custom(B=1, T=65537, H=1, dk=dk, dv=dv, dtype="bf16", gate_scale=0.01,
+                 init_state=True, seed=32)
+    _check(W.generate(w), torch.bfloat16)
+
+
+def _guarded(shape, dtype, guard=4096):
+    """A tensor of `shape` inside a buffer with `guard` canary elements on each
+    side (the view stays 16-byte aligned)."""
+    n = int(np.prod(shape))
+    buf = torch.full((guard + n + guard,), -1234.5, dtype=dtype, device="cuda")
+    return buf, buf[guard:guard + n].view(shape)
+
+
+def _guards_intact(buf, guard=4096):
+    return bool(torch.all(buf[:guard] == -1234.5)) and bool(torch.all(buf[-guard:] == -1234.5))
+
+
+@pytest.mark.parametrize("dtype,dk,dv", [("bf16", 64, 64), ("bf16", 128, 128), ("fp32", 64, 96)])
+def test_outputs_stay_inside_their_buffers(dtype, dk, dv):
+    """Canary regions around o and the final state are untouched: no kernel
+    writes outside its outputs (ragged varlen tails included)."""
+    lens = [1, 63, 65, 0, 130, 7]
+    w = W.custom(num_seqs=len(lens), len_range=(0, 130), H=2, dk=dk, dv=dv, dtype=dtype,
+                 init_state=True, seed=33)
+    inp = parity.to_dev(W.generate(w, lengths=lens))
+    tdt = W._DTYPES[dtype]
+    obuf, o = _guarded(inp["v"].shape, tdt)
+    sbuf, s = _guarded(inp["initial_state"].shape, torch.float32)
+    G.gdn_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["initial_state"],
+              inp["cu_seqlens"], o=o, final_state=s, check=True)
+    torch.cuda.synchronize()
+    assert _guards_intact(obuf) and _guards_intact(sbuf)
+    o_ref, s_ref = parity.oracle_forward(W.generate(w, lengths=lens))
+    to, ts = parity.TOL[tdt]
+    assert parity.rel(o.double().cpu().numpy(), o_ref) <= to
+    assert parity.rel(s.double().cpu().numpy(), s_ref) <= ts
