@@ -1079,10 +1079,13 @@ def bench_bwd(args, w: W.Workload, rank: int, world: int, local: int):
     cpu_secs = time.perf_counter() - t_c
     clk = clocks.summary(wall0, wall1, _bus_id(local))
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "metric": "GDN backward tokens/s (gdn_bwd), 1 GPU", "value": value, "unit": UNIT,
+        "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic",
+        # the chunked path multiplies bf16 operands with fp32 accumulation; the
+        # token-serial path computes in fp32
+        "dtype": "bf16" if chunked else "f32", "data": "synthetic",
         "timing": TIMING_NOTE[args.eager],
         "config": {"workload": w.name, "pass": "backward", "B": w.B, "T": w.T, "H": w.H,
                    "dk": w.dk, "dv": w.dv, "storage": w.dtype, "kernel": "bwd",
