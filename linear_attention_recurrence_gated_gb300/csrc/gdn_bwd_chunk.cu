@@ -316,42 +316,50 @@ __device__ __forceinline__ void block_inverse(PrepSmem<DK, DV> &s) {
     for (int i = 0; i < 16; ++i) Tb[i * LA + j] = t[i];
   }
   __syncthreads();
+  // Each thread forms four rows (4rq .. 4rq + 3) of one column c of a block, so
+  // that the column loads serve four rows.
   for (int L = 1; L < 4; ++L) {
     const int nb = 4 - L;   // blocks (j + L, j), j = 0..nb-1
-    for (int e = tid; e < nb * 256; e += kPrepThreads) {
-      const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + L;
-      const float *Arow = s.A + (16 * i + r) * LA;
-      float x = 0.f;
+    for (int e = tid; e < nb * 64; e += kPrepThreads) {
+      const int j = e >> 6, rq = (e >> 4) & 3, c = e & 15, i = j + L;
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
       for (int kb = j; kb < i; ++kb) {   // T_{kb, j}: the diagonal block (in A) or one below it
         const bool diag = kb == j;
         const float *Tc = diag ? s.A + 16 * j * LA + 16 * j + c : s.Toff[kb * (kb - 1) / 2 + j] + c;
         const int ld = diag ? LA : LB;
 #pragma unroll
         for (int m4 = 0; m4 < 4; ++m4) {
-          const float4 a = *reinterpret_cast<const float4 *>(Arow + 16 * kb + 4 * m4);
-          x = fmaf(a.x, Tc[(4 * m4) * ld], x);
-          x = fmaf(a.y, Tc[(4 * m4 + 1) * ld], x);
-          x = fmaf(a.z, Tc[(4 * m4 + 2) * ld], x);
-          x = fmaf(a.w, Tc[(4 * m4 + 3) * ld], x);
+          const float t0 = Tc[(4 * m4) * ld], t1 = Tc[(4 * m4 + 1) * ld];
+          const float t2 = Tc[(4 * m4 + 2) * ld], t3 = Tc[(4 * m4 + 3) * ld];
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) {
+            const float4 a = *reinterpret_cast<const float4 *>(
+                s.A + (16 * i + 4 * rq + rr) * LA + 16 * kb + 4 * m4);
+            x[rr] = fmaf(a.x, t0, fmaf(a.y, t1, fmaf(a.z, t2, fmaf(a.w, t3, x[rr]))));
+          }
         }
       }
-      s.X[j][r * LB + c] = x;
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) s.X[j][(4 * rq + rr) * LB + c] = x[rr];
     }
     __syncthreads();
-    for (int e = tid; e < nb * 256; e += kPrepThreads) {
-      const int j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + L;
-      const float *Trow = s.A + (16 * i + r) * LA + 16 * i;   // T_ii, lower triangular
+    for (int e = tid; e < nb * 64; e += kPrepThreads) {
+      const int j = e >> 6, rq = (e >> 4) & 3, c = e & 15, i = j + L;
       const float *Xc = s.X[j] + c;
-      float x = 0.f;
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int m4 = 0; m4 < 4; ++m4) {
-        const float4 t = *reinterpret_cast<const float4 *>(Trow + 4 * m4);
-        x = fmaf(t.x, Xc[(4 * m4) * LB], x);
-        x = fmaf(t.y, Xc[(4 * m4 + 1) * LB], x);
-        x = fmaf(t.z, Xc[(4 * m4 + 2) * LB], x);
-        x = fmaf(t.w, Xc[(4 * m4 + 3) * LB], x);
+        const float t0 = Xc[(4 * m4) * LB], t1 = Xc[(4 * m4 + 1) * LB];
+        const float t2 = Xc[(4 * m4 + 2) * LB], t3 = Xc[(4 * m4 + 3) * LB];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {   // T_ii, lower triangular
+          const float4 a = *reinterpret_cast<const float4 *>(
+              s.A + (16 * i + 4 * rq + rr) * LA + 16 * i + 4 * m4);
+          x[rr] = fmaf(a.x, t0, fmaf(a.y, t1, fmaf(a.z, t2, fmaf(a.w, t3, x[rr]))));
+        }
       }
-      s.Toff[i * (i - 1) / 2 + j][r * LB + c] = -x;
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) s.Toff[i * (i - 1) / 2 + j][(4 * rq + rr) * LB + c] = -x[rr];
     }
     __syncthreads();
   }
