@@ -126,3 +126,27 @@ def test_pins_catch_planted_mistake(name, old, new, tmp_path):
     spec.loader.exec_module(mod)
     bad = _bad(pin_finite_differences(mod)) + _bad(pin_beta_zero(mod))
     assert bad, f"no pin caught the planted mistake: {name}"
+
+
+def test_chunked_backward_equals_autograd():
+    """The chunked (WY-form) statement of the backward, oracle.chunked_grad,
+    equals the autograd oracle to fp64 rounding: several chunks, a ragged
+    last chunk, packed sequences with an empty one, slow and fast gates."""
+    import torch
+    import oracle.chunked_grad as CG
+    rng = np.random.default_rng(71)
+    cases = [(1, 150, 2, 8, 4, None, 1.0), (2, 64, 1, 4, 6, None, 1.0),
+             (1, 140, 1, 6, 5, [0, 70, 70, 71, 140], 0.01)]
+    for B, T, H, dk, dv, cu, scale in cases:
+        q, k, v, g, beta, _ = _inputs(rng, B, T, H, dk, dv)
+        g = g * scale
+        N = B if cu is None else len(cu) - 1
+        h0 = rng.standard_normal((N, H, dk, dv)) * 0.3
+        d_o = rng.standard_normal((B, T, H, dv))
+        dhN = rng.standard_normal((N, H, dk, dv))
+        t = [torch.from_numpy(x) for x in (q, k, v, g, beta, h0, d_o, dhN)]
+        cu_t = None if cu is None else torch.tensor(cu)
+        ref = OG.backward(t[0], t[1], t[2], t[3], t[4], t[5], t[6], t[7], cu_t)
+        got = CG.backward(q, k, v, g, beta, h0, d_o, dhN, cu)
+        for name in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
+            assert rel(got[name], ref[name]) < 1e-10, (name, B, T, cu)
