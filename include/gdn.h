@@ -87,7 +87,13 @@ size_t gdn_fwd_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_
 
 /* Enqueue a zero fill of the first `workspace_bytes` bytes of `workspace` on
  * `stream`.  A workspace must be zeroed once before its first use by gdn_fwd
- * (gdn_check clears the status word it reports, so one fill is enough). */
+ * (gdn_check clears the status word it reports, so one fill is enough).
+ * No passage of the pages defines a workspace: it carries the device status
+ * word through which this library surfaces errors found on the GPU (the
+ * pages' kernel raises instead of falling back: "Optimization Quartet",
+ * Triton GDN kernel section 3.5).  Returns GDN_ERR_WORKSPACE for a NULL or
+ * too small (< 256 bytes) workspace, GDN_ERR_CUDA if the fill cannot be
+ * enqueued; the workspace stays owned by the caller. */
 gdn_status gdn_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -167,17 +173,21 @@ gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
  * the GPU (different streams, no ordering between them) race on the array and
  * may report each other's device errors; serialise them.
  *
- * The first call on a device, with that device current, looks up the array's
- * device address (cudaGetSymbolAddress) and caches it; make that first call
- * before any stream capture begins.
+ * Each call made outside stream capture, with the device current, looks up the
+ * array's device address (cudaGetSymbolAddress, which allocates nothing) and
+ * remembers it per device; a call made while `stream` is capturing uses the
+ * remembered address.  So make the first call on a device before any stream
+ * capture begins, and after a cudaDeviceReset make one uncaptured call before
+ * capturing again.
  *
  * Arguments are those of gdn_fwd without workspace/workspace_bytes, plus
  * `check`: when nonzero the call synchronises `stream` after the launch and
  * returns any error the kernel recorded (GDN_ERR_BAD_SEQLENS, ...); when zero
  * it returns once the work is enqueued and device-detected errors are not
- * reported.  Sizes whose scratch need (gdn_fwd_workspace_size) exceeds the
- * 256-byte array are rejected with GDN_ERR_WORKSPACE before anything is
- * enqueued.  The call performs no device allocation or free.
+ * reported.  Every host-side check of gdn_fwd runs first; a call that fails
+ * one, or whose scratch need (gdn_fwd_workspace_size) exceeds the 256-byte
+ * array (GDN_ERR_WORKSPACE), returns its error and enqueues nothing.  The
+ * call performs no device allocation or free.
  */
 gdn_status gdn_fwd_static_scratch(const void *q, const void *k, const void *v, const float *g,
                                   const void *beta, const float *initial_state,
@@ -367,10 +377,20 @@ gdn_status gdn_bwd(const void *q, const void *k, const void *v, const float *g,
 
 /* Synchronise `stream`, read the status word in `workspace`, clear it, and
  * return it (GDN_OK if no kernel recorded an error since the last check).
- * Also returns GDN_ERR_CUDA if the stream synchronisation itself failed. */
+ * Also returns GDN_ERR_CUDA if the stream synchronisation itself failed, and
+ * GDN_ERR_WORKSPACE for a NULL workspace.  This is how errors that only the
+ * kernels can see (bad device-side cu_seqlens, a bounded wait that gave up,
+ * a GDN_DEBUG_CHECKS violation) reach the caller as a clear error code
+ * rather than a silent wrong result.  No passage of the pages defines this
+ * call; it follows their rule that failures surface as errors, with no silent
+ * fallback ("Optimization Quartet", Triton GDN kernel section 3.5). */
 gdn_status gdn_check(void *workspace, void *stream);
 
-/* Static, human-readable name of a status code (never NULL). */
+/* Static, human-readable name of a status code (never NULL; the string is
+ * owned by the library).  Unknown codes give "GDN_ERR_UNKNOWN".  No passage
+ * of the pages defines it: it gives the clear error message that the pages'
+ * no-silent-fallback rule asks for ("Optimization Quartet", Triton GDN kernel
+ * section 3.5). */
 const char *gdn_status_string(int32_t status);
 
 /* Name of the kernel gdn_fwd would launch for these arguments with

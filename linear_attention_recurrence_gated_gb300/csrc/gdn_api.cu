@@ -20,6 +20,13 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 bool supported_dk(int dk) { return dk == 32 || dk == 64 || dk == 128; }
 bool supported_dv(int dv) { return dv >= 32 && dv <= 256 && dv % 32 == 0; }
 
+bool use_tc(int dk, int dv, gdn_dtype dtype, uint32_t flags) {
+  // The tensor-core kernel multiplies the TMA-loaded q/k tiles as they arrive,
+  // so in-kernel q/k normalisation runs on the fp32 kernel.
+  return dtype == GDN_BF16 && !(flags & (GDN_FORCE_SIMT | GDN_QK_L2NORM)) &&
+         gdn::tc_supported(dk, dv);
+}
+
 }  // namespace
 
 namespace gdn {
@@ -33,6 +40,100 @@ gdn_status pass_states(const float *from, float *to, size_t bytes, cudaStream_t 
                         : from == to    ? cudaSuccess
                                         : cudaMemcpyAsync(to, from, bytes, cudaMemcpyDeviceToDevice, s);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+}  // namespace gdn
+
+namespace gdn {
+// Every host-side check of gdn_fwd, in one place, so that each entry point
+// that runs the forward pass validates its arguments before it enqueues any
+// work.  Fills `call` on success.
+gdn_status fwd_validate(const void *q, const void *k, const void *v, const float *g,
+                        const void *beta, const float *initial_state,
+                        const int32_t *cu_seqlens, void *o, float *final_state, int32_t batch,
+                        int32_t seq_len, int32_t num_heads, int32_t head_dim_k,
+                        int32_t head_dim_v, int32_t num_seqs, int32_t chunk_size,
+                        gdn_dtype dtype, uint32_t flags, void *workspace,
+                        size_t workspace_bytes, FwdCall *call) {
+  // ---- shapes ----
+  if (batch <= 0 || seq_len < 0 || num_heads <= 0 || head_dim_k <= 0 || head_dim_v <= 0 ||
+      num_seqs <= 0)
+    return GDN_ERR_INVALID_ARG;
+  if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  if (flags & ~(uint32_t)(GDN_QK_L2NORM | GDN_FORCE_SIMT)) return GDN_ERR_INVALID_ARG;
+  if (cu_seqlens ? batch != 1 : num_seqs != batch) return GDN_ERR_INVALID_ARG;
+  if (!supported_dk(head_dim_k) || !supported_dv(head_dim_v)) return GDN_ERR_UNSUPPORTED;
+  if (!simt_chunk_supported(chunk_size, head_dim_k)) return GDN_ERR_UNSUPPORTED;
+  if (num_seqs > 65535 || num_heads > 65535) return GDN_ERR_UNSUPPORTED;
+  const size_t b_state = (size_t)num_seqs * num_heads * head_dim_k * head_dim_v * 4;
+  call->states_only = seq_len == 0;
+  call->state_bytes = b_state;
+  call->chunk = chunk_size;
+  call->dtype = dtype;
+  if (seq_len == 0) {  // no tokens: every state passes through, nothing else is read
+    if (final_state == nullptr) { call->p.s0 = initial_state; call->p.sN = nullptr; return GDN_OK; }
+    if (!aligned16(final_state) || (initial_state && !aligned16(initial_state)))
+      return GDN_ERR_INVALID_ARG;
+    if (initial_state && initial_state != final_state &&
+        overlaps(initial_state, b_state, final_state, b_state))
+      return GDN_ERR_INVALID_ARG;
+    call->p.s0 = initial_state;
+    call->p.sN = final_state;
+    return GDN_OK;
+  }
+
+  // ---- pointers ----
+  if (!q || !k || !v || !g || !beta || !o) return GDN_ERR_INVALID_ARG;
+  const void *ptrs[] = {q, k, v, g, beta, initial_state, cu_seqlens, o, final_state};
+  for (const void *ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
+  if (!workspace) return GDN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return GDN_ERR_INVALID_ARG;
+  if (workspace_bytes <
+      gdn_fwd_workspace_size(num_seqs, num_heads, head_dim_k, head_dim_v, flags))
+    return GDN_ERR_WORKSPACE;
+
+  // ---- aliasing: outputs must not overlap inputs (initial_state == final_state allowed) ----
+  const size_t e = dtype == GDN_F32 ? 4 : 2;
+  const size_t rows = (size_t)batch * (size_t)seq_len * (size_t)num_heads;
+  const size_t b_qk = rows * head_dim_k * e, b_v = rows * head_dim_v * e;
+  const size_t b_g = rows * 4, b_beta = rows * e;
+  const size_t b_cu = cu_seqlens ? (size_t)(num_seqs + 1) * 4 : 0;
+  struct Range { const void *p; size_t n; };
+  const Range inputs[] = {{q, b_qk}, {k, b_qk}, {v, b_v}, {g, b_g}, {beta, b_beta},
+                          {cu_seqlens, b_cu}, {workspace, workspace_bytes}};
+  for (const Range &r : inputs) {
+    if (overlaps(o, b_v, r.p, r.n)) return GDN_ERR_INVALID_ARG;
+    if (overlaps(final_state, b_state, r.p, r.n)) return GDN_ERR_INVALID_ARG;
+  }
+  if (overlaps(o, b_v, initial_state, b_state) || overlaps(o, b_v, final_state, b_state))
+    return GDN_ERR_INVALID_ARG;
+  if (initial_state && final_state && initial_state != final_state &&
+      overlaps(initial_state, b_state, final_state, b_state))
+    return GDN_ERR_INVALID_ARG;
+  if (overlaps(workspace, workspace_bytes, initial_state, b_state)) return GDN_ERR_INVALID_ARG;
+
+  FwdParams &p = call->p;
+  p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g;
+  p.s0 = initial_state; p.cu = cu_seqlens; p.o = o; p.sN = final_state;
+  p.status = static_cast<DeviceStatus *>(workspace);
+  p.ckpt = nullptr;
+  p.seq_len = seq_len;
+  p.num_heads = num_heads; p.dk = head_dim_k; p.dv = head_dim_v; p.num_seqs = num_seqs;
+  p.flags = flags;
+  return GDN_OK;
+}
+
+// Enqueue the kernels of a call that fwd_validate accepted.
+gdn_status fwd_launch(const FwdCall &call, cudaStream_t stream) {
+  if (call.states_only)
+    return call.p.sN ? pass_states(call.p.s0, call.p.sN, call.state_bytes, stream) : GDN_OK;
+  // the tensor-core kernels are built for 64-token chunks; other chunk sizes
+  // run on the fp32 CUDA-core kernel
+  const FwdParams &p = call.p;
+  const cudaError_t err = call.chunk == kChunk && use_tc(p.dk, p.dv, call.dtype, p.flags)
+                              ? launch_fwd_tc(p, stream)
+                              : launch_fwd_simt(p, call.dtype, call.chunk, stream);
+  return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 }  // namespace gdn
 
@@ -52,15 +153,6 @@ gdn_status gdn_workspace_init(void *workspace, size_t workspace_bytes, void *str
   return GDN_OK;
 }
 
-namespace {
-bool use_tc(int dk, int dv, gdn_dtype dtype, uint32_t flags) {
-  // The tensor-core kernel multiplies the TMA-loaded q/k tiles as they arrive,
-  // so in-kernel q/k normalisation runs on the fp32 kernel.
-  return dtype == GDN_BF16 && !(flags & (GDN_FORCE_SIMT | GDN_QK_L2NORM)) &&
-         gdn::tc_supported(dk, dv);
-}
-}  // namespace
-
 const char *gdn_fwd_kernel_name(int32_t head_dim_k, int32_t head_dim_v, gdn_dtype dtype,
                                 uint32_t flags) {
   if (!supported_dk(head_dim_k) || !supported_dv(head_dim_v)) return nullptr;
@@ -76,69 +168,13 @@ gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
                    int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
                    int32_t num_seqs, int32_t chunk_size, gdn_dtype dtype, uint32_t flags,
                    void *workspace, size_t workspace_bytes, void *stream) {
-  // ---- shapes ----
-  if (batch <= 0 || seq_len < 0 || num_heads <= 0 || head_dim_k <= 0 || head_dim_v <= 0 ||
-      num_seqs <= 0)
-    return GDN_ERR_INVALID_ARG;
-  if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
-  if (flags & ~(uint32_t)(GDN_QK_L2NORM | GDN_FORCE_SIMT)) return GDN_ERR_INVALID_ARG;
-  if (cu_seqlens ? batch != 1 : num_seqs != batch) return GDN_ERR_INVALID_ARG;
-  if (!supported_dk(head_dim_k) || !supported_dv(head_dim_v)) return GDN_ERR_UNSUPPORTED;
-  if (!gdn::simt_chunk_supported(chunk_size, head_dim_k)) return GDN_ERR_UNSUPPORTED;
-  if (num_seqs > 65535 || num_heads > 65535) return GDN_ERR_UNSUPPORTED;
-  if (seq_len == 0)   // no tokens: every state passes through, nothing else is read
-    return gdn::pass_states(initial_state, final_state,
-                            (size_t)num_seqs * num_heads * head_dim_k * head_dim_v * 4,
-                            (cudaStream_t)stream);
-
-  // ---- pointers ----
-  if (!q || !k || !v || !g || !beta || !o) return GDN_ERR_INVALID_ARG;
-  const void *ptrs[] = {q, k, v, g, beta, initial_state, cu_seqlens, o, final_state};
-  for (const void *ptr : ptrs)
-    if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
-  if (!workspace) return GDN_ERR_WORKSPACE;
-  if (!aligned16(workspace)) return GDN_ERR_INVALID_ARG;
-  if (workspace_bytes <
-      gdn_fwd_workspace_size(num_seqs, num_heads, head_dim_k, head_dim_v, flags))
-    return GDN_ERR_WORKSPACE;
-
-  // ---- aliasing: outputs must not overlap inputs (initial_state == final_state allowed) ----
-  const size_t e = dtype == GDN_F32 ? 4 : 2;
-  const size_t rows = (size_t)batch * (size_t)seq_len * (size_t)num_heads;
-  const size_t b_qk = rows * head_dim_k * e, b_v = rows * head_dim_v * e;
-  const size_t b_g = rows * 4, b_beta = rows * e;
-  const size_t b_state = (size_t)num_seqs * num_heads * head_dim_k * head_dim_v * 4;
-  const size_t b_cu = cu_seqlens ? (size_t)(num_seqs + 1) * 4 : 0;
-  struct Range { const void *p; size_t n; };
-  const Range inputs[] = {{q, b_qk}, {k, b_qk}, {v, b_v}, {g, b_g}, {beta, b_beta},
-                          {cu_seqlens, b_cu}, {workspace, workspace_bytes}};
-  for (const Range &r : inputs) {
-    if (overlaps(o, b_v, r.p, r.n)) return GDN_ERR_INVALID_ARG;
-    if (overlaps(final_state, b_state, r.p, r.n)) return GDN_ERR_INVALID_ARG;
-  }
-  if (overlaps(o, b_v, initial_state, b_state) || overlaps(o, b_v, final_state, b_state))
-    return GDN_ERR_INVALID_ARG;
-  if (initial_state && final_state && initial_state != final_state &&
-      overlaps(initial_state, b_state, final_state, b_state))
-    return GDN_ERR_INVALID_ARG;
-  if (overlaps(workspace, workspace_bytes, initial_state, b_state)) return GDN_ERR_INVALID_ARG;
-
-  gdn::FwdParams p;
-  p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g;
-  p.s0 = initial_state; p.cu = cu_seqlens; p.o = o; p.sN = final_state;
-  p.status = static_cast<gdn::DeviceStatus *>(workspace);
-  p.ckpt = nullptr;
-  p.seq_len = seq_len;
-  p.num_heads = num_heads; p.dk = head_dim_k; p.dv = head_dim_v; p.num_seqs = num_seqs;
-  p.flags = flags;
-
-  // the tensor-core kernels are built for 64-token chunks; other chunk sizes
-  // run on the fp32 CUDA-core kernel
-  const cudaError_t err =
-      chunk_size == gdn::kChunk && use_tc(head_dim_k, head_dim_v, dtype, flags)
-          ? gdn::launch_fwd_tc(p, (cudaStream_t)stream)
-          : gdn::launch_fwd_simt(p, dtype, chunk_size, (cudaStream_t)stream);
-  return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  gdn::FwdCall call;
+  const gdn_status st = gdn::fwd_validate(q, k, v, g, beta, initial_state, cu_seqlens, o,
+                                          final_state, batch, seq_len, num_heads, head_dim_k,
+                                          head_dim_v, num_seqs, chunk_size, dtype, flags,
+                                          workspace, workspace_bytes, &call);
+  if (st != GDN_OK) return st;
+  return gdn::fwd_launch(call, (cudaStream_t)stream);
 }
 
 gdn_status gdn_check(void *workspace, void *stream) {

@@ -30,7 +30,7 @@
 //
 // Roles (24 warps, one CTA per SM; warp w reaches the TMEM lanes 32*(w%4)..+31
 // and issues on SM sub-partition w%4):
-//   warp 16        producer: gate vectors + TMA loads of Q, K, V (ring of 3
+//   warp 16        producer: gate vectors + TMA loads of Q, K, V (ring of 4
 //                  slots), and an L2 prefetch of the tiles that next reuse the slot
 //   warp 13        [Q; K] K^T issuer (tcgen05.mma + commit); owns tensor memory
 //   warps 8,9      drain the P rows of [Q; K] K^T (masked decay, bf16)

@@ -98,6 +98,25 @@ __host__ __device__ inline int64_t ckpt_slots(int64_t num_seqs, int64_t seq_len)
   return dense > packed ? dense : packed;
 }
 
+// A forward call that passed the host-side checks, ready to launch.
+struct FwdCall {
+  FwdParams p;
+  bool states_only;     // seq_len == 0: the states pass through, no kernel runs
+  size_t state_bytes;   // bytes of one [N, H, dk, dv] fp32 state array
+  int chunk;
+  gdn_dtype dtype;
+};
+// Every host-side check of gdn_fwd (shapes, alignment, workspace size,
+// aliasing); returns GDN_OK and fills `call`, or the error and enqueues nothing.
+gdn_status fwd_validate(const void *q, const void *k, const void *v, const float *g,
+                        const void *beta, const float *initial_state,
+                        const int32_t *cu_seqlens, void *o, float *final_state, int32_t batch,
+                        int32_t seq_len, int32_t num_heads, int32_t head_dim_k,
+                        int32_t head_dim_v, int32_t num_seqs, int32_t chunk_size,
+                        gdn_dtype dtype, uint32_t flags, void *workspace,
+                        size_t workspace_bytes, FwdCall *call);
+gdn_status fwd_launch(const FwdCall &call, cudaStream_t stream);
+
 // Launchers (one per kernel family).  Return a cudaError_t from the launch.
 cudaError_t launch_fwd_simt(const FwdParams &p, gdn_dtype dtype, int chunk, cudaStream_t stream);
 bool simt_chunk_supported(int chunk, int dk);   // chunk in {32, 64, 128}, not 128 with dk 128

@@ -19,14 +19,21 @@ constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 void *g_scratch_addr[kMaxDevices] = {};
 
-// Device address of the array on the current device, looked up once per
-// device (host code may not use the symbol itself as a device pointer).
-gdn_status scratch_address(void **out) {
+// Device address of the array on the current device.  Host code may not use
+// the symbol itself as a device pointer, so the address comes from
+// cudaGetSymbolAddress with the device current.  Outside stream capture it is
+// looked up again on every call (the lookup allocates nothing), so a context
+// that was reset and created anew is seen; during capture the address cached
+// by the last uncaptured call on this device is used, since the lookup could
+// initialise state that capture does not allow.
+gdn_status scratch_address(cudaStream_t s, void **out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return GDN_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
+  if (cap == cudaStreamCaptureStatusNone || g_scratch_addr[dev] == nullptr) {
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr)
       return GDN_ERR_CUDA;
@@ -49,17 +56,21 @@ extern "C" gdn_status gdn_fwd_static_scratch(
   if (need == 0) return GDN_ERR_INVALID_ARG;
   if (need > kStaticScratchBytes) return GDN_ERR_WORKSPACE;  // beyond the static maximum
 
+  cudaStream_t s = (cudaStream_t)stream;
   void *scratch = nullptr;
-  gdn_status st = scratch_address(&scratch);
+  gdn_status st = scratch_address(s, &scratch);
   if (st != GDN_OK) return st;
 
-  cudaStream_t s = (cudaStream_t)stream;
+  // every host-side check of gdn_fwd runs before anything is enqueued
+  gdn::FwdCall call;
+  st = gdn::fwd_validate(q, k, v, g, beta, initial_state, cu_seqlens, o, final_state, batch,
+                         seq_len, num_heads, head_dim_k, head_dim_v, num_seqs, chunk_size,
+                         dtype, flags, scratch, kStaticScratchBytes, &call);
+  if (st != GDN_OK) return st;
+
   // The array keeps the previous call's contents: the status must start at zero.
   if (cudaMemsetAsync(scratch, 0, kStaticScratchBytes, s) != cudaSuccess) return GDN_ERR_CUDA;
-
-  st = gdn_fwd(q, k, v, g, beta, initial_state, cu_seqlens, o, final_state, batch, seq_len,
-               num_heads, head_dim_k, head_dim_v, num_seqs, chunk_size, dtype, flags, scratch,
-               kStaticScratchBytes, stream);
+  st = gdn::fwd_launch(call, s);
   if (st != GDN_OK || !check) return st;
 
   gdn::DeviceStatus rec;

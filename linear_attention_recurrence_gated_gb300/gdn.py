@@ -155,6 +155,43 @@ def gdn_fwd_kernel_name(head_dim_k, head_dim_v, dtype: torch.dtype, flags: int =
     return None if r is None else r.decode()
 
 
+def _check_fwd_tensors(where, q, k, v, g, beta, initial_state, cu_seqlens, o, final_state):
+    """The tensor checks every forward entry point makes before it calls the
+    library: device, contiguity, dtypes and shapes of inputs and of any output
+    passed in.  Returns (N, H, dk, dv)."""
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError(f"{where}: q, k, v must be [B, T, H, D]")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    tensors = [q, k, v, g, beta] + [t for t in (initial_state, cu_seqlens, o, final_state)
+                                    if t is not None]
+    for t in tensors:
+        if not t.is_cuda:
+            raise ValueError(f"{where}: every tensor must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError(f"{where}: every tensor must be contiguous")
+    _dtype_code(q.dtype)
+    if k.dtype != q.dtype or v.dtype != q.dtype or beta.dtype != q.dtype:
+        raise TypeError(f"{where}: q, k, v and beta must share one storage dtype")
+    if g.dtype != torch.float32:
+        raise TypeError(f"{where}: g must be float32")
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3] or g.shape != (B, T, H) or \
+            beta.shape != (B, T, H):
+        raise ValueError(f"{where}: shape mismatch among q, k, v, g, beta")
+    if initial_state is not None and (initial_state.dtype != torch.float32 or
+                                      initial_state.shape != (N, H, dk, dv)):
+        raise ValueError(f"{where}: initial_state must be float32 [N, H, dk, dv]")
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError(f"{where}: cu_seqlens must be int32")
+    if o is not None and (o.shape != v.shape or o.dtype != v.dtype):
+        raise ValueError(f"{where}: o must match v in shape and dtype")
+    if final_state is not None and (final_state.dtype != torch.float32 or
+                                    final_state.shape != (N, H, dk, dv)):
+        raise ValueError(f"{where}: final_state must be float32 [N, H, dk, dv]")
+    return N, H, dk, dv
+
+
 def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
             final_state=None, output_final_state=True, workspace=None,
             qk_l2norm=False, force_simt=False, chunk_size=CHUNK_SIZE, stream=None, check=False):
@@ -169,38 +206,14 @@ def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
     default) or 128.  Returns ``(o, final_state)``.
     With ``check=True`` the call synchronises and raises on a device-side error.
     """
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
-    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
-    tensors = [q, k, v, g, beta] + [t for t in (initial_state, cu_seqlens, o, final_state)
-                                    if t is not None]
-    for t in tensors:
-        if not t.is_cuda:
-            raise ValueError("gdn_fwd: every tensor must be on a CUDA device")
-        if not t.is_contiguous():
-            raise ValueError("gdn_fwd: every tensor must be contiguous")
-    dcode = _dtype_code(q.dtype)
-    if k.dtype != q.dtype or v.dtype != q.dtype or beta.dtype != q.dtype:
-        raise TypeError("gdn_fwd: q, k, v and beta must share one storage dtype")
-    if g.dtype != torch.float32:
-        raise TypeError("gdn_fwd: g must be float32")
-    if k.shape != q.shape or v.shape[:3] != q.shape[:3] or g.shape != (B, T, H) or \
-            beta.shape != (B, T, H):
-        raise ValueError("gdn_fwd: shape mismatch among q, k, v, g, beta")
-    if initial_state is not None and (initial_state.dtype != torch.float32 or
-                                      initial_state.shape != (N, H, dk, dv)):
-        raise ValueError("gdn_fwd: initial_state must be float32 [N, H, dk, dv]")
-    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
-        raise TypeError("gdn_fwd: cu_seqlens must be int32")
+    N, H, dk, dv = _check_fwd_tensors("gdn_fwd", q, k, v, g, beta, initial_state, cu_seqlens,
+                                      o, final_state)
     if o is None:
         o = torch.empty_like(v)
-    elif o.shape != v.shape or o.dtype != v.dtype:
-        raise ValueError("gdn_fwd: o must match v in shape and dtype")
     if final_state is None and output_final_state:
         final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
-    if final_state is not None and (final_state.dtype != torch.float32 or
-                                    final_state.shape != (N, H, dk, dv)):
-        raise ValueError("gdn_fwd: final_state must be float32 [N, H, dk, dv]")
+    B, T = q.shape[:2]
+    dcode = _dtype_code(q.dtype)
     flags = (GDN_QK_L2NORM if qk_l2norm else 0) | (GDN_FORCE_SIMT if force_simt else 0)
     if workspace is None:
         workspace = new_workspace(N, H, dk, dv, flags, device=q.device)
@@ -227,9 +240,11 @@ def gdn_fwd_static_scratch(q, k, v, g, beta, initial_state, cu_seqlens, o, final
     ``check`` the call synchronises and returns the device status code; the
     status is returned, not raised, so the caller decides.
     """
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
-    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if o is None:
+        raise ValueError("gdn_fwd_static_scratch: o must be passed in (the call allocates nothing)")
+    N, H, dk, dv = _check_fwd_tensors("gdn_fwd_static_scratch", q, k, v, g, beta,
+                                      initial_state, cu_seqlens, o, final_state)
+    B, T = q.shape[:2]
     flags = (GDN_QK_L2NORM if qk_l2norm else 0) | (GDN_FORCE_SIMT if force_simt else 0)
     return int(lib().gdn_fwd_static_scratch(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens),

@@ -10,3 +10,15 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Print the parity margins of the full-size workloads (if any ran)."""
+    try:
+        import parity
+    except Exception:
+        return
+    if parity.MARGINS:
+        terminalreporter.write_sep("-", "parity margins of the full-size workloads")
+        for line in parity.MARGINS:
+            terminalreporter.write_line(line)

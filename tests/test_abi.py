@@ -199,3 +199,71 @@ def call_diag(L, **over):
 ])
 def test_diag_host_validation_rejects_before_launch(L, over, code):
     assert call_diag(L, **over) == code
+
+
+class _OnDevice:
+    """A CPU tensor that reports itself as a CUDA tensor, so that the
+    binding's tensor checks can be exercised on a machine without a GPU."""
+
+    is_cuda = True
+
+    def __init__(self, t):
+        self.t = t
+        self.dtype, self.shape = t.dtype, t.shape
+
+    def is_contiguous(self):
+        return self.t.is_contiguous()
+
+    def dim(self):
+        return self.t.dim()
+
+    def numel(self):
+        return self.t.numel()
+
+
+def _fwd_inputs(B=1, T=8, H=2, dk=32, dv=32):
+    import torch
+    bf = torch.bfloat16
+    mk = lambda *s, dt=bf: _OnDevice(torch.zeros(*s, dtype=dt))
+    return (mk(B, T, H, dk), mk(B, T, H, dk), mk(B, T, H, dv), mk(B, T, H, dt=torch.float32),
+            mk(B, T, H))
+
+
+@pytest.mark.parametrize("bad", ["o_shape", "o_dtype", "state_shape", "state_dtype", "o_cpu",
+                                 "o_missing"])
+def test_static_scratch_rejects_bad_outputs_before_the_library(monkeypatch, bad):
+    import torch
+    q, k, v, g, beta = _fwd_inputs()
+    o = _OnDevice(torch.zeros(1, 8, 2, 32, dtype=torch.bfloat16))
+    s = _OnDevice(torch.zeros(1, 2, 32, 32, dtype=torch.float32))
+    if bad == "o_shape":
+        o = _OnDevice(torch.zeros(1, 7, 2, 32, dtype=torch.bfloat16))
+    elif bad == "o_dtype":
+        o = _OnDevice(torch.zeros(1, 8, 2, 32, dtype=torch.float32))
+    elif bad == "state_shape":
+        s = _OnDevice(torch.zeros(1, 2, 32, 16, dtype=torch.float32))
+    elif bad == "state_dtype":
+        s = _OnDevice(torch.zeros(1, 2, 32, 32, dtype=torch.bfloat16))
+    elif bad == "o_cpu":
+        o = torch.zeros(1, 8, 2, 32, dtype=torch.bfloat16)
+    elif bad == "o_missing":
+        o = None
+
+    def no_library():
+        raise AssertionError("the library was called with malformed tensors")
+
+    monkeypatch.setattr(G, "lib", no_library)
+    with pytest.raises((ValueError, TypeError)):
+        G.gdn_fwd_static_scratch(q, k, v, g, beta, None, None, o, s)
+
+
+def test_static_scratch_entry_point_validates_before_enqueueing(L):
+    """Host-side rejections of the no-workspace entry point need no device:
+    a scratch need above the array's size, and zero sizes."""
+    vp, i32 = ctypes.c_void_p, ctypes.c_int32
+    fake = vp(1 << 40)
+    args = [fake] * 5 + [vp(None), vp(None), vp((1 << 40) + (1 << 30)), vp(None)]
+    # num_seqs = 0: no scratch size is defined
+    st = L.gdn_fwd_static_scratch(*args, i32(1), i32(8), i32(2), i32(32), i32(32), i32(0),
+                                  i32(64), ctypes.c_int(1), ctypes.c_uint32(0), i32(0), vp(0))
+    assert st == 1

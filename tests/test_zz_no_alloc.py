@@ -33,13 +33,25 @@ def test_static_scratch_matches_gdn_fwd_on_two_calls(dtype):
     # outputs are preallocated by the caller; the entry point allocates nothing
     o = torch.empty_like(o_ref)
     s = torch.empty_like(s_ref)
-    for call in range(2):
+    # a warm-up call, so that the allocator and the library's set-up are settled
+    assert G.gdn_fwd_static_scratch(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                    d["initial_state"], None, o, s, check=True) == 0
+    torch.cuda.synchronize()
+    for call in range(3):
         o.fill_(float("nan"))
         s.fill_(float("nan"))
+        torch.cuda.synchronize()
+        alloc0 = torch.cuda.memory_allocated()
+        free0 = torch.cuda.mem_get_info()[0]
+        # the last call does not check: it only enqueues, then the caller syncs
+        check = call < 2
         st = G.gdn_fwd_static_scratch(d["q"], d["k"], d["v"], d["g"], d["beta"],
-                                      d["initial_state"], None, o, s, check=True)
+                                      d["initial_state"], None, o, s, check=check)
         assert st == 0, f"call {call}: {G.status_string(st)}"
         torch.cuda.synchronize()
+        # no device memory was taken, by torch or by the library
+        assert torch.cuda.memory_allocated() == alloc0, f"call {call}: torch allocated"
+        assert torch.cuda.mem_get_info()[0] == free0, f"call {call}: device memory taken"
         assert parity.rel(o.double().cpu(), o_ref.double().cpu()) <= tol_o, f"call {call}: o"
         assert parity.rel(s.double().cpu(), s_ref.double().cpu()) <= tol_s, f"call {call}: state"
 
