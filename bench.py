@@ -354,6 +354,14 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
     host = W.generate(W.with_seed(w, w.seed + rank))
     N, tokens = host["N"], host["tokens"]
     names = ("q", "k", "v", "g", "beta")
+    fused = getattr(args, "fused", False)
+    if fused:  # the block parts fused into gdn_fwd: raw q/k, beta logits, skip and gate
+        ex = W.generate_block_extras(host, w.H, seed=w.seed + 1000 + rank, dtype=w.dtype)
+        host = dict(host, q=ex["q_raw"], k=ex["k_raw"], beta=ex["beta_logits"],
+                    D_skip=ex["D_skip"], out_gate=ex["out_gate"])
+        names = names + ("D_skip", "out_gate")
+    fkw = lambda d: dict(D_skip=d["D_skip"], out_gate=d["out_gate"], beta_logits=True,  # noqa: E731
+                         qk_l2norm=True) if fused else {}
     sets = []
     for _ in range(2):  # two resident input sets, alternated between steps
         d = {n: host[n].to(dev) for n in names}
@@ -363,7 +371,7 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
         d["final_state"] = torch.empty((N, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
         sets.append(d)
     ws = G.new_workspace(N, w.H, w.dk, w.dv, device=dev)
-    kname = G.gdn_fwd_kernel_name(w.dk, w.dv, host["q"].dtype)
+    kname = G.gdn_fwd_kernel_name(w.dk, w.dv, host["q"].dtype, G.GDN_QK_L2NORM if fused else 0)
     if args.chunk != CHUNK:   # other chunk sizes run on the fp32 CUDA-core kernel
         kname = "simt_" + ("fp32" if w.dtype == "fp32" else "bf16")
     stream = torch.cuda.current_stream(dev)
@@ -372,7 +380,7 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
         d = sets[i & 1]
         G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"],
                   d["cu_seqlens"], o=d["o"], final_state=d["final_state"], workspace=ws,
-                  chunk_size=args.chunk, stream=s)
+                  chunk_size=args.chunk, stream=s, **fkw(d))
 
     for i in range(args.warmup):
         step(i)
@@ -443,7 +451,7 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
             stream.wait_event(d2h_done[b])       # step i-2's result has been read back
         G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"],
                   d["cu_seqlens"], o=d["o"], final_state=d["final_state"], workspace=ws,
-                  chunk_size=args.chunk, stream=stream)
+                  chunk_size=args.chunk, stream=stream, **fkw(d))
         comp_done[b].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[b])
@@ -482,6 +490,8 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
 
     hbm_gbs, bf16_tflops, peak_src = measured_peaks()
     alg_bytes = algorithmic_bytes(w, tokens, N, host["initial_state"] is not None)
+    if fused:   # the fp32 output gate is read too (D_skip: H floats)
+        alg_bytes += tokens * w.H * 4 + w.H * 4
     alg_flops = algorithmic_flops(w, tokens)   # counted at the 64-token chunk
     achieved_gbs = alg_bytes / (per_launch_ms / 1e3) / 1e9
     achieved_tflops = alg_flops / (per_launch_ms / 1e3) / 1e12
@@ -497,6 +507,8 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
         "timing": TIMING_NOTE[args.eager],
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
                    "storage": w.dtype, "chunk": args.chunk, "kernel": kname,
+                   **({"fused": "q/k L2 norm + beta logits (sigmoid) + (o + D v) * out_gate "
+                                "epilogue in the kernel"} if fused else {}),
                    "l2": "two resident input sets of "
                          f"{sum(sets[0][n].numel() * sets[0][n].element_size() for n in names) / 1e6:.0f}"
                          " MB each (> 129 MB L2) alternate between steps",
@@ -1146,6 +1158,9 @@ def main(argv=None):
                     sorted(W.DIAG_WORKLOADS) + sorted(W.CONV_WORKLOADS))
     ap.add_argument("--eager", action="store_true",
                     help="time the steps launched one by one instead of as one CUDA graph")
+    ap.add_argument("--fused", action="store_true",
+                    help="fwd: raw q/k normalised in-kernel, beta as logits and the block "
+                         "epilogue (o + D v) * out_gate, all fused into gdn_fwd")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

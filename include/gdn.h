@@ -69,14 +69,23 @@ typedef enum gdn_dtype { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 
 /* Flags for gdn_fwd. */
 enum {
-  /* Normalise q_t and k_t in-kernel: x / sqrt(sum(x^2) + 1e-6), fp32. */
+  /* Normalise q_t and k_t in-kernel: x / sqrt(sum(x^2) + 1e-6), fp32 (the
+   * gated delta rule's q/k normalisation, part of the block's prologue).  The
+   * tensor-core kernels normalise the loaded bf16 tiles in shared memory and
+   * round the result back to bf16 before their products read it; the fp32
+   * kernel keeps it in fp32. */
   GDN_QK_L2NORM = 1u << 0,
   /* Use the fp32 CUDA-core kernel even for bf16 storage (the tensor-core
    * kernel is the default for bf16).  fp32 storage always uses it. */
   GDN_FORCE_SIMT = 1u << 1,
   /* gdn_diag_fwd only: g holds the gate's logits dt and the kernel uses
    * g = sigmoid(dt) ("Model Architecture Walkthrough", section 5.2.1). */
-  GDN_GATE_SIGMOID = 1u << 2
+  GDN_GATE_SIGMOID = 1u << 2,
+  /* gdn_fwd only: beta holds logits and the kernel uses beta_t =
+   * sigmoid(beta input) in fp32 (the write strength is a sigmoid of a
+   * projection in the gated delta rule block; the pages' block computes its
+   * gates the same way, "Model Architecture Walkthrough", section 5.4.3). */
+  GDN_BETA_LOGITS = 1u << 3
 };
 
 /* Bytes of device workspace gdn_fwd needs for these sizes (>= 256; the first
@@ -108,6 +117,19 @@ gdn_status gdn_workspace_init(void *workspace, size_t workspace_bytes, void *str
  *   cu_seqlens    [num_seqs + 1] int32 device, or NULL
  *   o             [batch, seq_len, num_heads, head_dim_v]    dtype     device (written)
  *   final_state   [num_seqs, num_heads, head_dim_k, head_dim_v] float32 device (written), or NULL
+ *   D_skip        [num_heads]                                float32   device, or NULL
+ *   out_gate      [batch, seq_len, num_heads]                float32   device, or NULL
+ *
+ * Block epilogue (optional, fused into the output store): the GDN block's
+ * skip connection and output gate ("Model Architecture Walkthrough", section
+ * 5.5, step 6, and section 5.6), with v the value input of the recurrence:
+ *
+ *     o_t <- (o_t + D_skip[h] v_t) * out_gate[t, h]
+ *
+ * A NULL D_skip reads as 0 and a NULL out_gate as 1; with both NULL o is the
+ * recurrence output itself.  out_gate is the per-(token, head) scalar the
+ * pages form by averaging sigmoid(g_proj x) over the head dimension (section
+ * 5.4.3); that projection stays with the caller.
  *
  * Sequences: with cu_seqlens == NULL the batch rows are the sequences and
  * num_seqs must equal batch.  With cu_seqlens != NULL, batch must be 1 and
@@ -122,9 +144,11 @@ gdn_status gdn_workspace_init(void *workspace, size_t workspace_bytes, void *str
  * included, and every final state is its initial state.
  *
  * Values: g_t is the natural log of the decay alpha_t (expected <= 0; not
- * clamped).  beta_t is used as given (expected in [0, 1]; not clamped).  The
- * state element (i, j) of H = S^T multiplies key dimension i and value
- * dimension j.
+ * clamped).  beta_t is used as given (expected in [0, 1]; not clamped), or
+ * with GDN_BETA_LOGITS as sigmoid(beta input).  The state element (i, j) of
+ * H = S^T multiplies key dimension i and value dimension j.
+ *
+ * flags: any of GDN_QK_L2NORM, GDN_BETA_LOGITS, GDN_FORCE_SIMT.
  *
  * Supported sizes: head_dim_k in {32, 64, 128}; head_dim_v a multiple of 32
  * in [32, 256]; num_heads >= 1; num_seqs in [1, 65535]; chunk_size in {32,
@@ -151,6 +175,7 @@ gdn_status gdn_workspace_init(void *workspace, size_t workspace_bytes, void *str
 gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
                    const void *beta, const float *initial_state,
                    const int32_t *cu_seqlens, void *o, float *final_state,
+                   const float *D_skip, const float *out_gate,
                    int32_t batch, int32_t seq_len, int32_t num_heads,
                    int32_t head_dim_k, int32_t head_dim_v, int32_t num_seqs,
                    int32_t chunk_size, gdn_dtype dtype, uint32_t flags,
@@ -192,7 +217,7 @@ gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
 gdn_status gdn_fwd_static_scratch(const void *q, const void *k, const void *v, const float *g,
                                   const void *beta, const float *initial_state,
                                   const int32_t *cu_seqlens, void *o, float *final_state,
-                                  int32_t batch, int32_t seq_len, int32_t num_heads,
+                                  const float *D_skip, const float *out_gate, int32_t batch, int32_t seq_len, int32_t num_heads,
                                   int32_t head_dim_k, int32_t head_dim_v, int32_t num_seqs,
                                   int32_t chunk_size, gdn_dtype dtype, uint32_t flags,
                                   int32_t check, void *stream);

@@ -21,10 +21,7 @@ bool supported_dk(int dk) { return dk == 32 || dk == 64 || dk == 128; }
 bool supported_dv(int dv) { return dv >= 32 && dv <= 256 && dv % 32 == 0; }
 
 bool use_tc(int dk, int dv, gdn_dtype dtype, uint32_t flags) {
-  // The tensor-core kernel multiplies the TMA-loaded q/k tiles as they arrive,
-  // so in-kernel q/k normalisation runs on the fp32 kernel.
-  return dtype == GDN_BF16 && !(flags & (GDN_FORCE_SIMT | GDN_QK_L2NORM)) &&
-         gdn::tc_supported(dk, dv);
+  return dtype == GDN_BF16 && !(flags & GDN_FORCE_SIMT) && gdn::tc_supported(dk, dv);
 }
 
 }  // namespace
@@ -49,7 +46,8 @@ namespace gdn {
 // work.  Fills `call` on success.
 gdn_status fwd_validate(const void *q, const void *k, const void *v, const float *g,
                         const void *beta, const float *initial_state,
-                        const int32_t *cu_seqlens, void *o, float *final_state, int32_t batch,
+                        const int32_t *cu_seqlens, void *o, float *final_state,
+                        const float *D_skip, const float *out_gate, int32_t batch,
                         int32_t seq_len, int32_t num_heads, int32_t head_dim_k,
                         int32_t head_dim_v, int32_t num_seqs, int32_t chunk_size,
                         gdn_dtype dtype, uint32_t flags, void *workspace,
@@ -59,7 +57,8 @@ gdn_status fwd_validate(const void *q, const void *k, const void *v, const float
       num_seqs <= 0)
     return GDN_ERR_INVALID_ARG;
   if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
-  if (flags & ~(uint32_t)(GDN_QK_L2NORM | GDN_FORCE_SIMT)) return GDN_ERR_INVALID_ARG;
+  if (flags & ~(uint32_t)(GDN_QK_L2NORM | GDN_FORCE_SIMT | GDN_BETA_LOGITS))
+    return GDN_ERR_INVALID_ARG;
   if (cu_seqlens ? batch != 1 : num_seqs != batch) return GDN_ERR_INVALID_ARG;
   if (!supported_dk(head_dim_k) || !supported_dv(head_dim_v)) return GDN_ERR_UNSUPPORTED;
   if (!simt_chunk_supported(chunk_size, head_dim_k)) return GDN_ERR_UNSUPPORTED;
@@ -83,7 +82,8 @@ gdn_status fwd_validate(const void *q, const void *k, const void *v, const float
 
   // ---- pointers ----
   if (!q || !k || !v || !g || !beta || !o) return GDN_ERR_INVALID_ARG;
-  const void *ptrs[] = {q, k, v, g, beta, initial_state, cu_seqlens, o, final_state};
+  const void *ptrs[] = {q, k, v, g, beta, initial_state, cu_seqlens, o, final_state, D_skip,
+                        out_gate};
   for (const void *ptr : ptrs)
     if (ptr && !aligned16(ptr)) return GDN_ERR_INVALID_ARG;
   if (!workspace) return GDN_ERR_WORKSPACE;
@@ -100,7 +100,9 @@ gdn_status fwd_validate(const void *q, const void *k, const void *v, const float
   const size_t b_cu = cu_seqlens ? (size_t)(num_seqs + 1) * 4 : 0;
   struct Range { const void *p; size_t n; };
   const Range inputs[] = {{q, b_qk}, {k, b_qk}, {v, b_v}, {g, b_g}, {beta, b_beta},
-                          {cu_seqlens, b_cu}, {workspace, workspace_bytes}};
+                          {cu_seqlens, b_cu}, {workspace, workspace_bytes},
+                          {D_skip, D_skip ? (size_t)num_heads * 4 : 0},
+                          {out_gate, out_gate ? b_g : 0}};
   for (const Range &r : inputs) {
     if (overlaps(o, b_v, r.p, r.n)) return GDN_ERR_INVALID_ARG;
     if (overlaps(final_state, b_state, r.p, r.n)) return GDN_ERR_INVALID_ARG;
@@ -115,6 +117,7 @@ gdn_status fwd_validate(const void *q, const void *k, const void *v, const float
   FwdParams &p = call->p;
   p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g;
   p.s0 = initial_state; p.cu = cu_seqlens; p.o = o; p.sN = final_state;
+  p.d_skip = D_skip; p.out_gate = out_gate;
   p.status = static_cast<DeviceStatus *>(workspace);
   p.ckpt = nullptr;
   p.seq_len = seq_len;
@@ -164,13 +167,14 @@ const char *gdn_fwd_kernel_name(int32_t head_dim_k, int32_t head_dim_v, gdn_dtyp
 
 gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
                    const void *beta, const float *initial_state, const int32_t *cu_seqlens,
-                   void *o, float *final_state, int32_t batch, int32_t seq_len,
+                   void *o, float *final_state, const float *D_skip, const float *out_gate,
+                   int32_t batch, int32_t seq_len,
                    int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
                    int32_t num_seqs, int32_t chunk_size, gdn_dtype dtype, uint32_t flags,
                    void *workspace, size_t workspace_bytes, void *stream) {
   gdn::FwdCall call;
   const gdn_status st = gdn::fwd_validate(q, k, v, g, beta, initial_state, cu_seqlens, o,
-                                          final_state, batch, seq_len, num_heads, head_dim_k,
+                                          final_state, D_skip, out_gate, batch, seq_len, num_heads, head_dim_k,
                                           head_dim_v, num_seqs, chunk_size, dtype, flags,
                                           workspace, workspace_bytes, &call);
   if (st != GDN_OK) return st;

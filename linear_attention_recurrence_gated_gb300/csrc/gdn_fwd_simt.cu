@@ -110,7 +110,7 @@ gdn_fwd_simt_kernel(const FwdParams p) {
       if (tid < rows) {
         const size_t off = (size_t)(start + c0 + tid) * H + h;
         gg = p.g[off];
-        bb = to_f32(beta[off]);
+        bb = beta_value(to_f32(beta[off]), p.flags);
       }
       sG[tid] = gg;
       sB[tid] = bb;
@@ -225,7 +225,11 @@ gdn_fwd_simt_kernel(const FwdParams p) {
         const float *pi = sA + i * L::A_LD;
         float acc = sO[i * DVT + c];
         for (int j = 0; j <= i; ++j) acc = fmaf(pi[j], sU[j * L::U_LD + c], acc);
-        store_out(o + ((size_t)(start + c0 + i) * H + h) * dv + col0 + c, acc);
+        const size_t orow = (size_t)(start + c0 + i) * H + h;
+        if (p.d_skip || p.out_gate)  // block epilogue (o + D_h v) * gate
+          acc = block_epilogue(acc, to_f32(v[orow * dv + col0 + c]), p.d_skip ? p.d_skip[h] : 0.f,
+                               p.out_gate ? p.out_gate[orow] : 1.f);
+        store_out(o + orow * dv + col0 + c, acc);
       }
     }
     const float gam_last = sGam[C - 1];

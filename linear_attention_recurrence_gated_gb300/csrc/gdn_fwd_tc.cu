@@ -65,7 +65,8 @@ struct TcLayout {
   static constexpr int QK_PAIR = 2 * SUB;
   static constexpr int OFF_V = (DK / 64) * QK_PAIR;
   static constexpr int OFF_GATE = OFF_V + SUB;
-  static constexpr int GATE = 2048;  // f32 [8][64]: G*log2e, gamma, decay-to-end, beta, E
+  // f32 [8][64]: G*log2e, gamma, decay-to-end, beta, E, output gate (kFEpi)
+  static constexpr int GATE = 2048;
   static constexpr int SLOT = OFF_GATE + GATE;
   static constexpr int STAGE = (DK / 64) * SUB + 2 * SUB;  // W, U~, P of one chunk
   static constexpr int OFF_IN = 0;
@@ -84,12 +85,26 @@ struct TcLayout {
   static constexpr int OFF_BAR = OFF_TMEM + 16;
   static constexpr int NBAR = 2 * NIN + 10;
   static constexpr int OFF_FLAG = OFF_BAR + NBAR * 8;
-  static constexpr int BYTES = OFF_FLAG + 16;
+  // kFL2 only: per input slot, fp32 vectors r_q [0,64), r_k [64,128),
+  // G - log2 r_k [128,192) and E r_k [192,256); then the two mbarriers that
+  // gather the drain threads' norms of a chunk
+  static constexpr int RN_SLOT = 4 * 64;
+  static constexpr int OFF_RN = OFF_FLAG + 16;
+  static constexpr int OFF_NBAR = OFF_RN + NIN * RN_SLOT * 4;
+  static constexpr int BYTES = OFF_NBAR + 16;
   static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024
   static_assert(SLOT % 1024 == 0 && STAGE % 1024 == 0, "tiles need 1024-byte alignment");
+  static_assert(ALLOC <= 232448, "shared memory budget");
 };
 
-template <int DK, int NIN>
+// Fused GDN block parts, as in the head_dim_k = 64 kernel: beta logits in
+// every instance; the mask kF selects the instance with the q/k L2
+// normalisation folded into fp32 row factors and column vectors (kFL2) and
+// the one with the output epilogue (kFEpi), so that the plain pass carries
+// none of their code.
+constexpr int kFL2 = 1, kFEpi = 2;
+
+template <int DK, int NIN, int kF>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gdn_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_k,
@@ -143,6 +158,10 @@ gdn_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_q,
       mbar_init(tmem_empty(s), kCarryThreads);
       mbar_init(s_ready(s), kCarryThreads);
     }
+    if constexpr ((kF & kFL2) != 0) {
+      mbar_init(sbase + L::OFF_NBAR, kCarryThreads);
+      mbar_init(sbase + L::OFF_NBAR + 8, kCarryThreads);
+    }
     *S.abort_flag = 0;
     fence_mbar_init();
   }
@@ -158,9 +177,10 @@ gdn_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_q,
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     const __nv_bfloat16 *betap = static_cast<const __nv_bfloat16 *>(p.beta);
-    float gv0 = 0.f, gv1 = 0.f, bv0 = 0.f, bv1 = 0.f;
+    float gv0 = 0.f, gv1 = 0.f, bv0 = 0.f, bv1 = 0.f, og0 = 1.f, og1 = 1.f;
     auto load_gates = [&](int c) {
       gv0 = gv1 = bv0 = bv1 = 0.f;
+      og0 = og1 = 1.f;
       const int64_t t0 = (int64_t)c * 64 + 2 * lane;
       if (c < nc && t0 < len) {
         const size_t off = (size_t)(start + t0) * H + h;
@@ -169,6 +189,16 @@ gdn_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_q,
         if (t0 + 1 < len) {
           gv1 = p.g[off + H];
           bv1 = __bfloat162float(betap[off + H]);
+        }
+        if constexpr ((kF & kFEpi) != 0) {
+          if (p.out_gate) {
+            og0 = p.out_gate[off];
+            og1 = t0 + 1 < len ? p.out_gate[off + H] : 1.f;
+          }
+        }
+        if (p.flags & GDN_BETA_LOGITS) {  // beta from logits (uniform branch, any instance)
+          bv0 = beta_value(bv0, p.flags);
+          bv1 = t0 + 1 < len ? beta_value(bv1, p.flags) : 0.f;
         }
       }
     };
@@ -204,6 +234,8 @@ gdn_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_q,
         *reinterpret_cast<float2 *>(gate + 256 + 2 * lane) =
             make_float2(ex2(Gb - G0), ex2(Gb - G1));
         if (lane == 0) sgc[slot] = ex2(Gl);
+        if constexpr ((kF & kFEpi) != 0)
+          *reinterpret_cast<float2 *>(gate + 320 + 2 * lane) = make_float2(og0, og1);
       }
       load_gates(c + 1);
       __syncwarp();
@@ -317,7 +349,9 @@ gdn_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_q,
           for (int r = k + 1; r < 16; ++r) x[r] = fmaf(-Ab[r * L::A_LD + k], xk, x[r]);
         }
         const float bj = beta[16 * w + l];
-        const float bgj = bj * gam[16 * w + l];
+        float bgj = bj * gam[16 * w + l];
+        if constexpr ((kF & kFL2) != 0)  // W = T diag(beta gamma r_k) K
+          bgj *= reinterpret_cast<const float *>(smem + L::OFF_RN)[slot * L::RN_SLOT + 64 + 16 * w + l];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
           sTf[(w * 16 + r) * L::TF_LD + l] = x[r];
@@ -489,7 +523,43 @@ gdn_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_q,
       const int ilim = isP ? i + 1 : i;  // P keeps j <= i, A keeps j < i
       const bool rowok = i < valid;
       const float Gi = G2[i];
-      const float bi = isP ? 1.f : beta[i];
+      float bi = isP ? 1.f : beta[i];
+      // column vectors: G_j and E_j, or under the normalisation G_j - log2 r_k_j
+      // and E_j r_k_j (the column factor r_k folded in)
+      const float *Gc = G2, *Ec = E;
+      if constexpr ((kF & kFL2) != 0) {
+        // this thread's row norm (q_i for P rows, k_i for A rows) from the
+        // tile, shared with the other drain threads
+        float *rn = reinterpret_cast<float *>(smem + L::OFF_RN) + slot * L::RN_SLOT;
+        const uint32_t tb = slot_base(slot) + (isP ? 0 : L::SUB);
+        float ss = 0.f;
+#pragma unroll
+        for (int q8 = 0; q8 < DK / 8; ++q8) {
+          uint32_t w[4];
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                       : "r"(qk_addr(tb, i, 8 * q8)));
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = bf16_lo(w[e]), hi = bf16_hi(w[e]);
+            ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+          }
+        }
+        const float rr = rsqrtf(ss + 1e-6f);
+        if (isP) {
+          rn[i] = rr;
+        } else {
+          rn[64 + i] = rr;
+          rn[128 + i] = Gi - __log2f(rr);
+          rn[192 + i] = E[i] * rr;
+        }
+        const uint32_t nb = sbase + L::OFF_NBAR + 8 * (cc & 1);
+        mbar_arrive(nb);
+        if (!__all_sync(0xffffffffu, role_wait(nb, (cc >> 1) & 1, S, p, n, h, 30))) return false;
+        bi *= rr;  // row factor: r_q (P) or beta_i r_k (A)
+        Gc = rn + 128;
+        Ec = rn + 192;
+      }
       float val[64];
       // Gamma_ij = 2^(G_i - G_j): a direct exponent for the 16-column blocks that
       // meet this warp's rows; for blocks entirely before them, two factors that
@@ -497,7 +567,7 @@ gdn_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_q,
       if ((cw & 1) == 0) {  // rows 0..31: columns 0..31
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 gg = *reinterpret_cast<const float4 *>(G2 + 4 * j4);
+          const float4 gg = *reinterpret_cast<const float4 *>(Gc + 4 * j4);
           const float gj[4] = {gg.x, gg.y, gg.z, gg.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -510,7 +580,7 @@ gdn_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_q,
         const float F0 = ex2(Gi - G2[15]) * bi, F1 = ex2(Gi - G2[31]) * bi;
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 ee = *reinterpret_cast<const float4 *>(E + 4 * j4);
+          const float4 ee = *reinterpret_cast<const float4 *>(Ec + 4 * j4);
           const float ej[4] = {ee.x, ee.y, ee.z, ee.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -521,7 +591,7 @@ gdn_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_q,
         }
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 gg = *reinterpret_cast<const float4 *>(G2 + 32 + 4 * j4);
+          const float4 gg = *reinterpret_cast<const float4 *>(Gc + 32 + 4 * j4);
           const float gj[4] = {gg.x, gg.y, gg.z, gg.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -638,7 +708,11 @@ gdn_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_q,
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         const int j0 = 16 * s + 2 * t, j1 = j0 + 8;
-        const float d00 = dec[j0], d01 = dec[j0 + 1], d10 = dec[j1], d11 = dec[j1 + 1];
+        float d00 = dec[j0], d01 = dec[j0 + 1], d10 = dec[j1], d11 = dec[j1 + 1];
+        if constexpr ((kF & kFL2) != 0) {  // Ud = diag(d r_k) U
+          const float *rk = reinterpret_cast<const float *>(smem + L::OFF_RN) + slot * L::RN_SLOT + 64;
+          d00 *= rk[j0]; d01 *= rk[j0 + 1]; d10 *= rk[j1]; d11 *= rk[j1 + 1];
+        }
         const float *u0 = uacc[2 * s], *u1 = uacc[2 * s + 1];
         ub[s][0] = pack_bf16(-u0[0], -u0[1]);
         ub[s][1] = pack_bf16(-u0[2], -u0[3]);
@@ -668,7 +742,12 @@ gdn_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_q,
       // O^T: scale the H-part by gamma_i, then add U^T P^T (lower-triangular blocks only)
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float ga = gam[8 * j + 2 * t], gb = gam[8 * j + 2 * t + 1];
+        float ga = gam[8 * j + 2 * t], gb = gam[8 * j + 2 * t + 1];
+        if constexpr ((kF & kFL2) != 0) {  // O = diag(gamma r_q) Q H + P U
+          const float *rq = reinterpret_cast<const float *>(smem + L::OFF_RN) + slot * L::RN_SLOT;
+          ga *= rq[8 * j + 2 * t];
+          gb *= rq[8 * j + 2 * t + 1];
+        }
         oacc[j][0] *= ga;
         oacc[j][1] *= gb;
         oacc[j][2] *= ga;
@@ -686,6 +765,30 @@ gdn_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_q,
             mma_bf16(oacc[2 * pp + 1], ub[s][0], ub[s][1], ub[s][2], ub[s][3], b2, b3);
           }
       GDN_PHASE(4);
+      if constexpr ((kF & kFEpi) != 0) {
+        // block epilogue (o + D_h v) * gate, with v from this chunk's V tile:
+        // ldmatrix.trans hands each thread v at (token 8j + 2t, +1; column
+        // 16cw + g, +8), the accumulator's own layout
+        const uint32_t Vs = slot_base(slot) + L::OFF_V;
+        const float dh = p.d_skip ? p.d_skip[h] : 0.f;
+        const float *ogate = gate_ptr(slot) + 320;  // staged by the producer
+#pragma unroll
+        for (int jp = 0; jp < 4; ++jp) {
+          uint32_t vb[4];
+          ldsm_x4_t(tile_addr(Vs, 16 * jp + 8 * (lmi >> 1) + lrow, 16 * cw + 8 * (lmi & 1)), vb[0],
+                    vb[1], vb[2], vb[3]);
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            const int j = 2 * jp + jj;
+            const float2 og = *reinterpret_cast<const float2 *>(ogate + 8 * j + 2 * t);
+            const uint32_t lo = vb[2 * jj], hi = vb[2 * jj + 1];  // columns g and g + 8
+            oacc[j][0] = block_epilogue(oacc[j][0], bf16_lo(lo), dh, og.x);
+            oacc[j][1] = block_epilogue(oacc[j][1], bf16_hi(lo), dh, og.y);
+            oacc[j][2] = block_epilogue(oacc[j][2], bf16_lo(hi), dh, og.x);
+            oacc[j][3] = block_epilogue(oacc[j][3], bf16_hi(hi), dh, og.y);
+          }
+        }
+      }
       // this chunk's input slot is no longer read (its stage is reused by this
       // warp group's own epilogue of chunk c+2, after the barrier below)
       mbar_arrive(empty_in(slot));
@@ -763,7 +866,12 @@ cudaError_t launch_tc(const FwdParams &p, cudaStream_t stream) {
       !make_tmap(&tv, p.v, p.dv, p.num_heads, tokens) ||
       !make_tmap(&to, p.o, p.dv, p.num_heads, tokens))
     return cudaErrorInvalidValue;
-  auto kern = gdn_fwd_tc_kernel<DK, NIN>;
+  // the block parts fused into the pass run in their own instantiation
+  const int feat = ((p.flags & GDN_QK_L2NORM) ? kFL2 : 0) | ((p.d_skip || p.out_gate) ? kFEpi : 0);
+  auto kern = feat == 0        ? gdn_fwd_tc_kernel<DK, NIN, 0>
+              : feat == kFL2   ? gdn_fwd_tc_kernel<DK, NIN, kFL2>
+              : feat == kFEpi  ? gdn_fwd_tc_kernel<DK, NIN, kFEpi>
+                               : gdn_fwd_tc_kernel<DK, NIN, kFL2 | kFEpi>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (err != cudaSuccess) return err;

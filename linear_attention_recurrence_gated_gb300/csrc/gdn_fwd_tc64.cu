@@ -45,6 +45,22 @@
 //                  per warp, the state in registers; warp 6 then issues the next MMA1
 //   warps 14,15    output (E2b): each thread stores its row of O
 // Every wait is bounded; a timeout records GDN_ERR_TIMEOUT and ends the loops.
+//
+// GDN block parts that gdn_fwd can fuse into the pass.  Beta given as logits
+// (a sigmoid in the producer, behind a uniform branch) is in every instance.
+// The other two have instances of their own, selected by the mask kF, so that
+// the plain pass carries none of their code:
+//   kFL2   the q/k L2 normalisation, folded into fp32 scalars so that the
+//          tensor cores still read the stored bf16 q and k.  With r_q = 1/|q_i|
+//          and r_k = 1/|k_j| (|x| = sqrt(sum x^2 + 1e-6)), P_ij and A_ij take
+//          the row factor r_q (P) or beta_i r_k (A) and the column factor r_k,
+//          the latter through the column vectors G_j - log2 r_k_j and
+//          E_j r_k_j that the drains read in place of G and E; W = T
+//          diag(beta gamma r_k) K; Ud = diag(d r_k) U; O = diag(gamma r_q) Q H
+//          + P U.  The drain threads compute the norms of their own rows of
+//          the tiles as soon as the inputs land.
+//   kFEpi  the output epilogue (o + D_h v) * gate; the producer stages the
+//          per-token gate beside the other gate vectors.
 #include "gdn_tc_common.cuh"
 
 namespace gdn {
@@ -107,7 +123,13 @@ struct L64 {
   static constexpr int OFF_BAR = OFF_TMEM + 16;
   static constexpr int NBAR = 32;
   static constexpr int OFF_FLAG = OFF_BAR + NBAR * 8;
-  static constexpr int BYTES = OFF_FLAG + 16;
+  // fused instances only: per input slot, fp32 vectors r_q [0,64), r_k
+  // [64,128), the output gate [128,192), G - log2 r_k [192,256) and E r_k
+  // [256,320); then the two mbarriers that gather the drain threads' norms
+  static constexpr int RN_SLOT = 5 * 64;
+  static constexpr int OFF_RN = OFF_FLAG + 16;
+  static constexpr int OFF_NBAR = OFF_RN + NIN * RN_SLOT * 4;
+  static constexpr int BYTES = OFF_NBAR + 16;
   static constexpr int ALLOC = BYTES + 1024;
   static_assert(SLOT % 1024 == 0 && OFF_H % 1024 == 0 && OFF_P % 1024 == 0,
                 "alignment");
@@ -175,10 +197,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint64_t v) {
 // block's last token); the two blocks that meet the rows take one exponent
 // per element.  One shared (not inlined) copy keeps the instruction footprint
 // small.
-__device__ __noinline__ void drain_s_row(uint32_t taddr, const float *G2, const float *E, int i,
-                                         int half, bool isP, float bi, int ilim, bool rowok,
-                                         uint32_t Ps, float *Ablk, uint8_t *smem,
-                                         uint32_t sbase) {
+// The column factors come from Gc (in place of G_j) and Ec (in place of E_j),
+// which carry a column scale when the q/k normalisation is folded in; the row
+// factor comes in through bi.
+__device__ __noinline__ void drain_s_row(uint32_t taddr, const float *G2, const float *Gc,
+                                         const float *Ec, int i, int half, bool isP, float bi,
+                                         int ilim, bool rowok, uint32_t Ps, float *Ablk,
+                                         uint8_t *smem, uint32_t sbase) {
   const float Gi = G2[i];
   // |beta_i| folded into the exponent (log2 0 = -inf gives 0; a negative beta
   // flips the sign afterwards), rows past the end of the sequence by an empty
@@ -200,7 +225,7 @@ __device__ __noinline__ void drain_s_row(uint32_t taddr, const float *G2, const 
       const bool before = cb < 2 * half;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const float4 x = *reinterpret_cast<const float4 *>((before ? E : G2) + 16 * cb + 4 * q);
+        const float4 x = *reinterpret_cast<const float4 *>((before ? Ec : Gc) + 16 * cb + 4 * q);
         f[4 * q] = x.x;
         f[4 * q + 1] = x.y;
         f[4 * q + 2] = x.z;
@@ -241,6 +266,9 @@ __device__ __noinline__ void drain_s_row(uint32_t taddr, const float *G2, const 
   }
 }
 
+constexpr int kFL2 = 1, kFEpi = 2;
+
+template <int kF>
 __global__ void __launch_bounds__(kThreads64, 1)
 gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_q,
                     const __grid_constant__ CUtensorMap tmap_k,
@@ -298,6 +326,10 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
     mbar_init(bar(B_U_READY), 128);
     for (int s = 0; s < 3; ++s) mbar_init(bar(B_P_FREE + s), 1);
     mbar_init(bar(B_DH_FULL), 1);
+    if constexpr ((kF & kFL2) != 0) {
+      mbar_init(sbase + L::OFF_NBAR, 128);
+      mbar_init(sbase + L::OFF_NBAR + 8, 128);
+    }
     *S.abort_flag = 0;
     fence_mbar_init();
   }
@@ -318,9 +350,10 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
     const __nv_bfloat16 *betap = static_cast<const __nv_bfloat16 *>(p.beta);
-    float gv0 = 0.f, gv1 = 0.f, bv0 = 0.f, bv1 = 0.f;
+    float gv0 = 0.f, gv1 = 0.f, bv0 = 0.f, bv1 = 0.f, og0 = 1.f, og1 = 1.f;
     auto load_gates = [&](int c) {
       gv0 = gv1 = bv0 = bv1 = 0.f;
+      og0 = og1 = 1.f;
       const int64_t t0 = (int64_t)c * 64 + 2 * lane;
       if (c < nc && t0 < len) {
         const size_t off = (size_t)(start + t0) * H + h;
@@ -329,6 +362,16 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
         if (t0 + 1 < len) {
           gv1 = p.g[off + H];
           bv1 = __bfloat162float(betap[off + H]);
+        }
+        if constexpr ((kF & kFEpi) != 0) {
+          if (p.out_gate) {
+            og0 = p.out_gate[off];
+            og1 = t0 + 1 < len ? p.out_gate[off + H] : 1.f;
+          }
+        }
+        if (p.flags & GDN_BETA_LOGITS) {  // beta from logits (uniform branch, any instance)
+          bv0 = beta_value(bv0, p.flags);
+          bv1 = t0 + 1 < len ? beta_value(bv1, p.flags) : 0.f;
         }
       }
     };
@@ -354,6 +397,7 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
       const float2 vE = make_float2(ex2(Gb - G0), ex2(Gb - G1));
       const float2 vB = make_float2(bv0, bv1);
       const float gC = ex2(Gl);
+      const float2 vO = make_float2(og0, og1);
       load_gates(c + 1);
       GDN_PHASE(0);
       bool ok = true;
@@ -367,6 +411,9 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
         *reinterpret_cast<float2 *>(gate + 128 + 2 * lane) = vB;
         *reinterpret_cast<float2 *>(gate + 192 + 2 * lane) = vE;
         if (lane == 0) sgc[slot] = gC;
+        if constexpr ((kF & kFEpi) != 0)
+          *reinterpret_cast<float2 *>(reinterpret_cast<float *>(smem + L::OFF_RN) +
+                                      slot * L::RN_SLOT + 128 + 2 * lane) = vO;
       }
       __syncwarp();
       if (lane == 0) {
@@ -400,25 +447,63 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
     for (int c = 0; c < nc; ++c) {
       const int slot = c % NIN, buf = c & 1;
       GDN_PHASE(8);
-      bool ok = role_wait(bar(B_TMEM_FULL + buf), (c >> 1) & 1, S, p, n, h, 7);
-      if (ok) ok = role_wait(bar(B_FULL_IN + slot), (c / NIN) & 1, S, p, n, h, 8);
+      constexpr bool l2 = (kF & kFL2) != 0;
+      const float *gate = gate_ptr(slot);
+      const float *G2 = gate, *beta = gate + 128, *E = gate + 192;
+      float *rn = reinterpret_cast<float *>(smem + L::OFF_RN) + slot * L::RN_SLOT;
+      bool ok = true;
+      float r = 1.f;
+      if constexpr (l2) {
+        // This thread's row norm, q_i (P rows) or k_i (A rows), from the input
+        // tile as soon as it lands; it is published before the accumulator and
+        // buffer waits, so the P drains (which need every r_k as a column
+        // factor) do not wait on the A drains' buffer.
+        ok = role_wait(bar(B_FULL_IN + slot), (c / NIN) & 1, S, p, n, h, 8);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const uint32_t tb = slot_base(slot) + (isP ? L::SQ : L::SK);
+        float ss = 0.f;
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+          const uint4 x = S4(tile_addr(tb, i, 8 * q8));
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = bf16_lo(w[e]), hi = bf16_hi(w[e]);
+            ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+          }
+        }
+        r = rsqrtf(ss + 1e-6f);
+        if (isP) {
+          rn[i] = r;
+        } else {
+          rn[64 + i] = r;
+          rn[192 + i] = G2[i] - __log2f(r);  // column j: 2^(G_i - G_j) r_k_j
+          rn[256 + i] = E[i] * r;
+        }
+        mbar_arrive(sbase + L::OFF_NBAR + 8 * (c & 1));
+        ok = role_wait(bar(B_TMEM_FULL + buf), (c >> 1) & 1, S, p, n, h, 7);
+      } else {
+        ok = role_wait(bar(B_TMEM_FULL + buf), (c >> 1) & 1, S, p, n, h, 7);
+        if (ok) ok = role_wait(bar(B_FULL_IN + slot), (c / NIN) & 1, S, p, n, h, 8);
+      }
       // the P buffer was last read by MMA2 of chunk c-3; the A buffer by the
       // inverse and couplings of chunk c-2
       if (ok && isP && c >= 3)
         ok = role_wait(bar(B_P_FREE + c % 3), ((c / 3) - 1) & 1, S, p, n, h, 10);
       if (ok && !isP && c >= 2)
         ok = role_wait(bar(B_A_FREE + buf), ((c - 2) >> 1) & 1, S, p, n, h, 21);
+      if constexpr (l2)
+        if (ok) ok = role_wait(sbase + L::OFF_NBAR + 8 * (c & 1), (c >> 1) & 1, S, p, n, h, 30);
       GDN_PHASE(9);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const int valid = valid_rows(c);
-      const float *gate = gate_ptr(slot);
-      const float *G2 = gate, *beta = gate + 128, *E = gate + 192;
       const int ilim = isP ? i + 1 : i;  // P keeps j <= i, A keeps j < i
-      const float bi = isP ? 1.f : beta[i];
+      // row factor: 1, or r_q (P) / beta_i r_k (A) under the normalisation
+      const float bi = (isP ? 1.f : beta[i]) * r;
       float *Ablk = reinterpret_cast<float *>(smem + L::OFF_A) + buf * L::A_BUF;
-      drain_s_row(tq + kColS + buf * 64, G2, E, i, wq & 1, isP, bi, ilim, i < valid,
-                  p_base(c % 3), Ablk, smem, sbase);
+      drain_s_row(tq + kColS + buf * 64, G2, l2 ? rn + 192 : G2, l2 ? rn + 256 : E, i, wq & 1,
+                  isP, bi, ilim, i < valid, p_base(c % 3), Ablk, smem, sbase);
       tc_fence_before();
       mbar_arrive(bar(B_TMEM_EMPTY + buf));
       if (isP) fence_proxy_async_smem();  // P is read by MMA2 (async proxy)
@@ -529,7 +614,9 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
           *reinterpret_cast<float4 *>(tcol + 4 * q) =
               make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
         const float bj = beta[16 * blk + l];
-        const float bgj = bj * ex2(G2[16 * blk + l]);  // beta_j gamma_j
+        float bgj = bj * ex2(G2[16 * blk + l]);  // beta_j gamma_j
+        if constexpr ((kF & kFL2) != 0)  // times r_k_j: W = T diag(beta gamma r_k) K
+          bgj *= reinterpret_cast<const float *>(smem + L::OFF_RN)[slot * L::RN_SLOT + 64 + 16 * blk + l];
         uint32_t wg[8], wb[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -703,7 +790,9 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
         if (warp == kWarpE1Issue && lane == 0 && c >= 2)
           pu_free = mbar_test(bar(B_PU_FREE + buf), ((c >> 1) - 1) & 1);
         const uint32_t Ut = slot_base(slot) + L::SV;  // U~ (written over V by prep)
-        const float dj = gate[64 + row];
+        float dj = gate[64 + row];
+        if constexpr ((kF & kFL2) != 0)  // Ud = diag(d r_k) U
+          dj *= reinterpret_cast<const float *>(smem + L::OFF_RN)[slot * L::RN_SLOT + 64 + row];
         const uint64_t dj2 = pk2(dj, dj);
         {
           uint32_t w[32];
@@ -776,22 +865,36 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
         mbar_wait_bounded(bar(B_PU_FULL + ((done - 1) & 1)), ((done - 1) >> 1) & 1, kWaitTimeoutNs);
     } else if (warp == 14 || warp == 15) {
       // ---- output (warps 14,15) ----
+      constexpr bool epi = (kF & kFEpi) != 0;  // the block epilogue (o + D_h v) * gate
+      float dh = 0.f;
+      if constexpr (epi)
+        if (p.d_skip) dh = p.d_skip[h];
       for (int c = 0; c < nc; ++c) {
         const int slot = c % NIN, buf = c & 1;
         const int valid = valid_rows(c);
         const float *gate = gate_ptr(slot);
         // ---- E2b: O = diag(gamma) (Q H) + P U (row = token); each thread
         // stores its own 128-byte row of O ----
+        const size_t orow_idx = (size_t)(start + (int64_t)c * 64 + row) * H + h;
+        const __nv_bfloat16 *vrow = static_cast<const __nv_bfloat16 *>(p.v) + orow_idx * dv + col0;
+        if (epi && row < valid) {  // v is reloaded (its tile now holds U~)
+          prefetch_l1(vrow);
+          prefetch_l1(vrow + 63);
+        }
         GDN_PHASE(0);
         bool ok = role_wait(bar(B_PU_FULL + buf), (c >> 1) & 1, S, p, n, h, 13);
         if (!__all_sync(0xffffffffu, ok)) break;
         GDN_PHASE(1);
         tc_fence_after();
         {
-          const float gi = ex2(gate[row]);  // gamma_i
+          float gi = ex2(gate[row]);  // gamma_i
+          __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) + orow_idx * dv + col0;
+          // gamma_i r_q_i under the normalisation; the output gate staged by the producer
+          const float *rn = reinterpret_cast<const float *>(smem + L::OFF_RN) + slot * L::RN_SLOT;
+          float og = 1.f;
+          if constexpr ((kF & kFL2) != 0) gi *= rn[row];
+          if constexpr (epi) og = rn[128 + row];
           const uint64_t gi2 = pk2(gi, gi);
-          __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) +
-                                ((size_t)(start + (int64_t)c * 64 + row) * H + h) * dv + col0;
 #pragma unroll 1
           for (int q2 = 0; q2 < 4; ++q2) {
             uint32_t a[16], b[16];
@@ -803,6 +906,21 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
             for (int e = 0; e < 8; ++e)
               w8[e] = pack_bf16x2(fma2(gi2, pk2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1])),
                                        pk2(__uint_as_float(b[2 * e]), __uint_as_float(b[2 * e + 1]))));
+            if constexpr (epi) {
+              if (row < valid) {
+                const uint4 v0 = reinterpret_cast<const uint4 *>(vrow + 16 * q2)[0];
+                const uint4 v1 = reinterpret_cast<const uint4 *>(vrow + 16 * q2)[1];
+                const uint32_t vw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const float o0 = fmaf(gi, __uint_as_float(a[2 * e]), __uint_as_float(b[2 * e]));
+                  const float o1 =
+                      fmaf(gi, __uint_as_float(a[2 * e + 1]), __uint_as_float(b[2 * e + 1]));
+                  w8[e] = pack_bf16(block_epilogue(o0, bf16_lo(vw[e]), dh, og),
+                                    block_epilogue(o1, bf16_hi(vw[e]), dh, og));
+                }
+              }
+            }
             if (row < valid) {
               reinterpret_cast<uint4 *>(orow + 16 * q2)[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
               reinterpret_cast<uint4 *>(orow + 16 * q2)[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
@@ -924,11 +1042,18 @@ cudaError_t launch_fwd_tc64(const FwdParams &p, cudaStream_t stream) {
       !make_tmap(&tk, p.k, DK, p.num_heads, tokens) ||
       !make_tmap(&tv, p.v, p.dv, p.num_heads, tokens))
     return cudaErrorInvalidValue;
-  cudaError_t err = cudaFuncSetAttribute(gdn_fwd_tc64_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+  // the block parts fused into the pass run in their own instantiation, so
+  // the plain pass carries none of their code
+  const int feat = ((p.flags & GDN_QK_L2NORM) ? kFL2 : 0) | ((p.d_skip || p.out_gate) ? kFEpi : 0);
+  auto kern = feat == 0             ? gdn_fwd_tc64_kernel<0>
+              : feat == kFL2        ? gdn_fwd_tc64_kernel<kFL2>
+              : feat == kFEpi       ? gdn_fwd_tc64_kernel<kFEpi>
+                                    : gdn_fwd_tc64_kernel<kFL2 | kFEpi>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (err != cudaSuccess) return err;
   const dim3 grid(p.dv / kDvt, p.num_heads, p.num_seqs);
-  gdn_fwd_tc64_kernel<<<grid, kThreads64, L::ALLOC, stream>>>(p, tq, tk, tv);
+  kern<<<grid, kThreads64, L::ALLOC, stream>>>(p, tq, tk, tv);
   return cudaGetLastError();
 }
 

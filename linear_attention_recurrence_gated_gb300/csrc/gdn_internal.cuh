@@ -30,6 +30,8 @@ struct FwdParams {
   const int32_t *cu;
   void *o;
   float *sN;
+  const float *d_skip;    // [H] skip weights of the block epilogue, or NULL (0)
+  const float *out_gate;  // [tokens][H] output gate of the block epilogue, or NULL (1)
   DeviceStatus *status;
   float *ckpt;          // backward only: state at every 64-token chunk start (else NULL)
   int64_t seq_len;      // tokens per batch row (dense) or packed total (varlen)
@@ -81,6 +83,16 @@ __device__ __forceinline__ void pass_state_through(const FwdParams &p, int n, in
   }
 }
 
+// The block epilogue (o + D_h v) * gate of one output element (a NULL skip
+// reads as 0, a NULL gate as 1).
+__device__ __forceinline__ float block_epilogue(float o, float v, float d_h, float gate) {
+  return (o + d_h * v) * gate;
+}
+// beta as stored, or sigmoid of it when the caller passes logits
+__device__ __forceinline__ float beta_value(float b, uint32_t flags) {
+  return (flags & GDN_BETA_LOGITS) ? 1.f / (1.f + expf(-b)) : b;
+}
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ void store_out(float *p, float x) { *p = x; }
@@ -110,7 +122,8 @@ struct FwdCall {
 // aliasing); returns GDN_OK and fills `call`, or the error and enqueues nothing.
 gdn_status fwd_validate(const void *q, const void *k, const void *v, const float *g,
                         const void *beta, const float *initial_state,
-                        const int32_t *cu_seqlens, void *o, float *final_state, int32_t batch,
+                        const int32_t *cu_seqlens, void *o, float *final_state,
+                        const float *D_skip, const float *out_gate, int32_t batch,
                         int32_t seq_len, int32_t num_heads, int32_t head_dim_k,
                         int32_t head_dim_v, int32_t num_seqs, int32_t chunk_size,
                         gdn_dtype dtype, uint32_t flags, void *workspace,

@@ -75,6 +75,11 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int 
 }
 
 // Prefetch a 3-D tile into L2 (no shared-memory destination, no completion).
+// Hint: bring the 128-byte line holding addr into L1 (no register is written).
+__device__ __forceinline__ void prefetch_l1(const void *addr) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(addr));
+}
+
 __device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int x, int y, int z) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
                    reinterpret_cast<uint64_t>(tmap)),

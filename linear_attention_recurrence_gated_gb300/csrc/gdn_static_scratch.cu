@@ -48,8 +48,8 @@ gdn_status scratch_address(cudaStream_t s, void **out) {
 extern "C" gdn_status gdn_fwd_static_scratch(
     const void *q, const void *k, const void *v, const float *g, const void *beta,
     const float *initial_state, const int32_t *cu_seqlens, void *o, float *final_state,
-    int32_t batch, int32_t seq_len, int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
-    int32_t num_seqs, int32_t chunk_size, gdn_dtype dtype, uint32_t flags, int32_t check,
+    const float *D_skip, const float *out_gate, int32_t batch, int32_t seq_len,
+    int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v, int32_t num_seqs, int32_t chunk_size, gdn_dtype dtype, uint32_t flags, int32_t check,
     void *stream) {
   const size_t need =
       gdn_fwd_workspace_size(num_seqs, num_heads, head_dim_k, head_dim_v, flags);
@@ -63,9 +63,9 @@ extern "C" gdn_status gdn_fwd_static_scratch(
 
   // every host-side check of gdn_fwd runs before anything is enqueued
   gdn::FwdCall call;
-  st = gdn::fwd_validate(q, k, v, g, beta, initial_state, cu_seqlens, o, final_state, batch,
-                         seq_len, num_heads, head_dim_k, head_dim_v, num_seqs, chunk_size,
-                         dtype, flags, scratch, kStaticScratchBytes, &call);
+  st = gdn::fwd_validate(q, k, v, g, beta, initial_state, cu_seqlens, o, final_state, D_skip,
+                         out_gate, batch, seq_len, num_heads, head_dim_k, head_dim_v, num_seqs,
+                         chunk_size, dtype, flags, scratch, kStaticScratchBytes, &call);
   if (st != GDN_OK) return st;
 
   // The array keeps the previous call's contents: the status must start at zero.

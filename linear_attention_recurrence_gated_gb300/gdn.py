@@ -25,6 +25,7 @@ GDN_F32, GDN_BF16 = 0, 1
 GDN_QK_L2NORM = 1 << 0
 GDN_FORCE_SIMT = 1 << 1
 GDN_GATE_SIGMOID = 1 << 2
+GDN_BETA_LOGITS = 1 << 3
 CHUNK_SIZE = 64
 
 # Every symbol include/gdn.h declares.
@@ -61,7 +62,7 @@ def lib() -> ctypes.CDLL:
             L.gdn_workspace_init.restype = ctypes.c_int
             L.gdn_workspace_init.argtypes = [vp, sz, vp]
             L.gdn_fwd.restype = ctypes.c_int
-            L.gdn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
+            L.gdn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                   i32, i32, i32, i32, i32, i32, i32, ctypes.c_int, u32,
                                   vp, sz, vp]
             L.gdn_check.restype = ctypes.c_int
@@ -73,7 +74,7 @@ def lib() -> ctypes.CDLL:
             L.gdn_fwd_kernel_name.restype = ctypes.c_char_p
             L.gdn_fwd_kernel_name.argtypes = [i32, i32, ctypes.c_int, u32]
             L.gdn_fwd_static_scratch.restype = ctypes.c_int
-            L.gdn_fwd_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
+            L.gdn_fwd_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                  i32, i32, i32, i32, i32, i32, i32,
                                                  ctypes.c_int, u32, i32, vp]
             L.gdn_decode.restype = ctypes.c_int
@@ -155,7 +156,8 @@ def gdn_fwd_kernel_name(head_dim_k, head_dim_v, dtype: torch.dtype, flags: int =
     return None if r is None else r.decode()
 
 
-def _check_fwd_tensors(where, q, k, v, g, beta, initial_state, cu_seqlens, o, final_state):
+def _check_fwd_tensors(where, q, k, v, g, beta, initial_state, cu_seqlens, o, final_state,
+                       D_skip=None, out_gate=None):
     """The tensor checks every forward entry point makes before it calls the
     library: device, contiguity, dtypes and shapes of inputs and of any output
     passed in.  Returns (N, H, dk, dv)."""
@@ -164,8 +166,8 @@ def _check_fwd_tensors(where, q, k, v, g, beta, initial_state, cu_seqlens, o, fi
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     N = B if cu_seqlens is None else cu_seqlens.numel() - 1
-    tensors = [q, k, v, g, beta] + [t for t in (initial_state, cu_seqlens, o, final_state)
-                                    if t is not None]
+    tensors = [q, k, v, g, beta] + [t for t in (initial_state, cu_seqlens, o, final_state,
+                                                D_skip, out_gate) if t is not None]
     for t in tensors:
         if not t.is_cuda:
             raise ValueError(f"{where}: every tensor must be on a CUDA device")
@@ -189,12 +191,17 @@ def _check_fwd_tensors(where, q, k, v, g, beta, initial_state, cu_seqlens, o, fi
     if final_state is not None and (final_state.dtype != torch.float32 or
                                     final_state.shape != (N, H, dk, dv)):
         raise ValueError(f"{where}: final_state must be float32 [N, H, dk, dv]")
+    if D_skip is not None and (D_skip.dtype != torch.float32 or tuple(D_skip.shape) != (H,)):
+        raise ValueError(f"{where}: D_skip must be float32 [H]")
+    if out_gate is not None and (out_gate.dtype != torch.float32 or out_gate.shape != (B, T, H)):
+        raise ValueError(f"{where}: out_gate must be float32 [B, T, H]")
     return N, H, dk, dv
 
 
 def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
-            final_state=None, output_final_state=True, workspace=None,
-            qk_l2norm=False, force_simt=False, chunk_size=CHUNK_SIZE, stream=None, check=False):
+            final_state=None, output_final_state=True, workspace=None, D_skip=None,
+            out_gate=None, qk_l2norm=False, beta_logits=False, force_simt=False,
+            chunk_size=CHUNK_SIZE, stream=None, check=False):
     """Forward pass of the gated delta rule through the C ABI.
 
     q, k ``[B, T, H, dk]``; v ``[B, T, H, dv]``; g ``[B, T, H]`` fp32; beta
@@ -204,22 +211,26 @@ def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
     ``o`` / ``final_state`` may be given to write into preallocated outputs
     (``final_state`` may be ``initial_state``).  ``chunk_size`` is 32, 64 (the
     default) or 128.  Returns ``(o, final_state)``.
+    ``D_skip`` ``[H]`` and ``out_gate`` ``[B, T, H]`` (fp32, optional) fuse the
+    block epilogue o <- (o + D_skip[h] v) * out_gate; ``beta_logits`` makes the
+    kernel use sigmoid(beta); ``qk_l2norm`` normalises q and k in-kernel.
     With ``check=True`` the call synchronises and raises on a device-side error.
     """
     N, H, dk, dv = _check_fwd_tensors("gdn_fwd", q, k, v, g, beta, initial_state, cu_seqlens,
-                                      o, final_state)
+                                      o, final_state, D_skip, out_gate)
     if o is None:
         o = torch.empty_like(v)
     if final_state is None and output_final_state:
         final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
     B, T = q.shape[:2]
     dcode = _dtype_code(q.dtype)
-    flags = (GDN_QK_L2NORM if qk_l2norm else 0) | (GDN_FORCE_SIMT if force_simt else 0)
+    flags = (GDN_QK_L2NORM if qk_l2norm else 0) | (GDN_FORCE_SIMT if force_simt else 0) | \
+        (GDN_BETA_LOGITS if beta_logits else 0)
     if workspace is None:
         workspace = new_workspace(N, H, dk, dv, flags, device=q.device)
     st = lib().gdn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
-                       _ptr(cu_seqlens), _ptr(o), _ptr(final_state), B, T, H, dk, dv, N,
-                       chunk_size, dcode, flags, _ptr(workspace),
+                       _ptr(cu_seqlens), _ptr(o), _ptr(final_state), _ptr(D_skip),
+                       _ptr(out_gate), B, T, H, dk, dv, N, chunk_size, dcode, flags, _ptr(workspace),
                        workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_fwd")
@@ -231,7 +242,8 @@ def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
 
 
 def gdn_fwd_static_scratch(q, k, v, g, beta, initial_state, cu_seqlens, o, final_state, *,
-                           qk_l2norm=False, force_simt=False, check=True, stream=None) -> int:
+                           D_skip=None, out_gate=None, qk_l2norm=False, beta_logits=False,
+                           force_simt=False, check=True, stream=None) -> int:
     """Forward pass for callers that cannot allocate device memory.
 
     Same tensors as ``gdn_fwd`` but every output must be passed in (this call
@@ -243,12 +255,15 @@ def gdn_fwd_static_scratch(q, k, v, g, beta, initial_state, cu_seqlens, o, final
     if o is None:
         raise ValueError("gdn_fwd_static_scratch: o must be passed in (the call allocates nothing)")
     N, H, dk, dv = _check_fwd_tensors("gdn_fwd_static_scratch", q, k, v, g, beta,
-                                      initial_state, cu_seqlens, o, final_state)
+                                      initial_state, cu_seqlens, o, final_state, D_skip,
+                                      out_gate)
     B, T = q.shape[:2]
-    flags = (GDN_QK_L2NORM if qk_l2norm else 0) | (GDN_FORCE_SIMT if force_simt else 0)
+    flags = (GDN_QK_L2NORM if qk_l2norm else 0) | (GDN_FORCE_SIMT if force_simt else 0) | \
+        (GDN_BETA_LOGITS if beta_logits else 0)
     return int(lib().gdn_fwd_static_scratch(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens),
-        _ptr(o), _ptr(final_state), B, T, H, dk, dv, N, CHUNK_SIZE, _dtype_code(q.dtype),
+        _ptr(o), _ptr(final_state), _ptr(D_skip), _ptr(out_gate), B, T, H, dk, dv, N, CHUNK_SIZE,
+        _dtype_code(q.dtype),
         flags, 1 if check else 0, _stream_handle(stream)))
 
 

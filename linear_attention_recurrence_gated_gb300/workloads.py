@@ -148,6 +148,28 @@ def generate(w: Workload, lengths=None):
             "cu_seqlens": cu, "N": N, "tokens": B * T}
 
 
+def generate_block_extras(inputs, H: int, seed: int, dtype: str = "bf16"):
+    """Extra inputs of the fused block parts of a forward call, drawn from their
+    own stream (seed) so the base draw is unchanged: ``beta_logits`` N(0, 1) in
+    the storage dtype (the kernel applies the sigmoid), ``D_skip`` ``[H]``
+    N(1, 0.5^2) fp32 (the pages initialise D to 1), ``out_gate`` ``[B, T, H]``
+    U(0, 1) fp32 (a mean of sigmoid outputs on the pages), and raw q/k of
+    random lengths for the in-kernel normalisation: ``q_raw``/``k_raw`` the
+    base q/k rows each scaled by U(0.5, 5)."""
+    rng = np.random.default_rng(seed)
+    dt = _DTYPES[dtype]
+    B, T = inputs["q"].shape[:2]
+    z = torch.from_numpy(rng.standard_normal((B, T, H))).to(dt)
+    d_skip = torch.from_numpy(1.0 + 0.5 * rng.standard_normal(H)).to(torch.float32)
+    gate = torch.from_numpy(rng.uniform(0.0, 1.0, (B, T, H))).to(torch.float32)
+    sq = torch.from_numpy(rng.uniform(0.5, 5.0, (B, T, H, 1)))
+    sk = torch.from_numpy(rng.uniform(0.5, 5.0, (B, T, H, 1)))
+    q_raw = (inputs["q"].double() * sq).to(dt)
+    k_raw = (inputs["k"].double() * sk).to(dt)
+    return {"beta_logits": z.contiguous(), "D_skip": d_skip.contiguous(),
+            "out_gate": gate.contiguous(), "q_raw": q_raw.contiguous(), "k_raw": k_raw.contiguous()}
+
+
 def head_tokens(w: Workload, inputs=None) -> int:
     if inputs is not None:
         return inputs["tokens"] * w.H

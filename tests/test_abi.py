@@ -72,7 +72,8 @@ def test_kernel_names(L):
     assert G.gdn_fwd_kernel_name(128, 128, torch.bfloat16) == "tc128_bf16"
     assert G.gdn_fwd_kernel_name(32, 64, torch.bfloat16) == "simt_bf16"
     assert G.gdn_fwd_kernel_name(64, 96, torch.bfloat16) == "simt_bf16"
-    assert G.gdn_fwd_kernel_name(64, 64, torch.bfloat16, G.GDN_QK_L2NORM) == "simt_bf16"
+    assert G.gdn_fwd_kernel_name(64, 64, torch.bfloat16, G.GDN_QK_L2NORM) == "tc64_bf16"
+    assert G.gdn_fwd_kernel_name(128, 128, torch.bfloat16, G.GDN_QK_L2NORM) == "tc128_bf16"
     assert G.gdn_fwd_kernel_name(64, 64, torch.bfloat16, G.GDN_FORCE_SIMT) == "simt_bf16"
 
 
@@ -85,12 +86,13 @@ def call(L, **over):
     rows = B * T * H
     a = dict(q=BASE, k=BASE + (1 << 30), v=BASE + (2 << 30), g=BASE + (3 << 30),
              beta=BASE + (4 << 30), s0=None, cu=None, o=BASE + (5 << 30),
-             sN=BASE + (6 << 30), B=B, T=T, H=H, dk=dk, dv=dv, N=B, chunk=64,
-             dtype=G.GDN_BF16, flags=0, ws=BASE + (7 << 30), ws_bytes=256)
+             sN=BASE + (6 << 30), dskip=None, ogate=None, B=B, T=T, H=H, dk=dk, dv=dv, N=B,
+             chunk=64, dtype=G.GDN_BF16, flags=0, ws=BASE + (7 << 30), ws_bytes=256)
     a.update(over)
     vp = ctypes.c_void_p
     return L.gdn_fwd(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]),
-                     vp(a["s0"]), vp(a["cu"]), vp(a["o"]), vp(a["sN"]), a["B"], a["T"],
+                     vp(a["s0"]), vp(a["cu"]), vp(a["o"]), vp(a["sN"]), vp(a["dskip"]),
+                     vp(a["ogate"]), a["B"], a["T"],
                      a["H"], a["dk"], a["dv"], a["N"], a["chunk"], a["dtype"], a["flags"],
                      vp(a["ws"]), a["ws_bytes"], vp(0))
 
@@ -111,6 +113,10 @@ def call(L, **over):
     (dict(sN=BASE + (4 << 30)), 1),                        # final_state aliases beta
     (dict(s0=BASE + (6 << 30) + 16), 1),                   # initial/final partial overlap
     (dict(ws=BASE + (5 << 30)), 1),                        # workspace inside o
+    (dict(ogate=BASE + (5 << 30)), 1),                     # out_gate inside o
+    (dict(dskip=BASE + (6 << 30) + 32), 1),                # D_skip inside final_state
+    (dict(ogate=BASE + (9 << 30) + 4), 1),                 # out_gate misaligned
+    (dict(flags=G.GDN_GATE_SIGMOID), 1),                   # a gdn_diag_fwd flag
 ])
 def test_host_validation_rejects_before_launch(L, over, code):
     assert call(L, **over) == code
@@ -262,7 +268,8 @@ def test_static_scratch_entry_point_validates_before_enqueueing(L):
     a scratch need above the array's size, and zero sizes."""
     vp, i32 = ctypes.c_void_p, ctypes.c_int32
     fake = vp(1 << 40)
-    args = [fake] * 5 + [vp(None), vp(None), vp((1 << 40) + (1 << 30)), vp(None)]
+    args = [fake] * 5 + [vp(None), vp(None), vp((1 << 40) + (1 << 30)), vp(None), vp(None),
+                         vp(None)]
     # num_seqs = 0: no scratch size is defined
     st = L.gdn_fwd_static_scratch(*args, i32(1), i32(8), i32(2), i32(32), i32(32), i32(0),
                                   i32(64), ctypes.c_int(1), ctypes.c_uint32(0), i32(0), vp(0))

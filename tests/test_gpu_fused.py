@@ -1,0 +1,110 @@
+"""GPU parity of the GDN block parts fused into gdn_fwd ("Model Architecture
+Walkthrough", section 5.5 step 6 and section 5.4.3): the output epilogue
+o <- (o + D_h v) * out_gate, beta given as logits (sigmoid in the kernel) and
+in-kernel q/k L2 normalisation, on each forward kernel, against the composed
+oracle (oracle.block.epilogue over oracle.forward with sigmoid(beta))."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle.block as OB
+import parity
+from linear_attention_recurrence_gated_gb300 import gdn as G
+from linear_attention_recurrence_gated_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA not available: the GPU tests need a GB300")
+    G.lib()
+    oracle.build()
+
+
+def run(inp, ex, *, epi, logits, l2, force_simt=False, chunk=64):
+    d = parity.to_dev(inp)
+    e = parity.to_dev(ex)
+    q, k = (e["q_raw"], e["k_raw"]) if l2 else (d["q"], d["k"])
+    beta = e["beta_logits"] if logits else d["beta"]
+    o, s = G.gdn_fwd(q, k, d["v"], d["g"], beta, d["initial_state"], d["cu_seqlens"],
+                     D_skip=e["D_skip"] if epi else None, out_gate=e["out_gate"] if epi else None,
+                     beta_logits=logits, qk_l2norm=l2, force_simt=force_simt, chunk_size=chunk,
+                     check=True)
+    torch.cuda.synchronize()
+    # the oracle on the same stored inputs
+    beta_ref = OB.sigmoid(ex["beta_logits"]) if logits else inp["beta"]
+    qr, kr = (ex["q_raw"], ex["k_raw"]) if l2 else (inp["q"], inp["k"])
+    o_ref, s_ref = oracle.forward(qr, kr, inp["v"], inp["g"], beta_ref, inp["initial_state"],
+                                  inp["cu_seqlens"], qk_l2norm=l2)
+    if epi:
+        o_ref = OB.epilogue(o_ref, inp["v"], ex["D_skip"], ex["out_gate"])
+    o64 = o.double().cpu().numpy()
+    s64 = s.double().cpu().numpy()
+    assert np.all(np.isfinite(o64)) and np.all(np.isfinite(s64))
+    cu = None if inp["cu_seqlens"] is None else inp["cu_seqlens"].tolist()
+    return (parity.rel(o64, o_ref), parity.rel(s64, s_ref), parity.worst_unit_o(o64, o_ref, cu),
+            parity.worst_unit_state(s64, s_ref))
+
+
+def check(errs, dtype):
+    to, ts = parity.TOL[dtype]
+    ro, rs, uo, us = errs
+    msg = f"o={ro:.3e} state={rs:.3e} worst unit o={uo:.3e} state={us:.3e}"
+    assert ro <= to and rs <= ts and uo <= to and us <= ts, msg
+
+
+SHAPES = [(2, 200, 3, 64, 64), (1, 129, 2, 64, 128), (2, 150, 2, 128, 128), (1, 70, 2, 32, 64)]
+
+
+@pytest.mark.parametrize("B,T,H,dk,dv", SHAPES)
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("epi,logits", [(True, False), (False, True), (True, True)])
+def test_epilogue_and_beta_logits(B, T, H, dk, dv, dtype, epi, logits):
+    w = W.custom(B=B, T=T, H=H, dk=dk, dv=dv, dtype=dtype, init_state=True, seed=300 + T + dk)
+    inp = W.generate(w)
+    ex = W.generate_block_extras(inp, H, seed=77 + dv, dtype=dtype)
+    check(run(inp, ex, epi=epi, logits=logits, l2=False), W._DTYPES[dtype])
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128)])
+def test_fused_on_the_fp32_kernel_forced(dk, dv):
+    w = W.custom(B=1, T=200, H=2, dk=dk, dv=dv, dtype="bf16", init_state=True, seed=91)
+    inp = W.generate(w)
+    ex = W.generate_block_extras(inp, 2, seed=92)
+    check(run(inp, ex, epi=True, logits=True, l2=False, force_simt=True), torch.bfloat16)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 128)])
+def test_fused_varlen(dk, dv):
+    lens = [1, 63, 64, 65, 0, 300, 17]
+    w = W.custom(num_seqs=len(lens), len_range=(0, 300), H=3, dk=dk, dv=dv, dtype="bf16",
+                 init_state=True, seed=31)
+    inp = W.generate(w, lengths=lens)
+    ex = W.generate_block_extras(inp, 3, seed=32)
+    check(run(inp, ex, epi=True, logits=True, l2=False), torch.bfloat16)
+
+
+@pytest.mark.parametrize("l2", [False, True])
+def test_fused_full_hymo(l2):
+    w = W.WORKLOADS["hymo_bf16"]
+    inp = W.generate(w)
+    ex = W.generate_block_extras(inp, w.H, seed=5)
+    errs = run(inp, ex, epi=True, logits=True, l2=l2)
+    check(errs, torch.bfloat16)
+    parity.MARGINS.append(
+        f"hymo_bf16 + epilogue + beta logits{' + q/k L2 norm' if l2 else ''} "
+        f"[{G.gdn_fwd_kernel_name(w.dk, w.dv, torch.bfloat16, G.GDN_QK_L2NORM if l2 else 0)}]: "
+        f"rel L2 o={errs[0]:.3e} state={errs[1]:.3e}; worst (sequence, head) "
+        f"o={errs[2]:.3e} state={errs[3]:.3e}")
+
+
+@pytest.mark.parametrize("B,T,H,dk,dv", SHAPES)
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_qk_l2norm(B, T, H, dk, dv, dtype):
+    w = W.custom(B=B, T=T, H=H, dk=dk, dv=dv, dtype=dtype, init_state=True, seed=400 + T + dv)
+    inp = W.generate(w)
+    ex = W.generate_block_extras(inp, H, seed=88, dtype=dtype)
+    check(run(inp, ex, epi=False, logits=False, l2=True), W._DTYPES[dtype])
