@@ -71,9 +71,11 @@ typedef enum gdn_dtype { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 enum {
   /* Normalise q_t and k_t in-kernel: x / sqrt(sum(x^2) + 1e-6), fp32 (the
    * gated delta rule's q/k normalisation, part of the block's prologue).  The
-   * tensor-core kernels normalise the loaded bf16 tiles in shared memory and
-   * round the result back to bf16 before their products read it; the fp32
-   * kernel keeps it in fp32. */
+   * tensor-core kernels compute each row's factor 1/|x| in fp32 from the
+   * loaded bf16 tiles and fold it into the fp32 scaling of the products
+   * (row and column factors of Q K^T and K K^T, the rows of W, Ud and O), so
+   * the stored bf16 q and k reach the tensor cores unrounded a second time;
+   * the fp32 kernel normalises in fp32. */
   GDN_QK_L2NORM = 1u << 0,
   /* Use the fp32 CUDA-core kernel even for bf16 storage (the tensor-core
    * kernel is the default for bf16).  fp32 storage always uses it. */
@@ -85,7 +87,22 @@ enum {
    * sigmoid(beta input) in fp32 (the write strength is a sigmoid of a
    * projection in the gated delta rule block; the pages' block computes its
    * gates the same way, "Model Architecture Walkthrough", section 5.4.3). */
-  GDN_BETA_LOGITS = 1u << 3
+  GDN_BETA_LOGITS = 1u << 3,
+  /* gdn_fwd and gdn_fwd_static_scratch: before its first global access, every
+   * block of the forward kernels checks the whole index range it will touch
+   * in each buffer (q, k, v, g, beta, o, the states, out_gate: computed with
+   * the kernels' own index formulas, which are monotone in token, row and
+   * column) against the buffers' extents, and that each TMA box's innermost
+   * coordinate lies on a 16-byte boundary.  Extents come from the shapes, or
+   * are declared by the caller through gdn_fwd_debug, and the tensor maps are
+   * cut to them so that no TMA box reaches past.  A violation records
+   * GDN_ERR_DEVICE_CHECK with (sequence, head, site) in the status word
+   * (gdn_check_record reads them) and the block ends without any access: its
+   * outputs are left as they were.  The plain kernels carry one uniform
+   * branch for it.  The pages' kernel asserts its inputs and raises instead of
+   * falling back ("Optimization Quartet", Triton GDN kernel sections 3.3 and
+   * 3.5); this is the device-side counterpart. */
+  GDN_DEBUG_CHECKS = 1u << 4
 };
 
 /* Bytes of device workspace gdn_fwd needs for these sizes (>= 256; the first
@@ -148,7 +165,7 @@ gdn_status gdn_workspace_init(void *workspace, size_t workspace_bytes, void *str
  * with GDN_BETA_LOGITS as sigmoid(beta input).  The state element (i, j) of
  * H = S^T multiplies key dimension i and value dimension j.
  *
- * flags: any of GDN_QK_L2NORM, GDN_BETA_LOGITS, GDN_FORCE_SIMT.
+ * flags: any of GDN_QK_L2NORM, GDN_BETA_LOGITS, GDN_FORCE_SIMT, GDN_DEBUG_CHECKS.
  *
  * Supported sizes: head_dim_k in {32, 64, 128}; head_dim_v a multiple of 32
  * in [32, 256]; num_heads >= 1; num_seqs in [1, 65535]; chunk_size in {32,
@@ -180,6 +197,34 @@ gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
                    int32_t head_dim_k, int32_t head_dim_v, int32_t num_seqs,
                    int32_t chunk_size, gdn_dtype dtype, uint32_t flags,
                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* Elements (not bytes) each buffer of a forward call holds, for
+ * gdn_fwd_debug.  A field of a NULL buffer is ignored. */
+typedef struct gdn_extents {
+  int64_t q, k, v, g, beta, o;
+  int64_t initial_state, final_state, out_gate;
+} gdn_extents;
+
+/*
+ * gdn_fwd_debug -- gdn_fwd with GDN_DEBUG_CHECKS, against extents the caller
+ * declares (for views into larger allocations, or to test the checks).
+ * Arguments, validation and results are gdn_fwd's; `declared` is a host
+ * pointer read during the call (NULL = extents from the shapes).  Every field
+ * must be >= 0 (else GDN_ERR_INVALID_ARG).  A declared extent smaller than the
+ * range some block of the call would touch makes that block record
+ * GDN_ERR_DEVICE_CHECK and end without touching anything; the other blocks run
+ * as usual.  With seq_len = 0 the state copy is checked on the host and an
+ * undersized state extent returns GDN_ERR_INVALID_ARG.  No passage of the
+ * pages defines this call (see GDN_DEBUG_CHECKS).
+ */
+gdn_status gdn_fwd_debug(const void *q, const void *k, const void *v, const float *g,
+                         const void *beta, const float *initial_state,
+                         const int32_t *cu_seqlens, void *o, float *final_state,
+                         const float *D_skip, const float *out_gate, int32_t batch,
+                         int32_t seq_len, int32_t num_heads, int32_t head_dim_k,
+                         int32_t head_dim_v, int32_t num_seqs, int32_t chunk_size,
+                         gdn_dtype dtype, uint32_t flags, void *workspace,
+                         size_t workspace_bytes, const gdn_extents *declared, void *stream);
 
 /*
  * gdn_fwd_static_scratch -- gdn_fwd for callers that cannot allocate device
@@ -410,6 +455,16 @@ gdn_status gdn_bwd(const void *q, const void *k, const void *v, const float *g,
  * call; it follows their rule that failures surface as errors, with no silent
  * fallback ("Optimization Quartet", Triton GDN kernel section 3.5). */
 gdn_status gdn_check(void *workspace, void *stream);
+
+/* gdn_check that also returns where the recorded error arose: the sequence
+ * and head of the block that recorded it and a site code (for
+ * GDN_ERR_DEVICE_CHECK: 1 q, 2 k, 3 v, 4 g, 5 beta, 6 o, 7 initial_state,
+ * 8 final_state, 9 out_gate, 10 a TMA box coordinate off its 16-byte
+ * boundary; 0 otherwise).  Any output pointer may be NULL; with GDN_OK they
+ * read -1, -1, 0.  Same synchronisation, clearing and return values as
+ * gdn_check (and the same footing in the pages). */
+gdn_status gdn_check_record(void *workspace, void *stream, int32_t *seq, int32_t *head,
+                            int32_t *site);
 
 /* Static, human-readable name of a status code (never NULL; the string is
  * owned by the library).  Unknown codes give "GDN_ERR_UNKNOWN".  No passage

@@ -57,7 +57,7 @@ gdn_status fwd_validate(const void *q, const void *k, const void *v, const float
       num_seqs <= 0)
     return GDN_ERR_INVALID_ARG;
   if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
-  if (flags & ~(uint32_t)(GDN_QK_L2NORM | GDN_FORCE_SIMT | GDN_BETA_LOGITS))
+  if (flags & ~(uint32_t)(GDN_QK_L2NORM | GDN_FORCE_SIMT | GDN_BETA_LOGITS | GDN_DEBUG_CHECKS))
     return GDN_ERR_INVALID_ARG;
   if (cu_seqlens ? batch != 1 : num_seqs != batch) return GDN_ERR_INVALID_ARG;
   if (!supported_dk(head_dim_k) || !supported_dv(head_dim_v)) return GDN_ERR_UNSUPPORTED;
@@ -123,6 +123,12 @@ gdn_status fwd_validate(const void *q, const void *k, const void *v, const float
   p.seq_len = seq_len;
   p.num_heads = num_heads; p.dk = head_dim_k; p.dv = head_dim_v; p.num_seqs = num_seqs;
   p.flags = flags;
+  // extents from the shapes (gdn_fwd_debug may declare smaller ones)
+  const int64_t r = (int64_t)rows;
+  p.ext.q = p.ext.k = r * head_dim_k;
+  p.ext.v = p.ext.o = r * head_dim_v;
+  p.ext.g = p.ext.beta = p.ext.gate = r;
+  p.ext.s0 = p.ext.sN = (int64_t)num_seqs * num_heads * head_dim_k * head_dim_v;
   return GDN_OK;
 }
 
@@ -181,7 +187,44 @@ gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
   return gdn::fwd_launch(call, (cudaStream_t)stream);
 }
 
-gdn_status gdn_check(void *workspace, void *stream) {
+gdn_status gdn_fwd_debug(const void *q, const void *k, const void *v, const float *g,
+                         const void *beta, const float *initial_state, const int32_t *cu_seqlens,
+                         void *o, float *final_state, const float *D_skip, const float *out_gate,
+                         int32_t batch, int32_t seq_len, int32_t num_heads, int32_t head_dim_k,
+                         int32_t head_dim_v, int32_t num_seqs, int32_t chunk_size, gdn_dtype dtype,
+                         uint32_t flags, void *workspace, size_t workspace_bytes,
+                         const gdn_extents *declared, void *stream) {
+  gdn::FwdCall call;
+  const gdn_status st = gdn::fwd_validate(
+      q, k, v, g, beta, initial_state, cu_seqlens, o, final_state, D_skip, out_gate, batch,
+      seq_len, num_heads, head_dim_k, head_dim_v, num_seqs, chunk_size, dtype,
+      flags | GDN_DEBUG_CHECKS, workspace, workspace_bytes, &call);
+  if (st != GDN_OK) return st;
+  if (declared && call.states_only) {  // no kernel runs: the copy's extents are checked here
+    const int64_t need = (int64_t)(call.state_bytes / 4);
+    if ((call.p.sN && call.p.s0 && declared->initial_state < need) ||
+        (call.p.sN && declared->final_state < need))
+      return GDN_ERR_INVALID_ARG;
+  }
+  if (declared) {
+    const int64_t d[] = {declared->q, declared->k, declared->v, declared->g, declared->beta,
+                         declared->o, declared->initial_state, declared->final_state,
+                         declared->out_gate};
+    for (int64_t x : d)
+      if (x < 0) return GDN_ERR_INVALID_ARG;
+    gdn::Extents &e = call.p.ext;
+    e.q = declared->q; e.k = declared->k; e.v = declared->v; e.g = declared->g;
+    e.beta = declared->beta; e.o = declared->o; e.s0 = declared->initial_state;
+    e.sN = declared->final_state; e.gate = declared->out_gate;
+  }
+  return gdn::fwd_launch(call, (cudaStream_t)stream);
+}
+
+gdn_status gdn_check_record(void *workspace, void *stream, int32_t *seq, int32_t *head,
+                            int32_t *site) {
+  if (seq) *seq = -1;
+  if (head) *head = -1;
+  if (site) *site = 0;
   if (!workspace) return GDN_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;
   gdn::DeviceStatus st;
@@ -192,7 +235,14 @@ gdn_status gdn_check(void *workspace, void *stream) {
   if (st.code == 0) return GDN_OK;
   if (cudaMemsetAsync(workspace, 0, sizeof st, s) != cudaSuccess) return GDN_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (seq) *seq = (int32_t)st.seq;
+  if (head) *head = (int32_t)st.head;
+  if (site) *site = (int32_t)st.aux;
   return st.code <= GDN_ERR_DEVICE_CHECK ? (gdn_status)st.code : GDN_ERR_DEVICE_CHECK;
+}
+
+gdn_status gdn_check(void *workspace, void *stream) {
+  return gdn_check_record(workspace, stream, nullptr, nullptr, nullptr);
 }
 
 const char *gdn_status_string(int32_t status) {

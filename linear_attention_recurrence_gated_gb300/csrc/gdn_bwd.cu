@@ -611,6 +611,7 @@ extern "C" gdn_status gdn_bwd(const void *q, const void *k, const void *v, const
   f.q = q; f.k = k; f.v = v; f.beta = beta; f.g = g;
   f.s0 = initial_state; f.cu = cu_seqlens; f.o = nullptr; f.sN = nullptr;
   f.d_skip = nullptr; f.out_gate = nullptr;
+  f.ext = Extents{};
   f.status = reinterpret_cast<DeviceStatus *>(ws);
   f.ckpt = nullptr;
   f.seq_len = seq_len;

@@ -66,6 +66,9 @@ gdn_fwd_simt_kernel(const FwdParams p) {
 
   int64_t start, len;
   if (!sequence_bounds(p, n, h, start, len)) return;
+  if ((p.flags & GDN_DEBUG_CHECKS) &&
+      !debug_ranges_ok(p, n, h, start, len, col0, DVT, (int)sizeof(Tin), false))
+    return;  // recorded; nothing was accessed
   if (len == 0) {   // an empty sequence: the state passes through
     pass_state_through(p, n, h, col0, DVT);
     return;

@@ -123,6 +123,9 @@ gdn_fwd_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_q,
 
   int64_t start, len;
   if (!sequence_bounds(p, n, h, start, len)) return;  // uniform over the CTA
+  if ((p.flags & GDN_DEBUG_CHECKS) &&
+      !debug_ranges_ok(p, n, h, start, len, col0, kDvt, 2, true))
+    return;  // recorded; nothing was accessed
   if (len == 0) {   // an empty sequence: the state passes through
     pass_state_through(p, n, h, col0, kDvt);
     return;
@@ -861,10 +864,10 @@ cudaError_t launch_tc(const FwdParams &p, cudaStream_t stream) {
   using L = TcLayout<DK, NIN>;
   const int64_t tokens = p.cu ? p.seq_len : (int64_t)p.num_seqs * p.seq_len;
   CUtensorMap tq, tk, tv, to;
-  if (!make_tmap(&tq, p.q, DK, p.num_heads, tokens) ||
-      !make_tmap(&tk, p.k, DK, p.num_heads, tokens) ||
-      !make_tmap(&tv, p.v, p.dv, p.num_heads, tokens) ||
-      !make_tmap(&to, p.o, p.dv, p.num_heads, tokens))
+  if (!make_tmap(&tq, p.q, DK, p.num_heads, tmap_rows(p, tokens, p.ext.q, DK)) ||
+      !make_tmap(&tk, p.k, DK, p.num_heads, tmap_rows(p, tokens, p.ext.k, DK)) ||
+      !make_tmap(&tv, p.v, p.dv, p.num_heads, tmap_rows(p, tokens, p.ext.v, p.dv)) ||
+      !make_tmap(&to, p.o, p.dv, p.num_heads, tmap_rows(p, tokens, p.ext.o, p.dv)))
     return cudaErrorInvalidValue;
   // the block parts fused into the pass run in their own instantiation
   const int feat = ((p.flags & GDN_QK_L2NORM) ? kFL2 : 0) | ((p.d_skip || p.out_gate) ? kFEpi : 0);

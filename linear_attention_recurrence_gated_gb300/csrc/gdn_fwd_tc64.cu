@@ -286,6 +286,9 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
 
   int64_t start, len;
   if (!sequence_bounds(p, n, h, start, len)) return;  // uniform over the CTA
+  if ((p.flags & GDN_DEBUG_CHECKS) &&
+      !debug_ranges_ok(p, n, h, start, len, col0, kDvt, 2, true))
+    return;  // recorded; nothing was accessed
   if (len == 0) {   // an empty sequence: the state passes through
     pass_state_through(p, n, h, col0, kDvt);
     return;
@@ -1038,9 +1041,9 @@ cudaError_t launch_fwd_tc64(const FwdParams &p, cudaStream_t stream) {
   using L = L64;
   const int64_t tokens = p.cu ? p.seq_len : (int64_t)p.num_seqs * p.seq_len;
   CUtensorMap tq, tk, tv;
-  if (!make_tmap(&tq, p.q, DK, p.num_heads, tokens) ||
-      !make_tmap(&tk, p.k, DK, p.num_heads, tokens) ||
-      !make_tmap(&tv, p.v, p.dv, p.num_heads, tokens))
+  if (!make_tmap(&tq, p.q, DK, p.num_heads, tmap_rows(p, tokens, p.ext.q, DK)) ||
+      !make_tmap(&tk, p.k, DK, p.num_heads, tmap_rows(p, tokens, p.ext.k, DK)) ||
+      !make_tmap(&tv, p.v, p.dv, p.num_heads, tmap_rows(p, tokens, p.ext.v, p.dv)))
     return cudaErrorInvalidValue;
   // the block parts fused into the pass run in their own instantiation, so
   // the plain pass carries none of their code

@@ -22,6 +22,18 @@ struct DeviceStatus {
 };
 constexpr size_t kStatusBytes = 256;
 
+// Elements each buffer of a forward call holds: derived from the shapes, or
+// declared by the caller of gdn_fwd_debug.  Read only under GDN_DEBUG_CHECKS.
+struct Extents {
+  int64_t q, k, v, g, beta, o, s0, sN, gate;
+};
+
+// Sites recorded in DeviceStatus::aux by a failed GDN_DEBUG_CHECKS range check.
+enum DebugSite : uint32_t {
+  kSiteQ = 1, kSiteK, kSiteV, kSiteG, kSiteBeta, kSiteO, kSiteS0, kSiteSN, kSiteGate,
+  kSiteTmaX,  // a TMA box's innermost coordinate is not on a 16-byte boundary
+};
+
 // Everything one gdn_fwd launch needs, passed by value as a kernel argument.
 struct FwdParams {
   const void *q, *k, *v, *beta;
@@ -37,6 +49,7 @@ struct FwdParams {
   int64_t seq_len;      // tokens per batch row (dense) or packed total (varlen)
   int32_t num_heads, dk, dv, num_seqs;
   uint32_t flags;
+  Extents ext;
 };
 
 __device__ __forceinline__ void report(DeviceStatus *st, uint32_t code, uint32_t seq,
@@ -68,6 +81,46 @@ __device__ __forceinline__ bool sequence_bounds(const FwdParams &p, int n, int h
   start = s;
   len = e - s;
   return true;
+}
+
+// GDN_DEBUG_CHECKS: before its first global access, the block that owns value
+// columns [col0, col0 + ncols) of (sequence n, head h) checks the whole index
+// range it will touch in every buffer, with the kernels' own index formulas
+// (all monotone in the token, the row and the column), against the extents;
+// `tma_x` asks for the TMA rule that a box's innermost coordinate times the
+// element size be a multiple of 16 bytes (the q/k boxes start at column 0,
+// the v/o boxes at col0).  The first violation is recorded as
+// GDN_ERR_DEVICE_CHECK with (n, h, site) and the block must then end without
+// any access; returns false in that case.  Uniform over the block.
+__device__ __forceinline__ bool debug_ranges_ok(const FwdParams &p, int n, int h, int64_t start,
+                                                int64_t len, int col0, int ncols, int elem_bytes,
+                                                bool tma_x) {
+  const int64_t H = p.num_heads, dk = p.dk, dv = p.dv;
+  const Extents &x = p.ext;
+  uint32_t site = 0;
+  if (tma_x && ((int64_t)col0 * elem_bytes) % 16 != 0) site = kSiteTmaX;
+  if (len > 0 && site == 0) {
+    const int64_t t_hi = start + len - 1;            // last token of the sequence
+    const int64_t qk_hi = (t_hi * H + h) * dk + dk - 1;  // last q/k element read
+    const int64_t vo_hi = (t_hi * H + h) * dv + col0 + ncols - 1;
+    const int64_t row_hi = t_hi * H + h;              // last g / beta / gate element
+    if (start < 0) site = kSiteQ;
+    else if (qk_hi >= x.q) site = kSiteQ;
+    else if (qk_hi >= x.k) site = kSiteK;
+    else if (vo_hi >= x.v) site = kSiteV;
+    else if (row_hi >= x.g) site = kSiteG;
+    else if (row_hi >= x.beta) site = kSiteBeta;
+    else if (vo_hi >= x.o) site = kSiteO;
+    else if (p.out_gate && row_hi >= x.gate) site = kSiteGate;
+  }
+  if (site == 0) {
+    const int64_t st_hi = ((n * H + h) * dk + dk - 1) * dv + col0 + ncols - 1;
+    if (p.s0 && st_hi >= x.s0) site = kSiteS0;
+    else if (p.sN && st_hi >= x.sN) site = kSiteSN;
+  }
+  if (site == 0) return true;
+  if (threadIdx.x == 0) report(p.status, GDN_ERR_DEVICE_CHECK, (uint32_t)n, (uint32_t)h, site);
+  return false;
 }
 
 // An empty sequence leaves its state as it came: the CTA that owns value

@@ -123,6 +123,16 @@ inline EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Token rows of a tensor map: all of them, or under GDN_DEBUG_CHECKS no more
+// than the buffer's extent holds, so that no TMA box reaches past it (at least
+// one row, for a valid map: a block whose rows pass the extent returns before
+// its first copy).
+inline int64_t tmap_rows(const FwdParams &p, int64_t tokens, int64_t extent, int cols) {
+  if (!(p.flags & GDN_DEBUG_CHECKS)) return tokens;
+  const int64_t r = extent / ((int64_t)p.num_heads * cols);
+  return r < 1 ? 1 : r < tokens ? r : tokens;
+}
+
 // [tokens][heads][cols] bf16 viewed as a 3-D tensor; box = 64 cols x 1 head x 64 tokens.
 inline bool make_tmap(CUtensorMap *m, const void *ptr, int cols, int heads, int64_t tokens) {
   EncodeTiledFn enc = encode_fn();

@@ -18,6 +18,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgdn.so")
 
 GDN_OK = 0
+(GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA, GDN_ERR_TIMEOUT,
+ GDN_ERR_BAD_SEQLENS, GDN_ERR_DEVICE_CHECK) = range(1, 8)
 STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED",
                 3: "GDN_ERR_WORKSPACE", 4: "GDN_ERR_CUDA", 5: "GDN_ERR_TIMEOUT",
                 6: "GDN_ERR_BAD_SEQLENS", 7: "GDN_ERR_DEVICE_CHECK"}
@@ -26,13 +28,17 @@ GDN_QK_L2NORM = 1 << 0
 GDN_FORCE_SIMT = 1 << 1
 GDN_GATE_SIGMOID = 1 << 2
 GDN_BETA_LOGITS = 1 << 3
+GDN_DEBUG_CHECKS = 1 << 4
+# site codes of a GDN_ERR_DEVICE_CHECK record (gdn_check_record)
+DEBUG_SITES = {1: "q", 2: "k", 3: "v", 4: "g", 5: "beta", 6: "o", 7: "initial_state",
+               8: "final_state", 9: "out_gate", 10: "tma_x"}
 CHUNK_SIZE = 64
 
 # Every symbol include/gdn.h declares.
 EXPORTED = ("gdn_fwd_workspace_size", "gdn_workspace_init", "gdn_fwd", "gdn_check",
             "gdn_status_string", "gdn_fwd_kernel_name", "gdn_fwd_static_scratch",
             "gdn_decode", "gdn_diag_workspace_size", "gdn_diag_fwd", "gdn_conv_silu",
-            "gdn_bwd_workspace_size", "gdn_bwd")
+            "gdn_bwd_workspace_size", "gdn_bwd", "gdn_fwd_debug", "gdn_check_record")
 # ... and include/gdn_debug.h (self-tests of the failure reporting).
 DEBUG_EXPORTED = ("gdn_debug_wait_timeout",)
 
@@ -67,6 +73,13 @@ def lib() -> ctypes.CDLL:
                                   vp, sz, vp]
             L.gdn_check.restype = ctypes.c_int
             L.gdn_check.argtypes = [vp, vp]
+            L.gdn_check_record.restype = ctypes.c_int
+            L.gdn_check_record.argtypes = [vp, vp, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                           ctypes.POINTER(i32)]
+            L.gdn_fwd_debug.restype = ctypes.c_int
+            L.gdn_fwd_debug.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                        i32, i32, i32, i32, i32, i32, i32, ctypes.c_int, u32,
+                                        vp, sz, ctypes.POINTER(GdnExtents), vp]
             L.gdn_debug_wait_timeout.restype = ctypes.c_int
             L.gdn_debug_wait_timeout.argtypes = [vp, sz, vp]
             L.gdn_status_string.restype = ctypes.c_char_p
@@ -93,6 +106,12 @@ def lib() -> ctypes.CDLL:
                                        i32, i32, i32, i32, i32, ctypes.c_int, u32, vp, sz, vp]
             _lib = L
     return _lib
+
+
+class GdnExtents(ctypes.Structure):
+    """``gdn_extents``: elements each buffer of a forward call holds."""
+    _fields_ = [(n, ctypes.c_int64) for n in ("q", "k", "v", "g", "beta", "o", "initial_state",
+                                              "final_state", "out_gate")]
 
 
 def status_string(status: int) -> str:
@@ -140,6 +159,15 @@ def new_workspace(num_seqs, num_heads, head_dim_k, head_dim_v, flags=0, device=N
 def gdn_check(workspace: torch.Tensor, stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status word."""
     return int(lib().gdn_check(_ptr(workspace), _stream_handle(stream)))
+
+
+def gdn_check_record(workspace: torch.Tensor, stream=None):
+    """gdn_check that also returns where the error arose:
+    ``(status, seq, head, site)`` (site codes in ``DEBUG_SITES``)."""
+    seq, head, site = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    st = lib().gdn_check_record(_ptr(workspace), _stream_handle(stream), ctypes.byref(seq),
+                                ctypes.byref(head), ctypes.byref(site))
+    return int(st), seq.value, head.value, site.value
 
 
 def gdn_debug_wait_timeout(workspace: torch.Tensor, stream=None) -> int:
@@ -198,10 +226,15 @@ def _check_fwd_tensors(where, q, k, v, g, beta, initial_state, cu_seqlens, o, fi
     return N, H, dk, dv
 
 
+def _fwd_flags(qk_l2norm, beta_logits, force_simt, debug_checks):
+    return (GDN_QK_L2NORM if qk_l2norm else 0) | (GDN_FORCE_SIMT if force_simt else 0) | \
+        (GDN_BETA_LOGITS if beta_logits else 0) | (GDN_DEBUG_CHECKS if debug_checks else 0)
+
+
 def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
             final_state=None, output_final_state=True, workspace=None, D_skip=None,
             out_gate=None, qk_l2norm=False, beta_logits=False, force_simt=False,
-            chunk_size=CHUNK_SIZE, stream=None, check=False):
+            chunk_size=CHUNK_SIZE, stream=None, check=False, debug_checks=False):
     """Forward pass of the gated delta rule through the C ABI.
 
     q, k ``[B, T, H, dk]``; v ``[B, T, H, dv]``; g ``[B, T, H]`` fp32; beta
@@ -214,6 +247,7 @@ def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
     ``D_skip`` ``[H]`` and ``out_gate`` ``[B, T, H]`` (fp32, optional) fuse the
     block epilogue o <- (o + D_skip[h] v) * out_gate; ``beta_logits`` makes the
     kernel use sigmoid(beta); ``qk_l2norm`` normalises q and k in-kernel.
+    ``debug_checks`` sets GDN_DEBUG_CHECKS (range checks before every access).
     With ``check=True`` the call synchronises and raises on a device-side error.
     """
     N, H, dk, dv = _check_fwd_tensors("gdn_fwd", q, k, v, g, beta, initial_state, cu_seqlens,
@@ -224,8 +258,7 @@ def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
         final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
     B, T = q.shape[:2]
     dcode = _dtype_code(q.dtype)
-    flags = (GDN_QK_L2NORM if qk_l2norm else 0) | (GDN_FORCE_SIMT if force_simt else 0) | \
-        (GDN_BETA_LOGITS if beta_logits else 0)
+    flags = _fwd_flags(qk_l2norm, beta_logits, force_simt, debug_checks)
     if workspace is None:
         workspace = new_workspace(N, H, dk, dv, flags, device=q.device)
     st = lib().gdn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
@@ -243,7 +276,8 @@ def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
 
 def gdn_fwd_static_scratch(q, k, v, g, beta, initial_state, cu_seqlens, o, final_state, *,
                            D_skip=None, out_gate=None, qk_l2norm=False, beta_logits=False,
-                           force_simt=False, check=True, stream=None) -> int:
+                           force_simt=False, check=True, stream=None,
+                           debug_checks=False) -> int:
     """Forward pass for callers that cannot allocate device memory.
 
     Same tensors as ``gdn_fwd`` but every output must be passed in (this call
@@ -258,13 +292,41 @@ def gdn_fwd_static_scratch(q, k, v, g, beta, initial_state, cu_seqlens, o, final
                                       initial_state, cu_seqlens, o, final_state, D_skip,
                                       out_gate)
     B, T = q.shape[:2]
-    flags = (GDN_QK_L2NORM if qk_l2norm else 0) | (GDN_FORCE_SIMT if force_simt else 0) | \
-        (GDN_BETA_LOGITS if beta_logits else 0)
+    flags = _fwd_flags(qk_l2norm, beta_logits, force_simt, debug_checks)
     return int(lib().gdn_fwd_static_scratch(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens),
         _ptr(o), _ptr(final_state), _ptr(D_skip), _ptr(out_gate), B, T, H, dk, dv, N, CHUNK_SIZE,
         _dtype_code(q.dtype),
         flags, 1 if check else 0, _stream_handle(stream)))
+
+
+def gdn_fwd_debug(q, k, v, g, beta, initial_state, cu_seqlens, o, final_state, workspace, *,
+                  declared=None, D_skip=None, out_gate=None, qk_l2norm=False,
+                  beta_logits=False, force_simt=False, chunk_size=CHUNK_SIZE, stream=None):
+    """``gdn_fwd_debug``: the forward pass with GDN_DEBUG_CHECKS against
+    declared extents.  ``declared`` maps buffer names (``GdnExtents`` fields)
+    to element counts; missing names take the count of the tensor passed (0
+    for None).  Outputs and workspace are passed in.  Returns the host status;
+    read the device record with ``gdn_check_record``."""
+    N, H, dk, dv = _check_fwd_tensors("gdn_fwd_debug", q, k, v, g, beta, initial_state,
+                                      cu_seqlens, o, final_state, D_skip, out_gate)
+    B, T = q.shape[:2]
+    ext = None
+    if declared is not None:
+        have = dict(q=q, k=k, v=v, g=g, beta=beta, o=o, initial_state=initial_state,
+                    final_state=final_state, out_gate=out_gate)
+        unknown = set(declared) - set(have)
+        if unknown:
+            raise ValueError(f"gdn_fwd_debug: unknown extents {sorted(unknown)}")
+        ext = GdnExtents(**{n: int(declared.get(n, 0 if t is None else t.numel()))
+                            for n, t in have.items()})
+    flags = _fwd_flags(qk_l2norm, beta_logits, force_simt, True)
+    return int(lib().gdn_fwd_debug(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens),
+        _ptr(o), _ptr(final_state), _ptr(D_skip), _ptr(out_gate), B, T, H, dk, dv, N,
+        chunk_size, _dtype_code(q.dtype), flags, _ptr(workspace),
+        workspace.numel() * workspace.element_size(),
+        None if ext is None else ctypes.byref(ext), _stream_handle(stream)))
 
 
 def gdn_decode(q, k, v, g, beta, state=None, *, o=None, state_out=None, qk_l2norm=False,

@@ -122,6 +122,65 @@ def test_host_validation_rejects_before_launch(L, over, code):
     assert call(L, **over) == code
 
 
+def call_debug(L, declared, **over):
+    """gdn_fwd_debug with the fake addresses of `call` and declared extents
+    (None = from the shapes)."""
+    B, T, H, dk, dv = 2, 100, 3, 64, 64
+    a = dict(q=BASE, k=BASE + (1 << 30), v=BASE + (2 << 30), g=BASE + (3 << 30),
+             beta=BASE + (4 << 30), s0=None, cu=None, o=BASE + (5 << 30),
+             sN=BASE + (6 << 30), B=B, T=T, H=H, dk=dk, dv=dv, N=B, flags=0,
+             ws=BASE + (7 << 30), ws_bytes=256)
+    a.update(over)
+    vp = ctypes.c_void_p
+    ext = None if declared is None else ctypes.byref(G.GdnExtents(**declared))
+    return L.gdn_fwd_debug(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]),
+                           vp(a["s0"]), vp(a["cu"]), vp(a["o"]), vp(a["sN"]), vp(None),
+                           vp(None), a["B"], a["T"], a["H"], a["dk"], a["dv"], a["N"], 64,
+                           G.GDN_BF16, a["flags"], vp(a["ws"]), a["ws_bytes"], ext, vp(0))
+
+
+FULL = dict(q=2 * 100 * 3 * 64, k=2 * 100 * 3 * 64, v=2 * 100 * 3 * 64, g=600, beta=600,
+            o=2 * 100 * 3 * 64, initial_state=2 * 3 * 64 * 64, final_state=2 * 3 * 64 * 64,
+            out_gate=600)
+
+
+def test_debug_flag_and_extents_layout():
+    assert G.GDN_DEBUG_CHECKS == 1 << 4
+    hdr = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    assert "GDN_DEBUG_CHECKS = 1u << 4" in hdr
+    fields = re.search(r"typedef struct gdn_extents \{(.*?)\} gdn_extents;", hdr, re.S).group(1)
+    names = re.findall(r"\b([a-z_]+)\s*[,;]", fields)
+    assert names == [n for n, _ in G.GdnExtents._fields_]
+    assert ctypes.sizeof(G.GdnExtents) == 8 * len(names)
+
+
+@pytest.mark.parametrize("declared,over,code", [
+    (dict(FULL, q=-1), {}, 1),                        # a negative extent
+    (dict(FULL, out_gate=-5), {}, 1),                 # even for a NULL buffer
+    (FULL, dict(dk=48), 2),                           # gdn_fwd's own validation first
+    (FULL, dict(ws=None), 3),
+    (FULL, dict(flags=1 << 9), 1),
+    (dict(FULL, final_state=10), dict(T=0), 1),       # no tokens: the state copy is checked here
+    (dict(FULL, initial_state=10), dict(T=0, s0=BASE + (8 << 30)), 1),
+    (dict(FULL, final_state=10), dict(T=0, sN=None), 0),  # nothing to copy
+])
+def test_fwd_debug_validates_on_host(L, declared, over, code):
+    assert call_debug(L, declared, **over) == code
+
+
+def test_debug_flag_accepted_by_validation(L):
+    # the flag passes gdn_fwd's mask: a malformed call still fails for its real reason
+    assert call(L, flags=G.GDN_DEBUG_CHECKS, dk=48) == 2
+    assert call(L, flags=G.GDN_DEBUG_CHECKS, T=0, sN=None) == 0
+
+
+def test_check_record_null_workspace(L):
+    seq, head, site = ctypes.c_int32(5), ctypes.c_int32(5), ctypes.c_int32(5)
+    assert L.gdn_check_record(None, ctypes.c_void_p(0), ctypes.byref(seq), ctypes.byref(head),
+                              ctypes.byref(site)) == 3
+    assert (seq.value, head.value, site.value) == (-1, -1, 0)
+
+
 def test_workspace_init_rejects_small(L):
     assert L.gdn_workspace_init(ctypes.c_void_p(BASE), 16, ctypes.c_void_p(0)) == 3
     assert L.gdn_workspace_init(None, 4096, ctypes.c_void_p(0)) == 3
