@@ -226,7 +226,7 @@ KERNEL_SOURCES = {
     "simt_fp32": "gdn_fwd_simt.cu",
     "simt_bf16": "gdn_fwd_simt.cu",
     "tc64_bf16": "gdn_fwd_tc64.cu",
-    "tc128_bf16": "gdn_fwd_tc.cu",
+    "tc128_bf16": "gdn_fwd_tc128.cu",
     "diag_bf16": "gdn_diag.cu",
     "diag_fp32": "gdn_diag.cu",
     "conv_bf16": "gdn_conv.cu",
