@@ -31,18 +31,18 @@
 // MN-major M = 128 operand over both groups.  "*" rows are whatever finite
 // tile precedes P in shared memory; their products land in rows nobody reads.
 //
-// Roles (22 warps, one CTA per SM; warp w reaches the TMEM lanes
+// Roles (24 warps, one CTA per SM; warp w reaches the TMEM lanes
 // 32*(w%4)..+31 and issues on SM sub-partition w%4):
 //   warp 16        producer: gate vectors + TMA loads of Q, K (two boxes
 //                  each), V (ring of 2 slots of 57 KB), L2 prefetch
 //   warp 13        [Q; K] K^T issuer (tcgen05.mma + commit); owns tensor memory
 //   warps 8,9      drain the P rows of [Q; K] K^T (masked decay, bf16)
 //   warps 18,19    drain the A rows (masked decay and beta, fp32)
-//   warps 2,3,14,15  prep, one team on every chunk (with two slots only one
-//                  chunk is ahead of the chain): diagonal 16x16 inverses of
-//                  (I + A) (fp32), couplings (tf32 mma), blocked substitution
-//                  for the 192 columns of [W | U~] (bf16 mma), three 16-column
-//                  pieces per warp
+//   warps 2,3,14,15,22,23  prep, one team of six on every chunk (with two
+//                  slots only one chunk is ahead of the chain): diagonal 16x16
+//                  inverses of (I + A) (fp32), couplings (tf32 mma), blocked
+//                  substitution for the 192 columns of [W | U~] (bf16 mma), two
+//                  16-column pieces per warp
 //   warps 4,5,12,17  E1 (U, Ud from W H) on lane quarters 0,1; warp 4 then
 //                  issues MMA3 and MMA2
 //   warps 0,1,20,21,6,7,10,11  E2a (state update), two warps (value columns
@@ -66,13 +66,17 @@ using namespace tc;
 constexpr int DK = 128;
 // The input-slot ring, the warps and the warp map.
 struct Cfg {
-  static constexpr int NIN = 2, kWarps = 22, kTeams = 1;
+  static constexpr int NIN = 2, kWarps = 24, kTeams = 1, kPrepThreads = 192;
   static constexpr int kWarpSIssue = 13, kWarpProducer = 16;
   // the next MMA1 is issued from an E2a warp that stores no output, so that
   // its wait for the next chunk's prep does not hold back this chunk's output
   static constexpr int kWarpE1Issue = 4, kWarpE2aIssue = 0;
-  __device__ __forceinline__ static bool is_prep(int w) { return w == 2 || w == 3 || w == 14 || w == 15; }
-  __device__ __forceinline__ static int prep_index(int w) { return (w & 3) - 2 + (w >= 14 ? 2 : 0); }
+  __device__ __forceinline__ static bool is_prep(int w) {
+    return w == 2 || w == 3 || w == 14 || w == 15 || w == 22 || w == 23;
+  }
+  __device__ __forceinline__ static int prep_index(int w) {
+    return (w & 3) - 2 + (w >= 22 ? 4 : (w >= 14 ? 2 : 0));
+  }
   __device__ __forceinline__ static bool is_drain(int w) { return w == 8 || w == 9 || w == 18 || w == 19; }
   __device__ __forceinline__ static bool is_e1(int w) { return w == 4 || w == 5 || w == 12 || w == 17; }
   __device__ __forceinline__ static bool is_e2a(int w) {
@@ -145,8 +149,8 @@ struct Layout {
 // mbarrier indices
 enum : int {
   B_FULL_IN = 0,     // [4]  TMA bytes landed (+ producer arrival)
-  B_EMPTY_IN = 4,    // [4]  E2a and output warps done with the slot (192)
-  B_FULL_ST = 8,     // [2]  prep wrote W and U~ (128)
+  B_EMPTY_IN = 4,    // [4]  slot free: MMA3/MMA2 commit + the output threads' reads (129)
+  B_FULL_ST = 8,     // [2]  prep wrote W and U~ (192)
   B_TMEM_FULL = 10,  // [2]  Q K^T / K K^T accumulator ready (commit)
   B_TMEM_EMPTY = 12, // [2]  ... drained (128, the drain warps)
   B_S_READY = 14,    // [2]  P and A in shared memory (128, the drain warps)
@@ -157,7 +161,7 @@ enum : int {
   B_DH_FULL = 22,    //      MMA3 done (commit)
   B_PU_FULL = 23,    // [2]  MMA2 done (commit)
   B_PU_FREE = 25,    // [2]  DPU drained (64)
-  B_A_FREE = 27,     // [2]  A buffer read by the prep (inverse, couplings) (128)
+  B_A_FREE = 27,     // [2]  A buffer read by the prep (inverse, couplings) (192)
   B_P_FREE = 29,     // [3]  P buffer read by MMA2 (commit)
 };
 
@@ -320,16 +324,16 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
   if (tid == 0) {
     for (int s = 0; s < NIN; ++s) {
       mbar_init(bar(B_FULL_IN + s), 1);
-      mbar_init(bar(B_EMPTY_IN + s), C::kE2aThreads);
+      mbar_init(bar(B_EMPTY_IN + s), 1 + C::kOutThreads);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(B_FULL_ST + s), 128);
+      mbar_init(bar(B_FULL_ST + s), C::kPrepThreads);
       mbar_init(bar(B_TMEM_FULL + s), 1);
       mbar_init(bar(B_TMEM_EMPTY + s), 128);
       mbar_init(bar(B_S_READY + s), 128);
       mbar_init(bar(B_D1_FULL + s), 1);
       mbar_init(bar(B_D1_FREE + s), 128 + C::kOutThreads);
-      mbar_init(bar(B_A_FREE + s), 128);
+      mbar_init(bar(B_A_FREE + s), C::kPrepThreads);
       mbar_init(bar(B_PU_FULL + s), 1);
       mbar_init(bar(B_PU_FREE + s), C::kOutThreads);
     }
@@ -421,7 +425,7 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
         *reinterpret_cast<float2 *>(gate + 64 + 2 * lane) = vD;
         *reinterpret_cast<float2 *>(gate + 128 + 2 * lane) = vB;
         *reinterpret_cast<float2 *>(gate + 192 + 2 * lane) = vE;
-        if (lane == 0) sgc[slot] = gC;
+        if (lane == 0) sgc[c & 3] = gC;  // a ring of 4: E2a may read it after the slot is freed
         if constexpr ((kF & kFEpi) != 0)
           *reinterpret_cast<float2 *>(reinterpret_cast<float *>(smem + L::OFF_RN) +
                                       slot * L::RN_SLOT + 128 + 2 * lane) = vO;
@@ -556,7 +560,7 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
     __syncwarp();
   } else if (C::is_prep(warp)) {
     // ------------------------------------------------------------ prep
-    // One team of four warps takes every chunk; pw is the warp within the team.
+    // One team of six warps takes every chunk; pw is the warp within the team.
     const int pw = C::prep_index(warp), ptid = 32 * pw + lane;
     const uint32_t kBar = kBarPrep;
     __nv_bfloat16 *sTB = reinterpret_cast<__nv_bfloat16 *>(smem + L::OFF_TB);
@@ -585,28 +589,28 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
       // rows past the end of the sequence: zero Q, K, V (the Q K^T MMA has read them)
       if (ok && valid < 64) {
         constexpr int kPerRow = (2 * NG + 1) * 8;  // 16-byte granules of Q_g, K_g, V
-        for (int idx = ptid; idx < (64 - valid) * kPerRow; idx += 128) {
+        for (int idx = ptid; idx < (64 - valid) * kPerRow; idx += C::kPrepThreads) {
           const int row = valid + idx / kPerRow, q = idx % kPerRow, t8 = q >> 3;
           const uint32_t tb = t8 == 2 * NG ? Vs : sb + (t8 >> 1) * L::GSTRIDE + ((t8 & 1) ? L::SK : L::SQ);
           S4(tile_addr(tb, row, (q & 7) * 8)) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      if (lane == 0) vote[vset * 4 + pw] = ok ? 1 : 0;
-      named_sync(kBar, 128);
+      if (lane == 0) vote[vset * 8 + pw] = ok ? 1 : 0;
+      named_sync(kBar, C::kPrepThreads);
       GDN_PHASE(2);
       {
-        const int *v = vote + vset * 4;
-        if (!(v[0] && v[1] && v[2] && v[3])) break;
+        const int *v = vote + vset * 8;
+        if (!(v[0] && v[1] && v[2] && v[3] && v[4] && v[5])) break;
       }
 
-      // ---- 16x16 diagonal blocks of T = (I + A)^-1 (fp32).  Warps 2,3 take two
-      // blocks each, one per half-warp; lane l builds column l of its block by
+      // ---- 16x16 diagonal blocks of T = (I + A)^-1 (fp32).  Team warps 4,5 take
+      // two blocks each, one per half-warp; lane l builds column l of its block by
       // forward substitution, T_rl = [r == l] - sum_{k<r} A_rk T_kl, reading
       // rows of A as float4 (broadcast within the half-warp).  T is stored
       // column-major: fp32 for the couplings, and as bf16 T diag(beta gamma) and
       // T diag(beta) for the substitution. ----
-      if (pw >= 2) {
-        const int blk = 2 * (pw - 2) + (lane >> 4), l = lane & 15;
+      if (pw >= 4) {
+        const int blk = 2 * (pw - 4) + (lane >> 4), l = lane & 15;
         const float *Ab = sA + ((blk * (blk + 1)) / 2 + blk) * L::A_BLK;
         float x[16];
 #pragma unroll
@@ -650,12 +654,12 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
         tb[1] = make_uint4(wb[4], wb[5], wb[6], wb[7]);
       }
       GDN_PHASE(3);
-      named_sync(kBar, 128);
+      named_sync(kBar, C::kPrepThreads);
       GDN_PHASE(4);
 
       // ---- M_ik = T_ii A_ik (i > k) on tf32 tensor cores, stored negated (bf16) ----
 #pragma unroll 1
-      for (int blk = pw; blk < 6; blk += 4) {
+      for (int blk = pw; blk < 6; blk += 6) {
         const int i = blk == 0 ? 1 : (blk < 3 ? 2 : 3);
         const int k = blk - (i * (i - 1)) / 2;
         // T_ii, column-major in the diagonal block of A: T(row, col) = T[col * A_LD + row]
@@ -685,18 +689,18 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
         }
       }
       GDN_PHASE(5);
-      named_sync(kBar, 128);
+      named_sync(kBar, C::kPrepThreads);
       mbar_arrive(bar(B_A_FREE + stage));  // A of this buffer is no longer read
       GDN_PHASE(6);
 
       // ---- block forward substitution, left-looking (a compact loop):
       // X_i = T_ii B_i + sum_{k<i} (-M_ik) X_k for X = [W | U~], B = [K | V] (the
       // beta, gamma scalings are folded into the T_ii tiles).  The 192 columns of
-      // [W | U~] go to the four warps as three 16-column pieces each.  A warp
+      // [W | U~] go to the six warps as two 16-column pieces each.  A warp
       // reads back only its own columns of the earlier block rows, so the levels
       // need no CTA-wide barrier. ----
       {
-        constexpr int NP = (DK + 64) / 64;  // 16-column pieces per warp
+        constexpr int NP = (DK + 64) / 16 / 6;  // 16-column pieces per warp
         const int arow = lrow + (lmi & 1) * 8, acol = (lmi >> 1) * 8;
         const int trow = lrow + (lmi >> 1) * 8, tcol = (lmi & 1) * 8;  // column-major T tiles
         uint32_t xt[NP], bsrc[NP];
@@ -808,10 +812,11 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
     float dh = 0.f;
     if constexpr (epi)
       if (p.d_skip) dh = p.d_skip[h];
-    auto output_chunk = [&](int c, int ocb, int nq) -> bool {
-        const int slot = c % NIN, buf = c & 1;
+    // gi: gamma_i (times r_q_i under the normalisation) and og: the output gate,
+    // both read from the slot before it was released
+    auto output_chunk = [&](int c, int ocb, int nq, float gi, float og) -> bool {
+        const int buf = c & 1;
         const int valid = valid_rows(c);
-        const float *gate = gate_ptr(slot);
         // ---- E2b: O = diag(gamma) (Q H) + P U (row = token); each thread
         // stores its row of O, value columns ocb .. ocb + 16 nq - 1 ----
         const size_t orow_idx = (size_t)(start + (int64_t)c * 64 + row) * H + h;
@@ -826,13 +831,7 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
         GDN_PHASE(1);
         tc_fence_after();
         {
-          float gi = ex2(gate[row]);  // gamma_i
           __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) + orow_idx * dv + col0;
-          // gamma_i r_q_i under the normalisation; the output gate staged by the producer
-          const float *rn = reinterpret_cast<const float *>(smem + L::OFF_RN) + slot * L::RN_SLOT;
-          float og = 1.f;
-          if constexpr ((kF & kFL2) != 0) gi *= rn[row];
-          if constexpr (epi) og = rn[128 + row];
           const uint64_t gi2 = pk2(gi, gi);
 #pragma unroll 1
           for (int q2 = ocb / 16; q2 < ocb / 16 + nq; ++q2) {
@@ -868,7 +867,6 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
           tc_fence_before();
           mbar_arrive(bar(B_D1_FREE + buf));
           mbar_arrive(bar(B_PU_FREE + buf));
-          mbar_arrive(bar(B_EMPTY_IN + slot));
         }
         return true;
     };
@@ -956,6 +954,11 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
               GDN_PROBE_AT(warp, c, 11, clock64());
               umma_commit(bar(B_PU_FULL + buf));
               umma_commit(bar(B_P_FREE + c % 3));
+              // MMA3 was the last reader of the slot's tiles (W, Q by MMA1 and
+              // U~ by E1 are done before it is issued); the output threads'
+              // arrivals cover the gate values.  No commit for the last NIN
+              // chunks: no slot reload waits on it.
+              if (c + NIN < nc) umma_commit(bar(B_EMPTY_IN + slot));
               GDN_PROBE_AT(warp, c, 5, clock64());
             }
           }
@@ -1013,6 +1016,22 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
       }
       for (int c = 0; c < nc && alive; ++c) {
         const int slot = c % NIN;
+        // The output threads read their per-token values of chunk c from the
+        // slot first and release it: gamma_i (times r_q_i under the
+        // normalisation) and the output gate.
+        float gi = 1.f, og = 1.f;
+        if (also_out) {
+          bool okin = role_wait(bar(B_FULL_IN + slot), (c / NIN) & 1, S, p, n, h, 24);
+          // r_q comes from the P drains: wait for the chunk's norms
+          if constexpr ((kF & kFL2) != 0)
+            if (okin) okin = role_wait(sbase + L::OFF_NBAR + 8 * (c & 1), (c >> 1) & 1, S, p, n, h, 25);
+          if (!__all_sync(0xffffffffu, okin)) break;
+          gi = ex2(gate_ptr(slot)[row]);
+          const float *rn = reinterpret_cast<const float *>(smem + L::OFF_RN) + slot * L::RN_SLOT;
+          if constexpr ((kF & kFL2) != 0) gi *= rn[row];
+          if constexpr (epi) og = rn[128 + row];
+          if (c + NIN < nc) mbar_arrive(bar(B_EMPTY_IN + slot));
+        }
         GDN_PHASE(3);
         bool ok = role_wait(bar(B_DH_FULL), c & 1, S, p, n, h, 12);
         if (!__all_sync(0xffffffffu, ok)) break;
@@ -1021,7 +1040,7 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
         bool pre = false;
         if (warp == C::kWarpE2aIssue && lane == 0 && c + 1 < nc) pre = mma1_pre(c + 1);
         {
-          const float gC = sgc[slot];
+          const float gC = sgc[c & 3];
           uint32_t w[32];
           tmem_ld32(tm(kColH + cb), w);
           tmem_wait_ld();
@@ -1035,7 +1054,6 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
         store_seg(Hs, hrow);
         fence_proxy_async_smem();
         mbar_arrive(bar(B_H_READY));
-        if (!also_out) mbar_arrive(bar(B_EMPTY_IN + slot));  // else after the output
         GDN_PHASE(5);
         if (warp == C::kWarpE2aIssue && c + 1 < nc) {
           if (lane == 0) {
@@ -1049,7 +1067,7 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
           alive = __shfl_sync(0xffffffffu, ok, 0);
           if (alive) issued = c + 2;
         }
-        if (also_out && alive && !output_chunk(c, cb, 2)) alive = false;
+        if (also_out && alive && !output_chunk(c, cb, 2, gi, og)) alive = false;
       }
       // the last MMA1 has completed before tensor memory is released
       if (warp == C::kWarpE2aIssue && lane == 0 && issued > 0)
@@ -1107,3 +1125,9 @@ cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t stream) {
 }
 
 }  // namespace gdn
+
+#ifdef GDN_PHASE_PROBE
+extern "C" int gdn_phase_probe_read_tc128(unsigned long long *host) {
+  return (int)cudaMemcpyFromSymbol(host, gdn::tc::g_phase_probe, sizeof(gdn::tc::g_phase_probe));
+}
+#endif
