@@ -795,6 +795,7 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
       bool ok = true;
       if (!pre && c >= 2)
         ok = role_wait(bar(B_D1_FREE + (c & 1)), ((c >> 1) - 1) & 1, S, p, n, h, 18);
+      GDN_PROBE_AT(warp, c, 12, clock64());
       if (ok && !pre) ok = role_wait(bar(B_FULL_ST + (c & 1)), (c >> 1) & 1, S, p, n, h, 16);
       GDN_PROBE_AT(warp, c, 8, clock64());
       if (ok) ok = role_wait(bar(B_H_READY), c & 1, S, p, n, h, 17);
@@ -944,6 +945,11 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
                           umma_desc_sw128_mn(Uds + kk * 2048, L::SUB), kIdescMM, kk > 0);
               GDN_PROBE_AT(warp, c, 9, clock64());
               umma_commit(bar(B_DH_FULL));
+              // MMA3 was the last reader of the slot's tiles (W, Q by MMA1 and
+              // U~ by E1 are done before it is issued; MMA2 reads P and U); the
+              // output threads' arrivals cover the gate values.  No commit for
+              // the last NIN chunks: no slot reload waits on it.
+              if (c + NIN < nc) umma_commit(bar(B_EMPTY_IN + slot));
               GDN_PROBE_AT(warp, c, 10, clock64());
               // MMA2: [*; P] U  (rows 64..127 = P U)
               const uint32_t ap = p_base(c % 3) - L::SUB;
@@ -954,11 +960,6 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
               GDN_PROBE_AT(warp, c, 11, clock64());
               umma_commit(bar(B_PU_FULL + buf));
               umma_commit(bar(B_P_FREE + c % 3));
-              // MMA3 was the last reader of the slot's tiles (W, Q by MMA1 and
-              // U~ by E1 are done before it is issued); the output threads'
-              // arrivals cover the gate values.  No commit for the last NIN
-              // chunks: no slot reload waits on it.
-              if (c + NIN < nc) umma_commit(bar(B_EMPTY_IN + slot));
               GDN_PROBE_AT(warp, c, 5, clock64());
             }
           }

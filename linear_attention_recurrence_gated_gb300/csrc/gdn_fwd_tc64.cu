@@ -761,6 +761,7 @@ gdn_fwd_tc64_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap_
       bool ok = true;
       if (!pre && c >= 2)
         ok = role_wait(bar(B_D1_FREE + (c & 1)), ((c >> 1) - 1) & 1, S, p, n, h, 18);
+      GDN_PROBE_AT(warp, c, 12, clock64());
       if (ok && !pre) ok = role_wait(bar(B_FULL_ST + (c & 1)), (c >> 1) & 1, S, p, n, h, 16);
       GDN_PROBE_AT(warp, c, 8, clock64());
       if (ok) ok = role_wait(bar(B_H_READY), c & 1, S, p, n, h, 17);
