@@ -227,6 +227,8 @@ KERNEL_SOURCES = {
     "simt_bf16": "gdn_fwd_simt.cu",
     "tc64_bf16": "gdn_fwd_tc64.cu",
     "tc128_bf16": "gdn_fwd_tc128.cu",
+    "tcc32_bf16": "gdn_fwd_tcc.cu",
+    "tcc128_bf16": "gdn_fwd_tcc.cu",
     "diag_bf16": "gdn_diag.cu",
     "diag_fp32": "gdn_diag.cu",
     "conv_bf16": "gdn_conv.cu",
@@ -371,9 +373,8 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
         d["final_state"] = torch.empty((N, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
         sets.append(d)
     ws = G.new_workspace(N, w.H, w.dk, w.dv, device=dev)
-    kname = G.gdn_fwd_kernel_name(w.dk, w.dv, host["q"].dtype, G.GDN_QK_L2NORM if fused else 0)
-    if args.chunk != CHUNK:   # other chunk sizes run on the fp32 CUDA-core kernel
-        kname = "simt_" + ("fp32" if w.dtype == "fp32" else "bf16")
+    kname = G.gdn_fwd_kernel_name(w.dk, w.dv, host["q"].dtype, G.GDN_QK_L2NORM if fused else 0,
+                                  chunk_size=args.chunk)
     stream = torch.cuda.current_stream(dev)
 
     def step(i, s=stream):
@@ -1152,7 +1153,8 @@ def main(argv=None):
     ap.add_argument("--pass", dest="pass_", choices=("fwd", "bwd"), default="fwd",
                     help="fwd: gdn_fwd; bwd: gdn_bwd (the prefill workloads)")
     ap.add_argument("--chunk", type=int, default=CHUNK, choices=(32, 64, 128),
-                    help="chunk size of gdn_fwd (32 and 128 run on the fp32 CUDA-core kernel)")
+                    help="chunk size of gdn_fwd (32 and 128: the tensor-core chunk-size variants "
+                         "for bf16 with head_dim_k 64)")
     ap.add_argument("--workload", default="hymo_bf16",
                     choices=sorted(W.WORKLOADS) + sorted(W.DECODE_WORKLOADS) +
                     sorted(W.DIAG_WORKLOADS) + sorted(W.CONV_WORKLOADS))

@@ -170,10 +170,11 @@ gdn_status gdn_workspace_init(void *workspace, size_t workspace_bytes, void *str
  * Supported sizes: head_dim_k in {32, 64, 128}; head_dim_v a multiple of 32
  * in [32, 256]; num_heads >= 1; num_seqs in [1, 65535]; chunk_size in {32,
  * 64, 128} except 128 with head_dim_k 128.  The result does not depend on
- * chunk_size beyond rounding; 64 is the pages' default and the only size the
- * tensor-core kernels take, so 32 and 128 always run on the fp32 CUDA-core
- * kernel (the pages sweep chunk_size over {32, 64, 128}: "v1.0 Architecture &
- * Design Spec", section 2.3).
+ * chunk_size beyond rounding; 64 is the pages' default.  With bf16 storage
+ * and head_dim_k 64, 32 and 128 run on tensor-core variants of their own
+ * (gdn_fwd_kernel_name_chunk names the kernel); other chunk sizes of other
+ * shapes run on the fp32 CUDA-core kernel (the pages sweep chunk_size over
+ * {32, 64, 128}: "v1.0 Architecture & Design Spec", section 2.3).
  * Anything else returns GDN_ERR_UNSUPPORTED (or INVALID_ARG if malformed).
  *
  * Aliasing: o and final_state must not overlap any input.  final_state may be
@@ -475,10 +476,16 @@ const char *gdn_status_string(int32_t status);
 
 /* Name of the kernel gdn_fwd would launch for these arguments with
  * chunk_size 64 ("simt_fp32", "simt_bf16", "tc64_bf16", "tc128_bf16") or NULL
- * when the arguments are unsupported.  Other chunk sizes always launch
- * "simt_fp32" / "simt_bf16".  Host only. */
+ * when the arguments are unsupported.  Host only. */
 const char *gdn_fwd_kernel_name(int32_t head_dim_k, int32_t head_dim_v,
                                 gdn_dtype dtype, uint32_t flags);
+
+/* The same for any chunk_size: "tcc32_bf16" / "tcc128_bf16" for the
+ * tensor-core chunk-size variants (bf16 storage, head_dim_k 64, chunk_size 32
+ * or 128), else the names above; NULL when the arguments are unsupported.
+ * Host only. */
+const char *gdn_fwd_kernel_name_chunk(int32_t head_dim_k, int32_t head_dim_v,
+                                      int32_t chunk_size, gdn_dtype dtype, uint32_t flags);
 
 #ifdef __cplusplus
 }

@@ -23,6 +23,10 @@ bool supported_dv(int dv) { return dv >= 32 && dv <= 256 && dv % 32 == 0; }
 bool use_tc(int dk, int dv, gdn_dtype dtype, uint32_t flags) {
   return dtype == GDN_BF16 && !(flags & GDN_FORCE_SIMT) && gdn::tc_supported(dk, dv);
 }
+// the tensor-core chunk-size variants (chunk_size 32 and 128)
+bool use_tcc(int chunk, int dk, int dv, gdn_dtype dtype, uint32_t flags) {
+  return dtype == GDN_BF16 && !(flags & GDN_FORCE_SIMT) && gdn::tcc_supported(chunk, dk, dv);
+}
 
 }  // namespace
 
@@ -136,12 +140,16 @@ gdn_status fwd_validate(const void *q, const void *k, const void *v, const float
 gdn_status fwd_launch(const FwdCall &call, cudaStream_t stream) {
   if (call.states_only)
     return call.p.sN ? pass_states(call.p.s0, call.p.sN, call.state_bytes, stream) : GDN_OK;
-  // the tensor-core kernels are built for 64-token chunks; other chunk sizes
-  // run on the fp32 CUDA-core kernel
+  // bf16 storage runs on the tensor-core kernels: the 64-token ones, or the
+  // chunk-size variants for 32 and 128; everything else on the fp32
+  // CUDA-core kernel
   const FwdParams &p = call.p;
-  const cudaError_t err = call.chunk == kChunk && use_tc(p.dk, p.dv, call.dtype, p.flags)
-                              ? launch_fwd_tc(p, stream)
-                              : launch_fwd_simt(p, call.dtype, call.chunk, stream);
+  const cudaError_t err =
+      call.chunk == kChunk && use_tc(p.dk, p.dv, call.dtype, p.flags)
+          ? launch_fwd_tc(p, stream)
+      : use_tcc(call.chunk, p.dk, p.dv, call.dtype, p.flags)
+          ? launch_fwd_tcc(p, call.chunk, stream)
+          : launch_fwd_simt(p, call.dtype, call.chunk, stream);
   return err == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 }  // namespace gdn
@@ -162,13 +170,21 @@ gdn_status gdn_workspace_init(void *workspace, size_t workspace_bytes, void *str
   return GDN_OK;
 }
 
-const char *gdn_fwd_kernel_name(int32_t head_dim_k, int32_t head_dim_v, gdn_dtype dtype,
-                                uint32_t flags) {
+const char *gdn_fwd_kernel_name_chunk(int32_t head_dim_k, int32_t head_dim_v,
+                                      int32_t chunk_size, gdn_dtype dtype, uint32_t flags) {
   if (!supported_dk(head_dim_k) || !supported_dv(head_dim_v)) return nullptr;
   if (dtype != GDN_F32 && dtype != GDN_BF16) return nullptr;
-  if (use_tc(head_dim_k, head_dim_v, dtype, flags))
+  if (!gdn::simt_chunk_supported(chunk_size, head_dim_k)) return nullptr;
+  if (chunk_size == gdn::kChunk && use_tc(head_dim_k, head_dim_v, dtype, flags))
     return head_dim_k == 64 ? "tc64_bf16" : "tc128_bf16";
+  if (use_tcc(chunk_size, head_dim_k, head_dim_v, dtype, flags))
+    return chunk_size == 32 ? "tcc32_bf16" : "tcc128_bf16";
   return dtype == GDN_F32 ? "simt_fp32" : "simt_bf16";
+}
+
+const char *gdn_fwd_kernel_name(int32_t head_dim_k, int32_t head_dim_v, gdn_dtype dtype,
+                                uint32_t flags) {
+  return gdn_fwd_kernel_name_chunk(head_dim_k, head_dim_v, gdn::kChunk, dtype, flags);
 }
 
 gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,

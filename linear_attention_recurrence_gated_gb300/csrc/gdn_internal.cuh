@@ -189,5 +189,8 @@ bool simt_chunk_supported(int chunk, int dk);   // chunk in {32, 64, 128}, not 1
 cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t stream);    // bf16 storage only
 cudaError_t launch_fwd_tc64(const FwdParams &p, cudaStream_t stream);  // bf16, head_dim_k 64
 bool tc_supported(int dk, int dv);
+// chunk_size 32 and 128 on the tensor cores: bf16, head_dim_k 64
+bool tcc_supported(int chunk, int dk, int dv);
+cudaError_t launch_fwd_tcc(const FwdParams &p, int chunk, cudaStream_t stream);
 
 }  // namespace gdn

@@ -133,13 +133,15 @@ inline int64_t tmap_rows(const FwdParams &p, int64_t tokens, int64_t extent, int
   return r < 1 ? 1 : r < tokens ? r : tokens;
 }
 
-// [tokens][heads][cols] bf16 viewed as a 3-D tensor; box = 64 cols x 1 head x 64 tokens.
-inline bool make_tmap(CUtensorMap *m, const void *ptr, int cols, int heads, int64_t tokens) {
+// [tokens][heads][cols] bf16 viewed as a 3-D tensor; box = 64 cols x 1 head x
+// box_rows tokens (the chunk: 64, or 32 / 128 for the chunk-size variants).
+inline bool make_tmap(CUtensorMap *m, const void *ptr, int cols, int heads, int64_t tokens,
+                      int box_rows = 64) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)heads, (cuuint64_t)tokens};
   const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * heads * 2};
-  const cuuint32_t box[3] = {64, 1, 64};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -38,7 +38,8 @@ CHUNK_SIZE = 64
 EXPORTED = ("gdn_fwd_workspace_size", "gdn_workspace_init", "gdn_fwd", "gdn_check",
             "gdn_status_string", "gdn_fwd_kernel_name", "gdn_fwd_static_scratch",
             "gdn_decode", "gdn_diag_workspace_size", "gdn_diag_fwd", "gdn_conv_silu",
-            "gdn_bwd_workspace_size", "gdn_bwd", "gdn_fwd_debug", "gdn_check_record")
+            "gdn_bwd_workspace_size", "gdn_bwd", "gdn_fwd_debug", "gdn_check_record",
+            "gdn_fwd_kernel_name_chunk")
 # ... and include/gdn_debug.h (self-tests of the failure reporting).
 DEBUG_EXPORTED = ("gdn_debug_wait_timeout",)
 
@@ -86,6 +87,8 @@ def lib() -> ctypes.CDLL:
             L.gdn_status_string.argtypes = [i32]
             L.gdn_fwd_kernel_name.restype = ctypes.c_char_p
             L.gdn_fwd_kernel_name.argtypes = [i32, i32, ctypes.c_int, u32]
+            L.gdn_fwd_kernel_name_chunk.restype = ctypes.c_char_p
+            L.gdn_fwd_kernel_name_chunk.argtypes = [i32, i32, i32, ctypes.c_int, u32]
             L.gdn_fwd_static_scratch.restype = ctypes.c_int
             L.gdn_fwd_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                  i32, i32, i32, i32, i32, i32, i32,
@@ -179,8 +182,10 @@ def gdn_debug_wait_timeout(workspace: torch.Tensor, stream=None) -> int:
                                             _stream_handle(stream)))
 
 
-def gdn_fwd_kernel_name(head_dim_k, head_dim_v, dtype: torch.dtype, flags: int = 0):
-    r = lib().gdn_fwd_kernel_name(head_dim_k, head_dim_v, _dtype_code(dtype), flags)
+def gdn_fwd_kernel_name(head_dim_k, head_dim_v, dtype: torch.dtype, flags: int = 0,
+                        chunk_size: int = CHUNK_SIZE):
+    r = lib().gdn_fwd_kernel_name_chunk(head_dim_k, head_dim_v, chunk_size, _dtype_code(dtype),
+                                        flags)
     return None if r is None else r.decode()
 
 

@@ -75,6 +75,16 @@ def test_kernel_names(L):
     assert G.gdn_fwd_kernel_name(64, 64, torch.bfloat16, G.GDN_QK_L2NORM) == "tc64_bf16"
     assert G.gdn_fwd_kernel_name(128, 128, torch.bfloat16, G.GDN_QK_L2NORM) == "tc128_bf16"
     assert G.gdn_fwd_kernel_name(64, 64, torch.bfloat16, G.GDN_FORCE_SIMT) == "simt_bf16"
+    # chunk sizes 32 and 128: tensor-core variants for bf16 with head_dim_k 64
+    assert G.gdn_fwd_kernel_name(64, 64, torch.bfloat16, chunk_size=32) == "tcc32_bf16"
+    assert G.gdn_fwd_kernel_name(64, 128, torch.bfloat16, chunk_size=128) == "tcc128_bf16"
+    assert G.gdn_fwd_kernel_name(64, 64, torch.bfloat16, G.GDN_QK_L2NORM, chunk_size=32) == "tcc32_bf16"
+    assert G.gdn_fwd_kernel_name(128, 128, torch.bfloat16, chunk_size=32) == "simt_bf16"
+    assert G.gdn_fwd_kernel_name(64, 96, torch.bfloat16, chunk_size=128) == "simt_bf16"
+    assert G.gdn_fwd_kernel_name(64, 64, torch.float32, chunk_size=32) == "simt_fp32"
+    assert G.gdn_fwd_kernel_name(64, 64, torch.bfloat16, G.GDN_FORCE_SIMT, chunk_size=128) == "simt_bf16"
+    assert G.gdn_fwd_kernel_name(64, 64, torch.bfloat16, chunk_size=16) is None
+    assert G.gdn_fwd_kernel_name(128, 128, torch.bfloat16, chunk_size=128) is None
 
 
 # ---- host-side validation with fake (never dereferenced) device addresses ----

@@ -31,6 +31,28 @@ def _setup():
 CASES = [(4, 200, 2, 64, 64, "bf16"), (3, 130, 2, 128, 128, "bf16"), (3, 100, 2, 64, 64, "fp32")]
 
 
+@pytest.mark.parametrize("chunk", [32, 128])
+def test_debug_checks_on_the_chunk_variants(chunk):
+    """The chunk-size variants run the same range checks: results unchanged
+    with the checks on, and an undersized q extent caught for sequences 2.."""
+    B, T, H, dk, dv = 4, 150, 2, 64, 64
+    inp = make(B, T, H, dk, dv, "bf16")
+    d = parity.to_dev(inp)
+    o0, s0 = G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"], None,
+                       chunk_size=chunk, check=True)
+    o1, s1 = G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"], None,
+                       chunk_size=chunk, check=True, debug_checks=True)
+    assert torch.equal(o0, o1) and torch.equal(s0, s1)
+    o, s = outputs_like(d, B, H, dk, dv)
+    ws = G.new_workspace(B, H, dk, dv)
+    assert G.gdn_fwd_debug(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"], None,
+                           o, s, ws, declared=dict(q=2 * T * H * dk),
+                           chunk_size=chunk) == G.GDN_OK
+    st, seq, head, site = G.gdn_check_record(ws)
+    assert st == G.GDN_ERR_DEVICE_CHECK and seq >= 2 and site == SITE["q"]
+    assert torch.equal(o[:2], o0[:2]) and torch.isnan(o[2:].float()).all()
+
+
 def make(B, T, H, dk, dv, dtype, seed=11, varlen=None):
     if varlen is None:
         w = W.custom(name="dbg", B=B, T=T, H=H, dk=dk, dv=dv, dtype=dtype, init_state=True,

@@ -183,7 +183,8 @@ def test_bad_seqlens_reported(cu):
     assert G.gdn_check(ws) == 0  # the check cleared the status word
 
 
-# ---------------- chunk-size variants (32 and 128, fp32 CUDA-core kernel) ----------------
+# ---------------- chunk-size variants (32 and 128: the tensor-core variants for bf16
+# with head_dim_k 64 and dv a multiple of 64, the fp32 CUDA-core kernel otherwise) ----------------
 CHUNK_SHAPES = [(1, 1, 1, 32, 32), (2, 31, 2, 64, 64), (1, 32, 1, 32, 64), (1, 33, 2, 64, 32),
                 (2, 127, 2, 32, 96), (1, 128, 1, 64, 64), (1, 129, 2, 64, 128),
                 (2, 300, 3, 128, 64), (1, 1000, 1, 64, 64)]
