@@ -362,8 +362,15 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
         host = dict(host, q=ex["q_raw"], k=ex["k_raw"], beta=ex["beta_logits"],
                     D_skip=ex["D_skip"], out_gate=ex["out_gate"])
         names = names + ("D_skip", "out_gate")
-    fkw = lambda d: dict(D_skip=d["D_skip"], out_gate=d["out_gate"], beta_logits=True,  # noqa: E731
-                         qk_l2norm=True) if fused else {}
+    split = getattr(args, "seq_split", False)
+    segments = 1
+    if split:
+        segments = G.gdn_fwd_split_segments(N, host["q"].shape[1], w.H, w.dk, w.dv,
+                                            host["q"].dtype, G.GDN_SEQ_SPLIT, args.chunk,
+                                            varlen=host["cu_seqlens"] is not None)
+    fkw = lambda d: dict(  # noqa: E731
+        **(dict(D_skip=d["D_skip"], out_gate=d["out_gate"], beta_logits=True, qk_l2norm=True)
+           if fused else {}), **(dict(seq_split=True) if split else {}))
     sets = []
     for _ in range(2):  # two resident input sets, alternated between steps
         d = {n: host[n].to(dev) for n in names}
@@ -372,7 +379,7 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
         d["o"] = torch.empty_like(d["v"])
         d["final_state"] = torch.empty((N, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
         sets.append(d)
-    ws = G.new_workspace(N, w.H, w.dk, w.dv, device=dev)
+    ws = G.new_workspace(N, w.H, w.dk, w.dv, G.GDN_SEQ_SPLIT if split else 0, device=dev)
     kname = G.gdn_fwd_kernel_name(w.dk, w.dv, host["q"].dtype, G.GDN_QK_L2NORM if fused else 0,
                                   chunk_size=args.chunk)
     stream = torch.cuda.current_stream(dev)
@@ -413,7 +420,7 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
 
     local_ms = t_start.elapsed_time(t_end)
     total_ms = max_over_ranks(local_ms, world)
-    per_launch_ms = local_ms / args.steps   # one gdn_fwd launch per step
+    per_launch_ms = local_ms / args.steps   # one gdn_fwd call per step
     value = tokens * world * args.steps / (total_ms / 1e3)
 
     # ---- end to end: pinned host inputs -> device -> gdn_fwd -> host result ----
@@ -510,6 +517,12 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
                    "storage": w.dtype, "chunk": args.chunk, "kernel": kname,
                    **({"fused": "q/k L2 norm + beta logits (sigmoid) + (o + D v) * out_gate "
                                 "epilogue in the kernel"} if fused else {}),
+                   **({"seq_split": f"GDN_SEQ_SPLIT: {segments} segment(s) per sequence"
+                                    + (" (first launch: segment 0 + the middle segments' state "
+                                       "maps; compose; second launch: segments 1..; kernel_ms "
+                                       "is the whole call)" if segments > 1 else
+                                       " (not split: the units fill the SMs)")}
+                      if split else {}),
                    "l2": "two resident input sets of "
                          f"{sum(sets[0][n].numel() * sets[0][n].element_size() for n in names) / 1e6:.0f}"
                          " MB each (> 129 MB L2) alternate between steps",
@@ -529,7 +542,8 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "overlap": "two device sets: step i+1's inputs copy in while step i "
                            "computes and step i-1's result copies out"},
-        "gpu_launches": args.steps * launches_per_step(kname),
+        # a split call launches the first pass, the composition and the second pass
+        "gpu_launches": args.steps * (3 if segments > 1 else launches_per_step(kname)),
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
@@ -1160,6 +1174,9 @@ def main(argv=None):
                     sorted(W.DIAG_WORKLOADS) + sorted(W.CONV_WORKLOADS))
     ap.add_argument("--eager", action="store_true",
                     help="time the steps launched one by one instead of as one CUDA graph")
+    ap.add_argument("--seq-split", action="store_true",
+                    help="fwd: GDN_SEQ_SPLIT (dense head_dim_k 128 sequences cut into segments "
+                         "computed in parallel when units alone leave SMs idle)")
     ap.add_argument("--fused", action="store_true",
                     help="fwd: raw q/k normalised in-kernel, beta as logits and the block "
                          "epilogue (o + D v) * out_gate, all fused into gdn_fwd")

@@ -102,11 +102,24 @@ enum {
    * branch for it.  The pages' kernel asserts its inputs and raises instead of
    * falling back ("Optimization Quartet", Triton GDN kernel sections 3.3 and
    * 3.5); this is the device-side counterpart. */
-  GDN_DEBUG_CHECKS = 1u << 4
+  GDN_DEBUG_CHECKS = 1u << 4,
+  /* gdn_fwd: let the head_dim_k 128 tensor-core kernel cut each sequence of a
+   * dense call (cu_seqlens NULL) into up to 3 segments of whole chunks when
+   * the (sequence, head, 64 value columns) units alone leave SMs idle.  The
+   * chunk transition is affine in the state, H' = M H + X, so a segment's
+   * transition composes its chunks' ones: a first launch runs segment 0 and,
+   * at the same time, the middle segments from a zero state with dk extra
+   * identity columns (giving their X and M); a small kernel composes the
+   * segments' entry states; a second launch runs segments 1.. from them and
+   * writes the outputs.  The result equals the unsplit one up to rounding.
+   * The workspace must be sized with this flag (gdn_fwd_workspace_size).
+   * Other calls ignore the flag. */
+  GDN_SEQ_SPLIT = 1u << 5
 };
 
 /* Bytes of device workspace gdn_fwd needs for these sizes (>= 256; the first
- * 256 bytes hold the device status word).  Never fails; returns 0 only for
+ * 256 bytes hold the device status word; with GDN_SEQ_SPLIT and head_dim_k
+ * 128, the segments' states and maps follow).  Never fails; returns 0 only for
  * nonsensical sizes (any argument <= 0). */
 size_t gdn_fwd_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_dim_k,
                               int32_t head_dim_v, uint32_t flags);
@@ -165,7 +178,8 @@ gdn_status gdn_workspace_init(void *workspace, size_t workspace_bytes, void *str
  * with GDN_BETA_LOGITS as sigmoid(beta input).  The state element (i, j) of
  * H = S^T multiplies key dimension i and value dimension j.
  *
- * flags: any of GDN_QK_L2NORM, GDN_BETA_LOGITS, GDN_FORCE_SIMT, GDN_DEBUG_CHECKS.
+ * flags: any of GDN_QK_L2NORM, GDN_BETA_LOGITS, GDN_FORCE_SIMT, GDN_DEBUG_CHECKS,
+ * GDN_SEQ_SPLIT.
  *
  * Supported sizes: head_dim_k in {32, 64, 128}; head_dim_v a multiple of 32
  * in [32, 256]; num_heads >= 1; num_seqs in [1, 65535]; chunk_size in {32,
@@ -198,6 +212,17 @@ gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
                    int32_t head_dim_k, int32_t head_dim_v, int32_t num_seqs,
                    int32_t chunk_size, gdn_dtype dtype, uint32_t flags,
                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* The number of segments GDN_SEQ_SPLIT cuts each sequence of a gdn_fwd call
+ * with these arguments into, on the current device (the plan depends on its
+ * SM count): 3 or more when the call is split, and then gdn_fwd launches
+ * three kernels (segment 0 with the middle segments' maps, their
+ * composition, the later segments); 1 when it is not split (one kernel).
+ * varlen != 0 stands for a call with cu_seqlens (never split).  Returns 0
+ * for sizes gdn_fwd rejects.  Host only; launches nothing. */
+int32_t gdn_fwd_split_segments(int32_t num_seqs, int32_t seq_len, int32_t num_heads,
+                               int32_t head_dim_k, int32_t head_dim_v, int32_t chunk_size,
+                               gdn_dtype dtype, uint32_t flags, int32_t varlen);
 
 /* Elements (not bytes) each buffer of a forward call holds, for
  * gdn_fwd_debug.  A field of a NULL buffer is ignored. */

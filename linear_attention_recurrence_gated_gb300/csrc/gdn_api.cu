@@ -61,7 +61,8 @@ gdn_status fwd_validate(const void *q, const void *k, const void *v, const float
       num_seqs <= 0)
     return GDN_ERR_INVALID_ARG;
   if (dtype != GDN_F32 && dtype != GDN_BF16) return GDN_ERR_INVALID_ARG;
-  if (flags & ~(uint32_t)(GDN_QK_L2NORM | GDN_FORCE_SIMT | GDN_BETA_LOGITS | GDN_DEBUG_CHECKS))
+  if (flags & ~(uint32_t)(GDN_QK_L2NORM | GDN_FORCE_SIMT | GDN_BETA_LOGITS | GDN_DEBUG_CHECKS |
+                          GDN_SEQ_SPLIT))
     return GDN_ERR_INVALID_ARG;
   if (cu_seqlens ? batch != 1 : num_seqs != batch) return GDN_ERR_INVALID_ARG;
   if (!supported_dk(head_dim_k) || !supported_dv(head_dim_v)) return GDN_ERR_UNSUPPORTED;
@@ -136,6 +137,24 @@ gdn_status fwd_validate(const void *q, const void *k, const void *v, const float
   return GDN_OK;
 }
 
+// The split plan of GDN_SEQ_SPLIT: fills p.seg_len / p.seg_count (0 when
+// the call is not split) and returns the segment count (1: not split).
+int plan_segments(FwdParams &p, int chunk, gdn_dtype dtype) {
+  p.seg_len = p.seg_count = 0;
+  if (!(p.flags & GDN_SEQ_SPLIT) || chunk != kChunk || !use_tc(p.dk, p.dv, dtype, p.flags))
+    return 1;
+  // cut each sequence into segments of whole chunks, computed in parallel
+  const int s = seq_split_segments(p);
+  if (s < 3) return 1;
+  const int64_t chunks = (p.seq_len + kChunk - 1) / kChunk;
+  const int64_t seg_len = ((chunks + s - 1) / s) * kChunk;
+  const int64_t count = (p.seq_len + seg_len - 1) / seg_len;
+  if (count < 3 || count > kMaxSegments) return 1;
+  p.seg_len = (int32_t)seg_len;
+  p.seg_count = (int32_t)count;
+  return p.seg_count;
+}
+
 // Enqueue the kernels of a call that fwd_validate accepted.
 gdn_status fwd_launch(const FwdCall &call, cudaStream_t stream) {
   if (call.states_only)
@@ -143,7 +162,16 @@ gdn_status fwd_launch(const FwdCall &call, cudaStream_t stream) {
   // bf16 storage runs on the tensor-core kernels: the 64-token ones, or the
   // chunk-size variants for 32 and 128; everything else on the fp32
   // CUDA-core kernel
-  const FwdParams &p = call.p;
+  FwdParams p = call.p;
+  if (plan_segments(p, call.chunk, call.dtype) > 1) {
+    // the segments' states, X and M follow the status record in the workspace
+    float *base = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(p.status) +
+                                            kStatusBytes);
+    const size_t vals = (size_t)p.num_seqs * kMaxSegments * p.num_heads * p.dk * p.dv;
+    p.seg_state = base;
+    p.seg_x = base + vals;
+    p.seg_m = base + 2 * vals;
+  }
   const cudaError_t err =
       call.chunk == kChunk && use_tc(p.dk, p.dv, call.dtype, p.flags)
           ? launch_fwd_tc(p, stream)
@@ -158,9 +186,32 @@ extern "C" {
 
 size_t gdn_fwd_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_dim_k,
                               int32_t head_dim_v, uint32_t flags) {
-  (void)flags;
   if (num_seqs <= 0 || num_heads <= 0 || head_dim_k <= 0 || head_dim_v <= 0) return 0;
-  return gdn::kStatusBytes;
+  size_t bytes = gdn::kStatusBytes;
+  if ((flags & GDN_SEQ_SPLIT) && head_dim_k == 128)  // per segment: a state, X and M
+    bytes += (size_t)4 * num_seqs * gdn::kMaxSegments * num_heads * head_dim_k *
+             (2 * (size_t)head_dim_v + head_dim_k);
+  return bytes;
+}
+
+int32_t gdn_fwd_split_segments(int32_t num_seqs, int32_t seq_len, int32_t num_heads,
+                               int32_t head_dim_k, int32_t head_dim_v, int32_t chunk_size,
+                               gdn_dtype dtype, uint32_t flags, int32_t varlen) {
+  if (num_seqs < 1 || num_seqs > 65535 || seq_len < 0 || num_heads < 1 ||
+      !supported_dk(head_dim_k) || !supported_dv(head_dim_v) ||
+      (dtype != GDN_F32 && dtype != GDN_BF16) ||
+      !gdn::simt_chunk_supported(chunk_size, head_dim_k))
+    return 0;
+  gdn::FwdParams p{};
+  p.num_seqs = num_seqs;
+  p.seq_len = seq_len;
+  p.num_heads = num_heads;
+  p.dk = head_dim_k;
+  p.dv = head_dim_v;
+  p.flags = flags;
+  static const int32_t kNonNull = 0;
+  p.cu = varlen ? &kNonNull : nullptr;  // only its presence is read
+  return gdn::plan_segments(p, chunk_size, dtype);
 }
 
 gdn_status gdn_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {

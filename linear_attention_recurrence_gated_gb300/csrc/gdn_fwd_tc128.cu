@@ -276,7 +276,8 @@ __device__ __noinline__ void drain_s_row(uint32_t taddr, const float *G2, const 
   }
 }
 
-constexpr int kFL2 = 1, kFEpi = 2;
+// kFSeg: one segment of a split sequence (launched only by the split plan)
+constexpr int kFL2 = 1, kFEpi = 2, kFSeg = 4;
 
 template <int kF>
 __global__ void __launch_bounds__(Cfg::kWarps * 32, 1)
@@ -293,13 +294,32 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
   const uint32_t sbase = raw + pad;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tile = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
-  const int H = p.num_heads, dv = p.dv, col0 = tile * kDvt;
+  const int tile = blockIdx.x, h = blockIdx.y;
+  const int H = p.num_heads, dv = p.dv;
 
+  // The unit: a whole sequence, or one segment of a split sequence (dense
+  // inputs).  A transport segment also has dk/64 extra column tiles that carry
+  // the identity through the segment's chunks (its state map's M).
+  constexpr bool segm = (kF & kFSeg) != 0;
+  int n = blockIdx.z, seg = 0;
+  bool transport = false;
   int64_t start, len;
-  if (!sequence_bounds(p, n, h, start, len)) return;  // uniform over the CTA
+  if constexpr (segm) {
+    n = blockIdx.z / p.seg_launch;
+    seg = p.seg_first + blockIdx.z % p.seg_launch;
+    transport = seg >= p.seg_transport;
+    start = (int64_t)n * p.seq_len + (int64_t)seg * p.seg_len;
+    const int64_t rest = p.seq_len - (int64_t)seg * p.seg_len;  // > 0 by construction
+    len = rest < p.seg_len ? rest : p.seg_len;
+  } else {
+    if (!sequence_bounds(p, n, h, start, len)) return;  // uniform over the CTA
+  }
+  const bool mtile = segm && tile * kDvt >= dv;  // a transport column tile
+  if (mtile && !transport) return;
+  // value columns col0.. of v, o and the states, or transport columns col0..
+  const int col0 = mtile ? tile * kDvt - dv : tile * kDvt;
   if ((p.flags & GDN_DEBUG_CHECKS) &&
-      !debug_ranges_ok(p, n, h, start, len, col0, kDvt, 2, true))
+      !debug_ranges_ok(p, n, h, start, len, mtile ? 0 : col0, kDvt, 2, true))
     return;  // recorded; nothing was accessed
   if (len == 0) {   // an empty sequence: the state passes through
     pass_state_through(p, n, h, col0, kDvt);
@@ -348,6 +368,12 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
     *S.abort_flag = 0;
     fence_mbar_init();
   }
+  if (mtile) {  // V = 0 on the transport columns (no load ever writes these tiles)
+    for (int idx = tid; idx < NIN * (L::SUB / 16); idx += C::kWarps * 32) {
+      const int sl = idx / (L::SUB / 16), q = idx % (L::SUB / 16);
+      reinterpret_cast<uint4 *>(smem + L::OFF_IN + sl * L::SLOT + L::SV)[q] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
   if (warp == C::kWarpSIssue) tmem_alloc(sbase + L::OFF_TMEM, kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -391,7 +417,7 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
       }
     };
     load_gates(0);
-    constexpr uint32_t kTx = (2 * NG + 1) * L::SUB;
+    const uint32_t kTx = (2 * NG + (mtile ? 0 : 1)) * L::SUB;
     int issued = 0;
     for (int c = 0; c < nc; ++c) {
       const int slot = c % NIN;
@@ -440,7 +466,7 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
           tma_load_3d(sb + g * L::GSTRIDE + L::SQ, &tmap_q, 64 * g, h, row, bar(B_FULL_IN + slot));
           tma_load_3d(sb + g * L::GSTRIDE + L::SK, &tmap_k, 64 * g, h, row, bar(B_FULL_IN + slot));
         }
-        tma_load_3d(sb + L::SV, &tmap_v, col0, h, row, bar(B_FULL_IN + slot));
+        if (!mtile) tma_load_3d(sb + L::SV, &tmap_v, col0, h, row, bar(B_FULL_IN + slot));
         if (c + NIN < nc) {  // warm L2 with the tiles of the chunk that reuses this slot
           const int prow = row + NIN * 64;
 #pragma unroll
@@ -448,7 +474,7 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
             tma_prefetch_3d(&tmap_q, 64 * g, h, prow);
             tma_prefetch_3d(&tmap_k, 64 * g, h, prow);
           }
-          tma_prefetch_3d(&tmap_v, col0, h, prow);
+          if (!mtile) tma_prefetch_3d(&tmap_v, col0, h, prow);
         }
       }
       GDN_PHASE(2);
@@ -821,8 +847,9 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
         // ---- E2b: O = diag(gamma) (Q H) + P U (row = token); each thread
         // stores its row of O, value columns ocb .. ocb + 16 nq - 1 ----
         const size_t orow_idx = (size_t)(start + (int64_t)c * 64 + row) * H + h;
+        const bool st = row < valid && !transport;  // (a transport segment stores no output)
         const __nv_bfloat16 *vrow = static_cast<const __nv_bfloat16 *>(p.v) + orow_idx * dv + col0;
-        if (epi && row < valid) {  // v is reloaded (its tile now holds U~)
+        if (epi && st) {  // v is reloaded (its tile now holds U~)
           prefetch_l1(vrow + ocb);
           prefetch_l1(vrow + ocb + 16 * nq - 1);
         }
@@ -846,7 +873,7 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
               w8[e] = pack_bf16x2(fma2(gi2, pk2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1])),
                                        pk2(__uint_as_float(b[2 * e]), __uint_as_float(b[2 * e + 1]))));
             if constexpr (epi) {
-              if (row < valid) {
+              if (st) {
                 const uint4 v0 = reinterpret_cast<const uint4 *>(vrow + 16 * q2)[0];
                 const uint4 v1 = reinterpret_cast<const uint4 *>(vrow + 16 * q2)[1];
                 const uint32_t vw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -860,7 +887,7 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
                 }
               }
             }
-            if (row < valid) {
+            if (st) {
               reinterpret_cast<uint4 *>(orow + 16 * q2)[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
               reinterpret_cast<uint4 *>(orow + 16 * q2)[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
             }
@@ -982,6 +1009,9 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
       const bool also_out = wq >= 2;
       const size_t state_row =
           ((size_t)n * H + h) * (size_t)DK * dv + (size_t)krow * dv + col0 + cb;
+      // a split sequence's per-segment arrays: [N][seg_count][H][dk][dv or dk]
+      const size_t unit = ((size_t)n * p.seg_count + seg) * H + h;
+      const size_t seg_row = unit * DK * dv + (size_t)krow * dv + col0 + cb;
       float hrow[32];
       auto store_seg = [&](uint32_t tilebase, const float *x) {
 #pragma unroll
@@ -990,14 +1020,25 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
               make_uint4(pack_bf16(x[8 * q], x[8 * q + 1]), pack_bf16(x[8 * q + 2], x[8 * q + 3]),
                          pack_bf16(x[8 * q + 4], x[8 * q + 5]), pack_bf16(x[8 * q + 6], x[8 * q + 7]));
       };
+      // the initial state: the caller's (whole sequence, first segment), the
+      // composed one of a later segment, zero (a transport segment's value
+      // columns) or the identity (its transport columns)
+      const float *s_in = transport ? nullptr
+                          : seg > 0 ? p.seg_state + seg_row
+                          : p.s0    ? p.s0 + state_row
+                                    : nullptr;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (p.s0) v4 = *reinterpret_cast<const float4 *>(p.s0 + state_row + 4 * q);
+        if (s_in) v4 = *reinterpret_cast<const float4 *>(s_in + 4 * q);
         hrow[4 * q] = v4.x;
         hrow[4 * q + 1] = v4.y;
         hrow[4 * q + 2] = v4.z;
         hrow[4 * q + 3] = v4.w;
+      }
+      if (mtile) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) hrow[j] = (krow == col0 + cb + j) ? 1.f : 0.f;
       }
       store_seg(Hs, hrow);
       fence_proxy_async_smem();
@@ -1074,10 +1115,17 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
       if (warp == C::kWarpE2aIssue && lane == 0 && issued > 0)
         mbar_wait_bounded(bar(B_D1_FULL + ((issued - 1) & 1)), ((issued - 1) >> 1) & 1,
                           kWaitTimeoutNs);
-      if (p.sN && !*S.abort_flag) {
+      // the final state: the caller's (whole or last segment), the next
+      // segment's initial state, or a transport segment's X / M
+      float *s_out = nullptr;
+      if (mtile) s_out = p.seg_m + unit * DK * DK + (size_t)krow * DK + col0 + cb;
+      else if (transport) s_out = p.seg_x + seg_row;
+      else if (!segm || seg == p.seg_count - 1) s_out = p.sN ? p.sN + state_row : nullptr;
+      else if (p.seg_write_next) s_out = p.seg_state + seg_row + (size_t)H * DK * dv;  // segment seg + 1
+      if (s_out && !*S.abort_flag) {
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<float4 *>(p.sN + state_row + 4 * q) =
+          *reinterpret_cast<float4 *>(s_out + 4 * q) =
               make_float4(hrow[4 * q], hrow[4 * q + 1], hrow[4 * q + 2], hrow[4 * q + 3]);
       }
     }
@@ -1087,6 +1135,27 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
   if (warp == C::kWarpSIssue) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// H_(s+1) = M_s H_s + X_s for s = 1 .. S-2, per (sequence, head) and 32 value
+// columns, in fp32 (one CTA walks the segments in order; M_s is dk x dk).
+__global__ void __launch_bounds__(256) seg_compose_kernel(const FwdParams p) {
+  const int c0 = blockIdx.x * 32, h = blockIdx.y, n = blockIdx.z;
+  const int H = p.num_heads, dv = p.dv, S = p.seg_count;
+  for (int s = 1; s + 1 < S; ++s) {
+    const size_t unit = ((size_t)n * S + s) * H + h;
+    const float *M = p.seg_m + unit * DK * DK;
+    const float *Hs = p.seg_state + unit * DK * dv;
+    const float *X = p.seg_x + unit * DK * dv;
+    float *Hn = p.seg_state + (unit + H) * DK * dv;  // segment s + 1
+    for (int idx = threadIdx.x; idx < DK * 32; idx += blockDim.x) {
+      const int r = idx >> 5, c = c0 + (idx & 31);
+      float acc = X[(size_t)r * dv + c];
+      for (int k = 0; k < DK; ++k) acc = fmaf(M[(size_t)r * DK + k], Hs[(size_t)k * dv + c], acc);
+      Hn[(size_t)r * dv + c] = acc;
+    }
+    __syncthreads();  // the next segment reads what this one wrote (this CTA's columns only)
   }
 }
 
@@ -1100,22 +1169,83 @@ cudaError_t launch_tc128(const FwdParams &p, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   // the block parts fused into the pass run in their own instantiation, so
   // the plain pass carries none of their code
-  const int feat = ((p.flags & GDN_QK_L2NORM) ? kFL2 : 0) | ((p.d_skip || p.out_gate) ? kFEpi : 0);
-  auto kern = feat == 0             ? gdn_fwd_tc128_kernel<0>
-              : feat == kFL2        ? gdn_fwd_tc128_kernel<kFL2>
-              : feat == kFEpi       ? gdn_fwd_tc128_kernel<kFEpi>
-                                    : gdn_fwd_tc128_kernel<kFL2 | kFEpi>;
+  using Kern = decltype(&gdn_fwd_tc128_kernel<0>);
+  const Kern inst[8] = {gdn_fwd_tc128_kernel<0>,
+                        gdn_fwd_tc128_kernel<kFL2>,
+                        gdn_fwd_tc128_kernel<kFEpi>,
+                        gdn_fwd_tc128_kernel<kFL2 | kFEpi>,
+                        gdn_fwd_tc128_kernel<kFSeg>,
+                        gdn_fwd_tc128_kernel<kFSeg | kFL2>,
+                        gdn_fwd_tc128_kernel<kFSeg | kFEpi>,
+                        gdn_fwd_tc128_kernel<kFSeg | kFL2 | kFEpi>};
+  const int feat = ((p.flags & GDN_QK_L2NORM) ? kFL2 : 0) | ((p.d_skip || p.out_gate) ? kFEpi : 0) |
+                   (p.seg_len > 0 ? kFSeg : 0);
+  const Kern kern = inst[feat];
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (err != cudaSuccess) return err;
-  const dim3 grid(p.dv / kDvt, p.num_heads, p.num_seqs);
-  kern<<<grid, Cfg::kWarps * 32, L::ALLOC, stream>>>(p, tq, tk, tv);
+  if (p.seg_len == 0) {
+    const dim3 grid(p.dv / kDvt, p.num_heads, p.num_seqs);
+    kern<<<grid, Cfg::kWarps * 32, L::ALLOC, stream>>>(p, tq, tk, tv);
+    return cudaGetLastError();
+  }
+  // A split sequence (the segments' affine state maps H -> M H + X, composed
+  // in order; "Optimization Quartet", Triton GDN kernel section 3.2, names the
+  // inter-chunk carry as the serial part of the chunked form):
+  //   1. segment 0 as usual, writing the state that enters segment 1; at the
+  //      same time segments 1 .. S-2 in transport mode (X and M);
+  //   2. the composition H_(s+1) = M_s H_s + X_s for s = 1 .. S-2;
+  //   3. segments 1 .. S-1 from their composed states, writing the outputs
+  //      and, for the last one, the caller's final state.
+  const int S = p.seg_count;
+  FwdParams a = p;
+  a.seg_first = 0;
+  a.seg_launch = S - 1;
+  a.seg_transport = 1;
+  a.seg_write_next = 1;
+  const dim3 grid_a(p.dv / kDvt + (S > 2 ? DK / kDvt : 0), p.num_heads, p.num_seqs * (S - 1));
+  kern<<<grid_a, Cfg::kWarps * 32, L::ALLOC, stream>>>(a, tq, tk, tv);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (S > 2) {
+    seg_compose_kernel<<<dim3(p.dv / 32, p.num_heads, p.num_seqs), 256, 0, stream>>>(p);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
+  FwdParams b = p;
+  b.seg_first = 1;
+  b.seg_launch = S - 1;
+  b.seg_transport = S;  // none
+  b.seg_write_next = 0;
+  const dim3 grid_b(p.dv / kDvt, p.num_heads, p.num_seqs * (S - 1));
+  kern<<<grid_b, Cfg::kWarps * 32, L::ALLOC, stream>>>(b, tq, tk, tv);
   return cudaGetLastError();
+}
+
+// The number of segments a sequence is split into: as many as the SMs take
+// in the first launch (segment 0 of every unit plus S - 2 transport
+// segments with dk/64 extra column tiles each), at most kMaxSegments and at
+// least 4 chunks per segment; 1 (no split) when that is fewer than 3.
+int choose_segments(const FwdParams &p) {
+  static int sms[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (sms[dev] == 0 &&
+      cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 1;
+  const int64_t units_v = (int64_t)p.num_seqs * p.num_heads * (p.dv / kDvt);
+  const int64_t units_t = (int64_t)p.num_seqs * p.num_heads * ((p.dv + DK) / kDvt);
+  if (units_v >= sms[dev]) return 1;
+  int64_t s = 2 + (sms[dev] - units_v) / units_t;
+  const int64_t chunks = (p.seq_len + 63) / 64;
+  if (s > kMaxSegments) s = kMaxSegments;
+  if (s > chunks / 4) s = chunks / 4;
+  return s >= 3 ? (int)s : 1;
 }
 
 }  // namespace
 
 bool tc_supported(int dk, int dv) { return (dk == 64 || dk == 128) && dv % kDvt == 0; }
+
+int seq_split_segments(const FwdParams &p) { return p.dk == DK && p.cu == nullptr ? choose_segments(p) : 1; }
 
 cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t stream) {
   switch (p.dk) {

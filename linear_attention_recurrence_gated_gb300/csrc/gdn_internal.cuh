@@ -11,6 +11,7 @@
 namespace gdn {
 
 constexpr int kChunk = 64;  // tokens per chunk of the tensor-core kernels (the default)
+constexpr int kMaxSegments = 3;  // GDN_SEQ_SPLIT: segments per sequence at most
 
 // Device status record at the start of the workspace.  The first error wins
 // (atomicCAS from 0); `seq` and `head` locate it, `aux` carries a detail.
@@ -50,6 +51,21 @@ struct FwdParams {
   int32_t num_heads, dk, dv, num_seqs;
   uint32_t flags;
   Extents ext;
+  // Sequence split (dense inputs, head_dim_k 128; GDN_SEQ_SPLIT): each
+  // sequence is cut into seg_count segments of seg_len tokens; a launch covers
+  // segments seg_first .. seg_first + seg_launch - 1 (grid z = sequence *
+  // seg_launch + segment - seg_first).  Segments >= seg_transport run in
+  // transport mode: zero initial state on the value columns and the identity
+  // on dk extra "transport" columns, no output; their final states are the
+  // segment's affine state map H -> M H + X (X to seg_x, M to seg_m).  Other
+  // segments start from the caller's state (segment 0) or seg_state, and end
+  // in the caller's final state (last segment) or, when seg_write_next, in
+  // seg_state of the next segment.  seg_len = 0: no split.
+  int32_t seg_len = 0, seg_count = 0, seg_first = 0, seg_launch = 0, seg_transport = 0,
+          seg_write_next = 0;
+  float *seg_state = nullptr;  // [N][seg_count][H][dk][dv]
+  float *seg_x = nullptr;      // [N][seg_count][H][dk][dv]
+  float *seg_m = nullptr;      // [N][seg_count][H][dk][dk]
 };
 
 __device__ __forceinline__ void report(DeviceStatus *st, uint32_t code, uint32_t seq,
@@ -188,6 +204,8 @@ cudaError_t launch_fwd_simt(const FwdParams &p, gdn_dtype dtype, int chunk, cuda
 bool simt_chunk_supported(int chunk, int dk);   // chunk in {32, 64, 128}, not 128 with dk 128
 cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t stream);    // bf16 storage only
 cudaError_t launch_fwd_tc64(const FwdParams &p, cudaStream_t stream);  // bf16, head_dim_k 64
+// GDN_SEQ_SPLIT: segments to cut each sequence of this call into (1 = no split)
+int seq_split_segments(const FwdParams &p);
 bool tc_supported(int dk, int dv);
 // chunk_size 32 and 128 on the tensor cores: bf16, head_dim_k 64
 bool tcc_supported(int chunk, int dk, int dv);

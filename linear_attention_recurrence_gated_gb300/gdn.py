@@ -29,6 +29,7 @@ GDN_FORCE_SIMT = 1 << 1
 GDN_GATE_SIGMOID = 1 << 2
 GDN_BETA_LOGITS = 1 << 3
 GDN_DEBUG_CHECKS = 1 << 4
+GDN_SEQ_SPLIT = 1 << 5
 # site codes of a GDN_ERR_DEVICE_CHECK record (gdn_check_record)
 DEBUG_SITES = {1: "q", 2: "k", 3: "v", 4: "g", 5: "beta", 6: "o", 7: "initial_state",
                8: "final_state", 9: "out_gate", 10: "tma_x"}
@@ -39,7 +40,7 @@ EXPORTED = ("gdn_fwd_workspace_size", "gdn_workspace_init", "gdn_fwd", "gdn_chec
             "gdn_status_string", "gdn_fwd_kernel_name", "gdn_fwd_static_scratch",
             "gdn_decode", "gdn_diag_workspace_size", "gdn_diag_fwd", "gdn_conv_silu",
             "gdn_bwd_workspace_size", "gdn_bwd", "gdn_fwd_debug", "gdn_check_record",
-            "gdn_fwd_kernel_name_chunk")
+            "gdn_fwd_kernel_name_chunk", "gdn_fwd_split_segments")
 # ... and include/gdn_debug.h (self-tests of the failure reporting).
 DEBUG_EXPORTED = ("gdn_debug_wait_timeout",)
 
@@ -89,6 +90,9 @@ def lib() -> ctypes.CDLL:
             L.gdn_fwd_kernel_name.argtypes = [i32, i32, ctypes.c_int, u32]
             L.gdn_fwd_kernel_name_chunk.restype = ctypes.c_char_p
             L.gdn_fwd_kernel_name_chunk.argtypes = [i32, i32, i32, ctypes.c_int, u32]
+            L.gdn_fwd_split_segments.restype = i32
+            L.gdn_fwd_split_segments.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.c_int, u32,
+                                                 i32]
             L.gdn_fwd_static_scratch.restype = ctypes.c_int
             L.gdn_fwd_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                  i32, i32, i32, i32, i32, i32, i32,
@@ -189,6 +193,17 @@ def gdn_fwd_kernel_name(head_dim_k, head_dim_v, dtype: torch.dtype, flags: int =
     return None if r is None else r.decode()
 
 
+def gdn_fwd_split_segments(num_seqs, seq_len, num_heads, head_dim_k, head_dim_v,
+                           dtype: torch.dtype, flags: int = 0, chunk_size: int = CHUNK_SIZE,
+                           varlen: bool = False) -> int:
+    """Segments per sequence a gdn_fwd call with these sizes is cut into on the
+    current device (1: not split, one kernel launch; >= 3: three launches);
+    0 for sizes gdn_fwd rejects."""
+    return int(lib().gdn_fwd_split_segments(num_seqs, seq_len, num_heads, head_dim_k,
+                                            head_dim_v, chunk_size, _dtype_code(dtype), flags,
+                                            1 if varlen else 0))
+
+
 def _check_fwd_tensors(where, q, k, v, g, beta, initial_state, cu_seqlens, o, final_state,
                        D_skip=None, out_gate=None):
     """The tensor checks every forward entry point makes before it calls the
@@ -231,15 +246,17 @@ def _check_fwd_tensors(where, q, k, v, g, beta, initial_state, cu_seqlens, o, fi
     return N, H, dk, dv
 
 
-def _fwd_flags(qk_l2norm, beta_logits, force_simt, debug_checks):
+def _fwd_flags(qk_l2norm, beta_logits, force_simt, debug_checks, seq_split=False):
     return (GDN_QK_L2NORM if qk_l2norm else 0) | (GDN_FORCE_SIMT if force_simt else 0) | \
-        (GDN_BETA_LOGITS if beta_logits else 0) | (GDN_DEBUG_CHECKS if debug_checks else 0)
+        (GDN_BETA_LOGITS if beta_logits else 0) | (GDN_DEBUG_CHECKS if debug_checks else 0) | \
+        (GDN_SEQ_SPLIT if seq_split else 0)
 
 
 def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
             final_state=None, output_final_state=True, workspace=None, D_skip=None,
             out_gate=None, qk_l2norm=False, beta_logits=False, force_simt=False,
-            chunk_size=CHUNK_SIZE, stream=None, check=False, debug_checks=False):
+            chunk_size=CHUNK_SIZE, stream=None, check=False, debug_checks=False,
+            seq_split=False):
     """Forward pass of the gated delta rule through the C ABI.
 
     q, k ``[B, T, H, dk]``; v ``[B, T, H, dv]``; g ``[B, T, H]`` fp32; beta
@@ -252,7 +269,10 @@ def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
     ``D_skip`` ``[H]`` and ``out_gate`` ``[B, T, H]`` (fp32, optional) fuse the
     block epilogue o <- (o + D_skip[h] v) * out_gate; ``beta_logits`` makes the
     kernel use sigmoid(beta); ``qk_l2norm`` normalises q and k in-kernel.
-    ``debug_checks`` sets GDN_DEBUG_CHECKS (range checks before every access).
+    ``debug_checks`` sets GDN_DEBUG_CHECKS (range checks before every access);
+    ``seq_split`` sets GDN_SEQ_SPLIT (long dense sequences with head_dim_k 128
+    cut into segments computed in parallel; a given ``workspace`` must be sized
+    with the flag).
     With ``check=True`` the call synchronises and raises on a device-side error.
     """
     N, H, dk, dv = _check_fwd_tensors("gdn_fwd", q, k, v, g, beta, initial_state, cu_seqlens,
@@ -263,7 +283,7 @@ def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
         final_state = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
     B, T = q.shape[:2]
     dcode = _dtype_code(q.dtype)
-    flags = _fwd_flags(qk_l2norm, beta_logits, force_simt, debug_checks)
+    flags = _fwd_flags(qk_l2norm, beta_logits, force_simt, debug_checks, seq_split)
     if workspace is None:
         workspace = new_workspace(N, H, dk, dv, flags, device=q.device)
     st = lib().gdn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),

@@ -58,7 +58,26 @@ def test_status_strings(L):
 
 def test_workspace_size(L):
     assert G.gdn_fwd_workspace_size(8, 16, 64, 64) >= 256
+    # GDN_SEQ_SPLIT with head_dim_k 128: 3 segments' states, X (dk x dv) and M (dk x dk)
+    assert G.gdn_fwd_workspace_size(1, 16, 128, 128, G.GDN_SEQ_SPLIT) == \
+        256 + 4 * 1 * 3 * 16 * 128 * (2 * 128 + 128)
+    assert G.gdn_fwd_workspace_size(1, 16, 64, 64, G.GDN_SEQ_SPLIT) == 256
     assert G.gdn_fwd_workspace_size(0, 16, 64, 64) == 0
+
+
+def test_split_segments_host_rules(L):
+    """The split query's host-side rules (no device attribute is read on these
+    paths): rejected sizes give 0; no GDN_SEQ_SPLIT, fp32 storage, other chunk
+    sizes or head_dim_k 64 give 1 (never split)."""
+    import torch
+    S = G.gdn_fwd_split_segments
+    assert S(0, 65536, 16, 128, 128, torch.bfloat16, G.GDN_SEQ_SPLIT) == 0
+    assert S(1, 65536, 16, 48, 128, torch.bfloat16, G.GDN_SEQ_SPLIT) == 0
+    assert S(1, 65536, 16, 128, 100, torch.bfloat16, G.GDN_SEQ_SPLIT) == 0
+    assert S(1, 65536, 16, 128, 128, torch.bfloat16, 0) == 1
+    assert S(1, 65536, 16, 128, 128, torch.float32, G.GDN_SEQ_SPLIT) == 1
+    assert S(1, 65536, 16, 128, 128, torch.bfloat16, G.GDN_SEQ_SPLIT, chunk_size=32) == 1
+    assert S(1, 65536, 16, 64, 128, torch.bfloat16, G.GDN_SEQ_SPLIT) == 1
 
 
 def test_kernel_names(L):

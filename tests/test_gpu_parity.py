@@ -316,3 +316,81 @@ def test_outputs_stay_inside_their_buffers(dtype, dk, dv):
     to, ts = parity.TOL[tdt]
     assert parity.rel(o.double().cpu().numpy(), o_ref) <= to
     assert parity.rel(s.double().cpu().numpy(), s_ref) <= ts
+
+
+# ---------------- GDN_SEQ_SPLIT: long dense sequences cut into segments ----------------
+@pytest.mark.parametrize("T,H,dv,init,l2,gs", [(2000, 2, 128, True, False, 1e-3),
+                                                (2000, 2, 128, False, True, 0.0),
+                                                (4097, 1, 256, True, False, 1e-3),
+                                                (777, 3, 128, True, False, 1e-3)])
+def test_seq_split(T, H, dv, init, l2, gs):
+    """A split call equals the oracle within the bf16 bounds and the unsplit
+    call up to rounding; with dk = 128 and few units the call takes 3 segments.
+    The gates are slow (gs = 0 is the plain delta rule) so that a segment's
+    map M keeps weight: with fast gates M underflows to zero and the split
+    result is the unsplit one bit for bit."""
+    w = W.custom(B=1, T=T, H=H, dk=128, dv=dv, dtype="bf16", init_state=init, gate_scale=gs,
+                 seed=700 + T + dv)
+    inp = W.generate(w)
+    kw = dict(qk_l2norm=True) if l2 else {}
+    if l2:
+        ex = W.generate_block_extras(inp, H, seed=701)
+        inp = dict(inp, q=ex["q_raw"], k=ex["k_raw"])
+    d = parity.to_dev(inp)
+    o0, s0 = G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"], None,
+                       check=True, **kw)
+    o1, s1 = G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"], None,
+                       check=True, seq_split=True, **kw)
+    o_ref, s_ref = oracle.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                  inp["initial_state"], None, qk_l2norm=l2)
+    o64, s64 = o1.double().cpu().numpy(), s1.double().cpu().numpy()
+    to, ts = parity.TOL[torch.bfloat16]
+    assert parity.rel(o64, o_ref) <= to and parity.rel(s64, s_ref) <= ts
+    assert parity.worst_unit_state(s64, s_ref) <= ts
+    # close to the unsplit call (the segments' maps add bf16 operand rounding)
+    assert parity.rel(o64, o0.double().cpu().numpy()) <= 5e-3
+    assert parity.rel(s64, s0.double().cpu().numpy()) <= 5e-3
+    assert not torch.equal(s0, s1)  # the split path ran (its composition rounds differently)
+
+
+def test_seq_split_long_full_size():
+    """long_bf16 (B=1, T=65536, H=16, dk=dv=128, slow gates) split into segments,
+    against the oracle on the whole tensors and the worst (sequence, head)."""
+    w = W.WORKLOADS["long_bf16"]
+    inp = W.generate(w)
+    d = parity.to_dev(inp)
+    o, s = G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"], None,
+                     check=True, seq_split=True)
+    o_ref, s_ref = oracle.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                  inp["initial_state"], None)
+    o64, s64 = o.double().cpu().numpy(), s.double().cpu().numpy()
+    ro, rs = parity.rel(o64, o_ref), parity.rel(s64, s_ref)
+    uo, us = parity.worst_unit_o(o64, o_ref, None), parity.worst_unit_state(s64, s_ref)
+    parity.MARGINS.append(f"long_bf16 split into segments [tc128_bf16]: rel L2 o={ro:.3e} "
+                          f"state={rs:.3e}; worst (sequence, head) o={uo:.3e} state={us:.3e}")
+    to, ts = parity.TOL[torch.bfloat16]
+    assert ro <= to and rs <= ts and uo <= to and us <= ts
+
+
+def test_seq_split_plan():
+    """The library's split plan on this device: the long workload (16 units of
+    two column tiles) takes 3 segments; the wide one (128 units) fills the SMs
+    unsplit; packed varlen calls and short sequences are never split."""
+    S = G.gdn_fwd_split_segments
+    bf = torch.bfloat16
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # 32 value-column CTAs plus 64 per transport segment
+    assert S(1, 65536, 16, 128, 128, bf, G.GDN_SEQ_SPLIT) == (3 if sms >= 32 + 64 else 1)
+    assert S(4, 8192, 16, 128, 128, bf, G.GDN_SEQ_SPLIT) == 1
+    assert S(1, 140000, 8, 128, 256, bf, G.GDN_SEQ_SPLIT, varlen=True) == 1
+    assert S(1, 11 * 64, 1, 128, 128, bf, G.GDN_SEQ_SPLIT) == 1  # under 4 chunks a segment
+    assert S(1, 12 * 64, 1, 128, 128, bf, G.GDN_SEQ_SPLIT) == 3
+
+
+def test_seq_split_needs_its_workspace():
+    w = W.custom(B=1, T=1000, H=2, dk=128, dv=128, dtype="bf16", init_state=True, seed=9)
+    d = parity.to_dev(W.generate(w))
+    small = G.new_workspace(1, 2, 128, 128)  # sized without the flag
+    with pytest.raises(G.GdnError):
+        G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"], None,
+                  workspace=small, seq_split=True)
