@@ -18,7 +18,8 @@ Contents
 ``diag``         the HyMo pages' own recurrence, per-state-row decay
                  exp(g_t A) with A = -exp(A_log), write key b, read key c
                  ("Model Architecture Walkthrough" section 5.2.1), token by
-                 token in fp64 numpy.
+                 token in fp64 numpy; ``diag.forward_delta`` the same decay
+                 combined with the delta rule's erase and beta.
 ``grad``         the backward pass (dq, dk, dv, dg, dbeta, d initial state):
                  torch.autograd over the fp64 token loop on the CPU.
 ``block``        the GDN block's prologue (causal depthwise conv1d + SiLU) and

@@ -161,6 +161,120 @@ def pin_chaining(forward, seed=15):
             ("chained final", rel(h2, hN), 1e-13)]
 
 
+# ==========================================================================
+# The per-row decay combined with the delta rule (``oracle.diag.forward_delta``):
+#   hbar = exp(g_t A) (.) h,  h_t = hbar + beta_t b_t (v_t - hbar^T b_t)^T,  o_t = c_t^T h_t
+# ==========================================================================
+def delta_inputs(rng, B, T, H, S, D, A_log_const=False):
+    """Unit write keys (the delta rule's erase is a projection for beta <= 1
+    then), read keys and values N(0, 1), beta in (0, 1), gates in (0, 1)."""
+    v, b, c, g, A_log = inputs(rng, B, T, H, S, D, A_log_const)
+    b = b / np.linalg.norm(b, axis=-1, keepdims=True)
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((B, T, H))))
+    return v, b, c, g, A_log, beta
+
+
+# All rates of a head equal: a scalar decay exp(g_t A) per head, i.e. the
+# gated delta rule of the sequential C oracle with q = c, k = b and the
+# natural-log gate g_t * A (an independent implementation in C).
+def pin_delta_scalar_rates(forward_delta, forward_gdn, seed=21):
+    rng = np.random.default_rng(seed)
+    B, T, H, S, D = 2, 23, 3, 6, 5
+    v, b, c, g, A_log, beta = delta_inputs(rng, B, T, H, S, D, A_log_const=True)
+    h0 = rng.standard_normal((B, H, S, D))
+    o, hN = forward_delta(v, b, c, g, A_log, beta, h0)
+    A = -np.exp(A_log[:, 0])                                             # [H]
+    o2, h2 = forward_gdn(c, b, v, g * A[None, None, :], beta, h0)
+    return [("delta scalar rates o", rel(o, o2), 1e-12),
+            ("delta scalar rates final", rel(hN, h2), 1e-12)]
+
+
+# beta = 0: no erase and no write, only the decay: row s of h_t is
+# exp(A_s sum_{j<=t} g_j) times row s of h_0.
+def pin_delta_pure_decay(forward_delta, seed=22):
+    rng = np.random.default_rng(seed)
+    B, T, H, S, D = 2, 17, 2, 5, 4
+    v, b, c, g, A_log, beta = delta_inputs(rng, B, T, H, S, D)
+    h0 = rng.standard_normal((B, H, S, D))
+    o, hN = forward_delta(v, b, c, g, A_log, np.zeros_like(beta), h0)
+    A = -np.exp(A_log)                                                   # [H, S]
+    Gc = np.cumsum(g, axis=1)                                            # [B, T, H]
+    scale = np.exp(Gc[..., None] * A[None, None])                        # [B, T, H, S]
+    o_ref = np.einsum("bths,bhsd->bthd", c * scale, h0)
+    h_ref = scale[:, -1, :, :, None] * h0
+    return [("delta pure decay o", rel(o, o_ref), 1e-12),
+            ("delta pure decay final", rel(hN, h_ref), 1e-12)]
+
+
+# The delta rule's overwrite: with beta_t = 1 and a unit key b_t, reading the
+# state with c_t = b_t right after the write returns v_t, whatever the state
+# held and however its rows decayed.
+def pin_delta_overwrite(forward_delta, seed=23):
+    rng = np.random.default_rng(seed)
+    B, T, H, S, D = 2, 19, 2, 6, 4
+    v, b, c, g, A_log, beta = delta_inputs(rng, B, T, H, S, D)
+    h0 = rng.standard_normal((B, H, S, D))
+    o, _ = forward_delta(v, b, b, g, A_log, np.ones_like(beta), h0)
+    return [("delta overwrite", rel(o, v), 1e-12)]
+
+
+# Basis-vector write keys b_t = e_{s_t} decouple the rows: row r decays by
+# d_r = exp(g_t A_r) and, when r = s_t, becomes (1 - beta_t) d_r h_r + beta_t v_t.
+def pin_delta_basis_keys(forward_delta, seed=24):
+    rng = np.random.default_rng(seed)
+    B, T, H, S, D = 1, 25, 2, 4, 3
+    v, _, c, g, A_log, beta = delta_inputs(rng, B, T, H, S, D)
+    sel = rng.integers(0, S, size=(B, T, H))
+    b = np.zeros((B, T, H, S))
+    for bb in range(B):
+        for t in range(T):
+            for hh in range(H):
+                b[bb, t, hh, sel[bb, t, hh]] = 1.0
+    h0 = rng.standard_normal((B, H, S, D))
+    o, hN = forward_delta(v, b, c, g, A_log, beta, h0)
+    A = -np.exp(A_log)
+    o_ref = np.zeros_like(o)
+    h_ref = np.zeros_like(hN)
+    for bb in range(B):
+        for hh in range(H):
+            rows = [h0[bb, hh, r].copy() for r in range(S)]
+            for t in range(T):
+                for r in range(S):
+                    d = np.exp(g[bb, t, hh] * A[hh, r])
+                    if r == sel[bb, t, hh]:
+                        rows[r] = (1.0 - beta[bb, t, hh]) * d * rows[r] + beta[bb, t, hh] * v[bb, t, hh]
+                    else:
+                        rows[r] = d * rows[r]
+                o_ref[bb, t, hh] = sum(c[bb, t, hh, r] * rows[r] for r in range(S))
+            for r in range(S):
+                h_ref[bb, hh, r] = rows[r]
+    return [("delta basis keys o", rel(o, o_ref), 1e-12),
+            ("delta basis keys final", rel(hN, h_ref), 1e-12)]
+
+
+def pin_delta_chaining(forward_delta, seed=25):
+    rng = np.random.default_rng(seed)
+    B, T, H, S, D = 2, 24, 2, 4, 5
+    v, b, c, g, A_log, beta = delta_inputs(rng, B, T, H, S, D)
+    h0 = rng.standard_normal((B, H, S, D))
+    o, hN = forward_delta(v, b, c, g, A_log, beta, h0)
+    m = 9
+    o1, h1 = forward_delta(v[:, :m], b[:, :m], c[:, :m], g[:, :m], A_log, beta[:, :m], h0)
+    o2, h2 = forward_delta(v[:, m:], b[:, m:], c[:, m:], g[:, m:], A_log, beta[:, m:], h1)
+    return [("delta chained o", rel(np.concatenate([o1, o2], axis=1), o), 1e-13),
+            ("delta chained final", rel(h2, hN), 1e-13)]
+
+
+def all_delta_pins(forward_delta, forward_gdn):
+    res = []
+    res += pin_delta_scalar_rates(forward_delta, forward_gdn)
+    res += pin_delta_pure_decay(forward_delta)
+    res += pin_delta_overwrite(forward_delta)
+    res += pin_delta_basis_keys(forward_delta)
+    res += pin_delta_chaining(forward_delta)
+    return res
+
+
 def all_pins(forward, forward_gla):
     res = []
     res += pin_golden_page_decay(forward)

@@ -48,6 +48,31 @@ def test_chaining():
     _check(pins_diag.pin_chaining(oracle.diag.forward))
 
 
+def _gdn():
+    oracle.build()
+    return oracle.forward
+
+
+def test_delta_scalar_rates_equal_gated_delta_rule():
+    _check(pins_diag.pin_delta_scalar_rates(oracle.diag.forward_delta, _gdn()))
+
+
+def test_delta_pure_decay():
+    _check(pins_diag.pin_delta_pure_decay(oracle.diag.forward_delta))
+
+
+def test_delta_overwrite():
+    _check(pins_diag.pin_delta_overwrite(oracle.diag.forward_delta))
+
+
+def test_delta_basis_keys():
+    _check(pins_diag.pin_delta_basis_keys(oracle.diag.forward_delta))
+
+
+def test_delta_chaining():
+    _check(pins_diag.pin_delta_chaining(oracle.diag.forward_delta))
+
+
 # (name, text in oracle/diag.py, replacement)
 MUTANTS = [
     ("decay grows (A sign)", "A = -np.exp(A_log)", "A = np.exp(A_log)"),
@@ -90,4 +115,38 @@ def test_pins_catch_planted_mistake(name, old, new, tmp_path):
         failing = pins.run(pins_diag.all_pins(mod.forward, _gla()))
     except (ValueError, IndexError):
         failing = ["shape error"]          # a mutant that cannot even run is caught
+    assert failing, f"no pin caught the planted mistake: {name}"
+
+
+# Planted mistakes in forward_delta (anchors that occur only there).
+MUTANTS_DELTA = [
+    ("erase reads the undecayed state", 'pred = np.einsum("bhs,bhsd->bhd", bt, hbar)',
+     'pred = np.einsum("bhs,bhsd->bhd", bt, h)'),
+    ("write without beta", "err = beta[:, t, :, None] * (v[:, t] - pred)",
+     "err = (v[:, t] - pred)"),
+    ("erase without beta", "err = beta[:, t, :, None] * (v[:, t] - pred)",
+     "err = beta[:, t, :, None] * v[:, t] - pred"),
+    ("decay after the update", "h = hbar + bt[..., None] * err[:, :, None, :]",
+     "h = decay[..., None] * (h + bt[..., None] * err[:, :, None, :])"),
+    ("delta decay per value column", "hbar = decay[..., None] * h",
+     "hbar = decay[..., None, :] * h"),
+    ("erase sign", "h = hbar + bt[..., None] * err[:, :, None, :]",
+     "h = hbar - bt[..., None] * err[:, :, None, :]"),
+    ("delta read with the write key",
+     'err[:, :, None, :]\n        o[:, t] = np.einsum("bhs,bhsd->bhd", c[:, t], h)',
+     'err[:, :, None, :]\n        o[:, t] = np.einsum("bhs,bhsd->bhd", bt, h)'),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS_DELTA, ids=[m[0] for m in MUTANTS_DELTA])
+def test_delta_pins_catch_planted_mistake(name, old, new, tmp_path):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not unique: {old!r}"
+    path = tmp_path / "diag_delta_mutant.py"
+    path.write_text(src.replace(old, new, 1))
+    mod = _load_mutant(str(path))
+    try:
+        failing = pins.run(pins_diag.all_delta_pins(mod.forward_delta, _gdn()))
+    except (ValueError, IndexError):
+        failing = ["shape error"]
     assert failing, f"no pin caught the planted mistake: {name}"
