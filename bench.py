@@ -231,6 +231,8 @@ KERNEL_SOURCES = {
     "tcc128_bf16": "gdn_fwd_tcc.cu",
     "diag_bf16": "gdn_diag.cu",
     "diag_fp32": "gdn_diag.cu",
+    "diag_delta_bf16": "gdn_diag_delta.cu",
+    "diag_delta_fp32": "gdn_diag_delta.cu",
     "conv_bf16": "gdn_conv.cu",
     "conv_fp32": "gdn_conv.cu",
     "bwd_chunk": "gdn_bwd_chunk.cu",
@@ -674,11 +676,12 @@ def bench_decode(args, w: W.Workload, rank: int, world: int, local: int):
 
 
 def diag_bytes(w: W.DiagWorkload) -> float:
-    """HBM bytes of one gdn_diag_fwd call: v, b, c read and o written in the
-    storage dtype, g read as fp32, per (token, head); the fp32 final state
+    """HBM bytes of one gdn_diag_fwd (or gdn_diag_delta_fwd) call: v, b, c (and
+    beta) read and o written in the storage dtype, g read as fp32, per (token,
+    head); the fp32 final state
     written (and the initial state read, when given) per (batch row, head)."""
     e = 4 if w.dtype == "fp32" else 2
-    per_head_token = e * (2 * w.D + 2 * w.S) + 4
+    per_head_token = e * (2 * w.D + 2 * w.S + (1 if w.delta else 0)) + 4   # + beta
     state = 4 * w.S * w.D * w.B * w.H * (2 if w.init_state else 1)
     return float(w.B * w.T * w.H * per_head_token + state)
 
@@ -688,8 +691,12 @@ def _diag_oracle_pass(host, b_rows=None):
     sel = slice(None) if b_rows is None else b_rows
     h0 = host["initial_state"]
     t = time.perf_counter()
-    oracle.diag.forward(host["v"][sel], host["b"][sel], host["c"][sel], host["g"][sel],
-                        host["A_log"], None if h0 is None else h0[sel])
+    if "beta" in host:
+        oracle.diag.forward_delta(host["v"][sel], host["b"][sel], host["c"][sel], host["g"][sel],
+                                  host["A_log"], host["beta"][sel], None if h0 is None else h0[sel])
+    else:
+        oracle.diag.forward(host["v"][sel], host["b"][sel], host["c"][sel], host["g"][sel],
+                            host["A_log"], None if h0 is None else h0[sel])
     return time.perf_counter() - t
 
 
@@ -721,7 +728,8 @@ def bench_diag_reference(args, w: W.DiagWorkload, rank: int, world: int):
 
 
 def bench_diag(args, w: W.DiagWorkload, rank: int, world: int, local: int):
-    """The pages' diagonal-decay recurrence (gdn_diag_fwd), one call per step."""
+    """The pages' diagonal-decay recurrence (gdn_diag_fwd), or the same decay
+    combined with the delta rule (gdn_diag_delta_fwd), one call per step."""
     from linear_attention_recurrence_gated_gb300 import gdn as G
     if not torch.cuda.is_available():
         raise RuntimeError("bench.py needs a CUDA GPU (no CPU fallback)")
@@ -730,7 +738,7 @@ def bench_diag(args, w: W.DiagWorkload, rank: int, world: int, local: int):
     G.lib()
     from dataclasses import replace
     host = W.generate_diag(replace(w, seed=w.seed + rank))
-    names = ("v", "b", "c", "g")
+    names = ("v", "b", "c", "g") + (("beta",) if w.delta else ())
     sets = []
     for _ in range(2):  # two resident input sets, alternated between steps
         d = {n: host[n].to(dev) for n in names}
@@ -739,13 +747,22 @@ def bench_diag(args, w: W.DiagWorkload, rank: int, world: int, local: int):
         d["o"] = torch.empty_like(d["v"])
         d["final_state"] = torch.empty((w.B, w.H, w.S, w.D), dtype=torch.float32, device=dev)
         sets.append(d)
-    ws = G.new_diag_workspace(w.B, w.T, w.H, w.S, w.D, device=dev)
-    kname = "diag_" + w.dtype
+    if w.delta:
+        ws = G.new_diag_delta_workspace(w.B, w.T, w.H, w.S, w.D, device=dev)
+        kname = "diag_delta_" + w.dtype
+    else:
+        ws = G.new_diag_workspace(w.B, w.T, w.H, w.S, w.D, device=dev)
+        kname = "diag_" + w.dtype
     stream = torch.cuda.current_stream(dev)
 
     def call(d, s=stream):
-        G.gdn_diag_fwd(d["v"], d["b"], d["c"], d["g"], d["A_log"], d["initial_state"],
-                       o=d["o"], final_state=d["final_state"], workspace=ws, stream=s)
+        if w.delta:
+            G.gdn_diag_delta_fwd(d["v"], d["b"], d["c"], d["g"], d["A_log"], d["beta"],
+                                 d["initial_state"], o=d["o"], final_state=d["final_state"],
+                                 workspace=ws, stream=s)
+        else:
+            G.gdn_diag_fwd(d["v"], d["b"], d["c"], d["g"], d["A_log"], d["initial_state"],
+                           o=d["o"], final_state=d["final_state"], workspace=ws, stream=s)
 
     for i in range(args.warmup):
         call(sets[i & 1])
@@ -826,7 +843,7 @@ def bench_diag(args, w: W.DiagWorkload, rank: int, world: int, local: int):
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "S": w.S, "D": w.D,
                    "storage": w.dtype, "a_log": w.a_log, "kernel": kname,
                    "l2": f"two resident input sets of {in_mb:.0f} MB each alternate between "
-                         "steps (257 MB > 129 MB L2)",
+                         f"steps ({2 * in_mb:.0f} MB > 129 MB L2)",
                    "parallelism": f"replicas x{world}"},
         "head_tokens_per_s": value * w.H,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",

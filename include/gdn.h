@@ -80,10 +80,10 @@ enum {
   /* Use the fp32 CUDA-core kernel even for bf16 storage (the tensor-core
    * kernel is the default for bf16).  fp32 storage always uses it. */
   GDN_FORCE_SIMT = 1u << 1,
-  /* gdn_diag_fwd only: g holds the gate's logits dt and the kernel uses
+  /* gdn_diag_fwd and gdn_diag_delta_fwd: g holds the gate's logits dt and the kernel uses
    * g = sigmoid(dt) ("Model Architecture Walkthrough", section 5.2.1). */
   GDN_GATE_SIGMOID = 1u << 2,
-  /* gdn_fwd only: beta holds logits and the kernel uses beta_t =
+  /* gdn_fwd and gdn_diag_delta_fwd: beta holds logits and the kernel uses beta_t =
    * sigmoid(beta input) in fp32 (the write strength is a sigmoid of a
    * projection in the gated delta rule block; the pages' block computes its
    * gates the same way, "Model Architecture Walkthrough", section 5.4.3). */
@@ -386,6 +386,62 @@ gdn_status gdn_diag_fwd(const void *v, const void *b, const void *c, const float
                         float *final_state, int32_t batch, int32_t seq_len, int32_t num_heads,
                         int32_t d_state, int32_t head_dim, gdn_dtype dtype, uint32_t flags,
                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * gdn_diag_delta_fwd -- the pages' per-row (diagonal) decay combined with the
+ * delta rule: the decay of gdn_diag_fwd ("Model Architecture Walkthrough",
+ * section 5.2.1: exp(g_t A) scales row s of the state by exp(g_t A_s), A =
+ * -exp(A_log[h])) followed by the gated delta rule's erase and write with
+ * strength beta_t, the write key b_t also being the erase key.  Per batch row
+ * n and head h, tokens t = 1..seq_len:
+ *
+ *     hbar = exp(g_t A) (.) h_{t-1}
+ *     h_t  = hbar + beta_t b_t (v_t - hbar^T b_t)^T,     o_t = h_t^T c_t
+ *
+ * h_t is d_state x head_dim (fp32).  With beta_t = 1 and a unit b_t the state
+ * returns v_t for the key b_t right after the write; with all rates of a
+ * head equal it is gdn_fwd's recurrence with q = c, k = b and the natural-log
+ * gate g_t A.  Arithmetic is fp32 inside; o is stored in the caller's dtype.
+ *
+ *   v              [batch, seq_len, num_heads, head_dim]       dtype    device
+ *   b, c           [batch, seq_len, num_heads, d_state]        dtype    device
+ *   g              [batch, seq_len, num_heads]                 float32  device
+ *   A_log          [num_heads, d_state]                        float32  device
+ *   beta           [batch, seq_len, num_heads]                 dtype    device
+ *   D_skip         [num_heads]                                 float32  device, or NULL
+ *   out_gate       [batch, seq_len, num_heads]                 float32  device, or NULL
+ *   initial_state  [batch, num_heads, d_state, head_dim]       float32  device, or NULL (= zeros)
+ *   o              [batch, seq_len, num_heads, head_dim]       dtype    device (written)
+ *   final_state    [batch, num_heads, d_state, head_dim]       float32  device (written), or NULL
+ *
+ * flags: GDN_GATE_SIGMOID (g holds logits, g_t = sigmoid(g input)) and
+ * GDN_BETA_LOGITS (beta_t = sigmoid(beta input)); the block epilogue
+ * o_t <- (o_t + D_skip[h] v_t) * out_gate[n, t, h] as in gdn_diag_fwd.  Keys
+ * are used as given (the erase is a projection only for beta_t |b_t|^2 <= 2).
+ *
+ * Supported sizes: d_state == 32 and head_dim == 32; batch, num_heads,
+ * seq_len >= 1 with batch * num_heads * ceil(seq_len / 128) < 2^31.  Anything
+ * else returns GDN_ERR_UNSUPPORTED (or INVALID_ARG if malformed).  Aliasing as
+ * gdn_diag_fwd.
+ *
+ * workspace: device, at least gdn_diag_delta_workspace_size(...) bytes, zeroed
+ * once before its first use (gdn_workspace_init); it carries a launch counter
+ * from call to call (a call that failed to complete requires a new
+ * gdn_workspace_init), and calls sharing it must be ordered (same stream).
+ * The 128-token segments of a sequence run in parallel and are joined through
+ * their affine state maps in the workspace.  Device-detected errors
+ * (GDN_ERR_TIMEOUT) are reported by gdn_check.  Returns GDN_OK once enqueued,
+ * or an error code with nothing enqueued.
+ */
+size_t gdn_diag_delta_workspace_size(int32_t batch, int32_t seq_len, int32_t num_heads,
+                                     int32_t d_state, int32_t head_dim);
+gdn_status gdn_diag_delta_fwd(const void *v, const void *b, const void *c, const float *g,
+                              const float *A_log, const void *beta, const float *D_skip,
+                              const float *out_gate, const float *initial_state, void *o,
+                              float *final_state, int32_t batch, int32_t seq_len,
+                              int32_t num_heads, int32_t d_state, int32_t head_dim,
+                              gdn_dtype dtype, uint32_t flags, void *workspace,
+                              size_t workspace_bytes, void *stream);
 
 /*
  * gdn_conv_silu -- prologue of the HyMo GDN block: causal depthwise conv1d,

@@ -40,7 +40,8 @@ EXPORTED = ("gdn_fwd_workspace_size", "gdn_workspace_init", "gdn_fwd", "gdn_chec
             "gdn_status_string", "gdn_fwd_kernel_name", "gdn_fwd_static_scratch",
             "gdn_decode", "gdn_diag_workspace_size", "gdn_diag_fwd", "gdn_conv_silu",
             "gdn_bwd_workspace_size", "gdn_bwd", "gdn_fwd_debug", "gdn_check_record",
-            "gdn_fwd_kernel_name_chunk", "gdn_fwd_split_segments")
+            "gdn_fwd_kernel_name_chunk", "gdn_fwd_split_segments",
+            "gdn_diag_delta_workspace_size", "gdn_diag_delta_fwd")
 # ... and include/gdn_debug.h (self-tests of the failure reporting).
 DEBUG_EXPORTED = ("gdn_debug_wait_timeout",)
 
@@ -111,6 +112,12 @@ def lib() -> ctypes.CDLL:
             L.gdn_diag_fwd.restype = ctypes.c_int
             L.gdn_diag_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                        i32, i32, i32, i32, i32, ctypes.c_int, u32, vp, sz, vp]
+            L.gdn_diag_delta_workspace_size.restype = sz
+            L.gdn_diag_delta_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+            L.gdn_diag_delta_fwd.restype = ctypes.c_int
+            L.gdn_diag_delta_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                             i32, i32, i32, i32, i32, ctypes.c_int, u32, vp, sz,
+                                             vp]
             _lib = L
     return _lib
 
@@ -464,6 +471,76 @@ def gdn_diag_fwd(v, b, c, g, A_log, initial_state=None, *, D_skip=None, out_gate
         st = gdn_check(workspace, stream)
         if st != GDN_OK:
             raise GdnError(st, "gdn_diag_fwd (device)")
+    return o, final_state
+
+
+def gdn_diag_delta_workspace_size(batch: int, seq_len: int, num_heads: int, d_state: int,
+                                  head_dim: int) -> int:
+    return int(lib().gdn_diag_delta_workspace_size(batch, seq_len, num_heads, d_state,
+                                                   head_dim))
+
+
+def new_diag_delta_workspace(batch, seq_len, num_heads, d_state, head_dim, device=None):
+    """A zeroed workspace of the size gdn_diag_delta_fwd needs (the caller keeps it)."""
+    n = gdn_diag_delta_workspace_size(batch, seq_len, num_heads, d_state, head_dim)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def gdn_diag_delta_fwd(v, b, c, g, A_log, beta, initial_state=None, *, D_skip=None,
+                       out_gate=None, gate_sigmoid=False, beta_logits=False, o=None,
+                       final_state=None, output_final_state=True, workspace=None, stream=None,
+                       check=False):
+    """The pages' diagonal decay combined with the delta rule, through the C ABI.
+
+    Tensors as ``gdn_diag_fwd`` plus beta ``[B, T, H]`` in the storage dtype of
+    v, b, c.  ``beta_logits`` makes beta the logits of the write strength
+    (sigmoid in the kernel).  Returns ``(o, final_state)``.  A workspace made by
+    ``new_diag_delta_workspace`` for the same sizes may be reused across calls
+    on one stream.
+    """
+    B, T, H, D = v.shape
+    S = b.shape[-1]
+    for t in [v, b, c, g, A_log, beta] + [t for t in (initial_state, o, final_state, D_skip,
+                                                      out_gate) if t is not None]:
+        if not t.is_cuda:
+            raise ValueError("gdn_diag_delta_fwd: every tensor must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("gdn_diag_delta_fwd: every tensor must be contiguous")
+    dcode = _dtype_code(v.dtype)
+    if b.dtype != v.dtype or c.dtype != v.dtype or beta.dtype != v.dtype:
+        raise TypeError("gdn_diag_delta_fwd: v, b, c and beta must share one storage dtype")
+    if g.dtype != torch.float32 or A_log.dtype != torch.float32:
+        raise TypeError("gdn_diag_delta_fwd: g and A_log must be float32")
+    if b.shape != (B, T, H, S) or c.shape != (B, T, H, S) or g.shape != (B, T, H) or \
+            beta.shape != (B, T, H) or A_log.shape != (H, S):
+        raise ValueError("gdn_diag_delta_fwd: shape mismatch among v, b, c, g, beta, A_log")
+    for name, t in (("initial_state", initial_state), ("final_state", final_state)):
+        if t is not None and (t.dtype != torch.float32 or t.shape != (B, H, S, D)):
+            raise ValueError(f"gdn_diag_delta_fwd: {name} must be float32 [B, H, S, D]")
+    if D_skip is not None and (D_skip.dtype != torch.float32 or D_skip.shape != (H,)):
+        raise ValueError("gdn_diag_delta_fwd: D_skip must be float32 [H]")
+    if out_gate is not None and (out_gate.dtype != torch.float32 or out_gate.shape != (B, T, H)):
+        raise ValueError("gdn_diag_delta_fwd: out_gate must be float32 [B, T, H]")
+    if o is None:
+        o = torch.empty_like(v)
+    elif o.shape != v.shape or o.dtype != v.dtype:
+        raise ValueError("gdn_diag_delta_fwd: o must match v in shape and dtype")
+    if final_state is None and output_final_state:
+        final_state = torch.empty((B, H, S, D), dtype=torch.float32, device=v.device)
+    if workspace is None:
+        workspace = new_diag_delta_workspace(B, T, H, S, D, device=v.device)
+    flags = (GDN_GATE_SIGMOID if gate_sigmoid else 0) | (GDN_BETA_LOGITS if beta_logits else 0)
+    st = lib().gdn_diag_delta_fwd(_ptr(v), _ptr(b), _ptr(c), _ptr(g), _ptr(A_log), _ptr(beta),
+                                  _ptr(D_skip), _ptr(out_gate), _ptr(initial_state), _ptr(o),
+                                  _ptr(final_state), B, T, H, S, D, dcode, flags,
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream_handle(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_diag_delta_fwd")
+    if check:
+        st = gdn_check(workspace, stream)
+        if st != GDN_OK:
+            raise GdnError(st, "gdn_diag_delta_fwd (device)")
     return o, final_state
 
 

@@ -187,7 +187,9 @@ class DiagWorkload:
     "pages": A_log[h, s] = log(h + 1) for every s, the initialisation the pages
     give ("Model Architecture Walkthrough", section 5.3.2: A = -1 ... -H);
     "uniform": A_log[h, s] ~ U(-2, 2) independently (a different rate per row);
-    "slow": A_log[h, s] ~ U(-6, -3) (per-token factors near 1: long memory)."""
+    "slow": A_log[h, s] ~ U(-6, -3) (per-token factors near 1: long memory).
+    ``delta`` selects the inputs of ``gdn_diag_delta_fwd`` (the same decay
+    combined with the delta rule): unit write keys and a write strength beta."""
     name: str
     B: int
     T: int
@@ -198,6 +200,7 @@ class DiagWorkload:
     a_log: str = "pages"
     init_state: bool = False
     seed: int = 0
+    delta: bool = False
     notes: str = field(default="", compare=False)
 
 
@@ -209,6 +212,10 @@ DIAG_WORKLOADS = {
     "diag_small_fp32": DiagWorkload("diag_small_fp32", B=2, T=300, H=3, dtype="fp32",
                                     a_log="uniform", init_state=True,
                                     notes="parity case: several CTAs and a ragged tail"),
+    "hymo_diag_delta_bf16": DiagWorkload("hymo_diag_delta_bf16", B=4, T=4096, H=40,
+                                         dtype="bf16", a_log="pages", delta=True,
+                                         notes="the pages' production shape with the delta "
+                                               "rule's erase added (diagonal decay + delta rule)"),
 }
 
 
@@ -218,12 +225,17 @@ def generate_diag(w: DiagWorkload):
     ``[B, T, H, S]``; g = sigmoid(z), z ~ N(0, 1) ``[B, T, H]`` fp32 (the pages'
     g is a sigmoid output); A_log ``[H, S]`` fp32 per ``w.a_log``; initial
     state ~ N(0, 0.1^2) ``[B, H, S, D]`` fp32 when ``w.init_state``.  v, b, c
-    are cast to the storage dtype (round to nearest even)."""
+    are cast to the storage dtype (round to nearest even).  With ``w.delta``
+    each row b_t is divided by its L2 norm in fp64 before the cast (the delta
+    rule's erase is a projection for unit keys) and, drawn last, beta =
+    sigmoid(z), z ~ N(0, 1) ``[B, T, H]`` in the storage dtype."""
     rng = np.random.default_rng(w.seed)
     dt = _DTYPES[w.dtype]
     B, T, H, S, D = w.B, w.T, w.H, w.S, w.D
     v = torch.from_numpy(rng.standard_normal((B, T, H, D))).to(dt)
-    b = torch.from_numpy(rng.standard_normal((B, T, H, S)) / np.sqrt(S)).to(dt)
+    b64 = rng.standard_normal((B, T, H, S))
+    b64 = b64 / np.linalg.norm(b64, axis=-1, keepdims=True) if w.delta else b64 / np.sqrt(S)
+    b = torch.from_numpy(b64).to(dt)
     c = torch.from_numpy(rng.standard_normal((B, T, H, S)) / np.sqrt(S)).to(dt)
     g = torch.from_numpy(_sigmoid(rng.standard_normal((B, T, H)))).to(torch.float32)
     if w.a_log == "pages":
@@ -238,8 +250,11 @@ def generate_diag(w: DiagWorkload):
     h0 = None
     if w.init_state:
         h0 = torch.from_numpy(0.1 * rng.standard_normal((B, H, S, D))).to(torch.float32)
-    return {"v": v.contiguous(), "b": b.contiguous(), "c": c.contiguous(),
-            "g": g.contiguous(), "A_log": A_log.contiguous(), "initial_state": h0}
+    out = {"v": v.contiguous(), "b": b.contiguous(), "c": c.contiguous(),
+           "g": g.contiguous(), "A_log": A_log.contiguous(), "initial_state": h0}
+    if w.delta:
+        out["beta"] = torch.from_numpy(_sigmoid(rng.standard_normal((B, T, H)))).to(dt).contiguous()
+    return out
 
 
 # ---------------------------------------------------------------------------

@@ -295,6 +295,49 @@ def test_diag_host_validation_rejects_before_launch(L, over, code):
     assert call_diag(L, **over) == code
 
 
+# ---- gdn_diag_delta_fwd (diagonal decay combined with the delta rule) ----
+def test_diag_delta_workspace_size(L):
+    # 4 x 40 heads x 32 segments of 128 tokens: a flag and an end state each
+    n = G.gdn_diag_delta_workspace_size(4, 4096, 40, 32, 32)
+    tasks = 4 * 40 * 32
+    assert n >= 256 + tasks * (4 + 32 * 32 * 4)
+    assert G.gdn_diag_delta_workspace_size(1, 1, 1, 32, 32) > 256
+    assert G.gdn_diag_delta_workspace_size(0, 1, 1, 32, 32) == 0
+    assert G.gdn_diag_delta_workspace_size(1, 0, 1, 32, 32) == 0
+
+
+def call_diag_delta(L, **over):
+    B, T, H, S, D = 2, 300, 3, 32, 32
+    ws_need = G.gdn_diag_delta_workspace_size(B, T, H, S, D)
+    a = dict(v=BASE, b=BASE + (1 << 30), c=BASE + (2 << 30), g=BASE + (3 << 30),
+             A=BASE + (4 << 30), beta=BASE + (8 << 30), Dk=None, og=None, s0=None,
+             o=BASE + (5 << 30), sN=BASE + (6 << 30),
+             B=B, T=T, H=H, S=S, D=D, dtype=G.GDN_BF16, flags=0, ws=BASE + (7 << 30),
+             ws_bytes=ws_need)
+    a.update(over)
+    vp = ctypes.c_void_p
+    return L.gdn_diag_delta_fwd(vp(a["v"]), vp(a["b"]), vp(a["c"]), vp(a["g"]), vp(a["A"]),
+                                vp(a["beta"]), vp(a["Dk"]), vp(a["og"]), vp(a["s0"]),
+                                vp(a["o"]), vp(a["sN"]), a["B"], a["T"], a["H"], a["S"],
+                                a["D"], a["dtype"], a["flags"], vp(a["ws"]), a["ws_bytes"],
+                                vp(0))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(S=16), 2), (dict(D=64), 2), (dict(S=0), 1), (dict(B=0), 1), (dict(T=0), 1),
+    (dict(dtype=5), 1), (dict(flags=1), 1), (dict(flags=G.GDN_QK_L2NORM), 1),
+    (dict(beta=None), 1), (dict(v=None), 1), (dict(A=None), 1), (dict(o=None), 1),
+    (dict(beta=BASE + (8 << 30) + 2), 1),                   # misaligned beta
+    (dict(o=BASE + (8 << 30)), 1),                          # o aliases beta
+    (dict(sN=BASE + (8 << 30)), 1),                         # final state aliases beta
+    (dict(ws=None), 3), (dict(ws_bytes=256), 3),
+    (dict(sN=BASE + (7 << 30) + 4096), 1),                  # final state inside the workspace
+    (dict(B=1 << 16, H=1 << 16), 2),                        # too many segments
+])
+def test_diag_delta_host_validation_rejects_before_launch(L, over, code):
+    assert call_diag_delta(L, **over) == code
+
+
 class _OnDevice:
     """A CPU tensor that reports itself as a CUDA tensor, so that the
     binding's tensor checks can be exercised on a machine without a GPU."""
