@@ -14,7 +14,7 @@
 // from the unit vector e_k with v = 0 (the read of that run: r_t = M_t^T c_t).
 //
 // Work split: one CTA of two warps per (batch row, head, 128-token segment).
-// Lane j of a warp owns column j of a 32 x 32 state in registers.  Warp 0
+// A warp holds a 32 x 32 state in registers, an 8 x 4 block per lane.  Warp 0
 // runs the segment from a zero state (from the initial state in segment 0),
 // keeping o0 in shared memory; warp 1 runs it from the identity with v = 0,
 // keeping r.  Then the segment's start state comes from its predecessor
@@ -23,8 +23,9 @@
 // CTAs take their segment from a ticket counter in launch order, segment-major,
 // so a CTA only waits on a CTA that started before it; every wait is bounded.
 //
-// Per token a warp reads four 32-float rows from shared memory (b (.) d, d, b,
-// c, broadcast to every lane) and does 64 packed two-lane fp32 operations.
+// Per token a lane reads 8 rows of d, b and c and 4 values of v from shared
+// memory and does 64 packed two-lane fp32 operations; the column sums over
+// the state rows take 16 shuffles.
 #include "gdn_internal.cuh"
 #include "gdn_ptx.cuh"
 
@@ -87,18 +88,34 @@ struct Params {
   uint32_t opts;                    // GDN_GATE_SIGMOID, GDN_BETA_LOGITS
 };
 
+// o0 and r are kept in the storage type T (bf16 storage: the outputs are
+// rounded to bf16 anyway, and the smaller buffers let 6 CTAs share an SM)
+template <typename T>
 struct Smem {
-  // staged tiles, double-buffered: rows [b (.) d, d, b, c][token][s]; after
-  // the token loop the first buffer holds M and X for the composition
-  float row[2][4][kTile][kS];
+  // staged tiles, double-buffered: rows [d, b, c][token][s], v and beta;
+  // after the token loop the tile rows hold M^T and X
+  float row[2][3][kTile][kS];
   float vt[2][kTile][kD];
   float bt[2][kTile];
-  float obuf[kSeg][kD];             // o0 (warp 0)
-  float rbuf[kSeg][kS];             // r (warp 1)
+  float hs[kS][kD];                 // h_start
+  T obuf[kSeg][kD];                 // o0 (warp 0)
+  T rbuf[kSeg][kS];                 // r (warp 1)
   uint32_t misc[4];
 };
 
+__device__ __forceinline__ void st4(float *p, float4 x) { *reinterpret_cast<float4 *>(p) = x; }
+__device__ __forceinline__ void st4(__nv_bfloat16 *p, float4 x) {
+  *reinterpret_cast<uint2 *>(p) = make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
+}
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16 *p) {
+  const uint2 u = *reinterpret_cast<const uint2 *>(p);
+  return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+}
+
 __device__ __forceinline__ float ldf(const float *p) { return __ldg(p); }
+__device__ __forceinline__ float lds(const float *p) { return *p; }
+__device__ __forceinline__ float lds(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 __device__ __forceinline__ float ldf(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 __device__ __forceinline__ void stf(float *p, float x) { *p = x; }
 __device__ __forceinline__ void stf(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
@@ -108,10 +125,8 @@ __device__ __forceinline__ uint64_t pk2(float lo, float hi) {
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
   return r;
 }
-__device__ __forceinline__ float sum2(uint64_t v) {
-  float lo, hi;
+__device__ __forceinline__ void upk2(uint64_t v, float &lo, float &hi) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  return lo + hi;
 }
 __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;
@@ -123,28 +138,57 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ float sigmoid(float x) { return 1.f / (1.f + ex2(-x * kLog2e)); }
 
-// sum over s of row[s] * h[s] (h packed in pairs), four independent chains
-__device__ __forceinline__ float dot32(const float *row, const uint64_t (&h2)[16]) {
-  const ulonglong2 *r = reinterpret_cast<const ulonglong2 *>(row);
-  uint64_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+// Sum over the four row groups (lane bits 3 and 4) of a lane's partial sums
+// for its four columns, as two packed pairs; every lane gets the totals.
+__device__ __forceinline__ float4 rows_reduce(uint64_t a, uint64_t b) {
+  float4 r;
+  upk2(a, r.x, r.y);
+  upk2(b, r.z, r.w);
 #pragma unroll
-  for (int i = 0; i < 8; i += 2) {
-    const ulonglong2 x = r[i], y = r[i + 1];
-    a0 = fma2(x.x, h2[2 * i], a0);
-    a1 = fma2(x.y, h2[2 * i + 1], a1);
-    a2 = fma2(y.x, h2[2 * i + 2], a2);
-    a3 = fma2(y.y, h2[2 * i + 3], a3);
+  for (int m = 8; m <= 16; m <<= 1) {
+    r.x += __shfl_xor_sync(0xffffffffu, r.x, m);
+    r.y += __shfl_xor_sync(0xffffffffu, r.y, m);
+    r.z += __shfl_xor_sync(0xffffffffu, r.z, m);
+    r.w += __shfl_xor_sync(0xffffffffu, r.w, m);
   }
-  return (sum2(a0) + sum2(a1)) + (sum2(a2) + sum2(a3));
+  return r;
 }
 
+// sum over this lane's 8 rows of x[row] * h[row][four columns] (two pairs)
+template <typename X>
+__device__ __forceinline__ float4 rows_dot(const X *x8, const uint64_t (&h2)[8][2]) {
+  const float4 x0 = ld4(x8);
+  const float4 x1 = ld4(x8 + 4);
+  const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+  uint64_t a0 = 0, a1 = 0, b0 = 0, b1 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    const uint64_t xe = pk2(xv[i], xv[i]), xo = pk2(xv[i + 1], xv[i + 1]);
+    a0 = fma2(xe, h2[i][0], a0);
+    a1 = fma2(xe, h2[i][1], a1);
+    b0 = fma2(xo, h2[i + 1][0], b0);
+    b1 = fma2(xo, h2[i + 1][1], b1);
+  }
+  return rows_reduce(add2(a0, b0), add2(a1, b1));
+}
+
+// Lane layout: lane = 8 rg + cg holds the state rows 8 rg .. 8 rg + 7 and the
+// columns 4 cg .. 4 cg + 3 (h2[i][p]: row 8 rg + i, columns 4 cg + 2p, +1), so
+// that a token reads 8 rows of d, b, c and 4 values of v from shared memory
+// per lane, and the column sums over the rows take two shuffle levels.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) gdn_diag_delta_kernel(const Params p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
+  Smem<T> &sm = *reinterpret_cast<Smem<T> *>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rg = lane >> 3, cg = lane & 7, r0 = 8 * rg, c0 = 4 * cg;
   const int H = p.num_heads, Tn = p.seq_len;
   if (tid == 0) {
     sm.misc[0] = atomicAdd(&p.ctr->ticket, 1u);
@@ -160,8 +204,8 @@ __global__ void __launch_bounds__(kThreads) gdn_diag_delta_kernel(const Params p
   const int len = (int)min((int64_t)kSeg, (int64_t)Tn - t0);
   const bool first = seg == 0, last = seg == p.nseg - 1;
   const bool transport = warp == 1;
-  const bool runs = !(first && transport);
-  GDN_DDPROBE(0);      // segment 0 needs no transport run
+  const bool runs = !(first && transport);      // segment 0 needs no transport run
+  GDN_DDPROBE(0);
   const T *vp = static_cast<const T *>(p.v), *bp = static_cast<const T *>(p.b);
   const T *cp = static_cast<const T *>(p.c), *betap = static_cast<const T *>(p.beta);
   // element (token t of this segment, s) of a [B][T][H][32] tensor
@@ -169,31 +213,30 @@ __global__ void __launch_bounds__(kThreads) gdn_diag_delta_kernel(const Params p
     return (((int64_t)bb * Tn + t0 + t) * H + hd) * 32 + s;
   };
   auto gate_at = [&](int t) -> int64_t { return ((int64_t)bb * Tn + t0 + t) * H + hd; };
+  const size_t srow = ((size_t)bb * H + hd) * kS * kD;
 
   const float a2 = -expf(p.A_log[hd * kS + lane]) * kLog2e;   // row `lane`: d = 2^(g a2)
   const bool gate_sig = (p.opts & GDN_GATE_SIGMOID) != 0;
   const bool beta_sig = (p.opts & GDN_BETA_LOGITS) != 0;
 
-  // the state column `lane`: zero, the initial state, or the identity column
-  uint64_t h2[16];
-  {
-    const size_t srow = ((size_t)bb * H + hd) * kS * kD;
+  // the state block: zero, the initial state, or the identity
+  uint64_t h2[8][2];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float x0 = 0.f, x1 = 0.f;
-      if (transport) {
-        x0 = (2 * i == lane) ? 1.f : 0.f;
-        x1 = (2 * i + 1 == lane) ? 1.f : 0.f;
-      } else if (first && p.h0) {
-        x0 = p.h0[srow + (size_t)(2 * i) * kD + lane];
-        x1 = p.h0[srow + (size_t)(2 * i + 1) * kD + lane];
-      }
-      h2[i] = pk2(x0, x1);
+  for (int i = 0; i < 8; ++i) {
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (transport) {
+      const int s = r0 + i;
+      x = make_float4(s == c0 ? 1.f : 0.f, s == c0 + 1 ? 1.f : 0.f, s == c0 + 2 ? 1.f : 0.f,
+                      s == c0 + 3 ? 1.f : 0.f);
+    } else if (first && p.h0) {
+      x = *reinterpret_cast<const float4 *>(p.h0 + srow + (size_t)(r0 + i) * kD + c0);
     }
+    h2[i][0] = pk2(x.x, x.y);
+    h2[i][1] = pk2(x.z, x.w);
   }
 
   // ---- staging: thread (warp w, lane s) handles tokens 8w .. 8w+7 of a tile ----
-  float rb[8], rc[8], rg[8], rv[8], rbeta = 0.f;
+  float rb[8], rc[8], rg8[8], rv[8], rbeta = 0.f;
   auto fetch = [&](int tt) {   // tile starting at segment token tt, into registers
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -202,7 +245,7 @@ __global__ void __launch_bounds__(kThreads) gdn_diag_delta_kernel(const Params p
       rb[i] = ok ? ldf(bp + at(t, lane)) : 0.f;
       rc[i] = ok ? ldf(cp + at(t, lane)) : 0.f;
       rv[i] = ok ? ldf(vp + at(t, lane)) : 0.f;
-      rg[i] = ok ? p.g[gate_at(t)] : 0.f;
+      rg8[i] = ok ? p.g[gate_at(t)] : 0.f;
     }
     const int tb = tt + 8 * warp + lane;
     rbeta = (lane < 8 && tb < len) ? ldf(betap + gate_at(tb)) : 0.f;
@@ -212,12 +255,10 @@ __global__ void __launch_bounds__(kThreads) gdn_diag_delta_kernel(const Params p
     for (int i = 0; i < 8; ++i) {
       const int tl = 8 * warp + i;
       const bool ok = tt + tl < len;   // a padded token is an identity step
-      const float g = gate_sig ? sigmoid(rg[i]) : rg[i];
-      const float d = ok ? ex2(g * a2) : 1.f;
-      sm.row[buf][0][tl][lane] = rb[i] * d;
-      sm.row[buf][1][tl][lane] = d;
-      sm.row[buf][2][tl][lane] = rb[i];
-      sm.row[buf][3][tl][lane] = rc[i];
+      const float g = gate_sig ? sigmoid(rg8[i]) : rg8[i];
+      sm.row[buf][0][tl][lane] = ok ? ex2(g * a2) : 1.f;
+      sm.row[buf][1][tl][lane] = rb[i];
+      sm.row[buf][2][tl][lane] = rc[i];
       sm.vt[buf][tl][lane] = rv[i];
     }
     if (lane < 8) {
@@ -234,50 +275,71 @@ __global__ void __launch_bounds__(kThreads) gdn_diag_delta_kernel(const Params p
     const int buf = it & 1, tt = it * kTile;
     if (it + 1 < ntiles) fetch(tt + kTile);
     if (runs) {
-      float *out = transport ? &sm.rbuf[0][0] : &sm.obuf[0][0];
+      T *out = transport ? &sm.rbuf[0][0] : &sm.obuf[0][0];
 #pragma unroll 1
       for (int tl = 0; tl < kTile; ++tl) {
-        const float *r_bd = sm.row[buf][0][tl], *r_d = sm.row[buf][1][tl];
-        const float *r_b = sm.row[buf][2][tl], *r_c = sm.row[buf][3][tl];
-        const float pred = dot32(r_bd, h2);              // hbar^T b, column `lane`
-        const float vj = transport ? 0.f : sm.vt[buf][tl][lane];
-        const float u = sm.bt[buf][tl] * (vj - pred);
-        const uint64_t uu = pk2(u, u);
-        const ulonglong2 *D2 = reinterpret_cast<const ulonglong2 *>(r_d);
-        const ulonglong2 *B2 = reinterpret_cast<const ulonglong2 *>(r_b);
+        const float *rd = &sm.row[buf][0][tl][r0], *rbk = &sm.row[buf][1][tl][r0];
+        const float4 d0 = *reinterpret_cast<const float4 *>(rd);
+        const float4 d1 = *reinterpret_cast<const float4 *>(rd + 4);
+        const float4 k0 = *reinterpret_cast<const float4 *>(rbk);
+        const float4 k1 = *reinterpret_cast<const float4 *>(rbk + 4);
+        const float dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+        const float kv[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+        // hbar = d (.) h, and b^T hbar over this lane's rows
+        uint64_t a0 = 0, a1 = 0, e0 = 0, e1 = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const ulonglong2 d = D2[i], bk = B2[i];
-          h2[2 * i] = fma2(bk.x, uu, mul2(d.x, h2[2 * i]));
-          h2[2 * i + 1] = fma2(bk.y, uu, mul2(d.y, h2[2 * i + 1]));
+          const uint64_t dd = pk2(dv[i], dv[i]), kk = pk2(kv[i], kv[i]);
+          h2[i][0] = mul2(dd, h2[i][0]);
+          h2[i][1] = mul2(dd, h2[i][1]);
+          if (i & 1) {
+            e0 = fma2(kk, h2[i][0], e0);
+            e1 = fma2(kk, h2[i][1], e1);
+          } else {
+            a0 = fma2(kk, h2[i][0], a0);
+            a1 = fma2(kk, h2[i][1], a1);
+          }
         }
-        const float o = dot32(r_c, h2);
-        if (tt + tl < len) out[(tt + tl) * 32 + lane] = o;
+        const float4 pred = rows_reduce(add2(a0, e0), add2(a1, e1));
+        const float4 vv = transport ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                    : *reinterpret_cast<const float4 *>(&sm.vt[buf][tl][c0]);
+        const float be = sm.bt[buf][tl];
+        const uint64_t u0 = pk2(be * (vv.x - pred.x), be * (vv.y - pred.y));
+        const uint64_t u1 = pk2(be * (vv.z - pred.z), be * (vv.w - pred.w));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint64_t kk = pk2(kv[i], kv[i]);
+          h2[i][0] = fma2(kk, u0, h2[i][0]);
+          h2[i][1] = fma2(kk, u1, h2[i][1]);
+        }
+        const float4 o = rows_dot(&sm.row[buf][2][tl][r0], h2);
+        if (rg == 0 && tt + tl < len) st4(out + (tt + tl) * 32 + c0, o);
       }
     }
     if (it + 1 < ntiles) commit(buf ^ 1, tt + kTile);
     __syncthreads();
   }
-
   GDN_DDPROBE(1);
+
   // ---- the start state and the composition ----
-  // M[s][k] (column k is transport lane k) over rows 0-1 of the first
-  // buffer, X[s][j] over rows 2-3 (32 x 32 floats each)
-  float (*Ms)[kS] = reinterpret_cast<float (*)[kS]>(&sm.row[0][0][0][0]);
-  float (*Xs)[kD] = reinterpret_cast<float (*)[kD]>(&sm.row[0][2][0][0]);
-  {
-    float x[32];
+  // M^T[m][s] = M[s][m] (column m of M is the run from e_m) and X[s][j], over
+  // the tile rows (dead after the loop)
+  float (*Mt)[kS] = reinterpret_cast<float (*)[kS]>(&sm.row[0][0][0][0]);
+  float (*Xs)[kD] = Mt + kS;
+  if (runs) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float lo, hi;
-      asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(h2[i]));
-      x[2 * i] = lo;
-      x[2 * i + 1] = hi;
-    }
-    float(*dst)[32] = transport ? Ms : Xs;
-    if (runs) {
-#pragma unroll
-      for (int s = 0; s < 32; ++s) dst[s][lane] = x[s];
+    for (int i = 0; i < 8; ++i) {
+      float x0, x1, x2, x3;
+      upk2(h2[i][0], x0, x1);
+      upk2(h2[i][1], x2, x3);
+      if (transport) {
+        Mt[c0][r0 + i] = x0;
+        Mt[c0 + 1][r0 + i] = x1;
+        Mt[c0 + 2][r0 + i] = x2;
+        Mt[c0 + 3][r0 + i] = x3;
+      } else {
+        *reinterpret_cast<float4 *>(&Xs[r0 + i][c0]) = make_float4(x0, x1, x2, x3);
+      }
     }
   }
   if (!first && tid == 0) {
@@ -296,27 +358,46 @@ __global__ void __launch_bounds__(kThreads) gdn_diag_delta_kernel(const Params p
   }
   GDN_DDPROBE(2);
   __syncthreads();
-  // h_start column `lane` (segment 0: M = I, X = its run, so nothing to add)
-  float hs[32];
+  // h_start (segment 0: M = I and X is already its end state, so zero here)
   const bool have_start = !first && sm.misc[2] != 0u;
   {
     const float *src = p.hend + (size_t)(ticket - (first ? 0u : (uint32_t)units)) * kS * kD;
-#pragma unroll
-    for (int s = 0; s < 32; ++s) hs[s] = have_start ? __ldcg(src + s * kD + lane) : 0.f;
+    for (int q = tid; q < kS * kD / 4; q += kThreads) {
+      const float4 x = have_start ? __ldcg(reinterpret_cast<const float4 *>(src) + q)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      reinterpret_cast<float4 *>(&sm.hs[0][0])[q] = x;
+    }
   }
-  // end state rows 16 w .. 16 w + 15: X + M h_start (segment 0: X)
+  __syncthreads();
+  // end state X + M h_start: thread tid computes row tid / 2, columns
+  // 16 (tid & 1) .. + 15
   {
-    uint64_t hs2[16];
+    const int s = tid >> 1, cb = 16 * (tid & 1);
+    float e[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) hs2[i] = pk2(hs[2 * i], hs[2 * i + 1]);
-    float *dst = p.hend + (size_t)ticket * kS * kD;
-    float *fin = last && p.hN ? p.hN + ((size_t)bb * H + hd) * kS * kD : nullptr;
+    for (int j = 0; j < 16; ++j) e[j] = Xs[s][cb + j];
+    if (!first) {
 #pragma unroll 4
-    for (int r = 0; r < 16; ++r) {
-      const int s = 16 * warp + r;
-      const float e = Xs[s][lane] + (first ? 0.f : dot32(Ms[s], hs2));
-      __stcg(dst + s * kD + lane, e);
-      if (fin) fin[s * kD + lane] = e;
+      for (int m = 0; m < kS; ++m) {
+        const float msm = Mt[m][s];
+        const float4 *hr = reinterpret_cast<const float4 *>(&sm.hs[m][cb]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 x = hr[q];
+          e[4 * q] = fmaf(msm, x.x, e[4 * q]);
+          e[4 * q + 1] = fmaf(msm, x.y, e[4 * q + 1]);
+          e[4 * q + 2] = fmaf(msm, x.z, e[4 * q + 2]);
+          e[4 * q + 3] = fmaf(msm, x.w, e[4 * q + 3]);
+        }
+      }
+    }
+    float *dst = p.hend + (size_t)ticket * kS * kD + (size_t)s * kD + cb;
+    float *fin = last && p.hN ? p.hN + srow + (size_t)s * kD + cb : nullptr;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 x = make_float4(e[4 * q], e[4 * q + 1], e[4 * q + 2], e[4 * q + 3]);
+      __stcg(reinterpret_cast<float4 *>(dst) + q, x);
+      if (fin) reinterpret_cast<float4 *>(fin)[q] = x;
     }
     __threadfence();
   }
@@ -325,16 +406,28 @@ __global__ void __launch_bounds__(kThreads) gdn_diag_delta_kernel(const Params p
   GDN_DDPROBE(3);
 
   // ---- outputs: o = o0 + r^T h_start, then the block epilogue ----
+  // lane j: column j of h_start in registers, the row r_t broadcast
   {
-    uint64_t hs2[16];
+    float hcol[32];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) hs2[i] = pk2(hs[2 * i], hs[2 * i + 1]);
+    for (int q = 0; q < 32; ++q) hcol[q] = sm.hs[q][lane];
     const float dsk = p.D_skip ? p.D_skip[hd] : 0.f;
     T *op = static_cast<T *>(p.o);
 #pragma unroll 1
     for (int t = warp; t < len; t += 2) {
-      float o = sm.obuf[t][lane];
-      if (!first) o += dot32(sm.rbuf[t], hs2);
+      float o = lds(&sm.obuf[t][lane]);
+      if (!first) {
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < 32; q += 4) {
+          const float4 r = ld4(&sm.rbuf[t][q]);
+          a[0] = fmaf(r.x, hcol[q], a[0]);
+          a[1] = fmaf(r.y, hcol[q + 1], a[1]);
+          a[2] = fmaf(r.z, hcol[q + 2], a[2]);
+          a[3] = fmaf(r.w, hcol[q + 3], a[3]);
+        }
+        o += (a[0] + a[1]) + (a[2] + a[3]);
+      }
       if (p.D_skip) o = fmaf(dsk, ldf(vp + at(t, lane)), o);
       if (p.out_gate) o *= p.out_gate[gate_at(t)];
       stf(op + at(t, lane), o);
@@ -356,7 +449,7 @@ __global__ void __launch_bounds__(kThreads) gdn_diag_delta_kernel(const Params p
 
 template <typename T>
 cudaError_t launch_t(const Params &p, int64_t tasks, cudaStream_t stream) {
-  const int smem = (int)sizeof(Smem);
+  const int smem = (int)sizeof(Smem<T>);
   cudaError_t err = cudaFuncSetAttribute(gdn_diag_delta_kernel<T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
