@@ -1138,24 +1138,48 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
   }
 }
 
-// H_(s+1) = M_s H_s + X_s for s = 1 .. S-2, per (sequence, head) and 32 value
-// columns, in fp32 (one CTA walks the segments in order; M_s is dk x dk).
-__global__ void __launch_bounds__(256) seg_compose_kernel(const FwdParams p) {
-  const int c0 = blockIdx.x * 32, h = blockIdx.y, n = blockIdx.z;
-  const int H = p.num_heads, dv = p.dv, S = p.seg_count;
-  for (int s = 1; s + 1 < S; ++s) {
-    const size_t unit = ((size_t)n * S + s) * H + h;
-    const float *M = p.seg_m + unit * DK * DK;
-    const float *Hs = p.seg_state + unit * DK * dv;
-    const float *X = p.seg_x + unit * DK * dv;
-    float *Hn = p.seg_state + (unit + H) * DK * dv;  // segment s + 1
-    for (int idx = threadIdx.x; idx < DK * 32; idx += blockDim.x) {
-      const int r = idx >> 5, c = c0 + (idx & 31);
-      float acc = X[(size_t)r * dv + c];
-      for (int k = 0; k < DK; ++k) acc = fmaf(M[(size_t)r * DK + k], Hs[(size_t)k * dv + c], acc);
-      Hn[(size_t)r * dv + c] = acc;
+// One step of the composition, H_(s+1) = M_s H_s + X_s (fp32; M_s is dk x dk),
+// for a block of 32 rows and 32 value columns of one (sequence, head): the
+// CTA stages its 32 rows of M_s and the 32 columns of H_s in shared memory
+// (every load in flight at once), then lane = column and each warp takes 4
+// rows.  grid: (dv / 32 * dk / 32, H, N).
+__global__ void __launch_bounds__(256) seg_compose_kernel(const FwdParams p, int s) {
+  __shared__ __align__(16) float ms[32][DK + 4];
+  __shared__ __align__(16) float hs[DK][32];
+  const int nc = p.dv / 32;
+  const int c0 = (blockIdx.x % nc) * 32, r0 = (blockIdx.x / nc) * 32;
+  const int h = blockIdx.y, n = blockIdx.z;
+  const int H = p.num_heads, dv = p.dv, S = p.seg_count, tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const size_t unit = ((size_t)n * S + s) * H + h;
+  const float *M = p.seg_m + unit * DK * DK;
+  const float *Hs = p.seg_state + unit * DK * dv;
+  const float *X = p.seg_x + unit * DK * dv;
+  float *Hn = p.seg_state + (unit + H) * DK * dv;  // segment s + 1
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int q = tid + 256 * e;                  // 1024 float4 of each tile
+    const int mr = q / (DK / 4), mc = q % (DK / 4);
+    *reinterpret_cast<float4 *>(&ms[mr][4 * mc]) =
+        *reinterpret_cast<const float4 *>(M + (size_t)(r0 + mr) * DK + 4 * mc);
+    const int hr = q / 8, hc = q % 8;
+    *reinterpret_cast<float4 *>(&hs[hr][4 * hc]) =
+        *reinterpret_cast<const float4 *>(Hs + (size_t)hr * dv + c0 + 4 * hc);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 4 * warp + i;
+    float a0 = X[(size_t)(r0 + r) * dv + c0 + lane], a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 8
+    for (int q = 0; q < DK / 4; ++q) {
+      const float4 m = *reinterpret_cast<const float4 *>(&ms[r][4 * q]);
+      a0 = fmaf(m.x, hs[4 * q][lane], a0);
+      a1 = fmaf(m.y, hs[4 * q + 1][lane], a1);
+      a2 = fmaf(m.z, hs[4 * q + 2][lane], a2);
+      a3 = fmaf(m.w, hs[4 * q + 3][lane], a3);
     }
-    __syncthreads();  // the next segment reads what this one wrote (this CTA's columns only)
+    Hn[(size_t)(r0 + r) * dv + c0 + lane] = (a0 + a1) + (a2 + a3);
   }
 }
 
@@ -1206,8 +1230,9 @@ cudaError_t launch_tc128(const FwdParams &p, cudaStream_t stream) {
   const dim3 grid_a(p.dv / kDvt + (S > 2 ? DK / kDvt : 0), p.num_heads, p.num_seqs * (S - 1));
   kern<<<grid_a, Cfg::kWarps * 32, L::ALLOC, stream>>>(a, tq, tk, tv);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  if (S > 2) {
-    seg_compose_kernel<<<dim3(p.dv / 32, p.num_heads, p.num_seqs), 256, 0, stream>>>(p);
+  for (int s = 1; s + 1 < S; ++s) {   // one launch per step, in order
+    seg_compose_kernel<<<dim3(p.dv / 32 * (DK / 32), p.num_heads, p.num_seqs), 256, 0, stream>>>(
+        p, s);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   FwdParams b = p;
