@@ -381,7 +381,8 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
         d["o"] = torch.empty_like(d["v"])
         d["final_state"] = torch.empty((N, w.H, w.dk, w.dv), dtype=torch.float32, device=dev)
         sets.append(d)
-    ws = G.new_workspace(N, w.H, w.dk, w.dv, G.GDN_SEQ_SPLIT if split else 0, device=dev)
+    ws = G.new_workspace(N, w.H, w.dk, w.dv, G.GDN_SEQ_SPLIT if split else 0, device=dev,
+                         seq_len=host["q"].shape[1] if split and host["cu_seqlens"] is None else None)
     kname = G.gdn_fwd_kernel_name(w.dk, w.dv, host["q"].dtype, G.GDN_QK_L2NORM if fused else 0,
                                   chunk_size=args.chunk)
     stream = torch.cuda.current_stream(dev)
@@ -520,10 +521,10 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
                    **({"fused": "q/k L2 norm + beta logits (sigmoid) + (o + D v) * out_gate "
                                 "epilogue in the kernel"} if fused else {}),
                    **({"seq_split": f"GDN_SEQ_SPLIT: {segments} segment(s) per sequence"
-                                    + (" (first launch: segment 0 + the middle segments' state "
-                                       "maps; compose; second launch: segments 1..; kernel_ms "
-                                       "is the whole call)" if segments > 1 else
-                                       " (not split: the units fill the SMs)")}
+                                    + (" (one launch: segment 0 + the later segments from zero "
+                                       "and from the identity; composition steps; output "
+                                       "correction; kernel_ms is the whole call)" if segments > 1
+                                       else " (not split: the units fill the SMs)")}
                       if split else {}),
                    "l2": "two resident input sets of "
                          f"{sum(sets[0][n].numel() * sets[0][n].element_size() for n in names) / 1e6:.0f}"
@@ -544,8 +545,8 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "overlap": "two device sets: step i+1's inputs copy in while step i "
                            "computes and step i-1's result copies out"},
-        # a split call launches the first pass, the composition and the second pass
-        "gpu_launches": args.steps * (3 if segments > 1 else launches_per_step(kname)),
+        # a split call: the segments, S - 1 composition steps and the correction
+        "gpu_launches": args.steps * (segments + 1 if segments > 1 else launches_per_step(kname)),
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

@@ -104,25 +104,37 @@ enum {
    * 3.5); this is the device-side counterpart. */
   GDN_DEBUG_CHECKS = 1u << 4,
   /* gdn_fwd: let the head_dim_k 128 tensor-core kernel cut each sequence of a
-   * dense call (cu_seqlens NULL) into up to 3 segments of whole chunks when
-   * the (sequence, head, 64 value columns) units alone leave SMs idle.  The
-   * chunk transition is affine in the state, H' = M H + X, so a segment's
-   * transition composes its chunks' ones: a first launch runs segment 0 and,
-   * at the same time, the middle segments from a zero state with dk extra
-   * identity columns (giving their X and M); a small kernel composes the
-   * segments' entry states; a second launch runs segments 1.. from them and
-   * writes the outputs.  The result equals the unsplit one up to rounding.
-   * The workspace must be sized with this flag (gdn_fwd_workspace_size).
+   * dense call (cu_seqlens NULL, no block epilogue) into up to 8 segments of
+   * whole chunks when the (sequence, head, 64 value columns) units alone
+   * leave SMs idle (gdn_fwd_split_segments gives the plan).  The chunk
+   * transition is affine in the state, H' = M H + X, and each output is
+   * affine in the state entering the segment, o = o0 + r H, so: one launch
+   * runs segment 0 from the caller's state and every later segment from a
+   * zero state (o0, X) and, on dk extra columns, from the identity (r, M);
+   * small kernels compose the segments' entry states in order and add r H to
+   * the later segments' outputs.  The result equals the unsplit one up to
+   * rounding.  The workspace must be sized with gdn_fwd_split_workspace_size.
    * Other calls ignore the flag. */
   GDN_SEQ_SPLIT = 1u << 5
 };
 
 /* Bytes of device workspace gdn_fwd needs for these sizes (>= 256; the first
- * 256 bytes hold the device status word; with GDN_SEQ_SPLIT and head_dim_k
- * 128, the segments' states and maps follow).  Never fails; returns 0 only for
- * nonsensical sizes (any argument <= 0). */
+ * 256 bytes hold the device status word).  Not enough for a call that
+ * GDN_SEQ_SPLIT cuts into segments: size those with
+ * gdn_fwd_split_workspace_size.  Never fails; returns 0 only for nonsensical
+ * sizes (any argument <= 0). */
 size_t gdn_fwd_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_dim_k,
                               int32_t head_dim_v, uint32_t flags);
+
+/* Bytes of device workspace a dense gdn_fwd call with GDN_SEQ_SPLIT needs
+ * (batch = num_seqs sequences of seq_len tokens): the status word, each
+ * segment's entry state, X and M (fp32, up to 8 segments), and with
+ * head_dim_k 128 the per-token maps r of the segments (bf16, [tokens][heads]
+ * [head_dim_k]).  A split call with less returns GDN_ERR_WORKSPACE; calls the
+ * plan leaves unsplit need only gdn_fwd_workspace_size.  Returns 0 for
+ * nonsensical sizes. */
+size_t gdn_fwd_split_workspace_size(int32_t num_seqs, int32_t seq_len, int32_t num_heads,
+                                    int32_t head_dim_k, int32_t head_dim_v);
 
 /* Enqueue a zero fill of the first `workspace_bytes` bytes of `workspace` on
  * `stream`.  A workspace must be zeroed once before its first use by gdn_fwd
@@ -213,13 +225,14 @@ gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
                    int32_t chunk_size, gdn_dtype dtype, uint32_t flags,
                    void *workspace, size_t workspace_bytes, void *stream);
 
-/* The number of segments GDN_SEQ_SPLIT cuts each sequence of a gdn_fwd call
- * with these arguments into, on the current device (the plan depends on its
- * SM count): 3 or more when the call is split, and then gdn_fwd launches
- * three kernels (segment 0 with the middle segments' maps, their
- * composition, the later segments); 1 when it is not split (one kernel).
- * varlen != 0 stands for a call with cu_seqlens (never split).  Returns 0
- * for sizes gdn_fwd rejects.  Host only; launches nothing. */
+/* The number of segments S GDN_SEQ_SPLIT cuts each sequence of a gdn_fwd
+ * call with these arguments (and no block epilogue: a call with D_skip or
+ * out_gate is never split) into, on the current device (the plan depends on
+ * its SM count): S >= 2 when the call is split, and then gdn_fwd launches S +
+ * 1 kernels (every segment in one launch, S - 1 composition steps, the
+ * output correction); 1 when it is not split (one kernel).  varlen != 0
+ * stands for a call with cu_seqlens (never split).  Returns 0 for sizes
+ * gdn_fwd rejects.  Host only; launches nothing. */
 int32_t gdn_fwd_split_segments(int32_t num_seqs, int32_t seq_len, int32_t num_heads,
                                int32_t head_dim_k, int32_t head_dim_v, int32_t chunk_size,
                                gdn_dtype dtype, uint32_t flags, int32_t varlen);

@@ -48,6 +48,8 @@ namespace gdn {
 // Every host-side check of gdn_fwd, in one place, so that each entry point
 // that runs the forward pass validates its arguments before it enqueues any
 // work.  Fills `call` on success.
+int plan_segments(FwdParams &p, int chunk, gdn_dtype dtype);
+
 gdn_status fwd_validate(const void *q, const void *k, const void *v, const float *g,
                         const void *beta, const float *initial_state,
                         const int32_t *cu_seqlens, void *o, float *final_state,
@@ -134,25 +136,40 @@ gdn_status fwd_validate(const void *q, const void *k, const void *v, const float
   p.ext.v = p.ext.o = r * head_dim_v;
   p.ext.g = p.ext.beta = p.ext.gate = r;
   p.ext.s0 = p.ext.sN = (int64_t)num_seqs * num_heads * head_dim_k * head_dim_v;
+  // a call that will be split keeps its per-token maps in the workspace
+  FwdParams plan = p;
+  if (plan_segments(plan, chunk_size, dtype) > 1 &&
+      workspace_bytes <
+          gdn_fwd_split_workspace_size(num_seqs, seq_len, num_heads, head_dim_k, head_dim_v))
+    return GDN_ERR_WORKSPACE;
   return GDN_OK;
 }
 
 // The split plan of GDN_SEQ_SPLIT: fills p.seg_len / p.seg_count (0 when
-// the call is not split) and returns the segment count (1: not split).
+// the call is not split) and returns the segment count (1: not split).  The
+// block epilogue is not combined with a split (the correction would have to
+// pass through it): such calls run unsplit.
 int plan_segments(FwdParams &p, int chunk, gdn_dtype dtype) {
   p.seg_len = p.seg_count = 0;
-  if (!(p.flags & GDN_SEQ_SPLIT) || chunk != kChunk || !use_tc(p.dk, p.dv, dtype, p.flags))
+  if (!(p.flags & GDN_SEQ_SPLIT) || chunk != kChunk || !use_tc(p.dk, p.dv, dtype, p.flags) ||
+      p.d_skip || p.out_gate)
     return 1;
   // cut each sequence into segments of whole chunks, computed in parallel
   const int s = seq_split_segments(p);
-  if (s < 3) return 1;
+  if (s < 2) return 1;
   const int64_t chunks = (p.seq_len + kChunk - 1) / kChunk;
   const int64_t seg_len = ((chunks + s - 1) / s) * kChunk;
   const int64_t count = (p.seq_len + seg_len - 1) / seg_len;
-  if (count < 3 || count > kMaxSegments) return 1;
+  if (count < 2 || count > kMaxSegments) return 1;
   p.seg_len = (int32_t)seg_len;
   p.seg_count = (int32_t)count;
   return p.seg_count;
+}
+
+// Byte offset of the per-token maps r in a split call's workspace.
+size_t split_r_offset(int64_t num_seqs, int64_t num_heads, int64_t dk, int64_t dv) {
+  const size_t seg = (size_t)4 * num_seqs * kMaxSegments * num_heads * dk * (2 * dv + dk);
+  return (kStatusBytes + seg + 255) & ~(size_t)255;
 }
 
 // Enqueue the kernels of a call that fwd_validate accepted.
@@ -164,13 +181,15 @@ gdn_status fwd_launch(const FwdCall &call, cudaStream_t stream) {
   // CUDA-core kernel
   FwdParams p = call.p;
   if (plan_segments(p, call.chunk, call.dtype) > 1) {
-    // the segments' states, X and M follow the status record in the workspace
-    float *base = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(p.status) +
-                                            kStatusBytes);
+    // the segments' states, X and M follow the status record in the
+    // workspace, then the per-token maps r (fwd_validate checked the size)
+    unsigned char *ws = reinterpret_cast<unsigned char *>(p.status);
+    float *base = reinterpret_cast<float *>(ws + kStatusBytes);
     const size_t vals = (size_t)p.num_seqs * kMaxSegments * p.num_heads * p.dk * p.dv;
     p.seg_state = base;
     p.seg_x = base + vals;
     p.seg_m = base + 2 * vals;
+    p.seg_r = ws + split_r_offset(p.num_seqs, p.num_heads, p.dk, p.dv);
   }
   const cudaError_t err =
       call.chunk == kChunk && use_tc(p.dk, p.dv, call.dtype, p.flags)
@@ -192,6 +211,16 @@ size_t gdn_fwd_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_
     bytes += (size_t)4 * num_seqs * gdn::kMaxSegments * num_heads * head_dim_k *
              (2 * (size_t)head_dim_v + head_dim_k);
   return bytes;
+}
+
+size_t gdn_fwd_split_workspace_size(int32_t num_seqs, int32_t seq_len, int32_t num_heads,
+                                    int32_t head_dim_k, int32_t head_dim_v) {
+  if (num_seqs <= 0 || seq_len < 0 || num_heads <= 0 || head_dim_k <= 0 || head_dim_v <= 0)
+    return 0;
+  if (head_dim_k != 128)
+    return gdn_fwd_workspace_size(num_seqs, num_heads, head_dim_k, head_dim_v, GDN_SEQ_SPLIT);
+  return gdn::split_r_offset(num_seqs, num_heads, head_dim_k, head_dim_v) +
+         (size_t)2 * num_seqs * seq_len * num_heads * head_dim_k;
 }
 
 int32_t gdn_fwd_split_segments(int32_t num_seqs, int32_t seq_len, int32_t num_heads,

@@ -298,16 +298,17 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
   const int H = p.num_heads, dv = p.dv;
 
   // The unit: a whole sequence, or one segment of a split sequence (dense
-  // inputs).  A transport segment also has dk/64 extra column tiles that carry
-  // the identity through the segment's chunks (its state map's M).
+  // inputs).  Segments after the first run from zero ("transport" mode) and
+  // have dk/64 extra column tiles that carry the identity through the
+  // segment's chunks (its state map's M and its per-token reads r).
   constexpr bool segm = (kF & kFSeg) != 0;
   int n = blockIdx.z, seg = 0;
   bool transport = false;
   int64_t start, len;
   if constexpr (segm) {
-    n = blockIdx.z / p.seg_launch;
-    seg = p.seg_first + blockIdx.z % p.seg_launch;
-    transport = seg >= p.seg_transport;
+    n = blockIdx.z / p.seg_count;
+    seg = blockIdx.z % p.seg_count;
+    transport = seg > 0;
     start = (int64_t)n * p.seq_len + (int64_t)seg * p.seg_len;
     const int64_t rest = p.seq_len - (int64_t)seg * p.seg_len;  // > 0 by construction
     len = rest < p.seg_len ? rest : p.seg_len;
@@ -847,7 +848,7 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
         // ---- E2b: O = diag(gamma) (Q H) + P U (row = token); each thread
         // stores its row of O, value columns ocb .. ocb + 16 nq - 1 ----
         const size_t orow_idx = (size_t)(start + (int64_t)c * 64 + row) * H + h;
-        const bool st = row < valid && !transport;  // (a transport segment stores no output)
+        const bool st = row < valid;
         const __nv_bfloat16 *vrow = static_cast<const __nv_bfloat16 *>(p.v) + orow_idx * dv + col0;
         if (epi && st) {  // v is reloaded (its tile now holds U~)
           prefetch_l1(vrow + ocb);
@@ -859,7 +860,10 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
         GDN_PHASE(1);
         tc_fence_after();
         {
-          __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.o) + orow_idx * dv + col0;
+          // o (a later segment's o0), or r on the transport columns
+          __nv_bfloat16 *orow =
+              mtile ? static_cast<__nv_bfloat16 *>(p.seg_r) + orow_idx * DK + col0
+                    : static_cast<__nv_bfloat16 *>(p.o) + orow_idx * dv + col0;
           const uint64_t gi2 = pk2(gi, gi);
 #pragma unroll 1
           for (int q2 = ocb / 16; q2 < ocb / 16 + nq; ++q2) {
@@ -1020,13 +1024,10 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
               make_uint4(pack_bf16(x[8 * q], x[8 * q + 1]), pack_bf16(x[8 * q + 2], x[8 * q + 3]),
                          pack_bf16(x[8 * q + 4], x[8 * q + 5]), pack_bf16(x[8 * q + 6], x[8 * q + 7]));
       };
-      // the initial state: the caller's (whole sequence, first segment), the
-      // composed one of a later segment, zero (a transport segment's value
-      // columns) or the identity (its transport columns)
-      const float *s_in = transport ? nullptr
-                          : seg > 0 ? p.seg_state + seg_row
-                          : p.s0    ? p.s0 + state_row
-                                    : nullptr;
+      // the initial state: the caller's (whole sequence, first segment), zero
+      // (a later segment's value columns) or the identity (its transport
+      // columns)
+      const float *s_in = transport ? nullptr : p.s0 ? p.s0 + state_row : nullptr;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1115,13 +1116,13 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
       if (warp == C::kWarpE2aIssue && lane == 0 && issued > 0)
         mbar_wait_bounded(bar(B_D1_FULL + ((issued - 1) & 1)), ((issued - 1) >> 1) & 1,
                           kWaitTimeoutNs);
-      // the final state: the caller's (whole or last segment), the next
-      // segment's initial state, or a transport segment's X / M
+      // the final state: the caller's (whole sequence), the state entering
+      // segment 1 (segment 0), or a later segment's X / M
       float *s_out = nullptr;
       if (mtile) s_out = p.seg_m + unit * DK * DK + (size_t)krow * DK + col0 + cb;
       else if (transport) s_out = p.seg_x + seg_row;
-      else if (!segm || seg == p.seg_count - 1) s_out = p.sN ? p.sN + state_row : nullptr;
-      else if (p.seg_write_next) s_out = p.seg_state + seg_row + (size_t)H * DK * dv;  // segment seg + 1
+      else if (segm) s_out = p.seg_state + seg_row + (size_t)H * DK * dv;  // segment 1
+      else s_out = p.sN ? p.sN + state_row : nullptr;
       if (s_out && !*S.abort_flag) {
 #pragma unroll
         for (int q = 0; q < 8; ++q)
@@ -1138,8 +1139,9 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
   }
 }
 
-// One step of the composition, H_(s+1) = M_s H_s + X_s (fp32; M_s is dk x dk),
-// for a block of 32 rows and 32 value columns of one (sequence, head): the
+// One step of the composition, H_(s+1) = M_s H_s + X_s (fp32; M_s is dk x dk;
+// the last step gives the caller's final state), for a block of 32 rows and
+// 32 value columns of one (sequence, head): the
 // CTA stages its 32 rows of M_s and the 32 columns of H_s in shared memory
 // (every load in flight at once), then lane = column and each warp takes 4
 // rows.  grid: (dv / 32 * dk / 32, H, N).
@@ -1155,7 +1157,10 @@ __global__ void __launch_bounds__(256) seg_compose_kernel(const FwdParams p, int
   const float *M = p.seg_m + unit * DK * DK;
   const float *Hs = p.seg_state + unit * DK * dv;
   const float *X = p.seg_x + unit * DK * dv;
-  float *Hn = p.seg_state + (unit + H) * DK * dv;  // segment s + 1
+  // segment s + 1, or after the last segment the caller's final state
+  float *Hn = s + 1 < S ? p.seg_state + (unit + H) * DK * dv
+                        : p.sN ? p.sN + ((size_t)n * H + h) * DK * dv : nullptr;
+  if (Hn == nullptr) return;  // uniform over the CTA
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const int q = tid + 256 * e;                  // 1024 float4 of each tile
@@ -1180,6 +1185,126 @@ __global__ void __launch_bounds__(256) seg_compose_kernel(const FwdParams p, int
       a3 = fmaf(m.w, hs[4 * q + 3][lane], a3);
     }
     Hn[(size_t)(r0 + r) * dv + c0 + lane] = (a0 + a1) + (a2 + a3);
+  }
+}
+
+// The correction of a split sequence's later segments: o[t] += r[t] H_s for
+// every token t of segment s >= 1 (r [tokens][H][dk] and H_s in bf16 on
+// mma.sync, fp32 sums, o read and written in bf16).  A CTA takes up to
+// kCorrBlocks blocks of 64 tokens inside one segment and 64 NT value columns
+// of one (sequence, head), so that each row of r is read once per NT column
+// tiles: H_s is converted once, and the next block's rows of r and o are
+// fetched (cp.async) while the current one is computed; warp w computes rows
+// 16 (w % 4) .. + 15 of a block, value columns 64 (w / 4) .. + 63.  grid:
+// (dv / (64 NT), (S - 1) * block groups per segment, N H).
+constexpr int kCorrBlocks = 4;
+constexpr int kCorrLR = DK + 8;   // padded bf16 rows (16-byte multiples)
+template <int NT>
+struct CorrSmem {
+  static constexpr int LH = 64 * NT + 8;
+  static constexpr int BYTES = (DK * LH + 2 * 64 * kCorrLR + 2 * 64 * LH) * 2;
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool ok) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(ok ? 16 : 0)
+               : "memory");
+}
+
+template <int NT>
+__global__ void __launch_bounds__(128 * NT) seg_correct_kernel(const FwdParams p, int groups) {
+  constexpr int kCorrLH = CorrSmem<NT>::LH, NTH = 128 * NT, NCOL = 64 * NT;
+  extern __shared__ __align__(16) uint8_t corr_smem[];
+  __nv_bfloat16 *sh = reinterpret_cast<__nv_bfloat16 *>(corr_smem);   // [DK][LH]
+  __nv_bfloat16 *sr = sh + DK * kCorrLH;                                // [2][64][LR]
+  __nv_bfloat16 *so = sr + 2 * 64 * kCorrLR;                            // [2][64][LH]
+  const int H = p.num_heads, dv = p.dv, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c0 = blockIdx.x * NCOL, n = blockIdx.z / H, h = blockIdx.z % H;
+  const int s = 1 + (int)blockIdx.y / groups, grp = (int)blockIdx.y % groups;
+  const int64_t seg0 = (int64_t)s * p.seg_len;                        // segment start
+  const int64_t seg_end = seg0 + p.seg_len < p.seq_len ? seg0 + p.seg_len : p.seq_len;
+  const int64_t t_first = seg0 + (int64_t)grp * kCorrBlocks * 64;
+  if (t_first >= seg_end) return;   // uniform over the CTA
+  const int nb = (int)((seg_end - t_first + 63) / 64) < kCorrBlocks
+                     ? (int)((seg_end - t_first + 63) / 64)
+                     : kCorrBlocks;
+  const __nv_bfloat16 *r = static_cast<const __nv_bfloat16 *>(p.seg_r);
+  __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
+  const size_t tok0 = (size_t)n * p.seq_len;   // token index of the sequence's start
+  auto fetch = [&](int b) {   // rows of r and o of block b into buffer b & 1
+    const int64_t t = t_first + (int64_t)b * 64;
+    const int valid = (int)(seg_end - t < 64 ? seg_end - t : 64);
+    __nv_bfloat16 *dr = sr + (b & 1) * 64 * kCorrLR, *dO = so + (b & 1) * 64 * kCorrLH;
+    for (int idx = tid; idx < 64 * DK / 8; idx += NTH) {
+      const int rr = idx / (DK / 8), cc = (idx % (DK / 8)) * 8;
+      const bool ok = rr < valid;
+      cp_async16(smem_u32(dr + rr * kCorrLR + cc),
+                 r + (((tok0 + t + (ok ? rr : 0)) * H + h) * DK + cc), ok);
+    }
+    for (int idx = tid; idx < 64 * NCOL / 8; idx += NTH) {
+      const int rr = idx / (NCOL / 8), cc = (idx % (NCOL / 8)) * 8;
+      const bool ok = rr < valid;
+      cp_async16(smem_u32(dO + rr * kCorrLH + cc),
+                 o + (((tok0 + t + (ok ? rr : 0)) * H + h) * dv + c0 + cc), ok);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  fetch(0);
+  {  // H_s, columns c0 .. c0 + 64 NT - 1, in bf16
+    const float *Hs = p.seg_state + (((size_t)n * p.seg_count + s) * H + h) * DK * dv + c0;
+    for (int idx = tid; idx < DK * NCOL / 4; idx += NTH) {
+      const int k = idx / (NCOL / 4), cc = (idx % (NCOL / 4)) * 4;
+      const float4 x = *reinterpret_cast<const float4 *>(Hs + (size_t)k * dv + cc);
+      *reinterpret_cast<uint2 *>(&sh[k * kCorrLH + cc]) =
+          make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
+    }
+  }
+  const int m0 = 16 * (warp & 3), n0 = 64 * (warp >> 2);
+  for (int b = 0; b < nb; ++b) {
+    if (b + 1 < nb) {
+      fetch(b + 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
+    __syncthreads();   // block b's rows (and, the first time, H_s) are in place
+    const __nv_bfloat16 *br = sr + (b & 1) * 64 * kCorrLR;
+    const __nv_bfloat16 *bo = so + (b & 1) * 64 * kCorrLH;
+    float acc[8][4];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+#pragma unroll
+    for (int k0 = 0; k0 < DK; k0 += 16) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(smem_u32(br + (m0 + (lane & 7) + ((lane >> 3) & 1) * 8) * kCorrLR + k0 +
+                       (lane >> 4) * 8),
+              a0, a1, a2, a3);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = lane >> 3;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(smem_u32(sh + (k0 + (i & 1) * 8 + (lane & 7)) * kCorrLH + n0 + 16 * q +
+                           (i >> 1) * 8),
+                  b0, b1, b2, b3);
+        mma_bf16(acc[2 * q], a0, a1, a2, a3, b0, b1);
+        mma_bf16(acc[2 * q + 1], a0, a1, a2, a3, b2, b3);
+      }
+    }
+    const int64_t t = t_first + (int64_t)b * 64;
+    const int valid = (int)(seg_end - t < 64 ? seg_end - t : 64);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int rr = m0 + (lane >> 2) + 8 * half, cc = n0 + 8 * q + 2 * (lane & 3);
+        if (rr < valid) {
+          const uint32_t w = *reinterpret_cast<const uint32_t *>(bo + rr * kCorrLH + cc);
+          *reinterpret_cast<uint32_t *>(o + ((tok0 + t + rr) * H + h) * dv + c0 + cc) =
+              pack_bf16(bf16_lo(w) + acc[q][2 * half], bf16_hi(w) + acc[q][2 * half + 1]);
+        }
+      }
+    }
+    __syncthreads();   // buffer b & 1 is refilled by the fetch of block b + 2
   }
 }
 
@@ -1213,42 +1338,50 @@ cudaError_t launch_tc128(const FwdParams &p, cudaStream_t stream) {
     kern<<<grid, Cfg::kWarps * 32, L::ALLOC, stream>>>(p, tq, tk, tv);
     return cudaGetLastError();
   }
-  // A split sequence (the segments' affine state maps H -> M H + X, composed
-  // in order; "Optimization Quartet", Triton GDN kernel section 3.2, names the
-  // inter-chunk carry as the serial part of the chunked form):
-  //   1. segment 0 as usual, writing the state that enters segment 1; at the
-  //      same time segments 1 .. S-2 in transport mode (X and M);
-  //   2. the composition H_(s+1) = M_s H_s + X_s for s = 1 .. S-2;
-  //   3. segments 1 .. S-1 from their composed states, writing the outputs
-  //      and, for the last one, the caller's final state.
+  // A split sequence (each segment maps its entry state H to M H + X and
+  // its outputs o to o0 + r H; "Optimization Quartet", Triton GDN kernel
+  // section 3.2, names the inter-chunk carry as the serial part of the
+  // chunked form):
+  //   1. one launch: segment 0 from the caller's state, writing the state
+  //      that enters segment 1; segments 1 .. S-1 from zero (o0, X) and from
+  //      the identity on dk extra columns (r, M);
+  //   2. the composition H_(s+1) = M_s H_s + X_s for s = 1 .. S-1, in order
+  //      (the last gives the caller's final state);
+  //   3. the correction o += r H_s over segments 1 .. S-1.
   const int S = p.seg_count;
-  FwdParams a = p;
-  a.seg_first = 0;
-  a.seg_launch = S - 1;
-  a.seg_transport = 1;
-  a.seg_write_next = 1;
-  const dim3 grid_a(p.dv / kDvt + (S > 2 ? DK / kDvt : 0), p.num_heads, p.num_seqs * (S - 1));
-  kern<<<grid_a, Cfg::kWarps * 32, L::ALLOC, stream>>>(a, tq, tk, tv);
+  const dim3 grid(p.dv / kDvt + DK / kDvt, p.num_heads, p.num_seqs * S);
+  kern<<<grid, Cfg::kWarps * 32, L::ALLOC, stream>>>(p, tq, tk, tv);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  for (int s = 1; s + 1 < S; ++s) {   // one launch per step, in order
+  for (int s = 1; s < S; ++s) {   // one launch per step, in order
     seg_compose_kernel<<<dim3(p.dv / 32 * (DK / 32), p.num_heads, p.num_seqs), 256, 0, stream>>>(
         p, s);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
-  FwdParams b = p;
-  b.seg_first = 1;
-  b.seg_launch = S - 1;
-  b.seg_transport = S;  // none
-  b.seg_write_next = 0;
-  const dim3 grid_b(p.dv / kDvt, p.num_heads, p.num_seqs * (S - 1));
-  kern<<<grid_b, Cfg::kWarps * 32, L::ALLOC, stream>>>(b, tq, tk, tv);
+  const int groups = (p.seg_len / 64 + kCorrBlocks - 1) / kCorrBlocks;
+  const dim3 cgrid((p.dv % 128 == 0 ? p.dv / 128 : p.dv / 64), (S - 1) * groups,
+                     p.num_seqs * p.num_heads);
+  if (p.dv % 128 == 0) {   // 128 value columns a CTA: each row of r read once per two tiles
+    if ((err = cudaFuncSetAttribute(seg_correct_kernel<2>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    CorrSmem<2>::BYTES)) != cudaSuccess)
+      return err;
+    seg_correct_kernel<2><<<cgrid, 256, CorrSmem<2>::BYTES, stream>>>(p, groups);
+  } else {
+    if ((err = cudaFuncSetAttribute(seg_correct_kernel<1>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    CorrSmem<1>::BYTES)) != cudaSuccess)
+      return err;
+    seg_correct_kernel<1><<<cgrid, 128, CorrSmem<1>::BYTES, stream>>>(p, groups);
+  }
   return cudaGetLastError();
 }
 
-// The number of segments a sequence is split into: as many as the SMs take
-// in the first launch (segment 0 of every unit plus S - 2 transport
-// segments with dk/64 extra column tiles each), at most kMaxSegments and at
-// least 4 chunks per segment; 1 (no split) when that is fewer than 3.
+// The number of segments a sequence is split into: the count that minimises
+// (launch waves) / S over 2 .. kMaxSegments, where the one launch holds the
+// first segment's value tiles and (value + dk/64 transport) tiles for each
+// later segment, one CTA per SM; at least 4 chunks a segment, and 1 (no
+// split) unless that beats the unsplit launch by a quarter (the composition
+// and the correction cost a little).
 int choose_segments(const FwdParams &p) {
   static int sms[64] = {};
   int dev = 0;
@@ -1256,14 +1389,22 @@ int choose_segments(const FwdParams &p) {
   if (sms[dev] == 0 &&
       cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return 1;
+  const int64_t sm = sms[dev];
   const int64_t units_v = (int64_t)p.num_seqs * p.num_heads * (p.dv / kDvt);
   const int64_t units_t = (int64_t)p.num_seqs * p.num_heads * ((p.dv + DK) / kDvt);
-  if (units_v >= sms[dev]) return 1;
-  int64_t s = 2 + (sms[dev] - units_v) / units_t;
   const int64_t chunks = (p.seq_len + 63) / 64;
-  if (s > kMaxSegments) s = kMaxSegments;
-  if (s > chunks / 4) s = chunks / 4;
-  return s >= 3 ? (int)s : 1;
+  const double cost1 = (double)((units_v + sm - 1) / sm);
+  int best = 1;
+  double best_cost = 0.75 * cost1;
+  for (int s = 2; s <= kMaxSegments && s <= chunks / 4; ++s) {
+    const int64_t ctas = units_v + (int64_t)(s - 1) * units_t;
+    const double cost = (double)((ctas + sm - 1) / sm) / s;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
 }
 
 }  // namespace

@@ -11,7 +11,7 @@
 namespace gdn {
 
 constexpr int kChunk = 64;  // tokens per chunk of the tensor-core kernels (the default)
-constexpr int kMaxSegments = 3;  // GDN_SEQ_SPLIT: segments per sequence at most
+constexpr int kMaxSegments = 8;  // GDN_SEQ_SPLIT: segments per sequence at most
 
 // Device status record at the start of the workspace.  The first error wins
 // (atomicCAS from 0); `seq` and `head` locate it, `aux` carries a detail.
@@ -52,20 +52,18 @@ struct FwdParams {
   uint32_t flags;
   Extents ext;
   // Sequence split (dense inputs, head_dim_k 128; GDN_SEQ_SPLIT): each
-  // sequence is cut into seg_count segments of seg_len tokens; a launch covers
-  // segments seg_first .. seg_first + seg_launch - 1 (grid z = sequence *
-  // seg_launch + segment - seg_first).  Segments >= seg_transport run in
-  // transport mode: zero initial state on the value columns and the identity
-  // on dk extra "transport" columns, no output; their final states are the
-  // segment's affine state map H -> M H + X (X to seg_x, M to seg_m).  Other
-  // segments start from the caller's state (segment 0) or seg_state, and end
-  // in the caller's final state (last segment) or, when seg_write_next, in
-  // seg_state of the next segment.  seg_len = 0: no split.
-  int32_t seg_len = 0, seg_count = 0, seg_first = 0, seg_launch = 0, seg_transport = 0,
-          seg_write_next = 0;
-  float *seg_state = nullptr;  // [N][seg_count][H][dk][dv]
+  // sequence is cut into seg_count segments of seg_len tokens, all run by one
+  // launch (grid z = sequence * seg_count + segment).  Segment 0 starts from
+  // the caller's state and ends in seg_state of segment 1.  Later segments
+  // start from zero on the value columns (their outputs o0 and end state X)
+  // and from the identity on dk extra columns (their per-token reads r, to
+  // seg_r, and end state M): the segment maps H -> M H + X and o -> o0 + r H.
+  // seg_len = 0: no split.
+  int32_t seg_len = 0, seg_count = 0;
+  float *seg_state = nullptr;  // [N][seg_count][H][dk][dv]: entry states (s >= 1)
   float *seg_x = nullptr;      // [N][seg_count][H][dk][dv]
   float *seg_m = nullptr;      // [N][seg_count][H][dk][dk]
+  void *seg_r = nullptr;       // [N * seq_len][H][dk] bf16
 };
 
 __device__ __forceinline__ void report(DeviceStatus *st, uint32_t code, uint32_t seq,

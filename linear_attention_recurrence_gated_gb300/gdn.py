@@ -40,7 +40,7 @@ EXPORTED = ("gdn_fwd_workspace_size", "gdn_workspace_init", "gdn_fwd", "gdn_chec
             "gdn_status_string", "gdn_fwd_kernel_name", "gdn_fwd_static_scratch",
             "gdn_decode", "gdn_diag_workspace_size", "gdn_diag_fwd", "gdn_conv_silu",
             "gdn_bwd_workspace_size", "gdn_bwd", "gdn_fwd_debug", "gdn_check_record",
-            "gdn_fwd_kernel_name_chunk", "gdn_fwd_split_segments",
+            "gdn_fwd_kernel_name_chunk", "gdn_fwd_split_segments", "gdn_fwd_split_workspace_size",
             "gdn_diag_delta_workspace_size", "gdn_diag_delta_fwd")
 # ... and include/gdn_debug.h (self-tests of the failure reporting).
 DEBUG_EXPORTED = ("gdn_debug_wait_timeout",)
@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
             L.gdn_fwd_kernel_name.argtypes = [i32, i32, ctypes.c_int, u32]
             L.gdn_fwd_kernel_name_chunk.restype = ctypes.c_char_p
             L.gdn_fwd_kernel_name_chunk.argtypes = [i32, i32, i32, ctypes.c_int, u32]
+            L.gdn_fwd_split_workspace_size.restype = sz
+            L.gdn_fwd_split_workspace_size.argtypes = [i32, i32, i32, i32, i32]
             L.gdn_fwd_split_segments.restype = i32
             L.gdn_fwd_split_segments.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.c_int, u32,
                                                  i32]
@@ -164,9 +166,21 @@ def gdn_workspace_init(workspace: torch.Tensor, stream=None) -> None:
         raise GdnError(st, "gdn_workspace_init")
 
 
-def new_workspace(num_seqs, num_heads, head_dim_k, head_dim_v, flags=0, device=None):
-    """A zeroed workspace of the size gdn_fwd needs (the caller keeps it)."""
-    n = gdn_fwd_workspace_size(num_seqs, num_heads, head_dim_k, head_dim_v, flags)
+def gdn_fwd_split_workspace_size(num_seqs: int, seq_len: int, num_heads: int, head_dim_k: int,
+                                 head_dim_v: int) -> int:
+    return int(lib().gdn_fwd_split_workspace_size(num_seqs, seq_len, num_heads, head_dim_k,
+                                                  head_dim_v))
+
+
+def new_workspace(num_seqs, num_heads, head_dim_k, head_dim_v, flags=0, device=None,
+                  seq_len=None):
+    """A zeroed workspace of the size gdn_fwd needs (the caller keeps it).
+    With GDN_SEQ_SPLIT in ``flags`` pass ``seq_len`` (tokens per sequence of a
+    dense call): a split call keeps per-token maps in the workspace."""
+    if (flags & GDN_SEQ_SPLIT) and seq_len is not None:
+        n = gdn_fwd_split_workspace_size(num_seqs, seq_len, num_heads, head_dim_k, head_dim_v)
+    else:
+        n = gdn_fwd_workspace_size(num_seqs, num_heads, head_dim_k, head_dim_v, flags)
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
@@ -279,7 +293,8 @@ def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
     ``debug_checks`` sets GDN_DEBUG_CHECKS (range checks before every access);
     ``seq_split`` sets GDN_SEQ_SPLIT (long dense sequences with head_dim_k 128
     cut into segments computed in parallel; a given ``workspace`` must be sized
-    with the flag).
+    by ``gdn_fwd_split_workspace_size``, e.g. ``new_workspace(..., GDN_SEQ_SPLIT,
+    seq_len=T)``).
     With ``check=True`` the call synchronises and raises on a device-side error.
     """
     N, H, dk, dv = _check_fwd_tensors("gdn_fwd", q, k, v, g, beta, initial_state, cu_seqlens,
@@ -292,7 +307,8 @@ def gdn_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, *, o=None,
     dcode = _dtype_code(q.dtype)
     flags = _fwd_flags(qk_l2norm, beta_logits, force_simt, debug_checks, seq_split)
     if workspace is None:
-        workspace = new_workspace(N, H, dk, dv, flags, device=q.device)
+        workspace = new_workspace(N, H, dk, dv, flags, device=q.device,
+                                  seq_len=T if cu_seqlens is None else None)
     st = lib().gdn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
                        _ptr(cu_seqlens), _ptr(o), _ptr(final_state), _ptr(D_skip),
                        _ptr(out_gate), B, T, H, dk, dv, N, chunk_size, dcode, flags, _ptr(workspace),

@@ -58,10 +58,15 @@ def test_status_strings(L):
 
 def test_workspace_size(L):
     assert G.gdn_fwd_workspace_size(8, 16, 64, 64) >= 256
-    # GDN_SEQ_SPLIT with head_dim_k 128: 3 segments' states, X (dk x dv) and M (dk x dk)
-    assert G.gdn_fwd_workspace_size(1, 16, 128, 128, G.GDN_SEQ_SPLIT) == \
-        256 + 4 * 1 * 3 * 16 * 128 * (2 * 128 + 128)
+    # GDN_SEQ_SPLIT with head_dim_k 128: 8 segments' states, X (dk x dv) and M (dk x dk)
+    seg = 256 + 4 * 1 * 8 * 16 * 128 * (2 * 128 + 128)
+    assert G.gdn_fwd_workspace_size(1, 16, 128, 128, G.GDN_SEQ_SPLIT) == seg
     assert G.gdn_fwd_workspace_size(1, 16, 64, 64, G.GDN_SEQ_SPLIT) == 256
+    # ... and for a split call the per-token maps r, bf16 [tokens][heads][dk], 256-aligned
+    assert G.gdn_fwd_split_workspace_size(1, 65536, 16, 128, 128) == \
+        (seg + 255) // 256 * 256 + 2 * 65536 * 16 * 128
+    assert G.gdn_fwd_split_workspace_size(1, 1000, 2, 64, 64) == 256
+    assert G.gdn_fwd_split_workspace_size(0, 1000, 2, 128, 128) == 0
     assert G.gdn_fwd_workspace_size(0, 16, 64, 64) == 0
 
 

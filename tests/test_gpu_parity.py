@@ -319,18 +319,20 @@ def test_outputs_stay_inside_their_buffers(dtype, dk, dv):
 
 
 # ---------------- GDN_SEQ_SPLIT: long dense sequences cut into segments ----------------
-@pytest.mark.parametrize("T,H,dv,init,l2,gs", [(2000, 2, 128, True, False, 1e-3),
-                                                (2000, 2, 128, False, True, 0.0),
-                                                (4097, 1, 256, True, False, 1e-3),
-                                                (777, 3, 128, True, False, 1e-3)])
-def test_seq_split(T, H, dv, init, l2, gs):
+@pytest.mark.parametrize("B,T,H,dv,init,l2,gs", [(1, 2000, 2, 128, True, False, 1e-3),
+                                                  (1, 2000, 2, 128, False, True, 0.0),
+                                                  (1, 4097, 1, 256, True, False, 1e-3),
+                                                  (1, 777, 3, 128, True, False, 1e-3),
+                                                  (2, 1500, 1, 128, True, False, 1e-3)])
+def test_seq_split(B, T, H, dv, init, l2, gs):
     """A split call equals the oracle within the bf16 bounds and the unsplit
     call up to rounding; with dk = 128 and few units the call takes 3 segments.
     The gates are slow (gs = 0 is the plain delta rule) so that a segment's
     map M keeps weight: with fast gates M underflows to zero and the split
     result is the unsplit one bit for bit."""
-    w = W.custom(B=1, T=T, H=H, dk=128, dv=dv, dtype="bf16", init_state=init, gate_scale=gs,
+    w = W.custom(B=B, T=T, H=H, dk=128, dv=dv, dtype="bf16", init_state=init, gate_scale=gs,
                  seed=700 + T + dv)
+    assert G.gdn_fwd_split_segments(B, T, H, 128, dv, torch.bfloat16, G.GDN_SEQ_SPLIT) > 1
     inp = W.generate(w)
     kw = dict(qk_l2norm=True) if l2 else {}
     if l2:
@@ -353,6 +355,21 @@ def test_seq_split(T, H, dv, init, l2, gs):
     assert not torch.equal(s0, s1)  # the split path ran (its composition rounds differently)
 
 
+def test_seq_split_with_epilogue_runs_unsplit():
+    """The block epilogue is not combined with a split: such a call runs
+    unsplit (same result as without the flag, bit for bit)."""
+    w = W.custom(B=1, T=2000, H=2, dk=128, dv=128, dtype="bf16", init_state=True,
+                 gate_scale=1e-3, seed=31)
+    inp = W.generate(w)
+    ex = W.generate_block_extras(inp, w.H, seed=32)
+    d = parity.to_dev(inp)
+    kw = dict(D_skip=ex["D_skip"].cuda(), out_gate=ex["out_gate"].cuda(), check=True)
+    o0, s0 = G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"], None, **kw)
+    o1, s1 = G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"], None,
+                       seq_split=True, **kw)
+    assert torch.equal(o0, o1) and torch.equal(s0, s1)
+
+
 def test_seq_split_long_full_size():
     """long_bf16 (B=1, T=65536, H=16, dk=dv=128, slow gates) split into segments,
     against the oracle on the whole tensors and the worst (sequence, head)."""
@@ -372,25 +389,49 @@ def test_seq_split_long_full_size():
     assert ro <= to and rs <= ts and uo <= to and us <= ts
 
 
+def _expected_segments(N, T, H, dv, sms):
+    """The documented plan rule: minimise waves / S over S = 2 .. 8 (at least 4
+    chunks a segment; one CTA per SM holding the first segment's value tiles
+    and value + transport tiles for each later one), and split only when that
+    beats the unsplit launch's waves by a quarter."""
+    units_v, units_t = N * H * dv // 64, N * H * (dv + 128) // 64
+    best, best_cost = 1, 0.75 * -(-units_v // sms)
+    for S in range(2, min(8, ((T + 63) // 64) // 4) + 1):
+        cost = -(-(units_v + (S - 1) * units_t) // sms) / S
+        if cost < best_cost:
+            best, best_cost = S, cost
+    return best
+
+
 def test_seq_split_plan():
-    """The library's split plan on this device: the long workload (16 units of
-    two column tiles) takes 3 segments; the wide one (128 units) fills the SMs
-    unsplit; packed varlen calls and short sequences are never split."""
+    """The library's split plan on this device follows the documented rule:
+    the long workload (16 units of two column tiles) is split, the wide one
+    (128 units) fills the SMs unsplit, packed varlen calls and sequences of
+    fewer than 8 chunks are never split."""
     S = G.gdn_fwd_split_segments
     bf = torch.bfloat16
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    # 32 value-column CTAs plus 64 per transport segment
-    assert S(1, 65536, 16, 128, 128, bf, G.GDN_SEQ_SPLIT) == (3 if sms >= 32 + 64 else 1)
+    for (N, T, H, dv) in [(1, 65536, 16, 128), (4, 8192, 16, 128), (1, 12 * 64, 1, 128),
+                          (1, 4097, 1, 256), (2, 2000, 3, 128)]:
+        assert S(N, T, H, 128, dv, bf, G.GDN_SEQ_SPLIT) == _expected_segments(N, T, H, dv, sms)
+    assert S(1, 65536, 16, 128, 128, bf, G.GDN_SEQ_SPLIT) >= 2
     assert S(4, 8192, 16, 128, 128, bf, G.GDN_SEQ_SPLIT) == 1
     assert S(1, 140000, 8, 128, 256, bf, G.GDN_SEQ_SPLIT, varlen=True) == 1
-    assert S(1, 11 * 64, 1, 128, 128, bf, G.GDN_SEQ_SPLIT) == 1  # under 4 chunks a segment
-    assert S(1, 12 * 64, 1, 128, 128, bf, G.GDN_SEQ_SPLIT) == 3
+    assert S(1, 7 * 64, 1, 128, 128, bf, G.GDN_SEQ_SPLIT) == 1   # under 8 chunks
 
 
 def test_seq_split_needs_its_workspace():
+    """A call the plan splits needs gdn_fwd_split_workspace_size bytes: one
+    sized without the flag, or with it but without the token count, is
+    refused before any launch."""
     w = W.custom(B=1, T=1000, H=2, dk=128, dv=128, dtype="bf16", init_state=True, seed=9)
     d = parity.to_dev(W.generate(w))
-    small = G.new_workspace(1, 2, 128, 128)  # sized without the flag
-    with pytest.raises(G.GdnError):
-        G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"], None,
-                  workspace=small, seq_split=True)
+    assert G.gdn_fwd_split_segments(1, 1000, 2, 128, 128, torch.bfloat16, G.GDN_SEQ_SPLIT) > 1
+    for small in (G.new_workspace(1, 2, 128, 128),
+                  G.new_workspace(1, 2, 128, 128, G.GDN_SEQ_SPLIT)):
+        with pytest.raises(G.GdnError):
+            G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"], None,
+                      workspace=small, seq_split=True)
+    ok = G.new_workspace(1, 2, 128, 128, G.GDN_SEQ_SPLIT, seq_len=1000)
+    G.gdn_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["initial_state"], None,
+              workspace=ok, seq_split=True, check=True)
