@@ -323,7 +323,8 @@ def test_outputs_stay_inside_their_buffers(dtype, dk, dv):
                                                   (1, 2000, 2, 128, False, True, 0.0),
                                                   (1, 4097, 1, 256, True, False, 1e-3),
                                                   (1, 777, 3, 128, True, False, 1e-3),
-                                                  (2, 1500, 1, 128, True, False, 1e-3)])
+                                                  (2, 1500, 1, 128, True, False, 1e-3),
+                                                  (1, 1700, 1, 192, True, False, 1e-3)])
 def test_seq_split(B, T, H, dv, init, l2, gs):
     """A split call equals the oracle within the bf16 bounds and the unsplit
     call up to rounding; with dk = 128 and few units the call takes 3 segments.
