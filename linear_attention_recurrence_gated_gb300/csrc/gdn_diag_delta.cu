@@ -24,8 +24,8 @@
 // so a CTA only waits on a CTA that started before it; every wait is bounded.
 //
 // Per token a lane reads 8 rows of d, b and c and 4 values of v from shared
-// memory and does 64 packed two-lane fp32 operations; the column sums over
-// the state rows take 16 shuffles.
+// memory and does 64 packed two-lane fp32 operations on pairs of state rows;
+// the column sums over the state rows take 16 shuffles.
 #include "gdn_internal.cuh"
 #include "gdn_ptx.cuh"
 
@@ -138,19 +138,17 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
 __device__ __forceinline__ float sigmoid(float x) { return 1.f / (1.f + ex2(-x * kLog2e)); }
 
-// Sum over the four row groups (lane bits 3 and 4) of a lane's partial sums
-// for its four columns, as two packed pairs; every lane gets the totals.
-__device__ __forceinline__ float4 rows_reduce(uint64_t a, uint64_t b) {
+// Four column partial sums, each a packed pair over two rows: add the pair,
+// then sum over the four row groups (lane bits 3 and 4).
+__device__ __forceinline__ float4 cols_reduce(const uint64_t (&acc)[4]) {
   float4 r;
-  upk2(a, r.x, r.y);
-  upk2(b, r.z, r.w);
+  float lo, hi;
+  upk2(acc[0], lo, hi); r.x = lo + hi;
+  upk2(acc[1], lo, hi); r.y = lo + hi;
+  upk2(acc[2], lo, hi); r.z = lo + hi;
+  upk2(acc[3], lo, hi); r.w = lo + hi;
 #pragma unroll
   for (int m = 8; m <= 16; m <<= 1) {
     r.x += __shfl_xor_sync(0xffffffffu, r.x, m);
@@ -161,28 +159,11 @@ __device__ __forceinline__ float4 rows_reduce(uint64_t a, uint64_t b) {
   return r;
 }
 
-// sum over this lane's 8 rows of x[row] * h[row][four columns] (two pairs)
-template <typename X>
-__device__ __forceinline__ float4 rows_dot(const X *x8, const uint64_t (&h2)[8][2]) {
-  const float4 x0 = ld4(x8);
-  const float4 x1 = ld4(x8 + 4);
-  const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-  uint64_t a0 = 0, a1 = 0, b0 = 0, b1 = 0;
-#pragma unroll
-  for (int i = 0; i < 8; i += 2) {
-    const uint64_t xe = pk2(xv[i], xv[i]), xo = pk2(xv[i + 1], xv[i + 1]);
-    a0 = fma2(xe, h2[i][0], a0);
-    a1 = fma2(xe, h2[i][1], a1);
-    b0 = fma2(xo, h2[i + 1][0], b0);
-    b1 = fma2(xo, h2[i + 1][1], b1);
-  }
-  return rows_reduce(add2(a0, b0), add2(a1, b1));
-}
-
 // Lane layout: lane = 8 rg + cg holds the state rows 8 rg .. 8 rg + 7 and the
-// columns 4 cg .. 4 cg + 3 (h2[i][p]: row 8 rg + i, columns 4 cg + 2p, +1), so
-// that a token reads 8 rows of d, b, c and 4 values of v from shared memory
-// per lane, and the column sums over the rows take two shuffle levels.
+// columns 4 cg .. 4 cg + 3, packed in pairs of rows (h2[q][k]: rows 8 rg + 2q
+// and + 1 of column 4 cg + k), so that a token reads 8 rows of d, b, c (as
+// pairs, no repacking) and 4 values of v from shared memory per lane, and the
+// column sums over the rows take two shuffle levels.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) gdn_diag_delta_kernel(const Params p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -220,19 +201,27 @@ __global__ void __launch_bounds__(kThreads) gdn_diag_delta_kernel(const Params p
   const bool beta_sig = (p.opts & GDN_BETA_LOGITS) != 0;
 
   // the state block: zero, the initial state, or the identity
-  uint64_t h2[8][2];
+  // h2[q][k] packs rows r0 + 2q and r0 + 2q + 1 of column c0 + k, so that the
+  // per-row factors d, b, c load from shared memory as ready-made pairs
+  uint64_t h2[4][4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (transport) {
-      const int s = r0 + i;
-      x = make_float4(s == c0 ? 1.f : 0.f, s == c0 + 1 ? 1.f : 0.f, s == c0 + 2 ? 1.f : 0.f,
-                      s == c0 + 3 ? 1.f : 0.f);
-    } else if (first && p.h0) {
-      x = *reinterpret_cast<const float4 *>(p.h0 + srow + (size_t)(r0 + i) * kD + c0);
+  for (int q = 0; q < 4; ++q) {
+    float4 x[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int s = r0 + 2 * q + e;
+      x[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (transport) {
+        x[e] = make_float4(s == c0 ? 1.f : 0.f, s == c0 + 1 ? 1.f : 0.f, s == c0 + 2 ? 1.f : 0.f,
+                           s == c0 + 3 ? 1.f : 0.f);
+      } else if (first && p.h0) {
+        x[e] = *reinterpret_cast<const float4 *>(p.h0 + srow + (size_t)s * kD + c0);
+      }
     }
-    h2[i][0] = pk2(x.x, x.y);
-    h2[i][1] = pk2(x.z, x.w);
+    h2[q][0] = pk2(x[0].x, x[1].x);
+    h2[q][1] = pk2(x[0].y, x[1].y);
+    h2[q][2] = pk2(x[0].z, x[1].z);
+    h2[q][3] = pk2(x[0].w, x[1].w);
   }
 
   // ---- staging: thread (warp w, lane s) handles tokens 8w .. 8w+7 of a tile ----
@@ -278,41 +267,45 @@ __global__ void __launch_bounds__(kThreads) gdn_diag_delta_kernel(const Params p
       T *out = transport ? &sm.rbuf[0][0] : &sm.obuf[0][0];
 #pragma unroll 1
       for (int tl = 0; tl < kTile; ++tl) {
-        const float *rd = &sm.row[buf][0][tl][r0], *rbk = &sm.row[buf][1][tl][r0];
-        const float4 d0 = *reinterpret_cast<const float4 *>(rd);
-        const float4 d1 = *reinterpret_cast<const float4 *>(rd + 4);
-        const float4 k0 = *reinterpret_cast<const float4 *>(rbk);
-        const float4 k1 = *reinterpret_cast<const float4 *>(rbk + 4);
-        const float dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-        const float kv[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-        // hbar = d (.) h, and b^T hbar over this lane's rows
-        uint64_t a0 = 0, a1 = 0, e0 = 0, e1 = 0;
+        // rows r0 .. r0 + 7 of d, b, c as four packed pairs each
+        const ulonglong2 *rd = reinterpret_cast<const ulonglong2 *>(&sm.row[buf][0][tl][r0]);
+        const ulonglong2 *rbk = reinterpret_cast<const ulonglong2 *>(&sm.row[buf][1][tl][r0]);
+        const ulonglong2 *rc = reinterpret_cast<const ulonglong2 *>(&sm.row[buf][2][tl][r0]);
+        const ulonglong2 d01 = rd[0], d23 = rd[1], k01 = rbk[0], k23 = rbk[1];
+        const uint64_t dp[4] = {d01.x, d01.y, d23.x, d23.y};
+        const uint64_t kp[4] = {k01.x, k01.y, k23.x, k23.y};
+        // hbar = d (.) h, and b^T hbar over this lane's rows (pairs of rows)
+        uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint64_t dd = pk2(dv[i], dv[i]), kk = pk2(kv[i], kv[i]);
-          h2[i][0] = mul2(dd, h2[i][0]);
-          h2[i][1] = mul2(dd, h2[i][1]);
-          if (i & 1) {
-            e0 = fma2(kk, h2[i][0], e0);
-            e1 = fma2(kk, h2[i][1], e1);
-          } else {
-            a0 = fma2(kk, h2[i][0], a0);
-            a1 = fma2(kk, h2[i][1], a1);
+        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            h2[q][k] = mul2(dp[q], h2[q][k]);
+            acc[k] = fma2(kp[q], h2[q][k], acc[k]);
           }
         }
-        const float4 pred = rows_reduce(add2(a0, e0), add2(a1, e1));
+        const float4 pred = cols_reduce(acc);
         const float4 vv = transport ? make_float4(0.f, 0.f, 0.f, 0.f)
                                     : *reinterpret_cast<const float4 *>(&sm.vt[buf][tl][c0]);
         const float be = sm.bt[buf][tl];
-        const uint64_t u0 = pk2(be * (vv.x - pred.x), be * (vv.y - pred.y));
-        const uint64_t u1 = pk2(be * (vv.z - pred.z), be * (vv.w - pred.w));
+        const float u[4] = {be * (vv.x - pred.x), be * (vv.y - pred.y), be * (vv.z - pred.z),
+                            be * (vv.w - pred.w)};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint64_t kk = pk2(kv[i], kv[i]);
-          h2[i][0] = fma2(kk, u0, h2[i][0]);
-          h2[i][1] = fma2(kk, u1, h2[i][1]);
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t uu = pk2(u[k], u[k]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) h2[q][k] = fma2(kp[q], uu, h2[q][k]);
         }
-        const float4 o = rows_dot(&sm.row[buf][2][tl][r0], h2);
+        // o = c^T h over this lane's rows, then over the row groups
+        const ulonglong2 c01 = rc[0], c23 = rc[1];
+        const uint64_t cp2[4] = {c01.x, c01.y, c23.x, c23.y};
+        uint64_t oacc[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) oacc[k] = fma2(cp2[q], h2[q][k], oacc[k]);
+        }
+        const float4 o = cols_reduce(oacc);
         if (rg == 0 && tt + tl < len) st4(out + (tt + tl) * 32 + c0, o);
       }
     }
@@ -328,17 +321,20 @@ __global__ void __launch_bounds__(kThreads) gdn_diag_delta_kernel(const Params p
   float (*Xs)[kD] = Mt + kS;
   if (runs) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float x0, x1, x2, x3;
-      upk2(h2[i][0], x0, x1);
-      upk2(h2[i][1], x2, x3);
+    for (int q = 0; q < 4; ++q) {
+      float lo[4], hi[4];   // rows r0 + 2q and r0 + 2q + 1, columns c0 .. c0 + 3
+#pragma unroll
+      for (int k = 0; k < 4; ++k) upk2(h2[q][k], lo[k], hi[k]);
       if (transport) {
-        Mt[c0][r0 + i] = x0;
-        Mt[c0 + 1][r0 + i] = x1;
-        Mt[c0 + 2][r0 + i] = x2;
-        Mt[c0 + 3][r0 + i] = x3;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          Mt[c0 + k][r0 + 2 * q] = lo[k];
+          Mt[c0 + k][r0 + 2 * q + 1] = hi[k];
+        }
       } else {
-        *reinterpret_cast<float4 *>(&Xs[r0 + i][c0]) = make_float4(x0, x1, x2, x3);
+        *reinterpret_cast<float4 *>(&Xs[r0 + 2 * q][c0]) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<float4 *>(&Xs[r0 + 2 * q + 1][c0]) =
+            make_float4(hi[0], hi[1], hi[2], hi[3]);
       }
     }
   }
