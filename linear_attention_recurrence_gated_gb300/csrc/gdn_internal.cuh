@@ -204,6 +204,11 @@ cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t stream);    // bf16 s
 cudaError_t launch_fwd_tc64(const FwdParams &p, cudaStream_t stream);  // bf16, head_dim_k 64
 // GDN_SEQ_SPLIT: segments to cut each sequence of this call into (1 = no split)
 int seq_split_segments(const FwdParams &p);
+// The split's composition step s (H_(s+1) = M_s H_s + X_s; the last step gives
+// the caller's final state) and the correction o += r H_s of the later
+// segments (gdn_seq_split.cu).
+cudaError_t launch_seg_compose(const FwdParams &p, int s, cudaStream_t stream);
+cudaError_t launch_seg_correct(const FwdParams &p, cudaStream_t stream);
 bool tc_supported(int dk, int dv);
 // chunk_size 32 and 128 on the tensor cores: bf16, head_dim_k 64
 bool tcc_supported(int chunk, int dk, int dv);
