@@ -104,7 +104,7 @@ enum {
    * 3.5); this is the device-side counterpart. */
   GDN_DEBUG_CHECKS = 1u << 4,
   /* gdn_fwd: let the head_dim_k 128 tensor-core kernel cut each sequence of a
-   * dense call (cu_seqlens NULL, no block epilogue) into up to 8 segments of
+   * dense call (cu_seqlens NULL, no block epilogue, no GDN_DEBUG_CHECKS) into up to 8 segments of
    * whole chunks when the (sequence, head, 64 value columns) units alone
    * leave SMs idle (gdn_fwd_split_segments gives the plan).  The chunk
    * transition is affine in the state, H' = M H + X, and each output is
@@ -227,7 +227,8 @@ gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
 
 /* The number of segments S GDN_SEQ_SPLIT cuts each sequence of a gdn_fwd
  * call with these arguments (and no block epilogue: a call with D_skip or
- * out_gate is never split) into, on the current device (the plan depends on
+ * out_gate is never split, nor one with GDN_DEBUG_CHECKS) into, on the
+ * current device (the plan depends on
  * its SM count): S >= 2 when the call is split, and then gdn_fwd launches S +
  * 1 kernels (every segment in one launch, S - 1 composition steps, the
  * output correction); 1 when it is not split (one kernel).  varlen != 0

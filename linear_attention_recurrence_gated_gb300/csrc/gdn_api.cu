@@ -148,11 +148,12 @@ gdn_status fwd_validate(const void *q, const void *k, const void *v, const float
 // The split plan of GDN_SEQ_SPLIT: fills p.seg_len / p.seg_count (0 when
 // the call is not split) and returns the segment count (1: not split).  The
 // block epilogue is not combined with a split (the correction would have to
-// pass through it): such calls run unsplit.
+// pass through it), nor GDN_DEBUG_CHECKS (the composition and correction
+// kernels check no declared extents): such calls run unsplit.
 int plan_segments(FwdParams &p, int chunk, gdn_dtype dtype) {
   p.seg_len = p.seg_count = 0;
-  if (!(p.flags & GDN_SEQ_SPLIT) || chunk != kChunk || !use_tc(p.dk, p.dv, dtype, p.flags) ||
-      p.d_skip || p.out_gate)
+  if (!(p.flags & GDN_SEQ_SPLIT) || (p.flags & GDN_DEBUG_CHECKS) || chunk != kChunk ||
+      !use_tc(p.dk, p.dv, dtype, p.flags) || p.d_skip || p.out_gate)
     return 1;
   // cut each sequence into segments of whole chunks, computed in parallel
   const int s = seq_split_segments(p);

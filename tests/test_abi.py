@@ -83,6 +83,8 @@ def test_split_segments_host_rules(L):
     assert S(1, 65536, 16, 128, 128, torch.float32, G.GDN_SEQ_SPLIT) == 1
     assert S(1, 65536, 16, 128, 128, torch.bfloat16, G.GDN_SEQ_SPLIT, chunk_size=32) == 1
     assert S(1, 65536, 16, 64, 128, torch.bfloat16, G.GDN_SEQ_SPLIT) == 1
+    # debug calls run unsplit (the split's extra kernels check no declared extents)
+    assert S(1, 65536, 16, 128, 128, torch.bfloat16, G.GDN_SEQ_SPLIT | G.GDN_DEBUG_CHECKS) == 1
 
 
 def test_kernel_names(L):
