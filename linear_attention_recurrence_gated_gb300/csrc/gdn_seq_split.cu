@@ -69,16 +69,17 @@ __global__ void __launch_bounds__(256) seg_compose_kernel(const FwdParams p, int
 // mma.sync, fp32 sums, o read and written in bf16).  A CTA takes up to
 // kCorrBlocks blocks of 64 tokens inside one segment and 64 NT value columns
 // of one (sequence, head), so that each row of r is read once per NT column
-// tiles: H_s is converted once, and the next block's rows of r and o are
-// fetched (cp.async) while the current one is computed; warp w computes rows
-// 16 (w % 4) .. + 15 of a block, value columns 64 (w / 4) .. + 63.  grid:
-// (dv / (64 NT), (S - 1) * block groups per segment, N H).
-constexpr int kCorrBlocks = 4;
+// tiles: H_s is converted once; the next block's rows of r are fetched
+// (cp.async) and its o values loaded into registers while the current block
+// is computed.  Warp w computes rows 16 (w % 4) .. + 15 of a block, value
+// columns 64 (w / 4) .. + 63.  grid: (dv / (64 NT), (S - 1) * block groups
+// per segment, N H).
+constexpr int kCorrBlocks = 8;
 constexpr int kCorrLR = kSplitDK + 8;   // padded bf16 rows (16-byte multiples)
 template <int NT>
 struct CorrSmem {
   static constexpr int LH = 64 * NT + 8;
-  static constexpr int BYTES = (kSplitDK * LH + 2 * 64 * kCorrLR + 2 * 64 * LH) * 2;
+  static constexpr int BYTES = (kSplitDK * LH + 2 * 64 * kCorrLR) * 2;
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool ok) {
@@ -93,7 +94,6 @@ __global__ void __launch_bounds__(128 * NT) seg_correct_kernel(const FwdParams p
   extern __shared__ __align__(16) uint8_t corr_smem[];
   __nv_bfloat16 *sh = reinterpret_cast<__nv_bfloat16 *>(corr_smem);   // [dk][LH]
   __nv_bfloat16 *sr = sh + kSplitDK * kCorrLH;                          // [2][64][LR]
-  __nv_bfloat16 *so = sr + 2 * 64 * kCorrLR;                            // [2][64][LH]
   const int H = p.num_heads, dv = p.dv, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c0 = blockIdx.x * NCOL, n = blockIdx.z / H, h = blockIdx.z % H;
   const int s = 1 + (int)blockIdx.y / groups, grp = (int)blockIdx.y % groups;
@@ -107,25 +107,42 @@ __global__ void __launch_bounds__(128 * NT) seg_correct_kernel(const FwdParams p
   const __nv_bfloat16 *r = static_cast<const __nv_bfloat16 *>(p.seg_r);
   __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
   const size_t tok0 = (size_t)n * p.seq_len;   // token index of the sequence's start
-  auto fetch = [&](int b) {   // rows of r and o of block b into buffer b & 1
+  const int m0 = 16 * (warp & 3), n0 = 64 * (warp >> 2);
+  auto rows_of = [&](int b) {   // valid rows of block b
     const int64_t t = t_first + (int64_t)b * 64;
-    const int valid = (int)(seg_end - t < 64 ? seg_end - t : 64);
-    __nv_bfloat16 *dr = sr + (b & 1) * 64 * kCorrLR, *dO = so + (b & 1) * 64 * kCorrLH;
+    return (int)(seg_end - t < 64 ? seg_end - t : 64);
+  };
+  auto fetch = [&](int b) {   // rows of r of block b into buffer b & 1
+    const int64_t t = t_first + (int64_t)b * 64;
+    const int valid = rows_of(b);
+    __nv_bfloat16 *dr = sr + (b & 1) * 64 * kCorrLR;
     for (int idx = tid; idx < 64 * kSplitDK / 8; idx += NTH) {
       const int rr = idx / (kSplitDK / 8), cc = (idx % (kSplitDK / 8)) * 8;
       const bool ok = rr < valid;
       cp_async16(smem_u32(dr + rr * kCorrLR + cc),
                  r + (((tok0 + t + (ok ? rr : 0)) * H + h) * kSplitDK + cc), ok);
     }
-    for (int idx = tid; idx < 64 * NCOL / 8; idx += NTH) {
-      const int rr = idx / (NCOL / 8), cc = (idx % (NCOL / 8)) * 8;
-      const bool ok = rr < valid;
-      cp_async16(smem_u32(dO + rr * kCorrLH + cc),
-                 o + (((tok0 + t + (ok ? rr : 0)) * H + h) * dv + c0 + cc), ok);
-    }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
+  // this thread's o values of block b (the accumulator positions), two bf16 a word
+  auto load_o = [&](int b, uint32_t (&w)[8][2]) {
+    const int64_t t = t_first + (int64_t)b * 64;
+    const int valid = rows_of(b);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int rr = m0 + (lane >> 2) + 8 * half, cc = n0 + 8 * q + 2 * (lane & 3);
+        w[q][half] = rr < valid
+                         ? *reinterpret_cast<const uint32_t *>(o + ((tok0 + t + rr) * H + h) * dv +
+                                                               c0 + cc)
+                         : 0u;
+      }
+    }
+  };
   fetch(0);
+  uint32_t ow[8][2], onext[8][2];
+  load_o(0, ow);
   {  // H_s, columns c0 .. c0 + 64 NT - 1, in bf16
     const float *Hs = p.seg_state + (((size_t)n * p.seg_count + s) * H + h) * kSplitDK * dv + c0;
     for (int idx = tid; idx < kSplitDK * NCOL / 4; idx += NTH) {
@@ -135,17 +152,16 @@ __global__ void __launch_bounds__(128 * NT) seg_correct_kernel(const FwdParams p
           make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
     }
   }
-  const int m0 = 16 * (warp & 3), n0 = 64 * (warp >> 2);
   for (int b = 0; b < nb; ++b) {
     if (b + 1 < nb) {
       fetch(b + 1);
+      load_o(b + 1, onext);
       asm volatile("cp.async.wait_group 1;" ::: "memory");
     } else {
       asm volatile("cp.async.wait_group 0;" ::: "memory");
     }
-    __syncthreads();   // block b's rows (and, the first time, H_s) are in place
+    __syncthreads();   // block b's rows of r (and, the first time, H_s) are in place
     const __nv_bfloat16 *br = sr + (b & 1) * 64 * kCorrLR;
-    const __nv_bfloat16 *bo = so + (b & 1) * 64 * kCorrLH;
     float acc[8][4];
 #pragma unroll
     for (int t = 0; t < 8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
@@ -167,18 +183,23 @@ __global__ void __launch_bounds__(128 * NT) seg_correct_kernel(const FwdParams p
       }
     }
     const int64_t t = t_first + (int64_t)b * 64;
-    const int valid = (int)(seg_end - t < 64 ? seg_end - t : 64);
+    const int valid = rows_of(b);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int rr = m0 + (lane >> 2) + 8 * half, cc = n0 + 8 * q + 2 * (lane & 3);
         if (rr < valid) {
-          const uint32_t w = *reinterpret_cast<const uint32_t *>(bo + rr * kCorrLH + cc);
+          const uint32_t w = ow[q][half];
           *reinterpret_cast<uint32_t *>(o + ((tok0 + t + rr) * H + h) * dv + c0 + cc) =
               pack_bf16(bf16_lo(w) + acc[q][2 * half], bf16_hi(w) + acc[q][2 * half + 1]);
         }
       }
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      ow[q][0] = onext[q][0];
+      ow[q][1] = onext[q][1];
     }
     __syncthreads();   // buffer b & 1 is refilled by the fetch of block b + 2
   }
