@@ -509,18 +509,22 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
         ok = role_wait(bar(B_FULL_IN + slot), (c / NIN) & 1, S, p, n, h, 8);
         if (!__all_sync(0xffffffffu, ok)) break;
         const uint32_t tb = slot_base(slot) + (isP ? L::SQ : L::SK);
-        float ss = 0.f;
+        // eight independent partial sums, so that the norm is a short
+        // dependent chain on the slot's path
+        float ss[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int q8 = 0; q8 < DK / 8; ++q8) {
           const uint4 x = S4(swz<L::GSTRIDE>(tb, i, 8 * q8));
           const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+          float a = ss[q8 & 7];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float lo = bf16_lo(w[e]), hi = bf16_hi(w[e]);
-            ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+            a = fmaf(lo, lo, fmaf(hi, hi, a));
           }
+          ss[q8 & 7] = a;
         }
-        r = rsqrtf(ss + 1e-6f);
+        r = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) + ((ss[4] + ss[5]) + (ss[6] + ss[7])) + 1e-6f);
         if (isP) {
           rn[i] = r;
         } else {
