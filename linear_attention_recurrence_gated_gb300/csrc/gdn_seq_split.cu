@@ -17,10 +17,10 @@ constexpr int kSplitDK = 128;
 
 // One step of the composition, H_(s+1) = M_s H_s + X_s (fp32; M_s is dk x dk;
 // the last step gives the caller's final state), for a block of 32 rows and
-// 32 value columns of one (sequence, head): the
-// CTA stages its 32 rows of M_s and the 32 columns of H_s in shared memory
-// (every load in flight at once), then lane = column and each warp takes 4
-// rows.  grid: (dv / 32 * dk / 32, H, N).
+// 32 value columns of one (sequence, head): the CTA stages its 32 rows of M_s
+// and the 32 columns of H_s in shared memory (every load in flight at once),
+// then lane = column and each warp takes 4 rows.  grid: (dv / 32 * dk / 32,
+// H, N).
 __global__ void __launch_bounds__(256) seg_compose_kernel(const FwdParams p, int s) {
   __shared__ __align__(16) float ms[32][kSplitDK + 4];
   __shared__ __align__(16) float hs[kSplitDK][32];
