@@ -324,7 +324,8 @@ def test_outputs_stay_inside_their_buffers(dtype, dk, dv):
                                                   (1, 4097, 1, 256, True, False, 1e-3),
                                                   (1, 777, 3, 128, True, False, 1e-3),
                                                   (2, 1500, 1, 128, True, False, 1e-3),
-                                                  (1, 1700, 1, 192, True, False, 1e-3)])
+                                                  (1, 1700, 1, 192, True, False, 1e-3),
+                                                  (1, 600, 2, 128, True, False, 1e-3)])
 def test_seq_split(B, T, H, dv, init, l2, gs):
     """A split call equals the oracle within the bf16 bounds and the unsplit
     call up to rounding; with dk = 128 and few units the call takes 3 segments.
@@ -413,7 +414,7 @@ def test_seq_split_plan():
     bf = torch.bfloat16
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     for (N, T, H, dv) in [(1, 65536, 16, 128), (4, 8192, 16, 128), (1, 12 * 64, 1, 128),
-                          (1, 4097, 1, 256), (2, 2000, 3, 128)]:
+                          (1, 4097, 1, 256), (2, 2000, 3, 128), (1, 600, 2, 128)]:
         assert S(N, T, H, 128, dv, bf, G.GDN_SEQ_SPLIT) == _expected_segments(N, T, H, dv, sms)
     assert S(1, 65536, 16, 128, 128, bf, G.GDN_SEQ_SPLIT) >= 2
     assert S(4, 8192, 16, 128, 128, bf, G.GDN_SEQ_SPLIT) == 1
