@@ -276,8 +276,35 @@ __device__ __noinline__ void drain_s_row(uint32_t taddr, const float *G2, const 
   }
 }
 
-// kFSeg: one segment of a split sequence (launched only by the split plan)
-constexpr int kFL2 = 1, kFEpi = 2, kFSeg = 4;
+// kFSeg: one segment of a split sequence (launched only by the split plan);
+// kFRank: packed sequences taken longest first (below)
+constexpr int kFL2 = 1, kFEpi = 2, kFSeg = 4, kFRank = 8;
+
+// Packed sequences (cu_seqlens): CTAs start in launch order, so the sequence
+// of launch index z is the z-th longest (ties by index) rather than the z-th,
+// and the longest chains do not start last.  Each thread t < N ranks sequence
+// t against all others; up to kRankedSeqs sequences, else launch order.  Runs
+// before any other use of shared memory (its first word holds the result).
+constexpr int kRankedSeqs = 128;
+__device__ __forceinline__ int longest_first(const FwdParams &p, int z, uint8_t *smem) {
+  int *pick = reinterpret_cast<int *>(smem);
+  const int t = threadIdx.x;
+  if (t == 0) *pick = z;
+  __syncthreads();
+  if (t < p.num_seqs) {
+    const int64_t lt = (int64_t)p.cu[t + 1] - p.cu[t];
+    int rank = 0;
+    for (int u = 0; u < p.num_seqs; ++u) {
+      const int64_t lu = (int64_t)p.cu[u + 1] - p.cu[u];
+      rank += (lu > lt || (lu == lt && u < t)) ? 1 : 0;
+    }
+    if (rank == z) *pick = t;
+  }
+  __syncthreads();
+  const int n = *pick;
+  __syncthreads();  // every thread has read the word before shared memory is reused
+  return n;
+}
 
 template <int kF>
 __global__ void __launch_bounds__(Cfg::kWarps * 32, 1)
@@ -313,6 +340,7 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
     const int64_t rest = p.seq_len - (int64_t)seg * p.seg_len;  // > 0 by construction
     len = rest < p.seg_len ? rest : p.seg_len;
   } else {
+    if constexpr ((kF & kFRank) != 0) n = longest_first(p, blockIdx.z, smem);
     if (!sequence_bounds(p, n, h, start, len)) return;  // uniform over the CTA
   }
   const bool mtile = segm && tile * kDvt >= dv;  // a transport column tile
@@ -1154,17 +1182,22 @@ cudaError_t launch_tc128(const FwdParams &p, cudaStream_t stream) {
   // the block parts fused into the pass run in their own instantiation, so
   // the plain pass carries none of their code
   using Kern = decltype(&gdn_fwd_tc128_kernel<0>);
-  const Kern inst[8] = {gdn_fwd_tc128_kernel<0>,
-                        gdn_fwd_tc128_kernel<kFL2>,
-                        gdn_fwd_tc128_kernel<kFEpi>,
-                        gdn_fwd_tc128_kernel<kFL2 | kFEpi>,
-                        gdn_fwd_tc128_kernel<kFSeg>,
-                        gdn_fwd_tc128_kernel<kFSeg | kFL2>,
-                        gdn_fwd_tc128_kernel<kFSeg | kFEpi>,
-                        gdn_fwd_tc128_kernel<kFSeg | kFL2 | kFEpi>};
-  const int feat = ((p.flags & GDN_QK_L2NORM) ? kFL2 : 0) | ((p.d_skip || p.out_gate) ? kFEpi : 0) |
-                   (p.seg_len > 0 ? kFSeg : 0);
-  const Kern kern = inst[feat];
+  const Kern inst[12] = {gdn_fwd_tc128_kernel<0>,
+                         gdn_fwd_tc128_kernel<kFL2>,
+                         gdn_fwd_tc128_kernel<kFEpi>,
+                         gdn_fwd_tc128_kernel<kFL2 | kFEpi>,
+                         gdn_fwd_tc128_kernel<kFSeg>,
+                         gdn_fwd_tc128_kernel<kFSeg | kFL2>,
+                         gdn_fwd_tc128_kernel<kFSeg | kFEpi>,
+                         gdn_fwd_tc128_kernel<kFSeg | kFL2 | kFEpi>,
+                         gdn_fwd_tc128_kernel<kFRank>,
+                         gdn_fwd_tc128_kernel<kFRank | kFL2>,
+                         gdn_fwd_tc128_kernel<kFRank | kFEpi>,
+                         gdn_fwd_tc128_kernel<kFRank | kFL2 | kFEpi>};
+  // packed sequences (never split) take the longest-first instances
+  const bool rank = p.cu != nullptr && p.num_seqs > 1 && p.num_seqs <= kRankedSeqs;
+  const int feat = ((p.flags & GDN_QK_L2NORM) ? kFL2 : 0) | ((p.d_skip || p.out_gate) ? kFEpi : 0);
+  const Kern kern = p.seg_len > 0 ? inst[kFSeg | feat] : rank ? inst[8 | feat] : inst[feat];
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (err != cudaSuccess) return err;
