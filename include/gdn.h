@@ -106,7 +106,10 @@ enum {
   /* gdn_fwd: let the head_dim_k 128 tensor-core kernel cut each sequence of a
    * dense call (cu_seqlens NULL, no block epilogue, no GDN_DEBUG_CHECKS) into up to 8 segments of
    * whole chunks when the (sequence, head, 64 value columns) units alone
-   * leave SMs idle (gdn_fwd_split_segments gives the plan).  The chunk
+   * leave SMs idle (gdn_fwd_split_segments gives the plan).  The later
+   * segments are of equal length; the first takes the rest of the sequence
+   * and is often the longest, its few CTAs starting first while the SMs they
+   * leave free run the later ones.  The chunk
    * transition is affine in the state, H' = M H + X, and each output is
    * affine in the state entering the segment, o = o0 + r H, so: one launch
    * runs segment 0 from the caller's state and every later segment from a

@@ -145,25 +145,86 @@ gdn_status fwd_validate(const void *q, const void *k, const void *v, const float
   return GDN_OK;
 }
 
+// The split plan's cost model: the time, in chunk steps, of one launch that
+// dispatches `a` CTAs of `first` chunks (segment 0's value tiles) and then
+// `b` CTAs of `len` chunks (the later segments' value and transport tiles)
+// on `sm` SMs, one CTA per SM, each CTA to the first SM that frees.  The
+// sm - a SMs that segment 0 leaves free take later CTAs from the start, the
+// other a from `first` on.  a < sm.
+int64_t split_makespan(int64_t a, int64_t b, int64_t first, int64_t len, int64_t sm) {
+  const int64_t free = sm - a;
+  int64_t done = 0, rounds_free = 0, rounds_a = 0, last = 0;
+  while (done < b) {
+    const int64_t tf = free > 0 ? rounds_free * len : INT64_MAX, ta = first + rounds_a * len;
+    if (tf <= ta) {
+      done += free;
+      last = tf;
+      ++rounds_free;
+    } else {
+      done += a;
+      last = ta;
+      ++rounds_a;
+    }
+  }
+  return last + len > first ? last + len : first;
+}
+
+constexpr int kMaxFirstLens = 16;   // segment 0: at most this many later lengths
+
 // The split plan of GDN_SEQ_SPLIT: fills p.seg_len / p.seg_count (0 when
 // the call is not split) and returns the segment count (1: not split).  The
 // block epilogue is not combined with a split (the correction would have to
 // pass through it), nor GDN_DEBUG_CHECKS (the composition and correction
 // kernels check no declared extents): such calls run unsplit.
+//
+// Segments 1 .. S-1 hold seg_len tokens each (whole chunks, the last ending
+// at the sequence's end); segment 0 takes the chunks they leave at the
+// front.  Its CTAs are few (value tiles only) and are dispatched first, so it
+// can be k times longer while the SMs it leaves free run the later segments.
+// The plan takes the S in 2 .. kMaxSegments and k in 1 .. kMaxFirstLens
+// (seg_len = chunks / (k + S - 1), at least 4 chunks) with the shortest
+// split_makespan, the fewest segments among equals, and splits only when
+// that beats the unsplit launch by a quarter (the composition steps and the
+// correction cost a little).  A call whose first segments alone fill the SMs
+// is not split.
 int plan_segments(FwdParams &p, int chunk, gdn_dtype dtype) {
   p.seg_len = p.seg_count = 0;
   if (!(p.flags & GDN_SEQ_SPLIT) || (p.flags & GDN_DEBUG_CHECKS) || chunk != kChunk ||
       !use_tc(p.dk, p.dv, dtype, p.flags) || p.d_skip || p.out_gate)
     return 1;
-  // cut each sequence into segments of whole chunks, computed in parallel
-  const int s = seq_split_segments(p);
-  if (s < 2) return 1;
+  const int most = seq_split_segments(p);   // what the tensor-core launch takes
+  if (most < 2) return 1;
+  static int sms[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (sms[dev] == 0 &&
+      cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 1;
+  const int64_t sm = sms[dev];
+  const int64_t units = (int64_t)p.num_seqs * p.num_heads;
+  const int64_t a = units * (p.dv / 64);            // segment 0: value tiles
+  const int64_t u = units * ((p.dv + p.dk) / 64);   // a later segment: value + transport
   const int64_t chunks = (p.seq_len + kChunk - 1) / kChunk;
-  const int64_t seg_len = ((chunks + s - 1) / s) * kChunk;
-  const int64_t count = (p.seq_len + seg_len - 1) / seg_len;
-  if (count < 2 || count > kMaxSegments) return 1;
-  p.seg_len = (int32_t)seg_len;
-  p.seg_count = (int32_t)count;
+  if (a >= sm) return 1;
+  double best_span = 0.75 * (double)chunks;   // the unsplit launch: one wave of all chunks
+  int best_s = 1;
+  int64_t best_len = 0;
+  for (int s = 2; s <= most && s <= kMaxSegments; ++s) {
+    for (int k = 1; k <= kMaxFirstLens; ++k) {
+      const int64_t len = chunks / (k + s - 1);
+      if (len < 4) break;
+      const int64_t first = chunks - (int64_t)(s - 1) * len;
+      const int64_t span = split_makespan(a, (int64_t)(s - 1) * u, first, len, sm);
+      if ((double)span < best_span) {
+        best_span = (double)span;
+        best_s = s;
+        best_len = len;
+      }
+    }
+  }
+  if (best_s < 2) return 1;
+  p.seg_len = (int32_t)(best_len * kChunk);
+  p.seg_count = best_s;
   return p.seg_count;
 }
 

@@ -333,12 +333,19 @@ gdn_fwd_tc128_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmap
   bool transport = false;
   int64_t start, len;
   if constexpr (segm) {
-    n = blockIdx.z / p.seg_count;
-    seg = blockIdx.z % p.seg_count;
+    // grid z = segment * num_seqs + sequence, so that every sequence's first
+    // segment is dispatched first.  The later segments hold seg_len tokens
+    // each and end at the last chunk's end; segment 0 takes the chunks they
+    // leave at the front.
+    n = blockIdx.z % p.num_seqs;
+    seg = blockIdx.z / p.num_seqs;
     transport = seg > 0;
-    start = (int64_t)n * p.seq_len + (int64_t)seg * p.seg_len;
-    const int64_t rest = p.seq_len - (int64_t)seg * p.seg_len;  // > 0 by construction
-    len = rest < p.seg_len ? rest : p.seg_len;
+    const int64_t first = (p.seq_len + 63) / 64 * 64 - (int64_t)(p.seg_count - 1) * p.seg_len;
+    const int64_t s0 = seg == 0 ? 0 : first + (int64_t)(seg - 1) * p.seg_len;
+    const int64_t sl = seg == 0 ? first : p.seg_len;
+    start = (int64_t)n * p.seq_len + s0;
+    const int64_t rest = p.seq_len - s0;  // > 0 by construction
+    len = rest < sl ? rest : sl;
   } else {
     if constexpr ((kF & kFRank) != 0) n = longest_first(p, blockIdx.z, smem);
     if (!sequence_bounds(p, n, h, start, len)) return;  // uniform over the CTA
@@ -1212,7 +1219,8 @@ cudaError_t launch_tc128(const FwdParams &p, cudaStream_t stream) {
   // chunked form):
   //   1. one launch: segment 0 from the caller's state, writing the state
   //      that enters segment 1; segments 1 .. S-1 from zero (o0, X) and from
-  //      the identity on dk extra columns (r, M);
+  //      the identity on dk extra columns (r, M); the first segments'
+  //      CTAs are dispatched first, the longest;
   //   2. the composition H_(s+1) = M_s H_s + X_s for s = 1 .. S-1, in order
   //      (the last gives the caller's final state);
   //   3. the correction o += r H_s over segments 1 .. S-1.
@@ -1225,42 +1233,14 @@ cudaError_t launch_tc128(const FwdParams &p, cudaStream_t stream) {
   return launch_seg_correct(p, stream);
 }
 
-// The number of segments a sequence is split into: the count that minimises
-// (launch waves) / S over 2 .. kMaxSegments, where the one launch holds the
-// first segment's value tiles and (value + dk/64 transport) tiles for each
-// later segment, one CTA per SM; at least 4 chunks a segment, and 1 (no
-// split) unless that beats the unsplit launch by a quarter (the composition
-// and the correction cost a little).
-int choose_segments(const FwdParams &p) {
-  static int sms[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-  if (sms[dev] == 0 &&
-      cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return 1;
-  const int64_t sm = sms[dev];
-  const int64_t units_v = (int64_t)p.num_seqs * p.num_heads * (p.dv / kDvt);
-  const int64_t units_t = (int64_t)p.num_seqs * p.num_heads * ((p.dv + DK) / kDvt);
-  const int64_t chunks = (p.seq_len + 63) / 64;
-  const double cost1 = (double)((units_v + sm - 1) / sm);
-  int best = 1;
-  double best_cost = 0.75 * cost1;
-  for (int s = 2; s <= kMaxSegments && s <= chunks / 4; ++s) {
-    const int64_t ctas = units_v + (int64_t)(s - 1) * units_t;
-    const double cost = (double)((ctas + sm - 1) / sm) / s;
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = s;
-    }
-  }
-  return best;
-}
-
 }  // namespace
 
 bool tc_supported(int dk, int dv) { return (dk == 64 || dk == 128) && dv % kDvt == 0; }
 
-int seq_split_segments(const FwdParams &p) { return p.dk == DK && p.cu == nullptr ? choose_segments(p) : 1; }
+// the split launch above takes dense dk = 128 calls, up to kMaxSegments segments
+int seq_split_segments(const FwdParams &p) {
+  return p.dk == DK && p.cu == nullptr ? kMaxSegments : 1;
+}
 
 cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t stream) {
   switch (p.dk) {

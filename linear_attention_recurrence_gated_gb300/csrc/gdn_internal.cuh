@@ -52,8 +52,10 @@ struct FwdParams {
   uint32_t flags;
   Extents ext;
   // Sequence split (dense inputs, head_dim_k 128; GDN_SEQ_SPLIT): each
-  // sequence is cut into seg_count segments of seg_len tokens, all run by one
-  // launch (grid z = sequence * seg_count + segment).  Segment 0 starts from
+  // sequence is cut into seg_count segments, all run by one launch (grid z =
+  // segment * num_seqs + sequence).  Segments 1 .. seg_count-1 hold seg_len
+  // tokens each (whole chunks, the last ending at the sequence's end);
+  // segment 0 takes the chunks they leave at the front.  Segment 0 starts from
   // the caller's state and ends in seg_state of segment 1.  Later segments
   // start from zero on the value columns (their outputs o0 and end state X)
   // and from the identity on dk extra columns (their per-token reads r, to
@@ -202,7 +204,8 @@ cudaError_t launch_fwd_simt(const FwdParams &p, gdn_dtype dtype, int chunk, cuda
 bool simt_chunk_supported(int chunk, int dk);   // chunk in {32, 64, 128}, not 128 with dk 128
 cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t stream);    // bf16 storage only
 cudaError_t launch_fwd_tc64(const FwdParams &p, cudaStream_t stream);  // bf16, head_dim_k 64
-// GDN_SEQ_SPLIT: segments to cut each sequence of this call into (1 = no split)
+// GDN_SEQ_SPLIT: the most segments the tensor-core launch cuts each sequence
+// of this call into (1: the call cannot be split); the host plan picks the count
 int seq_split_segments(const FwdParams &p);
 // The split's composition step s (H_(s+1) = M_s H_s + X_s; the last step gives
 // the caller's final state) and the correction o += r H_s of the later

@@ -97,7 +97,10 @@ __global__ void __launch_bounds__(128 * NT) seg_correct_kernel(const FwdParams p
   const int H = p.num_heads, dv = p.dv, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c0 = blockIdx.x * NCOL, n = blockIdx.z / H, h = blockIdx.z % H;
   const int s = 1 + (int)blockIdx.y / groups, grp = (int)blockIdx.y % groups;
-  const int64_t seg0 = (int64_t)s * p.seg_len;                        // segment start
+  // segment s >= 1 starts after segment 0, which takes the chunks that the
+  // later segments (seg_len tokens each, ending at the last chunk's end) leave
+  const int64_t first = (p.seq_len + 63) / 64 * 64 - (int64_t)(p.seg_count - 1) * p.seg_len;
+  const int64_t seg0 = first + (int64_t)(s - 1) * p.seg_len;          // segment start
   const int64_t seg_end = seg0 + p.seg_len < p.seq_len ? seg0 + p.seg_len : p.seq_len;
   const int64_t t_first = seg0 + (int64_t)grp * kCorrBlocks * 64;
   if (t_first >= seg_end) return;   // uniform over the CTA

@@ -325,10 +325,15 @@ def test_outputs_stay_inside_their_buffers(dtype, dk, dv):
                                                   (1, 777, 3, 128, True, False, 1e-3),
                                                   (2, 1500, 1, 128, True, False, 1e-3),
                                                   (1, 1700, 1, 192, True, False, 1e-3),
-                                                  (1, 600, 2, 128, True, False, 1e-3)])
+                                                  (1, 600, 2, 128, True, False, 1e-3),
+                                                  (2, 1700, 1, 128, True, False, 1e-3),
+                                                  (2, 4096, 8, 128, True, False, 1e-3)])
 def test_seq_split(B, T, H, dv, init, l2, gs):
     """A split call equals the oracle within the bf16 bounds and the unsplit
-    call up to rounding; with dk = 128 and few units the call takes 3 segments.
+    call up to rounding; with dk = 128 and few units the call takes 2 to 8
+    segments.  On 152 SMs the last two cases give the first segment more
+    chunks than the later ones (7 against 5 with a ragged last chunk; 24
+    against 8 with 16 units a sequence), each with two sequences.
     The gates are slow (gs = 0 is the plain delta rule) so that a segment's
     map M keeps weight: with fast gates M underflows to zero and the split
     result is the unsplit one bit for bit."""
@@ -391,17 +396,41 @@ def test_seq_split_long_full_size():
     assert ro <= to and rs <= ts and uo <= to and us <= ts
 
 
+def _split_makespan(a, b, first, seg, sms):
+    """Chunk steps of one launch that dispatches a CTAs of `first` chunks and
+    then b of `seg` chunks on sms SMs, each CTA to the first SM that frees
+    (the sms - a SMs left free start at 0, the other a at `first`)."""
+    free, done, rf, ra, last = sms - a, 0, 0, 0, 0
+    while done < b:
+        tf = rf * seg if free > 0 else float("inf")
+        ta = first + ra * seg
+        if tf <= ta:
+            done, last, rf = done + free, tf, rf + 1
+        else:
+            done, last, ra = done + a, ta, ra + 1
+    return max(first, last + seg)
+
+
 def _expected_segments(N, T, H, dv, sms):
-    """The documented plan rule: minimise waves / S over S = 2 .. 8 (at least 4
-    chunks a segment; one CTA per SM holding the first segment's value tiles
-    and value + transport tiles for each later one), and split only when that
-    beats the unsplit launch's waves by a quarter."""
-    units_v, units_t = N * H * dv // 64, N * H * (dv + 128) // 64
-    best, best_cost = 1, 0.75 * -(-units_v // sms)
-    for S in range(2, min(8, ((T + 63) // 64) // 4) + 1):
-        cost = -(-(units_v + (S - 1) * units_t) // sms) / S
-        if cost < best_cost:
-            best, best_cost = S, cost
+    """The documented plan rule: the later segments are of equal length
+    chunks / (k + S - 1) (at least 4 chunks), the first takes the rest; over S
+    = 2 .. 8 and k = 1 .. 16 take the shortest launch (the first segments'
+    value tiles dispatched first, then each later segment's value and
+    transport tiles, one CTA per SM), the fewest segments among equals, and
+    split only when that beats the unsplit launch by a quarter.  Calls whose
+    first segments alone fill the SMs are not split."""
+    a, u, chunks = N * H * dv // 64, N * H * (dv + 128) // 64, (T + 63) // 64
+    if a >= sms:
+        return 1
+    best, best_span = 1, 0.75 * chunks
+    for S in range(2, 9):
+        for k in range(1, 17):
+            seg = chunks // (k + S - 1)
+            if seg < 4:
+                break
+            span = _split_makespan(a, (S - 1) * u, chunks - (S - 1) * seg, seg, sms)
+            if span < best_span:
+                best, best_span = S, span
     return best
 
 
