@@ -545,8 +545,8 @@ def bench_ours(args, w: W.Workload, rank: int, world: int, local: int):
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "overlap": "two device sets: step i+1's inputs copy in while step i "
                            "computes and step i-1's result copies out"},
-        # a split call: the segments, S - 1 composition steps and the correction
-        "gpu_launches": args.steps * (segments + 1 if segments > 1 else launches_per_step(kname)),
+        # a split call: the segments, the composition steps and the correction
+        "gpu_launches": args.steps * (3 if segments > 1 else launches_per_step(kname)),
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

@@ -232,9 +232,9 @@ gdn_status gdn_fwd(const void *q, const void *k, const void *v, const float *g,
  * call with these arguments (and no block epilogue: a call with D_skip or
  * out_gate is never split, nor one with GDN_DEBUG_CHECKS) into, on the
  * current device (the plan depends on
- * its SM count): S >= 2 when the call is split, and then gdn_fwd launches S +
- * 1 kernels (every segment in one launch, S - 1 composition steps, the
- * output correction); 1 when it is not split (one kernel).  varlen != 0
+ * its SM count): S >= 2 when the call is split, and then gdn_fwd launches 3
+ * kernels (every segment in one launch, the S - 1 composition steps in one,
+ * the output correction); 1 when it is not split (one kernel).  varlen != 0
  * stands for a call with cu_seqlens (never split).  Returns 0 for sizes
  * gdn_fwd rejects.  Host only; launches nothing. */
 int32_t gdn_fwd_split_segments(int32_t num_seqs, int32_t seq_len, int32_t num_heads,

@@ -1221,15 +1221,14 @@ cudaError_t launch_tc128(const FwdParams &p, cudaStream_t stream) {
   //      that enters segment 1; segments 1 .. S-1 from zero (o0, X) and from
   //      the identity on dk extra columns (r, M); the first segments'
   //      CTAs are dispatched first, the longest;
-  //   2. the composition H_(s+1) = M_s H_s + X_s for s = 1 .. S-1, in order
-  //      (the last gives the caller's final state);
+  //   2. the composition H_(s+1) = M_s H_s + X_s for s = 1 .. S-1, in order,
+  //      in one launch (the last step gives the caller's final state);
   //   3. the correction o += r H_s over segments 1 .. S-1.
   const int S = p.seg_count;
   const dim3 grid(p.dv / kDvt + DK / kDvt, p.num_heads, p.num_seqs * S);
   kern<<<grid, Cfg::kWarps * 32, L::ALLOC, stream>>>(p, tq, tk, tv);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  for (int s = 1; s < S; ++s)   // one launch per step, in order
-    if ((err = launch_seg_compose(p, s, stream)) != cudaSuccess) return err;
+  if ((err = launch_seg_compose(p, 1, stream)) != cudaSuccess) return err;
   return launch_seg_correct(p, stream);
 }
 

@@ -207,9 +207,9 @@ cudaError_t launch_fwd_tc64(const FwdParams &p, cudaStream_t stream);  // bf16, 
 // GDN_SEQ_SPLIT: the most segments the tensor-core launch cuts each sequence
 // of this call into (1: the call cannot be split); the host plan picks the count
 int seq_split_segments(const FwdParams &p);
-// The split's composition step s (H_(s+1) = M_s H_s + X_s; the last step gives
-// the caller's final state) and the correction o += r H_s of the later
-// segments (gdn_seq_split.cu).
+// The split's composition steps s .. seg_count-1 in one launch (H_(s+1) =
+// M_s H_s + X_s in order; the last step gives the caller's final state) and
+// the correction o += r H_s of the later segments (gdn_seq_split.cu).
 cudaError_t launch_seg_compose(const FwdParams &p, int s, cudaStream_t stream);
 cudaError_t launch_seg_correct(const FwdParams &p, cudaStream_t stream);
 bool tc_supported(int dk, int dv);

@@ -1,7 +1,7 @@
 // The two small kernels of a split sequence (GDN_SEQ_SPLIT, head_dim_k 128)
 // that follow the segments' chain launch: the composition of the segments'
-// affine state maps, H_(s+1) = M_s H_s + X_s, one step per launch in segment
-// order, and the correction of the later segments' outputs, o += r H_s.
+// affine state maps, H_(s+1) = M_s H_s + X_s, every step in segment order in
+// one launch, and the correction of the later segments' outputs, o += r H_s.
 // ("Optimization Quartet", Triton GDN kernel section 3.2, names the
 // inter-chunk carry as the serial part of the chunked form; the maps and
 // their composition are what lets the segments run at the same time.)
@@ -15,52 +15,105 @@ using namespace ptx;
 
 constexpr int kSplitDK = 128;
 
-// One step of the composition, H_(s+1) = M_s H_s + X_s (fp32; M_s is dk x dk;
-// the last step gives the caller's final state), for a block of 32 rows and
-// 32 value columns of one (sequence, head): the CTA stages its 32 rows of M_s
-// and the 32 columns of H_s in shared memory (every load in flight at once),
-// then lane = column and each warp takes 4 rows.  grid: (dv / 32 * dk / 32,
-// H, N).
-__global__ void __launch_bounds__(256) seg_compose_kernel(const FwdParams p, int s) {
-  __shared__ __align__(16) float ms[32][kSplitDK + 4];
-  __shared__ __align__(16) float hs[kSplitDK][32];
-  const int nc = p.dv / 32;
-  const int c0 = (blockIdx.x % nc) * 32, r0 = (blockIdx.x / nc) * 32;
-  const int h = blockIdx.y, n = blockIdx.z;
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool ok) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(ok ? 16 : 0)
+               : "memory");
+}
+
+// The composition, H_(s+1) = M_s H_s + X_s for s = s_first .. S-1 in order
+// (fp32; M_s is dk x dk; the last step gives the caller's final state), in one
+// launch.  M_s mixes rows only, so value columns evolve independently: a CTA
+// takes kCompCols value columns of one (sequence, head) through every step
+// with nothing exchanged between CTAs.  Thread (row tid / 2, half tid % 2)
+// forms 8 columns of its row; H_s sits in shared memory, M_s too (rows
+// padded to kCompLM floats), and M_(s+1) is fetched into the other buffer
+// (cp.async) and X_(s+1) into registers while step s is computed.  grid:
+// (dv / kCompCols, H, N), 256 threads.
+constexpr int kCompCols = 16;
+constexpr int kCompLM = kSplitDK + 4;
+constexpr int kCompBytes = (2 * kSplitDK * kCompLM + kSplitDK * kCompCols) * 4;
+
+__global__ void __launch_bounds__(256) seg_compose_kernel(const FwdParams p, int s_first) {
+  extern __shared__ __align__(16) float comp_smem[];
+  float *ms = comp_smem;                          // [2][dk][kCompLM]
+  float *hs = comp_smem + 2 * kSplitDK * kCompLM;  // [dk][kCompCols]
+  const int c0 = blockIdx.x * kCompCols, h = blockIdx.y, n = blockIdx.z;
   const int H = p.num_heads, dv = p.dv, S = p.seg_count, tid = threadIdx.x;
-  const int lane = tid & 31, warp = tid >> 5;
-  const size_t unit = ((size_t)n * S + s) * H + h;
-  const float *M = p.seg_m + unit * kSplitDK * kSplitDK;
-  const float *Hs = p.seg_state + unit * kSplitDK * dv;
-  const float *X = p.seg_x + unit * kSplitDK * dv;
-  // segment s + 1, or after the last segment the caller's final state
-  float *Hn = s + 1 < S ? p.seg_state + (unit + H) * kSplitDK * dv
-                        : p.sN ? p.sN + ((size_t)n * H + h) * kSplitDK * dv : nullptr;
-  if (Hn == nullptr) return;  // uniform over the CTA
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int q = tid + 256 * e;                  // 1024 float4 of each tile
-    const int mr = q / (kSplitDK / 4), mc = q % (kSplitDK / 4);
-    *reinterpret_cast<float4 *>(&ms[mr][4 * mc]) =
-        *reinterpret_cast<const float4 *>(M + (size_t)(r0 + mr) * kSplitDK + 4 * mc);
-    const int hr = q / 8, hc = q % 8;
-    *reinterpret_cast<float4 *>(&hs[hr][4 * hc]) =
-        *reinterpret_cast<const float4 *>(Hs + (size_t)hr * dv + c0 + 4 * hc);
-  }
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = 4 * warp + i;
-    float a0 = X[(size_t)(r0 + r) * dv + c0 + lane], a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll 8
-    for (int q = 0; q < kSplitDK / 4; ++q) {
-      const float4 m = *reinterpret_cast<const float4 *>(&ms[r][4 * q]);
-      a0 = fmaf(m.x, hs[4 * q][lane], a0);
-      a1 = fmaf(m.y, hs[4 * q + 1][lane], a1);
-      a2 = fmaf(m.z, hs[4 * q + 2][lane], a2);
-      a3 = fmaf(m.w, hs[4 * q + 3][lane], a3);
+  const int r = tid >> 1, cl = 8 * (tid & 1);     // this thread's row and first column
+  auto unit = [&](int s) { return ((size_t)n * S + s) * H + h; };
+  auto fetch_m = [&](int s) {   // M_s into buffer s & 1: 4096 pieces of 16 bytes
+    const float *M = p.seg_m + unit(s) * kSplitDK * kSplitDK;
+    float *dst = ms + (s & 1) * kSplitDK * kCompLM;
+#pragma unroll 4
+    for (int i = tid; i < kSplitDK * kSplitDK / 4; i += 256) {
+      const int mr = i / (kSplitDK / 4), mc = 4 * (i % (kSplitDK / 4));
+      cp_async16(smem_u32(dst + mr * kCompLM + mc), M + (size_t)mr * kSplitDK + mc, true);
     }
-    Hn[(size_t)(r0 + r) * dv + c0 + lane] = (a0 + a1) + (a2 + a3);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  auto load_x = [&](int s, float4 &x0, float4 &x1) {   // this thread's 8 values of X_s
+    const float *X = p.seg_x + unit(s) * kSplitDK * dv + (size_t)r * dv + c0 + cl;
+    x0 = *reinterpret_cast<const float4 *>(X);
+    x1 = *reinterpret_cast<const float4 *>(X + 4);
+  };
+  fetch_m(s_first);
+  {  // H_(s_first), the state entering that segment: 512 float4, two a thread
+    const float *Hs = p.seg_state + unit(s_first) * kSplitDK * dv + c0;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int i = tid + 256 * e, hr = i / 4, hc = 4 * (i % 4);
+      *reinterpret_cast<float4 *>(&hs[hr * kCompCols + hc]) =
+          *reinterpret_cast<const float4 *>(Hs + (size_t)hr * dv + hc);
+    }
+  }
+  float4 x0, x1;
+  load_x(s_first, x0, x1);
+  for (int s = s_first; s < S; ++s) {
+    float4 xn0 = x0, xn1 = x1;
+    if (s + 1 < S) {
+      fetch_m(s + 1);
+      load_x(s + 1, xn0, xn1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
+    __syncthreads();   // M_s and H_s in place
+    float acc[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    const float *mrow = ms + (s & 1) * kSplitDK * kCompLM + r * kCompLM;
+#pragma unroll 4
+    for (int k = 0; k < kSplitDK; k += 4) {
+      const float4 m4 = *reinterpret_cast<const float4 *>(mrow + k);
+      const float mk[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 a = *reinterpret_cast<const float4 *>(&hs[(k + j) * kCompCols + cl]);
+        const float4 b = *reinterpret_cast<const float4 *>(&hs[(k + j) * kCompCols + cl + 4]);
+        acc[0] = fmaf(mk[j], a.x, acc[0]);
+        acc[1] = fmaf(mk[j], a.y, acc[1]);
+        acc[2] = fmaf(mk[j], a.z, acc[2]);
+        acc[3] = fmaf(mk[j], a.w, acc[3]);
+        acc[4] = fmaf(mk[j], b.x, acc[4]);
+        acc[5] = fmaf(mk[j], b.y, acc[5]);
+        acc[6] = fmaf(mk[j], b.z, acc[6]);
+        acc[7] = fmaf(mk[j], b.w, acc[7]);
+      }
+    }
+    __syncthreads();   // H_s and buffer s & 1 read by every thread
+    const float4 y0 = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    const float4 y1 = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    *reinterpret_cast<float4 *>(&hs[r * kCompCols + cl]) = y0;
+    *reinterpret_cast<float4 *>(&hs[r * kCompCols + cl + 4]) = y1;
+    // segment s + 1's entry state (the correction reads it), or after the last
+    // segment the caller's final state
+    float *Hn = s + 1 < S ? p.seg_state + unit(s + 1) * kSplitDK * dv
+                          : p.sN ? p.sN + ((size_t)n * H + h) * kSplitDK * dv : nullptr;
+    if (Hn) {
+      *reinterpret_cast<float4 *>(Hn + (size_t)r * dv + c0 + cl) = y0;
+      *reinterpret_cast<float4 *>(Hn + (size_t)r * dv + c0 + cl + 4) = y1;
+    }
+    x0 = xn0;
+    x1 = xn1;
   }
 }
 
@@ -81,12 +134,6 @@ struct CorrSmem {
   static constexpr int LH = 64 * NT + 8;
   static constexpr int BYTES = (kSplitDK * LH + 2 * 64 * kCorrLR) * 2;
 };
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool ok) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(ok ? 16 : 0)
-               : "memory");
-}
 
 template <int NT>
 __global__ void __launch_bounds__(128 * NT) seg_correct_kernel(const FwdParams p, int groups) {
@@ -211,7 +258,11 @@ __global__ void __launch_bounds__(128 * NT) seg_correct_kernel(const FwdParams p
 }  // namespace
 
 cudaError_t launch_seg_compose(const FwdParams &p, int s, cudaStream_t stream) {
-  seg_compose_kernel<<<dim3(p.dv / 32 * (kSplitDK / 32), p.num_heads, p.num_seqs), 256, 0,
+  cudaError_t err =
+      cudaFuncSetAttribute(seg_compose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kCompBytes);
+  if (err != cudaSuccess) return err;
+  seg_compose_kernel<<<dim3(p.dv / kCompCols, p.num_heads, p.num_seqs), 256, kCompBytes,
                        stream>>>(p, s);
   return cudaGetLastError();
 }
