@@ -122,25 +122,28 @@ __global__ void __launch_bounds__(256) seg_compose_kernel(const FwdParams p, int
 // mma.sync, fp32 sums, o read and written in bf16).  A CTA takes up to
 // kCorrBlocks blocks of 64 tokens inside one segment and 64 NT value columns
 // of one (sequence, head), so that each row of r is read once per NT column
-// tiles: H_s is converted once; the next block's rows of r are fetched
-// (cp.async) and its o values loaded into registers while the current block
-// is computed.  Warp w computes rows 16 (w % 4) .. + 15 of a block, value
-// columns 64 (w / 4) .. + 63.  grid: (dv / (64 NT), (S - 1) * block groups
-// per segment, N H).
+// tiles; H_s is converted once.  Block b + 2's rows of r are fetched
+// (cp.async, three buffers) and its o values loaded into registers (three
+// sets) while block b is computed, so every load has two blocks' time to
+// land; the block loop is unrolled so that the register sets stay distinct.
+// Warp w computes rows 16 (w % 4) .. + 15 of a block, value columns
+// 64 (w / 4) .. + 63.  grid: (dv / (64 NT), (S - 1) * block groups per
+// segment, N H).
 constexpr int kCorrBlocks = 8;
+constexpr int kCorrBufs = 3;
 constexpr int kCorrLR = kSplitDK + 8;   // padded bf16 rows (16-byte multiples)
 template <int NT>
 struct CorrSmem {
   static constexpr int LH = 64 * NT + 8;
-  static constexpr int BYTES = (kSplitDK * LH + 2 * 64 * kCorrLR) * 2;
+  static constexpr int BYTES = (kSplitDK * LH + kCorrBufs * 64 * kCorrLR) * 2;
 };
 
 template <int NT>
-__global__ void __launch_bounds__(128 * NT) seg_correct_kernel(const FwdParams p, int groups) {
+__global__ void __launch_bounds__(128 * NT, 2) seg_correct_kernel(const FwdParams p, int groups) {
   constexpr int kCorrLH = CorrSmem<NT>::LH, NTH = 128 * NT, NCOL = 64 * NT;
   extern __shared__ __align__(16) uint8_t corr_smem[];
   __nv_bfloat16 *sh = reinterpret_cast<__nv_bfloat16 *>(corr_smem);   // [dk][LH]
-  __nv_bfloat16 *sr = sh + kSplitDK * kCorrLH;                          // [2][64][LR]
+  __nv_bfloat16 *sr = sh + kSplitDK * kCorrLH;                          // [3][64][LR]
   const int H = p.num_heads, dv = p.dv, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c0 = blockIdx.x * NCOL, n = blockIdx.z / H, h = blockIdx.z % H;
   const int s = 1 + (int)blockIdx.y / groups, grp = (int)blockIdx.y % groups;
@@ -162,11 +165,13 @@ __global__ void __launch_bounds__(128 * NT) seg_correct_kernel(const FwdParams p
     const int64_t t = t_first + (int64_t)b * 64;
     return (int)(seg_end - t < 64 ? seg_end - t : 64);
   };
-  auto fetch = [&](int b) {   // rows of r of block b into buffer b & 1
+  auto fetch = [&](int b) {   // rows of r of block b into buffer b % 3
     const int64_t t = t_first + (int64_t)b * 64;
     const int valid = rows_of(b);
-    __nv_bfloat16 *dr = sr + (b & 1) * 64 * kCorrLR;
-    for (int idx = tid; idx < 64 * kSplitDK / 8; idx += NTH) {
+    __nv_bfloat16 *dr = sr + (b % kCorrBufs) * 64 * kCorrLR;
+#pragma unroll
+    for (int e = 0; e < 64 * kSplitDK / 8 / NTH; ++e) {
+      const int idx = tid + e * NTH;
       const int rr = idx / (kSplitDK / 8), cc = (idx % (kSplitDK / 8)) * 8;
       const bool ok = rr < valid;
       cp_async16(smem_u32(dr + rr * kCorrLR + cc),
@@ -190,68 +195,74 @@ __global__ void __launch_bounds__(128 * NT) seg_correct_kernel(const FwdParams p
       }
     }
   };
+  uint32_t ow[kCorrBufs][8][2];
   fetch(0);
-  uint32_t ow[8][2], onext[8][2];
-  load_o(0, ow);
-  {  // H_s, columns c0 .. c0 + 64 NT - 1, in bf16
+  load_o(0, ow[0]);
+  if (nb > 1) {
+    fetch(1);
+    load_o(1, ow[1]);
+  }
+  {  // H_s, columns c0 .. c0 + 64 NT - 1, in bf16 (eight loads in flight a thread)
     const float *Hs = p.seg_state + (((size_t)n * p.seg_count + s) * H + h) * kSplitDK * dv + c0;
-    for (int idx = tid; idx < kSplitDK * NCOL / 4; idx += NTH) {
+#pragma unroll 8
+    for (int e = 0; e < kSplitDK * NCOL / 4 / NTH; ++e) {
+      const int idx = tid + e * NTH;
       const int k = idx / (NCOL / 4), cc = (idx % (NCOL / 4)) * 4;
       const float4 x = *reinterpret_cast<const float4 *>(Hs + (size_t)k * dv + cc);
       *reinterpret_cast<uint2 *>(&sh[k * kCorrLH + cc]) =
           make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
     }
   }
-  for (int b = 0; b < nb; ++b) {
-    if (b + 1 < nb) {
-      fetch(b + 1);
-      load_o(b + 1, onext);
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-    } else {
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-    }
-    __syncthreads();   // block b's rows of r (and, the first time, H_s) are in place
-    const __nv_bfloat16 *br = sr + (b & 1) * 64 * kCorrLR;
-    float acc[8][4];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-#pragma unroll
-    for (int k0 = 0; k0 < kSplitDK; k0 += 16) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(smem_u32(br + (m0 + (lane & 7) + ((lane >> 3) & 1) * 8) * kCorrLR + k0 +
-                       (lane >> 4) * 8),
-              a0, a1, a2, a3);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int i = lane >> 3;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(smem_u32(sh + (k0 + (i & 1) * 8 + (lane & 7)) * kCorrLH + n0 + 16 * q +
-                           (i >> 1) * 8),
-                  b0, b1, b2, b3);
-        mma_bf16(acc[2 * q], a0, a1, a2, a3, b0, b1);
-        mma_bf16(acc[2 * q + 1], a0, a1, a2, a3, b2, b3);
+  for (int b = 0; b < kCorrBlocks; ++b) {
+    if (b < nb) {   // uniform over the CTA
+      if (b + 2 < nb) {
+        fetch(b + 2);
+        load_o(b + 2, ow[(b + 2) % kCorrBufs]);
+        asm volatile("cp.async.wait_group 2;" ::: "memory");
+      } else if (b + 1 < nb) {
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+      } else {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
       }
-    }
-    const int64_t t = t_first + (int64_t)b * 64;
-    const int valid = rows_of(b);
+      __syncthreads();   // block b's rows of r (and, the first time, H_s) are in place
+      const __nv_bfloat16 *br = sr + (b % kCorrBufs) * 64 * kCorrLR;
+      float acc[8][4];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+      for (int t = 0; t < 8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int rr = m0 + (lane >> 2) + 8 * half, cc = n0 + 8 * q + 2 * (lane & 3);
-        if (rr < valid) {
-          const uint32_t w = ow[q][half];
-          *reinterpret_cast<uint32_t *>(o + ((tok0 + t + rr) * H + h) * dv + c0 + cc) =
-              pack_bf16(bf16_lo(w) + acc[q][2 * half], bf16_hi(w) + acc[q][2 * half + 1]);
+      for (int k0 = 0; k0 < kSplitDK; k0 += 16) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(smem_u32(br + (m0 + (lane & 7) + ((lane >> 3) & 1) * 8) * kCorrLR + k0 +
+                         (lane >> 4) * 8),
+                a0, a1, a2, a3);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int i = lane >> 3;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(smem_u32(sh + (k0 + (i & 1) * 8 + (lane & 7)) * kCorrLH + n0 + 16 * q +
+                             (i >> 1) * 8),
+                    b0, b1, b2, b3);
+          mma_bf16(acc[2 * q], a0, a1, a2, a3, b0, b1);
+          mma_bf16(acc[2 * q + 1], a0, a1, a2, a3, b2, b3);
         }
       }
-    }
+      const int64_t t = t_first + (int64_t)b * 64;
+      const int valid = rows_of(b);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      ow[q][0] = onext[q][0];
-      ow[q][1] = onext[q][1];
+      for (int q = 0; q < 8; ++q) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int rr = m0 + (lane >> 2) + 8 * half, cc = n0 + 8 * q + 2 * (lane & 3);
+          if (rr < valid) {
+            const uint32_t w = ow[b % kCorrBufs][q][half];
+            *reinterpret_cast<uint32_t *>(o + ((tok0 + t + rr) * H + h) * dv + c0 + cc) =
+                pack_bf16(bf16_lo(w) + acc[q][2 * half], bf16_hi(w) + acc[q][2 * half + 1]);
+          }
+        }
+      }
+      __syncthreads();   // buffer b % 3 is refilled by the fetch of block b + 3
     }
-    __syncthreads();   // buffer b & 1 is refilled by the fetch of block b + 2
   }
 }
 
