@@ -152,14 +152,14 @@ gdn_status fwd_validate(const void *q, const void *k, const void *v, const float
 // sm - a SMs that segment 0 leaves free take later CTAs from the start, the
 // other a from `first` on.  a < sm.
 int64_t split_makespan(int64_t a, int64_t b, int64_t first, int64_t len, int64_t sm) {
-  const int64_t free = sm - a;
-  int64_t done = 0, rounds_free = 0, rounds_a = 0, last = 0;
+  const int64_t idle = sm - a;   // SMs that segment 0 leaves free
+  int64_t done = 0, rounds_idle = 0, rounds_a = 0, last = 0;
   while (done < b) {
-    const int64_t tf = free > 0 ? rounds_free * len : INT64_MAX, ta = first + rounds_a * len;
+    const int64_t tf = idle > 0 ? rounds_idle * len : INT64_MAX, ta = first + rounds_a * len;
     if (tf <= ta) {
-      done += free;
+      done += idle;
       last = tf;
-      ++rounds_free;
+      ++rounds_idle;
     } else {
       done += a;
       last = ta;
