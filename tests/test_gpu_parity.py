@@ -333,7 +333,7 @@ def test_seq_split(B, T, H, dv, init, l2, gs):
     call up to rounding; with dk = 128 and few units the call takes 2 to 8
     segments.  On 152 SMs the last two cases give the first segment more
     chunks than the later ones (7 against 5 with a ragged last chunk; 24
-    against 8 with 16 units a sequence), each with two sequences.
+    against 8 with 8 heads), each with two sequences.
     The gates are slow (gs = 0 is the plain delta rule) so that a segment's
     map M keeps weight: with fast gates M underflows to zero and the split
     result is the unsplit one bit for bit."""
